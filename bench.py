@@ -1,0 +1,342 @@
+#!/usr/bin/env python3
+"""Throughput of the MXFP4 routed MoE block on GB300.
+
+One step = one forward of the whole block (norm + router + top-k + softmax,
+permutation, MXFP4 gate/up + SwiGLU, MXFP4 down, weighted combine + residual)
+over one batch of the workload: the gpt-oss MoE block decoding a batch of 8
+tokens with two hot experts (hidden 2880, 32 experts, top-4, expert_hidden
+2880).  Weights are seeded synthetic MXFP4 tensors of that architecture.  The
+steps rotate over several independently seeded weight sets whose touched
+experts together exceed the 129 MB L2, so no step finds its weights in L2.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE block tokens/s; decode HBM GB/s and prefill TFLOP/s vs GB300 peak"
+WORKLOAD = 1
+TOKENS = 8
+KERNEL_SLOTS = ["route_permute", "gateup_swiglu", "down_weighted", "combine_residual"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sets", type=int, default=4, help="weight sets rotated over the steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="timed region only (no clock pre-roll, kernel timing, e2e or CPU baseline); for ncu")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def traffic_record(kernel: str):
+    """ncu DRAM bytes per launch of `kernel`, if taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["sha256"]:
+        return None
+    return rec
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.p.terminate()
+        self.p.wait()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from mxfp4_mixture_experts_rms_gb300 import synth
+    cores = os.cpu_count() or 1
+    blk = synth.make_block(WORKLOAD)
+    x = synth.make_tokens(WORKLOAD, TOKENS, blk["shape"].hidden)
+    oracle.moe_forward(blk, x[:1], nthreads=1)  # warm the library
+    t0 = time.perf_counter()
+    oracle.moe_forward(blk, x[:1], nthreads=1)
+    t_tok = time.perf_counter() - t0
+    # tokens per step so that the whole run takes about three minutes on all cores
+    budget = 180.0
+    per_step = max(1, min(TOKENS, int(budget * cores / max(1e-9, (args.steps + args.warmup) * t_tok))))
+    nthr = min(cores, per_step)
+    for i in range(args.warmup):
+        oracle.moe_forward(blk, np.ascontiguousarray(x[(i % TOKENS):(i % TOKENS) + 1].repeat(per_step, 0)), nthreads=nthr)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        xs = np.ascontiguousarray(np.roll(x, -i, axis=0)[:per_step]) if per_step <= TOKENS else x
+        oracle.moe_forward(blk, xs, nthreads=nthr)
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    sample = f"{per_step} of the {TOKENS} tokens of each step (full block per token), {nthr} threads"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": synth.WORKLOADS[WORKLOAD].name, "tokens_per_step": TOKENS,
+                       "hidden": 2880, "n_experts": 32, "top_k": 4, "expert_hidden": 2880},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthr, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def algorithmic_bytes(shape, counts, T):
+    """Bytes the gate/up and down kernels must move at least once per launch."""
+    H, F = shape.hidden, shape.expert_hidden
+    distinct = int((counts > 0).sum()) + shape.n_shared
+    routes = int(counts.sum()) + shape.n_shared * T
+    mat = F * H // 2 + F * H // 32
+    gateup = distinct * (2 * mat + 2 * F * 4) + T * H * 2 + routes * F * 2
+    down = distinct * (mat + H * 4) + routes * F * 2 + routes * H * 4
+    return gateup, down, distinct
+
+
+def cpu_baseline(blk, x):
+    import oracle
+    cores = os.cpu_count() or 1
+    n = min(x.shape[0], cores)
+    oracle.moe_forward(blk, x[:1], nthreads=1)
+    t0 = time.perf_counter()
+    oracle.moe_forward(blk, x[:n], nthreads=n)
+    el = time.perf_counter() - t0
+    return {"value": n / el, "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "sample": f"{n} tokens of one step (weight set 0), whole block per token, {el:.1f} s wall"}
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from mxfp4_mixture_experts_rms_gb300 import moe, synth
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    wl = synth.WORKLOADS[WORKLOAD]
+    shape = wl.shape
+    H, K = shape.hidden, shape.top_k
+    sets = []
+    for s in range(args.sets):
+        layer = s + 100 * rank
+        blk = synth.make_block(WORKLOAD, layer=layer)
+        xb = synth.make_tokens(WORKLOAD, TOKENS, H, layer=layer)
+        plan = moe.Plan(shape, max_tokens=TOKENS).alloc_workspace().load_weights(moe.DeviceBlock(blk))
+        x = torch.from_numpy(xb.view(np.int16)).cuda()
+        out = torch.empty((TOKENS, H), dtype=torch.float32, device="cuda")
+        ids = torch.empty((TOKENS, K), dtype=torch.int32, device="cuda")
+        sets.append(dict(blk=blk if s == 0 else None, xb=xb if s == 0 else None, plan=plan, x=x, out=out, ids=ids))
+        del blk
+    st = torch.cuda.current_stream()
+
+    def step(i):
+        d = sets[i % len(sets)]
+        d["plan"].forward(d["x"], d["out"], d["ids"], stream=st)
+
+    # per-set routing facts for the algorithmic byte counts
+    facts = []
+    for i, d in enumerate(sets):
+        step(i)
+        c = torch.empty(shape.n_experts, dtype=torch.int32, device="cuda")
+        d["plan"].expert_counts(c)
+        torch.cuda.synchronize()
+        facts.append(algorithmic_bytes(shape, c.cpu().numpy(), TOKENS))
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    # pre-roll so that the clock samples see this load for about a second
+    clocks = Clocks(local)
+    t_end = time.perf_counter() + (0.0 if args.quick else 1.0)
+    i = 0
+    while time.perf_counter() < t_end:
+        for _ in range(64):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+    # ---- timed region: exactly K steps
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(st)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(st)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * TOKENS * args.steps / (ms / 1e3)
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "ms_per_step": ms / args.steps,
+                              "quick": True}), flush=True)
+        return
+
+    # ---- kernel durations over the same K steps, with per-launch CUDA events
+    for d in sets:
+        d["plan"].set_i("profile", 1)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        step(i)
+    tot = [0.0] * 4
+    cnt = [0] * 4
+    for d in sets:
+        m, c = d["plan"].profile_read()
+        tot = [a + b for a, b in zip(tot, m)]
+        cnt = [a + b for a, b in zip(cnt, c)]
+        d["plan"].set_i("profile", 0)
+    avg_ms = [t / c if c else 0.0 for t, c in zip(tot, cnt)]
+    share = [t / sum(tot) for t in tot]
+    gu_bytes = sum(facts[i % len(sets)][0] for i in range(args.steps)) / args.steps
+    dn_bytes = sum(facts[i % len(sets)][1] for i in range(args.steps)) / args.steps
+    distinct = sum(facts[i % len(sets)][2] for i in range(args.steps)) / args.steps
+    hbm, _, peak_kind = peaks()
+    dom = max(range(4), key=lambda k: tot[k])
+    dom_bytes = {1: gu_bytes, 2: dn_bytes}.get(dom, gu_bytes)
+    achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9
+    tr = traffic_record(KERNEL_SLOTS[dom])
+    step_bytes = gu_bytes + dn_bytes
+    step_gbs = step_bytes / (ms / args.steps / 1e3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    hx = [d["x"].cpu().pin_memory() for d in sets]
+    hout = [torch.empty((TOKENS, H), dtype=torch.float32).pin_memory() for _ in sets]
+    hids = [torch.empty((TOKENS, K), dtype=torch.int32).pin_memory() for _ in sets]
+
+    def e2e_step(i):
+        j = i % len(sets)
+        d = sets[j]
+        d["x"].copy_(hx[j], non_blocking=True)
+        d["plan"].forward(d["x"], d["out"], d["ids"], stream=st)
+        hout[j].copy_(d["out"], non_blocking=True)
+        hids[j].copy_(d["ids"], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(st)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e = {"value": world * TOKENS * args.steps / (e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": TOKENS * H * 2, "d2h_bytes_per_step": TOKENS * H * 4 + TOKENS * K * 4}
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world >= 1:
+        cpu = cpu_baseline(sets[0]["blk"], sets[0]["xb"])
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "tokens_per_step": TOKENS, "hidden": H, "n_experts": shape.n_experts,
+                   "top_k": K, "expert_hidden": shape.expert_hidden, "weights": "mxfp4 (e2m1 + e8m0/32)",
+                   "weight_sets": len(sets), "l2": "inputs larger than L2: steps rotate over independently "
+                   "seeded weight sets", "distinct_experts_per_step": distinct,
+                   "algorithmic_bytes_per_step": step_bytes, "step_hbm_gbs": step_gbs,
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": KERNEL_SLOTS[dom], "achieved": achieved, "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": tr["bytes_per_launch"] if tr else None,
+                     "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": avg_ms[dom]},
+        "kernels": {KERNEL_SLOTS[k]: {"avg_us": 1e3 * avg_ms[k], "share": share[k], "launches": cnt[k]}
+                    for k in range(4)},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": 4 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,156 @@
+/*
+ * moe.h -- C-ABI of the GB300 (sm_103a) MXFP4 routed mixture-of-experts block.
+ *
+ * The block (turbospark-runtime gptoss/mod.rs, module doc comment; goosedump
+ * gpt_oss.rs, `forward` and `mixture_of_experts`):
+ *
+ *     m   = rms_norm(x, gamma, eps)                     -- bf16 x_hat
+ *     l   = m @ router_w^T + router_b                   -- raw logits
+ *     ids = top_k(l)  (strict '>', ties to the lower index, NaN never chosen)
+ *     w   = weight_scale * softmax(l[ids])
+ *     out = x + Σ_slot w_slot * expert_{ids[slot]}(m)  (+ shared expert, weight 1)
+ *     expert(m) = Wd * bf16(swiglu(Wg m + bg, Wu m + bu)) + bd
+ *     swiglu(g, u) = min(g, L) * sigmoid(alpha * min(g, L)) * (clamp(u, -L, L) + 1)
+ *
+ * with MXFP4 expert weights (E2M1 nibbles in 32-element blocks with one E8M0
+ * scale each; E2M1 table from ds4.c `dsv4_e2m1fn_value_cpu`).
+ *
+ * Conventions
+ *  - All tensor pointers are DEVICE pointers unless a parameter says "host".
+ *    The library never takes ownership: weights and workspace are borrowed
+ *    and must outlive every forward call that uses them.
+ *  - Every function returns MOE_OK (0) or a negative MOE_E* status; the
+ *    thread-local text of the last failure is available from moe_last_error().
+ *    Functions that return a pointer return NULL on failure.
+ *  - moe_forward only enqueues kernels on the given CUDA stream: no host
+ *    synchronisation, no allocation.  Errors found on the device (a bounded
+ *    wait that timed out inside a kernel) set a device flag that
+ *    moe_get_device_status() reads back.
+ *  - bf16 values are passed as their 16-bit patterns.
+ *
+ * Canonical MXFP4 layout (per matrix, leading expert dimension E):
+ *   codes  uint8 [E][rows][cols/2]: element 2i of a row in the low nibble of
+ *          byte i, element 2i+1 in the high nibble; nibble bit 3 = sign,
+ *          bits 0..2 = index into {0, 0.5, 1, 1.5, 2, 3, 4, 6}
+ *   scales uint8 [E][rows][cols/32]: E8M0, value 2^(s-127); 0xFF (NaN) is rejected
+ *   bias   float [E][rows]
+ *   gate, up: rows = expert_hidden (F), cols = hidden (H)   (goosedump gpt_oss.rs
+ *   down:     rows = H, cols = F                              tensor validation)
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    MOE_OK = 0,
+    MOE_EINVAL = -1,    /* bad argument: NULL pointer, unknown key, bad value */
+    MOE_ESHAPE = -2,    /* shape not supported (see moe_plan_create) */
+    MOE_ENOTREADY = -3, /* weights or workspace missing */
+    MOE_ECUDA = -4,     /* a CUDA runtime call failed */
+    MOE_ENOMEM = -5,    /* workspace too small / token count above max_tokens */
+    MOE_EDEVICE = -6    /* a kernel reported a device-side failure */
+};
+
+typedef struct moe_plan moe_plan;
+
+/* One MXFP4 matrix of all experts (device pointers, canonical layout). */
+typedef struct {
+    const uint8_t *codes;
+    const uint8_t *scales;
+    const float *bias;
+} moe_mxfp4_matrix;
+
+typedef struct {
+    const float *gamma;        /* rms_norm weight [H] */
+    const uint16_t *router_w;  /* bf16 [E][H] */
+    const float *router_b;     /* [E] */
+    moe_mxfp4_matrix gate, up, down;            /* routed experts, leading dim E */
+    moe_mxfp4_matrix sh_gate, sh_up, sh_down;   /* shared expert, leading dim 1;
+                                                   read only when n_shared_experts = 1 */
+} moe_weights;
+
+/* Create a plan for one block shape.
+ * hidden (H) and expert_hidden (F) must be positive multiples of 32;
+ * 1 <= top_k <= min(n_experts, 8); 1 <= n_experts <= 256; swiglu_limit > 0.
+ * Defaults: rms_eps 1e-5 (goosedump gpt_oss.rs EPSILON), no shared expert,
+ * max_tokens 4096.  Returns NULL (see moe_last_error) on bad arguments. */
+moe_plan *moe_plan_create(int hidden, int expert_hidden, int n_experts, int top_k,
+                          float swiglu_alpha, float swiglu_limit, float weight_scale);
+void moe_plan_destroy(moe_plan *plan);
+
+/* Integer options:
+ *   "n_shared_experts"  0 or 1: an always-on expert added with weight 1
+ *                       (ds4.c DS4_SHAPE_FLASH n_expert_shared)
+ *   "max_tokens"        largest token count per forward (sizes the workspace)
+ *   "decode_max_tokens" forwards with tokens <= this use the GEMV decode path,
+ *                       larger ones the tensor-core grouped-GEMM path (default 16)
+ *   "path"              0 auto, 1 force decode, 2 force prefill (testing)
+ *   "router_exact"      1: compute every router logit in fp64 (testing)
+ *   "profile"           1: time each kernel launch with CUDA events (see
+ *                       moe_profile_read); 0: off (default)
+ * Options that change the workspace size must be set before moe_set_workspace. */
+int moe_plan_set_i(moe_plan *plan, const char *key, long long value);
+/* Floating options: "rms_eps". */
+int moe_plan_set_f(moe_plan *plan, const char *key, double value);
+
+/* Bytes of device workspace a forward of up to max_tokens tokens needs
+ * (max_tokens <= 0: the plan's max_tokens).  0 on error. */
+size_t moe_workspace_bytes(const moe_plan *plan, int max_tokens);
+/* Hand the plan a device buffer of at least moe_workspace_bytes() bytes,
+ * 256-byte aligned.  The plan borrows it (the caller frees it). */
+int moe_set_workspace(moe_plan *plan, void *dev_ptr, size_t bytes);
+
+/* Register the weights (device pointers, borrowed).  Checks pointer
+ * alignment (16 bytes) and scans every scale tensor for the NaN code 0xFF
+ * (this one call synchronises the current device).  Must precede moe_forward. */
+int moe_load_weights(moe_plan *plan, const moe_weights *w);
+
+/* out[T][H] (float) = x + MoE(x) for x bf16 [T][H]; route_ids_out int32
+ * [T][top_k] (may be NULL) gets the selected experts of each token in
+ * descending-logit order.  x and out must not alias.  tokens = 0 is a no-op.
+ * Enqueue only; graph-capturable; stream is a cudaStream_t (NULL = legacy). */
+int moe_forward(moe_plan *plan, const uint16_t *x, int tokens, float *out,
+                int32_t *route_ids_out, void *stream);
+/* As moe_forward, also writing the route weights [T][top_k] (float) and the
+ * normalised activations x_hat [T][H] (bf16) when those pointers are non-NULL. */
+int moe_forward_ex(moe_plan *plan, const uint16_t *x, int tokens, float *out,
+                   int32_t *route_ids_out, float *route_w_out, uint16_t *xhat_out, void *stream);
+
+/* Per-expert token counts of the last forward: int32 [n_experts] (device), enqueued. */
+int moe_get_expert_counts(const moe_plan *plan, int32_t *dev_counts_out, void *stream);
+/* Token->expert grouping of the last forward (device outputs, enqueued):
+ * offsets [n_experts + n_shared + 1] (exclusive prefix sums of the counts),
+ * perm_token / perm_slot [tokens*(top_k + n_shared)]: the routes of each expert
+ * in ascending (token, slot) order; the shared expert comes last with slot top_k. */
+int moe_get_permutation(const moe_plan *plan, int32_t *offsets, int32_t *perm_token,
+                        int32_t *perm_slot, void *stream);
+/* Dequantise one expert matrix (which: 0 gate, 1 up, 2 down; expert = n_experts
+ * selects the shared expert) to float [rows][cols] on the device.  Test hook. */
+int moe_debug_dequant(const moe_plan *plan, int expert, int which, float *dev_out, void *stream);
+
+/* Kernel timing for benchmarks.  After moe_plan_set_i(plan, "profile", 1)
+ * every forward records a CUDA event pair around each of its kernel launches,
+ * on the forward's stream.  moe_profile_read synchronises on those events and
+ * returns, per kernel slot (0 routing + permutation, 1 gate/up + SwiGLU,
+ * 2 down + route weight, 3 combine + residual), the summed milliseconds and
+ * the launch count since the previous read (at most 4096 forwards are kept),
+ * then forgets them.  n_slots: length of the two output arrays (host). */
+int moe_profile_read(moe_plan *plan, double *total_ms, int *launches, int n_slots);
+
+/* Synchronises the stream and returns the device-side status of the plan's
+ * kernels in *status (0 = fine); clears it. */
+int moe_get_device_status(moe_plan *plan, int *status, void *stream);
+
+/* Text of the last failure on this thread ("" if none). */
+const char *moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

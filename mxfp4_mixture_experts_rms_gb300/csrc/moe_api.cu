@@ -1,0 +1,404 @@
+// moe_api.cu -- the C-ABI of include/moe.h: plan, argument checks, workspace
+// carving, weight registration and the per-forward launch sequence.
+//
+// Error conventions follow goosedump gpt_oss.rs, where every shape mismatch or
+// out-of-range route is an `Err` (`ensure!` in `mixture_of_experts_batch`,
+// `mix_expert_outputs`, the tensor validation): here every violation is a
+// negative status with a message, never a crash.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "moe_common.cuh"
+
+size_t decode_smem_bytes(bool gateup, int nt, int K);
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(MOE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+struct moe_plan {
+    BlockParams bp;
+    int max_tokens = 4096;
+    int decode_max_tokens = 16;
+    int path = 0;
+    int router_exact = 0;
+    void *ws_ptr = nullptr;
+    size_t ws_bytes = 0;
+    Workspace ws{};
+    bool have_ws = false;
+    bool have_w = false;
+    moe_weights w{};
+    MatPtrs gate{}, up{}, down{};
+    // kernel timing (profile option)
+    static constexpr int kSlots = 4, kMaxRec = 4096 * kSlots;
+    std::vector<cudaEvent_t> ev;     // 2 events per record
+    std::vector<int> rec_slot;       // slot of each pending record
+    bool profile = false;
+};
+
+namespace {
+
+struct Carve {
+    size_t off = 0;
+    template <class T>
+    T *take(char *base, size_t n) {
+        T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+        off = align256(off + n * sizeof(T));
+        return p;
+    }
+};
+
+int max_tiles_for(const moe_plan *p, int T) {
+    const int R = T * (p->bp.K + p->bp.n_shared);
+    return R / 8 + 2 * (p->bp.E + p->bp.n_shared) + 8;
+}
+
+// Lays the workspace out for T tokens; with base == nullptr only sizes it.
+size_t carve(const moe_plan *p, int T, char *base, Workspace *ws) {
+    const BlockParams &b = p->bp;
+    const size_t R = (size_t)T * (b.K + b.n_shared);
+    Carve c;
+    Workspace w{};
+    w.xhat = c.take<uint16_t>(base, (size_t)T * b.H);
+    w.xhat_mma = c.take<uint16_t>(base, (size_t)T * b.H);
+    w.ids = c.take<int32_t>(base, (size_t)T * b.K);
+    w.route_w = c.take<float>(base, (size_t)T * b.K);
+    w.counts = c.take<int32_t>(base, b.E + 1);
+    w.offsets = c.take<int32_t>(base, b.E + 2);
+    w.perm_token = c.take<int32_t>(base, R);
+    w.perm_slot = c.take<int32_t>(base, R);
+    w.perm_w = c.take<float>(base, R);
+    w.loc = c.take<int32_t>(base, R);
+    w.max_tiles = max_tiles_for(p, T);
+    w.tiles = c.take<int4>(base, w.max_tiles);
+    w.n_tiles = c.take<int32_t>(base, 4);
+    w.h = c.take<uint16_t>(base, R * b.F);
+    w.y = c.take<float>(base, R * b.H);
+    w.status = c.take<int32_t>(base, 4);
+    w.ticket = c.take<uint32_t>(base, 4);
+    if (ws) *ws = w;
+    return c.off;
+}
+
+MatPtrs mat_of(const moe_mxfp4_matrix &m, const moe_mxfp4_matrix &sh, int rows, int cols) {
+    MatPtrs r;
+    r.codes = m.codes;
+    r.scales = m.scales;
+    r.bias = m.bias;
+    r.sh_codes = sh.codes;
+    r.sh_scales = sh.scales;
+    r.sh_bias = sh.bias;
+    r.rows = rows;
+    r.cols = cols;
+    return r;
+}
+
+int check_matrix(const moe_mxfp4_matrix &m, const char *name) {
+    if (!m.codes || !m.scales || !m.bias) return fail(MOE_EINVAL, "%s: NULL pointer", name);
+    if (!aligned16(m.codes) || !aligned16(m.scales) || !aligned16(m.bias))
+        return fail(MOE_EINVAL, "%s: pointers must be 16-byte aligned", name);
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_last_error(void) { return g_err; }
+
+moe_plan *moe_plan_create(int hidden, int expert_hidden, int n_experts, int top_k, float swiglu_alpha,
+                          float swiglu_limit, float weight_scale) {
+    if (hidden <= 0 || hidden % 32 || expert_hidden <= 0 || expert_hidden % 32) {
+        fail(MOE_ESHAPE, "hidden and expert_hidden must be positive multiples of 32 (got %d, %d)", hidden,
+             expert_hidden);
+        return nullptr;
+    }
+    if (n_experts < 1 || n_experts > MOE_MAX_EXPERTS) {
+        fail(MOE_ESHAPE, "n_experts must be in [1, %d] (got %d)", MOE_MAX_EXPERTS, n_experts);
+        return nullptr;
+    }
+    if (top_k < 1 || top_k > n_experts || top_k > MOE_MAX_TOPK) {
+        fail(MOE_ESHAPE, "top_k must be in [1, min(n_experts, %d)] (got %d)", MOE_MAX_TOPK, top_k);
+        return nullptr;
+    }
+    if (!(swiglu_limit > 0.f) || !(swiglu_alpha == swiglu_alpha) || !(weight_scale == weight_scale)) {
+        fail(MOE_EINVAL, "swiglu_limit must be > 0 and alpha, weight_scale finite");
+        return nullptr;
+    }
+    moe_plan *p = new (std::nothrow) moe_plan();
+    if (!p) {
+        fail(MOE_ENOMEM, "out of host memory");
+        return nullptr;
+    }
+    p->bp.H = hidden;
+    p->bp.F = expert_hidden;
+    p->bp.E = n_experts;
+    p->bp.K = top_k;
+    p->bp.n_shared = 0;
+    p->bp.alpha = swiglu_alpha;
+    p->bp.limit = swiglu_limit;
+    p->bp.wscale = weight_scale;
+    p->bp.eps = 1e-5;
+    g_err[0] = 0;
+    return p;
+}
+
+void moe_plan_destroy(moe_plan *plan) {
+    if (!plan) return;
+    for (auto &e : plan->ev) cudaEventDestroy(e);
+    delete plan;
+}
+
+int moe_plan_set_i(moe_plan *p, const char *key, long long v) {
+    if (!p || !key) return fail(MOE_EINVAL, "NULL plan or key");
+    if (!strcmp(key, "n_shared_experts")) {
+        if (v != 0 && v != 1) return fail(MOE_EINVAL, "n_shared_experts must be 0 or 1");
+        if (p->have_ws) return fail(MOE_EINVAL, "n_shared_experts must be set before moe_set_workspace");
+        p->bp.n_shared = (int)v;
+        p->have_w = false;
+    } else if (!strcmp(key, "max_tokens")) {
+        if (v < 1 || v > (1 << 20)) return fail(MOE_EINVAL, "max_tokens must be in [1, 2^20]");
+        if (p->have_ws) return fail(MOE_EINVAL, "max_tokens must be set before moe_set_workspace");
+        p->max_tokens = (int)v;
+    } else if (!strcmp(key, "decode_max_tokens")) {
+        if (v < 0 || v > (1 << 20)) return fail(MOE_EINVAL, "decode_max_tokens out of range");
+        p->decode_max_tokens = (int)v;
+    } else if (!strcmp(key, "path")) {
+        if (v < 0 || v > 2) return fail(MOE_EINVAL, "path must be 0, 1 or 2");
+        p->path = (int)v;
+    } else if (!strcmp(key, "router_exact")) {
+        p->router_exact = v ? 1 : 0;
+    } else if (!strcmp(key, "profile")) {
+        if (v && p->ev.empty()) {
+            p->ev.resize(2 * moe_plan::kMaxRec);
+            for (auto &e : p->ev)
+                if (cudaEventCreate(&e) != cudaSuccess) return fail(MOE_ECUDA, "cudaEventCreate failed");
+        }
+        p->profile = v != 0;
+        p->rec_slot.clear();
+    } else {
+        return fail(MOE_EINVAL, "unknown integer option '%s'", key);
+    }
+    return MOE_OK;
+}
+
+int moe_plan_set_f(moe_plan *p, const char *key, double v) {
+    if (!p || !key) return fail(MOE_EINVAL, "NULL plan or key");
+    if (!strcmp(key, "rms_eps")) {
+        if (!(v >= 0.0)) return fail(MOE_EINVAL, "rms_eps must be >= 0");
+        p->bp.eps = v;
+    } else {
+        return fail(MOE_EINVAL, "unknown floating option '%s'", key);
+    }
+    return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_plan *p, int max_tokens) {
+    if (!p) {
+        fail(MOE_EINVAL, "NULL plan");
+        return 0;
+    }
+    int T = max_tokens > 0 ? max_tokens : p->max_tokens;
+    return carve(p, T, nullptr, nullptr);
+}
+
+int moe_set_workspace(moe_plan *p, void *dev_ptr, size_t bytes) {
+    if (!p || !dev_ptr) return fail(MOE_EINVAL, "NULL plan or workspace");
+    if (((uintptr_t)dev_ptr & 255u) != 0) return fail(MOE_EINVAL, "workspace must be 256-byte aligned");
+    size_t need = carve(p, p->max_tokens, nullptr, nullptr);
+    if (bytes < need) return fail(MOE_ENOMEM, "workspace too small: %zu < %zu bytes", bytes, need);
+    carve(p, p->max_tokens, static_cast<char *>(dev_ptr), &p->ws);
+    cudaError_t e = cudaMemset(p->ws.status, 0, 16);
+    if (e == cudaSuccess) e = cudaMemset(p->ws.ticket, 0, 16);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "moe_set_workspace");
+    p->ws_ptr = dev_ptr;
+    p->ws_bytes = bytes;
+    p->have_ws = true;
+    return MOE_OK;
+}
+
+int moe_load_weights(moe_plan *p, const moe_weights *w) {
+    if (!p || !w) return fail(MOE_EINVAL, "NULL plan or weights");
+    if (!w->gamma || !w->router_w || !w->router_b) return fail(MOE_EINVAL, "NULL gamma/router pointer");
+    if (!aligned16(w->gamma) || !aligned16(w->router_w) || !aligned16(w->router_b))
+        return fail(MOE_EINVAL, "gamma/router pointers must be 16-byte aligned");
+    int rc;
+    if ((rc = check_matrix(w->gate, "gate")) || (rc = check_matrix(w->up, "up")) ||
+        (rc = check_matrix(w->down, "down")))
+        return rc;
+    if (p->bp.n_shared) {
+        if ((rc = check_matrix(w->sh_gate, "sh_gate")) || (rc = check_matrix(w->sh_up, "sh_up")) ||
+            (rc = check_matrix(w->sh_down, "sh_down")))
+            return rc;
+    }
+    const BlockParams &b = p->bp;
+    // reject the NaN scale code (0xFF) up front
+    int32_t *flag = nullptr;
+    cudaError_t e = cudaMalloc(&flag, 4);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_load_weights");
+    e = cudaMemset(flag, 0, 4);
+    const size_t n_gu = (size_t)b.F * (b.H / 32), n_d = (size_t)b.H * (b.F / 32);
+    const moe_mxfp4_matrix *ms[6] = {&w->gate, &w->up, &w->down, &w->sh_gate, &w->sh_up, &w->sh_down};
+    for (int i = 0; i < (b.n_shared ? 6 : 3) && e == cudaSuccess; i++) {
+        size_t n = (i % 3 == 2 ? n_d : n_gu) * (i < 3 ? b.E : 1);
+        e = launch_scan_scales(ms[i]->scales, n, flag, 0);
+    }
+    int32_t h = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&h, flag, 4, cudaMemcpyDeviceToHost);
+    cudaFree(flag);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_load_weights scale scan");
+    if (h) return fail(MOE_EINVAL, "an E8M0 scale holds the NaN code 0xFF");
+    p->w = *w;
+    p->gate = mat_of(w->gate, w->sh_gate, b.F, b.H);
+    p->up = mat_of(w->up, w->sh_up, b.F, b.H);
+    p->down = mat_of(w->down, w->sh_down, b.H, b.F);
+    p->have_w = true;
+    return MOE_OK;
+}
+
+int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32_t *ids_out, float *rw_out,
+                   uint16_t *xhat_out, void *stream) {
+    if (!p) return fail(MOE_EINVAL, "NULL plan");
+    if (tokens < 0) return fail(MOE_EINVAL, "tokens must be >= 0");
+    if (tokens == 0) return MOE_OK;
+    if (!x || !out) return fail(MOE_EINVAL, "NULL x or out");
+    if (!p->have_w) return fail(MOE_ENOTREADY, "moe_load_weights has not been called");
+    if (!p->have_ws) return fail(MOE_ENOTREADY, "moe_set_workspace has not been called");
+    if (tokens > p->max_tokens) return fail(MOE_ENOMEM, "tokens %d > max_tokens %d", tokens, p->max_tokens);
+    if (!aligned16(x) || !aligned16(out)) return fail(MOE_EINVAL, "x and out must be 16-byte aligned");
+    const BlockParams &b = p->bp;
+    const char *xb = reinterpret_cast<const char *>(x), *ob = reinterpret_cast<const char *>(out);
+    if (xb < ob + (size_t)tokens * b.H * 4 && ob < xb + (size_t)tokens * b.H * 2)
+        return fail(MOE_EINVAL, "x and out must not alias");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool decode = p->path == 1 || (p->path == 0 && tokens <= p->decode_max_tokens);
+    const int nt = tokens <= 8 ? 1 : 2;
+    const int tile_rows = decode ? 8 * nt : 8 * nt;  // prefill tiles: see launch_prefill
+    auto mark = [&](int slot, bool begin) {
+        if (!p->profile) return;
+        if (begin) {
+            if ((int)p->rec_slot.size() >= moe_plan::kMaxRec) return;
+            p->rec_slot.push_back(slot);
+            cudaEventRecord(p->ev[2 * (p->rec_slot.size() - 1)], st);
+        } else if (!p->rec_slot.empty() && p->rec_slot.back() == slot) {
+            cudaEventRecord(p->ev[2 * (p->rec_slot.size() - 1) + 1], st);
+        }
+    };
+    mark(0, true);
+    cudaError_t e = launch_route(b, p->ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, rw_out,
+                                 xhat_out, tile_rows, p->router_exact, 1, st);
+    mark(0, false);
+    if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
+    mark(1, true);
+    e = launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, st);
+    mark(1, false);
+    if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
+    mark(2, true);
+    e = launch_decode_stage(b, p->ws, p->down, p->down, false, tokens, nt, st);
+    mark(2, false);
+    if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
+    mark(3, true);
+    e = launch_combine(b, p->ws, x, tokens, out, st);
+    mark(3, false);
+    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    return MOE_OK;
+}
+
+int moe_forward(moe_plan *p, const uint16_t *x, int tokens, float *out, int32_t *ids_out, void *stream) {
+    return moe_forward_ex(p, x, tokens, out, ids_out, nullptr, nullptr, stream);
+}
+
+int moe_get_expert_counts(const moe_plan *p, int32_t *dev_counts_out, void *stream) {
+    if (!p || !dev_counts_out) return fail(MOE_EINVAL, "NULL argument");
+    if (!p->have_ws) return fail(MOE_ENOTREADY, "no workspace");
+    cudaError_t e = cudaMemcpyAsync(dev_counts_out, p->ws.counts, sizeof(int32_t) * p->bp.E,
+                                    cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_get_expert_counts");
+}
+
+int moe_get_permutation(const moe_plan *p, int32_t *offsets, int32_t *perm_token, int32_t *perm_slot,
+                        void *stream) {
+    if (!p || !offsets || !perm_token || !perm_slot) return fail(MOE_EINVAL, "NULL argument");
+    if (!p->have_ws) return fail(MOE_ENOTREADY, "no workspace");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int EE = p->bp.E + p->bp.n_shared;
+    // route count of the last forward = offsets[EE]; copy the maximum extent
+    const size_t R = (size_t)p->max_tokens * (p->bp.K + p->bp.n_shared);
+    cudaError_t e = cudaMemcpyAsync(offsets, p->ws.offsets, sizeof(int32_t) * (EE + 1), cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(perm_token, p->ws.perm_token, sizeof(int32_t) * R, cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(perm_slot, p->ws.perm_slot, sizeof(int32_t) * R, cudaMemcpyDeviceToDevice, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_get_permutation");
+}
+
+int moe_debug_dequant(const moe_plan *p, int expert, int which, float *dev_out, void *stream) {
+    if (!p || !dev_out) return fail(MOE_EINVAL, "NULL argument");
+    if (!p->have_w) return fail(MOE_ENOTREADY, "moe_load_weights has not been called");
+    if (which < 0 || which > 2) return fail(MOE_EINVAL, "which must be 0 (gate), 1 (up) or 2 (down)");
+    if (expert < 0 || expert > p->bp.E || (expert == p->bp.E && !p->bp.n_shared))
+        return fail(MOE_EINVAL, "expert %d out of range", expert);
+    const MatPtrs &m = which == 0 ? p->gate : which == 1 ? p->up : p->down;
+    cudaError_t e = launch_dequant(m, expert, p->bp.E, dev_out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_debug_dequant");
+}
+
+int moe_profile_read(moe_plan *p, double *total_ms, int *launches, int n_slots) {
+    if (!p || !total_ms || !launches || n_slots < 0) return fail(MOE_EINVAL, "NULL argument");
+    for (int i = 0; i < n_slots; i++) {
+        total_ms[i] = 0.0;
+        launches[i] = 0;
+    }
+    for (size_t r = 0; r < p->rec_slot.size(); r++) {
+        cudaError_t e = cudaEventSynchronize(p->ev[2 * r + 1]);
+        float ms = 0.f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, p->ev[2 * r], p->ev[2 * r + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_profile_read");
+        int s = p->rec_slot[r];
+        if (s < n_slots) {
+            total_ms[s] += ms;
+            launches[s] += 1;
+        }
+    }
+    p->rec_slot.clear();
+    return MOE_OK;
+}
+
+int moe_get_device_status(moe_plan *p, int *status, void *stream) {
+    if (!p || !status) return fail(MOE_EINVAL, "NULL argument");
+    if (!p->have_ws) return fail(MOE_ENOTREADY, "no workspace");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t h[4] = {0, 0, 0, 0};
+    cudaError_t e = cudaMemcpyAsync(h, p->ws.status, 16, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->ws.status, 0, 16, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_get_device_status");
+    *status = h[0];
+    if (h[0]) return fail(MOE_EDEVICE, "device status %d (detail %d)", h[0], h[1]);
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,127 @@
+// moe_common.cuh -- shared device helpers and the plan's kernel parameters.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define MOE_MAX_TOPK 8
+#define MOE_MAX_EXPERTS 256
+
+// Device status codes written into MoeWorkspace::status[0]
+#define MOE_DEV_OK 0
+#define MOE_DEV_WAIT_TIMEOUT 1
+#define MOE_DEV_BAD_ROUTE 2
+
+// Pointers to one expert matrix of all experts plus the shared expert.
+struct MatPtrs {
+    const uint8_t *codes;     // [E][rows][cols/2]
+    const uint8_t *scales;    // [E][rows][cols/32]
+    const float *bias;        // [E][rows]
+    const uint8_t *sh_codes;  // shared expert (index E), may be null
+    const uint8_t *sh_scales;
+    const float *sh_bias;
+    int rows, cols;
+};
+
+__device__ __forceinline__ const uint8_t *mat_codes(const MatPtrs &m, int e, int n_experts) {
+    return e < n_experts ? m.codes + (size_t)e * m.rows * (m.cols / 2) : m.sh_codes;
+}
+__device__ __forceinline__ const uint8_t *mat_scales(const MatPtrs &m, int e, int n_experts) {
+    return e < n_experts ? m.scales + (size_t)e * m.rows * (m.cols / 32) : m.sh_scales;
+}
+__device__ __forceinline__ const float *mat_bias(const MatPtrs &m, int e, int n_experts) {
+    return e < n_experts ? m.bias + (size_t)e * m.rows : m.sh_bias;
+}
+
+// Device-side view of the workspace carved by the host plan.
+struct Workspace {
+    uint16_t *xhat;        // [T][H] bf16
+    uint16_t *xhat_mma;    // [T][H] bf16, 32-blocks reordered for the decode MMA fragments
+    int32_t *ids;          // [T][K]
+    float *route_w;        // [T][K]
+    int32_t *counts;       // [E + 1] (index E: shared expert)
+    int32_t *offsets;      // [E + 2]
+    int32_t *perm_token;   // [R]
+    int32_t *perm_slot;    // [R]
+    float *perm_w;         // [R]
+    int32_t *loc;          // [T][K + n_shared]
+    int4 *tiles;           // [max_tiles]: (expert, route start, route count, 0)
+    int32_t *n_tiles;      // [1]
+    uint16_t *h;           // [R][F] bf16 (layout depends on the path)
+    float *y;              // [R][H] weighted expert outputs
+    int32_t *status;       // [4] device error flag + detail
+    uint32_t *ticket;      // [1] last-block counter of the routing kernel
+    int max_tiles;
+};
+
+struct BlockParams {
+    int H, F, E, K, n_shared;
+    float alpha, limit, wscale;
+    double eps;
+};
+
+// bf16 bits <-> float
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// Round a double to bf16 with one rounding (nearest, ties to even), working on
+// the IEEE-754 bit pattern: keep 7 fraction bits in the normal range, quantum
+// 2^-133 below 2^-126.
+__device__ __forceinline__ uint16_t bf16_from_double_rne(double v) {
+    unsigned long long b = (unsigned long long)__double_as_longlong(v);
+    uint16_t sign = (uint16_t)((b >> 48) & 0x8000u);
+    unsigned long long a = b & 0x7FFFFFFFFFFFFFFFull;
+    if (a > 0x7FF0000000000000ull) return 0x7FC0;            // NaN
+    if (a >= (897ull << 52)) {                                 // |v| >= 2^-126
+        unsigned long long lsb = (a >> 45) & 1ull;
+        a += 0x00000FFFFFFFFFFFull + lsb;                      // 2^44 - 1 + lsb
+        a &= ~0x00001FFFFFFFFFFFull;                           // clear 45 bits
+        long long ex = (long long)(a >> 52) - 1023;
+        if (ex > 127) return sign | 0x7F80;                    // overflow / inf
+        return sign | (uint16_t)(((ex + 127) << 7) | ((a >> 45) & 0x7F));
+    }
+    double m = rint(__longlong_as_double((long long)a) * 0x1p133);  // exact scaling
+    return sign | (uint16_t)m;                                 // m in [0, 128]
+}
+
+__device__ __forceinline__ void set_device_error(int32_t *status, int code, int detail) {
+    if (atomicCAS(status, 0, code) == 0) status[1] = detail;
+}
+
+// Clamped SwiGLU (gate clamped from above, up to [-L, L]); NaN propagates.
+__device__ __forceinline__ float swiglu_clamped(float g, float u, float alpha, float limit) {
+    float gc = (g > limit) ? limit : g;
+    float uc = (u > limit) ? limit : ((u < -limit) ? -limit : u);
+    float glu = gc / (1.0f + expf(-alpha * gc));
+    return glu * (uc + 1.0f);
+}
+
+// Position of element j inside its 32-element block in the decode-MMA order:
+// element 8q + i + 4hh (q, i in 0..3, hh in 0..1) goes to 8q + 2i + hh, so that
+// elements (8q+i, 8q+i+4) form one bf16x2 pair, matching the nibble pairs the
+// dequantiser extracts from one 32-bit word of codes.
+__device__ __forceinline__ int mma_perm_pos(int j) {
+    int b = j & ~31, e = j & 31;
+    int q = e >> 3, r = e & 7, i = r & 3, hh = r >> 2;
+    return b + (q << 3) + (i << 1) + hh;
+}
+
+// Host+device-visible launch helpers
+#define MOE_CUDA_TRY(expr)                                  \
+    do {                                                    \
+        cudaError_t _e = (expr);                            \
+        if (_e != cudaSuccess) return _e;                   \
+    } while (0)
+
+// Launchers implemented in the .cu files (host side).
+cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x,
+                         const float *gamma, const uint16_t *router_w, const float *router_b,
+                         int T, int32_t *ids_out, float *rw_out, uint16_t *xhat_out, int tile_rows,
+                         int router_exact, int write_mma_layout, cudaStream_t st);
+cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
+                                const MatPtrs &a1, bool gateup, int T, int nt, cudaStream_t st);
+cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T,
+                           float *out, cudaStream_t st);
+cudaError_t launch_prefill(const BlockParams &bp, const Workspace &ws, const MatPtrs &gate,
+                           const MatPtrs &up, const MatPtrs &down, int T, cudaStream_t st);
+cudaError_t launch_dequant(const MatPtrs &m, int expert, int n_experts, float *out, cudaStream_t st);
+cudaError_t launch_scan_scales(const uint8_t *scales, size_t n, int32_t *flag, cudaStream_t st);

@@ -1,0 +1,225 @@
+"""Thin ctypes binding of ``include/moe.h`` (argument marshalling only).
+
+Every step of the block runs in the CUDA kernels of ``lib/libmoe.so``; this
+module only passes device pointers and sizes.  PyTorch provides device memory
+and streams.  There is no fallback: if the library is missing or fails to
+load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+MOE_OK, MOE_EINVAL, MOE_ESHAPE, MOE_ENOTREADY, MOE_ECUDA, MOE_ENOMEM, MOE_EDEVICE = 0, -1, -2, -3, -4, -5, -6
+_STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ESHAPE", -3: "MOE_ENOTREADY", -4: "MOE_ECUDA",
+                 -5: "MOE_ENOMEM", -6: "MOE_EDEVICE"}
+
+_lib = None
+
+EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_plan_set_i", "moe_plan_set_f", "moe_workspace_bytes",
+           "moe_set_workspace", "moe_load_weights", "moe_forward", "moe_forward_ex", "moe_get_expert_counts",
+           "moe_get_permutation", "moe_debug_dequant", "moe_profile_read", "moe_get_device_status",
+           "moe_last_error"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class Mat(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("bias", C.c_void_p)]
+
+
+class Weights(C.Structure):
+    _fields_ = [("gamma", C.c_void_p), ("router_w", C.c_void_p), ("router_b", C.c_void_p),
+                ("gate", Mat), ("up", Mat), ("down", Mat),
+                ("sh_gate", Mat), ("sh_up", Mat), ("sh_down", Mat)]
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load ``libmoe.so`` (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise MoeError(MOE_ENOTREADY, f"CUDA library not built: {_build.LIB}")
+    L = C.CDLL(_build.LIB)
+    P, I, LL, D, SZ = C.c_void_p, C.c_int, C.c_longlong, C.c_double, C.c_size_t
+    L.moe_plan_create.restype = P
+    L.moe_plan_create.argtypes = [I, I, I, I, C.c_float, C.c_float, C.c_float]
+    L.moe_plan_destroy.restype = None
+    L.moe_plan_destroy.argtypes = [P]
+    L.moe_plan_set_i.argtypes = [P, C.c_char_p, LL]
+    L.moe_plan_set_f.argtypes = [P, C.c_char_p, D]
+    L.moe_workspace_bytes.restype = SZ
+    L.moe_workspace_bytes.argtypes = [P, I]
+    L.moe_set_workspace.argtypes = [P, P, SZ]
+    L.moe_load_weights.argtypes = [P, C.POINTER(Weights)]
+    L.moe_forward.argtypes = [P, P, I, P, P, P]
+    L.moe_forward_ex.argtypes = [P, P, I, P, P, P, P, P]
+    L.moe_get_expert_counts.argtypes = [P, P, P]
+    L.moe_get_permutation.argtypes = [P, P, P, P, P]
+    L.moe_debug_dequant.argtypes = [P, I, I, P, P]
+    L.moe_get_device_status.argtypes = [P, C.POINTER(I), P]
+    L.moe_profile_read.argtypes = [P, C.POINTER(C.c_double), C.POINTER(I), I]
+    L.moe_last_error.restype = C.c_char_p
+    L.moe_last_error.argtypes = []
+    for name in EXPORTS:
+        if name not in ("moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_last_error"):
+            getattr(L, name).restype = C.c_int
+    _lib = L
+    return L
+
+
+def _check(rc: int):
+    if rc != MOE_OK:
+        raise MoeError(rc, load().moe_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+class DeviceBlock:
+    """Device copies (torch tensors) of one block's weights, in the canonical layout."""
+
+    def __init__(self, blk: dict, device="cuda"):
+        import torch
+        shape = blk["shape"]
+        self.shape = shape
+
+        def up(a, dt=None):
+            a = np.ascontiguousarray(a)
+            t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+            return t.to(device)
+
+        self.gamma = up(blk["gamma"])
+        self.router_w = up(blk["router_w"])
+        self.router_b = up(blk["router_b"])
+        self.mats = {m: (up(blk["codes"][m]), up(blk["scales"][m]), up(blk["bias"][m])) for m in ("gate", "up", "down")}
+        self.shared = None
+        if shape.n_shared:
+            sh = blk["shared"]
+            self.shared = {m: (up(sh["codes"][m]), up(sh["scales"][m]), up(sh["bias"][m])) for m in ("gate", "up", "down")}
+
+    def cstruct(self) -> Weights:
+        w = Weights()
+        w.gamma, w.router_w, w.router_b = _ptr(self.gamma), _ptr(self.router_w), _ptr(self.router_b)
+        for m in ("gate", "up", "down"):
+            c, s, b = self.mats[m]
+            setattr(w, m, Mat(_ptr(c), _ptr(s), _ptr(b)))
+            if self.shared is not None:
+                c, s, b = self.shared[m]
+                setattr(w, "sh_" + m, Mat(_ptr(c), _ptr(s), _ptr(b)))
+        return w
+
+
+class Plan:
+    """One block shape: owns the plan handle and a torch-allocated workspace."""
+
+    def __init__(self, shape, max_tokens: int = 4096, device="cuda", **opts):
+        self.L = load()
+        self.shape = shape
+        h = self.L.moe_plan_create(shape.hidden, shape.expert_hidden, shape.n_experts, shape.top_k,
+                                   shape.swiglu_alpha, shape.swiglu_limit, shape.weight_scale)
+        if not h:
+            raise MoeError(MOE_ESHAPE, self.L.moe_last_error().decode())
+        self.h = C.c_void_p(h)
+        self.set_i("n_shared_experts", shape.n_shared)
+        self.set_f("rms_eps", shape.rms_eps)
+        self.set_i("max_tokens", max_tokens)
+        for k, v in opts.items():
+            self.set_i(k, int(v))
+        self.max_tokens = max_tokens
+        self.device = device
+        self.ws = None
+        self.weights = None
+
+    def set_i(self, key: str, v: int):
+        _check(self.L.moe_plan_set_i(self.h, key.encode(), int(v)))
+
+    def set_f(self, key: str, v: float):
+        _check(self.L.moe_plan_set_f(self.h, key.encode(), float(v)))
+
+    def workspace_bytes(self, max_tokens: int = 0) -> int:
+        return int(self.L.moe_workspace_bytes(self.h, max_tokens))
+
+    def alloc_workspace(self):
+        import torch
+        n = self.workspace_bytes()
+        self.ws = torch.empty(n + 256, dtype=torch.uint8, device=self.device)
+        p = self.ws.data_ptr()
+        off = (-p) % 256
+        _check(self.L.moe_set_workspace(self.h, C.c_void_p(p + off), n))
+        return self
+
+    def load_weights(self, dev: DeviceBlock):
+        self.weights = dev  # keep alive
+        self._wstruct = dev.cstruct()
+        _check(self.L.moe_load_weights(self.h, C.byref(self._wstruct)))
+        return self
+
+    def forward(self, x, out, ids=None, stream=None):
+        _check(self.L.moe_forward(self.h, C.c_void_p(_ptr(x)), int(x.shape[0]), C.c_void_p(_ptr(out)),
+                                  C.c_void_p(_ptr(ids)), _stream_ptr(stream)))
+
+    def forward_ex(self, x, out, ids=None, route_w=None, xhat=None, stream=None):
+        _check(self.L.moe_forward_ex(self.h, C.c_void_p(_ptr(x)), int(x.shape[0]), C.c_void_p(_ptr(out)),
+                                     C.c_void_p(_ptr(ids)), C.c_void_p(_ptr(route_w)), C.c_void_p(_ptr(xhat)),
+                                     _stream_ptr(stream)))
+
+    def expert_counts(self, out, stream=None):
+        _check(self.L.moe_get_expert_counts(self.h, C.c_void_p(_ptr(out)), _stream_ptr(stream)))
+
+    def permutation(self, offsets, perm_token, perm_slot, stream=None):
+        _check(self.L.moe_get_permutation(self.h, C.c_void_p(_ptr(offsets)), C.c_void_p(_ptr(perm_token)),
+                                          C.c_void_p(_ptr(perm_slot)), _stream_ptr(stream)))
+
+    def debug_dequant(self, expert: int, which: int, out, stream=None):
+        _check(self.L.moe_debug_dequant(self.h, int(expert), int(which), C.c_void_p(_ptr(out)), _stream_ptr(stream)))
+
+    def profile_read(self, n_slots: int = 4):
+        """(total ms, launches) per kernel slot since the last read (profile option)."""
+        ms = (C.c_double * n_slots)()
+        cnt = (C.c_int * n_slots)()
+        _check(self.L.moe_profile_read(self.h, ms, cnt, n_slots))
+        return list(ms), list(cnt)
+
+    def device_status(self, stream=None) -> int:
+        s = C.c_int(0)
+        rc = self.L.moe_get_device_status(self.h, C.byref(s), _stream_ptr(stream))
+        if rc not in (MOE_OK, MOE_EDEVICE):
+            _check(rc)
+        return s.value
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.L.moe_plan_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,84 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library must build for sm_103a, load, export every function that
+include/moe.h declares, and reject bad arguments with the documented status
+codes before touching the device.
+"""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from mxfp4_mixture_experts_rms_gb300 import build, moe, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return moe.load()
+
+
+def test_library_exports_every_declared_function(L):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(moe.EXPORTS)
+
+
+def test_plan_create_rejects_bad_shapes(L):
+    bad = [(30, 64, 4, 2), (64, 0, 4, 2), (64, 64, 0, 1), (64, 64, 4, 5), (64, 64, 300, 4), (64, 64, 16, 9)]
+    for H, F, E, K in bad:
+        assert not L.moe_plan_create(H, F, E, K, 1.702, 7.0, 1.0)
+        assert L.moe_last_error()
+    assert not L.moe_plan_create(64, 64, 4, 2, 1.702, 0.0, 1.0)
+
+
+def test_options_and_workspace_sizing(L):
+    h = L.moe_plan_create(2880, 2880, 32, 4, 1.702, 7.0, 1.0)
+    assert h
+    h = C.c_void_p(h)
+    assert L.moe_plan_set_i(h, b"n_shared_experts", 2) == moe.MOE_EINVAL
+    assert L.moe_plan_set_i(h, b"no_such_key", 1) == moe.MOE_EINVAL
+    assert L.moe_plan_set_f(h, b"rms_eps", -1.0) == moe.MOE_EINVAL
+    assert L.moe_plan_set_i(h, b"max_tokens", 8) == moe.MOE_OK
+    small = L.moe_workspace_bytes(h, 0)
+    assert L.moe_plan_set_i(h, b"max_tokens", 512) == moe.MOE_OK
+    big = L.moe_workspace_bytes(h, 0)
+    assert 0 < small < big
+    # the per-route fp32 outputs dominate: T*K*H*4 bytes
+    assert big >= 512 * 4 * 2880 * 4
+    L.moe_plan_destroy(h)
+
+
+def test_forward_before_weights_is_not_ready(L):
+    h = C.c_void_p(L.moe_plan_create(64, 64, 4, 2, 1.702, 7.0, 1.0))
+    rc = L.moe_forward(h, C.c_void_p(256), 1, C.c_void_p(4096), None, None)
+    assert rc == moe.MOE_ENOTREADY
+    assert b"moe_load_weights" in L.moe_last_error()
+    assert L.moe_forward(h, C.c_void_p(256), -1, C.c_void_p(4096), None, None) == moe.MOE_EINVAL
+    assert L.moe_forward(h, None, 0, None, None, None) == moe.MOE_OK   # empty batch: no-op
+    assert L.moe_load_weights(h, None) == moe.MOE_EINVAL
+    w = moe.Weights()
+    assert L.moe_load_weights(h, C.byref(w)) == moe.MOE_EINVAL       # NULL pointers
+    w.gamma = w.router_w = w.router_b = 0x1001                        # misaligned
+    assert L.moe_load_weights(h, C.byref(w)) == moe.MOE_EINVAL
+    assert L.moe_set_workspace(h, C.c_void_p(0x1008), 1 << 20) == moe.MOE_EINVAL  # misaligned
+    assert L.moe_debug_dequant(h, 0, 0, C.c_void_p(256), None) == moe.MOE_ENOTREADY
+    L.moe_plan_destroy(h)
+
+
+def test_generated_shapes_match_layout():
+    blk = synth.make_block(0)
+    assert blk["codes"]["gate"].shape == (32, 2880, 1440)
+    assert blk["scales"]["down"].shape == (32, 2880, 90)
+    assert synth.expert_bytes(synth.GPT_OSS) == 3 * (2880 * 1440 + 2880 * 90)

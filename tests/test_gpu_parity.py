@@ -1,0 +1,173 @@
+"""GPU parity: the CUDA library (through the C-ABI) against the CPU oracle.
+
+Bit-exact: MXFP4 dequantisation, x_hat, expert ids, per-expert counts and the
+token->expert permutation.  Within tolerance (relative L2 <= 1e-3 and max abs
+<= 2e-3 * max|ref|): the block output and the MoE delta.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from mxfp4_mixture_experts_rms_gb300 import moe, synth
+
+from gpu_helpers import (NTHREADS, check_close, check_permutation, oracle_routes, run_gpu, tiny_block)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.load()
+
+
+# ------------------------------------------------------------- dequantisation
+def test_dequant_bitexact_all_codes_and_exponents():
+    import torch
+    # gate rows r = 0..252 carry E8M0 exponent r, each row holds all 16 codes twice
+    shape = synth.tiny_shape(32, 256, 1, 1)
+    blk = tiny_block(1, shape)
+    nib = np.arange(32) % 16
+    row = (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8)
+    blk["codes"]["gate"][0] = row[None, :]
+    sc = np.minimum(np.arange(256), 252).astype(np.uint8)
+    blk["scales"]["gate"][0] = sc[:, None]
+    dev = moe.DeviceBlock(blk)
+    plan = moe.Plan(shape, max_tokens=1).alloc_workspace().load_weights(dev)
+    out = torch.empty((256, 32), dtype=torch.float32, device="cuda")
+    plan.debug_dequant(0, 0, out)
+    torch.cuda.synchronize()
+    want = oracle.mxfp4_dequant(blk["codes"]["gate"][0], blk["scales"]["gate"][0]).astype(np.float32)
+    got = out.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("cfg", [0, 4])
+def test_dequant_bitexact_workload_weights(cfg):
+    import torch
+    blk = synth.make_block(cfg)
+    shape = blk["shape"]
+    dev = moe.DeviceBlock(blk)
+    plan = moe.Plan(shape, max_tokens=1).alloc_workspace().load_weights(dev)
+    experts = [0, 5, shape.n_experts - 1] + ([shape.n_experts] if shape.n_shared else [])
+    for e in experts:
+        for which, m in enumerate(synth.MATS):
+            rows, cols = shape.mat_shape(m)
+            out = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+            plan.debug_dequant(e, which, out)
+            src = blk["shared"] if e == shape.n_experts else None
+            codes = src["codes"][m][0] if src else blk["codes"][m][e]
+            scales = src["scales"][m][0] if src else blk["scales"][m][e]
+            want = oracle.mxfp4_dequant(codes, scales).astype(np.float32)
+            assert np.array_equal(out.cpu().numpy(), want), (e, m)
+
+
+# --------------------------------------------------------------------- routing
+@pytest.mark.parametrize("cfg,T", [(0, 1), (1, 8), (3, 128), (4, 40)])
+def test_routing_bitexact(cfg, T):
+    blk = synth.make_block(cfg)
+    x = synth.make_tokens(cfg, T, blk["shape"].hidden)
+    r, plan, _ = run_gpu(blk, x)
+    ids, rw, xh = oracle_routes(blk, x)
+    assert r["status"] == 0
+    assert np.array_equal(r["xhat"], xh)
+    assert np.array_equal(r["ids"], ids)
+    np.testing.assert_allclose(r["route_w"], rw, rtol=2e-6, atol=1e-7)
+    check_permutation(r, ids, blk["shape"])
+
+
+def test_router_exact_mode_gives_same_routes():
+    blk = synth.make_block(3)
+    x = synth.make_tokens(3, 64, 2880)
+    a, _, dev = run_gpu(blk, x)
+    b, _, _ = run_gpu(blk, x, dev=dev, router_exact=1)
+    assert np.array_equal(a["ids"], b["ids"])
+    np.testing.assert_allclose(a["route_w"], b["route_w"], rtol=2e-6)
+
+
+def test_routing_near_ties_are_resolved_exactly():
+    # two router rows identical except one tiny bf16 step: fp32 cannot order them
+    # reliably, the certified path must fall back to exact logits
+    shape = synth.tiny_shape(256, 64, 8, 2)
+    blk = tiny_block(3, shape)
+    blk["router_w"][1] = blk["router_w"][0]
+    blk["router_w"][1, 7] ^= 1
+    blk["router_b"][:] = 0
+    blk["router_b"][[0, 1]] = 5.0
+    x = synth.make_tokens(3, 33, 256)
+    r, _, _ = run_gpu(blk, x)
+    ids, _, _ = oracle_routes(blk, x)
+    assert np.array_equal(r["ids"], ids)
+
+
+# ------------------------------------------------------------------ full block
+@pytest.mark.parametrize("H,F,E,K,T,ns,scale", [
+    (64, 96, 5, 3, 1, 0, 1.0), (64, 96, 5, 3, 3, 0, 1.0), (96, 64, 5, 3, 9, 0, 1.0),
+    (64, 96, 5, 3, 17, 1, 1.5), (128, 64, 8, 2, 33, 0, 1.0), (32, 32, 4, 2, 40, 1, 2.5),
+    (64, 64, 1, 1, 5, 0, 1.0), (160, 96, 16, 8, 12, 0, 1.0)])
+def test_block_parity_ragged_shapes(H, F, E, K, T, ns, scale):
+    shape = synth.tiny_shape(H, F, E, K, n_shared=ns, weight_scale=scale)
+    blk = tiny_block(H * 7 + T, shape)
+    x = synth.f32_to_bf16_bits(np.random.default_rng(T).normal(0, 1, (T, H)))
+    r, _, _ = run_gpu(blk, x)
+    ref = oracle.moe_forward(blk, x, nthreads=NTHREADS)
+    assert r["status"] == 0
+    assert np.array_equal(r["ids"], ref["ids"])
+    check_close(r["out"], ref["out"], x)
+
+
+@pytest.mark.parametrize("cfg,T", [(0, 1), (1, 8), (4, 1)])
+def test_block_parity_workloads(cfg, T):
+    blk = synth.make_block(cfg)
+    x = synth.make_tokens(cfg, T, blk["shape"].hidden)
+    r, _, _ = run_gpu(blk, x)
+    ref = oracle.moe_forward(blk, x, nthreads=NTHREADS)
+    assert np.array_equal(r["ids"], ref["ids"])
+    check_close(r["out"], ref["out"], x)
+
+
+@pytest.mark.parametrize("cfg,T,n_sample", [(3, 128, 12), (4, 64, 6)])
+def test_block_parity_sampled_tokens(cfg, T, n_sample):
+    blk = synth.make_block(cfg)
+    x = synth.make_tokens(cfg, T, blk["shape"].hidden)
+    r, _, _ = run_gpu(blk, x)
+    sample = np.random.default_rng(cfg).choice(T, n_sample, replace=False)
+    ref = oracle.moe_forward(blk, np.ascontiguousarray(x[sample]), nthreads=NTHREADS)
+    assert np.array_equal(r["ids"][sample], ref["ids"])
+    check_close(r["out"][sample], ref["out"], x[sample])
+
+
+def test_edge_token_counts():
+    import torch
+    shape = synth.tiny_shape(64, 64, 4, 2)
+    blk = tiny_block(5, shape)
+    plan = moe.Plan(shape, max_tokens=4).alloc_workspace().load_weights(moe.DeviceBlock(blk))
+    x = torch.zeros((5, 64), dtype=torch.int16, device="cuda")
+    out = torch.empty((5, 64), dtype=torch.float32, device="cuda")
+    plan.forward(x[:0], out[:0])                     # empty batch: no-op
+    with pytest.raises(moe.MoeError) as ei:
+        plan.forward(x, out)                         # above max_tokens
+    assert ei.value.status == moe.MOE_ENOMEM
+    with pytest.raises(moe.MoeError):
+        plan.forward(x[:2], x[:2].view(torch.float32).view(2, 32))  # x aliases out
+    assert plan.device_status() == 0
+
+
+def test_nan_scale_rejected_at_load():
+    shape = synth.tiny_shape(64, 64, 4, 2)
+    blk = tiny_block(6, shape)
+    blk["scales"]["down"][2, 5, 1] = 0xFF
+    plan = moe.Plan(shape, max_tokens=4).alloc_workspace()
+    with pytest.raises(moe.MoeError) as ei:
+        plan.load_weights(moe.DeviceBlock(blk))
+    assert ei.value.status == moe.MOE_EINVAL
+
+
+def test_repeated_forward_is_deterministic():
+    blk = synth.make_block(1)
+    x = synth.make_tokens(1, 8, 2880)
+    a, plan, dev = run_gpu(blk, x)
+    b, _, _ = run_gpu(blk, x, plan=plan, dev=dev)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["ids"], b["ids"])
