@@ -295,9 +295,13 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     if (xb < ob + (size_t)tokens * b.H * 4 && ob < xb + (size_t)tokens * b.H * 2)
         return fail(MOE_EINVAL, "x and out must not alias");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool decode = p->path == 1 || (p->path == 0 && tokens <= p->decode_max_tokens);
+    // The tensor-core grouped GEMM needs H and F in whole 64-element stages;
+    // other shapes always take the GEMV path (which handles any token count).
+    const bool prefill_ok = b.H % 64 == 0 && b.F % 64 == 0;
+    if (p->path == 2 && !prefill_ok) return fail(MOE_ESHAPE, "the prefill path needs H and F multiples of 64");
+    const bool decode = !prefill_ok || p->path == 1 || (p->path == 0 && tokens <= p->decode_max_tokens);
     const int nt = tokens <= 8 ? 1 : 2;
-    const int tile_rows = decode ? 8 * nt : 8 * nt;  // prefill tiles: see launch_prefill
+    const int tile_rows = decode ? 8 * nt : prefill_tile_rows();
     auto mark = [&](int slot, bool begin) {
         if (!p->profile) return;
         if (begin) {
@@ -314,11 +318,13 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     mark(0, false);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     mark(1, true);
-    e = launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, st);
+    e = decode ? launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, st)
+               : launch_prefill_stage(b, p->ws, p->gate, p->up, true, tokens, st);
     mark(1, false);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
     mark(2, true);
-    e = launch_decode_stage(b, p->ws, p->down, p->down, false, tokens, nt, st);
+    e = decode ? launch_decode_stage(b, p->ws, p->down, p->down, false, tokens, nt, st)
+               : launch_prefill_stage(b, p->ws, p->down, p->down, false, tokens, st);
     mark(2, false);
     if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
     mark(3, true);

@@ -121,7 +121,8 @@ cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, cons
                                 const MatPtrs &a1, bool gateup, int T, int nt, cudaStream_t st);
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T,
                            float *out, cudaStream_t st);
-cudaError_t launch_prefill(const BlockParams &bp, const Workspace &ws, const MatPtrs &gate,
-                           const MatPtrs &up, const MatPtrs &down, int T, cudaStream_t st);
+cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
+                                 const MatPtrs &a1, bool gateup, int T, cudaStream_t st);
+int prefill_tile_rows();
 cudaError_t launch_dequant(const MatPtrs &m, int expert, int n_experts, float *out, cudaStream_t st);
 cudaError_t launch_scan_scales(const uint8_t *scales, size_t n, int32_t *flag, cudaStream_t st);

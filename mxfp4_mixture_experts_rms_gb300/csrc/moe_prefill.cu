@@ -1,0 +1,442 @@
+// moe_prefill.cu -- prefill path: grouped per-expert GEMMs on the 5th-gen
+// tensor cores (tcgen05.mma kind::f16, bf16 operands in shared memory, fp32
+// accumulators in TMEM), with MXFP4 weight tiles staged by TMA and
+// dequantised to bf16 in shared memory.
+//
+// goosedump gpt_oss.rs `expert_batch_output` gathers the routed rows of one
+// expert and runs `matrix_matrix_pair(gate, up)` + bias, `swiglu_inplace`,
+// `matrix_matrix(down)` + bias and the route weight; `mix_expert_outputs`
+// then sums each token's slots.  Here one CTA computes one (expert tile of
+// <= 128 routes) x (weight row tile) block:
+//
+//   gate/up kernel: A = [64 gate rows ; the same 64 up rows] (M = 128),
+//                   B = the tile's x_hat rows, D = TMEM [128 lanes][N];
+//                   epilogue: bias + clamped SwiGLU -> h (bf16)
+//   down kernel:    A = 128 rows of Wd, B = the tile's h rows;
+//                   epilogue: bias, times the route weight -> per-route fp32
+//
+// Warp roles (192 threads): warp 0 issues the TMA loads of the packed codes;
+// warp 1 owns TMEM and issues the MMAs (one elected lane); warps 2..5
+// dequantise A, stage B, and run the epilogue.  A 4-stage mbarrier ring
+// connects them.  Activations use the same 32-block pair order as the decode
+// path (x_hat_mma / h), and A is written in that order straight from the
+// nibble-pair dequantiser, so the K permutation cancels in every dot product.
+//
+// Every wait is bounded (about 2 s of %globaltimer); on a timeout the kernel
+// records MOE_DEV_WAIT_TIMEOUT in the status word, drains what it issued,
+// frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include "moe_common.cuh"
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBK = 64;            // K elements per stage (one 128-byte swizzle row of bf16)
+constexpr int kBN = 128;           // max routes per tile
+constexpr int kThreads = 192;
+constexpr int kABytes = 128 * 128;     // A stage: 128 rows x 128 B
+constexpr int kBBytes = kBN * 128;     // B stage
+constexpr int kFp4Bytes = 128 * 32;    // packed codes of one stage
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct PrefillArgs {
+    BlockParams bp;
+    Workspace ws;
+    MatPtrs A0, A1;     // gate, up (GATEUP) or down
+    int Kdim;           // H (gate/up) or F (down)
+    int rows;           // F (gate/up) or H (down)
+};
+
+struct TmaMaps {
+    CUtensorMap a0, a1, sh0, sh1;  // routed and shared codes of A0 / A1
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(smem_u32(b)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: false (and the status word set) after ~2 s or when another
+// thread of the grid already reported a failure.
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int32_t *status, int where) {
+    if (mbar_try(b, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0;; i++) {
+        if (mbar_try(b, parity)) return true;
+        if ((i & 63) == 63) {
+            if (*(volatile int32_t *)status != 0) return false;
+            if (globaltimer() - t0 > kWaitNs) {
+                set_device_error(status, MOE_DEV_WAIT_TIMEOUT, where);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+        "[%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+    d |= (uint64_t)1 << 46;              // descriptor version
+    d |= (uint64_t)2 << 61;              // SWIZZLE_128B
+    return d;
+}
+// Instruction descriptor, kind::f16: D f32, A/B bf16, both K-major, M x N.
+__host__ __device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dtmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------- dequantisation
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+    __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+// 8 nibbles -> 4 bf16x2 in pair order (nibble i, nibble i+4), value*2^(s-127).
+__device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s1, uint32_t s2, bool big) {
+    uint32_t p0 = ((w << 6) & 0x01C001C0u) | ((w << 12) & 0x80008000u);
+    uint32_t p1 = ((w << 2) & 0x01C001C0u) | ((w << 8) & 0x80008000u);
+    uint32_t p2 = ((w >> 2) & 0x01C001C0u) | ((w << 4) & 0x80008000u);
+    uint32_t p3 = ((w >> 6) & 0x01C001C0u) | (w & 0x80008000u);
+    p0 = bmul2(p0, s1);
+    p1 = bmul2(p1, s1);
+    p2 = bmul2(p2, s1);
+    p3 = bmul2(p3, s1);
+    if (big) {
+        p0 = bmul2(p0, s2);
+        p1 = bmul2(p1, s2);
+        p2 = bmul2(p2, s2);
+        p3 = bmul2(p3, s2);
+    }
+    return make_uint4(p0, p1, p2, p3);
+}
+__device__ __forceinline__ uint32_t scale_lo(uint32_t s) {
+    uint32_t b = (s <= 128u) ? ((s + 126u) << 7) : (253u << 7);
+    return b | (b << 16);
+}
+__device__ __forceinline__ uint32_t scale_hi(uint32_t s) {
+    uint32_t b = (s <= 128u) ? 0x3F80u : (s << 7);
+    return b | (b << 16);
+}
+// byte offset of 16-byte chunk c of row r in a 128B-swizzled K-major tile
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_constant__ PrefillArgs a,
+                                                                    const __grid_constant__ TmaMaps maps) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sA = smem;                                   // [kStages][128 rows][128 B] swizzled
+    unsigned char *sB = sA + kStages * kABytes;                 // [kStages][kBN rows][128 B] swizzled
+    unsigned char *sF = sB + kStages * kBBytes;                 // [kStages][128 rows][32 B] packed codes
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sF + kStages * kFp4Bytes);
+    uint64_t *full_fp4 = bars, *full_ab = bars + kStages, *empty = bars + 2 * kStages;
+    uint64_t *acc_full = bars + 3 * kStages, *drain = acc_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+
+    const int tile_idx = blockIdx.x;
+    if (tile_idx >= *a.ws.n_tiles) return;
+    const int4 tile = a.ws.tiles[tile_idx];
+    const int e = tile.x, rstart = tile.y, rcount = tile.z;
+    const int E = a.bp.E, K = a.Kdim, nb = K / 32, nkb = K / kBK;
+    const int mt = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_mma = max(16, (rcount + 15) & ~15);
+    int32_t *status = a.ws.status;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(&full_fp4[s], 1);
+            mbar_init(&full_ab[s], 4);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(smem_u32(tmem_slot)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (codes)
+        if (lane == 0) {
+            const bool shared_e = e >= E;
+            const CUtensorMap *m0 = shared_e ? &maps.sh0 : &maps.a0;
+            const CUtensorMap *m1 = shared_e ? &maps.sh1 : &maps.a1;
+            const int ebase = shared_e ? 0 : e;
+            int issued_upto = 0;
+            bool ok = true;
+            for (int kb = 0; kb < nkb && ok; kb++) {
+                const int s = kb % kStages;
+                if (kb >= kStages) ok = mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, status, 10);
+                if (!ok) break;
+                mbar_expect_tx(&full_fp4[s], kFp4Bytes);
+                unsigned char *dst = sF + s * kFp4Bytes;
+                if (GATEUP) {
+                    const int y = ebase * a.rows + mt * 64;
+                    tma_load_2d(dst, m0, &full_fp4[s], kb * 32, y);
+                    tma_load_2d(dst + 64 * 32, m1, &full_fp4[s], kb * 32, y);
+                } else {
+                    tma_load_2d(dst, m0, &full_fp4[s], kb * 32, ebase * a.rows + mt * 128);
+                }
+                issued_upto = kb + 1;
+            }
+            // make sure every copy this thread issued has landed before exiting
+            for (int kb = max(0, issued_upto - kStages); kb < issued_upto; kb++)
+                mbar_wait(&full_fp4[kb % kStages], (kb / kStages) & 1, status, 11);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = umma_idesc_bf16(128, n_mma);
+            int done = 0;
+            bool ok = true;
+            for (int kb = 0; kb < nkb; kb++) {
+                const int s = kb % kStages;
+                ok = mbar_wait(&full_ab[s], (kb / kStages) & 1, status, 20);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + s * kABytes), b_addr = smem_u32(sB + s * kBBytes);
+#pragma unroll
+                for (int k = 0; k < kBK / 16; k++) {
+                    umma_bf16(tmem, umma_desc_sw128(a_addr + 32 * k), umma_desc_sw128(b_addr + 32 * k), idesc,
+                              (kb | k) != 0);
+                }
+                umma_commit(&empty[s]);
+                done = kb + 1;
+            }
+            if (ok && done == nkb) {
+                umma_commit(acc_full);
+            } else {
+                // drain the MMAs already issued before TMEM is released
+                umma_commit(drain);
+                mbar_wait(drain, 0, status, 21);
+            }
+        }
+    } else {
+        // ------------------------------------- dequant + B staging (warps 2..5)
+        const int t = threadIdx.x - 64;  // 0..127: A row of this thread
+        const MatPtrs &M = (GATEUP && t >= 64) ? a.A1 : a.A0;
+        int wrow;                        // weight row of A row t (may be >= rows for the last down tile)
+        if (GATEUP)
+            wrow = mt * 64 + (t & 63);
+        else
+            wrow = mt * 128 + t;
+        const bool row_ok = wrow < a.rows;
+        const uint8_t *srow = mat_scales(M, e, E) + (size_t)(row_ok ? wrow : 0) * nb;
+        const uint16_t *bsrc_base = GATEUP ? a.ws.xhat_mma : a.ws.h;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; kb++) {
+            const int s = kb % kStages;
+            if (kb >= kStages) {
+                ok = mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, status, 30);
+                if (!ok) break;
+            }
+            // B: rcount rows x 8 chunks of 16 bytes, gathered (gate/up) or contiguous (down)
+            unsigned char *bdst = sB + s * kBBytes;
+            for (int i = t; i < rcount * 8; i += 128) {
+                const int r = i >> 3, c = i & 7;
+                const size_t row = GATEUP ? (size_t)a.ws.perm_token[rstart + r] : (size_t)(rstart + r);
+                const uint4 v = *reinterpret_cast<const uint4 *>(bsrc_base + row * K + kb * kBK + c * 8);
+                *reinterpret_cast<uint4 *>(bdst + sw128(r, c)) = v;
+            }
+            // A: wait for the packed codes, dequantise row t
+            ok = mbar_wait(&full_fp4[s], (kb / kStages) & 1, status, 31);
+            if (!ok) break;
+            const uint4 *src = reinterpret_cast<const uint4 *>(sF + s * kFp4Bytes + t * 32);
+            const uint4 c0 = src[0], c1 = src[1];
+            uint32_t sc0 = row_ok ? srow[2 * kb] : 127u, sc1 = row_ok ? srow[2 * kb + 1] : 127u;
+            const bool big = (sc0 > 128u) || (sc1 > 128u);
+            const uint32_t l0 = scale_lo(sc0), h0 = scale_hi(sc0), l1 = scale_lo(sc1), h1 = scale_hi(sc1);
+            unsigned char *adst = sA + s * kABytes;
+            *reinterpret_cast<uint4 *>(adst + sw128(t, 0)) = dequant8(c0.x, l0, h0, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(t, 1)) = dequant8(c0.y, l0, h0, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(t, 2)) = dequant8(c0.z, l0, h0, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(t, 3)) = dequant8(c0.w, l0, h0, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(t, 4)) = dequant8(c1.x, l1, h1, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(t, 5)) = dequant8(c1.y, l1, h1, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(t, 6)) = dequant8(c1.z, l1, h1, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(t, 7)) = dequant8(c1.w, l1, h1, big);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_ab[s]);
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok) ok = mbar_wait(acc_full, 0, status, 40);
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
+        tc_fence_after();
+        const int q = warp & 3;                  // TMEM lane quarter of this warp
+        const int lrow = q * 32 + lane;          // accumulator row (= A row)
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+        float *xch = reinterpret_cast<float *>(sA);  // [64][33] exchange buffer (stages are idle now)
+        for (int c0 = 0; c0 < n_mma; c0 += 32) {
+            float v[32];
+            if (ok) tmem_ld32(taddr + c0, v);
+            if (GATEUP) {
+                if (q >= 2) {
+#pragma unroll
+                    for (int c = 0; c < 32; c++) xch[(lrow - 64) * 33 + c] = v[c];
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (q < 2 && ok) {
+                    const int j = mt * 64 + lrow;
+                    const float bg = mat_bias(a.A0, e, E)[j], bu = mat_bias(a.A1, e, E)[j];
+                    const int pj = mma_perm_pos(j);
+                    for (int c = 0; c < 32 && c0 + c < rcount; c++) {
+                        const float hv = swiglu_clamped(v[c] + bg, xch[lrow * 33 + c] + bu, a.bp.alpha, a.bp.limit);
+                        __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                        a.ws.h[(size_t)(rstart + c0 + c) * a.bp.F + pj] = *reinterpret_cast<uint16_t *>(&hb);
+                    }
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            } else if (ok) {
+                const int i = mt * 128 + lrow;
+                if (i < a.rows) {
+                    const float bd = mat_bias(a.A0, e, E)[i];
+                    for (int c = 0; c < 32 && c0 + c < rcount; c++) {
+                        const int route = rstart + c0 + c;
+                        a.ws.y[(size_t)route * a.bp.H + i] = a.ws.perm_w[route] * (v[c] + bd);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem));
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encoder() {
+    if (g_encode) return cudaSuccess;
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+// 2D map over packed codes: [n_rows][cols/2] bytes, box 32 bytes x box_rows.
+cudaError_t make_codes_map(CUtensorMap *m, const uint8_t *codes, size_t n_rows, int cols, int box_rows) {
+    if (!codes) {
+        memset(m, 0, sizeof *m);
+        return cudaSuccess;
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)(cols / 2), (cuuint64_t)n_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols / 2)};
+    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+size_t prefill_smem_bytes() { return 1024 + kStages * (kABytes + kBBytes + kFp4Bytes) + 256; }
+
+}  // namespace
+
+int prefill_tile_rows() { return kBN; }
+
+cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0, const MatPtrs &a1,
+                                 bool gateup, int T, cudaStream_t st) {
+    MOE_CUDA_TRY(get_encoder());
+    PrefillArgs args{bp, ws, a0, a1, gateup ? bp.H : bp.F, gateup ? bp.F : bp.H};
+    TmaMaps maps;
+    const int box_rows = gateup ? 64 : 128;
+    const int E = bp.E;
+    MOE_CUDA_TRY(make_codes_map(&maps.a0, a0.codes, (size_t)E * a0.rows, a0.cols, box_rows));
+    MOE_CUDA_TRY(make_codes_map(&maps.a1, a1.codes, (size_t)E * a1.rows, a1.cols, box_rows));
+    MOE_CUDA_TRY(make_codes_map(&maps.sh0, bp.n_shared ? a0.sh_codes : nullptr, a0.rows, a0.cols, box_rows));
+    MOE_CUDA_TRY(make_codes_map(&maps.sh1, bp.n_shared ? a1.sh_codes : nullptr, a1.rows, a1.cols, box_rows));
+    const int R = T * (bp.K + bp.n_shared);
+    int tiles = (R + kBN - 1) / kBN + bp.E + bp.n_shared;
+    if (tiles > ws.max_tiles) tiles = ws.max_tiles;
+    const int mtiles = gateup ? bp.F / 64 : (bp.H + 127) / 128;
+    const size_t sm = prefill_smem_bytes();
+    if (gateup) {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(moe_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+        moe_prefill_kernel<true><<<dim3(tiles, mtiles), kThreads, sm, st>>>(args, maps);
+    } else {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(moe_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+        moe_prefill_kernel<false><<<dim3(tiles, mtiles), kThreads, sm, st>>>(args, maps);
+    }
+    return cudaGetLastError();
+}

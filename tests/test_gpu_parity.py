@@ -171,3 +171,19 @@ def test_repeated_forward_is_deterministic():
     a, plan, dev = run_gpu(blk, x)
     b, _, _ = run_gpu(blk, x, plan=plan, dev=dev)
     assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["ids"], b["ids"])
+
+
+@pytest.mark.parametrize("cfg,T", [(3, 48), (4, 24)])
+def test_decode_and_prefill_paths_agree(cfg, T):
+    blk = synth.make_block(cfg)
+    x = synth.make_tokens(cfg, T, blk["shape"].hidden, sub=7)
+    dev = moe.DeviceBlock(blk)
+    a, _, _ = run_gpu(blk, x, dev=dev, path=1)
+    b, _, _ = run_gpu(blk, x, dev=dev, path=2)
+    assert a["status"] == 0 and b["status"] == 0
+    assert np.array_equal(a["ids"], b["ids"])
+    check_close(b["out"], a["out"], what="prefill vs decode")
+    sample = np.arange(0, T, max(1, T // 4))
+    ref = oracle.moe_forward(blk, np.ascontiguousarray(x[sample]), nthreads=NTHREADS)
+    check_close(b["out"][sample], ref["out"], x[sample], what="prefill vs oracle")
+    check_close(a["out"][sample], ref["out"], x[sample], what="decode vs oracle")
