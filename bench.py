@@ -198,40 +198,47 @@ def run_ours(args, rank, world, local):
         ids = torch.empty((TOKENS, K), dtype=torch.int32, device="cuda")
         sets.append(dict(blk=blk if s == 0 else None, xb=xb if s == 0 else None, plan=plan, x=x, out=out, ids=ids))
         del blk
-    st = torch.cuda.current_stream()
-
-    def step(i):
+    def step(i, stream):
         d = sets[i % len(sets)]
-        d["plan"].forward(d["x"], d["out"], d["ids"], stream=st)
+        d["plan"].forward(d["x"], d["out"], d["ids"], stream=stream)
 
+    def capture(n):
+        """One CUDA graph holding n consecutive steps (launch overhead off the clock)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream()
+            for i in range(n):
+                step(i, cs)
+        return g
+
+    st = torch.cuda.current_stream()
     # per-set routing facts for the algorithmic byte counts
     facts = []
     for i, d in enumerate(sets):
-        step(i)
+        step(i, st)
         c = torch.empty(shape.n_experts, dtype=torch.int32, device="cuda")
         d["plan"].expert_counts(c)
         torch.cuda.synchronize()
         facts.append(algorithmic_bytes(shape, c.cpu().numpy(), TOKENS))
     for i in range(args.warmup):
-        step(i)
+        step(i, st)
+    torch.cuda.synchronize()
+    graph = capture(args.steps)
+    graph.replay()
     torch.cuda.synchronize()
     # pre-roll so that the clock samples see this load for about a second
     clocks = Clocks(local)
     t_end = time.perf_counter() + (0.0 if args.quick else 1.0)
-    i = 0
     while time.perf_counter() < t_end:
-        for _ in range(64):
-            step(i)
-            i += 1
+        graph.replay()
         torch.cuda.synchronize()
-    # ---- timed region: exactly K steps
+    # ---- timed region: exactly K steps (one graph replay)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(st)
-    for i in range(args.steps):
-        step(i)
+    graph.replay()
     ev1.record(st)
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
@@ -247,12 +254,14 @@ def run_ours(args, rank, world, local):
                               "quick": True}), flush=True)
         return
 
-    # ---- kernel durations over the same K steps, with per-launch CUDA events
+    # ---- kernel durations over the same K steps: CUDA events the library
+    # records around each launch (captured into the graph as event nodes)
     for d in sets:
         d["plan"].set_i("profile", 1)
+    pgraph = capture(args.steps)
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        step(i)
+    pgraph.replay()
+    torch.cuda.synchronize()
     tot = [0.0] * 4
     cnt = [0] * 4
     for d in sets:
@@ -260,15 +269,16 @@ def run_ours(args, rank, world, local):
         tot = [a + b for a, b in zip(tot, m)]
         cnt = [a + b for a, b in zip(cnt, c)]
         d["plan"].set_i("profile", 0)
+    del pgraph
     avg_ms = [t / c if c else 0.0 for t, c in zip(tot, cnt)]
-    share = [t / sum(tot) for t in tot]
+    share = [t / sum(tot) for t in tot] if sum(tot) > 0 else [0.0] * 4
     gu_bytes = sum(facts[i % len(sets)][0] for i in range(args.steps)) / args.steps
     dn_bytes = sum(facts[i % len(sets)][1] for i in range(args.steps)) / args.steps
     distinct = sum(facts[i % len(sets)][2] for i in range(args.steps)) / args.steps
     hbm, _, peak_kind = peaks()
     dom = max(range(4), key=lambda k: tot[k])
     dom_bytes = {1: gu_bytes, 2: dn_bytes}.get(dom, gu_bytes)
-    achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9
+    achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9 if avg_ms[dom] > 0 else 0.0
     tr = traffic_record(KERNEL_SLOTS[dom])
     step_bytes = gu_bytes + dn_bytes
     step_gbs = step_bytes / (ms / args.steps / 1e3) / 1e9

@@ -52,6 +52,8 @@ struct moe_plan {
     bool have_w = false;
     moe_weights w{};
     MatPtrs gate{}, up{}, down{};
+    PrefillMaps maps{};
+    bool have_maps = false;
     // kernel timing (profile option)
     static constexpr int kSlots = 4, kMaxRec = 4096 * kSlots;
     std::vector<cudaEvent_t> ev;     // 2 events per record
@@ -276,6 +278,8 @@ int moe_load_weights(moe_plan *p, const moe_weights *w) {
     p->gate = mat_of(w->gate, w->sh_gate, b.F, b.H);
     p->up = mat_of(w->up, w->sh_up, b.F, b.H);
     p->down = mat_of(w->down, w->sh_down, b.H, b.F);
+    p->have_maps = (b.H % 64 == 0 && b.F % 64 == 0) &&
+                   prefill_make_maps(b, p->gate, p->up, p->down, &p->maps) == cudaSuccess;
     p->have_w = true;
     return MOE_OK;
 }
@@ -297,7 +301,7 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The tensor-core grouped GEMM needs H and F in whole 64-element stages;
     // other shapes always take the GEMV path (which handles any token count).
-    const bool prefill_ok = b.H % 64 == 0 && b.F % 64 == 0;
+    const bool prefill_ok = b.H % 64 == 0 && b.F % 64 == 0 && p->have_maps;
     if (p->path == 2 && !prefill_ok) return fail(MOE_ESHAPE, "the prefill path needs H and F multiples of 64");
     const bool decode = !prefill_ok || p->path == 1 || (p->path == 0 && tokens <= p->decode_max_tokens);
     const int nt = tokens <= 8 ? 1 : 2;
@@ -319,12 +323,12 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     mark(1, true);
     e = decode ? launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, st)
-               : launch_prefill_stage(b, p->ws, p->gate, p->up, true, tokens, st);
+               : launch_prefill_stage(b, p->ws, p->gate, p->up, true, tokens, p->maps.gateup, st);
     mark(1, false);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
     mark(2, true);
     e = decode ? launch_decode_stage(b, p->ws, p->down, p->down, false, tokens, nt, st)
-               : launch_prefill_stage(b, p->ws, p->down, p->down, false, tokens, st);
+               : launch_prefill_stage(b, p->ws, p->down, p->down, false, tokens, p->maps.down, st);
     mark(2, false);
     if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
     mark(3, true);

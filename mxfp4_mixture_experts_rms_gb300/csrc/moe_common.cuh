@@ -1,5 +1,6 @@
 // moe_common.cuh -- shared device helpers and the plan's kernel parameters.
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -105,6 +106,19 @@ __device__ __forceinline__ int mma_perm_pos(int j) {
     return b + (q << 3) + (i << 1) + hh;
 }
 
+// Raise a kernel's dynamic shared memory limit to the device maximum, once per
+// process (host-side setup; kept out of the per-forward launch sequence).
+template <class F>
+inline cudaError_t smem_optin_once(F *kernel, bool &done) {
+    if (done) return cudaSuccess;
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e == cudaSuccess) done = true;
+    return e;
+}
+
 // Host+device-visible launch helpers
 #define MOE_CUDA_TRY(expr)                                  \
     do {                                                    \
@@ -121,8 +135,17 @@ cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, cons
                                 const MatPtrs &a1, bool gateup, int T, int nt, cudaStream_t st);
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T,
                            float *out, cudaStream_t st);
+// TMA descriptors of the packed codes: [0] routed A0, [1] routed A1, [2] shared A0, [3] shared A1.
+struct TmaMaps {
+    CUtensorMap m[4];
+};
+struct PrefillMaps {
+    TmaMaps gateup, down;
+};
+cudaError_t prefill_make_maps(const BlockParams &bp, const MatPtrs &gate, const MatPtrs &up, const MatPtrs &down,
+                              PrefillMaps *out);
 cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
-                                 const MatPtrs &a1, bool gateup, int T, cudaStream_t st);
+                                 const MatPtrs &a1, bool gateup, int T, const TmaMaps &maps, cudaStream_t st);
 int prefill_tile_rows();
 cudaError_t launch_dequant(const MatPtrs &m, int expert, int n_experts, float *out, cudaStream_t st);
 cudaError_t launch_scan_scales(const uint8_t *scales, size_t n, int32_t *flag, cudaStream_t st);

@@ -308,7 +308,8 @@ size_t decode_smem_bytes(bool gateup, int nt, int K) {
 template <bool GATEUP, int NT>
 static cudaError_t launch_one(const DecodeArgs &a, int rows, int max_tiles, cudaStream_t st) {
     size_t sm = decode_smem_bytes(GATEUP, NT, a.Kdim);
-    MOE_CUDA_TRY(cudaFuncSetAttribute(moe_decode_kernel<GATEUP, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+    static bool done = false;
+    MOE_CUDA_TRY(smem_optin_once(moe_decode_kernel<GATEUP, NT>, done));
     dim3 grid(rows / 16, max_tiles);
     moe_decode_kernel<GATEUP, NT><<<grid, kDecThreads, sm, st>>>(a);
     return cudaGetLastError();

@@ -50,10 +50,6 @@ struct PrefillArgs {
     int rows;           // F (gate/up) or H (down)
 };
 
-struct TmaMaps {
-    CUtensorMap a0, a1, sh0, sh1;  // routed and shared codes of A0 / A1
-};
-
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -234,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
         // ------------------------------------------------ TMA producer (codes)
         if (lane == 0) {
             const bool shared_e = e >= E;
-            const CUtensorMap *m0 = shared_e ? &maps.sh0 : &maps.a0;
-            const CUtensorMap *m1 = shared_e ? &maps.sh1 : &maps.a1;
+            const CUtensorMap *m0 = shared_e ? &maps.m[2] : &maps.m[0];
+            const CUtensorMap *m1 = shared_e ? &maps.m[3] : &maps.m[1];
             const int ebase = shared_e ? 0 : e;
             int issued_upto = 0;
             bool ok = true;
@@ -415,27 +411,36 @@ size_t prefill_smem_bytes() { return 1024 + kStages * (kABytes + kBBytes + kFp4B
 
 int prefill_tile_rows() { return kBN; }
 
-cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0, const MatPtrs &a1,
-                                 bool gateup, int T, cudaStream_t st) {
+cudaError_t prefill_make_maps(const BlockParams &bp, const MatPtrs &gate, const MatPtrs &up, const MatPtrs &down,
+                              PrefillMaps *out) {
     MOE_CUDA_TRY(get_encoder());
-    PrefillArgs args{bp, ws, a0, a1, gateup ? bp.H : bp.F, gateup ? bp.F : bp.H};
-    TmaMaps maps;
-    const int box_rows = gateup ? 64 : 128;
     const int E = bp.E;
-    MOE_CUDA_TRY(make_codes_map(&maps.a0, a0.codes, (size_t)E * a0.rows, a0.cols, box_rows));
-    MOE_CUDA_TRY(make_codes_map(&maps.a1, a1.codes, (size_t)E * a1.rows, a1.cols, box_rows));
-    MOE_CUDA_TRY(make_codes_map(&maps.sh0, bp.n_shared ? a0.sh_codes : nullptr, a0.rows, a0.cols, box_rows));
-    MOE_CUDA_TRY(make_codes_map(&maps.sh1, bp.n_shared ? a1.sh_codes : nullptr, a1.rows, a1.cols, box_rows));
+    TmaMaps &g = out->gateup, &d = out->down;
+    MOE_CUDA_TRY(make_codes_map(&g.m[0], gate.codes, (size_t)E * gate.rows, gate.cols, 64));
+    MOE_CUDA_TRY(make_codes_map(&g.m[1], up.codes, (size_t)E * up.rows, up.cols, 64));
+    MOE_CUDA_TRY(make_codes_map(&g.m[2], bp.n_shared ? gate.sh_codes : nullptr, gate.rows, gate.cols, 64));
+    MOE_CUDA_TRY(make_codes_map(&g.m[3], bp.n_shared ? up.sh_codes : nullptr, up.rows, up.cols, 64));
+    MOE_CUDA_TRY(make_codes_map(&d.m[0], down.codes, (size_t)E * down.rows, down.cols, 128));
+    d.m[1] = d.m[0];
+    MOE_CUDA_TRY(make_codes_map(&d.m[2], bp.n_shared ? down.sh_codes : nullptr, down.rows, down.cols, 128));
+    d.m[3] = d.m[2];
+    return cudaSuccess;
+}
+
+cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0, const MatPtrs &a1,
+                                 bool gateup, int T, const TmaMaps &maps, cudaStream_t st) {
+    PrefillArgs args{bp, ws, a0, a1, gateup ? bp.H : bp.F, gateup ? bp.F : bp.H};
     const int R = T * (bp.K + bp.n_shared);
     int tiles = (R + kBN - 1) / kBN + bp.E + bp.n_shared;
     if (tiles > ws.max_tiles) tiles = ws.max_tiles;
     const int mtiles = gateup ? bp.F / 64 : (bp.H + 127) / 128;
     const size_t sm = prefill_smem_bytes();
+    static bool done_gu = false, done_dn = false;
     if (gateup) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(moe_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+        MOE_CUDA_TRY(smem_optin_once(moe_prefill_kernel<true>, done_gu));
         moe_prefill_kernel<true><<<dim3(tiles, mtiles), kThreads, sm, st>>>(args, maps);
     } else {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(moe_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+        MOE_CUDA_TRY(smem_optin_once(moe_prefill_kernel<false>, done_dn));
         moe_prefill_kernel<false><<<dim3(tiles, mtiles), kThreads, sm, st>>>(args, maps);
     }
     return cudaGetLastError();

@@ -418,14 +418,13 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
                          int router_exact, int write_mma_layout, cudaStream_t st) {
     RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows,
                 router_exact, write_mma_layout};
+    static bool done1 = false, done8 = false;
     if (T <= 32) {
-        size_t sm = route_smem_bytes(1, bp.H, bp.E);
-        MOE_CUDA_TRY(cudaFuncSetAttribute(moe_route_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-        moe_route_kernel<1><<<T, kRouteThreads, sm, st>>>(a);
+        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<1>, done1));
+        moe_route_kernel<1><<<T, kRouteThreads, route_smem_bytes(1, bp.H, bp.E), st>>>(a);
     } else {
-        size_t sm = route_smem_bytes(8, bp.H, bp.E);
-        MOE_CUDA_TRY(cudaFuncSetAttribute(moe_route_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-        moe_route_kernel<8><<<(T + 7) / 8, kRouteThreads, sm, st>>>(a);
+        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8>, done8));
+        moe_route_kernel<8><<<(T + 7) / 8, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
     }
     return cudaGetLastError();
 }
