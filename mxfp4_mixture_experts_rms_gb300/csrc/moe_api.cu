@@ -311,9 +311,10 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
         if (begin) {
             if ((int)p->rec_slot.size() >= moe_plan::kMaxRec) return;
             p->rec_slot.push_back(slot);
-            cudaEventRecord(p->ev[2 * (p->rec_slot.size() - 1)], st);
+            // external record: becomes an event node when the forward is graph-captured
+            cudaEventRecordWithFlags(p->ev[2 * (p->rec_slot.size() - 1)], st, cudaEventRecordExternal);
         } else if (!p->rec_slot.empty() && p->rec_slot.back() == slot) {
-            cudaEventRecord(p->ev[2 * (p->rec_slot.size() - 1) + 1], st);
+            cudaEventRecordWithFlags(p->ev[2 * (p->rec_slot.size() - 1) + 1], st, cudaEventRecordExternal);
         }
     };
     mark(0, true);
