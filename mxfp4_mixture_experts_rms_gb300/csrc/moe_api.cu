@@ -99,8 +99,10 @@ size_t carve(const moe_plan *p, int T, char *base, Workspace *ws) {
     w.n_tiles = c.take<int32_t>(base, 4);
     w.h = c.take<uint16_t>(base, R * b.F);
     w.y = c.take<float>(base, R * b.H);
+    w.logits = c.take<float>(base, (size_t)T * b.E);
+    w.lbound = c.take<float>(base, (size_t)T * b.E);
     w.status = c.take<int32_t>(base, 4);
-    w.ticket = c.take<uint32_t>(base, 4);
+    w.tickets = c.take<uint32_t>(base, route_ticket_count(T));
     if (ws) *ws = w;
     return c.off;
 }
@@ -234,7 +236,7 @@ int moe_set_workspace(moe_plan *p, void *dev_ptr, size_t bytes) {
     if (bytes < need) return fail(MOE_ENOMEM, "workspace too small: %zu < %zu bytes", bytes, need);
     carve(p, p->max_tokens, static_cast<char *>(dev_ptr), &p->ws);
     cudaError_t e = cudaMemset(p->ws.status, 0, 16);
-    if (e == cudaSuccess) e = cudaMemset(p->ws.ticket, 0, 16);
+    if (e == cudaSuccess) e = cudaMemset(p->ws.tickets, 0, sizeof(uint32_t) * route_ticket_count(p->max_tokens));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "moe_set_workspace");
     p->ws_ptr = dev_ptr;

@@ -50,8 +50,10 @@ struct Workspace {
     int32_t *n_tiles;      // [1]
     uint16_t *h;           // [R][F] bf16 (layout depends on the path)
     float *y;              // [R][H] weighted expert outputs
+    float *logits;         // [T][E] router logits (fp32) of the routing kernel
+    float *lbound;         // [T][E] their rounding-error bounds
     int32_t *status;       // [4] device error flag + detail
-    uint32_t *ticket;      // [1] last-block counter of the routing kernel
+    uint32_t *tickets;     // [T + 1] last-CTA counters of the routing kernel (grid, token groups)
     int max_tiles;
 };
 
@@ -130,6 +132,7 @@ inline cudaError_t smem_optin_once(F *kernel, bool &done) {
     } while (0)
 
 // Launchers implemented in the .cu files (host side).
+int route_ticket_count(int T);
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x,
                          const float *gamma, const uint16_t *router_w, const float *router_b,
                          int T, int32_t *ids_out, float *rw_out, uint16_t *xhat_out, int tile_rows,

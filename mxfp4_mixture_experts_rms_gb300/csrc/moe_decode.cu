@@ -8,15 +8,16 @@
 // outputs are summed in slot order and added to the residual in `forward`.
 //
 // Design (sm_103a):
-//  * work item = (tile of <= 8*NT routes of one expert, 16 weight rows);
-//    4 warps split the K dimension; each thread streams its rows' packed
-//    codes with 128-bit loads straight from HBM into registers;
+//  * work item = (tile of <= 8*NT routes of one expert, 16 weight rows),
+//    walked by persistent CTAs; 8 warps split the K dimension; each thread
+//    streams its rows' packed codes with 128-bit loads straight from HBM into
+//    registers, one iteration ahead;
 //  * dequantisation in registers: one 32-bit word of codes (8 nibbles) gives
 //    four bf16x2 pairs (nibble i, nibble i+4) by two shifts and two masks,
 //    scaled exactly by the E8M0 exponent with one bf16x2 multiply;
 //  * the multiply-accumulate runs on the tensor cores (m16n8k16 bf16, fp32
-//    accumulate) with the routed activations as the N=8 operand, staged in
-//    shared memory in the matching pair order;
+//    accumulate) with the routed activations as the N=8 operand, read in the
+//    matching pair order from L1/L2;
 //  * gate/up kernel: bias + clamped SwiGLU epilogue writes h (bf16);
 //    down kernel: bias, times the route weight, into a per-route fp32 buffer;
 //    the combine kernel sums the slots of each token in slot order and adds x.
@@ -24,13 +25,13 @@
 
 namespace {
 
-constexpr int kDecThreads = 128;  // 4 warps
 
 struct DecodeArgs {
     BlockParams bp;
     Workspace ws;
     MatPtrs A0, A1;   // gate, up (GATEUP) or down, unused
     int Kdim;         // reduction length: H for gate/up, F for down
+    int rows;         // output rows: F for gate/up, H for down
 };
 
 // 8 nibbles of one 32-bit word -> four bf16x2 (value * 2^-126, exact):
@@ -85,154 +86,170 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
     return r;
 }
 
-// Byte offset inside a staged activation row of 16-byte chunk k of 32-block b
-// (chunk rotation by b/2 keeps the fragment loads bank-conflict free).
-__device__ __forceinline__ int bstage_off(int b, int k) { return b * 64 + (((k + (b >> 1)) & 3) << 4); }
+// Persistent CTAs of 8 warps: each CTA walks the work items (tile, 16-row
+// block) with a grid stride; its 8 warps split K (32-element blocks in groups
+// of four per warp-iteration) and reduce through shared memory.  Each thread
+// keeps the next iteration's packed weights in flight (128-bit streaming
+// loads) while it dequantises and multiplies the current ones; the routed
+// activations (already in MMA pair order) are read from L1/L2.
+constexpr int kDecWarps = 8;
+constexpr int kMaxNb = 128;  // K <= 4096
+
+template <int NM>
+__device__ __forceinline__ void load_a(uint4 (&A)[2][2], const uint8_t *c0, const uint8_t *c1, size_t rowb, int g,
+                                       int b, bool valid) {
+#pragma unroll
+    for (int m = 0; m < 2; m++)
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            if (m < NM && valid)
+                A[m][h] = ldg_stream((m == 0 ? c0 : c1) + (size_t)(g + 8 * h) * rowb + 16 * b);
+            else
+                A[m][h] = make_uint4(0, 0, 0, 0);
+        }
+}
 
 template <bool GATEUP, int NT, bool BIG>
-__device__ __forceinline__ void decode_mainloop(const DecodeArgs &a, const uint8_t *c0, const uint8_t *c1,
-                                                const uint8_t *sc, const unsigned char *bst, int Sb,
-                                                float acc[2][NT][4]) {
+__device__ __forceinline__ void decode_mainloop(int K, const uint8_t *c0, const uint8_t *c1, const uint8_t *sc,
+                                                const uint16_t *const (&brow)[NT], float acc[2][NT][4]) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t4 = lane & 3;
-    const int K = a.Kdim, nb = K / 32, nq = (nb + 3) / 4;
+    const int nb = K / 32, nq = (nb + 3) / 4;
     const size_t rowb = (size_t)K / 2;
     constexpr int NM = GATEUP ? 2 : 1;
-    for (int q = warp; q < nq; q += 4) {
+    uint4 A[2][2];
+    int q = warp;
+    load_a<NM>(A, c0, c1, rowb, g, 4 * q + t4, q < nq && 4 * q + t4 < nb);
+    for (; q < nq; q += kDecWarps) {
         const int b = 4 * q + t4;
         const bool valid = b < nb;
-        uint4 A[NM][2];
-        uint32_t s1[NM][2], s2[NM][2];
+        uint4 An[2][2];
+        const int qn = q + kDecWarps;
+        load_a<NM>(An, c0, c1, rowb, g, 4 * qn + t4, qn < nq && 4 * qn + t4 < nb);
+        uint4 B[NT][4];
 #pragma unroll
-        for (int m = 0; m < NM; m++) {
-            const uint8_t *cb = (m == 0 ? c0 : c1);
+        for (int n = 0; n < NT; n++)
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+                B[n][k] = (valid && brow[n]) ? __ldg(reinterpret_cast<const uint4 *>(brow[n] + 32 * b) + k)
+                                            : make_uint4(0, 0, 0, 0);
+        uint32_t s1[2][2], s2[2][2];
+#pragma unroll
+        for (int m = 0; m < NM; m++)
 #pragma unroll
             for (int h = 0; h < 2; h++) {
-                if (valid) {
-                    A[m][h] = ldg_stream(cb + (size_t)(g + 8 * h) * rowb + 16 * b);
-                    uint32_t s = sc[(m * 16 + g + 8 * h) * nb + b];
-                    s1[m][h] = scale_lo(s);
-                    s2[m][h] = scale_hi(s);
-                } else {
-                    A[m][h] = make_uint4(0, 0, 0, 0);
-                    s1[m][h] = s2[m][h] = 0x3F803F80u;
-                }
+                const uint32_t s = valid ? sc[(m * 16 + g + 8 * h) * kMaxNb + b] : 127u;
+                s1[m][h] = scale_lo(s);
+                s2[m][h] = scale_hi(s);
             }
-        }
 #pragma unroll
         for (int k = 0; k < 4; k++) {
-            uint4 B[NT];
-#pragma unroll
-            for (int n = 0; n < NT; n++) {
-                B[n] = valid ? *reinterpret_cast<const uint4 *>(bst + (size_t)(n * 8 + g) * Sb + bstage_off(b, k))
-                             : make_uint4(0, 0, 0, 0);
-            }
 #pragma unroll
             for (int m = 0; m < NM; m++) {
-                uint32_t w0 = (&A[m][0].x)[k], w1 = (&A[m][1].x)[k];
                 uint32_t p0[4], p1[4];
-                dequant_word<BIG>(w0, s1[m][0], s2[m][0], p0);
-                dequant_word<BIG>(w1, s1[m][1], s2[m][1], p1);
+                dequant_word<BIG>((&A[m][0].x)[k], s1[m][0], s2[m][0], p0);
+                dequant_word<BIG>((&A[m][1].x)[k], s1[m][1], s2[m][1], p1);
 #pragma unroll
                 for (int n = 0; n < NT; n++) {
-                    mma_bf16_16816(acc[m][n], p0[0], p1[0], p0[1], p1[1], B[n].x, B[n].y);
-                    mma_bf16_16816(acc[m][n], p0[2], p1[2], p0[3], p1[3], B[n].z, B[n].w);
+                    mma_bf16_16816(acc[m][n], p0[0], p1[0], p0[1], p1[1], B[n][k].x, B[n][k].y);
+                    mma_bf16_16816(acc[m][n], p0[2], p1[2], p0[3], p1[3], B[n][k].z, B[n][k].w);
                 }
             }
         }
+#pragma unroll
+        for (int m = 0; m < 2; m++)
+#pragma unroll
+            for (int h = 0; h < 2; h++) A[m][h] = An[m][h];
     }
 }
 
 template <bool GATEUP, int NT>
-__global__ void __launch_bounds__(kDecThreads) moe_decode_kernel(DecodeArgs a) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    const int tile_idx = blockIdx.y;
-    if (tile_idx >= *a.ws.n_tiles) return;
-    const int4 tile = a.ws.tiles[tile_idx];
-    const int e = tile.x, rstart = tile.y, rcount = tile.z;
-    const int j0 = blockIdx.x * 16;
-    const int K = a.Kdim, nb = K / 32;
-    const int Sb = 2 * K + 32;                       // staged row stride (bytes)
-    const int tid = threadIdx.x;
-    const int E = a.bp.E;
+__global__ void __launch_bounds__(kDecWarps * 32) moe_decode_kernel(DecodeArgs a) {
     constexpr int NM = GATEUP ? 2 : 1;
-
-    unsigned char *bst = smem;                                     // [8*NT][Sb]
-    uint8_t *sc = smem + (size_t)8 * NT * Sb;                      // [NM][16][nb]
-    float *red = reinterpret_cast<float *>(sc + ((NM * 16 * nb + 15) & ~15));  // [4][NM][NT][16][8]
-
-    // stage the routed activations (already in MMA pair order) with the chunk rotation
-    const int nchunk = K / 8;
-    for (int i = tid; i < rcount * nchunk; i += kDecThreads) {
-        int n = i / nchunk, c = i - n * nchunk;
-        const uint16_t *src = GATEUP ? a.ws.xhat_mma + (size_t)a.ws.perm_token[rstart + n] * K
-                                     : a.ws.h + (size_t)(rstart + n) * K;
-        uint4 v = *reinterpret_cast<const uint4 *>(src + c * 8);
-        *reinterpret_cast<uint4 *>(bst + (size_t)n * Sb + bstage_off(c >> 2, c & 3)) = v;
-    }
-    // stage the E8M0 scales of the 16 rows (contiguous in the canonical layout)
-    const uint8_t *c0 = mat_codes(a.A0, e, E) + (size_t)j0 * (K / 2);
-    const uint8_t *c1 = GATEUP ? mat_codes(a.A1, e, E) + (size_t)j0 * (K / 2) : nullptr;
-    int big = 0;
-    for (int m = 0; m < NM; m++) {
-        const uint8_t *s = mat_scales(m == 0 ? a.A0 : a.A1, e, E) + (size_t)j0 * nb;
-        for (int i = tid; i < 16 * nb; i += kDecThreads) {
-            uint8_t v = s[i];
-            sc[m * 16 * nb + i] = v;
-            big |= (v > 128);
-        }
-    }
-    big = __syncthreads_or(big);
-
-    float acc[2][NT][4];
-#pragma unroll
-    for (int m = 0; m < 2; m++)
-#pragma unroll
-        for (int n = 0; n < NT; n++)
-#pragma unroll
-            for (int r = 0; r < 4; r++) acc[m][n][r] = 0.f;
-    if (big)
-        decode_mainloop<GATEUP, NT, true>(a, c0, c1, sc, bst, Sb, acc);
-    else
-        decode_mainloop<GATEUP, NT, false>(a, c0, c1, sc, bst, Sb, acc);
-
-    // cross-warp reduction of the split-K partials (fixed order)
-    const int lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
-#pragma unroll
-    for (int m = 0; m < NM; m++)
-#pragma unroll
-        for (int n = 0; n < NT; n++) {
-            float *r = red + (((warp * NM + m) * NT + n) * 16) * 8;
-            r[g * 8 + 2 * t4] = acc[m][n][0];
-            r[g * 8 + 2 * t4 + 1] = acc[m][n][1];
-            r[(g + 8) * 8 + 2 * t4] = acc[m][n][2];
-            r[(g + 8) * 8 + 2 * t4 + 1] = acc[m][n][3];
-        }
-    __syncthreads();
-    for (int idx = tid; idx < 16 * 8 * NT; idx += kDecThreads) {
-        const int row = idx & 15, col = idx >> 4;  // col = route within the tile
-        if (col >= rcount) continue;
-        const int n = col >> 3, c = col & 7;
-        float s[NM];
+    __shared__ __align__(16) uint8_t sc[NM * 16 * kMaxNb];              // E8M0 of the item's rows
+    __shared__ __align__(16) float red[kDecWarps][NM][NT][16][8];       // split-K partials
+    const int K = a.Kdim, nb = K / 32;
+    const int RB = a.rows / 16;
+    const int n_items = *a.ws.n_tiles * RB;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
+    const int E = a.bp.E;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int4 tile = a.ws.tiles[item / RB];
+        const int e = tile.x, rstart = tile.y, rcount = tile.z;
+        const int j0 = (item % RB) * 16;
+        const uint8_t *c0 = mat_codes(a.A0, e, E) + (size_t)j0 * (K / 2);
+        const uint8_t *c1 = GATEUP ? mat_codes(a.A1, e, E) + (size_t)j0 * (K / 2) : nullptr;
+        // scales of the 16 rows (contiguous in the canonical layout)
+        int big = 0;
 #pragma unroll
         for (int m = 0; m < NM; m++) {
-            float v = 0.f;
+            const uint8_t *s = mat_scales(m == 0 ? a.A0 : a.A1, e, E) + (size_t)j0 * nb;
+            for (int i = tid; i < 16 * nb; i += kDecWarps * 32) {
+                const int r = i / nb, b = i - r * nb;
+                const uint8_t v = s[i];
+                sc[(m * 16 + r) * kMaxNb + b] = v;
+                big |= (v > 128);
+            }
+        }
+        big = __syncthreads_or(big);
+        // activation rows of this thread's MMA column (route) in each n-tile
+        const uint16_t *brow[NT];
 #pragma unroll
-            for (int w = 0; w < 4; w++) v += red[(((w * NM + m) * NT + n) * 16 + row) * 8 + c];
-            s[m] = v;
+        for (int n = 0; n < NT; n++) {
+            const int col = n * 8 + g;
+            brow[n] = nullptr;
+            if (col < rcount)
+                brow[n] = GATEUP ? a.ws.xhat_mma + (size_t)a.ws.perm_token[rstart + col] * K
+                                 : a.ws.h + (size_t)(rstart + col) * K;
         }
-        const int j = j0 + row;
-        const int route = rstart + col;
-        if (GATEUP) {
-            float gg = s[0] + mat_bias(a.A0, e, E)[j];
-            float uu = s[1] + mat_bias(a.A1, e, E)[j];
-            float hv = swiglu_clamped(gg, uu, a.bp.alpha, a.bp.limit);
-            __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-            a.ws.h[(size_t)route * a.bp.F + mma_perm_pos(j)] = *reinterpret_cast<uint16_t *>(&hb);
-        } else {
-            float yv = s[0] + mat_bias(a.A0, e, E)[j];
-            a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * yv;
+        float acc[2][NT][4];
+#pragma unroll
+        for (int m = 0; m < 2; m++)
+#pragma unroll
+            for (int n = 0; n < NT; n++)
+#pragma unroll
+                for (int r = 0; r < 4; r++) acc[m][n][r] = 0.f;
+        if (big)
+            decode_mainloop<GATEUP, NT, true>(K, c0, c1, sc, brow, acc);
+        else
+            decode_mainloop<GATEUP, NT, false>(K, c0, c1, sc, brow, acc);
+#pragma unroll
+        for (int m = 0; m < NM; m++)
+#pragma unroll
+            for (int n = 0; n < NT; n++) {
+                float(*r)[8] = red[warp][m][n];
+                r[g][2 * t4] = acc[m][n][0];
+                r[g][2 * t4 + 1] = acc[m][n][1];
+                r[g + 8][2 * t4] = acc[m][n][2];
+                r[g + 8][2 * t4 + 1] = acc[m][n][3];
+            }
+        __syncthreads();
+        for (int idx = tid; idx < 16 * 8 * NT; idx += kDecWarps * 32) {
+            const int row = idx & 15, col = idx >> 4;  // col = route within the tile
+            if (col >= rcount) continue;
+            const int n = col >> 3, c = col & 7;
+            float s[NM];
+#pragma unroll
+            for (int m = 0; m < NM; m++) {
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < kDecWarps; w++) v += red[w][m][n][row][c];
+                s[m] = v;
+            }
+            const int j = j0 + row;
+            const int route = rstart + col;
+            if (GATEUP) {
+                const float gg = s[0] + mat_bias(a.A0, e, E)[j];
+                const float uu = s[1] + mat_bias(a.A1, e, E)[j];
+                const float hv = swiglu_clamped(gg, uu, a.bp.alpha, a.bp.limit);
+                __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                a.ws.h[(size_t)route * a.bp.F + mma_perm_pos(j)] = *reinterpret_cast<uint16_t *>(&hb);
+            } else {
+                const float yv = s[0] + mat_bias(a.A0, e, E)[j];
+                a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * yv;
+            }
         }
+        __syncthreads();  // red / sc are reused by the next item
     }
 }
 
@@ -298,20 +315,23 @@ __global__ void moe_scan_scales_kernel(const uint8_t *s, size_t n, int32_t *flag
 
 }  // namespace
 
-size_t decode_smem_bytes(bool gateup, int nt, int K) {
-    int NM = gateup ? 2 : 1;
-    size_t Sb = 2 * (size_t)K + 32;
-    size_t sc = ((size_t)NM * 16 * (K / 32) + 15) & ~(size_t)15;
-    return 8 * nt * Sb + sc + (size_t)4 * NM * nt * 16 * 8 * 4;
-}
+size_t decode_smem_bytes(bool, int, int) { return 0; }
 
 template <bool GATEUP, int NT>
-static cudaError_t launch_one(const DecodeArgs &a, int rows, int max_tiles, cudaStream_t st) {
-    size_t sm = decode_smem_bytes(GATEUP, NT, a.Kdim);
-    static bool done = false;
-    MOE_CUDA_TRY(smem_optin_once(moe_decode_kernel<GATEUP, NT>, done));
-    dim3 grid(rows / 16, max_tiles);
-    moe_decode_kernel<GATEUP, NT><<<grid, kDecThreads, sm, st>>>(a);
+static cudaError_t launch_one(const DecodeArgs &a, int n_items_max, cudaStream_t st) {
+    static int per_sm = 0, n_sm = 0;
+    if (!per_sm) {
+        int dev = 0;
+        MOE_CUDA_TRY(cudaGetDevice(&dev));
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+        MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_decode_kernel<GATEUP, NT>,
+                                                                   kDecWarps * 32, 0));
+        if (per_sm < 1) per_sm = 1;
+    }
+    int grid = n_sm * per_sm;
+    if (grid > n_items_max) grid = n_items_max;
+    if (grid < 1) grid = 1;
+    moe_decode_kernel<GATEUP, NT><<<grid, kDecWarps * 32, 0, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -322,11 +342,13 @@ cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, cons
     int tiles = (R + 8 * nt - 1) / (8 * nt) + bp.E + bp.n_shared;
     if (tiles > ws.max_tiles) tiles = ws.max_tiles;
     if (gateup) {
-        DecodeArgs gu{bp, ws, a0, a1, bp.H};
-        return nt == 1 ? launch_one<true, 1>(gu, bp.F, tiles, st) : launch_one<true, 2>(gu, bp.F, tiles, st);
+        DecodeArgs gu{bp, ws, a0, a1, bp.H, bp.F};
+        const int items = tiles * (bp.F / 16);
+        return nt == 1 ? launch_one<true, 1>(gu, items, st) : launch_one<true, 2>(gu, items, st);
     }
-    DecodeArgs dn{bp, ws, a0, a0, bp.F};
-    return nt == 1 ? launch_one<false, 1>(dn, bp.H, tiles, st) : launch_one<false, 2>(dn, bp.H, tiles, st);
+    DecodeArgs dn{bp, ws, a0, a0, bp.F, bp.H};
+    const int items = tiles * (bp.H / 16);
+    return nt == 1 ? launch_one<false, 1>(dn, items, st) : launch_one<false, 2>(dn, items, st);
 }
 
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T, float *out,

@@ -11,18 +11,28 @@
 //  * goosedump gpt_oss.rs `mixture_of_experts_batch` / `mix_expert_outputs`:
 //    routes appended per expert in token order, one output location per route.
 //
-// Exactness.  The norm statistic is accumulated in fp64 from exact squares and
-// x_hat is rounded once from fp64, so it matches a plain double evaluation
-// bit for bit.  Router logits are accumulated in fp32 with a rigorous error
-// bound per logit; when the bound cannot certify the top-k membership and
-// order, the candidate logits are recomputed in fp64 (exact for these
-// operands) and the selection is redone on them.
+// Grid: (token groups of G tokens) x (expert chunks of 8*EPW experts).  Every
+// CTA normalises its tokens (chunk 0 also stores x_hat), computes the router
+// logits of its experts and writes them with an error bound; the last CTA of a
+// token group selects the top-k of its tokens; the last CTA of the grid builds
+// the permutation.  "Last" is decided by atomic tickets, never by waiting.
+//
+// Exactness.  Σx² is accumulated exactly as a 128-bit fixed-point integer
+// (bf16 squares have 16-bit significands), rounded once to double, and
+// r = 1/sqrt(ms + eps) is evaluated in double, matching a plain double
+// evaluation.  x_hat = bf16(x * r * gamma) is computed in fp32 and recomputed
+// in fp64 whenever the fp32 value lies within its error bound of a bf16
+// rounding midpoint.  Router logits are accumulated in fp32 with a rigorous
+// error bound; when the bounds cannot certify top-k membership and order, the
+// candidate logits are recomputed in fp64 (exact for these operands) and the
+// selection is redone on them.
 #include "moe_common.cuh"
 
 namespace {
 
-constexpr int kRouteThreads = 512;
+constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kMaxChunks = 16;  // router row chunks of 256 elements per lane held in registers (H <= 4096)
 
 struct RouteArgs {
     BlockParams bp;
@@ -37,7 +47,6 @@ struct RouteArgs {
     uint16_t *xhat_out; // user copy, may be null
     int tile_rows;
     int router_exact;
-    int write_mma;
 };
 
 __device__ __forceinline__ double warp_sum_d(double v) {
@@ -51,16 +60,10 @@ __device__ __forceinline__ float warp_sum_f(float v) {
     return v;
 }
 
-// (value, index) order of `top_experts`: larger value first, equal values by
-// lower index.  Candidates that can never beat an empty (-inf) slot are invalid.
-__device__ __forceinline__ bool better(float v, int i, float w, int j) {
-    return v > w || (v == w && i < j);
-}
-__device__ __forceinline__ bool better_d(double v, int i, double w, int j) {
-    return v > w || (v == w && i < j);
-}
+// (value, index) order of `top_experts`: larger value first, equal values by lower index.
+__device__ __forceinline__ bool better(float v, int i, float w, int j) { return v > w || (v == w && i < j); }
+__device__ __forceinline__ bool better_d(double v, int i, double w, int j) { return v > w || (v == w && i < j); }
 
-// Warp-wide arg-best over per-lane candidates.
 __device__ __forceinline__ void warp_best(float &v, int &i) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
@@ -72,10 +75,10 @@ __device__ __forceinline__ void warp_best(float &v, int &i) {
         }
     }
 }
-// Exact (fp64) router logit of expert e for the x_hat row in shared memory,
-// computed by one warp.  Products of two bf16 values are exact in fp64.
-__device__ double exact_logit(const uint16_t *xh, const uint16_t *router_w, const float *router_b,
-                              int e, int H, int lane) {
+
+// Exact (fp64) router logit of expert e for an x_hat row in shared memory, by one warp.
+__device__ double exact_logit(const uint16_t *xh, const uint16_t *router_w, const float *router_b, int e, int H,
+                              int lane) {
     double acc = 0.0;
     const uint16_t *w = router_w + (size_t)e * H;
     for (int i = lane; i < H; i += 32) acc += (double)bf16_to_f32(xh[i]) * (double)bf16_to_f32(__ldg(w + i));
@@ -83,8 +86,7 @@ __device__ double exact_logit(const uint16_t *xh, const uint16_t *router_w, cons
     return acc + (double)router_b[e];
 }
 
-// Exclusive scan by one warp over n <= 1024 ints in shared memory (in place
-// into out[0..n], out[n] = total).
+// Exclusive scan by one warp over n <= 1024 ints (out[n] = total).
 __device__ void warp_exclusive_scan(const int32_t *in, int32_t *out, int n, int lane) {
     int per = (n + 31) / 32;
     int lo = lane * per, hi = min(n, lo + per);
@@ -105,124 +107,251 @@ __device__ void warp_exclusive_scan(const int32_t *in, int32_t *out, int n, int 
     if (lane == 31) out[n] = incl;
 }
 
-template <int G>
+// 128-bit unsigned accumulator (hi:lo)
+struct U128 {
+    unsigned long long lo, hi;
+};
+__device__ __forceinline__ void u128_add(U128 &a, const U128 &b) {
+    unsigned long long lo = a.lo + b.lo;
+    a.hi += b.hi + (lo < a.lo ? 1ull : 0ull);
+    a.lo = lo;
+}
+__device__ __forceinline__ U128 u128_shfl_xor(const U128 &a, int o) {
+    U128 r;
+    r.lo = __shfl_xor_sync(0xffffffffu, a.lo, o);
+    r.hi = __shfl_xor_sync(0xffffffffu, a.hi, o);
+    return r;
+}
+
+// Exact Σx² of one bf16 row, rounded once to double.  Squares are placed on a
+// fixed-point grid relative to the largest exponent of the row; a square more
+// than 80 binary places below the largest one (|x| < 2^-40 max|x|) contributes
+// less than 2^-60 of the sum and is dropped, far below double precision.
+__device__ double sumsq_exact(const uint16_t *xr, int H, int tid, int lane, int warp, int *s_maxexp, U128 *s_acc) {
+    int mx = 0;
+    for (int i = tid; i < H; i += kRouteThreads) mx = max(mx, (int)((xr[i] >> 7) & 0xFF));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_maxexp[warp] = mx;
+    __syncthreads();
+    int emax = 1;
+#pragma unroll
+    for (int w = 0; w < kRouteWarps; w++) emax = max(emax, s_maxexp[w]);
+    // value = M * 2^(ex - 134) with M = 128 + mant (ex >= 1) or M = mant (ex == 0, exponent taken as 1)
+    U128 acc{0ull, 0ull};
+    for (int i = tid; i < H; i += kRouteThreads) {
+        const uint32_t b = xr[i];
+        const int ex = (b >> 7) & 0xFF;
+        const uint32_t M = ex ? (128u + (b & 0x7Fu)) : (b & 0x7Fu);
+        const int d = 2 * (emax - (ex ? ex : 1));
+        if (M == 0 || d > 80) continue;
+        const unsigned long long v = (unsigned long long)M * M;  // < 2^16
+        const int sh = 80 - d;                                  // 0..80
+        U128 t;
+        if (sh == 0) {
+            t.lo = v;
+            t.hi = 0;
+        } else if (sh < 64) {
+            t.lo = v << sh;
+            t.hi = v >> (64 - sh);
+        } else {
+            t.lo = 0;
+            t.hi = v << (sh - 64);
+        }
+        u128_add(acc, t);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) u128_add(acc, u128_shfl_xor(acc, o));
+    __syncthreads();  // s_maxexp fully read before the next row reuses it
+    if (lane == 0) s_acc[warp] = acc;
+    __syncthreads();
+    U128 tot{0ull, 0ull};
+#pragma unroll
+    for (int w = 0; w < kRouteWarps; w++) u128_add(tot, s_acc[w]);
+    if (tot.hi == 0 && tot.lo == 0) return 0.0;
+    // value = tot * 2^(2*(emax - 134) - 80); take the top 64 significant bits and round to 53 (ties to even)
+    const int lz = tot.hi ? __clzll((long long)tot.hi) : 64 + __clzll((long long)tot.lo);
+    const int width = 128 - lz;  // significant bits of tot
+    unsigned long long top;
+    bool sticky;
+    int shift;  // tot = top * 2^shift (+ sticky part)
+    if (width > 64) {
+        shift = width - 64;
+        top = (tot.hi << (64 - shift)) | (tot.lo >> shift);
+        sticky = (tot.lo << (64 - shift)) != 0ull;
+    } else {
+        shift = width - 64;  // <= 0
+        top = (width == 64) ? tot.lo : (tot.lo << (-shift));
+        sticky = false;
+    }
+    unsigned long long mant = top >> 11;
+    const unsigned long long rem = top & 0x7FFull;
+    if (rem > 0x400ull || (rem == 0x400ull && (sticky || (mant & 1ull)))) mant += 1ull;
+    return ldexp((double)mant, 11 + shift + 2 * (emax - 134) - 80);
+}
+
+template <int G, int EPW>
 __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int H = a.bp.H, E = a.bp.E, K = a.bp.K;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint16_t *xh = reinterpret_cast<uint16_t *>(smem);                       // [G][H]
-    float *lg = reinterpret_cast<float *>(smem + (size_t)G * H * 2);          // [G][E]
-    float *bnd = lg + G * E;                                                  // [G][E]
-    __shared__ double red[kRouteWarps];
-    __shared__ int last_flag;
+    uint16_t *xh = reinterpret_cast<uint16_t *>(smem);  // [G][H]
+    __shared__ int s_maxexp[kRouteWarps];
+    __shared__ U128 s_acc[kRouteWarps];
+    __shared__ double s_r;
+    __shared__ int s_flag;
 
     const int t0 = blockIdx.x * G;
-    // ---------------------------------------------------------------- norm
-    for (int g = 0; g < G; g++) {
-        int t = t0 + g;
-        if (t >= a.T) break;  // uniform across the block
-        const uint16_t *xr = a.x + (size_t)t * H;
-        double ss = 0.0;
-        for (int i = tid; i < H; i += kRouteThreads) {
-            double xi = (double)bf16_to_f32(xr[i]);
-            ss += xi * xi;
-        }
-        ss = warp_sum_d(ss);
-        if (lane == 0) red[warp] = ss;
-        __syncthreads();
-        double tot = 0.0;
+    const int nt = min(G, a.T - t0);
+    const int e0 = blockIdx.y * (kRouteWarps * EPW);
+    const int nchunk = H / 8;                 // 16-byte chunks per router row
+    const int per_lane = (nchunk + 31) / 32;  // <= kMaxChunks
+
+    // Prefetch this warp's first router row before the norm: one HBM round trip.
+    uint4 wreg[kMaxChunks];
+    {
+        const int e = e0 + warp * EPW;
+        const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)min(e, E - 1) * H);
 #pragma unroll
-        for (int w = 0; w < kRouteWarps; w++) tot += red[w];
-        double r = 1.0 / sqrt(tot / (double)H + a.bp.eps);
-        uint16_t *xo = a.ws.xhat + (size_t)t * H;
+        for (int c = 0; c < kMaxChunks; c++) {
+            const int ch = lane + 32 * c;
+            wreg[c] = (c < per_lane && ch < nchunk && e < E) ? __ldg(wr + ch) : make_uint4(0, 0, 0, 0);
+        }
+    }
+
+    // ---------------------------------------------------------------- norm
+    const bool store = blockIdx.y == 0;
+    for (int g = 0; g < nt; g++) {
+        const int t = t0 + g;
+        const uint16_t *xr = a.x + (size_t)t * H;
+        const double ss = sumsq_exact(xr, H, tid, lane, warp, s_maxexp, s_acc);
+        if (tid == 0) s_r = 1.0 / sqrt(ss / (double)H + a.bp.eps);
+        __syncthreads();
+        const double r = s_r;
+        const float r32 = (float)r;
         for (int i = tid; i < H; i += kRouteThreads) {
-            double v = (double)bf16_to_f32(xr[i]) * r;
-            v = v * (double)a.gamma[i];
-            uint16_t hb = bf16_from_double_rne(v);
+            const float xf = bf16_to_f32(xr[i]);
+            const float gf = a.gamma[i];
+            const float v32 = (xf * r32) * gf;  // within 3 fp32 ulps of the exact product
+            const uint32_t low = __float_as_uint(v32) & 0xFFFFu;
+            const bool safe = fabsf(v32) >= 0x1p-120f && fabsf(v32) < 0x1p126f &&
+                              (low > 0x8000u + 8u || low + 8u < 0x8000u);
+            uint16_t hb;
+            if (safe) {
+                __nv_bfloat16 bb = __float2bfloat16_rn(v32);
+                hb = *reinterpret_cast<uint16_t *>(&bb);
+            } else {
+                hb = bf16_from_double_rne((double)xf * r * (double)gf);
+            }
             xh[g * H + i] = hb;
-            xo[i] = hb;
-            if (a.write_mma) a.ws.xhat_mma[(size_t)t * H + mma_perm_pos(i)] = hb;
-            if (a.xhat_out) a.xhat_out[(size_t)t * H + i] = hb;
+            if (store) {
+                a.ws.xhat[(size_t)t * H + i] = hb;
+                a.ws.xhat_mma[(size_t)t * H + mma_perm_pos(i)] = hb;
+                if (a.xhat_out) a.xhat_out[(size_t)t * H + i] = hb;
+            }
         }
         __syncthreads();
     }
-    const int nt = min(G, a.T - t0);
 
     // -------------------------------------------------------------- router
-    // Per (token, expert): fp32 FMA chain per lane over 8-element chunks, then
-    // a 5-level butterfly.  Rounding error bound: gamma_{n+6} * (Σ|p| + |b|)
-    // with n the per-lane chain length (products are exact in fp32).
-    const int nchunk = H / 8;
-    const int chain = 8 * ((nchunk + 31) / 32) + 6;
-    for (int e = warp; e < E; e += kRouteWarps) {
-        float acc[G], sab[G];
+    // fp32 chain per lane (products of two bf16 are exact in fp32), then a
+    // 5-level butterfly and the bias: error <= gamma_n * (Σ|p| + |b| + |l|),
+    // n = per-lane chain length + 6; stored doubled as a safety margin.
+    const int chain = 8 * per_lane + 6;
+    for (int k = 0; k < EPW; k++) {
+        const int e = e0 + warp * EPW + k;
+        if (k > 0) {
+            const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)min(e, E - 1) * H);
 #pragma unroll
-        for (int g = 0; g < G; g++) acc[g] = sab[g] = 0.f;
+            for (int c = 0; c < kMaxChunks; c++) {
+                const int ch = lane + 32 * c;
+                wreg[c] = (c < per_lane && ch < nchunk && e < E) ? __ldg(wr + ch) : make_uint4(0, 0, 0, 0);
+            }
+        }
+        if (e >= E) break;  // warp-uniform
         if (!a.router_exact) {
-            const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)e * H);
-            for (int c = lane; c < nchunk; c += 32) {
-                uint4 wv = __ldg(wr + c);
-                const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+            float acc[G], sab[G];
 #pragma unroll
-                for (int g = 0; g < G; g++) {
-                    if (g < nt) {
-                        uint4 xv = *reinterpret_cast<const uint4 *>(xh + g * H + c * 8);
-                        const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+            for (int g = 0; g < G; g++) acc[g] = sab[g] = 0.f;
 #pragma unroll
-                        for (int k = 0; k < 4; k++) {
-                            float w0 = __uint_as_float(ww[k] << 16), w1 = __uint_as_float(ww[k] & 0xFFFF0000u);
-                            float x0 = __uint_as_float(xx[k] << 16), x1 = __uint_as_float(xx[k] & 0xFFFF0000u);
-                            float p0 = x0 * w0, p1 = x1 * w1;  // exact
-                            acc[g] += p0;
-                            acc[g] += p1;
-                            sab[g] += fabsf(p0) + fabsf(p1);
+            for (int c = 0; c < kMaxChunks; c++) {
+                const int ch = lane + 32 * c;
+                if (c < per_lane && ch < nchunk) {
+                    const uint32_t ww[4] = {wreg[c].x, wreg[c].y, wreg[c].z, wreg[c].w};
+#pragma unroll
+                    for (int g = 0; g < G; g++) {
+                        if (g < nt) {
+                            const uint4 xv = *reinterpret_cast<const uint4 *>(xh + g * H + ch * 8);
+                            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                            for (int q = 0; q < 4; q++) {
+                                const float p0 = __uint_as_float(xx[q] << 16) * __uint_as_float(ww[q] << 16);
+                                const float p1 =
+                                    __uint_as_float(xx[q] & 0xFFFF0000u) * __uint_as_float(ww[q] & 0xFFFF0000u);
+                                acc[g] += p0;
+                                acc[g] += p1;
+                                sab[g] += fabsf(p0) + fabsf(p1);
+                            }
                         }
                     }
                 }
             }
 #pragma unroll
             for (int g = 0; g < G; g++) {
-                float s = warp_sum_f(acc[g]);
-                float ab = warp_sum_f(sab[g]);
+                const float s = warp_sum_f(acc[g]);
+                const float ab = warp_sum_f(sab[g]);
                 if (lane == 0 && g < nt) {
-                    float b = a.router_b[e];
-                    float l = s + b;
-                    lg[g * E + e] = l;
-                    bnd[g * E + e] = 2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
+                    const float b = a.router_b[e];
+                    const float l = s + b;
+                    a.ws.logits[(size_t)(t0 + g) * E + e] = l;
+                    a.ws.lbound[(size_t)(t0 + g) * E + e] =
+                        2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
                 }
             }
         } else {
             for (int g = 0; g < nt; g++) {
-                double l = exact_logit(xh + g * H, a.router_w, a.router_b, e, H, lane);
+                const double l = exact_logit(xh + g * H, a.router_w, a.router_b, e, H, lane);
                 if (lane == 0) {
-                    lg[g * E + e] = (float)l;
-                    bnd[g * E + e] = -1.f;  // marks "exact requested"
+                    a.ws.logits[(size_t)(t0 + g) * E + e] = (float)l;
+                    a.ws.lbound[(size_t)(t0 + g) * E + e] = 0.f;
                 }
             }
         }
     }
-    __syncthreads();
 
-    // ---------------------------------------------------------- top-k + softmax
+    // ------------------------------------- last CTA of the token group: top-k
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_flag = (atomicAdd(a.ws.tickets + 1 + blockIdx.x, 1u) == gridDim.y - 1);
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
     for (int g = warp; g < nt; g += kRouteWarps) {
         const int t = t0 + g;
-        const float *l = lg + g * E;
-        const float *bd = bnd + g * E;
+        const float *l = a.ws.logits + (size_t)t * E;
+        const float *bd = a.ws.lbound + (size_t)t * E;
         const bool exact_mode = a.router_exact != 0;
-        // K+1 best by (value, index) among valid candidates
         int sel[MOE_MAX_TOPK + 1];
         float selv[MOE_MAX_TOPK + 1];
-        uint32_t taken = 0;  // per lane: bit j set if local candidate j was taken (E <= 256 -> 8 per lane)
+        float lv[MOE_MAX_EXPERTS / 32];
+        uint32_t taken = 0;
         float dmax = 0.f;
-        for (int j = lane; j < E; j += 32) dmax = fmaxf(dmax, bd[j]);
+#pragma unroll
+        for (int q = 0; q < MOE_MAX_EXPERTS / 32; q++) {
+            const int j = lane + 32 * q;
+            lv[q] = j < E ? __ldcg(l + j) : -INFINITY;
+            if (j < E) dmax = fmaxf(dmax, __ldcg(bd + j));
+        }
 #pragma unroll
         for (int o = 16; o; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
         for (int r = 0; r <= K; r++) {
             float bv = -INFINITY;
             int bi = 0x7fffffff;
-            for (int j = lane, q = 0; j < E; j += 32, q++) {
-                float v = l[j];
-                if (!(v > -INFINITY) || (taken >> q & 1u)) continue;  // NaN / -inf never chosen
+#pragma unroll
+            for (int q = 0; q < MOE_MAX_EXPERTS / 32; q++) {
+                const int j = lane + 32 * q;
+                const float v = lv[q];
+                if (j >= E || !(v > -INFINITY) || (taken >> q & 1u)) continue;  // NaN / -inf never chosen
                 if (better(v, j, bv, bi)) {
                     bv = v;
                     bi = j;
@@ -233,32 +362,29 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
             selv[r] = bv;
             if (bi != 0x7fffffff && (bi & 31) == lane) taken |= 1u << (bi >> 5);
         }
-        // certification: consecutive gaps among the K+1 best must exceed 2*dmax
         bool certain = !exact_mode;
         if (certain) {
             for (int r = 0; r < K; r++) {
                 if (sel[r] == 0x7fffffff) break;
-                float nxt = (sel[r + 1] == 0x7fffffff) ? -INFINITY : selv[r + 1];
+                const float nxt = (sel[r + 1] == 0x7fffffff) ? -INFINITY : selv[r + 1];
                 if (!(selv[r] - nxt > 2.0f * dmax)) certain = false;
             }
         }
         double exactv[MOE_MAX_TOPK];
         bool have_exact = false;
         if (!certain) {
-            // candidates: every expert whose fp32 logit is within 2*dmax of the
-            // K-th best (all of them in exact mode); recompute them in fp64
-            float thr = exact_mode ? -INFINITY : ((sel[K - 1] == 0x7fffffff) ? -INFINITY : selv[K - 1] - 2.0f * dmax);
+            const float thr =
+                exact_mode ? -INFINITY : ((sel[K - 1] == 0x7fffffff) ? -INFINITY : selv[K - 1] - 2.0f * dmax);
             double bv_all[MOE_MAX_TOPK];
             int bi_all[MOE_MAX_TOPK];
             for (int r = 0; r < K; r++) {
                 bv_all[r] = -INFINITY;
                 bi_all[r] = 0x7fffffff;
             }
-            // insertion of candidates in index order (warp-uniform loop)
-            for (int j = 0; j < E; j++) {
-                float v = l[j];
+            for (int j = 0; j < E; j++) {  // warp-uniform
+                const float v = __ldcg(l + j);
                 if (!(v > -INFINITY) || v < thr) continue;
-                double ex = exact_logit(xh + g * H, a.router_w, a.router_b, j, H, lane);
+                const double ex = exact_logit(xh + g * H, a.router_w, a.router_b, j, H, lane);
                 if (!(ex > -INFINITY)) continue;
                 int pos = K;
                 for (int r = 0; r < K; r++)
@@ -283,19 +409,18 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
             have_exact = true;
         }
         if (lane == 0) {
-            // softmax over the selected raw logits, times the weight scale
             float m = -INFINITY;
             for (int r = 0; r < K; r++)
                 if (sel[r] != 0x7fffffff) m = fmaxf(m, selv[r]);
             float ew[MOE_MAX_TOPK], s = 0.f;
             for (int r = 0; r < K; r++) {
-                float d = have_exact ? (float)(exactv[r] - (double)m) : (selv[r] - m);
+                const float d = have_exact ? (float)(exactv[r] - (double)m) : (selv[r] - m);
                 ew[r] = (sel[r] == 0x7fffffff) ? 0.f : expf(d);
                 s += ew[r];
             }
             for (int r = 0; r < K; r++) {
-                int id = (sel[r] == 0x7fffffff) ? 0 : sel[r];  // unfilled slot: expert 0, weight 0
-                float w = (s > 0.f) ? a.bp.wscale * (ew[r] / s) : 0.f;
+                const int id = (sel[r] == 0x7fffffff) ? 0 : sel[r];  // unfilled slot: expert 0, weight 0
+                const float w = (s > 0.f) ? a.bp.wscale * (ew[r] / s) : 0.f;
                 a.ws.ids[t * K + r] = id;
                 a.ws.route_w[t * K + r] = w;
                 if (a.ids_out) a.ids_out[t * K + r] = id;
@@ -303,25 +428,26 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
             }
         }
     }
+    if (tid == 0) a.ws.tickets[1 + blockIdx.x] = 0u;  // re-arm the group ticket
 
-    // --------------------------------------------- last CTA: permutation
+    // --------------------------------------------- last CTA of the grid: permutation
     __threadfence();
     __syncthreads();
-    if (tid == 0) last_flag = (atomicAdd(a.ws.ticket, 1u) == gridDim.x - 1);
+    if (tid == 0) s_flag = (atomicAdd(a.ws.tickets, 1u) == gridDim.x - 1);
     __syncthreads();
-    if (!last_flag) return;
+    if (!s_flag) return;
     __threadfence();
 
     const int ns = a.bp.n_shared;
-    const int EE = E + ns;            // experts incl. the shared one
-    const int KK = K + ns;            // slots per token incl. the shared one
-    const int R = a.T * K;            // routed routes
-    int32_t *cnt = reinterpret_cast<int32_t *>(smem);   // [EE]      (reuses the x_hat area)
-    int32_t *offs = cnt + 264;                            // [EE + 1]
-    int32_t *run = offs + 264;                            // [EE]
-    int32_t *tcnt = run + 264;                            // [EE]
-    int32_t *toff = tcnt + 264;                           // [EE + 1]
-    int32_t *wcnt = toff + 264;                           // [kRouteWarps][EE]
+    const int EE = E + ns;
+    const int KK = K + ns;
+    const int R = a.T * K;
+    int32_t *cnt = reinterpret_cast<int32_t *>(smem);  // reuses the x_hat area
+    int32_t *offs = cnt + 264;
+    int32_t *run = offs + 264;
+    int32_t *tcnt = run + 264;
+    int32_t *toff = tcnt + 264;
+    int32_t *wcnt = toff + 264;  // [kRouteWarps][EE]
     for (int e = tid; e < EE; e += kRouteThreads) {
         cnt[e] = 0;
         run[e] = 0;
@@ -346,11 +472,11 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     }
     __syncthreads();
     for (int e = tid; e < EE; e += kRouteThreads) {
-        a.ws.counts[e] = cnt[e];
+        if (e < E) a.ws.counts[e] = cnt[e];
         a.ws.offsets[e] = offs[e];
-        int n = tcnt[e], base = toff[e];
+        const int n = tcnt[e], base = toff[e];
         for (int k = 0; k < n && base + k < a.ws.max_tiles; k++) {
-            int st = k * a.tile_rows;
+            const int st = k * a.tile_rows;
             a.ws.tiles[base + k] = make_int4(e, offs[e] + st, min(a.tile_rows, cnt[e] - st), 0);
         }
     }
@@ -359,26 +485,25 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
         *a.ws.n_tiles = min(toff[EE], a.ws.max_tiles);
         if (toff[EE] > a.ws.max_tiles) set_device_error(a.ws.status, MOE_DEV_BAD_ROUTE, -1);
     }
-    // stable scatter of the routed routes, in token-major (token, slot) order
     const unsigned lt_mask = (1u << lane) - 1u;
     for (int base = 0; base < R; base += kRouteThreads) {
         for (int i = tid; i < kRouteWarps * EE; i += kRouteThreads) wcnt[i] = 0;
         __syncthreads();
-        int r = base + tid;
+        const int r = base + tid;
         int e = -1;
         if (r < R) {
             e = __ldcg(a.ws.ids + r);
             if ((unsigned)e >= (unsigned)E) e = 0;
         }
-        unsigned peers = __match_any_sync(0xffffffffu, e);
-        int rank_w = __popc(peers & lt_mask);
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank_w = __popc(peers & lt_mask);
         if (e >= 0 && rank_w == 0) wcnt[warp * EE + e] = __popc(peers);
         __syncthreads();
         if (e >= 0) {
             int rank = run[e] + rank_w;
             for (int w = 0; w < warp; w++) rank += wcnt[w * EE + e];
-            int pos = offs[e] + rank;
-            int t = r / K, s = r - t * K;
+            const int pos = offs[e] + rank;
+            const int t = r / K, s = r - t * K;
             a.ws.perm_token[pos] = t;
             a.ws.perm_slot[pos] = s;
             a.ws.perm_w[pos] = __ldcg(a.ws.route_w + r);
@@ -394,37 +519,41 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     }
     if (ns) {
         for (int t = tid; t < a.T; t += kRouteThreads) {
-            int pos = offs[E] + t;
+            const int pos = offs[E] + t;
             a.ws.perm_token[pos] = t;
             a.ws.perm_slot[pos] = K;
             a.ws.perm_w[pos] = 1.0f;
             a.ws.loc[t * KK + K] = pos;
         }
     }
-    if (tid == 0) *a.ws.ticket = 0u;  // re-arm for the next launch
+    if (tid == 0) a.ws.tickets[0] = 0u;  // re-arm for the next launch
+}
+
+size_t route_smem_bytes(int G, int H, int E) {
+    const size_t a = (size_t)G * H * 2;
+    const size_t b = (size_t)(5 * 264 + kRouteWarps * (E + 1)) * 4;
+    return a > b ? a : b;
 }
 
 }  // namespace
 
-size_t route_smem_bytes(int G, int H, int E) {
-    size_t a = (size_t)G * H * 2 + (size_t)G * E * 8;
-    size_t b = (size_t)(5 * 264 + kRouteWarps * (E + 1)) * 4;
-    return a > b ? a : b;
-}
+int route_ticket_count(int T) { return T + 1; }
 
-cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x,
-                         const float *gamma, const uint16_t *router_w, const float *router_b, int T,
-                         int32_t *ids_out, float *rw_out, uint16_t *xhat_out, int tile_rows,
-                         int router_exact, int write_mma_layout, cudaStream_t st) {
-    RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows,
-                router_exact, write_mma_layout};
+cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x, const float *gamma,
+                         const uint16_t *router_w, const float *router_b, int T, int32_t *ids_out, float *rw_out,
+                         uint16_t *xhat_out, int tile_rows, int router_exact, int /*write_mma_layout*/,
+                         cudaStream_t st) {
+    if (bp.H / 8 > 32 * kMaxChunks) return cudaErrorInvalidValue;
+    RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact};
     static bool done1 = false, done8 = false;
     if (T <= 32) {
-        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<1>, done1));
-        moe_route_kernel<1><<<T, kRouteThreads, route_smem_bytes(1, bp.H, bp.E), st>>>(a);
+        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<1, 1>, done1));
+        dim3 grid(T, (bp.E + kRouteWarps - 1) / kRouteWarps);
+        moe_route_kernel<1, 1><<<grid, kRouteThreads, route_smem_bytes(1, bp.H, bp.E), st>>>(a);
     } else {
-        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8>, done8));
-        moe_route_kernel<8><<<(T + 7) / 8, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
+        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8, 8>, done8));
+        dim3 grid((T + 7) / 8, (bp.E + 8 * kRouteWarps - 1) / (8 * kRouteWarps));
+        moe_route_kernel<8, 8><<<grid, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
     }
     return cudaGetLastError();
 }
