@@ -123,13 +123,21 @@ __device__ __forceinline__ U128 u128_shfl_xor(const U128 &a, int o) {
     return r;
 }
 
-// Exact Σx² of one bf16 row, rounded once to double.  Squares are placed on a
-// fixed-point grid relative to the largest exponent of the row; a square more
-// than 80 binary places below the largest one (|x| < 2^-40 max|x|) contributes
-// less than 2^-60 of the sum and is dropped, far below double precision.
-__device__ double sumsq_exact(const uint16_t *xr, int H, int tid, int lane, int warp, int *s_maxexp, U128 *s_acc) {
+constexpr int kXC = 2;  // 16-byte chunks of one x row per thread (H <= 8 * 256 * kXC)
+
+// Exact Σx² of one bf16 row held in registers (kXC chunks of 8 per thread),
+// rounded once to double.  Squares are placed on a fixed-point grid relative
+// to the largest exponent of the row; a square more than 80 binary places
+// below the largest one (|x| < 2^-40 max|x|) contributes less than 2^-60 of
+// the sum and is dropped, far below double precision.
+__device__ double sumsq_exact(const uint4 (&xv)[kXC], int lane, int warp, int *s_maxexp, U128 *s_acc) {
     int mx = 0;
-    for (int i = tid; i < H; i += kRouteThreads) mx = max(mx, (int)((xr[i] >> 7) & 0xFF));
+#pragma unroll
+    for (int j = 0; j < kXC; j++) {
+        const uint32_t w4[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; q++) mx = max(mx, (int)max((w4[q] >> 7) & 0xFFu, (w4[q] >> 23) & 0xFFu));
+    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) s_maxexp[warp] = mx;
@@ -139,30 +147,34 @@ __device__ double sumsq_exact(const uint16_t *xr, int H, int tid, int lane, int 
     for (int w = 0; w < kRouteWarps; w++) emax = max(emax, s_maxexp[w]);
     // value = M * 2^(ex - 134) with M = 128 + mant (ex >= 1) or M = mant (ex == 0, exponent taken as 1)
     U128 acc{0ull, 0ull};
-    for (int i = tid; i < H; i += kRouteThreads) {
-        const uint32_t b = xr[i];
-        const int ex = (b >> 7) & 0xFF;
-        const uint32_t M = ex ? (128u + (b & 0x7Fu)) : (b & 0x7Fu);
-        const int d = 2 * (emax - (ex ? ex : 1));
-        if (M == 0 || d > 80) continue;
-        const unsigned long long v = (unsigned long long)M * M;  // < 2^16
-        const int sh = 80 - d;                                  // 0..80
-        U128 t;
-        if (sh == 0) {
-            t.lo = v;
-            t.hi = 0;
-        } else if (sh < 64) {
-            t.lo = v << sh;
-            t.hi = v >> (64 - sh);
-        } else {
-            t.lo = 0;
-            t.hi = v << (sh - 64);
+#pragma unroll
+    for (int j = 0; j < kXC; j++) {
+        const uint32_t w4[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            const uint32_t b = (w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+            const int ex = (b >> 7) & 0xFF;
+            const uint32_t M = ex ? (128u + (b & 0x7Fu)) : (b & 0x7Fu);
+            const int d = 2 * (emax - (ex ? ex : 1));
+            if (M == 0 || d > 80) continue;
+            const unsigned long long v = (unsigned long long)M * M;  // < 2^16
+            const int sh = 80 - d;                                  // 0..80
+            U128 t;
+            if (sh == 0) {
+                t.lo = v;
+                t.hi = 0;
+            } else if (sh < 64) {
+                t.lo = v << sh;
+                t.hi = v >> (64 - sh);
+            } else {
+                t.lo = 0;
+                t.hi = v << (sh - 64);
+            }
+            u128_add(acc, t);
         }
-        u128_add(acc, t);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) u128_add(acc, u128_shfl_xor(acc, o));
-    __syncthreads();  // s_maxexp fully read before the next row reuses it
     if (lane == 0) s_acc[warp] = acc;
     __syncthreads();
     U128 tot{0ull, 0ull};
@@ -171,7 +183,7 @@ __device__ double sumsq_exact(const uint16_t *xr, int H, int tid, int lane, int 
     if (tot.hi == 0 && tot.lo == 0) return 0.0;
     // value = tot * 2^(2*(emax - 134) - 80); take the top 64 significant bits and round to 53 (ties to even)
     const int lz = tot.hi ? __clzll((long long)tot.hi) : 64 + __clzll((long long)tot.lo);
-    const int width = 128 - lz;  // significant bits of tot
+    const int width = 128 - lz;  // significant bits of tot (<= 108)
     unsigned long long top;
     bool sticky;
     int shift;  // tot = top * 2^shift (+ sticky part)
@@ -188,6 +200,21 @@ __device__ double sumsq_exact(const uint16_t *xr, int H, int tid, int lane, int 
     const unsigned long long rem = top & 0x7FFull;
     if (rem > 0x400ull || (rem == 0x400ull && (sticky || (mant & 1ull)))) mant += 1ull;
     return ldexp((double)mant, 11 + shift + 2 * (emax - 134) - 80);
+}
+
+// bf16(x * r * gamma) of one element: fp32 value, recomputed in fp64 when it
+// lies within its error bound (3 fp32 ulps; 8 used) of a bf16 rounding midpoint.
+__device__ __forceinline__ uint32_t norm_elem(uint32_t xb, float gf, float r32, double r) {
+    const float xf = __uint_as_float(xb << 16);
+    const float v32 = (xf * r32) * gf;
+    const uint32_t low = __float_as_uint(v32) & 0xFFFFu;
+    const bool safe =
+        fabsf(v32) >= 0x1p-120f && fabsf(v32) < 0x1p126f && (low > 0x8000u + 8u || low + 8u < 0x8000u);
+    if (safe) {
+        __nv_bfloat16 bb = __float2bfloat16_rn(v32);
+        return *reinterpret_cast<uint16_t *>(&bb);
+    }
+    return bf16_from_double_rne((double)xf * r * (double)gf);
 }
 
 template <int G, int EPW>
@@ -220,36 +247,59 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     }
 
     // ---------------------------------------------------------------- norm
+    // x and gamma are read as 16-byte chunks held in registers: one round trip
+    // per row, issued ahead of use.
     const bool store = blockIdx.y == 0;
+    float4 gm[kXC][2];
+#pragma unroll
+    for (int j = 0; j < kXC; j++) {
+        const int c = tid + kRouteThreads * j;
+        const float4 *g4 = reinterpret_cast<const float4 *>(a.gamma) + 2 * c;
+        gm[j][0] = c < nchunk ? __ldg(g4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        gm[j][1] = c < nchunk ? __ldg(g4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    uint4 xv[kXC], xnext[kXC];
+    auto load_row = [&](int t, uint4(&dst)[kXC]) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
+#pragma unroll
+        for (int j = 0; j < kXC; j++) {
+            const int c = tid + kRouteThreads * j;
+            dst[j] = c < nchunk ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    if (nt > 0) load_row(t0, xv);
     for (int g = 0; g < nt; g++) {
         const int t = t0 + g;
-        const uint16_t *xr = a.x + (size_t)t * H;
-        const double ss = sumsq_exact(xr, H, tid, lane, warp, s_maxexp, s_acc);
+        if (g + 1 < nt) load_row(t + 1, xnext);
+        const double ss = sumsq_exact(xv, lane, warp, s_maxexp, s_acc);
         if (tid == 0) s_r = 1.0 / sqrt(ss / (double)H + a.bp.eps);
         __syncthreads();
         const double r = s_r;
         const float r32 = (float)r;
-        for (int i = tid; i < H; i += kRouteThreads) {
-            const float xf = bf16_to_f32(xr[i]);
-            const float gf = a.gamma[i];
-            const float v32 = (xf * r32) * gf;  // within 3 fp32 ulps of the exact product
-            const uint32_t low = __float_as_uint(v32) & 0xFFFFu;
-            const bool safe = fabsf(v32) >= 0x1p-120f && fabsf(v32) < 0x1p126f &&
-                              (low > 0x8000u + 8u || low + 8u < 0x8000u);
-            uint16_t hb;
-            if (safe) {
-                __nv_bfloat16 bb = __float2bfloat16_rn(v32);
-                hb = *reinterpret_cast<uint16_t *>(&bb);
-            } else {
-                hb = bf16_from_double_rne((double)xf * r * (double)gf);
-            }
-            xh[g * H + i] = hb;
+#pragma unroll
+        for (int j = 0; j < kXC; j++) {
+            const int c = tid + kRouteThreads * j;
+            if (c >= nchunk) continue;
+            const uint32_t w4[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+            const float gg[8] = {gm[j][0].x, gm[j][0].y, gm[j][0].z, gm[j][0].w,
+                                 gm[j][1].x, gm[j][1].y, gm[j][1].z, gm[j][1].w};
+            uint32_t hb[8];
+#pragma unroll
+            for (int q = 0; q < 8; q++) hb[q] = norm_elem((w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, gg[q], r32, r);
+            const uint4 nat = make_uint4(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16, hb[4] | hb[5] << 16,
+                                         hb[6] | hb[7] << 16);
+            *reinterpret_cast<uint4 *>(xh + g * H + 8 * c) = nat;
             if (store) {
-                a.ws.xhat[(size_t)t * H + i] = hb;
-                a.ws.xhat_mma[(size_t)t * H + mma_perm_pos(i)] = hb;
-                if (a.xhat_out) a.xhat_out[(size_t)t * H + i] = hb;
+                // decode-MMA pair order inside each 8-element chunk: (e0,e4),(e1,e5),(e2,e6),(e3,e7)
+                const uint4 prm = make_uint4(hb[0] | hb[4] << 16, hb[1] | hb[5] << 16, hb[2] | hb[6] << 16,
+                                             hb[3] | hb[7] << 16);
+                *reinterpret_cast<uint4 *>(a.ws.xhat + (size_t)t * H + 8 * c) = nat;
+                *reinterpret_cast<uint4 *>(a.ws.xhat_mma + (size_t)t * H + 8 * c) = prm;
+                if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + (size_t)t * H + 8 * c) = nat;
             }
         }
+#pragma unroll
+        for (int j = 0; j < kXC; j++) xv[j] = xnext[j];
         __syncthreads();
     }
 
@@ -543,7 +593,7 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
                          const uint16_t *router_w, const float *router_b, int T, int32_t *ids_out, float *rw_out,
                          uint16_t *xhat_out, int tile_rows, int router_exact, int /*write_mma_layout*/,
                          cudaStream_t st) {
-    if (bp.H / 8 > 32 * kMaxChunks) return cudaErrorInvalidValue;
+    if (bp.H / 8 > 32 * kMaxChunks || bp.H / 8 > kRouteThreads * kXC) return cudaErrorInvalidValue;
     RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact};
     static bool done1 = false, done8 = false;
     if (T <= 32) {
