@@ -86,6 +86,7 @@ size_t carve(const moe_plan *p, int T, char *base, Workspace *ws) {
     Workspace w{};
     w.xhat = c.take<uint16_t>(base, (size_t)T * b.H);
     w.xhat_mma = c.take<uint16_t>(base, (size_t)T * b.H);
+    w.xhat16 = c.take<uint16_t>(base, (size_t)T * b.H);
     w.ids = c.take<int32_t>(base, (size_t)T * b.K);
     w.route_w = c.take<float>(base, (size_t)T * b.K);
     w.counts = c.take<int32_t>(base, b.E + 1);
@@ -98,6 +99,7 @@ size_t carve(const moe_plan *p, int T, char *base, Workspace *ws) {
     w.tiles = c.take<int4>(base, w.max_tiles);
     w.n_tiles = c.take<int32_t>(base, 4);
     w.h = c.take<uint16_t>(base, R * b.F);
+    w.h16 = c.take<uint16_t>(base, R * b.F);
     w.y = c.take<float>(base, R * b.H);
     w.logits = c.take<float>(base, (size_t)T * b.E);
     w.lbound = c.take<float>(base, (size_t)T * b.E);

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,7 +38,8 @@ __device__ __forceinline__ const float *mat_bias(const MatPtrs &m, int e, int n_
 // Device-side view of the workspace carved by the host plan.
 struct Workspace {
     uint16_t *xhat;        // [T][H] bf16
-    uint16_t *xhat_mma;    // [T][H] bf16, 32-blocks reordered for the decode MMA fragments
+    uint16_t *xhat_mma;    // [T][H] bf16, pair order of the prefill dequantiser inside each 8-element chunk
+    uint16_t *xhat16;      // [T][H] fp16 copy of x_hat (decode GEMV operand)
     int32_t *ids;          // [T][K]
     float *route_w;        // [T][K]
     int32_t *counts;       // [E + 1] (index E: shared expert)
@@ -48,7 +50,8 @@ struct Workspace {
     int32_t *loc;          // [T][K + n_shared]
     int4 *tiles;           // [max_tiles]: (expert, route start, route count, 0)
     int32_t *n_tiles;      // [1]
-    uint16_t *h;           // [R][F] bf16 (layout depends on the path)
+    uint16_t *h;           // [R][F] bf16 (decode: natural order; prefill: pair order)
+    uint16_t *h16;         // [R][F] fp16 copy of h (decode GEMV operand)
     float *y;              // [R][H] weighted expert outputs
     float *logits;         // [T][E] router logits (fp32) of the routing kernel
     float *lbound;         // [T][E] their rounding-error bounds

@@ -86,12 +86,63 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
     return r;
 }
 
+// Two exact dequantisers feed the tensor cores:
+//  * fp16 (used when every E8M0 exponent of the work item lies in [104, 140],
+//    where e2m1 * 2^(s-127) is exactly representable in fp16): the hardware
+//    e2m1x2 -> f16x2 conversion turns one byte (two nibbles, low nibble =
+//    even element) into a natural-order pair, then one f16x2 multiply applies
+//    the power-of-two scale; MMA kind f16 against the fp16 activations;
+//  * bf16 (any exponent): the shift/mask construction above, re-paired into
+//    natural order with byte permutes, scaled by one or two bf16x2
+//    multiplies; MMA kind bf16 against the bf16 activations.
+// Both keep K in natural order, so the activations need no reordering.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t h[4]) {
+    asm("{ .reg .b8 a, b, c, d;\n"
+        "  mov.b32 {a, b, c, d}, %4;\n"
+        "  cvt.rn.f16x2.e2m1x2 %0, a;\n"
+        "  cvt.rn.f16x2.e2m1x2 %1, b;\n"
+        "  cvt.rn.f16x2.e2m1x2 %2, c;\n"
+        "  cvt.rn.f16x2.e2m1x2 %3, d; }"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+// fp16 bits of 2^(s-127) in both halves, s in [104, 140]
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t s) {
+    const uint32_t b = (s >= 113u) ? ((s - 112u) << 10) : (1u << (s - 103u));
+    return b | (b << 16);
+}
+__device__ __forceinline__ bool f16_exact_scale(uint32_t s) { return s >= 104u && s <= 140u; }
+
+// natural-order bf16 pairs (n0,n1),(n2,n3),(n4,n5),(n6,n7), exact, any exponent
+template <bool BIG>
+__device__ __forceinline__ void dequant_word_nat(uint32_t w, uint32_t s1, uint32_t s2, uint32_t o[4]) {
+    uint32_t p[4];
+    dequant_word<BIG>(w, s1, s2, p);
+    o[0] = __byte_perm(p[0], p[1], 0x5410);
+    o[1] = __byte_perm(p[2], p[3], 0x5410);
+    o[2] = __byte_perm(p[0], p[1], 0x7632);
+    o[3] = __byte_perm(p[2], p[3], 0x7632);
+}
+
+__device__ __forceinline__ void mma_f16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Persistent CTAs of 8 warps: each CTA walks the work items (tile, 16-row
 // block) with a grid stride; its 8 warps split K (32-element blocks in groups
 // of four per warp-iteration) and reduce through shared memory.  Each thread
 // keeps the next iteration's packed weights in flight (128-bit streaming
 // loads) while it dequantises and multiplies the current ones; the routed
-// activations (already in MMA pair order) are read from L1/L2.
+// activations are read from L1/L2.
 constexpr int kDecWarps = 8;
 constexpr int kMaxNb = 128;  // K <= 4096
 
@@ -109,7 +160,8 @@ __device__ __forceinline__ void load_a(uint4 (&A)[2][2], const uint8_t *c0, cons
         }
 }
 
-template <bool GATEUP, int NT, bool BIG>
+// PATH: 0 = fp16 conversion, 1 = bf16 (exponents <= 128), 2 = bf16 (any exponent)
+template <bool GATEUP, int NT, int PATH>
 __device__ __forceinline__ void decode_mainloop(int K, const uint8_t *c0, const uint8_t *c1, const uint8_t *sc,
                                                 const uint16_t *const (&brow)[NT], float acc[2][NT][4]) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -139,20 +191,40 @@ __device__ __forceinline__ void decode_mainloop(int K, const uint8_t *c0, const 
 #pragma unroll
             for (int h = 0; h < 2; h++) {
                 const uint32_t s = valid ? sc[(m * 16 + g + 8 * h) * kMaxNb + b] : 127u;
-                s1[m][h] = scale_lo(s);
-                s2[m][h] = scale_hi(s);
+                if (PATH == 0) {
+                    s1[m][h] = scale_f16x2(s);
+                    s2[m][h] = 0;
+                } else {
+                    s1[m][h] = scale_lo(s);
+                    s2[m][h] = scale_hi(s);
+                }
             }
 #pragma unroll
         for (int k = 0; k < 4; k++) {
 #pragma unroll
             for (int m = 0; m < NM; m++) {
                 uint32_t p0[4], p1[4];
-                dequant_word<BIG>((&A[m][0].x)[k], s1[m][0], s2[m][0], p0);
-                dequant_word<BIG>((&A[m][1].x)[k], s1[m][1], s2[m][1], p1);
+                if (PATH == 0) {
+                    e2m1x8_to_f16((&A[m][0].x)[k], p0);
+                    e2m1x8_to_f16((&A[m][1].x)[k], p1);
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        p0[i] = hmul2_f16(p0[i], s1[m][0]);
+                        p1[i] = hmul2_f16(p1[i], s1[m][1]);
+                    }
+                } else {
+                    dequant_word_nat<PATH == 2>((&A[m][0].x)[k], s1[m][0], s2[m][0], p0);
+                    dequant_word_nat<PATH == 2>((&A[m][1].x)[k], s1[m][1], s2[m][1], p1);
+                }
 #pragma unroll
                 for (int n = 0; n < NT; n++) {
-                    mma_bf16_16816(acc[m][n], p0[0], p1[0], p0[1], p1[1], B[n][k].x, B[n][k].y);
-                    mma_bf16_16816(acc[m][n], p0[2], p1[2], p0[3], p1[3], B[n][k].z, B[n][k].w);
+                    if (PATH == 0) {
+                        mma_f16_16816(acc[m][n], p0[0], p1[0], p0[1], p1[1], B[n][k].x, B[n][k].y);
+                        mma_f16_16816(acc[m][n], p0[2], p1[2], p0[3], p1[3], B[n][k].z, B[n][k].w);
+                    } else {
+                        mma_bf16_16816(acc[m][n], p0[0], p1[0], p0[1], p1[1], B[n][k].x, B[n][k].y);
+                        mma_bf16_16816(acc[m][n], p0[2], p1[2], p0[3], p1[3], B[n][k].z, B[n][k].w);
+                    }
                 }
             }
         }
@@ -180,7 +252,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) moe_decode_kernel(DecodeArgs a
         const uint8_t *c0 = mat_codes(a.A0, e, E) + (size_t)j0 * (K / 2);
         const uint8_t *c1 = GATEUP ? mat_codes(a.A1, e, E) + (size_t)j0 * (K / 2) : nullptr;
         // scales of the 16 rows (contiguous in the canonical layout)
-        int big = 0;
+        int not_f16 = 0, big = 0;
 #pragma unroll
         for (int m = 0; m < NM; m++) {
             const uint8_t *s = mat_scales(m == 0 ? a.A0 : a.A1, e, E) + (size_t)j0 * nb;
@@ -188,19 +260,27 @@ __global__ void __launch_bounds__(kDecWarps * 32) moe_decode_kernel(DecodeArgs a
                 const int r = i / nb, b = i - r * nb;
                 const uint8_t v = s[i];
                 sc[(m * 16 + r) * kMaxNb + b] = v;
+                not_f16 |= !f16_exact_scale(v);
                 big |= (v > 128);
             }
         }
+        not_f16 = __syncthreads_or(not_f16);
         big = __syncthreads_or(big);
+        const int path = not_f16 ? (big ? 2 : 1) : 0;
         // activation rows of this thread's MMA column (route) in each n-tile
         const uint16_t *brow[NT];
 #pragma unroll
         for (int n = 0; n < NT; n++) {
             const int col = n * 8 + g;
             brow[n] = nullptr;
-            if (col < rcount)
-                brow[n] = GATEUP ? a.ws.xhat_mma + (size_t)a.ws.perm_token[rstart + col] * K
-                                 : a.ws.h + (size_t)(rstart + col) * K;
+            if (col < rcount) {
+                if (GATEUP) {
+                    const size_t tok = (size_t)a.ws.perm_token[rstart + col];
+                    brow[n] = (path == 0 ? a.ws.xhat16 : a.ws.xhat) + tok * K;
+                } else {
+                    brow[n] = (path == 0 ? a.ws.h16 : a.ws.h) + (size_t)(rstart + col) * K;
+                }
+            }
         }
         float acc[2][NT][4];
 #pragma unroll
@@ -209,10 +289,12 @@ __global__ void __launch_bounds__(kDecWarps * 32) moe_decode_kernel(DecodeArgs a
             for (int n = 0; n < NT; n++)
 #pragma unroll
                 for (int r = 0; r < 4; r++) acc[m][n][r] = 0.f;
-        if (big)
-            decode_mainloop<GATEUP, NT, true>(K, c0, c1, sc, brow, acc);
+        if (path == 0)
+            decode_mainloop<GATEUP, NT, 0>(K, c0, c1, sc, brow, acc);
+        else if (path == 1)
+            decode_mainloop<GATEUP, NT, 1>(K, c0, c1, sc, brow, acc);
         else
-            decode_mainloop<GATEUP, NT, false>(K, c0, c1, sc, brow, acc);
+            decode_mainloop<GATEUP, NT, 2>(K, c0, c1, sc, brow, acc);
 #pragma unroll
         for (int m = 0; m < NM; m++)
 #pragma unroll
@@ -242,8 +324,10 @@ __global__ void __launch_bounds__(kDecWarps * 32) moe_decode_kernel(DecodeArgs a
                 const float gg = s[0] + mat_bias(a.A0, e, E)[j];
                 const float uu = s[1] + mat_bias(a.A1, e, E)[j];
                 const float hv = swiglu_clamped(gg, uu, a.bp.alpha, a.bp.limit);
-                __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                a.ws.h[(size_t)route * a.bp.F + mma_perm_pos(j)] = *reinterpret_cast<uint16_t *>(&hb);
+                const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                const __half h16 = __float2half_rn(__bfloat162float(hb));  // exact for |h| >= 2^-14
+                a.ws.h[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&hb);
+                a.ws.h16[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&h16);
             } else {
                 const float yv = s[0] + mat_bias(a.A0, e, E)[j];
                 a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * yv;
@@ -279,7 +363,8 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(BlockParams bp, Worksp
     *reinterpret_cast<float4 *>(out + (size_t)t * H + i4 * 4) = o;
 }
 
-// One thread per 32-element block: the GEMV's dequantisation, un-permuted.
+// One thread per 32-element block: the GEMV's element converters (fp16 where
+// the exponent allows it exactly, bf16 otherwise), written out in natural order.
 __global__ void moe_dequant_kernel(MatPtrs m, int expert, int n_experts, float *out) {
     const int nb = m.cols / 32;
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -287,20 +372,28 @@ __global__ void moe_dequant_kernel(MatPtrs m, int expert, int n_experts, float *
     const size_t row = i / nb, b = i - row * nb;
     const uint8_t *codes = mat_codes(m, expert, n_experts);
     const uint8_t *scales = mat_scales(m, expert, n_experts);
-    uint4 v = *reinterpret_cast<const uint4 *>(codes + row * (m.cols / 2) + 16 * b);
-    uint32_t s = scales[row * nb + b];
-    uint32_t s1 = scale_lo(s), s2 = scale_hi(s);
+    const uint4 v = *reinterpret_cast<const uint4 *>(codes + row * (m.cols / 2) + 16 * b);
+    const uint32_t s = scales[row * nb + b];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float *o = out + row * m.cols + 32 * b;
     for (int k = 0; k < 4; k++) {
         uint32_t p[4];
-        if (s > 128u)
-            dequant_word<true>(w[k], s1, s2, p);
-        else
-            dequant_word<false>(w[k], s1, s2, p);
-        for (int ii = 0; ii < 4; ii++) {
-            o[8 * k + ii] = __uint_as_float(p[ii] << 16);
-            o[8 * k + ii + 4] = __uint_as_float(p[ii] & 0xFFFF0000u);
+        if (f16_exact_scale(s)) {
+            e2m1x8_to_f16(w[k], p);
+            for (int ii = 0; ii < 4; ii++) p[ii] = hmul2_f16(p[ii], scale_f16x2(s));
+            for (int ii = 0; ii < 4; ii++) {
+                o[8 * k + 2 * ii] = __half2float(__ushort_as_half((unsigned short)(p[ii] & 0xFFFFu)));
+                o[8 * k + 2 * ii + 1] = __half2float(__ushort_as_half((unsigned short)(p[ii] >> 16)));
+            }
+        } else {
+            if (s > 128u)
+                dequant_word_nat<true>(w[k], scale_lo(s), scale_hi(s), p);
+            else
+                dequant_word_nat<false>(w[k], scale_lo(s), scale_hi(s), p);
+            for (int ii = 0; ii < 4; ii++) {
+                o[8 * k + 2 * ii] = __uint_as_float(p[ii] << 16);
+                o[8 * k + 2 * ii + 1] = __uint_as_float(p[ii] & 0xFFFF0000u);
+            }
         }
     }
 }

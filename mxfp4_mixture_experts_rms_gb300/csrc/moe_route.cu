@@ -76,14 +76,25 @@ __device__ __forceinline__ void warp_best(float &v, int &i) {
     }
 }
 
-// Exact (fp64) router logit of expert e for an x_hat row in shared memory, by one warp.
+// Exact (fp64) router logit of expert e for an x_hat row in shared memory, by
+// one warp: 16-byte loads of the router row, products of two bf16 values are
+// exact in fp64, four independent accumulators per lane.
 __device__ double exact_logit(const uint16_t *xh, const uint16_t *router_w, const float *router_b, int e, int H,
                               int lane) {
-    double acc = 0.0;
-    const uint16_t *w = router_w + (size_t)e * H;
-    for (int i = lane; i < H; i += 32) acc += (double)bf16_to_f32(xh[i]) * (double)bf16_to_f32(__ldg(w + i));
-    acc = warp_sum_d(acc);
-    return acc + (double)router_b[e];
+    double acc[4] = {0.0, 0.0, 0.0, 0.0};
+    const uint4 *w = reinterpret_cast<const uint4 *>(router_w + (size_t)e * H);
+    const uint4 *x = reinterpret_cast<const uint4 *>(xh);
+    for (int c = lane; c < H / 8; c += 32) {
+        const uint4 wv = __ldg(w + c), xv = x[c];
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w}, xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            acc[q] += (double)__uint_as_float(xx[q] << 16) * (double)__uint_as_float(ww[q] << 16);
+            acc[q] += (double)__uint_as_float(xx[q] & 0xFFFF0000u) * (double)__uint_as_float(ww[q] & 0xFFFF0000u);
+        }
+    }
+    double s = warp_sum_d((acc[0] + acc[1]) + (acc[2] + acc[3]));
+    return s + (double)router_b[e];
 }
 
 // Exclusive scan by one warp over n <= 1024 ints (out[n] = total).
@@ -295,6 +306,15 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
                                              hb[3] | hb[7] << 16);
                 *reinterpret_cast<uint4 *>(a.ws.xhat + (size_t)t * H + 8 * c) = nat;
                 *reinterpret_cast<uint4 *>(a.ws.xhat_mma + (size_t)t * H + 8 * c) = prm;
+                // fp16 copy (exact for |x_hat| >= 2^-14) for the fp16 tensor-core GEMV
+                uint32_t f[8];
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));
+                    f[q] = *reinterpret_cast<uint16_t *>(&hh);
+                }
+                *reinterpret_cast<uint4 *>(a.ws.xhat16 + (size_t)t * H + 8 * c) =
+                    make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
                 if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + (size_t)t * H + 8 * c) = nat;
             }
         }
@@ -304,10 +324,12 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     }
 
     // -------------------------------------------------------------- router
-    // fp32 chain per lane (products of two bf16 are exact in fp32), then a
-    // 5-level butterfly and the bias: error <= gamma_n * (Σ|p| + |b| + |l|),
-    // n = per-lane chain length + 6; stored doubled as a safety margin.
-    const int chain = 8 * per_lane + 6;
+    // Products of two bf16 are exact in fp32.  Each 8-product chunk is summed
+    // first (7 roundings), chunk sums are accumulated per lane (per_lane
+    // roundings), then a 5-level butterfly and the bias: every partial sum is
+    // bounded by Σ|p|, so the error is <= gamma_n * (Σ|p| + |b| + |l|) with
+    // n = 7 + per_lane + 6; the stored bound is doubled as a safety margin.
+    const int chain = 7 + per_lane + 6;
     for (int k = 0; k < EPW; k++) {
         const int e = e0 + warp * EPW + k;
         if (k > 0) {
@@ -333,15 +355,17 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
                         if (g < nt) {
                             const uint4 xv = *reinterpret_cast<const uint4 *>(xh + g * H + ch * 8);
                             const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+                            float cs = 0.f;
 #pragma unroll
                             for (int q = 0; q < 4; q++) {
                                 const float p0 = __uint_as_float(xx[q] << 16) * __uint_as_float(ww[q] << 16);
                                 const float p1 =
                                     __uint_as_float(xx[q] & 0xFFFF0000u) * __uint_as_float(ww[q] & 0xFFFF0000u);
-                                acc[g] += p0;
-                                acc[g] += p1;
+                                cs += p0;
+                                cs += p1;
                                 sab[g] += fabsf(p0) + fabsf(p1);
                             }
+                            acc[g] += cs;
                         }
                     }
                 }
