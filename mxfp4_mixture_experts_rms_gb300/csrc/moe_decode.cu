@@ -78,14 +78,6 @@ __device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const void *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
 // Two exact dequantisers feed the tensor cores:
 //  * fp16 (used when every E8M0 exponent of the work item lies in [104, 140],
 //    where e2m1 * 2^(s-127) is exactly representable in fp16): the hardware
@@ -137,60 +129,104 @@ __device__ __forceinline__ void mma_f16_16816(float d[4], uint32_t a0, uint32_t 
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Persistent CTAs of 8 warps: each CTA walks the work items (tile, 16-row
-// block) with a grid stride; its 8 warps split K (32-element blocks in groups
-// of four per warp-iteration) and reduce through shared memory.  Each thread
-// keeps the next iteration's packed weights in flight (128-bit streaming
-// loads) while it dequantises and multiplies the current ones; the routed
-// activations are read from L1/L2.
+// Persistent CTAs of 8 warps, each owning a contiguous range of work items
+// (tile, 16-row block).  The packed codes and E8M0 scales of an item (16 rows
+// of one or two matrices, contiguous rows in the canonical layout) are
+// streamed into a two-stage shared-memory ring by bulk asynchronous copies
+// (one per row, padded row stride for conflict-free fragment reads) while the
+// previous item is computed.  The 8 warps split K (32-element blocks in groups
+// of four per warp-iteration) and reduce through shared memory; each thread
+// prefetches the next iteration's activation fragments into registers.
 constexpr int kDecWarps = 8;
-constexpr int kMaxNb = 128;  // K <= 4096
+constexpr uint64_t kDecWaitNs = 2000000000ull;
 
-template <int NM>
-__device__ __forceinline__ void load_a(uint4 (&A)[2][2], const uint8_t *c0, const uint8_t *c1, size_t rowb, int g,
-                                       int b, bool valid) {
-#pragma unroll
-    for (int m = 0; m < 2; m++)
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-            if (m < NM && valid)
-                A[m][h] = ldg_stream((m == 0 ? c0 : c1) + (size_t)(g + 8 * h) * rowb + 16 * b);
-            else
-                A[m][h] = make_uint4(0, 0, 0, 0);
-        }
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+__device__ __forceinline__ bool dec_mbar_try(uint64_t *b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait (about 2 s, or until another CTA reported a failure).
+__device__ __forceinline__ bool dec_mbar_wait(uint64_t *b, uint32_t parity, int32_t *status, int where) {
+    if (dec_mbar_try(b, parity)) return true;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (uint32_t i = 0;; i++) {
+        if (dec_mbar_try(b, parity)) return true;
+        if ((i & 63) == 63) {
+            if (*(volatile int32_t *)status != 0) return false;
+            uint64_t t1;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+            if (t1 - t0 > kDecWaitNs) {
+                set_device_error(status, MOE_DEV_WAIT_TIMEOUT, where);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Shared-memory geometry of one stage for reduction length K.
+struct DecGeom {
+    int rs;        // padded row stride of packed codes (bytes); rs/4 = 16 (mod 32) banks
+    int scb;       // bytes of one matrix's 16 rows of scales, rounded to 16
+    int stage;     // bytes of one stage (NM matrices)
+    __host__ __device__ DecGeom(int K, int NM) {
+        const int rb = K / 2;
+        rs = rb + ((64 - (rb & 127)) & 127);
+        scb = (16 * (K / 32) + 15) & ~15;
+        stage = (NM * (16 * rs + scb) + 127) & ~127;
+    }
+};
 
 // PATH: 0 = fp16 conversion, 1 = bf16 (exponents <= 128), 2 = bf16 (any exponent)
 template <bool GATEUP, int NT, int PATH>
-__device__ __forceinline__ void decode_mainloop(int K, const uint8_t *c0, const uint8_t *c1, const uint8_t *sc,
+__device__ __forceinline__ void decode_mainloop(int K, const unsigned char *st, const DecGeom &geo,
                                                 const uint16_t *const (&brow)[NT], float acc[2][NT][4]) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t4 = lane & 3;
     const int nb = K / 32, nq = (nb + 3) / 4;
-    const size_t rowb = (size_t)K / 2;
     constexpr int NM = GATEUP ? 2 : 1;
-    uint4 A[2][2];
-    int q = warp;
-    load_a<NM>(A, c0, c1, rowb, g, 4 * q + t4, q < nq && 4 * q + t4 < nb);
-    for (; q < nq; q += kDecWarps) {
+    const unsigned char *codes = st;                    // [NM][16][rs]
+    const uint8_t *sc = st + NM * 16 * geo.rs;          // [NM][scb]
+    auto load_b = [&](uint4 (&B)[NT][4], int q) {
         const int b = 4 * q + t4;
-        const bool valid = b < nb;
-        uint4 An[2][2];
-        const int qn = q + kDecWarps;
-        load_a<NM>(An, c0, c1, rowb, g, 4 * qn + t4, qn < nq && 4 * qn + t4 < nb);
-        uint4 B[NT][4];
+        const bool valid = q < nq && b < nb;
 #pragma unroll
         for (int n = 0; n < NT; n++)
 #pragma unroll
             for (int k = 0; k < 4; k++)
                 B[n][k] = (valid && brow[n]) ? __ldg(reinterpret_cast<const uint4 *>(brow[n] + 32 * b) + k)
                                             : make_uint4(0, 0, 0, 0);
+    };
+    uint4 B[NT][4];
+    load_b(B, warp);
+    for (int q = warp; q < nq; q += kDecWarps) {
+        const int b = 4 * q + t4;
+        const bool valid = b < nb;
+        uint4 Bn[NT][4];
+        load_b(Bn, q + kDecWarps);
+        uint4 A[2][2];
         uint32_t s1[2][2], s2[2][2];
 #pragma unroll
         for (int m = 0; m < NM; m++)
 #pragma unroll
             for (int h = 0; h < 2; h++) {
-                const uint32_t s = valid ? sc[(m * 16 + g + 8 * h) * kMaxNb + b] : 127u;
+                const int r = g + 8 * h;
+                A[m][h] = valid ? *reinterpret_cast<const uint4 *>(codes + (m * 16 + r) * geo.rs + 16 * b)
+                                : make_uint4(0, 0, 0, 0);
+                const uint32_t s = valid ? sc[m * geo.scb + r * nb + b] : 127u;
                 if (PATH == 0) {
                     s1[m][h] = scale_f16x2(s);
                     s2[m][h] = 0;
@@ -229,56 +265,95 @@ __device__ __forceinline__ void decode_mainloop(int K, const uint8_t *c0, const 
             }
         }
 #pragma unroll
-        for (int m = 0; m < 2; m++)
+        for (int n = 0; n < NT; n++)
 #pragma unroll
-            for (int h = 0; h < 2; h++) A[m][h] = An[m][h];
+            for (int k = 0; k < 4; k++) B[n][k] = Bn[n][k];
     }
 }
 
 template <bool GATEUP, int NT>
-__global__ void __launch_bounds__(kDecWarps * 32) moe_decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kDecWarps * 32, 2) moe_decode_kernel(DecodeArgs a) {
     constexpr int NM = GATEUP ? 2 : 1;
-    __shared__ __align__(16) uint8_t sc[NM * 16 * kMaxNb];              // E8M0 of the item's rows
-    __shared__ __align__(16) float red[kDecWarps][NM][NT][16][8];       // split-K partials
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ __align__(16) float red[kDecWarps][NM][NT][16][8];  // split-K partials
+    __shared__ __align__(8) uint64_t full[2];
     const int K = a.Kdim, nb = K / 32;
+    const DecGeom geo(K, NM);
     const int RB = a.rows / 16;
     const int n_items = *a.ws.n_tiles * RB;
+    const int per = (n_items + gridDim.x - 1) / gridDim.x;
+    const int begin = blockIdx.x * per, end = min(n_items, begin + per);
+    const int n = end - begin;
+    if (n <= 0) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
     const int E = a.bp.E;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    int32_t *status = a.ws.status;
+
+    // producer (thread 0): all rows and scales of one item into stage s
+    auto issue = [&](int item, int s) {
         const int4 tile = a.ws.tiles[item / RB];
-        const int e = tile.x, rstart = tile.y, rcount = tile.z;
-        const int j0 = (item % RB) * 16;
-        const uint8_t *c0 = mat_codes(a.A0, e, E) + (size_t)j0 * (K / 2);
-        const uint8_t *c1 = GATEUP ? mat_codes(a.A1, e, E) + (size_t)j0 * (K / 2) : nullptr;
-        // scales of the 16 rows (contiguous in the canonical layout)
-        int not_f16 = 0, big = 0;
+        const int e = tile.x, j0 = (item % RB) * 16;
+        unsigned char *st = dsm + s * geo.stage;
+        const uint32_t bytes = NM * 16 * (K / 2) + NM * 16 * nb;
+        asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(
+                         smem_addr(&full[s])),
+                     "r"(bytes)
+                     : "memory");
 #pragma unroll
         for (int m = 0; m < NM; m++) {
-            const uint8_t *s = mat_scales(m == 0 ? a.A0 : a.A1, e, E) + (size_t)j0 * nb;
-            for (int i = tid; i < 16 * nb; i += kDecWarps * 32) {
-                const int r = i / nb, b = i - r * nb;
-                const uint8_t v = s[i];
-                sc[(m * 16 + r) * kMaxNb + b] = v;
+            const MatPtrs &M = m == 0 ? a.A0 : a.A1;
+            const uint8_t *src = mat_codes(M, e, E) + (size_t)j0 * (K / 2);
+            for (int r = 0; r < 16; r++) bulk_g2s(st + (m * 16 + r) * geo.rs, src + (size_t)r * (K / 2), K / 2, &full[s]);
+            bulk_g2s(st + NM * 16 * geo.rs + m * geo.scb, mat_scales(M, e, E) + (size_t)j0 * nb, 16 * nb, &full[s]);
+        }
+    };
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[0])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[1])));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(begin, 0);
+        if (n > 1) issue(begin + 1, 1);
+    }
+    __syncthreads();
+
+    int cur_tile = -1;
+    int4 tile = make_int4(0, 0, 0, 0);
+    for (int k = 0; k < n; k++) {
+        const int item = begin + k, s = k & 1;
+        if (item / RB != cur_tile) {
+            cur_tile = item / RB;
+            tile = a.ws.tiles[cur_tile];
+        }
+        const int e = tile.x, rstart = tile.y, rcount = tile.z;
+        const int j0 = (item % RB) * 16;
+        const bool ok = dec_mbar_wait(&full[s], (k >> 1) & 1, status, 50);
+        const unsigned char *st = dsm + s * geo.stage;
+        // dequantisation path of this item
+        int not_f16 = 0, big = 0;
+        if (ok) {
+            const uint8_t *sc = st + NM * 16 * geo.rs;
+            for (int i = tid; i < NM * 16 * nb; i += kDecWarps * 32) {
+                const int m = i / (16 * nb), rem = i - m * 16 * nb;
+                const uint32_t v = sc[m * geo.scb + rem];
                 not_f16 |= !f16_exact_scale(v);
-                big |= (v > 128);
+                big |= (v > 128u);
             }
         }
         not_f16 = __syncthreads_or(not_f16);
         big = __syncthreads_or(big);
         const int path = not_f16 ? (big ? 2 : 1) : 0;
-        // activation rows of this thread's MMA column (route) in each n-tile
         const uint16_t *brow[NT];
 #pragma unroll
-        for (int n = 0; n < NT; n++) {
-            const int col = n * 8 + g;
-            brow[n] = nullptr;
+        for (int nn = 0; nn < NT; nn++) {
+            const int col = nn * 8 + g;
+            brow[nn] = nullptr;
             if (col < rcount) {
                 if (GATEUP) {
                     const size_t tok = (size_t)a.ws.perm_token[rstart + col];
-                    brow[n] = (path == 0 ? a.ws.xhat16 : a.ws.xhat) + tok * K;
+                    brow[nn] = (path == 0 ? a.ws.xhat16 : a.ws.xhat) + tok * K;
                 } else {
-                    brow[n] = (path == 0 ? a.ws.h16 : a.ws.h) + (size_t)(rstart + col) * K;
+                    brow[nn] = (path == 0 ? a.ws.h16 : a.ws.h) + (size_t)(rstart + col) * K;
                 }
             }
         }
@@ -286,55 +361,64 @@ __global__ void __launch_bounds__(kDecWarps * 32) moe_decode_kernel(DecodeArgs a
 #pragma unroll
         for (int m = 0; m < 2; m++)
 #pragma unroll
-            for (int n = 0; n < NT; n++)
+            for (int nn = 0; nn < NT; nn++)
 #pragma unroll
-                for (int r = 0; r < 4; r++) acc[m][n][r] = 0.f;
-        if (path == 0)
-            decode_mainloop<GATEUP, NT, 0>(K, c0, c1, sc, brow, acc);
-        else if (path == 1)
-            decode_mainloop<GATEUP, NT, 1>(K, c0, c1, sc, brow, acc);
-        else
-            decode_mainloop<GATEUP, NT, 2>(K, c0, c1, sc, brow, acc);
+                for (int r = 0; r < 4; r++) acc[m][nn][r] = 0.f;
+        if (ok) {
+            if (path == 0)
+                decode_mainloop<GATEUP, NT, 0>(K, st, geo, brow, acc);
+            else if (path == 1)
+                decode_mainloop<GATEUP, NT, 1>(K, st, geo, brow, acc);
+            else
+                decode_mainloop<GATEUP, NT, 2>(K, st, geo, brow, acc);
+        }
 #pragma unroll
         for (int m = 0; m < NM; m++)
 #pragma unroll
-            for (int n = 0; n < NT; n++) {
-                float(*r)[8] = red[warp][m][n];
-                r[g][2 * t4] = acc[m][n][0];
-                r[g][2 * t4 + 1] = acc[m][n][1];
-                r[g + 8][2 * t4] = acc[m][n][2];
-                r[g + 8][2 * t4 + 1] = acc[m][n][3];
+            for (int nn = 0; nn < NT; nn++) {
+                float(*r)[8] = red[warp][m][nn];
+                r[g][2 * t4] = acc[m][nn][0];
+                r[g][2 * t4 + 1] = acc[m][nn][1];
+                r[g + 8][2 * t4] = acc[m][nn][2];
+                r[g + 8][2 * t4 + 1] = acc[m][nn][3];
             }
-        __syncthreads();
-        for (int idx = tid; idx < 16 * 8 * NT; idx += kDecWarps * 32) {
-            const int row = idx & 15, col = idx >> 4;  // col = route within the tile
-            if (col >= rcount) continue;
-            const int n = col >> 3, c = col & 7;
-            float s[NM];
+        __syncthreads();  // stage s fully read; partials visible
+        if (tid == 0 && k + 2 < n) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(item + 2, s);
+        }
+        if (ok) {
+            for (int idx = tid; idx < 16 * 8 * NT; idx += kDecWarps * 32) {
+                const int row = idx & 15, col = idx >> 4;  // col = route within the tile
+                if (col >= rcount) continue;
+                const int nn = col >> 3, c = col & 7;
+                float sm[NM];
 #pragma unroll
-            for (int m = 0; m < NM; m++) {
-                float v = 0.f;
+                for (int m = 0; m < NM; m++) {
+                    float v = 0.f;
 #pragma unroll
-                for (int w = 0; w < kDecWarps; w++) v += red[w][m][n][row][c];
-                s[m] = v;
-            }
-            const int j = j0 + row;
-            const int route = rstart + col;
-            if (GATEUP) {
-                const float gg = s[0] + mat_bias(a.A0, e, E)[j];
-                const float uu = s[1] + mat_bias(a.A1, e, E)[j];
-                const float hv = swiglu_clamped(gg, uu, a.bp.alpha, a.bp.limit);
-                const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                const __half h16 = __float2half_rn(__bfloat162float(hb));  // exact for |h| >= 2^-14
-                a.ws.h[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&hb);
-                a.ws.h16[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&h16);
-            } else {
-                const float yv = s[0] + mat_bias(a.A0, e, E)[j];
-                a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * yv;
+                    for (int w = 0; w < kDecWarps; w++) v += red[w][m][nn][row][c];
+                    sm[m] = v;
+                }
+                const int j = j0 + row;
+                const int route = rstart + col;
+                if (GATEUP) {
+                    const float gg = sm[0] + mat_bias(a.A0, e, E)[j];
+                    const float uu = sm[1] + mat_bias(a.A1, e, E)[j];
+                    const float hv = swiglu_clamped(gg, uu, a.bp.alpha, a.bp.limit);
+                    const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                    const __half h16 = __float2half_rn(__bfloat162float(hb));  // exact for |h| >= 2^-14
+                    a.ws.h[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&hb);
+                    a.ws.h16[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&h16);
+                } else {
+                    const float yv = sm[0] + mat_bias(a.A0, e, E)[j];
+                    a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * yv;
+                }
             }
         }
-        __syncthreads();  // red / sc are reused by the next item
+        __syncthreads();  // red is reused by the next item
     }
+    // every issued copy was waited for above (or timed out and was reported)
 }
 
 // out[t] = x[t] + Σ_slot y[loc[t][slot]] (slot order; the shared expert last)
@@ -408,23 +492,26 @@ __global__ void moe_scan_scales_kernel(const uint8_t *s, size_t n, int32_t *flag
 
 }  // namespace
 
-size_t decode_smem_bytes(bool, int, int) { return 0; }
+size_t decode_smem_bytes(bool gateup, int, int K) { return 2 * (size_t)DecGeom(K, gateup ? 2 : 1).stage; }
 
 template <bool GATEUP, int NT>
 static cudaError_t launch_one(const DecodeArgs &a, int n_items_max, cudaStream_t st) {
     static int per_sm = 0, n_sm = 0;
+    static bool done = false;
+    const size_t smem = decode_smem_bytes(GATEUP, NT, a.Kdim);
+    MOE_CUDA_TRY(smem_optin_once(moe_decode_kernel<GATEUP, NT>, done));
     if (!per_sm) {
         int dev = 0;
         MOE_CUDA_TRY(cudaGetDevice(&dev));
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
         MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_decode_kernel<GATEUP, NT>,
-                                                                   kDecWarps * 32, 0));
+                                                                   kDecWarps * 32, smem));
         if (per_sm < 1) per_sm = 1;
     }
     int grid = n_sm * per_sm;
     if (grid > n_items_max) grid = n_items_max;
     if (grid < 1) grid = 1;
-    moe_decode_kernel<GATEUP, NT><<<grid, kDecWarps * 32, 0, st>>>(a);
+    moe_decode_kernel<GATEUP, NT><<<grid, kDecWarps * 32, smem, st>>>(a);
     return cudaGetLastError();
 }
 
