@@ -181,26 +181,33 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 struct DecGeom {
     int rs;        // padded row stride of packed codes (bytes); rs/4 = 16 (mod 32) banks
     int scb;       // bytes of one matrix's 16 rows of scales, rounded to 16
+    int bias;      // offset of the [NM][16] fp32 biases in a stage
     int stage;     // bytes of one stage (NM matrices)
     __host__ __device__ DecGeom(int K, int NM) {
         const int rb = K / 2;
         rs = rb + ((64 - (rb & 127)) & 127);
         scb = (16 * (K / 32) + 15) & ~15;
-        stage = (NM * (16 * rs + scb) + 127) & ~127;
+        bias = NM * (16 * rs + scb);
+        stage = (bias + NM * 64 + 127) & ~127;
     }
 };
 
-// PATH: 0 = fp16 conversion, 1 = bf16 (exponents <= 128), 2 = bf16 (any exponent)
-template <bool GATEUP, int NT, int PATH>
+// One warp-iteration covers 16 rows x 4 blocks of 32 (per thread: block 4q+t4
+// of rows g and g+8).  If every exponent of the iteration admits the exact
+// fp16 conversion (warp vote) the fp16 path runs on the prefetched fp16
+// activations; otherwise the bf16 path runs on bf16 activations loaded for
+// this iteration.
+template <bool GATEUP, int NT>
 __device__ __forceinline__ void decode_mainloop(int K, const unsigned char *st, const DecGeom &geo,
-                                                const uint16_t *const (&brow)[NT], float acc[2][NT][4]) {
+                                                const uint16_t *const (&brow16)[NT],
+                                                const uint16_t *const (&browbf)[NT], float acc[2][NT][4]) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t4 = lane & 3;
     const int nb = K / 32, nq = (nb + 3) / 4;
     constexpr int NM = GATEUP ? 2 : 1;
     const unsigned char *codes = st;                    // [NM][16][rs]
     const uint8_t *sc = st + NM * 16 * geo.rs;          // [NM][scb]
-    auto load_b = [&](uint4 (&B)[NT][4], int q) {
+    auto load_b = [&](uint4 (&B)[NT][4], const uint16_t *const (&brow)[NT], int q) {
         const int b = 4 * q + t4;
         const bool valid = q < nq && b < nb;
 #pragma unroll
@@ -211,14 +218,15 @@ __device__ __forceinline__ void decode_mainloop(int K, const unsigned char *st, 
                                             : make_uint4(0, 0, 0, 0);
     };
     uint4 B[NT][4];
-    load_b(B, warp);
+    load_b(B, brow16, warp);
     for (int q = warp; q < nq; q += kDecWarps) {
         const int b = 4 * q + t4;
         const bool valid = b < nb;
         uint4 Bn[NT][4];
-        load_b(Bn, q + kDecWarps);
+        load_b(Bn, brow16, q + kDecWarps);
         uint4 A[2][2];
-        uint32_t s1[2][2], s2[2][2];
+        uint32_t sv[2][2];
+        bool f16ok = true;
 #pragma unroll
         for (int m = 0; m < NM; m++)
 #pragma unroll
@@ -226,40 +234,44 @@ __device__ __forceinline__ void decode_mainloop(int K, const unsigned char *st, 
                 const int r = g + 8 * h;
                 A[m][h] = valid ? *reinterpret_cast<const uint4 *>(codes + (m * 16 + r) * geo.rs + 16 * b)
                                 : make_uint4(0, 0, 0, 0);
-                const uint32_t s = valid ? sc[m * geo.scb + r * nb + b] : 127u;
-                if (PATH == 0) {
-                    s1[m][h] = scale_f16x2(s);
-                    s2[m][h] = 0;
-                } else {
-                    s1[m][h] = scale_lo(s);
-                    s2[m][h] = scale_hi(s);
-                }
+                sv[m][h] = valid ? sc[m * geo.scb + r * nb + b] : 127u;
+                f16ok = f16ok && f16_exact_scale(sv[m][h]);
             }
+        if (__all_sync(0xffffffffu, f16ok)) {
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
+            for (int k = 0; k < 4; k++) {
 #pragma unroll
-            for (int m = 0; m < NM; m++) {
-                uint32_t p0[4], p1[4];
-                if (PATH == 0) {
+                for (int m = 0; m < NM; m++) {
+                    uint32_t p0[4], p1[4];
                     e2m1x8_to_f16((&A[m][0].x)[k], p0);
                     e2m1x8_to_f16((&A[m][1].x)[k], p1);
+                    const uint32_t s0 = scale_f16x2(sv[m][0]), s1 = scale_f16x2(sv[m][1]);
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
-                        p0[i] = hmul2_f16(p0[i], s1[m][0]);
-                        p1[i] = hmul2_f16(p1[i], s1[m][1]);
+                        p0[i] = hmul2_f16(p0[i], s0);
+                        p1[i] = hmul2_f16(p1[i], s1);
                     }
-                } else {
-                    dequant_word_nat<PATH == 2>((&A[m][0].x)[k], s1[m][0], s2[m][0], p0);
-                    dequant_word_nat<PATH == 2>((&A[m][1].x)[k], s1[m][1], s2[m][1], p1);
-                }
 #pragma unroll
-                for (int n = 0; n < NT; n++) {
-                    if (PATH == 0) {
+                    for (int n = 0; n < NT; n++) {
                         mma_f16_16816(acc[m][n], p0[0], p1[0], p0[1], p1[1], B[n][k].x, B[n][k].y);
                         mma_f16_16816(acc[m][n], p0[2], p1[2], p0[3], p1[3], B[n][k].z, B[n][k].w);
-                    } else {
-                        mma_bf16_16816(acc[m][n], p0[0], p1[0], p0[1], p1[1], B[n][k].x, B[n][k].y);
-                        mma_bf16_16816(acc[m][n], p0[2], p1[2], p0[3], p1[3], B[n][k].z, B[n][k].w);
+                    }
+                }
+            }
+        } else {
+            uint4 Bb[NT][4];
+            load_b(Bb, browbf, q);
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+#pragma unroll
+                for (int m = 0; m < NM; m++) {
+                    uint32_t p0[4], p1[4];
+                    dequant_word_nat<true>((&A[m][0].x)[k], scale_lo(sv[m][0]), scale_hi(sv[m][0]), p0);
+                    dequant_word_nat<true>((&A[m][1].x)[k], scale_lo(sv[m][1]), scale_hi(sv[m][1]), p1);
+#pragma unroll
+                    for (int n = 0; n < NT; n++) {
+                        mma_bf16_16816(acc[m][n], p0[0], p1[0], p0[1], p1[1], Bb[n][k].x, Bb[n][k].y);
+                        mma_bf16_16816(acc[m][n], p0[2], p1[2], p0[3], p1[3], Bb[n][k].z, Bb[n][k].w);
                     }
                 }
             }
@@ -289,29 +301,42 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) moe_decode_kernel(DecodeArg
     const int E = a.bp.E;
     int32_t *status = a.ws.status;
 
-    // producer (thread 0): all rows and scales of one item into stage s
+    // producer (warp 0): rows, scales and biases of one item into stage s;
+    // lane r < 16 copies row r of each matrix, lane 16 + m the scales and biases of matrix m
     auto issue = [&](int item, int s) {
         const int4 tile = a.ws.tiles[item / RB];
         const int e = tile.x, j0 = (item % RB) * 16;
         unsigned char *st = dsm + s * geo.stage;
-        const uint32_t bytes = NM * 16 * (K / 2) + NM * 16 * nb;
-        asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(
-                         smem_addr(&full[s])),
-                     "r"(bytes)
-                     : "memory");
+        if (lane == 0) {
+            const uint32_t bytes = NM * (16 * (K / 2) + 16 * nb + 64);
+            asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(
+                             smem_addr(&full[s])),
+                         "r"(bytes)
+                         : "memory");
+        }
+        __syncwarp();
 #pragma unroll
         for (int m = 0; m < NM; m++) {
             const MatPtrs &M = m == 0 ? a.A0 : a.A1;
-            const uint8_t *src = mat_codes(M, e, E) + (size_t)j0 * (K / 2);
-            for (int r = 0; r < 16; r++) bulk_g2s(st + (m * 16 + r) * geo.rs, src + (size_t)r * (K / 2), K / 2, &full[s]);
-            bulk_g2s(st + NM * 16 * geo.rs + m * geo.scb, mat_scales(M, e, E) + (size_t)j0 * nb, 16 * nb, &full[s]);
+            if (lane < 16)
+                bulk_g2s(st + (m * 16 + lane) * geo.rs, mat_codes(M, e, E) + (size_t)(j0 + lane) * (K / 2), K / 2,
+                         &full[s]);
+            if (lane == 16 + m) {
+                bulk_g2s(st + NM * 16 * geo.rs + m * geo.scb, mat_scales(M, e, E) + (size_t)j0 * nb, 16 * nb, &full[s]);
+                bulk_g2s(st + geo.bias + m * 64, mat_bias(M, e, E) + j0, 64, &full[s]);
+            }
         }
     };
+    asm volatile("griddepcontrol.launch_dependents;");
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[0])));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[1])));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    // the tile table, activations and (for down) h come from the previous kernels
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __syncwarp();
+    if (warp == 0) {
         issue(begin, 0);
         if (n > 1) issue(begin + 1, 1);
     }
@@ -325,38 +350,30 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) moe_decode_kernel(DecodeArg
             cur_tile = item / RB;
             tile = a.ws.tiles[cur_tile];
         }
-        const int e = tile.x, rstart = tile.y, rcount = tile.z;
+        const int rstart = tile.y, rcount = tile.z;
         const int j0 = (item % RB) * 16;
         const bool ok = dec_mbar_wait(&full[s], (k >> 1) & 1, status, 50);
         const unsigned char *st = dsm + s * geo.stage;
-        // dequantisation path of this item
-        int not_f16 = 0, big = 0;
-        if (ok) {
-            const uint8_t *sc = st + NM * 16 * geo.rs;
-            for (int i = tid; i < NM * 16 * nb; i += kDecWarps * 32) {
-                const int m = i / (16 * nb), rem = i - m * 16 * nb;
-                const uint32_t v = sc[m * geo.scb + rem];
-                not_f16 |= !f16_exact_scale(v);
-                big |= (v > 128u);
-            }
-        }
-        not_f16 = __syncthreads_or(not_f16);
-        big = __syncthreads_or(big);
-        const int path = not_f16 ? (big ? 2 : 1) : 0;
-        const uint16_t *brow[NT];
+        const uint16_t *brow16[NT], *browbf[NT];
 #pragma unroll
         for (int nn = 0; nn < NT; nn++) {
             const int col = nn * 8 + g;
-            brow[nn] = nullptr;
+            brow16[nn] = browbf[nn] = nullptr;
             if (col < rcount) {
                 if (GATEUP) {
                     const size_t tok = (size_t)a.ws.perm_token[rstart + col];
-                    brow[nn] = (path == 0 ? a.ws.xhat16 : a.ws.xhat) + tok * K;
+                    brow16[nn] = a.ws.xhat16 + tok * K;
+                    browbf[nn] = a.ws.xhat + tok * K;
                 } else {
-                    brow[nn] = (path == 0 ? a.ws.h16 : a.ws.h) + (size_t)(rstart + col) * K;
+                    brow16[nn] = a.ws.h16 + (size_t)(rstart + col) * K;
+                    browbf[nn] = a.ws.h + (size_t)(rstart + col) * K;
                 }
             }
         }
+        // biases of this thread's epilogue row, read before the stage is released
+        const float *sb = reinterpret_cast<const float *>(st + geo.bias);
+        const float bias0 = ok ? sb[tid & 15] : 0.f;
+        const float bias1 = (ok && GATEUP) ? sb[16 + (tid & 15)] : 0.f;
         float acc[2][NT][4];
 #pragma unroll
         for (int m = 0; m < 2; m++)
@@ -364,14 +381,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) moe_decode_kernel(DecodeArg
             for (int nn = 0; nn < NT; nn++)
 #pragma unroll
                 for (int r = 0; r < 4; r++) acc[m][nn][r] = 0.f;
-        if (ok) {
-            if (path == 0)
-                decode_mainloop<GATEUP, NT, 0>(K, st, geo, brow, acc);
-            else if (path == 1)
-                decode_mainloop<GATEUP, NT, 1>(K, st, geo, brow, acc);
-            else
-                decode_mainloop<GATEUP, NT, 2>(K, st, geo, brow, acc);
-        }
+        if (ok) decode_mainloop<GATEUP, NT>(K, st, geo, brow16, browbf, acc);
 #pragma unroll
         for (int m = 0; m < NM; m++)
 #pragma unroll
@@ -383,7 +393,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) moe_decode_kernel(DecodeArg
                 r[g + 8][2 * t4 + 1] = acc[m][nn][3];
             }
         __syncthreads();  // stage s fully read; partials visible
-        if (tid == 0 && k + 2 < n) {
+        if (warp == 0 && k + 2 < n) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(item + 2, s);
         }
@@ -403,15 +413,15 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) moe_decode_kernel(DecodeArg
                 const int j = j0 + row;
                 const int route = rstart + col;
                 if (GATEUP) {
-                    const float gg = sm[0] + mat_bias(a.A0, e, E)[j];
-                    const float uu = sm[1] + mat_bias(a.A1, e, E)[j];
+                    const float gg = sm[0] + bias0;
+                    const float uu = sm[1] + bias1;
                     const float hv = swiglu_clamped(gg, uu, a.bp.alpha, a.bp.limit);
                     const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
                     const __half h16 = __float2half_rn(__bfloat162float(hb));  // exact for |h| >= 2^-14
                     a.ws.h[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&hb);
                     a.ws.h16[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&h16);
                 } else {
-                    const float yv = sm[0] + mat_bias(a.A0, e, E)[j];
+                    const float yv = sm[0] + bias0;
                     a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * yv;
                 }
             }
@@ -424,6 +434,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) moe_decode_kernel(DecodeArg
 // out[t] = x[t] + Σ_slot y[loc[t][slot]] (slot order; the shared expert last)
 __global__ void __launch_bounds__(256) moe_combine_kernel(BlockParams bp, Workspace ws, const uint16_t *x,
                                                           float *out, int T) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int t = blockIdx.y;
     const int KK = bp.K + bp.n_shared;
     const int H = bp.H;
@@ -511,8 +522,7 @@ static cudaError_t launch_one(const DecodeArgs &a, int n_items_max, cudaStream_t
     int grid = n_sm * per_sm;
     if (grid > n_items_max) grid = n_items_max;
     if (grid < 1) grid = 1;
-    moe_decode_kernel<GATEUP, NT><<<grid, kDecWarps * 32, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(moe_decode_kernel<GATEUP, NT>, dim3(grid), dim3(kDecWarps * 32), smem, st, a);
 }
 
 cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0, const MatPtrs &a1,
@@ -534,8 +544,7 @@ cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, cons
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T, float *out,
                            cudaStream_t st) {
     dim3 grid((bp.H / 4 + 255) / 256, T);
-    moe_combine_kernel<<<grid, 256, 0, st>>>(bp, ws, x, out, T);
-    return cudaGetLastError();
+    return launch_pdl(moe_combine_kernel, grid, dim3(256), 0, st, bp, ws, x, out, T);
 }
 
 cudaError_t launch_dequant(const MatPtrs &m, int expert, int n_experts, float *out, cudaStream_t st) {
