@@ -283,76 +283,94 @@ __device__ __forceinline__ void decode_mainloop(int K, const unsigned char *st, 
     }
 }
 
+__device__ __forceinline__ void dec_arrive(uint64_t *b) {
+    asm volatile("{ .reg .b64 t; mbarrier.arrive.shared::cta.b64 t, [%0]; }" ::"r"(smem_addr(b)) : "memory");
+}
+
+// Warp roles: warps 0..7 consume (split-K over the item's 16 rows), warp 8
+// produces (bulk copies).  mbarriers: full[s] (codes landed), empty[s] (8
+// consumer warps done with stage s), redfull[r] (8 partials written),
+// redempty[r] (epilogue done with reduction buffer r).  The epilogue of item
+// k runs on consumer warp k % 8; no CTA-wide barrier is used in the loop.
 template <bool GATEUP, int NT>
-__global__ void __launch_bounds__(kDecWarps * 32, 2) moe_decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__((kDecWarps + 1) * 32, 2) moe_decode_kernel(DecodeArgs a) {
     constexpr int NM = GATEUP ? 2 : 1;
     extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ __align__(16) float red[kDecWarps][NM][NT][16][8];  // split-K partials
-    __shared__ __align__(8) uint64_t full[2];
+    __shared__ __align__(16) float red[2][kDecWarps][NM][NT][16][8];  // split-K partials, double-buffered
+    __shared__ __align__(8) uint64_t bars[8];
+    uint64_t *full = bars, *empty = bars + 2, *redfull = bars + 4, *redempty = bars + 6;
     const int K = a.Kdim, nb = K / 32;
     const DecGeom geo(K, NM);
     const int RB = a.rows / 16;
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; i++) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty[i])), "r"(kDecWarps));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&redfull[i])), "r"(kDecWarps));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&redempty[i])));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // the tile table, activations and (for down) h come from the previous kernels
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_items = *a.ws.n_tiles * RB;
     const int per = (n_items + gridDim.x - 1) / gridDim.x;
     const int begin = blockIdx.x * per, end = min(n_items, begin + per);
     const int n = end - begin;
-    if (n <= 0) return;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
     const int E = a.bp.E;
     int32_t *status = a.ws.status;
 
-    // producer (warp 0): rows, scales and biases of one item into stage s;
-    // lane r < 16 copies row r of each matrix, lane 16 + m the scales and biases of matrix m
-    auto issue = [&](int item, int s) {
-        const int4 tile = a.ws.tiles[item / RB];
-        const int e = tile.x, j0 = (item % RB) * 16;
-        unsigned char *st = dsm + s * geo.stage;
-        if (lane == 0) {
-            const uint32_t bytes = NM * (16 * (K / 2) + 16 * nb + 64);
-            asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(
-                             smem_addr(&full[s])),
-                         "r"(bytes)
-                         : "memory");
-        }
-        __syncwarp();
-#pragma unroll
-        for (int m = 0; m < NM; m++) {
-            const MatPtrs &M = m == 0 ? a.A0 : a.A1;
-            if (lane < 16)
-                bulk_g2s(st + (m * 16 + lane) * geo.rs, mat_codes(M, e, E) + (size_t)(j0 + lane) * (K / 2), K / 2,
-                         &full[s]);
-            if (lane == 16 + m) {
-                bulk_g2s(st + NM * 16 * geo.rs + m * geo.scb, mat_scales(M, e, E) + (size_t)j0 * nb, 16 * nb, &full[s]);
-                bulk_g2s(st + geo.bias + m * 64, mat_bias(M, e, E) + j0, 64, &full[s]);
+    if (warp == kDecWarps) {
+        // ---------------------------------------------------------- producer
+        int issued = 0;
+        for (int k = 0; k < n; k++) {
+            const int s = k & 1, item = begin + k;
+            if (k >= 2 && !dec_mbar_wait(&empty[s], ((k >> 1) - 1) & 1, status, 51)) break;
+            const int4 tile = a.ws.tiles[item / RB];
+            const int e = tile.x, j0 = (item % RB) * 16;
+            unsigned char *st = dsm + s * geo.stage;
+            if (lane == 0) {
+                const uint32_t bytes = NM * (16 * (K / 2) + 16 * nb + 64);
+                asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(
+                                 smem_addr(&full[s])),
+                             "r"(bytes)
+                             : "memory");
             }
+            __syncwarp();
+#pragma unroll
+            for (int m = 0; m < NM; m++) {
+                const MatPtrs &M = m == 0 ? a.A0 : a.A1;
+                if (lane < 16)
+                    bulk_g2s(st + (m * 16 + lane) * geo.rs, mat_codes(M, e, E) + (size_t)(j0 + lane) * (K / 2), K / 2,
+                             &full[s]);
+                if (lane == 16 + m) {
+                    bulk_g2s(st + NM * 16 * geo.rs + m * geo.scb, mat_scales(M, e, E) + (size_t)j0 * nb, 16 * nb,
+                             &full[s]);
+                    bulk_g2s(st + geo.bias + m * 64, mat_bias(M, e, E) + j0, 64, &full[s]);
+                }
+            }
+            issued = k + 1;
         }
-    };
-    asm volatile("griddepcontrol.launch_dependents;");
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[0])));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[1])));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // the copies of the last two stages must have landed before this warp exits
+        for (int k = max(0, issued - 2); k < issued; k++) dec_mbar_wait(&full[k & 1], (k >> 1) & 1, status, 52);
+        return;
     }
-    // the tile table, activations and (for down) h come from the previous kernels
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    __syncwarp();
-    if (warp == 0) {
-        issue(begin, 0);
-        if (n > 1) issue(begin + 1, 1);
-    }
-    __syncthreads();
 
+    // -------------------------------------------------------------- consumers
     int cur_tile = -1;
     int4 tile = make_int4(0, 0, 0, 0);
     for (int k = 0; k < n; k++) {
-        const int item = begin + k, s = k & 1;
+        const int item = begin + k, s = k & 1, r = k & 1;
         if (item / RB != cur_tile) {
             cur_tile = item / RB;
             tile = a.ws.tiles[cur_tile];
         }
         const int rstart = tile.y, rcount = tile.z;
         const int j0 = (item % RB) * 16;
-        const bool ok = dec_mbar_wait(&full[s], (k >> 1) & 1, status, 50);
+        if (!dec_mbar_wait(&full[s], (k >> 1) & 1, status, 50)) break;
         const unsigned char *st = dsm + s * geo.stage;
         const uint16_t *brow16[NT], *browbf[NT];
 #pragma unroll
@@ -370,36 +388,42 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) moe_decode_kernel(DecodeArg
                 }
             }
         }
-        // biases of this thread's epilogue row, read before the stage is released
-        const float *sb = reinterpret_cast<const float *>(st + geo.bias);
-        const float bias0 = ok ? sb[tid & 15] : 0.f;
-        const float bias1 = (ok && GATEUP) ? sb[16 + (tid & 15)] : 0.f;
+        const bool epi = warp == (k % kDecWarps);
+        float b0 = 0.f, b1 = 0.f;  // biases of row lane & 15 (epilogue warp only), read before the stage is released
+        if (epi) {
+            const float *sb = reinterpret_cast<const float *>(st + geo.bias);
+            b0 = sb[lane & 15];
+            if (GATEUP) b1 = sb[16 + (lane & 15)];
+        }
         float acc[2][NT][4];
 #pragma unroll
         for (int m = 0; m < 2; m++)
 #pragma unroll
             for (int nn = 0; nn < NT; nn++)
 #pragma unroll
-                for (int r = 0; r < 4; r++) acc[m][nn][r] = 0.f;
-        if (ok) decode_mainloop<GATEUP, NT>(K, st, geo, brow16, browbf, acc);
+                for (int q = 0; q < 4; q++) acc[m][nn][q] = 0.f;
+        decode_mainloop<GATEUP, NT>(K, st, geo, brow16, browbf, acc);
+        __syncwarp();
+        if (lane == 0) dec_arrive(&empty[s]);  // this warp no longer reads stage s
+        if (k >= 2 && !dec_mbar_wait(&redempty[r], ((k >> 1) - 1) & 1, status, 53)) break;
 #pragma unroll
         for (int m = 0; m < NM; m++)
 #pragma unroll
             for (int nn = 0; nn < NT; nn++) {
-                float(*r)[8] = red[warp][m][nn];
-                r[g][2 * t4] = acc[m][nn][0];
-                r[g][2 * t4 + 1] = acc[m][nn][1];
-                r[g + 8][2 * t4] = acc[m][nn][2];
-                r[g + 8][2 * t4 + 1] = acc[m][nn][3];
+                float(*rp)[8] = red[r][warp][m][nn];
+                rp[g][2 * t4] = acc[m][nn][0];
+                rp[g][2 * t4 + 1] = acc[m][nn][1];
+                rp[g + 8][2 * t4] = acc[m][nn][2];
+                rp[g + 8][2 * t4 + 1] = acc[m][nn][3];
             }
-        __syncthreads();  // stage s fully read; partials visible
-        if (warp == 0 && k + 2 < n) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(item + 2, s);
-        }
-        if (ok) {
-            for (int idx = tid; idx < 16 * 8 * NT; idx += kDecWarps * 32) {
+        __syncwarp();
+        if (lane == 0) dec_arrive(&redfull[r]);
+        if (epi) {
+            if (!dec_mbar_wait(&redfull[r], (k >> 1) & 1, status, 54)) break;
+            for (int idx = lane; idx < 16 * 8 * NT; idx += 32) {
                 const int row = idx & 15, col = idx >> 4;  // col = route within the tile
+                const float bb0 = __shfl_sync(0xffffffffu, b0, row);
+                const float bb1 = __shfl_sync(0xffffffffu, b1, row);
                 if (col >= rcount) continue;
                 const int nn = col >> 3, c = col & 7;
                 float sm[NM];
@@ -407,28 +431,25 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) moe_decode_kernel(DecodeArg
                 for (int m = 0; m < NM; m++) {
                     float v = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kDecWarps; w++) v += red[w][m][nn][row][c];
+                    for (int w = 0; w < kDecWarps; w++) v += red[r][w][m][nn][row][c];
                     sm[m] = v;
                 }
                 const int j = j0 + row;
                 const int route = rstart + col;
                 if (GATEUP) {
-                    const float gg = sm[0] + bias0;
-                    const float uu = sm[1] + bias1;
-                    const float hv = swiglu_clamped(gg, uu, a.bp.alpha, a.bp.limit);
+                    const float hv = swiglu_clamped(sm[0] + bb0, sm[1] + bb1, a.bp.alpha, a.bp.limit);
                     const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
                     const __half h16 = __float2half_rn(__bfloat162float(hb));  // exact for |h| >= 2^-14
                     a.ws.h[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&hb);
                     a.ws.h16[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&h16);
                 } else {
-                    const float yv = sm[0] + bias0;
-                    a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * yv;
+                    a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * (sm[0] + bb0);
                 }
             }
+            __syncwarp();
+            if (lane == 0) dec_arrive(&redempty[r]);
         }
-        __syncthreads();  // red is reused by the next item
     }
-    // every issued copy was waited for above (or timed out and was reported)
 }
 
 // out[t] = x[t] + Σ_slot y[loc[t][slot]] (slot order; the shared expert last)
@@ -516,13 +537,13 @@ static cudaError_t launch_one(const DecodeArgs &a, int n_items_max, cudaStream_t
         MOE_CUDA_TRY(cudaGetDevice(&dev));
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
         MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_decode_kernel<GATEUP, NT>,
-                                                                   kDecWarps * 32, smem));
+                                                                   (kDecWarps + 1) * 32, smem));
         if (per_sm < 1) per_sm = 1;
     }
     int grid = n_sm * per_sm;
     if (grid > n_items_max) grid = n_items_max;
     if (grid < 1) grid = 1;
-    return launch_pdl(moe_decode_kernel<GATEUP, NT>, dim3(grid), dim3(kDecWarps * 32), smem, st, a);
+    return launch_pdl(moe_decode_kernel<GATEUP, NT>, dim3(grid), dim3((kDecWarps + 1) * 32), smem, st, a);
 }
 
 cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0, const MatPtrs &a1,

@@ -324,23 +324,28 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     }
 
     // -------------------------------------------------------------- router
-    // Products of two bf16 are exact in fp32.  Each 8-product chunk is summed
-    // first (7 roundings), chunk sums are accumulated per lane (per_lane
-    // roundings), then a 5-level butterfly and the bias: every partial sum is
-    // bounded by Σ|p|, so the error is <= gamma_n * (Σ|p| + |b| + |l|) with
-    // n = 7 + per_lane + 6; the stored bound is doubled as a safety margin.
-    const int chain = 7 + per_lane + 6;
+    // Products of two bf16 are exact in fp32 and enter the sums through FMA.
+    // Each 8-product chunk is summed first (8 roundings), chunk sums are
+    // accumulated per lane (per_lane roundings), then a 5-level butterfly and
+    // the bias: every partial sum is bounded by Σ|p|, so the error is
+    // <= gamma_n * (Σ|p| + |b| + |l|) with n = 8 + per_lane + 6; the stored
+    // bound is doubled as a safety margin.  The next expert's row is loaded
+    // while the current one is multiplied.
+    const int chain = 8 + per_lane + 6;
+    uint4 wnext[kMaxChunks];
     for (int k = 0; k < EPW; k++) {
         const int e = e0 + warp * EPW + k;
-        if (k > 0) {
-            const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)min(e, E - 1) * H);
+        if (e >= E) break;  // warp-uniform
+        const int en = e + 1;
+        const bool pre = (k + 1 < EPW) && en < E;
+        {
+            const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)min(en, E - 1) * H);
 #pragma unroll
             for (int c = 0; c < kMaxChunks; c++) {
                 const int ch = lane + 32 * c;
-                wreg[c] = (c < per_lane && ch < nchunk && e < E) ? __ldg(wr + ch) : make_uint4(0, 0, 0, 0);
+                wnext[c] = (pre && c < per_lane && ch < nchunk) ? __ldg(wr + ch) : make_uint4(0, 0, 0, 0);
             }
         }
-        if (e >= E) break;  // warp-uniform
         if (!a.router_exact) {
             float acc[G], sab[G];
 #pragma unroll
@@ -350,33 +355,39 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
                 const int ch = lane + 32 * c;
                 if (c < per_lane && ch < nchunk) {
                     const uint32_t ww[4] = {wreg[c].x, wreg[c].y, wreg[c].z, wreg[c].w};
+                    float wf[8];
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        wf[2 * q] = __uint_as_float(ww[q] << 16);
+                        wf[2 * q + 1] = __uint_as_float(ww[q] & 0xFFFF0000u);
+                    }
 #pragma unroll
                     for (int g = 0; g < G; g++) {
                         if (g < nt) {
                             const uint4 xv = *reinterpret_cast<const uint4 *>(xh + g * H + ch * 8);
                             const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
-                            float cs = 0.f;
+                            float cs = 0.f, ab = sab[g];
 #pragma unroll
                             for (int q = 0; q < 4; q++) {
-                                const float p0 = __uint_as_float(xx[q] << 16) * __uint_as_float(ww[q] << 16);
-                                const float p1 =
-                                    __uint_as_float(xx[q] & 0xFFFF0000u) * __uint_as_float(ww[q] & 0xFFFF0000u);
-                                cs += p0;
-                                cs += p1;
-                                sab[g] += fabsf(p0) + fabsf(p1);
+                                const float x0 = __uint_as_float(xx[q] << 16), x1 = __uint_as_float(xx[q] & 0xFFFF0000u);
+                                cs = fmaf(x0, wf[2 * q], cs);
+                                cs = fmaf(x1, wf[2 * q + 1], cs);
+                                ab = fmaf(fabsf(x0), fabsf(wf[2 * q]), ab);
+                                ab = fmaf(fabsf(x1), fabsf(wf[2 * q + 1]), ab);
                             }
                             acc[g] += cs;
+                            sab[g] = ab;
                         }
                     }
                 }
             }
 #pragma unroll
             for (int g = 0; g < G; g++) {
-                const float s = warp_sum_f(acc[g]);
+                const float sm = warp_sum_f(acc[g]);
                 const float ab = warp_sum_f(sab[g]);
                 if (lane == 0 && g < nt) {
                     const float b = a.router_b[e];
-                    const float l = s + b;
+                    const float l = sm + b;
                     a.ws.logits[(size_t)(t0 + g) * E + e] = l;
                     a.ws.lbound[(size_t)(t0 + g) * E + e] =
                         2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
@@ -391,6 +402,8 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
                 }
             }
         }
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; c++) wreg[c] = wnext[c];
     }
 
     // ------------------------------------- last CTA of the token group: top-k
@@ -603,405 +616,6 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     if (tid == 0) a.ws.tickets[0] = 0u;  // re-arm for the next launch
 }
 
-// ---------------------------------------------------------------------------
-// Small problems (decode: T <= 16, E <= 64, H <= 4096): one CTA of 16 warps
-// does the whole routing step, with __syncthreads between phases instead of
-// grid-wide tickets.  x and gamma are staged in shared memory by one bulk
-// asynchronous copy each; every warp prefetches its router row meanwhile.
-constexpr int kSmallThreads = 512;
-constexpr int kSmallWarps = 16;
-
-__device__ __forceinline__ uint32_t smem_u32r(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-
-// Top-k + softmax of one token by one warp (identical rules to the grid
-// kernel): fp32 selection certified by the error bounds, exact fp64
-// re-evaluation of the candidates when the bounds overlap.
-__device__ void topk_token_warp(const float *l, const float *bd, const uint16_t *xh, const RouteArgs &a, int t,
-                                int lane) {
-    const int E = a.bp.E, K = a.bp.K, H = a.bp.H;
-    const bool exact_mode = a.router_exact != 0;
-    int sel[MOE_MAX_TOPK + 1];
-    float selv[MOE_MAX_TOPK + 1];
-    float lv[2];
-    uint32_t taken = 0;
-    float dmax = 0.f;
-#pragma unroll
-    for (int q = 0; q < 2; q++) {
-        const int j = lane + 32 * q;
-        lv[q] = j < E ? l[j] : -INFINITY;
-        if (j < E) dmax = fmaxf(dmax, bd[j]);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
-    for (int r = 0; r <= K; r++) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int q = 0; q < 2; q++) {
-            const int j = lane + 32 * q;
-            const float v = lv[q];
-            if (j >= E || !(v > -INFINITY) || (taken >> q & 1u)) continue;
-            if (better(v, j, bv, bi)) {
-                bv = v;
-                bi = j;
-            }
-        }
-        warp_best(bv, bi);
-        sel[r] = bi;
-        selv[r] = bv;
-        if (bi != 0x7fffffff && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-    }
-    bool certain = !exact_mode;
-    if (certain) {
-        for (int r = 0; r < K; r++) {
-            if (sel[r] == 0x7fffffff) break;
-            const float nxt = (sel[r + 1] == 0x7fffffff) ? -INFINITY : selv[r + 1];
-            if (!(selv[r] - nxt > 2.0f * dmax)) certain = false;
-        }
-    }
-    double exactv[MOE_MAX_TOPK];
-    bool have_exact = false;
-    if (!certain) {
-        const float thr =
-            exact_mode ? -INFINITY : ((sel[K - 1] == 0x7fffffff) ? -INFINITY : selv[K - 1] - 2.0f * dmax);
-        double bv_all[MOE_MAX_TOPK];
-        int bi_all[MOE_MAX_TOPK];
-        for (int r = 0; r < K; r++) {
-            bv_all[r] = -INFINITY;
-            bi_all[r] = 0x7fffffff;
-        }
-        for (int j = 0; j < E; j++) {  // warp-uniform
-            const float v = l[j];
-            if (!(v > -INFINITY) || v < thr) continue;
-            const double ex = exact_logit(xh, a.router_w, a.router_b, j, H, lane);
-            if (!(ex > -INFINITY)) continue;
-            int pos = K;
-            for (int r = 0; r < K; r++)
-                if (better_d(ex, j, bv_all[r], bi_all[r])) {
-                    pos = r;
-                    break;
-                }
-            if (pos < K) {
-                for (int r = K - 1; r > pos; r--) {
-                    bv_all[r] = bv_all[r - 1];
-                    bi_all[r] = bi_all[r - 1];
-                }
-                bv_all[pos] = ex;
-                bi_all[pos] = j;
-            }
-        }
-        for (int r = 0; r < K; r++) {
-            sel[r] = bi_all[r];
-            exactv[r] = bv_all[r];
-            selv[r] = (float)bv_all[r];
-        }
-        have_exact = true;
-    }
-    if (lane == 0) {
-        float m = -INFINITY;
-        for (int r = 0; r < K; r++)
-            if (sel[r] != 0x7fffffff) m = fmaxf(m, selv[r]);
-        float ew[MOE_MAX_TOPK], s = 0.f;
-        for (int r = 0; r < K; r++) {
-            const float d = have_exact ? (float)(exactv[r] - (double)m) : (selv[r] - m);
-            ew[r] = (sel[r] == 0x7fffffff) ? 0.f : expf(d);
-            s += ew[r];
-        }
-        for (int r = 0; r < K; r++) {
-            const int id = (sel[r] == 0x7fffffff) ? 0 : sel[r];
-            const float w = (s > 0.f) ? a.bp.wscale * (ew[r] / s) : 0.f;
-            a.ws.ids[t * K + r] = id;
-            a.ws.route_w[t * K + r] = w;
-            if (a.ids_out) a.ids_out[t * K + r] = id;
-            if (a.rw_out) a.rw_out[t * K + r] = w;
-        }
-    }
-}
-
-__global__ void __launch_bounds__(kSmallThreads, 1) moe_route_small_kernel(RouteArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int H = a.bp.H, E = a.bp.E, K = a.bp.K, T = a.T;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);                  // [T][H] x, then x_hat in place
-    float *gs = reinterpret_cast<float *>(smem + (size_t)T * H * 2);     // [H] gamma
-    float *lg = gs + H;                                                   // [T][E] logits
-    float *lb = lg + T * E;                                               // [T][E] bounds
-    int *ires = reinterpret_cast<int *>(lb + T * E);                      // scratch ints
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ int s_ex[kSmallWarps];
-    __shared__ U128 s_acc[kSmallWarps];
-    __shared__ double s_r[16];
-
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32r(&bar)));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        const uint32_t xb = (uint32_t)T * H * 2, gb = (uint32_t)H * 4;
-        asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(smem_u32r(&bar)),
-                     "r"(xb + gb)
-                     : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                         smem_u32r(xs)),
-                     "l"(a.x), "r"(xb), "r"(smem_u32r(&bar))
-                     : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                         smem_u32r(gs)),
-                     "l"(a.gamma), "r"(gb), "r"(smem_u32r(&bar))
-                     : "memory");
-    }
-    // router row of this warp's first expert, in flight during the norm
-    const int nchunk = H / 8, per_lane = (nchunk + 31) / 32;
-    uint4 wreg[kMaxChunks];
-    auto load_row = [&](int e) {
-        const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)min(e, E - 1) * H);
-#pragma unroll
-        for (int c = 0; c < kMaxChunks; c++) {
-            const int ch = lane + 32 * c;
-            wreg[c] = (c < per_lane && ch < nchunk && e < E) ? __ldg(wr + ch) : make_uint4(0, 0, 0, 0);
-        }
-    };
-    load_row(warp);
-    __syncthreads();  // barrier initialised
-    {
-        // bounded wait for the staged x and gamma
-        uint32_t ok = 0;
-        uint64_t t0, t1;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-        for (;;) {
-            asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0; selp.u32 %0,1,0,p; }"
-                         : "=r"(ok)
-                         : "r"(smem_u32r(&bar))
-                         : "memory");
-            if (ok) break;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
-            if (t1 - t0 > 2000000000ull) {
-                set_device_error(a.ws.status, MOE_DEV_WAIT_TIMEOUT, 60);
-                return;  // nothing else was issued; every thread takes this path
-            }
-        }
-    }
-
-    // ---------------------------------------------------------------- norm
-    // token t is normalised by a group of tpg threads (contiguous warps)
-    int T2 = 1;
-    while (T2 < T) T2 <<= 1;
-    const int wpt = kSmallWarps / T2, tpg = wpt * 32;
-    const int tok = warp / wpt, gl = tid - tok * tpg;  // token of this thread, index in group
-    const bool active = tok < T;
-    int mx = 0;
-    if (active)
-        for (int c = gl; c < nchunk; c += tpg) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(xs + (size_t)tok * H + 8 * c);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 4; q++) mx = max(mx, (int)max((w4[q] >> 7) & 0xFFu, (w4[q] >> 23) & 0xFFu));
-        }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) s_ex[warp] = mx;
-    __syncthreads();
-    int emax = 1;
-    if (active)
-        for (int w = tok * wpt; w < (tok + 1) * wpt; w++) emax = max(emax, s_ex[w]);
-    U128 acc{0ull, 0ull};
-    if (active)
-        for (int c = gl; c < nchunk; c += tpg) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(xs + (size_t)tok * H + 8 * c);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const uint32_t b = (w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
-                const int ex = (b >> 7) & 0xFF;
-                const uint32_t M = ex ? (128u + (b & 0x7Fu)) : (b & 0x7Fu);
-                const int d = 2 * (emax - (ex ? ex : 1));
-                if (M == 0 || d > 80) continue;
-                const unsigned long long v64 = (unsigned long long)M * M;
-                const int sh = 80 - d;
-                U128 tt;
-                if (sh == 0) {
-                    tt.lo = v64;
-                    tt.hi = 0;
-                } else if (sh < 64) {
-                    tt.lo = v64 << sh;
-                    tt.hi = v64 >> (64 - sh);
-                } else {
-                    tt.lo = 0;
-                    tt.hi = v64 << (sh - 64);
-                }
-                u128_add(acc, tt);
-            }
-        }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) u128_add(acc, u128_shfl_xor(acc, o));
-    if (lane == 0) s_acc[warp] = acc;
-    __syncthreads();
-    if (active && gl == 0) {
-        U128 tot{0ull, 0ull};
-        for (int w = tok * wpt; w < (tok + 1) * wpt; w++) u128_add(tot, s_acc[w]);
-        double ss = 0.0;
-        if (tot.hi || tot.lo) {
-            const int lz = tot.hi ? __clzll((long long)tot.hi) : 64 + __clzll((long long)tot.lo);
-            const int width = 128 - lz;
-            unsigned long long top;
-            bool sticky;
-            int shift;
-            if (width > 64) {
-                shift = width - 64;
-                top = (tot.hi << (64 - shift)) | (tot.lo >> shift);
-                sticky = (tot.lo << (64 - shift)) != 0ull;
-            } else {
-                shift = width - 64;
-                top = (width == 64) ? tot.lo : (tot.lo << (-shift));
-                sticky = false;
-            }
-            unsigned long long mant = top >> 11;
-            const unsigned long long rem = top & 0x7FFull;
-            if (rem > 0x400ull || (rem == 0x400ull && (sticky || (mant & 1ull)))) mant += 1ull;
-            ss = ldexp((double)mant, 11 + shift + 2 * (emax - 134) - 80);
-        }
-        s_r[tok] = 1.0 / sqrt(ss / (double)H + a.bp.eps);
-    }
-    __syncthreads();
-    if (active) {
-        const double r = s_r[tok];
-        const float r32 = (float)r;
-        for (int c = gl; c < nchunk; c += tpg) {
-            uint16_t *px = xs + (size_t)tok * H + 8 * c;
-            const uint4 v = *reinterpret_cast<const uint4 *>(px);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            uint32_t hb[8];
-#pragma unroll
-            for (int q = 0; q < 8; q++)
-                hb[q] = norm_elem((w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, gs[8 * c + q], r32, r);
-            const uint4 nat = make_uint4(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16, hb[4] | hb[5] << 16,
-                                         hb[6] | hb[7] << 16);
-            const uint4 prm = make_uint4(hb[0] | hb[4] << 16, hb[1] | hb[5] << 16, hb[2] | hb[6] << 16,
-                                         hb[3] | hb[7] << 16);
-            uint32_t f[8];
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-                __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));
-                f[q] = *reinterpret_cast<uint16_t *>(&hh);
-            }
-            *reinterpret_cast<uint4 *>(px) = nat;  // x_hat in place of x
-            const size_t go = (size_t)tok * H + 8 * c;
-            *reinterpret_cast<uint4 *>(a.ws.xhat + go) = nat;
-            *reinterpret_cast<uint4 *>(a.ws.xhat_mma + go) = prm;
-            *reinterpret_cast<uint4 *>(a.ws.xhat16 + go) =
-                make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
-            if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + go) = nat;
-        }
-    }
-    __syncthreads();
-
-    // -------------------------------------------------------------- router
-    const int chain = 7 + per_lane + 6;
-    for (int e = warp; e < E; e += kSmallWarps) {
-        if (e != warp) load_row(e);
-        for (int t = 0; t < T; t++) {
-            float accf = 0.f, sab = 0.f;
-            if (!a.router_exact) {
-#pragma unroll
-                for (int c = 0; c < kMaxChunks; c++) {
-                    const int ch = lane + 32 * c;
-                    if (c < per_lane && ch < nchunk) {
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(xs + (size_t)t * H + 8 * ch);
-                        const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
-                        const uint32_t ww[4] = {wreg[c].x, wreg[c].y, wreg[c].z, wreg[c].w};
-                        float cs = 0.f;
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            const float p0 = __uint_as_float(xx[q] << 16) * __uint_as_float(ww[q] << 16);
-                            const float p1 = __uint_as_float(xx[q] & 0xFFFF0000u) * __uint_as_float(ww[q] & 0xFFFF0000u);
-                            cs += p0;
-                            cs += p1;
-                            sab += fabsf(p0) + fabsf(p1);
-                        }
-                        accf += cs;
-                    }
-                }
-                accf = warp_sum_f(accf);
-                sab = warp_sum_f(sab);
-                if (lane == 0) {
-                    const float b = a.router_b[e];
-                    const float l = accf + b;
-                    lg[t * E + e] = l;
-                    lb[t * E + e] = 2.0f * (float)chain * 0x1p-24f * (sab + fabsf(b) + fabsf(l)) + 1e-30f;
-                }
-            } else {
-                const double l = exact_logit(xs + (size_t)t * H, a.router_w, a.router_b, e, H, lane);
-                if (lane == 0) {
-                    lg[t * E + e] = (float)l;
-                    lb[t * E + e] = 0.f;
-                }
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---------------------------------------------------------- top-k + softmax
-    if (warp < T) topk_token_warp(lg + warp * E, lb + warp * E, xs + (size_t)warp * H, a, warp, lane);
-    __syncthreads();
-
-    // ------------------------------------------------------------ permutation (warp 0)
-    if (warp == 0) {
-        const int ns = a.bp.n_shared, EE = E + ns, KK = K + ns, R = T * K;
-        int *cnt = ires, *offs = ires + 72, *run = ires + 144, *tcnt = ires + 216, *toff = ires + 288;
-        for (int e = lane; e < EE; e += 32) {
-            cnt[e] = 0;
-            run[e] = 0;
-        }
-        __syncwarp();
-        for (int r = lane; r < R; r += 32) atomicAdd(&cnt[a.ws.ids[r]], 1);
-        __syncwarp();
-        if (ns && lane == 0) cnt[E] = T;
-        __syncwarp();
-        warp_exclusive_scan(cnt, offs, EE, lane);
-        for (int e = lane; e < EE; e += 32) tcnt[e] = (cnt[e] + a.tile_rows - 1) / a.tile_rows;
-        __syncwarp();
-        warp_exclusive_scan(tcnt, toff, EE, lane);
-        __syncwarp();
-        for (int e = lane; e < EE; e += 32) {
-            if (e < E) a.ws.counts[e] = cnt[e];
-            a.ws.offsets[e] = offs[e];
-            for (int k = 0; k < tcnt[e] && toff[e] + k < a.ws.max_tiles; k++) {
-                const int st = k * a.tile_rows;
-                a.ws.tiles[toff[e] + k] = make_int4(e, offs[e] + st, min(a.tile_rows, cnt[e] - st), 0);
-            }
-        }
-        if (lane == 0) {
-            a.ws.offsets[EE] = offs[EE];
-            *a.ws.n_tiles = min(toff[EE], a.ws.max_tiles);
-        }
-        const unsigned lt = (1u << lane) - 1u;
-        for (int base = 0; base < R; base += 32) {
-            const int r = base + lane;
-            const int e = r < R ? a.ws.ids[r] : -1;
-            const unsigned peers = __match_any_sync(0xffffffffu, e);
-            const int rk = __popc(peers & lt);
-            if (e >= 0) {
-                const int pos = offs[e] + run[e] + rk;
-                const int t = r / K, sl = r - t * K;
-                a.ws.perm_token[pos] = t;
-                a.ws.perm_slot[pos] = sl;
-                a.ws.perm_w[pos] = a.ws.route_w[r];
-                a.ws.loc[t * KK + sl] = pos;
-            }
-            __syncwarp();
-            if (e >= 0 && rk == 0) run[e] += __popc(peers);
-            __syncwarp();
-        }
-        if (ns) {
-            for (int t = lane; t < T; t += 32) {
-                const int pos = offs[E] + t;
-                a.ws.perm_token[pos] = t;
-                a.ws.perm_slot[pos] = K;
-                a.ws.perm_w[pos] = 1.0f;
-                a.ws.loc[t * KK + K] = pos;
-            }
-        }
-    }
-}
-
 size_t route_smem_bytes(int G, int H, int E) {
     const size_t a = (size_t)G * H * 2;
     const size_t b = (size_t)(5 * 264 + kRouteWarps * (E + 1)) * 4;
@@ -1018,19 +632,16 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
                          cudaStream_t st) {
     if (bp.H / 8 > 32 * kMaxChunks || bp.H / 8 > kRouteThreads * kXC) return cudaErrorInvalidValue;
     RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact};
-    static bool done1 = false, done8 = false, done_s = false;
-    const size_t small_smem = (size_t)T * bp.H * 2 + (size_t)bp.H * 4 + (size_t)T * bp.E * 8 + 360 * 4;
-    if (T <= 16 && bp.E + bp.n_shared <= 64 && small_smem <= 200 * 1024 && ((uintptr_t)x & 15) == 0) {
-        MOE_CUDA_TRY(smem_optin_once(moe_route_small_kernel, done_s));
-        moe_route_small_kernel<<<1, kSmallThreads, small_smem, st>>>(a);
-    } else if (T <= 32) {
-        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<1, 1>, done1));
-        dim3 grid(T, (bp.E + kRouteWarps - 1) / kRouteWarps);
-        moe_route_kernel<1, 1><<<grid, kRouteThreads, route_smem_bytes(1, bp.H, bp.E), st>>>(a);
+    static bool done1 = false, done8 = false;
+    if (T <= 32) {
+        // one token per CTA; 8 warps x 4 experts per CTA (all experts when E <= 32)
+        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<1, 4>, done1));
+        dim3 grid(T, (bp.E + 4 * kRouteWarps - 1) / (4 * kRouteWarps));
+        moe_route_kernel<1, 4><<<grid, kRouteThreads, route_smem_bytes(1, bp.H, bp.E), st>>>(a);
     } else {
-        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8, 8>, done8));
-        dim3 grid((T + 7) / 8, (bp.E + 8 * kRouteWarps - 1) / (8 * kRouteWarps));
-        moe_route_kernel<8, 8><<<grid, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
+        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8, 4>, done8));
+        dim3 grid((T + 7) / 8, (bp.E + 4 * kRouteWarps - 1) / (4 * kRouteWarps));
+        moe_route_kernel<8, 4><<<grid, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
     }
     return cudaGetLastError();
 }
