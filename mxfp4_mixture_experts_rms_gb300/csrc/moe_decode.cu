@@ -133,7 +133,7 @@ __device__ __forceinline__ void mma_f16_16816(float d[4], uint32_t a0, uint32_t 
 // (tile, 16-row block).  The packed codes and E8M0 scales of an item (16 rows
 // of one or two matrices, contiguous rows in the canonical layout) are
 // streamed into a two-stage shared-memory ring by bulk asynchronous copies
-// (one per row, padded row stride for conflict-free fragment reads) while the
+// (one per row) while the
 // previous item is computed.  The 8 warps split K (32-element blocks in groups
 // of four per warp-iteration) and reduce through shared memory; each thread
 // prefetches the next iteration's activation fragments into registers.
@@ -179,13 +179,13 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 
 // Shared-memory geometry of one stage for reduction length K.
 struct DecGeom {
-    int rs;        // padded row stride of packed codes (bytes); rs/4 = 16 (mod 32) banks
+    int rs;        // row stride of packed codes (bytes)
     int scb;       // bytes of one matrix's 16 rows of scales, rounded to 16
     int bias;      // offset of the [NM][16] fp32 biases in a stage
     int stage;     // bytes of one stage (NM matrices)
     __host__ __device__ DecGeom(int K, int NM) {
         const int rb = K / 2;
-        rs = rb + ((64 - (rb & 127)) & 127);
+        rs = rb;  // unpadded: two stages + the reductions of two CTAs fit one SM
         scb = (16 * (K / 32) + 15) & ~15;
         bias = NM * (16 * rs + scb);
         stage = (bias + NM * 64 + 127) & ~127;

@@ -28,6 +28,11 @@
 // selection is redone on them.
 #include "moe_common.cuh"
 
+// Phase marker (no-op unless an instrumented build defines it).
+#ifndef MOE_PHASE_MARK
+#define MOE_PHASE_MARK(i)
+#endif
+
 namespace {
 
 constexpr int kRouteThreads = 256;
@@ -257,6 +262,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
         }
     }
 
+    MOE_PHASE_MARK(0);
     // ---------------------------------------------------------------- norm
     // x and gamma are read as 16-byte chunks held in registers: one round trip
     // per row, issued ahead of use.
@@ -283,8 +289,10 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
         const int t = t0 + g;
         if (g + 1 < nt) load_row(t + 1, xnext);
         const double ss = sumsq_exact(xv, lane, warp, s_maxexp, s_acc);
+        MOE_PHASE_MARK(1);
         if (tid == 0) s_r = 1.0 / sqrt(ss / (double)H + a.bp.eps);
         __syncthreads();
+        MOE_PHASE_MARK(2);
         const double r = s_r;
         const float r32 = (float)r;
 #pragma unroll
@@ -323,6 +331,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
         __syncthreads();
     }
 
+    MOE_PHASE_MARK(3);
     // -------------------------------------------------------------- router
     // Products of two bf16 are exact in fp32 and enter the sums through FMA.
     // Each 8-product chunk is summed first (8 roundings), chunk sums are
@@ -406,6 +415,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
         for (int c = 0; c < kMaxChunks; c++) wreg[c] = wnext[c];
     }
 
+    MOE_PHASE_MARK(4);
     // ------------------------------------- last CTA of the token group: top-k
     __threadfence();
     __syncthreads();
@@ -516,6 +526,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
         }
     }
     if (tid == 0) a.ws.tickets[1 + blockIdx.x] = 0u;  // re-arm the group ticket
+    MOE_PHASE_MARK(5);
 
     // --------------------------------------------- last CTA of the grid: permutation
     __threadfence();
@@ -524,6 +535,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     __syncthreads();
     if (!s_flag) return;
     __threadfence();
+    MOE_PHASE_MARK(6);
 
     const int ns = a.bp.n_shared;
     const int EE = E + ns;
@@ -614,6 +626,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
         }
     }
     if (tid == 0) a.ws.tickets[0] = 0u;  // re-arm for the next launch
+    MOE_PHASE_MARK(7);
 }
 
 size_t route_smem_bytes(int G, int H, int E) {
