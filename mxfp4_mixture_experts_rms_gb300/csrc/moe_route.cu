@@ -52,6 +52,9 @@ struct RouteArgs {
     uint16_t *xhat_out; // user copy, may be null
     int tile_rows;
     int router_exact;
+    int epc;                      // experts per CTA (router rows staged in shared memory)
+    const uint8_t *pf_codes[2];   // gate / up codes to prefetch into L2 for the selected experts
+    size_t pf_bytes;              // bytes of one expert's codes (0: no prefetch)
 };
 
 __device__ __forceinline__ double warp_sum_d(double v) {
@@ -63,6 +66,10 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 // (value, index) order of `top_experts`: larger value first, equal values by lower index.
@@ -233,32 +240,162 @@ __device__ __forceinline__ uint32_t norm_elem(uint32_t xb, float gf, float r32, 
     return bf16_from_double_rne((double)xf * r * (double)gf);
 }
 
-template <int G, int EPW>
+// Top-k + softmax of one token by one warp: fp32 selection certified by the
+// error bounds, exact fp64 re-evaluation of the candidates when the bounds of
+// consecutive selections overlap.  l / bd: the token's logits and bounds of
+// experts [e0, e0 + ne) -- here always the whole [0, E).
+__device__ void topk_token_warp(const float *l, const float *bd, bool global_src, const uint16_t *xh,
+                                const RouteArgs &a, int t, int lane) {
+    const int E = a.bp.E, K = a.bp.K, H = a.bp.H;
+    const bool exact_mode = a.router_exact != 0;
+    auto ld = [&](const float *p) { return global_src ? __ldcg(p) : *p; };
+    int sel[MOE_MAX_TOPK + 1];
+    float selv[MOE_MAX_TOPK + 1];
+    float lv[MOE_MAX_EXPERTS / 32];
+    uint32_t taken = 0;
+    float dmax = 0.f;
+#pragma unroll
+    for (int q = 0; q < MOE_MAX_EXPERTS / 32; q++) {
+        const int j = lane + 32 * q;
+        lv[q] = j < E ? ld(l + j) : -INFINITY;
+        if (j < E) dmax = fmaxf(dmax, ld(bd + j));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
+    for (int r = 0; r <= K; r++) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int q = 0; q < MOE_MAX_EXPERTS / 32; q++) {
+            const int j = lane + 32 * q;
+            const float v = lv[q];
+            if (j >= E || !(v > -INFINITY) || (taken >> q & 1u)) continue;  // NaN / -inf never chosen
+            if (better(v, j, bv, bi)) {
+                bv = v;
+                bi = j;
+            }
+        }
+        warp_best(bv, bi);
+        sel[r] = bi;
+        selv[r] = bv;
+        if (bi != 0x7fffffff && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+    }
+    bool certain = !exact_mode;
+    if (certain) {
+        for (int r = 0; r < K; r++) {
+            if (sel[r] == 0x7fffffff) break;
+            const float nxt = (sel[r + 1] == 0x7fffffff) ? -INFINITY : selv[r + 1];
+            if (!(selv[r] - nxt > 2.0f * dmax)) certain = false;
+        }
+    }
+    double exactv[MOE_MAX_TOPK];
+    bool have_exact = false;
+    if (!certain) {
+        const float thr =
+            exact_mode ? -INFINITY : ((sel[K - 1] == 0x7fffffff) ? -INFINITY : selv[K - 1] - 2.0f * dmax);
+        double bv_all[MOE_MAX_TOPK];
+        int bi_all[MOE_MAX_TOPK];
+        for (int r = 0; r < K; r++) {
+            bv_all[r] = -INFINITY;
+            bi_all[r] = 0x7fffffff;
+        }
+        for (int j = 0; j < E; j++) {  // warp-uniform
+            const float v = ld(l + j);
+            if (!(v > -INFINITY) || v < thr) continue;
+            const double ex = exact_logit(xh, a.router_w, a.router_b, j, H, lane);
+            if (!(ex > -INFINITY)) continue;
+            int pos = K;
+            for (int r = 0; r < K; r++)
+                if (better_d(ex, j, bv_all[r], bi_all[r])) {
+                    pos = r;
+                    break;
+                }
+            if (pos < K) {
+                for (int r = K - 1; r > pos; r--) {
+                    bv_all[r] = bv_all[r - 1];
+                    bi_all[r] = bi_all[r - 1];
+                }
+                bv_all[pos] = ex;
+                bi_all[pos] = j;
+            }
+        }
+        for (int r = 0; r < K; r++) {
+            sel[r] = bi_all[r];
+            exactv[r] = bv_all[r];
+            selv[r] = (float)bv_all[r];
+        }
+        have_exact = true;
+    }
+    // softmax over the selected raw logits (lane 0), times the weight scale
+    if (lane == 0) {
+        float m = -INFINITY;
+        for (int r = 0; r < K; r++)
+            if (sel[r] != 0x7fffffff) m = fmaxf(m, selv[r]);
+        float ew[MOE_MAX_TOPK], s = 0.f;
+        for (int r = 0; r < K; r++) {
+            const float d = have_exact ? (float)(exactv[r] - (double)m) : (selv[r] - m);
+            ew[r] = (sel[r] == 0x7fffffff) ? 0.f : expf(d);
+            s += ew[r];
+        }
+        for (int r = 0; r < K; r++) {
+            const int id = (sel[r] == 0x7fffffff) ? 0 : sel[r];  // unfilled slot: expert 0, weight 0
+            const float w = (s > 0.f) ? a.bp.wscale * (ew[r] / s) : 0.f;
+            a.ws.ids[t * K + r] = id;
+            a.ws.route_w[t * K + r] = w;
+            if (a.ids_out) a.ids_out[t * K + r] = id;
+            if (a.rw_out) a.rw_out[t * K + r] = w;
+        }
+    }
+    // start pulling the selected experts' gate/up weights into L2 for the expert kernel
+    if (a.pf_bytes && lane < K && sel[lane] != 0x7fffffff) {
+        const size_t e = (size_t)sel[lane];
+        for (int m = 0; m < 2; m++) {
+            const uint8_t *base = a.pf_codes[m] + e * a.pf_bytes;
+            for (size_t off = 0; off < a.pf_bytes; off += 65536) {
+                const uint32_t n = (uint32_t)min((size_t)65536, a.pf_bytes - off);
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(n) : "memory");
+            }
+        }
+    }
+}
+
+template <int G>
 __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     const int H = a.bp.H, E = a.bp.E, K = a.bp.K;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint16_t *xh = reinterpret_cast<uint16_t *>(smem);  // [G][H]
+    const int epc = a.epc;                                                        // experts per CTA
+    uint16_t *wsm = reinterpret_cast<uint16_t *>(smem);                           // [epc][H] router rows
+    uint16_t *xh = wsm + (size_t)epc * H;                                         // [G][H] x_hat
+    float *lg = reinterpret_cast<float *>(xh + (size_t)G * H);                    // [G][epc] logits
+    float *lb = lg + G * epc;                                                     // [G][epc] bounds
     __shared__ int s_maxexp[kRouteWarps];
     __shared__ U128 s_acc[kRouteWarps];
     __shared__ double s_r;
     __shared__ int s_flag;
+    __shared__ __align__(8) uint64_t wbar;
 
     const int t0 = blockIdx.x * G;
     const int nt = min(G, a.T - t0);
-    const int e0 = blockIdx.y * (kRouteWarps * EPW);
-    const int nchunk = H / 8;                 // 16-byte chunks per router row
-    const int per_lane = (nchunk + 31) / 32;  // <= kMaxChunks
+    const int e0 = blockIdx.y * epc, ne = min(epc, E - e0);
+    const int nchunk = H / 8;  // 16-byte chunks per row
 
-    // Prefetch this warp's first router row before the norm: one HBM round trip.
-    uint4 wreg[kMaxChunks];
-    {
-        const int e = e0 + warp * EPW;
-        const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)min(e, E - 1) * H);
-#pragma unroll
-        for (int c = 0; c < kMaxChunks; c++) {
-            const int ch = lane + 32 * c;
-            wreg[c] = (c < per_lane && ch < nchunk && e < E) ? __ldg(wr + ch) : make_uint4(0, 0, 0, 0);
+    // router rows of this CTA's experts: one contiguous range, bulk-copied during the norm
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const size_t bytes = (size_t)ne * H * 2;
+        asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(smem_u32(&wbar)),
+                     "r"((uint32_t)bytes)
+                     : "memory");
+        const unsigned char *src = reinterpret_cast<const unsigned char *>(a.router_w + (size_t)e0 * H);
+        for (size_t off = 0; off < bytes; off += 32768) {
+            const uint32_t n = (uint32_t)min((size_t)32768, bytes - off);
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(reinterpret_cast<unsigned char *>(wsm) + off)),
+                "l"(src + off), "r"(n), "r"(smem_u32(&wbar))
+                : "memory");
         }
     }
 
@@ -309,21 +446,21 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
                                          hb[6] | hb[7] << 16);
             *reinterpret_cast<uint4 *>(xh + g * H + 8 * c) = nat;
             if (store) {
-                // decode-MMA pair order inside each 8-element chunk: (e0,e4),(e1,e5),(e2,e6),(e3,e7)
+                // prefill pair order inside each 8-element chunk: (e0,e4),(e1,e5),(e2,e6),(e3,e7)
                 const uint4 prm = make_uint4(hb[0] | hb[4] << 16, hb[1] | hb[5] << 16, hb[2] | hb[6] << 16,
                                              hb[3] | hb[7] << 16);
-                *reinterpret_cast<uint4 *>(a.ws.xhat + (size_t)t * H + 8 * c) = nat;
-                *reinterpret_cast<uint4 *>(a.ws.xhat_mma + (size_t)t * H + 8 * c) = prm;
-                // fp16 copy (exact for |x_hat| >= 2^-14) for the fp16 tensor-core GEMV
                 uint32_t f[8];
 #pragma unroll
                 for (int q = 0; q < 8; q++) {
-                    __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));
+                    __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));  // exact for |x_hat| >= 2^-14
                     f[q] = *reinterpret_cast<uint16_t *>(&hh);
                 }
-                *reinterpret_cast<uint4 *>(a.ws.xhat16 + (size_t)t * H + 8 * c) =
+                const size_t go = (size_t)t * H + 8 * c;
+                *reinterpret_cast<uint4 *>(a.ws.xhat + go) = nat;
+                *reinterpret_cast<uint4 *>(a.ws.xhat_mma + go) = prm;
+                *reinterpret_cast<uint4 *>(a.ws.xhat16 + go) =
                     make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
-                if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + (size_t)t * H + 8 * c) = nat;
+                if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + go) = nat;
             }
         }
 #pragma unroll
@@ -338,55 +475,60 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     // accumulated per lane (per_lane roundings), then a 5-level butterfly and
     // the bias: every partial sum is bounded by Σ|p|, so the error is
     // <= gamma_n * (Σ|p| + |b| + |l|) with n = 8 + per_lane + 6; the stored
-    // bound is doubled as a safety margin.  The next expert's row is loaded
-    // while the current one is multiplied.
+    // bound is doubled as a safety margin.
+    const int per_lane = (nchunk + 31) / 32;
     const int chain = 8 + per_lane + 6;
-    uint4 wnext[kMaxChunks];
-    for (int k = 0; k < EPW; k++) {
-        const int e = e0 + warp * EPW + k;
-        if (e >= E) break;  // warp-uniform
-        const int en = e + 1;
-        const bool pre = (k + 1 < EPW) && en < E;
-        {
-            const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)min(en, E - 1) * H);
-#pragma unroll
-            for (int c = 0; c < kMaxChunks; c++) {
-                const int ch = lane + 32 * c;
-                wnext[c] = (pre && c < per_lane && ch < nchunk) ? __ldg(wr + ch) : make_uint4(0, 0, 0, 0);
+    {
+        uint32_t ok = 0;
+        uint64_t c0, c1;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c0));
+        for (;;) {
+            asm volatile(
+                "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0; selp.u32 %0, 1, 0, p; }"
+                : "=r"(ok)
+                : "r"(smem_u32(&wbar))
+                : "memory");
+            if (ok) break;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c1));
+            if (c1 - c0 > 2000000000ull) {
+                set_device_error(a.ws.status, MOE_DEV_WAIT_TIMEOUT, 70);
+                break;
             }
         }
+        if (!ok) return;  // copies are reported lost; nothing else depends on this CTA
+    }
+    for (int el = warp; el < ne; el += kRouteWarps) {
+        const int e = e0 + el;
+        const uint16_t *wrow = wsm + (size_t)el * H;
         if (!a.router_exact) {
             float acc[G], sab[G];
 #pragma unroll
             for (int g = 0; g < G; g++) acc[g] = sab[g] = 0.f;
+            for (int ch = lane; ch < nchunk; ch += 32) {
+                const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + 8 * ch);
+                const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+                float wf[8];
 #pragma unroll
-            for (int c = 0; c < kMaxChunks; c++) {
-                const int ch = lane + 32 * c;
-                if (c < per_lane && ch < nchunk) {
-                    const uint32_t ww[4] = {wreg[c].x, wreg[c].y, wreg[c].z, wreg[c].w};
-                    float wf[8];
+                for (int q = 0; q < 4; q++) {
+                    wf[2 * q] = __uint_as_float(ww[q] << 16);
+                    wf[2 * q + 1] = __uint_as_float(ww[q] & 0xFFFF0000u);
+                }
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        wf[2 * q] = __uint_as_float(ww[q] << 16);
-                        wf[2 * q + 1] = __uint_as_float(ww[q] & 0xFFFF0000u);
-                    }
+                for (int g = 0; g < G; g++) {
+                    if (g < nt) {
+                        const uint4 xq = *reinterpret_cast<const uint4 *>(xh + g * H + ch * 8);
+                        const uint32_t xx[4] = {xq.x, xq.y, xq.z, xq.w};
+                        float cs = 0.f, ab = sab[g];
 #pragma unroll
-                    for (int g = 0; g < G; g++) {
-                        if (g < nt) {
-                            const uint4 xv = *reinterpret_cast<const uint4 *>(xh + g * H + ch * 8);
-                            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
-                            float cs = 0.f, ab = sab[g];
-#pragma unroll
-                            for (int q = 0; q < 4; q++) {
-                                const float x0 = __uint_as_float(xx[q] << 16), x1 = __uint_as_float(xx[q] & 0xFFFF0000u);
-                                cs = fmaf(x0, wf[2 * q], cs);
-                                cs = fmaf(x1, wf[2 * q + 1], cs);
-                                ab = fmaf(fabsf(x0), fabsf(wf[2 * q]), ab);
-                                ab = fmaf(fabsf(x1), fabsf(wf[2 * q + 1]), ab);
-                            }
-                            acc[g] += cs;
-                            sab[g] = ab;
+                        for (int q = 0; q < 4; q++) {
+                            const float x0 = __uint_as_float(xx[q] << 16), x1 = __uint_as_float(xx[q] & 0xFFFF0000u);
+                            cs = fmaf(x0, wf[2 * q], cs);
+                            cs = fmaf(x1, wf[2 * q + 1], cs);
+                            ab = fmaf(fabsf(x0), fabsf(wf[2 * q]), ab);
+                            ab = fmaf(fabsf(x1), fabsf(wf[2 * q + 1]), ab);
                         }
+                        acc[g] += cs;
+                        sab[g] = ab;
                     }
                 }
             }
@@ -397,135 +539,45 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
                 if (lane == 0 && g < nt) {
                     const float b = a.router_b[e];
                     const float l = sm + b;
-                    a.ws.logits[(size_t)(t0 + g) * E + e] = l;
-                    a.ws.lbound[(size_t)(t0 + g) * E + e] =
-                        2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
+                    lg[g * epc + el] = l;
+                    lb[g * epc + el] = 2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
                 }
             }
         } else {
             for (int g = 0; g < nt; g++) {
                 const double l = exact_logit(xh + g * H, a.router_w, a.router_b, e, H, lane);
                 if (lane == 0) {
-                    a.ws.logits[(size_t)(t0 + g) * E + e] = (float)l;
-                    a.ws.lbound[(size_t)(t0 + g) * E + e] = 0.f;
+                    lg[g * epc + el] = (float)l;
+                    lb[g * epc + el] = 0.f;
                 }
             }
         }
-#pragma unroll
-        for (int c = 0; c < kMaxChunks; c++) wreg[c] = wnext[c];
     }
-
+    __syncthreads();
     MOE_PHASE_MARK(4);
-    // ------------------------------------- last CTA of the token group: top-k
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_flag = (atomicAdd(a.ws.tickets + 1 + blockIdx.x, 1u) == gridDim.y - 1);
-    __syncthreads();
-    if (!s_flag) return;
-    __threadfence();
-    for (int g = warp; g < nt; g += kRouteWarps) {
-        const int t = t0 + g;
-        const float *l = a.ws.logits + (size_t)t * E;
-        const float *bd = a.ws.lbound + (size_t)t * E;
-        const bool exact_mode = a.router_exact != 0;
-        int sel[MOE_MAX_TOPK + 1];
-        float selv[MOE_MAX_TOPK + 1];
-        float lv[MOE_MAX_EXPERTS / 32];
-        uint32_t taken = 0;
-        float dmax = 0.f;
-#pragma unroll
-        for (int q = 0; q < MOE_MAX_EXPERTS / 32; q++) {
-            const int j = lane + 32 * q;
-            lv[q] = j < E ? __ldcg(l + j) : -INFINITY;
-            if (j < E) dmax = fmaxf(dmax, __ldcg(bd + j));
+
+    // ---------------------------------------------------------- top-k + softmax
+    if (gridDim.y == 1) {
+        // this CTA holds every logit of its tokens
+        for (int g = warp; g < nt; g += kRouteWarps)
+            topk_token_warp(lg + g * epc, lb + g * epc, false, xh + g * H, a, t0 + g, lane);
+    } else {
+        for (int i = tid; i < nt * ne; i += kRouteThreads) {
+            const int g = i / ne, el = i - g * ne;
+            a.ws.logits[(size_t)(t0 + g) * E + e0 + el] = lg[g * epc + el];
+            a.ws.lbound[(size_t)(t0 + g) * E + e0 + el] = lb[g * epc + el];
         }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
-        for (int r = 0; r <= K; r++) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int q = 0; q < MOE_MAX_EXPERTS / 32; q++) {
-                const int j = lane + 32 * q;
-                const float v = lv[q];
-                if (j >= E || !(v > -INFINITY) || (taken >> q & 1u)) continue;  // NaN / -inf never chosen
-                if (better(v, j, bv, bi)) {
-                    bv = v;
-                    bi = j;
-                }
-            }
-            warp_best(bv, bi);
-            sel[r] = bi;
-            selv[r] = bv;
-            if (bi != 0x7fffffff && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-        }
-        bool certain = !exact_mode;
-        if (certain) {
-            for (int r = 0; r < K; r++) {
-                if (sel[r] == 0x7fffffff) break;
-                const float nxt = (sel[r + 1] == 0x7fffffff) ? -INFINITY : selv[r + 1];
-                if (!(selv[r] - nxt > 2.0f * dmax)) certain = false;
-            }
-        }
-        double exactv[MOE_MAX_TOPK];
-        bool have_exact = false;
-        if (!certain) {
-            const float thr =
-                exact_mode ? -INFINITY : ((sel[K - 1] == 0x7fffffff) ? -INFINITY : selv[K - 1] - 2.0f * dmax);
-            double bv_all[MOE_MAX_TOPK];
-            int bi_all[MOE_MAX_TOPK];
-            for (int r = 0; r < K; r++) {
-                bv_all[r] = -INFINITY;
-                bi_all[r] = 0x7fffffff;
-            }
-            for (int j = 0; j < E; j++) {  // warp-uniform
-                const float v = __ldcg(l + j);
-                if (!(v > -INFINITY) || v < thr) continue;
-                const double ex = exact_logit(xh + g * H, a.router_w, a.router_b, j, H, lane);
-                if (!(ex > -INFINITY)) continue;
-                int pos = K;
-                for (int r = 0; r < K; r++)
-                    if (better_d(ex, j, bv_all[r], bi_all[r])) {
-                        pos = r;
-                        break;
-                    }
-                if (pos < K) {
-                    for (int r = K - 1; r > pos; r--) {
-                        bv_all[r] = bv_all[r - 1];
-                        bi_all[r] = bi_all[r - 1];
-                    }
-                    bv_all[pos] = ex;
-                    bi_all[pos] = j;
-                }
-            }
-            for (int r = 0; r < K; r++) {
-                sel[r] = bi_all[r];
-                exactv[r] = bv_all[r];
-                selv[r] = (float)bv_all[r];
-            }
-            have_exact = true;
-        }
-        if (lane == 0) {
-            float m = -INFINITY;
-            for (int r = 0; r < K; r++)
-                if (sel[r] != 0x7fffffff) m = fmaxf(m, selv[r]);
-            float ew[MOE_MAX_TOPK], s = 0.f;
-            for (int r = 0; r < K; r++) {
-                const float d = have_exact ? (float)(exactv[r] - (double)m) : (selv[r] - m);
-                ew[r] = (sel[r] == 0x7fffffff) ? 0.f : expf(d);
-                s += ew[r];
-            }
-            for (int r = 0; r < K; r++) {
-                const int id = (sel[r] == 0x7fffffff) ? 0 : sel[r];  // unfilled slot: expert 0, weight 0
-                const float w = (s > 0.f) ? a.bp.wscale * (ew[r] / s) : 0.f;
-                a.ws.ids[t * K + r] = id;
-                a.ws.route_w[t * K + r] = w;
-                if (a.ids_out) a.ids_out[t * K + r] = id;
-                if (a.rw_out) a.rw_out[t * K + r] = w;
-            }
-        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_flag = (atomicAdd(a.ws.tickets + 1 + blockIdx.x, 1u) == gridDim.y - 1);
+        __syncthreads();
+        if (!s_flag) return;
+        __threadfence();
+        for (int g = warp; g < nt; g += kRouteWarps)
+            topk_token_warp(a.ws.logits + (size_t)(t0 + g) * E, a.ws.lbound + (size_t)(t0 + g) * E, true,
+                            xh + g * H, a, t0 + g, lane);
+        if (tid == 0) a.ws.tickets[1 + blockIdx.x] = 0u;  // re-arm the group ticket
     }
-    if (tid == 0) a.ws.tickets[1 + blockIdx.x] = 0u;  // re-arm the group ticket
     MOE_PHASE_MARK(5);
 
     // --------------------------------------------- last CTA of the grid: permutation
@@ -541,7 +593,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     const int EE = E + ns;
     const int KK = K + ns;
     const int R = a.T * K;
-    int32_t *cnt = reinterpret_cast<int32_t *>(smem);  // reuses the x_hat area
+    int32_t *cnt = reinterpret_cast<int32_t *>(smem);  // reuses the router-row area
     int32_t *offs = cnt + 264;
     int32_t *run = offs + 264;
     int32_t *tcnt = run + 264;
@@ -629,8 +681,19 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
     MOE_PHASE_MARK(7);
 }
 
+// Experts per CTA so that their router rows plus G x_hat rows fit in shared memory.
+int route_epc(int G, int H, int E) {
+    const size_t budget = 200 * 1024;
+    const size_t xbytes = (size_t)G * H * 2;
+    int epc = (int)((budget - xbytes) / ((size_t)H * 2 + 8 * G));
+    if (epc > E) epc = E;
+    if (epc < 1) epc = 1;
+    return epc;
+}
+
 size_t route_smem_bytes(int G, int H, int E) {
-    const size_t a = (size_t)G * H * 2;
+    const int epc = route_epc(G, H, E);
+    const size_t a = (size_t)epc * H * 2 + (size_t)G * H * 2 + (size_t)G * epc * 8;
     const size_t b = (size_t)(5 * 264 + kRouteWarps * (E + 1)) * 4;
     return a > b ? a : b;
 }
@@ -641,20 +704,22 @@ int route_ticket_count(int T) { return T + 1; }
 
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x, const float *gamma,
                          const uint16_t *router_w, const float *router_b, int T, int32_t *ids_out, float *rw_out,
-                         uint16_t *xhat_out, int tile_rows, int router_exact, int /*write_mma_layout*/,
-                         cudaStream_t st) {
-    if (bp.H / 8 > 32 * kMaxChunks || bp.H / 8 > kRouteThreads * kXC) return cudaErrorInvalidValue;
-    RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact};
+                         uint16_t *xhat_out, int tile_rows, int router_exact, const uint8_t *pf_gate,
+                         const uint8_t *pf_up, size_t pf_bytes, cudaStream_t st) {
+    if (bp.H / 8 > kRouteThreads * kXC) return cudaErrorInvalidValue;
     static bool done1 = false, done8 = false;
     if (T <= 32) {
-        // one token per CTA; 8 warps x 4 experts per CTA (all experts when E <= 32)
-        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<1, 4>, done1));
-        dim3 grid(T, (bp.E + 4 * kRouteWarps - 1) / (4 * kRouteWarps));
-        moe_route_kernel<1, 4><<<grid, kRouteThreads, route_smem_bytes(1, bp.H, bp.E), st>>>(a);
+        RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact,
+                    route_epc(1, bp.H, bp.E), {pf_gate, pf_up}, pf_bytes};
+        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<1>, done1));
+        dim3 grid(T, (bp.E + a.epc - 1) / a.epc);
+        moe_route_kernel<1><<<grid, kRouteThreads, route_smem_bytes(1, bp.H, bp.E), st>>>(a);
     } else {
-        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8, 4>, done8));
-        dim3 grid((T + 7) / 8, (bp.E + 4 * kRouteWarps - 1) / (4 * kRouteWarps));
-        moe_route_kernel<8, 4><<<grid, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
+        RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact,
+                    route_epc(8, bp.H, bp.E), {nullptr, nullptr}, 0};
+        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8>, done8));
+        dim3 grid((T + 7) / 8, (bp.E + a.epc - 1) / a.epc);
+        moe_route_kernel<8><<<grid, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
     }
     return cudaGetLastError();
 }
