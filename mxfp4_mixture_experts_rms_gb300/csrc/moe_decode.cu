@@ -325,26 +325,10 @@ __global__ void __launch_bounds__((kDecWarps + 1) * 32, 2) moe_decode_kernel(Dec
 
     if (warp == kDecWarps) {
         // ---------------------------------------------------------- producer
-        // Besides the two-stage shared-memory ring, the codes of the items
-        // kPf ahead are requested into L2, so the HBM stream runs ahead of
-        // the ring without holding shared memory.
-        auto prefetch_l2 = [&](int item) {
-            const int4 tl = a.ws.tiles[item / RB];
-            const int j0p = (item % RB) * 16;
-            if (lane < NM) {
-                const MatPtrs &M = lane == 0 ? a.A0 : a.A1;
-                const uint8_t *src = mat_codes(M, tl.x, E) + (size_t)j0p * (K / 2);
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((uint32_t)(16 * (K / 2)))
-                             : "memory");
-            }
-        };
-        constexpr int kPf = 3;
-        for (int k = 2; k < min(n, 2 + kPf); k++) prefetch_l2(begin + k);
         int issued = 0;
         for (int k = 0; k < n; k++) {
             const int s = k & 1, item = begin + k;
             if (k >= 2 && !dec_mbar_wait(&empty[s], ((k >> 1) - 1) & 1, status, 51)) break;
-            if (k + 2 + kPf < n) prefetch_l2(begin + k + 2 + kPf);
             const int4 tile = a.ws.tiles[item / RB];
             const int e = tile.x, j0 = (item % RB) * 16;
             unsigned char *st = dsm + s * geo.stage;
