@@ -322,9 +322,8 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
         }
     };
     mark(0, true);
-    const size_t pf_bytes = 0;  // L2 prefetch of the selected experts from the routing kernel: off
     cudaError_t e = launch_route(b, p->ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, rw_out,
-                                 xhat_out, tile_rows, p->router_exact, p->gate.codes, p->up.codes, pf_bytes, st);
+                                 xhat_out, tile_rows, p->router_exact, st);
     mark(0, false);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     mark(1, true);

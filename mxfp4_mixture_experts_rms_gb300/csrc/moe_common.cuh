@@ -160,8 +160,7 @@ int route_ticket_count(int T);
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x,
                          const float *gamma, const uint16_t *router_w, const float *router_b,
                          int T, int32_t *ids_out, float *rw_out, uint16_t *xhat_out, int tile_rows,
-                         int router_exact, const uint8_t *pf_gate, const uint8_t *pf_up, size_t pf_bytes,
-                         cudaStream_t st);
+                         int router_exact, cudaStream_t st);
 cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
                                 const MatPtrs &a1, bool gateup, int T, int nt, cudaStream_t st);
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T,

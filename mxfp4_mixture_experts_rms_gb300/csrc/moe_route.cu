@@ -52,9 +52,7 @@ struct RouteArgs {
     uint16_t *xhat_out; // user copy, may be null
     int tile_rows;
     int router_exact;
-    int epc;                      // experts per CTA (router rows staged in shared memory)
-    const uint8_t *pf_codes[2];   // gate / up codes to prefetch into L2 for the selected experts
-    size_t pf_bytes;              // bytes of one expert's codes (0: no prefetch)
+    int epc;  // experts per CTA (router rows staged in shared memory)
 };
 
 __device__ __forceinline__ double warp_sum_d(double v) {
@@ -344,17 +342,6 @@ __device__ void topk_token_warp(const float *l, const float *bd, bool global_src
             a.ws.route_w[t * K + r] = w;
             if (a.ids_out) a.ids_out[t * K + r] = id;
             if (a.rw_out) a.rw_out[t * K + r] = w;
-        }
-    }
-    // start pulling the selected experts' gate/up weights into L2 for the expert kernel
-    if (a.pf_bytes && lane < K && sel[lane] != 0x7fffffff) {
-        const size_t e = (size_t)sel[lane];
-        for (int m = 0; m < 2; m++) {
-            const uint8_t *base = a.pf_codes[m] + e * a.pf_bytes;
-            for (size_t off = 0; off < a.pf_bytes; off += 65536) {
-                const uint32_t n = (uint32_t)min((size_t)65536, a.pf_bytes - off);
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(n) : "memory");
-            }
         }
     }
 }
@@ -704,19 +691,18 @@ int route_ticket_count(int T) { return T + 1; }
 
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x, const float *gamma,
                          const uint16_t *router_w, const float *router_b, int T, int32_t *ids_out, float *rw_out,
-                         uint16_t *xhat_out, int tile_rows, int router_exact, const uint8_t *pf_gate,
-                         const uint8_t *pf_up, size_t pf_bytes, cudaStream_t st) {
+                         uint16_t *xhat_out, int tile_rows, int router_exact, cudaStream_t st) {
     if (bp.H / 8 > kRouteThreads * kXC) return cudaErrorInvalidValue;
     static bool done1 = false, done8 = false;
     if (T <= 32) {
         RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact,
-                    route_epc(1, bp.H, bp.E), {pf_gate, pf_up}, pf_bytes};
+                    route_epc(1, bp.H, bp.E)};
         MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<1>, done1));
         dim3 grid(T, (bp.E + a.epc - 1) / a.epc);
         moe_route_kernel<1><<<grid, kRouteThreads, route_smem_bytes(1, bp.H, bp.E), st>>>(a);
     } else {
         RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact,
-                    route_epc(8, bp.H, bp.E), {nullptr, nullptr}, 0};
+                    route_epc(8, bp.H, bp.E)};
         MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8>, done8));
         dim3 grid((T + 7) / 8, (bp.E + a.epc - 1) / a.epc);
         moe_route_kernel<8><<<grid, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
