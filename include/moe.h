@@ -147,6 +147,26 @@ int moe_profile_read(moe_plan *plan, double *total_ms, int *launches, int n_slot
  * kernels in *status (0 = fine); clears it. */
 int moe_get_device_status(moe_plan *plan, int *status, void *stream);
 
+/* moe_forward without any device allocation, for callers that may not
+ * allocate device memory (a runtime that owns all device memory through its
+ * own pool and forbids cudaMalloc, or code that must avoid the implicit
+ * synchronisation an allocation can cause).  No passage of the source pages
+ * corresponds to it: it is a deployment variant of moe_forward.
+ *  - Scratch: a file-scope static device array of 16 MiB that every GPU
+ *    loading this library holds until exit; no moe_set_workspace is needed.
+ *    Token counts whose workspace (moe_workspace_bytes for that count) exceeds
+ *    it are rejected with MOE_ENOMEM and a message.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the array and it keeps the last call's contents; each
+ *    call clears the parts that must start at zero.  Calls that overlap on
+ *    the GPU (other streams, other plans, other threads) race on it.
+ *  - Calls no cudaMalloc, cudaFree or allocating library routine; weights,
+ *    x, out and route_ids_out are as for moe_forward. */
+int moe_forward_noalloc(moe_plan *plan, const uint16_t *x, int tokens, float *out,
+                        int32_t *route_ids_out, void *stream);
+
 /* Text of the last failure on this thread ("" if none). */
 const char *moe_last_error(void);
 

@@ -9,6 +9,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -413,6 +414,83 @@ int moe_get_device_status(moe_plan *p, int *status, void *stream) {
     if (e != cudaSuccess) return cuda_fail(e, "moe_get_device_status");
     *status = h[0];
     if (h[0]) return fail(MOE_EDEVICE, "device status %d (detail %d)", h[0], h[1]);
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Forward without any allocation: the workspace lives in a static device array.
+// Some callers cannot allocate device memory -- a runtime that owns every byte
+// of device memory through its own pool and forbids cudaMalloc, or code that
+// must not risk the implicit device synchronisation an allocation can cause.
+// For them the same kernels run on a fixed scratch array that every GPU
+// loading this library reserves once, at module load, until exit.
+#define MOE_NOALLOC_SCRATCH_BYTES (16u << 20)
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[256];  // device address of g_noalloc_scratch, per device ordinal
+
+// Once per device, with that device current: the device address of the array
+// (the name g_noalloc_scratch is only a host-side stand-in in host code).
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= 256) return fail(MOE_EINVAL, "moe_forward_noalloc: device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: cudaGetSymbolAddress");
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+}  // namespace
+
+int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, int32_t *ids_out, void *stream) {
+    if (!p) return fail(MOE_EINVAL, "NULL plan");
+    if (tokens < 0) return fail(MOE_EINVAL, "tokens must be >= 0");
+    if (tokens == 0) return MOE_OK;
+    if (!x || !out) return fail(MOE_EINVAL, "NULL x or out");
+    if (!p->have_w) return fail(MOE_ENOTREADY, "moe_load_weights has not been called");
+    if (!aligned16(x) || !aligned16(out)) return fail(MOE_EINVAL, "x and out must be 16-byte aligned");
+    const BlockParams &b = p->bp;
+    const char *xb = reinterpret_cast<const char *>(x), *ob = reinterpret_cast<const char *>(out);
+    if (xb < ob + (size_t)tokens * b.H * 4 && ob < xb + (size_t)tokens * b.H * 2)
+        return fail(MOE_EINVAL, "x and out must not alias");
+    const size_t need = carve(p, tokens, nullptr, nullptr);
+    if (need > MOE_NOALLOC_SCRATCH_BYTES)
+        return fail(MOE_ENOMEM, "moe_forward_noalloc: %d tokens need %zu bytes of scratch, the static array holds %u",
+                    tokens, need, MOE_NOALLOC_SCRATCH_BYTES);
+    void *base = nullptr;
+    int rc = noalloc_scratch(&base);
+    if (rc != MOE_OK) return rc;
+    Workspace ws;
+    carve(p, tokens, static_cast<char *>(base), &ws);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the array keeps the previous call's contents: the status word and the
+    // routing kernel's tickets must start at zero
+    cudaError_t e = cudaMemsetAsync(ws.status, 0, 16, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws.tickets, 0, sizeof(uint32_t) * route_ticket_count(tokens), st);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: clearing scratch");
+    const bool prefill_ok = b.H % 64 == 0 && b.F % 64 == 0 && p->have_maps;
+    const bool decode = !prefill_ok || p->path == 1 || (p->path == 0 && tokens <= p->decode_max_tokens);
+    const int nt = tokens <= 8 ? 1 : 2;
+    const int tile_rows = decode ? 8 * nt : prefill_tile_rows();
+    e = launch_route(b, ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, nullptr, nullptr,
+                     tile_rows, p->router_exact, st);
+    if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
+    e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, st)
+               : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
+    e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, st)
+               : launch_prefill_stage(b, ws, p->down, p->down, false, tokens, p->maps.down, st);
+    if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
+    e = launch_combine(b, ws, x, tokens, out, st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     return MOE_OK;
 }
 

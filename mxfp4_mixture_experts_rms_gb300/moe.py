@@ -23,7 +23,7 @@ _lib = None
 EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_plan_set_i", "moe_plan_set_f", "moe_workspace_bytes",
            "moe_set_workspace", "moe_load_weights", "moe_forward", "moe_forward_ex", "moe_get_expert_counts",
            "moe_get_permutation", "moe_debug_dequant", "moe_profile_read", "moe_get_device_status",
-           "moe_last_error"]
+           "moe_forward_noalloc", "moe_last_error"]
 
 
 class MoeError(RuntimeError):
@@ -74,6 +74,7 @@ def load(build_if_missing: bool = True):
     L.moe_debug_dequant.argtypes = [P, I, I, P, P]
     L.moe_get_device_status.argtypes = [P, C.POINTER(I), P]
     L.moe_profile_read.argtypes = [P, C.POINTER(C.c_double), C.POINTER(I), I]
+    L.moe_forward_noalloc.argtypes = [P, P, I, P, P, P]
     L.moe_last_error.restype = C.c_char_p
     L.moe_last_error.argtypes = []
     for name in EXPORTS:
