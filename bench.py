@@ -38,6 +38,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sets", type=int, default=4, help="weight sets rotated over the steps")
+    ap.add_argument("--workload", type=int, default=WORKLOAD,
+                    help="workload id of synth.WORKLOADS (default: the 8-token hot-2 decode batch)")
+    ap.add_argument("--tokens", type=int, default=0, help="tokens per step (default: the workload's largest)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only (no clock pre-roll, kernel timing, e2e or CPU baseline); for ncu")
@@ -282,6 +285,9 @@ def run_ours(args, rank, world, local):
     tr = traffic_record(KERNEL_SLOTS[dom])
     step_bytes = gu_bytes + dn_bytes
     step_gbs = step_bytes / (ms / args.steps / 1e3) / 1e9
+    routes = TOKENS * (K + shape.n_shared)
+    step_flops = 6.0 * routes * H * shape.expert_hidden
+    step_tflops = step_flops / (ms / args.steps / 1e3) / 1e12
 
     # ---- end to end through the public API with host buffers
     hx = [d["x"].cpu().pin_memory() for d in sets]
@@ -327,6 +333,8 @@ def run_ours(args, rank, world, local):
                    "weight_sets": len(sets), "l2": "inputs larger than L2: steps rotate over independently "
                    "seeded weight sets", "distinct_experts_per_step": distinct,
                    "algorithmic_bytes_per_step": step_bytes, "step_hbm_gbs": step_gbs,
+                   "algorithmic_flops_per_step": step_flops, "step_tflops": step_tflops,
+                   "step_tensor_frac_of_bf16_peak": step_tflops * 1e3 / peaks()[1],
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": KERNEL_SLOTS[dom], "achieved": achieved, "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
@@ -341,6 +349,10 @@ def run_ours(args, rank, world, local):
 
 def main():
     args = parse()
+    from mxfp4_mixture_experts_rms_gb300 import synth
+    global WORKLOAD, TOKENS
+    WORKLOAD = args.workload
+    TOKENS = args.tokens or max(synth.WORKLOADS[WORKLOAD].tokens)
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
