@@ -334,7 +334,7 @@ def run_ours(args, rank, world, local):
                    "seeded weight sets", "distinct_experts_per_step": distinct,
                    "algorithmic_bytes_per_step": step_bytes, "step_hbm_gbs": step_gbs,
                    "algorithmic_flops_per_step": step_flops, "step_tflops": step_tflops,
-                   "step_tensor_frac_of_bf16_peak": step_tflops * 1e3 / peaks()[1],
+                   "step_tensor_frac_of_bf16_peak": step_tflops / peaks()[1],
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": KERNEL_SLOTS[dom], "achieved": achieved, "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
