@@ -9,6 +9,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -16,7 +18,8 @@
 #include "../../include/moe.h"
 #include "moe_common.cuh"
 
-size_t decode_smem_bytes(bool gateup, int nt, int K);
+bool decode_supported(const BlockParams &bp);
+cudaError_t launch_absmax(const float *v, int n, uint32_t *out, cudaStream_t st);
 
 namespace {
 
@@ -55,6 +58,8 @@ struct moe_plan {
     MatPtrs gate{}, up{}, down{};
     PrefillMaps maps{};
     bool have_maps = false;
+    // the decode GEMVs carry x_hat / h as fp16 unless these can leave its range
+    bool x_bf16 = false, h_bf16 = false;
     // kernel timing (profile option)
     static constexpr int kSlots = 4, kMaxRec = 4096 * kSlots;
     std::vector<cudaEvent_t> ev;     // 2 events per record
@@ -73,6 +78,24 @@ struct Carve {
         return p;
     }
 };
+
+// Which projection kernels run for this token count: the GEMV (decode) path
+// or the tensor-core grouped GEMM (prefill) path.
+int choose_path(const moe_plan *p, int tokens, bool *decode, int *nt, int *tile_rows) {
+    const BlockParams &b = p->bp;
+    // the grouped GEMM needs H and F in whole 64-element stages; the GEMVs need
+    // H, F <= 4800 (register-resident activations)
+    const bool prefill_ok = b.H % 64 == 0 && b.F % 64 == 0 && p->have_maps;
+    const bool decode_ok = decode_supported(b);
+    if (p->path == 2 && !prefill_ok) return fail(MOE_ESHAPE, "the prefill path needs H and F multiples of 64");
+    if (p->path == 1 && !decode_ok) return fail(MOE_ESHAPE, "the decode path needs H and F <= 4800");
+    bool d = p->path == 1 || (p->path == 0 && (!prefill_ok || (decode_ok && tokens <= p->decode_max_tokens)));
+    if (d && !decode_ok) return fail(MOE_ESHAPE, "no kernel path for H=%d F=%d", b.H, b.F);
+    *decode = d;
+    *nt = tokens <= 8 ? 1 : 2;
+    *tile_rows = d ? 8 * *nt : prefill_tile_rows();
+    return MOE_OK;
+}
 
 int max_tiles_for(const moe_plan *p, int T) {
     const int R = T * (p->bp.K + p->bp.n_shared);
@@ -265,7 +288,7 @@ int moe_load_weights(moe_plan *p, const moe_weights *w) {
     const BlockParams &b = p->bp;
     // reject the NaN scale code (0xFF) up front
     int32_t *flag = nullptr;
-    cudaError_t e = cudaMalloc(&flag, 4);
+    cudaError_t e = cudaMalloc(&flag, 8);
     if (e != cudaSuccess) return cuda_fail(e, "moe_load_weights");
     e = cudaMemset(flag, 0, 4);
     const size_t n_gu = (size_t)b.F * (b.H / 32), n_d = (size_t)b.H * (b.F / 32);
@@ -274,17 +297,30 @@ int moe_load_weights(moe_plan *p, const moe_weights *w) {
         size_t n = (i % 3 == 2 ? n_d : n_gu) * (i < 3 ? b.E : 1);
         e = launch_scan_scales(ms[i]->scales, n, flag, 0);
     }
-    int32_t h = 0;
-    if (e == cudaSuccess) e = cudaMemcpy(&h, flag, 4, cudaMemcpyDeviceToHost);
+    // max |gamma| (second word of the flag buffer) bounds |x_hat| <= sqrt(H) max|gamma|
+    if (e == cudaSuccess) e = cudaMemset(flag + 1, 0, 4);
+    if (e == cudaSuccess) e = launch_absmax(w->gamma, b.H, reinterpret_cast<uint32_t *>(flag + 1), 0);
+    int32_t h[2] = {0, 0};
+    if (e == cudaSuccess) e = cudaMemcpy(h, flag, 8, cudaMemcpyDeviceToHost);
     cudaFree(flag);
     if (e != cudaSuccess) return cuda_fail(e, "moe_load_weights scale scan");
-    if (h) return fail(MOE_EINVAL, "an E8M0 scale holds the NaN code 0xFF");
+    if (h[0]) return fail(MOE_EINVAL, "an E8M0 scale holds the NaN code 0xFF");
+    float gmax;
+    memcpy(&gmax, &h[1], 4);
     p->w = *w;
     p->gate = mat_of(w->gate, w->sh_gate, b.F, b.H);
     p->up = mat_of(w->up, w->sh_up, b.F, b.H);
     p->down = mat_of(w->down, w->sh_down, b.H, b.F);
     p->have_maps = (b.H % 64 == 0 && b.F % 64 == 0) &&
                    prefill_make_maps(b, p->gate, p->up, p->down, &p->maps) == cudaSuccess;
+    // fp16 holds the GEMV activations below 65504: |x_hat| <= sqrt(H) max|gamma|;
+    // |h| <= max(|L|, 0.3/alpha) (|L| + 1), since x sigmoid(alpha x) >= -0.28/alpha
+    const double xb = std::sqrt((double)b.H) * (double)gmax * 1.01;
+    const double L = std::fabs((double)b.limit);
+    const double gb = b.alpha > 0.f ? std::max(L, 0.3 / (double)b.alpha) : INFINITY;
+    const double hb = gb * (L + 1.0) * 1.01;
+    p->x_bf16 = !(xb < 65504.0);
+    p->h_bf16 = !(hb < 65504.0);
     p->have_w = true;
     return MOE_OK;
 }
@@ -304,13 +340,9 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     if (xb < ob + (size_t)tokens * b.H * 4 && ob < xb + (size_t)tokens * b.H * 2)
         return fail(MOE_EINVAL, "x and out must not alias");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The tensor-core grouped GEMM needs H and F in whole 64-element stages;
-    // other shapes always take the GEMV path (which handles any token count).
-    const bool prefill_ok = b.H % 64 == 0 && b.F % 64 == 0 && p->have_maps;
-    if (p->path == 2 && !prefill_ok) return fail(MOE_ESHAPE, "the prefill path needs H and F multiples of 64");
-    const bool decode = !prefill_ok || p->path == 1 || (p->path == 0 && tokens <= p->decode_max_tokens);
-    const int nt = tokens <= 8 ? 1 : 2;
-    const int tile_rows = decode ? 8 * nt : prefill_tile_rows();
+    bool decode = false;
+    int nt = 1, tile_rows = 0;
+    if (int rc = choose_path(p, tokens, &decode, &nt, &tile_rows)) return rc;
     auto mark = [&](int slot, bool begin) {
         if (!p->profile) return;
         if (begin) {
@@ -328,12 +360,12 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     mark(0, false);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     mark(1, true);
-    e = decode ? launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, st)
+    e = decode ? launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
                : launch_prefill_stage(b, p->ws, p->gate, p->up, true, tokens, p->maps.gateup, st);
     mark(1, false);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
     mark(2, true);
-    e = decode ? launch_decode_stage(b, p->ws, p->down, p->down, false, tokens, nt, st)
+    e = decode ? launch_decode_stage(b, p->ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, st)
                : launch_prefill_stage(b, p->ws, p->down, p->down, false, tokens, p->maps.down, st);
     mark(2, false);
     if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
@@ -476,17 +508,16 @@ int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, 
     cudaError_t e = cudaMemsetAsync(ws.status, 0, 16, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(ws.tickets, 0, sizeof(uint32_t) * route_ticket_count(tokens), st);
     if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: clearing scratch");
-    const bool prefill_ok = b.H % 64 == 0 && b.F % 64 == 0 && p->have_maps;
-    const bool decode = !prefill_ok || p->path == 1 || (p->path == 0 && tokens <= p->decode_max_tokens);
-    const int nt = tokens <= 8 ? 1 : 2;
-    const int tile_rows = decode ? 8 * nt : prefill_tile_rows();
+    bool decode = false;
+    int nt = 1, tile_rows = 0;
+    if (int rc2 = choose_path(p, tokens, &decode, &nt, &tile_rows)) return rc2;
     e = launch_route(b, ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, nullptr, nullptr,
                      tile_rows, p->router_exact, st);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
-    e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, st)
+    e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
                : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, st);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
-    e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, st)
+    e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, st)
                : launch_prefill_stage(b, ws, p->down, p->down, false, tokens, p->maps.down, st);
     if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
     e = launch_combine(b, ws, x, tokens, out, st);

@@ -52,8 +52,8 @@ struct Workspace {
     int32_t *loc;          // [T][K + n_shared]
     int4 *tiles;           // [max_tiles]: (expert, route start, route count, 0)
     int32_t *n_tiles;      // [1]
-    uint16_t *h;           // [R][F] bf16 (decode: natural order; prefill: pair order)
-    uint16_t *h16;         // [R][F] fp16 copy of h (decode GEMV operand)
+    uint16_t *h;           // [R][F] bf16 (decode: natural order, bf16-activation plans only; prefill: pair order)
+    uint16_t *h16;         // [R][F] fp16 h of the decode GEMVs (natural order)
     float *y;              // [R][H] weighted expert outputs
     float *logits;         // [T][E] router logits (fp32) of the routing kernel
     float *lbound;         // [T][E] their rounding-error bounds
@@ -161,8 +161,10 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
                          const float *gamma, const uint16_t *router_w, const float *router_b,
                          int T, int32_t *ids_out, float *rw_out, uint16_t *xhat_out, int tile_rows,
                          int router_exact, cudaStream_t st);
+// x_bf16 / h_bf16: the gate/up (down) GEMV reads bf16 activations instead of fp16.
 cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
-                                const MatPtrs &a1, bool gateup, int T, int nt, cudaStream_t st);
+                                const MatPtrs &a1, bool gateup, int T, int nt, bool x_bf16, bool h_bf16,
+                                cudaStream_t st);
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T,
                            float *out, cudaStream_t st);
 // TMA descriptors of the packed codes: [0] routed A0, [1] routed A1, [2] shared A0, [3] shared A1.

@@ -1,93 +1,66 @@
 // moe_decode.cu -- decode path: MXFP4 dequant-in-register GEMVs over the
 // selected experts, the weighted combine with the residual, and the debug
-// dequantiser that shares the GEMV's dequantisation routine.
+// dequantiser that shares the GEMV's element converter.
 //
 // goosedump gpt_oss.rs `mixture_of_experts` (decode) evaluates, per selected
 // expert, `matrix_vector_pair(gate, up)` + bias, `swiglu_inplace`,
 // `matrix_vector(down)` + bias and scales by the route weight; the weighted
 // outputs are summed in slot order and added to the residual in `forward`.
 //
-// Design (sm_103a):
-//  * work item = (tile of <= 8*NT routes of one expert, 16 weight rows),
-//    walked by persistent CTAs; 8 warps split the K dimension; each thread
-//    streams its rows' packed codes with 128-bit loads straight from HBM into
-//    registers, one iteration ahead;
-//  * dequantisation in registers: one 32-bit word of codes (8 nibbles) gives
-//    four bf16x2 pairs (nibble i, nibble i+4) by two shifts and two masks,
-//    scaled exactly by the E8M0 exponent with one bf16x2 multiply;
-//  * the multiply-accumulate runs on the tensor cores (m16n8k16 bf16, fp32
-//    accumulate) with the routed activations as the N=8 operand, read in the
-//    matching pair order from L1/L2;
-//  * gate/up kernel: bias + clamped SwiGLU epilogue writes h (bf16);
-//    down kernel: bias, times the route weight, into a per-route fp32 buffer;
-//    the combine kernel sums the slots of each token in slot order and adds x.
+// Design (sm_103a), for each of the two projections:
+//  * one persistent CTA per SM: 15 consumer warps and 1 producer warp (16
+//    warps: 4 per SM sub-partition, up to 128 registers a thread);
+//  * work item = (tile of <= 8*NT routes of one expert, 16 weight rows); each
+//    CTA walks a contiguous range of items;
+//  * the producer streams every item into a ring of S shared-memory stages
+//    (S = 2..8, as deep as shared memory allows), so that several items are in
+//    flight from HBM while one is computed.  The item's 16 rows of packed codes
+//    are contiguous: one bulk asynchronous copy per matrix (the copy engine's
+//    cost is per copy, so it only gets large ranges); the E8M0 scales and the
+//    biases go by 16-byte asynchronous copies of the producer's 32 lanes;
+//  * the consumer warps split K in pairs of 32-element blocks; for tiles of up
+//    to 8 routes each keeps the routed activations of its K range in registers
+//    for the whole tile (16-route tiles load them per block pair, one ahead);
+//  * ldmatrix hands each thread one 32-bit word (8 codes) of two rows of a
+//    block; the hardware e2m1x2 -> f16x2 conversion yields the E2M1 values
+//    exactly; two m16n8k16 MMAs (fp32 accumulate) form the unscaled block dot
+//    product, which one FFMA per output multiplies by 2^(e-127) (exact) into
+//    the accumulator;
+//  * the 15 split-K partials meet in shared memory; a rotating consumer warp
+//    applies bias + clamped SwiGLU (gate/up) or bias x route weight (down).
+//
+// Activations are fp16 (x_hat and h are bf16 values; fp16 holds them exactly
+// for 2^-17 <= |v| < 65504) unless the plan found at load time that they can
+// leave the fp16 range (huge gamma or SwiGLU limit); then the bf16 variant
+// (template BF) converts the E2M1 values to bf16 and multiplies in bf16.
 #include "moe_common.cuh"
+
+// Timeline marker (no-op unless an instrumented build defines it).
+#ifndef MOE_DEC_MARK
+#define MOE_DEC_MARK(slot, k)
+#endif
 
 namespace {
 
+constexpr int kCW = 15;                      // consumer warps
+constexpr int kDecThreads = (kCW + 1) * 32;  // + 1 producer warp
+constexpr int kMaxPairs = 5;                 // block pairs per consumer warp: K <= 15 * 5 * 64 = 4800
+constexpr int kFewPairs = 3;                 // the variant for K <= 15 * 3 * 64 = 2880 (fewer registers)
+constexpr int kMaxStages = 8;
+constexpr uint64_t kDecWaitNs = 2000000000ull;
 
 struct DecodeArgs {
     BlockParams bp;
     Workspace ws;
-    MatPtrs A0, A1;   // gate, up (GATEUP) or down, unused
-    int Kdim;         // reduction length: H for gate/up, F for down
-    int rows;         // output rows: F for gate/up, H for down
+    MatPtrs A0, A1;  // gate, up (GATEUP) or down, unused
+    int Kdim;        // reduction length: H for gate/up, F for down
+    int rows;        // output rows: F for gate/up, H for down
+    int stages;      // shared-memory ring depth
+    int h_bf16;      // gate/up: write h as bf16 (else fp16)
 };
 
-// 8 nibbles of one 32-bit word -> four bf16x2 (value * 2^-126, exact):
-// pair i holds nibble i in the low half and nibble i+4 in the high half.
-__device__ __forceinline__ void nibbles_to_bf16x2(uint32_t w, uint32_t p[4]) {
-    p[0] = ((w << 6) & 0x01C001C0u) | ((w << 12) & 0x80008000u);
-    p[1] = ((w << 2) & 0x01C001C0u) | ((w << 8) & 0x80008000u);
-    p[2] = ((w >> 2) & 0x01C001C0u) | ((w << 4) & 0x80008000u);
-    p[3] = ((w >> 6) & 0x01C001C0u) | (w & 0x80008000u);
-}
-
-__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
-    __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
-    return *reinterpret_cast<uint32_t *>(&r);
-}
-
-// E8M0 exponent -> bf16x2 multiplier(s) turning value*2^-126 into value*2^(s-127).
-// For s <= 128 one factor 2^(s-1) suffices; above that two factors are used.
-__device__ __forceinline__ uint32_t scale_lo(uint32_t s) {
-    uint32_t b = (s <= 128u) ? ((s + 126u) << 7) : (253u << 7);  // 2^(s-1) or 2^126
-    return b | (b << 16);
-}
-__device__ __forceinline__ uint32_t scale_hi(uint32_t s) {
-    uint32_t b = (s <= 128u) ? 0x3F80u : (s << 7);                // 1 or 2^(s-127)
-    return b | (b << 16);
-}
-
-template <bool BIG>
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s1, uint32_t s2, uint32_t p[4]) {
-    nibbles_to_bf16x2(w, p);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        p[i] = bmul2(p[i], s1);
-        if (BIG) p[i] = bmul2(p[i], s2);
-    }
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Two exact dequantisers feed the tensor cores:
-//  * fp16 (used when every E8M0 exponent of the work item lies in [104, 140],
-//    where e2m1 * 2^(s-127) is exactly representable in fp16): the hardware
-//    e2m1x2 -> f16x2 conversion turns one byte (two nibbles, low nibble =
-//    even element) into a natural-order pair, then one f16x2 multiply applies
-//    the power-of-two scale; MMA kind f16 against the fp16 activations;
-//  * bf16 (any exponent): the shift/mask construction above, re-paired into
-//    natural order with byte permutes, scaled by one or two bf16x2
-//    multiplies; MMA kind bf16 against the bf16 activations.
-// Both keep K in natural order, so the activations need no reordering.
+// 8 E2M1 codes of one 32-bit word -> four f16x2 in natural order
+// (element 2i in the low half of h[i]), exact: byte i holds elements 2i, 2i+1.
 __device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t h[4]) {
     asm("{ .reg .b8 a, b, c, d;\n"
         "  mov.b32 {a, b, c, d}, %4;\n"
@@ -98,47 +71,52 @@ __device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t h[4]) {
         : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
         : "r"(w));
 }
-__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
-    __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
-    return *reinterpret_cast<uint32_t *>(&r);
-}
-// fp16 bits of 2^(s-127) in both halves, s in [104, 140]
-__device__ __forceinline__ uint32_t scale_f16x2(uint32_t s) {
-    const uint32_t b = (s >= 113u) ? ((s - 112u) << 10) : (1u << (s - 103u));
-    return b | (b << 16);
-}
-__device__ __forceinline__ bool f16_exact_scale(uint32_t s) { return s >= 104u && s <= 140u; }
 
-// natural-order bf16 pairs (n0,n1),(n2,n3),(n4,n5),(n6,n7), exact, any exponent
-template <bool BIG>
-__device__ __forceinline__ void dequant_word_nat(uint32_t w, uint32_t s1, uint32_t s2, uint32_t o[4]) {
-    uint32_t p[4];
-    dequant_word<BIG>(w, s1, s2, p);
-    o[0] = __byte_perm(p[0], p[1], 0x5410);
-    o[1] = __byte_perm(p[2], p[3], 0x5410);
-    o[2] = __byte_perm(p[0], p[1], 0x7632);
-    o[3] = __byte_perm(p[2], p[3], 0x7632);
+// f16x2 holding two E2M1 values (0, +-0.5 .. +-6) -> the same values as bf16x2.
+// Non-zero E2M1 magnitudes in fp16 are 0x3800..0x4600 (bit 13 or 14 set, low
+// byte zero); the bf16 pattern is (fp16 magnitude >> 3) + 0x3800.
+__device__ __forceinline__ uint32_t e2m1_f16x2_to_bf16x2(uint32_t h) {
+    const uint32_t mag = h & 0x7FFF7FFFu;
+    const uint32_t t = ((mag >> 3) & 0x0FFF0FFFu) + 0x38003800u;
+    const uint32_t nz = ((mag >> 13) | (mag >> 14)) & 0x00010001u;  // 1 per non-zero half
+    return (t & (nz * 0xFFFFu)) | (h & 0x80008000u);
 }
 
-__device__ __forceinline__ void mma_f16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// 2^(e-127) as fp32 (e = 0 gives the subnormal 2^-127); e = 255 is rejected at load.
+__device__ __forceinline__ float e8m0_f32(uint32_t e) { return __uint_as_float(max(e << 23, 0x00400000u)); }
+
+__device__ __forceinline__ void mma_16816(bool bf, float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    if (bf)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Persistent CTAs of 8 warps, each owning a contiguous range of work items
-// (tile, 16-row block).  The packed codes and E8M0 scales of an item (16 rows
-// of one or two matrices, contiguous rows in the canonical layout) are
-// streamed into a two-stage shared-memory ring by bulk asynchronous copies
-// (one per row) while the
-// previous item is computed.  The 8 warps split K (32-element blocks in groups
-// of four per warp-iteration) and reduce through shared memory; each thread
-// prefetches the next iteration's activation fragments into registers.
-constexpr int kDecWarps = 8;
-constexpr uint64_t kDecWaitNs = 2000000000ull;
+// d = A*B (C = 0)
+__device__ __forceinline__ void mma_16816_z(bool bf, float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1) {
+    if (bf)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%10,%10,%10,%10};\n"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%10,%10,%10,%10};\n"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -170,151 +148,69 @@ __device__ __forceinline__ bool dec_mbar_wait(uint64_t *b, uint32_t parity, int3
         }
     }
 }
+__device__ __forceinline__ void dec_arrive(uint64_t *b) {
+    asm volatile("{ .reg .b64 t; mbarrier.arrive.shared::cta.b64 t, [%0]; }" ::"r"(smem_addr(b)) : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_addr(dst)),
                  "l"(src), "r"(bytes), "r"(smem_addr(bar))
                  : "memory");
 }
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_addr(p)));
+}
 
 // Shared-memory geometry of one stage for reduction length K.
 struct DecGeom {
-    int rs;        // row stride of packed codes (bytes)
-    int scb;       // bytes of one matrix's 16 rows of scales, rounded to 16
-    int bias;      // offset of the [NM][16] fp32 biases in a stage
-    int stage;     // bytes of one stage (NM matrices)
+    int rs;     // row stride of packed codes (bytes)
+    int scb;    // bytes of one matrix's 16 rows of scales, rounded to 16
+    int bias;   // offset of the [NM][16] fp32 biases in a stage
+    int stage;  // bytes of one stage (NM matrices)
     __host__ __device__ DecGeom(int K, int NM) {
-        const int rb = K / 2;
-        rs = rb;  // unpadded: two stages + the reductions of two CTAs fit one SM
+        rs = K / 2;
         scb = (16 * (K / 32) + 15) & ~15;
         bias = NM * (16 * rs + scb);
         stage = (bias + NM * 64 + 127) & ~127;
     }
 };
+// split-K partials: [2][kCW][NM][NT][16 rows][8 columns] fp32
+__host__ __device__ constexpr size_t dec_red_bytes(int NM, int NT) { return (size_t)2 * kCW * NM * NT * 128 * 4; }
 
-// One warp-iteration covers 16 rows x 4 blocks of 32 (per thread: block 4q+t4
-// of rows g and g+8).  If every exponent of the iteration admits the exact
-// fp16 conversion (warp vote) the fp16 path runs on the prefetched fp16
-// activations; otherwise the bf16 path runs on bf16 activations loaded for
-// this iteration.
-template <bool GATEUP, int NT>
-__device__ __forceinline__ void decode_mainloop(int K, const unsigned char *st, const DecGeom &geo,
-                                                const uint16_t *const (&brow16)[NT],
-                                                const uint16_t *const (&browbf)[NT], float acc[2][NT][4]) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, t4 = lane & 3;
-    const int nb = K / 32, nq = (nb + 3) / 4;
-    constexpr int NM = GATEUP ? 2 : 1;
-    const unsigned char *codes = st;                    // [NM][16][rs]
-    const uint8_t *sc = st + NM * 16 * geo.rs;          // [NM][scb]
-    auto load_b = [&](uint4 (&B)[NT][4], const uint16_t *const (&brow)[NT], int q) {
-        const int b = 4 * q + t4;
-        const bool valid = q < nq && b < nb;
-#pragma unroll
-        for (int n = 0; n < NT; n++)
-#pragma unroll
-            for (int k = 0; k < 4; k++)
-                B[n][k] = (valid && brow[n]) ? __ldg(reinterpret_cast<const uint4 *>(brow[n] + 32 * b) + k)
-                                            : make_uint4(0, 0, 0, 0);
-    };
-    uint4 B[NT][4];
-    load_b(B, brow16, warp);
-    for (int q = warp; q < nq; q += kDecWarps) {
-        const int b = 4 * q + t4;
-        const bool valid = b < nb;
-        uint4 Bn[NT][4];
-        load_b(Bn, brow16, q + kDecWarps);
-        uint4 A[2][2];
-        uint32_t sv[2][2];
-        bool f16ok = true;
-#pragma unroll
-        for (int m = 0; m < NM; m++)
-#pragma unroll
-            for (int h = 0; h < 2; h++) {
-                const int r = g + 8 * h;
-                A[m][h] = valid ? *reinterpret_cast<const uint4 *>(codes + (m * 16 + r) * geo.rs + 16 * b)
-                                : make_uint4(0, 0, 0, 0);
-                sv[m][h] = valid ? sc[m * geo.scb + r * nb + b] : 127u;
-                f16ok = f16ok && f16_exact_scale(sv[m][h]);
-            }
-        if (__all_sync(0xffffffffu, f16ok)) {
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-#pragma unroll
-                for (int m = 0; m < NM; m++) {
-                    uint32_t p0[4], p1[4];
-                    e2m1x8_to_f16((&A[m][0].x)[k], p0);
-                    e2m1x8_to_f16((&A[m][1].x)[k], p1);
-                    const uint32_t s0 = scale_f16x2(sv[m][0]), s1 = scale_f16x2(sv[m][1]);
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        p0[i] = hmul2_f16(p0[i], s0);
-                        p1[i] = hmul2_f16(p1[i], s1);
-                    }
-#pragma unroll
-                    for (int n = 0; n < NT; n++) {
-                        mma_f16_16816(acc[m][n], p0[0], p1[0], p0[1], p1[1], B[n][k].x, B[n][k].y);
-                        mma_f16_16816(acc[m][n], p0[2], p1[2], p0[3], p1[3], B[n][k].z, B[n][k].w);
-                    }
-                }
-            }
-        } else {
-            uint4 Bb[NT][4];
-            load_b(Bb, browbf, q);
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-#pragma unroll
-                for (int m = 0; m < NM; m++) {
-                    uint32_t p0[4], p1[4];
-                    dequant_word_nat<true>((&A[m][0].x)[k], scale_lo(sv[m][0]), scale_hi(sv[m][0]), p0);
-                    dequant_word_nat<true>((&A[m][1].x)[k], scale_lo(sv[m][1]), scale_hi(sv[m][1]), p1);
-#pragma unroll
-                    for (int n = 0; n < NT; n++) {
-                        mma_bf16_16816(acc[m][n], p0[0], p1[0], p0[1], p1[1], Bb[n][k].x, Bb[n][k].y);
-                        mma_bf16_16816(acc[m][n], p0[2], p1[2], p0[3], p1[3], Bb[n][k].z, Bb[n][k].w);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int n = 0; n < NT; n++)
-#pragma unroll
-            for (int k = 0; k < 4; k++) B[n][k] = Bn[n][k];
-    }
-}
-
-__device__ __forceinline__ void dec_arrive(uint64_t *b) {
-    asm volatile("{ .reg .b64 t; mbarrier.arrive.shared::cta.b64 t, [%0]; }" ::"r"(smem_addr(b)) : "memory");
-}
-
-// Warp roles: warps 0..7 consume (split-K over the item's 16 rows), warp 8
-// produces (bulk copies).  mbarriers: full[s] (codes landed), empty[s] (8
-// consumer warps done with stage s), redfull[r] (8 partials written),
-// redempty[r] (epilogue done with reduction buffer r).  The epilogue of item
-// k runs on consumer warp k % 8; no CTA-wide barrier is used in the loop.
-template <bool GATEUP, int NT>
-__global__ void __launch_bounds__((kDecWarps + 1) * 32, 2) moe_decode_kernel(DecodeArgs a) {
+template <bool GATEUP, int NT, bool BF, int MP>
+__global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a) {
     constexpr int NM = GATEUP ? 2 : 1;
     extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ __align__(16) float red[2][kDecWarps][NM][NT][16][8];  // split-K partials, double-buffered
-    __shared__ __align__(8) uint64_t bars[8];
-    uint64_t *full = bars, *empty = bars + 2, *redfull = bars + 4, *redempty = bars + 6;
-    const int K = a.Kdim, nb = K / 32;
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 4];
+    uint64_t *full = bars, *empty = bars + kMaxStages, *redfull = bars + 2 * kMaxStages, *redempty = redfull + 2;
+    const int K = a.Kdim, nb = K / 32, S = a.stages;
     const DecGeom geo(K, NM);
+    float *red = reinterpret_cast<float *>(dsm + (size_t)S * geo.stage);
     const int RB = a.rows / 16;
-    asm volatile("griddepcontrol.launch_dependents;");
     if (threadIdx.x == 0) {
+        for (int i = 0; i < S; i++) {
+            // one arrival with the codes' byte count + one per producer lane (its small copies)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 33;" ::"r"(smem_addr(&full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty[i])), "r"(kCW));
+        }
         for (int i = 0; i < 2; i++) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[i])));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty[i])), "r"(kDecWarps));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&redfull[i])), "r"(kDecWarps));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&redfull[i])), "r"(kCW));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&redempty[i])));
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    // the tile table, activations and (for down) h come from the previous kernels
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Gate/up needs the routing kernel's results everywhere.  The down kernel
+    // is let in only once every gate/up CTA has passed its own wait, so the
+    // tile table is complete: its producer starts streaming weights at once
+    // (into the SMs gate/up has left) and only its consumers wait for h.
+    if (GATEUP || threadIdx.x < kCW * 32) asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int n_items = *a.ws.n_tiles * RB;
     const int per = (n_items + gridDim.x - 1) / gridDim.x;
     const int begin = blockIdx.x * per, end = min(n_items, begin + per);
@@ -323,130 +219,224 @@ __global__ void __launch_bounds__((kDecWarps + 1) * 32, 2) moe_decode_kernel(Dec
     const int E = a.bp.E;
     int32_t *status = a.ws.status;
 
-    if (warp == kDecWarps) {
+    if (warp == kCW) {
         // ---------------------------------------------------------- producer
         int issued = 0;
         for (int k = 0; k < n; k++) {
-            const int s = k & 1, item = begin + k;
-            if (k >= 2 && !dec_mbar_wait(&empty[s], ((k >> 1) - 1) & 1, status, 51)) break;
+            const int s = k % S, item = begin + k;
+            if (k >= S && !dec_mbar_wait(&empty[s], ((k / S) - 1) & 1, status, 51)) break;
             const int4 tile = a.ws.tiles[item / RB];
             const int e = tile.x, j0 = (item % RB) * 16;
-            unsigned char *st = dsm + s * geo.stage;
+            unsigned char *st = dsm + (size_t)s * geo.stage;
             if (lane == 0) {
-                const uint32_t bytes = NM * (16 * (K / 2) + 16 * nb + 64);
+                const uint32_t bytes = NM * 16 * (K / 2);
                 asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(
                                  smem_addr(&full[s])),
                              "r"(bytes)
                              : "memory");
+#pragma unroll
+                for (int m = 0; m < NM; m++) {
+                    const MatPtrs &M = m == 0 ? a.A0 : a.A1;
+                    bulk_g2s(st + m * 16 * geo.rs, mat_codes(M, e, E) + (size_t)j0 * (K / 2), 16 * (K / 2), &full[s]);
+                }
             }
-            __syncwarp();
 #pragma unroll
             for (int m = 0; m < NM; m++) {
                 const MatPtrs &M = m == 0 ? a.A0 : a.A1;
-                if (lane < 16)
-                    bulk_g2s(st + (m * 16 + lane) * geo.rs, mat_codes(M, e, E) + (size_t)(j0 + lane) * (K / 2), K / 2,
-                             &full[s]);
-                if (lane == 16 + m) {
-                    bulk_g2s(st + NM * 16 * geo.rs + m * geo.scb, mat_scales(M, e, E) + (size_t)j0 * nb, 16 * nb,
-                             &full[s]);
-                    bulk_g2s(st + geo.bias + m * 64, mat_bias(M, e, E) + j0, 64, &full[s]);
-                }
+                const uint8_t *scs = mat_scales(M, e, E) + (size_t)j0 * nb;
+                unsigned char *scd = st + NM * 16 * geo.rs + m * geo.scb;
+                for (int c = lane; c < nb; c += 32) cp_async16(scd + 16 * c, scs + 16 * c);
+                if (lane < 4) cp_async16(st + geo.bias + m * 64 + 16 * lane, mat_bias(M, e, E) + j0 + 4 * lane);
             }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&full[s])) : "memory");
             issued = k + 1;
+            if (lane == 0) MOE_DEC_MARK(0, k);
         }
-        // the copies of the last two stages must have landed before this warp exits
-        for (int k = max(0, issued - 2); k < issued; k++) dec_mbar_wait(&full[k & 1], (k >> 1) & 1, status, 52);
+        // the copies still in flight must land before this warp exits
+        for (int k = max(0, issued - S); k < issued; k++) dec_mbar_wait(&full[k % S], (k / S) & 1, status, 52);
         return;
     }
 
     // -------------------------------------------------------------- consumers
+    const int npairs = (nb + 1) >> 1;
+    // activations of pair p = warp + kCW*i: block 2p+bb, token column nn*8 + g,
+    // elements 8*t4 .. 8*t4+7 of the block (zero past the end of K or of the tile)
+    const uint16_t *brow[NT];
+    auto load_pair = [&](uint4(&dst)[2][NT], int i) {
+        const int p = warp + kCW * i;
+#pragma unroll
+        for (int bb = 0; bb < 2; bb++) {
+            const int b = 2 * p + bb;
+#pragma unroll
+            for (int nn = 0; nn < NT; nn++)
+                dst[bb][nn] = (p < npairs && b < nb && brow[nn])
+                                  ? __ldg(reinterpret_cast<const uint4 *>(brow[nn] + 32 * b + 8 * t4))
+                                  : make_uint4(0, 0, 0, 0);
+        }
+    };
+    constexpr bool kRegB = NT == 1;  // whole-tile activations in registers
+    uint4 Bc[kRegB ? MP : 1][2][NT];
     int cur_tile = -1;
-    int4 tile = make_int4(0, 0, 0, 0);
+    int rstart = 0, rcount = 0;
+    // ldmatrix row address pattern: matrices (rows 0-7, block 2p), (rows 8-15, 2p),
+    // (rows 0-7, 2p+1), (rows 8-15, 2p+1); this lane supplies row lrow of matrix lane/8
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lblk = lane >> 4;
+#pragma unroll 1
     for (int k = 0; k < n; k++) {
-        const int item = begin + k, s = k & 1, r = k & 1;
+        const int item = begin + k, s = k % S, r = k & 1;
         if (item / RB != cur_tile) {
             cur_tile = item / RB;
-            tile = a.ws.tiles[cur_tile];
-        }
-        const int rstart = tile.y, rcount = tile.z;
-        const int j0 = (item % RB) * 16;
-        if (!dec_mbar_wait(&full[s], (k >> 1) & 1, status, 50)) break;
-        const unsigned char *st = dsm + s * geo.stage;
-        const uint16_t *brow16[NT], *browbf[NT];
+            const int4 tile = a.ws.tiles[cur_tile];
+            rstart = tile.y;
+            rcount = tile.z;
 #pragma unroll
-        for (int nn = 0; nn < NT; nn++) {
-            const int col = nn * 8 + g;
-            brow16[nn] = browbf[nn] = nullptr;
-            if (col < rcount) {
-                if (GATEUP) {
-                    const size_t tok = (size_t)a.ws.perm_token[rstart + col];
-                    brow16[nn] = a.ws.xhat16 + tok * K;
-                    browbf[nn] = a.ws.xhat + tok * K;
-                } else {
-                    brow16[nn] = a.ws.h16 + (size_t)(rstart + col) * K;
-                    browbf[nn] = a.ws.h + (size_t)(rstart + col) * K;
+            for (int nn = 0; nn < NT; nn++) {
+                const int col = nn * 8 + g;
+                brow[nn] = nullptr;
+                if (col < rcount) {
+                    if (GATEUP)
+                        brow[nn] = (BF ? a.ws.xhat : a.ws.xhat16) + (size_t)a.ws.perm_token[rstart + col] * K;
+                    else
+                        brow[nn] = (BF ? a.ws.h : a.ws.h16) + (size_t)(rstart + col) * K;
                 }
             }
+            if (kRegB) {
+#pragma unroll
+                for (int i = 0; i < MP; i++) load_pair(Bc[kRegB ? i : 0], i);
+            }
         }
-        const bool epi = warp == (k % kDecWarps);
-        float b0 = 0.f, b1 = 0.f;  // biases of row lane & 15 (epilogue warp only), read before the stage is released
+        const int j0 = (item % RB) * 16;
+        uint4 Bcur[2][NT], Bnext[2][NT];
+        if (!kRegB) load_pair(Bcur, 0);
+        if (!dec_mbar_wait(&full[s], (k / S) & 1, status, 50)) break;
+        if (warp == 0 && lane == 0) MOE_DEC_MARK(1, k);
+        const unsigned char *st = dsm + (size_t)s * geo.stage;
+        const bool epi = warp == (k % kCW);
+        float b0 = 0.f, b1 = 0.f;  // biases of row lane/2 (epilogue warp only), read before the stage is released
         if (epi) {
             const float *sb = reinterpret_cast<const float *>(st + geo.bias);
-            b0 = sb[lane & 15];
-            if (GATEUP) b1 = sb[16 + (lane & 15)];
+            b0 = sb[lane >> 1];
+            if (GATEUP) b1 = sb[16 + (lane >> 1)];
         }
-        float acc[2][NT][4];
+        float acc[NM][NT][4];
 #pragma unroll
-        for (int m = 0; m < 2; m++)
+        for (int m = 0; m < NM; m++)
 #pragma unroll
             for (int nn = 0; nn < NT; nn++)
 #pragma unroll
                 for (int q = 0; q < 4; q++) acc[m][nn][q] = 0.f;
-        decode_mainloop<GATEUP, NT>(K, st, geo, brow16, browbf, acc);
+#pragma unroll
+        for (int i = 0; i < MP; i++) {
+            const int p = warp + kCW * i;
+            if (p < npairs) {
+                if (!kRegB && i + 1 < MP) load_pair(Bnext, i + 1);
+                const int bk0 = 2 * p, bk1 = min(2 * p + 1, nb - 1);  // a missing odd block has zero activations
+#pragma unroll
+                for (int m = 0; m < NM; m++) {
+                    const unsigned char *codes = st + m * 16 * geo.rs;
+                    const uint8_t *sc = st + NM * 16 * geo.rs + m * geo.scb;
+                    uint32_t wv[4];
+                    ldmatrix_x4(wv, codes + lrow * geo.rs + 16 * (lblk ? bk1 : bk0));
+                    const float f[2][2] = {{e8m0_f32(sc[g * nb + bk0]), e8m0_f32(sc[(g + 8) * nb + bk0])},
+                                           {e8m0_f32(sc[g * nb + bk1]), e8m0_f32(sc[(g + 8) * nb + bk1])}};
+#pragma unroll
+                    for (int bb = 0; bb < 2; bb++) {
+                        uint32_t hg[4], hg8[4];
+                        e2m1x8_to_f16(wv[2 * bb], hg);
+                        e2m1x8_to_f16(wv[2 * bb + 1], hg8);
+                        if (BF) {
+#pragma unroll
+                            for (int q = 0; q < 4; q++) {
+                                hg[q] = e2m1_f16x2_to_bf16x2(hg[q]);
+                                hg8[q] = e2m1_f16x2_to_bf16x2(hg8[q]);
+                            }
+                        }
+#pragma unroll
+                        for (int nn = 0; nn < NT; nn++) {
+                            float t[4];
+                            const uint4 bv = kRegB ? Bc[kRegB ? i : 0][bb][nn] : Bcur[bb][nn];
+                            mma_16816_z(BF, t, hg[0], hg8[0], hg[1], hg8[1], bv.x, bv.y);
+                            mma_16816(BF, t, hg[2], hg8[2], hg[3], hg8[3], bv.z, bv.w);
+                            acc[m][nn][0] = fmaf(t[0], f[bb][0], acc[m][nn][0]);
+                            acc[m][nn][1] = fmaf(t[1], f[bb][0], acc[m][nn][1]);
+                            acc[m][nn][2] = fmaf(t[2], f[bb][1], acc[m][nn][2]);
+                            acc[m][nn][3] = fmaf(t[3], f[bb][1], acc[m][nn][3]);
+                        }
+                    }
+                }
+                if (!kRegB) {
+#pragma unroll
+                    for (int bb = 0; bb < 2; bb++)
+#pragma unroll
+                        for (int nn = 0; nn < NT; nn++) Bcur[bb][nn] = Bnext[bb][nn];
+                }
+            }
+            // keep the shared-memory reads of one pair from being hoisted into the
+            // previous one (register pressure)
+            asm volatile("" ::: "memory");
+        }
         __syncwarp();
+        if (warp == 0 && lane == 0) MOE_DEC_MARK(2, k);
         if (lane == 0) dec_arrive(&empty[s]);  // this warp no longer reads stage s
         if (k >= 2 && !dec_mbar_wait(&redempty[r], ((k >> 1) - 1) & 1, status, 53)) break;
+        float *rw = red + (size_t)(r * kCW + warp) * NM * NT * 128;
 #pragma unroll
         for (int m = 0; m < NM; m++)
 #pragma unroll
             for (int nn = 0; nn < NT; nn++) {
-                float(*rp)[8] = red[r][warp][m][nn];
-                rp[g][2 * t4] = acc[m][nn][0];
-                rp[g][2 * t4 + 1] = acc[m][nn][1];
-                rp[g + 8][2 * t4] = acc[m][nn][2];
-                rp[g + 8][2 * t4 + 1] = acc[m][nn][3];
+                float *rp = rw + (m * NT + nn) * 128;
+                *reinterpret_cast<float2 *>(rp + g * 8 + 2 * t4) = make_float2(acc[m][nn][0], acc[m][nn][1]);
+                *reinterpret_cast<float2 *>(rp + (g + 8) * 8 + 2 * t4) = make_float2(acc[m][nn][2], acc[m][nn][3]);
             }
         __syncwarp();
         if (lane == 0) dec_arrive(&redfull[r]);
         if (epi) {
             if (!dec_mbar_wait(&redfull[r], (k >> 1) & 1, status, 54)) break;
-            for (int idx = lane; idx < 16 * 8 * NT; idx += 32) {
-                const int row = idx & 15, col = idx >> 4;  // col = route within the tile
-                const float bb0 = __shfl_sync(0xffffffffu, b0, row);
-                const float bb1 = __shfl_sync(0xffffffffu, b1, row);
-                if (col >= rcount) continue;
-                const int nn = col >> 3, c = col & 7;
-                float sm[NM];
+            if (lane == 0) MOE_DEC_MARK(3, k);
+            // lane: row lane/2, columns 4*(lane&1) .. +3 of every column group nn
+            const int row = lane >> 1, c0 = 4 * (lane & 1);
+            const float *rr = red + (size_t)r * kCW * NM * NT * 128;
+#pragma unroll
+            for (int nn = 0; nn < NT; nn++) {
+                float4 sm[NM];
 #pragma unroll
                 for (int m = 0; m < NM; m++) {
-                    float v = 0.f;
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int w = 0; w < kDecWarps; w++) v += red[r][w][m][nn][row][c];
+                    for (int w = 0; w < kCW; w++) {
+                        const float4 q =
+                            *reinterpret_cast<const float4 *>(rr + ((w * NM + m) * NT + nn) * 128 + row * 8 + c0);
+                        v.x += q.x;
+                        v.y += q.y;
+                        v.z += q.z;
+                        v.w += q.w;
+                    }
                     sm[m] = v;
                 }
+                const float s0[4] = {sm[0].x, sm[0].y, sm[0].z, sm[0].w};
+                const float s1[4] = {sm[NM - 1].x, sm[NM - 1].y, sm[NM - 1].z, sm[NM - 1].w};
                 const int j = j0 + row;
-                const int route = rstart + col;
-                if (GATEUP) {
-                    const float hv = swiglu_clamped(sm[0] + bb0, sm[1] + bb1, a.bp.alpha, a.bp.limit);
-                    const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                    const __half h16 = __float2half_rn(__bfloat162float(hb));  // exact for |h| >= 2^-14
-                    a.ws.h[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&hb);
-                    a.ws.h16[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&h16);
-                } else {
-                    a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * (sm[0] + bb0);
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const int col = nn * 8 + c0 + c;  // route within the tile
+                    if (col >= rcount) continue;
+                    const int route = rstart + col;
+                    if (GATEUP) {
+                        const float hv = swiglu_clamped(s0[c] + b0, s1[c] + b1, a.bp.alpha, a.bp.limit);
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                        if (a.h_bf16) {
+                            a.ws.h[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&hb);
+                        } else {
+                            const __half h16 = __float2half_rn(__bfloat162float(hb));
+                            a.ws.h16[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&h16);
+                        }
+                    } else {
+                        a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * (s0[c] + b0);
+                    }
                 }
             }
             __syncwarp();
+            if (lane == 0) MOE_DEC_MARK(4, k);
             if (lane == 0) dec_arrive(&redempty[r]);
         }
     }
@@ -479,8 +469,8 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(BlockParams bp, Worksp
     *reinterpret_cast<float4 *>(out + (size_t)t * H + i4 * 4) = o;
 }
 
-// One thread per 32-element block: the GEMV's element converters (fp16 where
-// the exponent allows it exactly, bf16 otherwise), written out in natural order.
+// One thread per 32-element block: the GEMV's element converter (E2M1 -> fp16,
+// exact) and its fp32 block scale, written out in natural order.
 __global__ void moe_dequant_kernel(MatPtrs m, int expert, int n_experts, float *out) {
     const int nb = m.cols / 32;
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -489,27 +479,15 @@ __global__ void moe_dequant_kernel(MatPtrs m, int expert, int n_experts, float *
     const uint8_t *codes = mat_codes(m, expert, n_experts);
     const uint8_t *scales = mat_scales(m, expert, n_experts);
     const uint4 v = *reinterpret_cast<const uint4 *>(codes + row * (m.cols / 2) + 16 * b);
-    const uint32_t s = scales[row * nb + b];
+    const float f = e8m0_f32(scales[row * nb + b]);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float *o = out + row * m.cols + 32 * b;
     for (int k = 0; k < 4; k++) {
         uint32_t p[4];
-        if (f16_exact_scale(s)) {
-            e2m1x8_to_f16(w[k], p);
-            for (int ii = 0; ii < 4; ii++) p[ii] = hmul2_f16(p[ii], scale_f16x2(s));
-            for (int ii = 0; ii < 4; ii++) {
-                o[8 * k + 2 * ii] = __half2float(__ushort_as_half((unsigned short)(p[ii] & 0xFFFFu)));
-                o[8 * k + 2 * ii + 1] = __half2float(__ushort_as_half((unsigned short)(p[ii] >> 16)));
-            }
-        } else {
-            if (s > 128u)
-                dequant_word_nat<true>(w[k], scale_lo(s), scale_hi(s), p);
-            else
-                dequant_word_nat<false>(w[k], scale_lo(s), scale_hi(s), p);
-            for (int ii = 0; ii < 4; ii++) {
-                o[8 * k + 2 * ii] = __uint_as_float(p[ii] << 16);
-                o[8 * k + 2 * ii + 1] = __uint_as_float(p[ii] & 0xFFFF0000u);
-            }
+        e2m1x8_to_f16(w[k], p);
+        for (int ii = 0; ii < 4; ii++) {
+            o[8 * k + 2 * ii] = __half2float(__ushort_as_half((unsigned short)(p[ii] & 0xFFFFu))) * f;
+            o[8 * k + 2 * ii + 1] = __half2float(__ushort_as_half((unsigned short)(p[ii] >> 16))) * f;
         }
     }
 }
@@ -522,44 +500,90 @@ __global__ void moe_scan_scales_kernel(const uint8_t *s, size_t n, int32_t *flag
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
 }
 
-}  // namespace
-
-size_t decode_smem_bytes(bool gateup, int, int K) { return 2 * (size_t)DecGeom(K, gateup ? 2 : 1).stage; }
-
-template <bool GATEUP, int NT>
-static cudaError_t launch_one(const DecodeArgs &a, int n_items_max, cudaStream_t st) {
-    static int per_sm = 0, n_sm = 0;
-    static bool done = false;
-    const size_t smem = decode_smem_bytes(GATEUP, NT, a.Kdim);
-    MOE_CUDA_TRY(smem_optin_once(moe_decode_kernel<GATEUP, NT>, done));
-    if (!per_sm) {
-        int dev = 0;
-        MOE_CUDA_TRY(cudaGetDevice(&dev));
-        MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
-        MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_decode_kernel<GATEUP, NT>,
-                                                                   (kDecWarps + 1) * 32, smem));
-        if (per_sm < 1) per_sm = 1;
+// max |v| over n floats (NaN counts as +inf), as the bit pattern of a
+// non-negative float: the integer order of such patterns is their value order.
+__global__ void moe_absmax_kernel(const float *v, int n, uint32_t *out) {
+    uint32_t m = 0;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const float a = fabsf(v[i]);
+        m = max(m, a != a ? 0x7F800000u : __float_as_uint(a));
     }
-    int grid = n_sm * per_sm;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(out, m);
+}
+
+struct KernelInfo {
+    bool done = false;
+    int n_sm = 0, avail = 0;
+};
+
+template <bool GATEUP, int NT, bool BF, int MP>
+static cudaError_t launch_one(DecodeArgs a, int n_items_max, cudaStream_t st) {
+    constexpr int NM = GATEUP ? 2 : 1;
+    static KernelInfo ki;
+    auto kern = moe_decode_kernel<GATEUP, NT, BF, MP>;
+    if (!ki.done) {
+        bool opt = false;
+        MOE_CUDA_TRY(smem_optin_once(kern, opt));
+        int dev = 0, optin = 0;
+        MOE_CUDA_TRY(cudaGetDevice(&dev));
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&ki.n_sm, cudaDevAttrMultiProcessorCount, dev));
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+        cudaFuncAttributes fa;
+        MOE_CUDA_TRY(cudaFuncGetAttributes(&fa, kern));
+        ki.avail = optin - (int)fa.sharedSizeBytes;
+        ki.done = true;
+    }
+    const DecGeom geo(a.Kdim, NM);
+    int S = (int)((ki.avail - (long long)dec_red_bytes(NM, NT)) / geo.stage);
+    if (S > kMaxStages) S = kMaxStages;
+    if (S < 2) return cudaErrorInvalidValue;
+    a.stages = S;
+    int grid = ki.n_sm;
     if (grid > n_items_max) grid = n_items_max;
     if (grid < 1) grid = 1;
-    return launch_pdl(moe_decode_kernel<GATEUP, NT>, dim3(grid), dim3((kDecWarps + 1) * 32), smem, st, a);
+    const size_t smem = (size_t)S * geo.stage + dec_red_bytes(NM, NT);
+    return launch_pdl(kern, dim3(grid), dim3(kDecThreads), smem, st, a);
+}
+
+// variant choice: bf16 activations, and the number of block pairs a warp covers
+// (fewer pairs, fewer registers for the activations of 8-route tiles)
+template <bool GATEUP, int NT>
+static cudaError_t launch_bf(const DecodeArgs &a, bool bf, int n_items_max, cudaStream_t st) {
+    const bool few = (a.Kdim / 32 + 1) / 2 <= kCW * kFewPairs;
+    if (few)
+        return bf ? launch_one<GATEUP, NT, true, kFewPairs>(a, n_items_max, st)
+                  : launch_one<GATEUP, NT, false, kFewPairs>(a, n_items_max, st);
+    return bf ? launch_one<GATEUP, NT, true, kMaxPairs>(a, n_items_max, st)
+              : launch_one<GATEUP, NT, false, kMaxPairs>(a, n_items_max, st);
+}
+
+}  // namespace
+
+bool decode_supported(const BlockParams &bp) {
+    // K range of the register-resident activations, and two ring stages next to the partials
+    const int kmax = kCW * kMaxPairs * 64;
+    if (bp.H > kmax || bp.F > kmax) return false;
+    const size_t optin = 227 * 1024;
+    return 2 * (size_t)DecGeom(bp.H, 2).stage + dec_red_bytes(2, 2) + 1024 <= optin &&
+           2 * (size_t)DecGeom(bp.F, 1).stage + dec_red_bytes(1, 2) + 1024 <= optin;
 }
 
 cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0, const MatPtrs &a1,
-                                bool gateup, int T, int nt, cudaStream_t st) {
+                                bool gateup, int T, int nt, bool x_bf16, bool h_bf16, cudaStream_t st) {
     const int R = T * (bp.K + bp.n_shared);
     // upper bound on the tile count: each expert's last tile may be partial
     int tiles = (R + 8 * nt - 1) / (8 * nt) + bp.E + bp.n_shared;
     if (tiles > ws.max_tiles) tiles = ws.max_tiles;
     if (gateup) {
-        DecodeArgs gu{bp, ws, a0, a1, bp.H, bp.F};
+        DecodeArgs gu{bp, ws, a0, a1, bp.H, bp.F, 0, h_bf16 ? 1 : 0};
         const int items = tiles * (bp.F / 16);
-        return nt == 1 ? launch_one<true, 1>(gu, items, st) : launch_one<true, 2>(gu, items, st);
+        return nt == 1 ? launch_bf<true, 1>(gu, x_bf16, items, st) : launch_bf<true, 2>(gu, x_bf16, items, st);
     }
-    DecodeArgs dn{bp, ws, a0, a0, bp.F, bp.H};
+    DecodeArgs dn{bp, ws, a0, a0, bp.F, bp.H, 0, 0};
     const int items = tiles * (bp.H / 16);
-    return nt == 1 ? launch_one<false, 1>(dn, items, st) : launch_one<false, 2>(dn, items, st);
+    return nt == 1 ? launch_bf<false, 1>(dn, h_bf16, items, st) : launch_bf<false, 2>(dn, h_bf16, items, st);
 }
 
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T, float *out,
@@ -576,5 +600,12 @@ cudaError_t launch_dequant(const MatPtrs &m, int expert, int n_experts, float *o
 
 cudaError_t launch_scan_scales(const uint8_t *scales, size_t n, int32_t *flag, cudaStream_t st) {
     moe_scan_scales_kernel<<<1024, 256, 0, st>>>(scales, n, flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_absmax(const float *v, int n, uint32_t *out, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    const int blocks = (n + 255) / 256 < 64 ? (n + 255) / 256 : 64;
+    moe_absmax_kernel<<<blocks, 256, 0, st>>>(v, n, out);
     return cudaGetLastError();
 }

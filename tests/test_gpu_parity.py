@@ -187,3 +187,20 @@ def test_decode_and_prefill_paths_agree(cfg, T):
     ref = oracle.moe_forward(blk, np.ascontiguousarray(x[sample]), nthreads=NTHREADS)
     check_close(b["out"][sample], ref["out"], x[sample], what="prefill vs oracle")
     check_close(a["out"][sample], ref["out"], x[sample], what="decode vs oracle")
+
+
+@pytest.mark.parametrize("H,F,gamma_mul,limit,T", [
+    (96, 64, 8000.0, 7.0, 5),      # |x_hat| beyond fp16: bf16 gate/up GEMV
+    (96, 64, 1.0, 300.0, 9),       # |h| beyond fp16: bf16 down GEMV
+    (128, 128, 8000.0, 300.0, 12)])
+def test_block_parity_bf16_activation_gemvs(H, F, gamma_mul, limit, T):
+    # activations that can leave the fp16 range switch the decode GEMVs to bf16 operands
+    shape = synth.tiny_shape(H, F, 4, 2, swiglu_limit=limit)
+    blk = tiny_block(H + T, shape)
+    blk["gamma"] = (blk["gamma"] * np.float32(gamma_mul)).astype(np.float32)
+    x = synth.f32_to_bf16_bits(np.random.default_rng(T).normal(0, 1, (T, H)))
+    r, _, _ = run_gpu(blk, x, path=1)
+    ref = oracle.moe_forward(blk, x, nthreads=NTHREADS)
+    assert r["status"] == 0
+    assert np.array_equal(r["ids"], ref["ids"])
+    check_close(r["out"], ref["out"], x)
