@@ -356,7 +356,7 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     };
     mark(0, true);
     cudaError_t e = launch_route(b, p->ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, rw_out,
-                                 xhat_out, tile_rows, p->router_exact, st);
+                                 xhat_out, tile_rows, p->router_exact, decode ? 0 : 1, st);
     mark(0, false);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     mark(1, true);
@@ -512,7 +512,7 @@ int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, 
     int nt = 1, tile_rows = 0;
     if (int rc2 = choose_path(p, tokens, &decode, &nt, &tile_rows)) return rc2;
     e = launch_route(b, ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, nullptr, nullptr,
-                     tile_rows, p->router_exact, st);
+                     tile_rows, p->router_exact, decode ? 0 : 1, st);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
                : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, st);

@@ -160,7 +160,7 @@ int route_ticket_count(int T);
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x,
                          const float *gamma, const uint16_t *router_w, const float *router_b,
                          int T, int32_t *ids_out, float *rw_out, uint16_t *xhat_out, int tile_rows,
-                         int router_exact, cudaStream_t st);
+                         int router_exact, int store_mma, cudaStream_t st);
 // x_bf16 / h_bf16: the gate/up (down) GEMV reads bf16 activations instead of fp16.
 cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
                                 const MatPtrs &a1, bool gateup, int T, int nt, bool x_bf16, bool h_bf16,

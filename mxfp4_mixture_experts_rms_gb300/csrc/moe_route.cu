@@ -11,11 +11,14 @@
 //  * goosedump gpt_oss.rs `mixture_of_experts_batch` / `mix_expert_outputs`:
 //    routes appended per expert in token order, one output location per route.
 //
-// Grid: (token groups of G tokens) x (expert chunks of 8*EPW experts).  Every
-// CTA normalises its tokens (chunk 0 also stores x_hat), computes the router
-// logits of its experts and writes them with an error bound; the last CTA of a
-// token group selects the top-k of its tokens; the last CTA of the grid builds
-// the permutation.  "Last" is decided by atomic tickets, never by waiting.
+// Two kernels.  Small batches (T <= 32, the decode regime): one thread-block
+// cluster per token, its CTAs splitting the experts; every CTA normalises the
+// token, computes its experts' logits with error bounds and writes them into
+// the shared memory of the cluster's first CTA, which selects the top-k after
+// a cluster barrier.  Larger batches: CTAs of 8 tokens x an expert chunk; the
+// last CTA of a token group (atomic ticket) selects the top-k of its tokens.
+// In both, the last token-owning CTA to finish (atomic ticket, never a wait)
+// builds the permutation.
 //
 // Exactness.  Σx² is accumulated exactly as a 128-bit fixed-point integer
 // (bf16 squares have 16-bit significands), rounded once to double, and
@@ -52,7 +55,9 @@ struct RouteArgs {
     uint16_t *xhat_out; // user copy, may be null
     int tile_rows;
     int router_exact;
-    int epc;  // experts per CTA (router rows staged in shared memory)
+    int epc;        // experts per CTA (router rows staged in shared memory)
+    int store_mma;  // also write x_hat in the grouped GEMM's pair order
+    double inv_h;   // 1 / H
 };
 
 __device__ __forceinline__ double warp_sum_d(double v) {
@@ -74,12 +79,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 __device__ __forceinline__ bool better(float v, int i, float w, int j) { return v > w || (v == w && i < j); }
 __device__ __forceinline__ bool better_d(double v, int i, double w, int j) { return v > w || (v == w && i < j); }
 
-__device__ __forceinline__ void warp_best(float &v, int &i) {
+template <class V>
+__device__ __forceinline__ void warp_best(V &v, int &i) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
-        float w = __shfl_xor_sync(0xffffffffu, v, o);
+        V w = __shfl_xor_sync(0xffffffffu, v, o);
         int j = __shfl_xor_sync(0xffffffffu, i, o);
-        if (better(w, j, v, i)) {
+        if (w > v || (w == v && j < i)) {
             v = w;
             i = j;
         }
@@ -238,349 +244,147 @@ __device__ __forceinline__ uint32_t norm_elem(uint32_t xb, float gf, float r32, 
     return bf16_from_double_rne((double)xf * r * (double)gf);
 }
 
-// Top-k + softmax of one token by one warp: fp32 selection certified by the
-// error bounds, exact fp64 re-evaluation of the candidates when the bounds of
-// consecutive selections overlap.  l / bd: the token's logits and bounds of
-// experts [e0, e0 + ne) -- here always the whole [0, E).
-__device__ void topk_token_warp(const float *l, const float *bd, bool global_src, const uint16_t *xh,
-                                const RouteArgs &a, int t, int lane) {
+// 1/sqrt(m) in double: Newton steps from the fp32 seed (two steps take its
+// ~2^-22 error below double rounding), plain division outside the seed's range.
+__device__ __forceinline__ double rsqrt_d(double m) {
+    if (!(m >= 1e-30 && m <= 1e30)) return 1.0 / sqrt(m);
+    double y = (double)rsqrtf((float)m);
+    y = y * (1.5 - 0.5 * m * y * y);
+    y = y * (1.5 - 0.5 * m * y * y);
+    return y;
+}
+
+constexpr int kInvalid = 0x7fffffff;
+
+// Top-k + softmax of one token by one warp (goosedump gpt_oss.rs
+// `top_experts` and `softmax`).  The logits l[0..E) and their error bounds
+// come from shared (GLOBAL = false) or global memory; lane j holds experts
+// j, j+32, ...; the r-th selection ends in lane r's registers.  The fp32
+// selection stands when consecutive selected values are further apart than
+// twice the largest bound; otherwise every candidate within reach of the k-th
+// value is recomputed exactly in fp64 (into exs[0..E), shared memory) and the
+// selection is redone on those.
+template <bool GLOBAL>
+__device__ void topk_token(const float *l, const float *bd, const uint16_t *xh, const RouteArgs &a, int t,
+                           int lane, double *exs) {
     const int E = a.bp.E, K = a.bp.K, H = a.bp.H;
     const bool exact_mode = a.router_exact != 0;
-    auto ld = [&](const float *p) { return global_src ? __ldcg(p) : *p; };
-    int sel[MOE_MAX_TOPK + 1];
-    float selv[MOE_MAX_TOPK + 1];
-    float lv[MOE_MAX_EXPERTS / 32];
-    uint32_t taken = 0;
+    auto ld = [&](const float *p) { return GLOBAL ? __ldcg(p) : *p; };
+    constexpr int NQ = MOE_MAX_EXPERTS / 32;
+    float lv[NQ];
     float dmax = 0.f;
 #pragma unroll
-    for (int q = 0; q < MOE_MAX_EXPERTS / 32; q++) {
+    for (int q = 0; q < NQ; q++) {
         const int j = lane + 32 * q;
         lv[q] = j < E ? ld(l + j) : -INFINITY;
         if (j < E) dmax = fmaxf(dmax, ld(bd + j));
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
+    uint32_t taken = 0;
+    float my_v = -INFINITY;
+    int my_i = kInvalid;
     for (int r = 0; r <= K; r++) {
         float bv = -INFINITY;
-        int bi = 0x7fffffff;
+        int bi = kInvalid;
 #pragma unroll
-        for (int q = 0; q < MOE_MAX_EXPERTS / 32; q++) {
+        for (int q = 0; q < NQ; q++) {
             const int j = lane + 32 * q;
             const float v = lv[q];
-            if (j >= E || !(v > -INFINITY) || (taken >> q & 1u)) continue;  // NaN / -inf never chosen
-            if (better(v, j, bv, bi)) {
+            // NaN and -inf are never chosen
+            if (j < E && v > -INFINITY && !(taken >> q & 1u) && better(v, j, bv, bi)) {
                 bv = v;
                 bi = j;
             }
         }
         warp_best(bv, bi);
-        sel[r] = bi;
-        selv[r] = bv;
-        if (bi != 0x7fffffff && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-    }
-    bool certain = !exact_mode;
-    if (certain) {
-        for (int r = 0; r < K; r++) {
-            if (sel[r] == 0x7fffffff) break;
-            const float nxt = (sel[r + 1] == 0x7fffffff) ? -INFINITY : selv[r + 1];
-            if (!(selv[r] - nxt > 2.0f * dmax)) certain = false;
+        if (lane == r) {
+            my_v = bv;
+            my_i = bi;
         }
+        if (bi != kInvalid && (bi & 31) == lane) taken |= 1u << (bi >> 5);
     }
-    double exactv[MOE_MAX_TOPK];
+    // certification: selection r must beat selection r+1 by more than 2 dmax
+    const float nx_v = __shfl_down_sync(0xffffffffu, my_v, 1);
+    const int nx_i = __shfl_down_sync(0xffffffffu, my_i, 1);
+    bool ok = true;
+    if (lane < K && my_i != kInvalid) ok = my_v - (nx_i == kInvalid ? -INFINITY : nx_v) > 2.0f * dmax;
+    const bool certain = !exact_mode && __all_sync(0xffffffffu, ok);
+    double my_d = 0.0;
     bool have_exact = false;
     if (!certain) {
-        const float thr =
-            exact_mode ? -INFINITY : ((sel[K - 1] == 0x7fffffff) ? -INFINITY : selv[K - 1] - 2.0f * dmax);
-        double bv_all[MOE_MAX_TOPK];
-        int bi_all[MOE_MAX_TOPK];
-        for (int r = 0; r < K; r++) {
-            bv_all[r] = -INFINITY;
-            bi_all[r] = 0x7fffffff;
-        }
+        const float kv = __shfl_sync(0xffffffffu, my_v, K - 1);
+        const int ki = __shfl_sync(0xffffffffu, my_i, K - 1);
+        const float thr = (exact_mode || ki == kInvalid) ? -INFINITY : kv - 2.0f * dmax;
         for (int j = 0; j < E; j++) {  // warp-uniform
             const float v = ld(l + j);
-            if (!(v > -INFINITY) || v < thr) continue;
-            const double ex = exact_logit(xh, a.router_w, a.router_b, j, H, lane);
-            if (!(ex > -INFINITY)) continue;
-            int pos = K;
-            for (int r = 0; r < K; r++)
-                if (better_d(ex, j, bv_all[r], bi_all[r])) {
-                    pos = r;
-                    break;
-                }
-            if (pos < K) {
-                for (int r = K - 1; r > pos; r--) {
-                    bv_all[r] = bv_all[r - 1];
-                    bi_all[r] = bi_all[r - 1];
-                }
-                bv_all[pos] = ex;
-                bi_all[pos] = j;
-            }
+            double ex = -INFINITY;
+            if (v > -INFINITY && !(v < thr)) ex = exact_logit(xh, a.router_w, a.router_b, j, H, lane);
+            if (lane == 0) exs[j] = ex;
         }
+        __syncwarp();
+        taken = 0;
+        my_i = kInvalid;
+        my_d = -INFINITY;
         for (int r = 0; r < K; r++) {
-            sel[r] = bi_all[r];
-            exactv[r] = bv_all[r];
-            selv[r] = (float)bv_all[r];
-        }
-        have_exact = true;
-    }
-    // softmax over the selected raw logits (lane 0), times the weight scale
-    if (lane == 0) {
-        float m = -INFINITY;
-        for (int r = 0; r < K; r++)
-            if (sel[r] != 0x7fffffff) m = fmaxf(m, selv[r]);
-        float ew[MOE_MAX_TOPK], s = 0.f;
-        for (int r = 0; r < K; r++) {
-            const float d = have_exact ? (float)(exactv[r] - (double)m) : (selv[r] - m);
-            ew[r] = (sel[r] == 0x7fffffff) ? 0.f : expf(d);
-            s += ew[r];
-        }
-        for (int r = 0; r < K; r++) {
-            const int id = (sel[r] == 0x7fffffff) ? 0 : sel[r];  // unfilled slot: expert 0, weight 0
-            const float w = (s > 0.f) ? a.bp.wscale * (ew[r] / s) : 0.f;
-            a.ws.ids[t * K + r] = id;
-            a.ws.route_w[t * K + r] = w;
-            if (a.ids_out) a.ids_out[t * K + r] = id;
-            if (a.rw_out) a.rw_out[t * K + r] = w;
-        }
-    }
-}
-
-template <int G>
-__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int H = a.bp.H, E = a.bp.E, K = a.bp.K;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int epc = a.epc;                                                        // experts per CTA
-    uint16_t *wsm = reinterpret_cast<uint16_t *>(smem);                           // [epc][H] router rows
-    uint16_t *xh = wsm + (size_t)epc * H;                                         // [G][H] x_hat
-    float *lg = reinterpret_cast<float *>(xh + (size_t)G * H);                    // [G][epc] logits
-    float *lb = lg + G * epc;                                                     // [G][epc] bounds
-    __shared__ int s_maxexp[kRouteWarps];
-    __shared__ U128 s_acc[kRouteWarps];
-    __shared__ double s_r;
-    __shared__ int s_flag;
-    __shared__ __align__(8) uint64_t wbar;
-
-    const int t0 = blockIdx.x * G;
-    const int nt = min(G, a.T - t0);
-    const int e0 = blockIdx.y * epc, ne = min(epc, E - e0);
-    const int nchunk = H / 8;  // 16-byte chunks per row
-
-    // router rows of this CTA's experts: one contiguous range, bulk-copied during the norm
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar)));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        const size_t bytes = (size_t)ne * H * 2;
-        asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(smem_u32(&wbar)),
-                     "r"((uint32_t)bytes)
-                     : "memory");
-        const unsigned char *src = reinterpret_cast<const unsigned char *>(a.router_w + (size_t)e0 * H);
-        for (size_t off = 0; off < bytes; off += 32768) {
-            const uint32_t n = (uint32_t)min((size_t)32768, bytes - off);
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_u32(reinterpret_cast<unsigned char *>(wsm) + off)),
-                "l"(src + off), "r"(n), "r"(smem_u32(&wbar))
-                : "memory");
-        }
-    }
-
-    MOE_PHASE_MARK(0);
-    // ---------------------------------------------------------------- norm
-    // x and gamma are read as 16-byte chunks held in registers: one round trip
-    // per row, issued ahead of use.
-    const bool store = blockIdx.y == 0;
-    float4 gm[kXC][2];
+            double bv = -INFINITY;
+            int bi = kInvalid;
 #pragma unroll
-    for (int j = 0; j < kXC; j++) {
-        const int c = tid + kRouteThreads * j;
-        const float4 *g4 = reinterpret_cast<const float4 *>(a.gamma) + 2 * c;
-        gm[j][0] = c < nchunk ? __ldg(g4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        gm[j][1] = c < nchunk ? __ldg(g4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    uint4 xv[kXC], xnext[kXC];
-    auto load_row = [&](int t, uint4(&dst)[kXC]) {
-        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
-#pragma unroll
-        for (int j = 0; j < kXC; j++) {
-            const int c = tid + kRouteThreads * j;
-            dst[j] = c < nchunk ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
-        }
-    };
-    if (nt > 0) load_row(t0, xv);
-    for (int g = 0; g < nt; g++) {
-        const int t = t0 + g;
-        if (g + 1 < nt) load_row(t + 1, xnext);
-        const double ss = sumsq_exact(xv, lane, warp, s_maxexp, s_acc);
-        MOE_PHASE_MARK(1);
-        if (tid == 0) s_r = 1.0 / sqrt(ss / (double)H + a.bp.eps);
-        __syncthreads();
-        MOE_PHASE_MARK(2);
-        const double r = s_r;
-        const float r32 = (float)r;
-#pragma unroll
-        for (int j = 0; j < kXC; j++) {
-            const int c = tid + kRouteThreads * j;
-            if (c >= nchunk) continue;
-            const uint32_t w4[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-            const float gg[8] = {gm[j][0].x, gm[j][0].y, gm[j][0].z, gm[j][0].w,
-                                 gm[j][1].x, gm[j][1].y, gm[j][1].z, gm[j][1].w};
-            uint32_t hb[8];
-#pragma unroll
-            for (int q = 0; q < 8; q++) hb[q] = norm_elem((w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, gg[q], r32, r);
-            const uint4 nat = make_uint4(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16, hb[4] | hb[5] << 16,
-                                         hb[6] | hb[7] << 16);
-            *reinterpret_cast<uint4 *>(xh + g * H + 8 * c) = nat;
-            if (store) {
-                // prefill pair order inside each 8-element chunk: (e0,e4),(e1,e5),(e2,e6),(e3,e7)
-                const uint4 prm = make_uint4(hb[0] | hb[4] << 16, hb[1] | hb[5] << 16, hb[2] | hb[6] << 16,
-                                             hb[3] | hb[7] << 16);
-                uint32_t f[8];
-#pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));  // exact for |x_hat| >= 2^-14
-                    f[q] = *reinterpret_cast<uint16_t *>(&hh);
-                }
-                const size_t go = (size_t)t * H + 8 * c;
-                *reinterpret_cast<uint4 *>(a.ws.xhat + go) = nat;
-                *reinterpret_cast<uint4 *>(a.ws.xhat_mma + go) = prm;
-                *reinterpret_cast<uint4 *>(a.ws.xhat16 + go) =
-                    make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
-                if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + go) = nat;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kXC; j++) xv[j] = xnext[j];
-        __syncthreads();
-    }
-
-    MOE_PHASE_MARK(3);
-    // -------------------------------------------------------------- router
-    // Products of two bf16 are exact in fp32 and enter the sums through FMA.
-    // Each 8-product chunk is summed first (8 roundings), chunk sums are
-    // accumulated per lane (per_lane roundings), then a 5-level butterfly and
-    // the bias: every partial sum is bounded by Σ|p|, so the error is
-    // <= gamma_n * (Σ|p| + |b| + |l|) with n = 8 + per_lane + 6; the stored
-    // bound is doubled as a safety margin.
-    const int per_lane = (nchunk + 31) / 32;
-    const int chain = 8 + per_lane + 6;
-    {
-        uint32_t ok = 0;
-        uint64_t c0, c1;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c0));
-        for (;;) {
-            asm volatile(
-                "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0; selp.u32 %0, 1, 0, p; }"
-                : "=r"(ok)
-                : "r"(smem_u32(&wbar))
-                : "memory");
-            if (ok) break;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c1));
-            if (c1 - c0 > 2000000000ull) {
-                set_device_error(a.ws.status, MOE_DEV_WAIT_TIMEOUT, 70);
-                break;
-            }
-        }
-        if (!ok) return;  // copies are reported lost; nothing else depends on this CTA
-    }
-    for (int el = warp; el < ne; el += kRouteWarps) {
-        const int e = e0 + el;
-        const uint16_t *wrow = wsm + (size_t)el * H;
-        if (!a.router_exact) {
-            float acc[G], sab[G];
-#pragma unroll
-            for (int g = 0; g < G; g++) acc[g] = sab[g] = 0.f;
-            for (int ch = lane; ch < nchunk; ch += 32) {
-                const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + 8 * ch);
-                const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-                float wf[8];
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    wf[2 * q] = __uint_as_float(ww[q] << 16);
-                    wf[2 * q + 1] = __uint_as_float(ww[q] & 0xFFFF0000u);
-                }
-#pragma unroll
-                for (int g = 0; g < G; g++) {
-                    if (g < nt) {
-                        const uint4 xq = *reinterpret_cast<const uint4 *>(xh + g * H + ch * 8);
-                        const uint32_t xx[4] = {xq.x, xq.y, xq.z, xq.w};
-                        float cs = 0.f, ab = sab[g];
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            const float x0 = __uint_as_float(xx[q] << 16), x1 = __uint_as_float(xx[q] & 0xFFFF0000u);
-                            cs = fmaf(x0, wf[2 * q], cs);
-                            cs = fmaf(x1, wf[2 * q + 1], cs);
-                            ab = fmaf(fabsf(x0), fabsf(wf[2 * q]), ab);
-                            ab = fmaf(fabsf(x1), fabsf(wf[2 * q + 1]), ab);
-                        }
-                        acc[g] += cs;
-                        sab[g] = ab;
+            for (int q = 0; q < NQ; q++) {
+                const int j = lane + 32 * q;
+                if (j < E && !(taken >> q & 1u)) {
+                    const double v = exs[j];
+                    if (v > -INFINITY && better_d(v, j, bv, bi)) {
+                        bv = v;
+                        bi = j;
                     }
                 }
             }
+            warp_best(bv, bi);
+            if (lane == r) {
+                my_d = bv;
+                my_i = bi;
+                my_v = (float)bv;
+            }
+            if (bi != kInvalid && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+        }
+        have_exact = true;
+    }
+    // softmax over the selected raw logits, times the weight scale; lane r owns slot r
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);
+    const double md = __shfl_sync(0xffffffffu, my_d, 0);
+    const bool valid = lane < K && my_i != kInvalid;
+    float ew = 0.f;
+    if (valid) ew = expf(have_exact ? (float)(my_d - md) : (my_v - m));
+    float ssum = ew;
 #pragma unroll
-            for (int g = 0; g < G; g++) {
-                const float sm = warp_sum_f(acc[g]);
-                const float ab = warp_sum_f(sab[g]);
-                if (lane == 0 && g < nt) {
-                    const float b = a.router_b[e];
-                    const float l = sm + b;
-                    lg[g * epc + el] = l;
-                    lb[g * epc + el] = 2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
-                }
-            }
-        } else {
-            for (int g = 0; g < nt; g++) {
-                const double l = exact_logit(xh + g * H, a.router_w, a.router_b, e, H, lane);
-                if (lane == 0) {
-                    lg[g * epc + el] = (float)l;
-                    lb[g * epc + el] = 0.f;
-                }
-            }
-        }
+    for (int o = 16; o; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+    if (lane < K) {
+        const int id = valid ? my_i : 0;  // unfilled slot: expert 0, weight 0
+        const float w = (valid && ssum > 0.f) ? a.bp.wscale * (ew / ssum) : 0.f;
+        a.ws.ids[t * K + lane] = id;
+        a.ws.route_w[t * K + lane] = w;
+        if (a.ids_out) a.ids_out[t * K + lane] = id;
+        if (a.rw_out) a.rw_out[t * K + lane] = w;
     }
-    __syncthreads();
-    MOE_PHASE_MARK(4);
+}
 
-    // ---------------------------------------------------------- top-k + softmax
-    if (gridDim.y == 1) {
-        // this CTA holds every logit of its tokens
-        for (int g = warp; g < nt; g += kRouteWarps)
-            topk_token_warp(lg + g * epc, lb + g * epc, false, xh + g * H, a, t0 + g, lane);
-    } else {
-        for (int i = tid; i < nt * ne; i += kRouteThreads) {
-            const int g = i / ne, el = i - g * ne;
-            a.ws.logits[(size_t)(t0 + g) * E + e0 + el] = lg[g * epc + el];
-            a.ws.lbound[(size_t)(t0 + g) * E + e0 + el] = lb[g * epc + el];
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) s_flag = (atomicAdd(a.ws.tickets + 1 + blockIdx.x, 1u) == gridDim.y - 1);
-        __syncthreads();
-        if (!s_flag) return;
-        __threadfence();
-        for (int g = warp; g < nt; g += kRouteWarps)
-            topk_token_warp(a.ws.logits + (size_t)(t0 + g) * E, a.ws.lbound + (size_t)(t0 + g) * E, true,
-                            xh + g * H, a, t0 + g, lane);
-        if (tid == 0) a.ws.tickets[1 + blockIdx.x] = 0u;  // re-arm the group ticket
-    }
-    MOE_PHASE_MARK(5);
+// Bytes of shared memory the permutation needs (per-expert counters).
+__host__ __device__ constexpr size_t perm_smem_bytes(int E) { return (size_t)(5 * 264 + kRouteWarps * (E + 1)) * 4; }
 
-    // --------------------------------------------- last CTA of the grid: permutation
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_flag = (atomicAdd(a.ws.tickets, 1u) == gridDim.x - 1);
-    __syncthreads();
-    if (!s_flag) return;
-    __threadfence();
-    MOE_PHASE_MARK(6);
-
+// The token->expert permutation (goosedump gpt_oss.rs `mixture_of_experts_batch`:
+// routes appended per expert in token order): per-expert histogram, exclusive
+// prefix sums of counts and of tiles, stable scatter of (token, slot, weight),
+// the inverse map and the tile table.  Run by one CTA once every token's ids
+// are in global memory.
+__device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = a.bp.E, K = a.bp.K;
     const int ns = a.bp.n_shared;
     const int EE = E + ns;
     const int KK = K + ns;
     const int R = a.T * K;
-    int32_t *cnt = reinterpret_cast<int32_t *>(smem);  // reuses the router-row area
+    int32_t *cnt = reinterpret_cast<int32_t *>(smem);
     int32_t *offs = cnt + 264;
     int32_t *run = offs + 264;
     int32_t *tcnt = run + 264;
@@ -665,13 +469,373 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
         }
     }
     if (tid == 0) a.ws.tickets[0] = 0u;  // re-arm for the next launch
+}
+
+// Normalise one token row held in registers into xh (shared) and, if `store`,
+// into the workspace copies: bf16 natural order, fp16, and (store_mma) the
+// grouped GEMM's pair order.
+__device__ __forceinline__ void normalise_row(const RouteArgs &a, const uint4 (&xv)[kXC], const float4 (&gm)[kXC][2],
+                                              int t, double r, uint16_t *xh, bool store) {
+    const int H = a.bp.H, nchunk = H / 8;
+    const float r32 = (float)r;
+#pragma unroll
+    for (int j = 0; j < kXC; j++) {
+        const int c = threadIdx.x + kRouteThreads * j;
+        if (c >= nchunk) continue;
+        const uint32_t w4[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        const float gg[8] = {gm[j][0].x, gm[j][0].y, gm[j][0].z, gm[j][0].w,
+                             gm[j][1].x, gm[j][1].y, gm[j][1].z, gm[j][1].w};
+        uint32_t hb[8];
+#pragma unroll
+        for (int q = 0; q < 8; q++) hb[q] = norm_elem((w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, gg[q], r32, r);
+        const uint4 nat = make_uint4(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16, hb[4] | hb[5] << 16,
+                                     hb[6] | hb[7] << 16);
+        *reinterpret_cast<uint4 *>(xh + 8 * c) = nat;
+        if (store) {
+            const size_t go = (size_t)t * H + 8 * c;
+            *reinterpret_cast<uint4 *>(a.ws.xhat + go) = nat;
+            if (a.store_mma) {
+                // pair order inside each 8-element chunk: (e0,e4),(e1,e5),(e2,e6),(e3,e7)
+                *reinterpret_cast<uint4 *>(a.ws.xhat_mma + go) = make_uint4(
+                    hb[0] | hb[4] << 16, hb[1] | hb[5] << 16, hb[2] | hb[6] << 16, hb[3] | hb[7] << 16);
+            }
+            uint32_t f[8];
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));  // exact for |x_hat| >= 2^-17
+                f[q] = *reinterpret_cast<uint16_t *>(&hh);
+            }
+            *reinterpret_cast<uint4 *>(a.ws.xhat16 + go) =
+                make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
+            if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + go) = nat;
+        }
+    }
+}
+
+// Router logit of expert e (row w, shared or global memory) for one x_hat row
+// in shared memory, by one warp: products of two bf16 are exact in fp32 and
+// enter the sums through FMA; each 8-product chunk is summed first (8
+// roundings), chunk sums are accumulated per lane (per_lane roundings), then a
+// 5-level butterfly and the bias: every partial sum is bounded by Σ|p|, so the
+// error is <= gamma_n (Σ|p| + |b| + |l|) with n = 8 + per_lane + 6; the bound
+// returned is doubled as a safety margin.
+template <bool GLOBAL_ROW>
+__device__ __forceinline__ void router_logit(const uint16_t *wrow, const uint16_t *xh, float b, int H, int lane,
+                                             float &l, float &bound) {
+    const int nchunk = H / 8, per_lane = (nchunk + 31) / 32, chain = 8 + per_lane + 6;
+    float acc = 0.f, sab = 0.f;
+    for (int ch = lane; ch < nchunk; ch += 32) {
+        const uint4 wv = GLOBAL_ROW ? __ldg(reinterpret_cast<const uint4 *>(wrow + 8 * ch))
+                                    : *reinterpret_cast<const uint4 *>(wrow + 8 * ch);
+        const uint4 xq = *reinterpret_cast<const uint4 *>(xh + 8 * ch);
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w}, xx[4] = {xq.x, xq.y, xq.z, xq.w};
+        float cs = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float w0 = __uint_as_float(ww[q] << 16), w1 = __uint_as_float(ww[q] & 0xFFFF0000u);
+            const float x0 = __uint_as_float(xx[q] << 16), x1 = __uint_as_float(xx[q] & 0xFFFF0000u);
+            cs = fmaf(x0, w0, cs);
+            cs = fmaf(x1, w1, cs);
+            sab = fmaf(fabsf(x0), fabsf(w0), sab);
+            sab = fmaf(fabsf(x1), fabsf(w1), sab);
+        }
+        acc += cs;
+    }
+    const float sm = warp_sum_f(acc), ab = warp_sum_f(sab);
+    l = sm + b;
+    bound = 2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(const float *local, uint32_t rank, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Small batches: grid (T, C), cluster (1, C): CTA c of token t's cluster
+// computes the logits of experts [c*epc, c*epc + epc) (router rows staged in
+// shared memory by a bulk copy when STAGED, read from global memory
+// otherwise) into CTA 0's shared memory; CTA 0 selects the top-k.
+template <bool STAGED>
+__global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int H = a.bp.H, E = a.bp.E;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t = blockIdx.x;
+    const uint32_t rank = cluster_ctarank();
+    const int epc = a.epc, e0 = (int)rank * epc, ne = max(0, min(epc, E - e0));
+    // layout: [router rows | permutation counters] [x_hat row] [logits E] [bounds E] [exact logits E]
+    const size_t rows_b = STAGED ? (size_t)epc * H * 2 : 0;
+    const size_t head = ((rows_b > perm_smem_bytes(E) ? rows_b : perm_smem_bytes(E)) + 127) & ~(size_t)127;
+    uint16_t *wsm = reinterpret_cast<uint16_t *>(smem);
+    uint16_t *xh = reinterpret_cast<uint16_t *>(smem + head);
+    float *lg = reinterpret_cast<float *>(smem + head + (size_t)H * 2);
+    float *lb = lg + E;
+    double *exs = reinterpret_cast<double *>(smem + ((head + (size_t)H * 2 + 8 * (size_t)E + 7) & ~(size_t)7));
+    __shared__ int s_maxexp[kRouteWarps];
+    __shared__ U128 s_acc[kRouteWarps];
+    __shared__ double s_r;
+    __shared__ int s_flag;
+    __shared__ __align__(8) uint64_t wbar;
+
+    if (STAGED && tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const size_t bytes = (size_t)ne * H * 2;
+        asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(smem_u32(&wbar)),
+                     "r"((uint32_t)bytes)
+                     : "memory");
+        const unsigned char *src = reinterpret_cast<const unsigned char *>(a.router_w + (size_t)e0 * H);
+        for (size_t off = 0; off < bytes; off += 32768) {
+            const uint32_t n = (uint32_t)min((size_t)32768, bytes - off);
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(reinterpret_cast<unsigned char *>(wsm) + off)),
+                "l"(src + off), "r"(n), "r"(smem_u32(&wbar))
+                : "memory");
+        }
+    }
+    MOE_PHASE_MARK(0);
+    // ---------------------------------------------------------------- norm
+    const int nchunk = H / 8;
+    float4 gm[kXC][2];
+    uint4 xv[kXC];
+    const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
+#pragma unroll
+    for (int j = 0; j < kXC; j++) {
+        const int c = tid + kRouteThreads * j;
+        const float4 *g4 = reinterpret_cast<const float4 *>(a.gamma) + 2 * c;
+        xv[j] = c < nchunk ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        gm[j][0] = c < nchunk ? __ldg(g4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        gm[j][1] = c < nchunk ? __ldg(g4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const double ss = sumsq_exact(xv, lane, warp, s_maxexp, s_acc);
+    MOE_PHASE_MARK(1);
+    if (tid == 0) s_r = rsqrt_d(ss * a.inv_h + a.bp.eps);
+    __syncthreads();
+    MOE_PHASE_MARK(2);
+    normalise_row(a, xv, gm, t, s_r, xh, rank == 0);
+    __syncthreads();
+    MOE_PHASE_MARK(3);
+    // -------------------------------------------------------------- router
+    bool rows_ok = true;
+    if (STAGED) {
+        uint32_t ok = 0;
+        uint64_t c0, c1;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c0));
+        for (;;) {
+            asm volatile(
+                "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0; selp.u32 %0, 1, 0, p; }"
+                : "=r"(ok)
+                : "r"(smem_u32(&wbar))
+                : "memory");
+            if (ok) break;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c1));
+            if (c1 - c0 > 2000000000ull) {
+                set_device_error(a.ws.status, MOE_DEV_WAIT_TIMEOUT, 70);
+                break;
+            }
+        }
+        rows_ok = ok != 0;
+    }
+    if (rows_ok) {
+        for (int el = warp; el < ne; el += kRouteWarps) {
+            const int e = e0 + el;
+            float l, bd;
+            if (!a.router_exact) {
+                if (STAGED)
+                    router_logit<false>(wsm + (size_t)el * H, xh, a.router_b[e], H, lane, l, bd);
+                else
+                    router_logit<true>(a.router_w + (size_t)e * H, xh, a.router_b[e], H, lane, l, bd);
+            } else {
+                l = (float)exact_logit(xh, a.router_w, a.router_b, e, H, lane);
+                bd = 0.f;
+            }
+            if (lane == 0) {
+                st_cluster_f32(lg + e, 0, l);
+                st_cluster_f32(lb + e, 0, bd);
+            }
+        }
+    }
+    // every CTA of the cluster arrives, whatever happened above
+    cluster_sync();
+    MOE_PHASE_MARK(4);
+    if (rank != 0) return;
+    // ---------------------------------------------------------- top-k + softmax
+    if (warp == 0) topk_token<false>(lg, lb, xh, a, t, lane, exs);
+    MOE_PHASE_MARK(5);
+    // ---------------------------------- last token to finish: permutation
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_flag = (atomicAdd(a.ws.tickets, 1u) == (unsigned)a.T - 1u);
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+    MOE_PHASE_MARK(6);
+    build_permutation(a, smem);
     MOE_PHASE_MARK(7);
+}
+
+// Larger batches: grid (token groups of G tokens) x (expert chunks of epc experts).
+template <int G>
+__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int H = a.bp.H, E = a.bp.E;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int epc = a.epc;                                                        // experts per CTA
+    uint16_t *wsm = reinterpret_cast<uint16_t *>(smem);                           // [epc][H] router rows
+    uint16_t *xh = wsm + (size_t)epc * H;                                         // [G][H] x_hat
+    float *lg = reinterpret_cast<float *>(xh + (size_t)G * H);                    // [G][epc] logits
+    float *lb = lg + G * epc;                                                     // [G][epc] bounds
+    double *exs = reinterpret_cast<double *>(lb + G * epc) + (size_t)warp * E;  // [warps][E] exact logits
+    __shared__ int s_maxexp[kRouteWarps];
+    __shared__ U128 s_acc[kRouteWarps];
+    __shared__ double s_r;
+    __shared__ int s_flag;
+    __shared__ __align__(8) uint64_t wbar;
+
+    const int t0 = blockIdx.x * G;
+    const int nt = min(G, a.T - t0);
+    const int e0 = blockIdx.y * epc, ne = min(epc, E - e0);
+    const int nchunk = H / 8;  // 16-byte chunks per row
+
+    // router rows of this CTA's experts: one contiguous range, bulk-copied during the norm
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const size_t bytes = (size_t)ne * H * 2;
+        asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(smem_u32(&wbar)),
+                     "r"((uint32_t)bytes)
+                     : "memory");
+        const unsigned char *src = reinterpret_cast<const unsigned char *>(a.router_w + (size_t)e0 * H);
+        for (size_t off = 0; off < bytes; off += 32768) {
+            const uint32_t n = (uint32_t)min((size_t)32768, bytes - off);
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(reinterpret_cast<unsigned char *>(wsm) + off)),
+                "l"(src + off), "r"(n), "r"(smem_u32(&wbar))
+                : "memory");
+        }
+    }
+
+    // ---------------------------------------------------------------- norm
+    // x and gamma are read as 16-byte chunks held in registers: one round trip
+    // per row, issued ahead of use.
+    const bool store = blockIdx.y == 0;
+    float4 gm[kXC][2];
+#pragma unroll
+    for (int j = 0; j < kXC; j++) {
+        const int c = tid + kRouteThreads * j;
+        const float4 *g4 = reinterpret_cast<const float4 *>(a.gamma) + 2 * c;
+        gm[j][0] = c < nchunk ? __ldg(g4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        gm[j][1] = c < nchunk ? __ldg(g4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    uint4 xv[kXC], xnext[kXC];
+    auto load_row = [&](int t, uint4(&dst)[kXC]) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
+#pragma unroll
+        for (int j = 0; j < kXC; j++) {
+            const int c = tid + kRouteThreads * j;
+            dst[j] = c < nchunk ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    if (nt > 0) load_row(t0, xv);
+    for (int g = 0; g < nt; g++) {
+        const int t = t0 + g;
+        if (g + 1 < nt) load_row(t + 1, xnext);
+        const double ss = sumsq_exact(xv, lane, warp, s_maxexp, s_acc);
+        if (tid == 0) s_r = rsqrt_d(ss * a.inv_h + a.bp.eps);
+        __syncthreads();
+        normalise_row(a, xv, gm, t, s_r, xh + g * H, store);
+#pragma unroll
+        for (int j = 0; j < kXC; j++) xv[j] = xnext[j];
+        __syncthreads();
+    }
+
+    // -------------------------------------------------------------- router
+    {
+        uint32_t ok = 0;
+        uint64_t c0, c1;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c0));
+        for (;;) {
+            asm volatile(
+                "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0; selp.u32 %0, 1, 0, p; }"
+                : "=r"(ok)
+                : "r"(smem_u32(&wbar))
+                : "memory");
+            if (ok) break;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c1));
+            if (c1 - c0 > 2000000000ull) {
+                set_device_error(a.ws.status, MOE_DEV_WAIT_TIMEOUT, 70);
+                break;
+            }
+        }
+        if (!ok) return;  // copies are reported lost; nothing else depends on this CTA
+    }
+    for (int el = warp; el < ne; el += kRouteWarps) {
+        const int e = e0 + el;
+        const uint16_t *wrow = wsm + (size_t)el * H;
+        for (int g = 0; g < nt; g++) {
+            float l, bd;
+            if (!a.router_exact) {
+                router_logit<false>(wrow, xh + g * H, a.router_b[e], H, lane, l, bd);
+            } else {
+                l = (float)exact_logit(xh + g * H, a.router_w, a.router_b, e, H, lane);
+                bd = 0.f;
+            }
+            if (lane == 0) {
+                lg[g * epc + el] = l;
+                lb[g * epc + el] = bd;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------- top-k + softmax
+    if (gridDim.y == 1) {
+        // this CTA holds every logit of its tokens
+        for (int g = warp; g < nt; g += kRouteWarps)
+            topk_token<false>(lg + g * epc, lb + g * epc, xh + g * H, a, t0 + g, lane, exs);
+    } else {
+        for (int i = tid; i < nt * ne; i += kRouteThreads) {
+            const int g = i / ne, el = i - g * ne;
+            a.ws.logits[(size_t)(t0 + g) * E + e0 + el] = lg[g * epc + el];
+            a.ws.lbound[(size_t)(t0 + g) * E + e0 + el] = lb[g * epc + el];
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_flag = (atomicAdd(a.ws.tickets + 1 + blockIdx.x, 1u) == gridDim.y - 1);
+        __syncthreads();
+        if (!s_flag) return;
+        __threadfence();
+        for (int g = warp; g < nt; g += kRouteWarps)
+            topk_token<true>(a.ws.logits + (size_t)(t0 + g) * E, a.ws.lbound + (size_t)(t0 + g) * E, xh + g * H, a,
+                             t0 + g, lane, exs);
+        if (tid == 0) a.ws.tickets[1 + blockIdx.x] = 0u;  // re-arm the group ticket
+    }
+
+    // --------------------------------------------- last CTA of the grid: permutation
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_flag = (atomicAdd(a.ws.tickets, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+    build_permutation(a, smem);  // reuses the router-row area
 }
 
 // Experts per CTA so that their router rows plus G x_hat rows fit in shared memory.
 int route_epc(int G, int H, int E) {
     const size_t budget = 200 * 1024;
-    const size_t xbytes = (size_t)G * H * 2;
+    const size_t xbytes = (size_t)G * H * 2 + (size_t)kRouteWarps * E * 8 + 64;
     int epc = (int)((budget - xbytes) / ((size_t)H * 2 + 8 * G));
     if (epc > E) epc = E;
     if (epc < 1) epc = 1;
@@ -680,9 +844,45 @@ int route_epc(int G, int H, int E) {
 
 size_t route_smem_bytes(int G, int H, int E) {
     const int epc = route_epc(G, H, E);
-    const size_t a = (size_t)epc * H * 2 + (size_t)G * H * 2 + (size_t)G * epc * 8;
-    const size_t b = (size_t)(5 * 264 + kRouteWarps * (E + 1)) * 4;
+    const size_t a = (size_t)epc * H * 2 + (size_t)G * H * 2 + (size_t)G * epc * 8 + (size_t)kRouteWarps * E * 8;
+    const size_t b = perm_smem_bytes(E);
     return a > b ? a : b;
+}
+
+// Small-batch geometry: C CTAs per token (a cluster, C <= 8), epc experts each.
+struct SmallGeo {
+    int C, epc;
+    bool staged;
+    size_t smem;
+};
+SmallGeo small_geo(int H, int E) {
+    SmallGeo g;
+    g.epc = E <= 8 * kRouteWarps ? kRouteWarps : (E + 7) / 8;  // one expert per warp while E <= 64
+    g.C = (E + g.epc - 1) / g.epc;
+    g.staged = (size_t)g.epc * H * 2 <= 160 * 1024;
+    const size_t rows_b = g.staged ? (size_t)g.epc * H * 2 : 0;
+    const size_t head = ((rows_b > perm_smem_bytes(E) ? rows_b : perm_smem_bytes(E)) + 127) & ~(size_t)127;
+    g.smem = ((head + (size_t)H * 2 + 8 * (size_t)E + 7) & ~(size_t)7) + 8 * (size_t)E;
+    return g;
+}
+
+template <bool STAGED>
+cudaError_t launch_small(const RouteArgs &a, const SmallGeo &g, cudaStream_t st) {
+    static bool done = false;
+    MOE_CUDA_TRY(smem_optin_once(moe_route_small_kernel<STAGED>, done));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.T, g.C);
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.dynamicSmemBytes = g.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = g.C;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_route_small_kernel<STAGED>, a);
 }
 
 }  // namespace
@@ -691,21 +891,20 @@ int route_ticket_count(int T) { return T + 1; }
 
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x, const float *gamma,
                          const uint16_t *router_w, const float *router_b, int T, int32_t *ids_out, float *rw_out,
-                         uint16_t *xhat_out, int tile_rows, int router_exact, cudaStream_t st) {
+                         uint16_t *xhat_out, int tile_rows, int router_exact, int store_mma, cudaStream_t st) {
     if (bp.H / 8 > kRouteThreads * kXC) return cudaErrorInvalidValue;
-    static bool done1 = false, done8 = false;
+    RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact, 0,
+                store_mma, 1.0 / (double)bp.H};
     if (T <= 32) {
-        RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact,
-                    route_epc(1, bp.H, bp.E)};
-        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<1>, done1));
-        dim3 grid(T, (bp.E + a.epc - 1) / a.epc);
-        moe_route_kernel<1><<<grid, kRouteThreads, route_smem_bytes(1, bp.H, bp.E), st>>>(a);
-    } else {
-        RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact,
-                    route_epc(8, bp.H, bp.E)};
-        MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8>, done8));
-        dim3 grid((T + 7) / 8, (bp.E + a.epc - 1) / a.epc);
-        moe_route_kernel<8><<<grid, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
+        const SmallGeo g = small_geo(bp.H, bp.E);
+        a.epc = g.epc;
+        MOE_CUDA_TRY(g.staged ? launch_small<true>(a, g, st) : launch_small<false>(a, g, st));
+        return cudaGetLastError();
     }
+    static bool done8 = false;
+    a.epc = route_epc(8, bp.H, bp.E);
+    MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8>, done8));
+    dim3 grid((T + 7) / 8, (bp.E + a.epc - 1) / a.epc);
+    moe_route_kernel<8><<<grid, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
     return cudaGetLastError();
 }
