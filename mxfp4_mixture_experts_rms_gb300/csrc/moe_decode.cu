@@ -8,8 +8,9 @@
 // outputs are summed in slot order and added to the residual in `forward`.
 //
 // Design (sm_103a), for each of the two projections:
-//  * one persistent CTA per SM: 15 consumer warps and 1 producer warp (16
-//    warps: 4 per SM sub-partition, up to 128 registers a thread);
+//  * one persistent CTA per SM: 14 consumer warps, 1 producer warp and 1
+//    epilogue warp (16 warps: 4 per SM sub-partition, up to 128 registers a
+//    thread);
 //  * work item = (tile of <= 8*NT routes of one expert, 16 weight rows); each
 //    CTA walks a contiguous range of items;
 //  * the producer streams every item into a ring of S shared-memory stages
@@ -26,8 +27,11 @@
 //    exactly; two m16n8k16 MMAs (fp32 accumulate) form the unscaled block dot
 //    product, which one FFMA per output multiplies by 2^(e-127) (exact) into
 //    the accumulator;
-//  * the 15 split-K partials meet in shared memory; a rotating consumer warp
-//    applies bias + clamped SwiGLU (gate/up) or bias x route weight (down).
+//  * the 14 split-K partials meet in shared memory; the epilogue warp sums
+//    them and applies bias + clamped SwiGLU (gate/up) or bias x route weight
+//    (down), off the consumers' critical path, while the producer warp does
+//    nothing but keep the copy engine busy (a bulk-copy issue blocks while the
+//    engine is saturated, so any other work there idles HBM).
 //
 // Activations are fp16 (x_hat and h are bf16 values; fp16 holds them exactly
 // for 2^-17 <= |v| < 65504) unless the plan found at load time that they can
@@ -42,10 +46,10 @@
 
 namespace {
 
-constexpr int kCW = 15;                      // consumer warps
-constexpr int kDecThreads = (kCW + 1) * 32;  // + 1 producer warp
-constexpr int kMaxPairs = 5;                 // block pairs per consumer warp: K <= 15 * 5 * 64 = 4800
-constexpr int kFewPairs = 3;                 // the variant for K <= 15 * 3 * 64 = 2880 (fewer registers)
+constexpr int kCW = 14;                      // consumer warps
+constexpr int kProd = kCW, kEpi = kCW + 1;   // producer warp, epilogue warp
+constexpr int kDecThreads = (kCW + 2) * 32;
+constexpr int kMaxPairs = 5;                 // block pairs per consumer warp: K <= 14 * 5 * 64 = 4480
 constexpr int kMaxStages = 8;
 constexpr uint64_t kDecWaitNs = 2000000000ull;
 
@@ -196,7 +200,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
         for (int i = 0; i < S; i++) {
             // one arrival with the codes' byte count + one per producer lane (its small copies)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 33;" ::"r"(smem_addr(&full[i])));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty[i])), "r"(kCW));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&empty[i])), "r"(kCW + 1));
         }
         for (int i = 0; i < 2; i++) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&redfull[i])), "r"(kCW));
@@ -208,8 +212,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     // Gate/up needs the routing kernel's results everywhere.  The down kernel
     // is let in only once every gate/up CTA has passed its own wait, so the
     // tile table is complete: its producer starts streaming weights at once
-    // (into the SMs gate/up has left) and only its consumers wait for h.
-    if (GATEUP || threadIdx.x < kCW * 32) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // (into the SMs gate/up has left) and only its consumers and epilogue wait
+    // for gate/up's results.
+    if (GATEUP || threadIdx.x < kCW * 32 || threadIdx.x >= kEpi * 32) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int n_items = *a.ws.n_tiles * RB;
     const int per = (n_items + gridDim.x - 1) / gridDim.x;
@@ -219,12 +224,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     const int E = a.bp.E;
     int32_t *status = a.ws.status;
 
-    if (warp == kCW) {
+    if (warp == kProd) {
         // ---------------------------------------------------------- producer
-        int issued = 0;
-        for (int k = 0; k < n; k++) {
+        auto issue = [&](int k) {
             const int s = k % S, item = begin + k;
-            if (k >= S && !dec_mbar_wait(&empty[s], ((k / S) - 1) & 1, status, 51)) break;
             const int4 tile = a.ws.tiles[item / RB];
             const int e = tile.x, j0 = (item % RB) * 16;
             unsigned char *st = dsm + (size_t)s * geo.stage;
@@ -249,11 +252,77 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
                 if (lane < 4) cp_async16(st + geo.bias + m * 64 + 16 * lane, mat_bias(M, e, E) + j0 + 4 * lane);
             }
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&full[s])) : "memory");
-            issued = k + 1;
             if (lane == 0) MOE_DEC_MARK(0, k);
+        };
+        for (int k = 0; k < n; k++) {
+            if (k >= S && !dec_mbar_wait(&empty[k % S], ((k / S) - 1) & 1, status, 51)) break;
+            issue(k);
         }
         // the copies still in flight must land before this warp exits
-        for (int k = max(0, issued - S); k < issued; k++) dec_mbar_wait(&full[k % S], (k / S) & 1, status, 52);
+        for (int k = max(0, n - S); k < n; k++) dec_mbar_wait(&full[k % S], (k / S) & 1, status, 52);
+        return;
+    }
+    if (warp == kEpi) {
+        // ---------------------------------------------------------- epilogue
+        for (int k = 0; k < n; k++) {
+            const int s = k % S, r = k & 1, item = begin + k;
+            // this item's biases, read before the stage may be refilled
+            if (!dec_mbar_wait(&full[s], (k / S) & 1, status, 55)) break;
+            const float *sb = reinterpret_cast<const float *>(dsm + (size_t)s * geo.stage + geo.bias);
+            const float b0 = sb[lane >> 1], b1 = GATEUP ? sb[16 + (lane >> 1)] : 0.f;
+            asm volatile("" ::"f"(b0), "f"(b1));
+            __syncwarp();
+            if (lane == 0) dec_arrive(&empty[s]);
+            if (!dec_mbar_wait(&redfull[r], (k >> 1) & 1, status, 54)) break;
+            if (lane == 0) MOE_DEC_MARK(3, k);
+            const int4 tile = a.ws.tiles[item / RB];
+            const int rstart = tile.y, rcount = tile.z, j0 = (item % RB) * 16;
+            // lane: row lane/2, columns 4*(lane&1) .. +3 of every column group nn
+            const int row = lane >> 1, c0 = 4 * (lane & 1);
+            const float *rr = red + (size_t)r * kCW * NM * NT * 128;
+#pragma unroll
+            for (int nn = 0; nn < NT; nn++) {
+                float4 sm[NM];
+#pragma unroll
+                for (int m = 0; m < NM; m++) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int w = 0; w < kCW; w++) {
+                        const float4 q =
+                            *reinterpret_cast<const float4 *>(rr + ((w * NM + m) * NT + nn) * 128 + row * 8 + c0);
+                        v.x += q.x;
+                        v.y += q.y;
+                        v.z += q.z;
+                        v.w += q.w;
+                    }
+                    sm[m] = v;
+                }
+                const float s0[4] = {sm[0].x, sm[0].y, sm[0].z, sm[0].w};
+                const float s1[4] = {sm[NM - 1].x, sm[NM - 1].y, sm[NM - 1].z, sm[NM - 1].w};
+                const int j = j0 + row;
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const int col = nn * 8 + c0 + c;  // route within the tile
+                    if (col >= rcount) continue;
+                    const int route = rstart + col;
+                    if (GATEUP) {
+                        const float hv = swiglu_clamped(s0[c] + b0, s1[c] + b1, a.bp.alpha, a.bp.limit);
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                        if (a.h_bf16) {
+                            a.ws.h[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&hb);
+                        } else {
+                            const __half h16 = __float2half_rn(__bfloat162float(hb));
+                            a.ws.h16[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&h16);
+                        }
+                    } else {
+                        a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * (s0[c] + b0);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) MOE_DEC_MARK(4, k);
+            if (lane == 0) dec_arrive(&redempty[r]);
+        }
         return;
     }
 
@@ -305,19 +374,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
                 for (int i = 0; i < MP; i++) load_pair(Bc[kRegB ? i : 0], i);
             }
         }
-        const int j0 = (item % RB) * 16;
         uint4 Bcur[2][NT], Bnext[2][NT];
         if (!kRegB) load_pair(Bcur, 0);
         if (!dec_mbar_wait(&full[s], (k / S) & 1, status, 50)) break;
         if (warp == 0 && lane == 0) MOE_DEC_MARK(1, k);
         const unsigned char *st = dsm + (size_t)s * geo.stage;
-        const bool epi = warp == (k % kCW);
-        float b0 = 0.f, b1 = 0.f;  // biases of row lane/2 (epilogue warp only), read before the stage is released
-        if (epi) {
-            const float *sb = reinterpret_cast<const float *>(st + geo.bias);
-            b0 = sb[lane >> 1];
-            if (GATEUP) b1 = sb[16 + (lane >> 1)];
-        }
         float acc[NM][NT][4];
 #pragma unroll
         for (int m = 0; m < NM; m++)
@@ -377,6 +438,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
         }
         __syncwarp();
         if (warp == 0 && lane == 0) MOE_DEC_MARK(2, k);
+        if (lane == 0) MOE_DEC_MARK(6 + warp, k);
         if (lane == 0) dec_arrive(&empty[s]);  // this warp no longer reads stage s
         if (k >= 2 && !dec_mbar_wait(&redempty[r], ((k >> 1) - 1) & 1, status, 53)) break;
         float *rw = red + (size_t)(r * kCW + warp) * NM * NT * 128;
@@ -390,55 +452,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
             }
         __syncwarp();
         if (lane == 0) dec_arrive(&redfull[r]);
-        if (epi) {
-            if (!dec_mbar_wait(&redfull[r], (k >> 1) & 1, status, 54)) break;
-            if (lane == 0) MOE_DEC_MARK(3, k);
-            // lane: row lane/2, columns 4*(lane&1) .. +3 of every column group nn
-            const int row = lane >> 1, c0 = 4 * (lane & 1);
-            const float *rr = red + (size_t)r * kCW * NM * NT * 128;
-#pragma unroll
-            for (int nn = 0; nn < NT; nn++) {
-                float4 sm[NM];
-#pragma unroll
-                for (int m = 0; m < NM; m++) {
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int w = 0; w < kCW; w++) {
-                        const float4 q =
-                            *reinterpret_cast<const float4 *>(rr + ((w * NM + m) * NT + nn) * 128 + row * 8 + c0);
-                        v.x += q.x;
-                        v.y += q.y;
-                        v.z += q.z;
-                        v.w += q.w;
-                    }
-                    sm[m] = v;
-                }
-                const float s0[4] = {sm[0].x, sm[0].y, sm[0].z, sm[0].w};
-                const float s1[4] = {sm[NM - 1].x, sm[NM - 1].y, sm[NM - 1].z, sm[NM - 1].w};
-                const int j = j0 + row;
-#pragma unroll
-                for (int c = 0; c < 4; c++) {
-                    const int col = nn * 8 + c0 + c;  // route within the tile
-                    if (col >= rcount) continue;
-                    const int route = rstart + col;
-                    if (GATEUP) {
-                        const float hv = swiglu_clamped(s0[c] + b0, s1[c] + b1, a.bp.alpha, a.bp.limit);
-                        const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                        if (a.h_bf16) {
-                            a.ws.h[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&hb);
-                        } else {
-                            const __half h16 = __float2half_rn(__bfloat162float(hb));
-                            a.ws.h16[(size_t)route * a.bp.F + j] = *reinterpret_cast<const uint16_t *>(&h16);
-                        }
-                    } else {
-                        a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * (s0[c] + b0);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) MOE_DEC_MARK(4, k);
-            if (lane == 0) dec_arrive(&redempty[r]);
-        }
     }
 }
 
@@ -549,14 +562,16 @@ static cudaError_t launch_one(DecodeArgs a, int n_items_max, cudaStream_t st) {
 
 // variant choice: bf16 activations, and the number of block pairs a warp covers
 // (fewer pairs, fewer registers for the activations of 8-route tiles)
+template <bool GATEUP, int NT, bool BF>
+static cudaError_t launch_mp(const DecodeArgs &a, int n_items_max, cudaStream_t st) {
+    const int ppw = ((a.Kdim / 32 + 1) / 2 + kCW - 1) / kCW;
+    if (ppw <= 3) return launch_one<GATEUP, NT, BF, 3>(a, n_items_max, st);
+    if (ppw <= 4) return launch_one<GATEUP, NT, BF, 4>(a, n_items_max, st);
+    return launch_one<GATEUP, NT, BF, kMaxPairs>(a, n_items_max, st);
+}
 template <bool GATEUP, int NT>
 static cudaError_t launch_bf(const DecodeArgs &a, bool bf, int n_items_max, cudaStream_t st) {
-    const bool few = (a.Kdim / 32 + 1) / 2 <= kCW * kFewPairs;
-    if (few)
-        return bf ? launch_one<GATEUP, NT, true, kFewPairs>(a, n_items_max, st)
-                  : launch_one<GATEUP, NT, false, kFewPairs>(a, n_items_max, st);
-    return bf ? launch_one<GATEUP, NT, true, kMaxPairs>(a, n_items_max, st)
-              : launch_one<GATEUP, NT, false, kMaxPairs>(a, n_items_max, st);
+    return bf ? launch_mp<GATEUP, NT, true>(a, n_items_max, st) : launch_mp<GATEUP, NT, false>(a, n_items_max, st);
 }
 
 }  // namespace

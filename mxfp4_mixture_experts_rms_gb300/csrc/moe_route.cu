@@ -40,7 +40,6 @@ namespace {
 
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
-constexpr int kMaxChunks = 16;  // router row chunks of 256 elements per lane held in registers (H <= 4096)
 
 struct RouteArgs {
     BlockParams bp;
@@ -572,9 +571,9 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     const int t = blockIdx.x;
     const uint32_t rank = cluster_ctarank();
     const int epc = a.epc, e0 = (int)rank * epc, ne = max(0, min(epc, E - e0));
-    // layout: [router rows | permutation counters] [x_hat row] [logits E] [bounds E] [exact logits E]
+    // layout: [router rows] [permutation counters] [x_hat row] [logits E] [bounds E] [exact logits E]
     const size_t rows_b = STAGED ? (size_t)epc * H * 2 : 0;
-    const size_t head = ((rows_b > perm_smem_bytes(E) ? rows_b : perm_smem_bytes(E)) + 127) & ~(size_t)127;
+    const size_t head = (rows_b + perm_smem_bytes(E) + 127) & ~(size_t)127;  // rows, then counters
     uint16_t *wsm = reinterpret_cast<uint16_t *>(smem);
     uint16_t *xh = reinterpret_cast<uint16_t *>(smem + head);
     float *lg = reinterpret_cast<float *>(smem + head + (size_t)H * 2);
@@ -680,7 +679,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     if (!s_flag) return;
     __threadfence();
     MOE_PHASE_MARK(6);
-    build_permutation(a, smem);
+    build_permutation(a, smem + rows_b);
     MOE_PHASE_MARK(7);
 }
 
@@ -861,7 +860,7 @@ SmallGeo small_geo(int H, int E) {
     g.C = (E + g.epc - 1) / g.epc;
     g.staged = (size_t)g.epc * H * 2 <= 160 * 1024;
     const size_t rows_b = g.staged ? (size_t)g.epc * H * 2 : 0;
-    const size_t head = ((rows_b > perm_smem_bytes(E) ? rows_b : perm_smem_bytes(E)) + 127) & ~(size_t)127;
+    const size_t head = (rows_b + perm_smem_bytes(E) + 127) & ~(size_t)127;
     g.smem = ((head + (size_t)H * 2 + 8 * (size_t)E + 7) & ~(size_t)7) + 8 * (size_t)E;
     return g;
 }
