@@ -283,25 +283,48 @@ __device__ void topk_token(const float *l, const float *bd, const uint16_t *xh, 
     uint32_t taken = 0;
     float my_v = -INFINITY;
     int my_i = kInvalid;
-    for (int r = 0; r <= K; r++) {
-        float bv = -INFINITY;
-        int bi = kInvalid;
+    if (E <= 32) {
+        // one logit per lane: its rank among the selectable ones (NaN and -inf
+        // never are) by 32 independent comparisons, then selection r moves to lane r
+        const float v = lv[0];
+        const bool ok_sel = lane < E && v > -INFINITY;
+        const uint32_t okm = __ballot_sync(0xffffffffu, ok_sel);
+        int rank = 0;
 #pragma unroll
-        for (int q = 0; q < NQ; q++) {
-            const int j = lane + 32 * q;
-            const float v = lv[q];
-            // NaN and -inf are never chosen
-            if (j < E && v > -INFINITY && !(taken >> q & 1u) && better(v, j, bv, bi)) {
-                bv = v;
-                bi = j;
+        for (int i = 0; i < 32; i++) {
+            const float vi = __shfl_sync(0xffffffffu, v, i);
+            rank += ((okm >> i) & 1u) && better(vi, i, v, lane);
+        }
+        for (int r = 0; r <= K; r++) {
+            const uint32_t mr = __ballot_sync(0xffffffffu, ok_sel && rank == r);
+            const int src = mr ? __ffs(mr) - 1 : 0;
+            const float vv = __shfl_sync(0xffffffffu, v, src);
+            if (lane == r && mr) {
+                my_v = vv;
+                my_i = src;
             }
         }
-        warp_best(bv, bi);
-        if (lane == r) {
-            my_v = bv;
-            my_i = bi;
+    } else {
+        for (int r = 0; r <= K; r++) {
+            float bv = -INFINITY;
+            int bi = kInvalid;
+#pragma unroll
+            for (int q = 0; q < NQ; q++) {
+                const int j = lane + 32 * q;
+                const float v = lv[q];
+                // NaN and -inf are never chosen
+                if (j < E && v > -INFINITY && !(taken >> q & 1u) && better(v, j, bv, bi)) {
+                    bv = v;
+                    bi = j;
+                }
+            }
+            warp_best(bv, bi);
+            if (lane == r) {
+                my_v = bv;
+                my_i = bi;
+            }
+            if (bi != kInvalid && (bi & 31) == lane) taken |= 1u << (bi >> 5);
         }
-        if (bi != kInvalid && (bi & 31) == lane) taken |= 1u << (bi >> 5);
     }
     // certification: selection r must beat selection r+1 by more than 2 dmax
     const float nx_v = __shfl_down_sync(0xffffffffu, my_v, 1);
@@ -523,6 +546,8 @@ __device__ __forceinline__ void router_logit(const uint16_t *wrow, const uint16_
                                              float &l, float &bound) {
     const int nchunk = H / 8, per_lane = (nchunk + 31) / 32, chain = 8 + per_lane + 6;
     float acc = 0.f, sab = 0.f;
+    // global rows: the loads of four chunks are issued before their use
+#pragma unroll 4
     for (int ch = lane; ch < nchunk; ch += 32) {
         const uint4 wv = GLOBAL_ROW ? __ldg(reinterpret_cast<const uint4 *>(wrow + 8 * ch))
                                     : *reinterpret_cast<const uint4 *>(wrow + 8 * ch);
@@ -848,15 +873,15 @@ size_t route_smem_bytes(int G, int H, int E) {
     return a > b ? a : b;
 }
 
-// Small-batch geometry: C CTAs per token (a cluster, C <= 8), epc experts each.
+// Small-batch geometry: C CTAs per token (a cluster, C <= cmax), epc experts each.
 struct SmallGeo {
     int C, epc;
     bool staged;
     size_t smem;
 };
-SmallGeo small_geo(int H, int E) {
+SmallGeo small_geo(int H, int E, int cmax) {
     SmallGeo g;
-    g.epc = E <= 8 * kRouteWarps ? kRouteWarps : (E + 7) / 8;  // one expert per warp while E <= 64
+    g.epc = E <= cmax * kRouteWarps ? kRouteWarps : (E + cmax - 1) / cmax;  // one expert per warp if possible
     g.C = (E + g.epc - 1) / g.epc;
     g.staged = (size_t)g.epc * H * 2 <= 160 * 1024;
     const size_t rows_b = g.staged ? (size_t)g.epc * H * 2 : 0;
@@ -867,8 +892,13 @@ SmallGeo small_geo(int H, int E) {
 
 template <bool STAGED>
 cudaError_t launch_small(const RouteArgs &a, const SmallGeo &g, cudaStream_t st) {
-    static bool done = false;
+    static bool done = false, nonportable = false;
     MOE_CUDA_TRY(smem_optin_once(moe_route_small_kernel<STAGED>, done));
+    if (g.C > 8 && !nonportable) {
+        MOE_CUDA_TRY(cudaFuncSetAttribute(moe_route_small_kernel<STAGED>,
+                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+        nonportable = true;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.T, g.C);
     cfg.blockDim = dim3(kRouteThreads);
@@ -884,6 +914,10 @@ cudaError_t launch_small(const RouteArgs &a, const SmallGeo &g, cudaStream_t st)
     return cudaLaunchKernelEx(&cfg, moe_route_small_kernel<STAGED>, a);
 }
 
+cudaError_t launch_small_geo(const RouteArgs &a, const SmallGeo &g, cudaStream_t st) {
+    return g.staged ? launch_small<true>(a, g, st) : launch_small<false>(a, g, st);
+}
+
 }  // namespace
 
 int route_ticket_count(int T) { return T + 1; }
@@ -895,9 +929,26 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
     RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact, 0,
                 store_mma, 1.0 / (double)bp.H};
     if (T <= 32) {
-        const SmallGeo g = small_geo(bp.H, bp.E);
+        // many experts: 16-CTA clusters (a non-portable size) keep every CTA's
+        // router rows in shared memory; where such a cluster cannot be
+        // launched, 8-CTA clusters read the rows from global memory
+        static int use16 = -1;
+        SmallGeo g = small_geo(bp.H, bp.E, 8);
+        if (!g.staged && use16 != 0) {
+            const SmallGeo g16 = small_geo(bp.H, bp.E, 16);
+            if (g16.staged) {
+                a.epc = g16.epc;
+                const cudaError_t e = launch_small_geo(a, g16, st);
+                if (e == cudaSuccess) {
+                    use16 = 1;
+                    return cudaSuccess;
+                }
+                cudaGetLastError();  // a launch-configuration error is not sticky
+                use16 = 0;
+            }
+        }
         a.epc = g.epc;
-        MOE_CUDA_TRY(g.staged ? launch_small<true>(a, g, st) : launch_small<false>(a, g, st));
+        MOE_CUDA_TRY(launch_small_geo(a, g, st));
         return cudaGetLastError();
     }
     static bool done8 = false;
