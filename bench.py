@@ -342,7 +342,7 @@ def run_ours(args, rank, world, local):
                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": avg_ms[dom]},
         "kernels": {KERNEL_SLOTS[k]: {"avg_us": 1e3 * avg_ms[k], "share": share[k], "launches": cnt[k]}
                     for k in range(4)},
-        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": 4 * args.steps,
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": int(sum(cnt)),
     }
     print(json.dumps(line), flush=True)
 
