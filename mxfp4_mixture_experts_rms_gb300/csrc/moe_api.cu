@@ -125,6 +125,7 @@ size_t carve(const moe_plan *p, int T, char *base, Workspace *ws) {
     w.h = c.take<uint16_t>(base, R * b.F);
     w.h16 = c.take<uint16_t>(base, R * b.F);
     w.y = c.take<float>(base, R * b.H);
+    w.xs = reinterpret_cast<uint16_t *>(w.y);
     w.logits = c.take<float>(base, (size_t)T * b.E);
     w.lbound = c.take<float>(base, (size_t)T * b.E);
     w.status = c.take<int32_t>(base, 4);
@@ -360,8 +361,10 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     mark(0, false);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     mark(1, true);
-    e = decode ? launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
-               : launch_prefill_stage(b, p->ws, p->gate, p->up, true, tokens, p->maps.gateup, st);
+    if (!decode) e = launch_gather(b, p->ws, tokens, st);
+    if (e == cudaSuccess)
+        e = decode ? launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
+                   : launch_prefill_stage(b, p->ws, p->gate, p->up, true, tokens, p->maps.gateup, st);
     mark(1, false);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
     mark(2, true);
@@ -514,8 +517,10 @@ int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, 
     e = launch_route(b, ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, nullptr, nullptr,
                      tile_rows, p->router_exact, decode ? 0 : 1, st);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
-    e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
-               : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, st);
+    if (!decode) e = launch_gather(b, ws, tokens, st);
+    if (e == cudaSuccess)
+        e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
+                   : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, st);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
     e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, st)
                : launch_prefill_stage(b, ws, p->down, p->down, false, tokens, p->maps.down, st);

@@ -55,6 +55,8 @@ struct Workspace {
     uint16_t *h;           // [R][F] bf16 (decode: natural order, bf16-activation plans only; prefill: pair order)
     uint16_t *h16;         // [R][F] fp16 h of the decode GEMVs (natural order)
     float *y;              // [R][H] weighted expert outputs
+    uint16_t *xs;          // [R][H] x_hat rows in route order, pair order (grouped GEMM operand; aliases y,
+                           //         which is written only after the gate/up GEMM has read these)
     float *logits;         // [T][E] router logits (fp32) of the routing kernel
     float *lbound;         // [T][E] their rounding-error bounds
     int32_t *status;       // [4] device error flag + detail
@@ -178,6 +180,8 @@ cudaError_t prefill_make_maps(const BlockParams &bp, const MatPtrs &gate, const 
                               PrefillMaps *out);
 cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
                                  const MatPtrs &a1, bool gateup, int T, const TmaMaps &maps, cudaStream_t st);
+// x_hat rows gathered into route order (ws.xs) for the grouped GEMM.
+cudaError_t launch_gather(const BlockParams &bp, const Workspace &ws, int T, cudaStream_t st);
 int prefill_tile_rows();
 cudaError_t launch_dequant(const MatPtrs &m, int expert, int n_experts, float *out, cudaStream_t st);
 cudaError_t launch_scan_scales(const uint8_t *scales, size_t n, int32_t *flag, cudaStream_t st);

@@ -15,12 +15,14 @@
 //   down kernel:    A = 128 rows of Wd, B = the tile's h rows;
 //                   epilogue: bias, times the route weight -> per-route fp32
 //
-// Warp roles (192 threads): warp 0 issues the TMA loads of the packed codes;
+// Warp roles (192 threads): warp 0 issues the TMA loads of the packed codes
+// and of the B tile (128-byte swizzled, straight into the MMA layout; the
+// x_hat rows are first gathered into route order by moe_gather_kernel);
 // warp 1 owns TMEM and issues the MMAs (one elected lane); warps 2..5
-// dequantise A, stage B, and run the epilogue.  A 4-stage mbarrier ring
-// connects them.  Activations use the same 32-block pair order as the decode
-// path (x_hat_mma / h), and A is written in that order straight from the
-// nibble-pair dequantiser, so the K permutation cancels in every dot product.
+// dequantise A and run the epilogue.  A 4-stage mbarrier ring connects them.
+// Activations use a 32-block pair order (x_hat_mma / h), and A is written in
+// that order straight from the nibble-pair dequantiser, so the K permutation
+// cancels in every dot product.
 //
 // Every wait is bounded (about 2 s of %globaltimer); on a timeout the kernel
 // records MOE_DEV_WAIT_TIMEOUT in the status word, drains what it issued,
@@ -186,15 +188,16 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 
 template <bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_constant__ PrefillArgs a,
-                                                                    const __grid_constant__ TmaMaps maps) {
+                                                                    const __grid_constant__ TmaMaps maps,
+                                                                    const __grid_constant__ CUtensorMap bmap) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *sA = smem;                                   // [kStages][128 rows][128 B] swizzled
     unsigned char *sB = sA + kStages * kABytes;                 // [kStages][kBN rows][128 B] swizzled
     unsigned char *sF = sB + kStages * kBBytes;                 // [kStages][128 rows][32 B] packed codes
     uint64_t *bars = reinterpret_cast<uint64_t *>(sF + kStages * kFp4Bytes);
-    uint64_t *full_fp4 = bars, *full_ab = bars + kStages, *empty = bars + 2 * kStages;
-    uint64_t *acc_full = bars + 3 * kStages, *drain = acc_full + 1;
+    uint64_t *full_fp4 = bars, *full_ab = bars + kStages, *empty = bars + 2 * kStages, *full_b = bars + 3 * kStages;
+    uint64_t *acc_full = bars + 4 * kStages, *drain = acc_full + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
     const int tile_idx = blockIdx.x;
@@ -211,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
         for (int s = 0; s < kStages; s++) {
             mbar_init(&full_fp4[s], 1);
             mbar_init(&full_ab[s], 4);
+            mbar_init(&full_b[s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
@@ -239,6 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                 const int s = kb % kStages;
                 if (kb >= kStages) ok = mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, status, 10);
                 if (!ok) break;
+                // B: the tile's 128 activation rows (rows past the tile belong to other
+                // tiles or lie outside the tensor, read as zeros: their columns are ignored)
+                mbar_expect_tx(&full_b[s], kBBytes);
+                tma_load_2d(sB + s * kBBytes, &bmap, &full_b[s], kb * kBK, rstart);
                 mbar_expect_tx(&full_fp4[s], kFp4Bytes);
                 unsigned char *dst = sF + s * kFp4Bytes;
                 if (GATEUP) {
@@ -251,8 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                 issued_upto = kb + 1;
             }
             // make sure every copy this thread issued has landed before exiting
-            for (int kb = max(0, issued_upto - kStages); kb < issued_upto; kb++)
+            for (int kb = max(0, issued_upto - kStages); kb < issued_upto; kb++) {
                 mbar_wait(&full_fp4[kb % kStages], (kb / kStages) & 1, status, 11);
+                mbar_wait(&full_b[kb % kStages], (kb / kStages) & 1, status, 12);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -262,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
             bool ok = true;
             for (int kb = 0; kb < nkb; kb++) {
                 const int s = kb % kStages;
-                ok = mbar_wait(&full_ab[s], (kb / kStages) & 1, status, 20);
+                ok = mbar_wait(&full_ab[s], (kb / kStages) & 1, status, 20) &&
+                     mbar_wait(&full_b[s], (kb / kStages) & 1, status, 22);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(sA + s * kABytes), b_addr = smem_u32(sB + s * kBBytes);
@@ -293,7 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
             wrow = mt * 128 + t;
         const bool row_ok = wrow < a.rows;
         const uint8_t *srow = mat_scales(M, e, E) + (size_t)(row_ok ? wrow : 0) * nb;
-        const uint16_t *bsrc_base = GATEUP ? a.ws.xhat_mma : a.ws.h;
+        // this row's two scale bytes per k-block, loaded four k-blocks ahead
+        auto ldsc = [&](int k) -> uint32_t {
+            return (k < nkb && row_ok) ? ((uint32_t)__ldg(srow + 2 * k) | ((uint32_t)__ldg(srow + 2 * k + 1) << 8))
+                                       : 0x7F7Fu;
+        };
+        uint32_t q0 = ldsc(0), q1 = ldsc(1), q2 = ldsc(2), q3 = ldsc(3);
         bool ok = true;
         for (int kb = 0; kb < nkb; kb++) {
             const int s = kb % kStages;
@@ -301,20 +317,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                 ok = mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, status, 30);
                 if (!ok) break;
             }
-            // B: rcount rows x 8 chunks of 16 bytes, gathered (gate/up) or contiguous (down)
-            unsigned char *bdst = sB + s * kBBytes;
-            for (int i = t; i < rcount * 8; i += 128) {
-                const int r = i >> 3, c = i & 7;
-                const size_t row = GATEUP ? (size_t)a.ws.perm_token[rstart + r] : (size_t)(rstart + r);
-                const uint4 v = *reinterpret_cast<const uint4 *>(bsrc_base + row * K + kb * kBK + c * 8);
-                *reinterpret_cast<uint4 *>(bdst + sw128(r, c)) = v;
-            }
+            const uint32_t sc0 = q0 & 0xFFu, sc1 = q0 >> 8;
+            q0 = q1;
+            q1 = q2;
+            q2 = q3;
+            q3 = ldsc(kb + 4);
             // A: wait for the packed codes, dequantise row t
             ok = mbar_wait(&full_fp4[s], (kb / kStages) & 1, status, 31);
             if (!ok) break;
             const uint4 *src = reinterpret_cast<const uint4 *>(sF + s * kFp4Bytes + t * 32);
             const uint4 c0 = src[0], c1 = src[1];
-            uint32_t sc0 = row_ok ? srow[2 * kb] : 127u, sc1 = row_ok ? srow[2 * kb + 1] : 127u;
             const bool big = (sc0 > 128u) || (sc1 > 128u);
             const uint32_t l0 = scale_lo(sc0), h0 = scale_hi(sc0), l1 = scale_lo(sc1), h1 = scale_hi(sc1);
             unsigned char *adst = sA + s * kABytes;
@@ -351,7 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                     const int j = mt * 64 + lrow;
                     const float bg = mat_bias(a.A0, e, E)[j], bu = mat_bias(a.A1, e, E)[j];
                     const int pj = mma_perm_pos(j);
-                    for (int c = 0; c < 32 && c0 + c < rcount; c++) {
+#pragma unroll
+                    for (int c = 0; c < 32; c++) {
+                        if (c0 + c >= rcount) continue;
                         const float hv = swiglu_clamped(v[c] + bg, xch[lrow * 33 + c] + bu, a.bp.alpha, a.bp.limit);
                         __nv_bfloat16 hb = __float2bfloat16_rn(hv);
                         a.ws.h[(size_t)(rstart + c0 + c) * a.bp.F + pj] = *reinterpret_cast<uint16_t *>(&hb);
@@ -362,7 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                 const int i = mt * 128 + lrow;
                 if (i < a.rows) {
                     const float bd = mat_bias(a.A0, e, E)[i];
-                    for (int c = 0; c < 32 && c0 + c < rcount; c++) {
+#pragma unroll
+                    for (int c = 0; c < 32; c++) {
+                        if (c0 + c >= rcount) continue;
                         const int route = rstart + c0 + c;
                         a.ws.y[(size_t)route * a.bp.H + i] = a.ws.perm_w[route] * (v[c] + bd);
                     }
@@ -407,6 +423,31 @@ cudaError_t make_codes_map(CUtensorMap *m, const uint8_t *codes, size_t n_rows, 
 
 size_t prefill_smem_bytes() { return 1024 + kStages * (kABytes + kBBytes + kFp4Bytes) + 256; }
 
+// 2D map over a bf16 activation matrix [rows][K]: box 64 elements (128 B) x 128
+// rows, 128-byte swizzle (the K-major layout the MMA descriptors expect).
+cudaError_t make_act_map(CUtensorMap *m, const uint16_t *base, int rows, int K) {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBN};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// xs[pos] = x_hat_mma[perm_token[pos]] (16-byte chunks), pos < R.
+__global__ void __launch_bounds__(256) moe_gather_kernel(Workspace ws, int H, int R) {
+    const int cpr = H / 8;  // 16-byte chunks per row
+    const size_t n = (size_t)R * cpr;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int pos = (int)(i / cpr), c = (int)(i - (size_t)pos * cpr);
+        const int tok = ws.perm_token[pos];
+        reinterpret_cast<uint4 *>(ws.xs + (size_t)pos * H)[c] =
+            reinterpret_cast<const uint4 *>(ws.xhat_mma + (size_t)tok * H)[c];
+    }
+}
+
 }  // namespace
 
 int prefill_tile_rows() { return kBN; }
@@ -427,10 +468,21 @@ cudaError_t prefill_make_maps(const BlockParams &bp, const MatPtrs &gate, const 
     return cudaSuccess;
 }
 
+cudaError_t launch_gather(const BlockParams &bp, const Workspace &ws, int T, cudaStream_t st) {
+    const int R = T * (bp.K + bp.n_shared);
+    const size_t n = (size_t)R * (bp.H / 8);
+    const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    moe_gather_kernel<<<blocks, 256, 0, st>>>(ws, bp.H, R);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0, const MatPtrs &a1,
                                  bool gateup, int T, const TmaMaps &maps, cudaStream_t st) {
     PrefillArgs args{bp, ws, a0, a1, gateup ? bp.H : bp.F, gateup ? bp.F : bp.H};
     const int R = T * (bp.K + bp.n_shared);
+    CUtensorMap bmap;
+    MOE_CUDA_TRY(get_encoder());
+    MOE_CUDA_TRY(make_act_map(&bmap, gateup ? ws.xs : ws.h, R, args.Kdim));
     int tiles = (R + kBN - 1) / kBN + bp.E + bp.n_shared;
     if (tiles > ws.max_tiles) tiles = ws.max_tiles;
     const int mtiles = gateup ? bp.F / 64 : (bp.H + 127) / 128;
@@ -438,10 +490,10 @@ cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, con
     static bool done_gu = false, done_dn = false;
     if (gateup) {
         MOE_CUDA_TRY(smem_optin_once(moe_prefill_kernel<true>, done_gu));
-        moe_prefill_kernel<true><<<dim3(tiles, mtiles), kThreads, sm, st>>>(args, maps);
+        moe_prefill_kernel<true><<<dim3(tiles, mtiles), kThreads, sm, st>>>(args, maps, bmap);
     } else {
         MOE_CUDA_TRY(smem_optin_once(moe_prefill_kernel<false>, done_dn));
-        moe_prefill_kernel<false><<<dim3(tiles, mtiles), kThreads, sm, st>>>(args, maps);
+        moe_prefill_kernel<false><<<dim3(tiles, mtiles), kThreads, sm, st>>>(args, maps, bmap);
     }
     return cudaGetLastError();
 }

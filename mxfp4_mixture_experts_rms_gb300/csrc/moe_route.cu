@@ -20,10 +20,9 @@
 // In both, the last token-owning CTA to finish (atomic ticket, never a wait)
 // builds the permutation.
 //
-// Exactness.  Σx² is accumulated exactly as a 128-bit fixed-point integer
-// (bf16 squares have 16-bit significands), rounded once to double, and
-// r = 1/sqrt(ms + eps) is evaluated in double, matching a plain double
-// evaluation.  x_hat = bf16(x * r * gamma) is computed in fp32 and recomputed
+// Accuracy.  Σx² is summed from exact fp32 squares with error-free two-sums
+// (relative error ~2^-44, the order of the reference's own double-sum
+// rounding) and r = 1/sqrt(ms + eps) is evaluated in double.  x_hat = bf16(x * r * gamma) is computed in fp32 and recomputed
 // in fp64 whenever the fp32 value lies within its error bound of a bf16
 // rounding midpoint.  Router logits are accumulated in fp32 with a rigorous
 // error bound; when the bounds cannot certify top-k membership and order, the
@@ -133,114 +132,130 @@ __device__ void warp_exclusive_scan(const int32_t *in, int32_t *out, int n, int 
     if (lane == 31) out[n] = incl;
 }
 
-// 128-bit unsigned accumulator (hi:lo)
-struct U128 {
-    unsigned long long lo, hi;
-};
-__device__ __forceinline__ void u128_add(U128 &a, const U128 &b) {
-    unsigned long long lo = a.lo + b.lo;
-    a.hi += b.hi + (lo < a.lo ? 1ull : 0ull);
-    a.lo = lo;
-}
-__device__ __forceinline__ U128 u128_shfl_xor(const U128 &a, int o) {
-    U128 r;
-    r.lo = __shfl_xor_sync(0xffffffffu, a.lo, o);
-    r.hi = __shfl_xor_sync(0xffffffffu, a.hi, o);
-    return r;
-}
-
 constexpr int kXC = 2;  // 16-byte chunks of one x row per thread (H <= 8 * 256 * kXC)
 
-// Exact Σx² of one bf16 row held in registers (kXC chunks of 8 per thread),
-// rounded once to double.  Squares are placed on a fixed-point grid relative
-// to the largest exponent of the row; a square more than 80 binary places
-// below the largest one (|x| < 2^-40 max|x|) contributes less than 2^-60 of
-// the sum and is dropped, far below double precision.
-__device__ double sumsq_exact(const uint4 (&xv)[kXC], int lane, int warp, int *s_maxexp, U128 *s_acc) {
-    int mx = 0;
+// Σx² of a bf16 row, to ~2^-44 relative (the reference statistic is itself a
+// double sum whose rounding is of that order).  Every value is scaled by
+// 2^(127 - emax), emax the row's largest exponent field, which is exact and
+// keeps the squares in fp32 range; squares of bf16 values are exact in fp32;
+// they are summed with error-free two-sums (Knuth), the error terms carried
+// alongside.
+struct Comp {
+    float s, c;
+};
+__device__ __forceinline__ void comp_add(Comp &a, float x) {
+    const float t = __fadd_rn(a.s, x);
+    const float z = __fadd_rn(t, -a.s);
+    a.c = __fadd_rn(a.c, __fadd_rn(__fadd_rn(a.s, -__fadd_rn(t, -z)), __fadd_rn(x, -z)));
+    a.s = t;
+}
+__device__ __forceinline__ void comp_merge(Comp &a, const Comp &b) {
+    comp_add(a, b.s);
+    a.c = __fadd_rn(a.c, b.c);
+}
+__device__ __forceinline__ Comp comp_warp(Comp a) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        Comp b;
+        b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+        b.c = __shfl_xor_sync(0xffffffffu, a.c, o);
+        comp_merge(a, b);
+    }
+    return a;
+}
+__device__ __forceinline__ int bf16_exp(uint32_t b) { return (int)((b >> 7) & 0xFFu); }
+// 2^(127 - emax) as fp32 (subnormal for emax = 254: exact all the same)
+__device__ __forceinline__ float exp_scale(int emax) {
+    const int k = 127 - emax + 127;  // biased exponent of the scale
+    return k >= 1 ? __uint_as_float((uint32_t)k << 23) : __uint_as_float(0x00400000u >> (-k));
+}
+__device__ __forceinline__ void comp_add_pair(Comp &a, uint32_t w2, float sc) {
+    const float v0 = __fmul_rn(__uint_as_float(w2 << 16), sc), v1 = __fmul_rn(__uint_as_float(w2 & 0xFFFF0000u), sc);
+    comp_add(a, __fmul_rn(v0, v0));
+    comp_add(a, __fmul_rn(v1, v1));
+}
+__device__ __forceinline__ double comp_result(const Comp &a, int emax) {
+    return ldexp((double)a.s + (double)a.c, 2 * (emax - 127));
+}
+
+// Σx² of one bf16 row (H elements, shared memory) by one warp; every lane gets it.
+__device__ double sumsq_row(const uint16_t *row, int H, int lane) {
+    const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
+    int mx = 1;
+    for (int c = lane; c < H / 8; c += 32) {
+        const uint4 v = r4[c];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; q++) mx = max(mx, max(bf16_exp(w[q]), bf16_exp(w[q] >> 16)));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float sc = exp_scale(mx);
+    Comp acc[2] = {{0.f, 0.f}, {0.f, 0.f}};  // two independent chains
+    for (int c = lane; c < H / 8; c += 32) {
+        const uint4 v = r4[c];
+        comp_add_pair(acc[0], v.x, sc);
+        comp_add_pair(acc[1], v.y, sc);
+        comp_add_pair(acc[0], v.z, sc);
+        comp_add_pair(acc[1], v.w, sc);
+    }
+    comp_merge(acc[0], acc[1]);
+    return comp_result(comp_warp(acc[0]), mx);
+}
+
+// Σx² of one bf16 row held in registers by the whole CTA (kXC chunks of 8 per
+// thread); every thread gets it.
+__device__ double sumsq_block(const uint4 (&xv)[kXC], int lane, int warp, int *s_maxexp, Comp *s_acc) {
+    int mx = 1;
 #pragma unroll
     for (int j = 0; j < kXC; j++) {
-        const uint32_t w4[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
-        for (int q = 0; q < 4; q++) mx = max(mx, (int)max((w4[q] >> 7) & 0xFFu, (w4[q] >> 23) & 0xFFu));
+        for (int q = 0; q < 4; q++) mx = max(mx, max(bf16_exp(w[q]), bf16_exp(w[q] >> 16)));
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) s_maxexp[warp] = mx;
     __syncthreads();
-    int emax = 1;
 #pragma unroll
-    for (int w = 0; w < kRouteWarps; w++) emax = max(emax, s_maxexp[w]);
-    // value = M * 2^(ex - 134) with M = 128 + mant (ex >= 1) or M = mant (ex == 0, exponent taken as 1)
-    U128 acc{0ull, 0ull};
+    for (int w = 0; w < kRouteWarps; w++) mx = max(mx, s_maxexp[w]);
+    const float sc = exp_scale(mx);
+    Comp acc{0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < kXC; j++) {
-        const uint32_t w4[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const uint32_t b = (w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
-            const int ex = (b >> 7) & 0xFF;
-            const uint32_t M = ex ? (128u + (b & 0x7Fu)) : (b & 0x7Fu);
-            const int d = 2 * (emax - (ex ? ex : 1));
-            if (M == 0 || d > 80) continue;
-            const unsigned long long v = (unsigned long long)M * M;  // < 2^16
-            const int sh = 80 - d;                                  // 0..80
-            U128 t;
-            if (sh == 0) {
-                t.lo = v;
-                t.hi = 0;
-            } else if (sh < 64) {
-                t.lo = v << sh;
-                t.hi = v >> (64 - sh);
-            } else {
-                t.lo = 0;
-                t.hi = v << (sh - 64);
-            }
-            u128_add(acc, t);
-        }
+        comp_add_pair(acc, xv[j].x, sc);
+        comp_add_pair(acc, xv[j].y, sc);
+        comp_add_pair(acc, xv[j].z, sc);
+        comp_add_pair(acc, xv[j].w, sc);
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) u128_add(acc, u128_shfl_xor(acc, o));
+    acc = comp_warp(acc);
     if (lane == 0) s_acc[warp] = acc;
     __syncthreads();
-    U128 tot{0ull, 0ull};
+    Comp tot = s_acc[0];
 #pragma unroll
-    for (int w = 0; w < kRouteWarps; w++) u128_add(tot, s_acc[w]);
-    if (tot.hi == 0 && tot.lo == 0) return 0.0;
-    // value = tot * 2^(2*(emax - 134) - 80); take the top 64 significant bits and round to 53 (ties to even)
-    const int lz = tot.hi ? __clzll((long long)tot.hi) : 64 + __clzll((long long)tot.lo);
-    const int width = 128 - lz;  // significant bits of tot (<= 108)
-    unsigned long long top;
-    bool sticky;
-    int shift;  // tot = top * 2^shift (+ sticky part)
-    if (width > 64) {
-        shift = width - 64;
-        top = (tot.hi << (64 - shift)) | (tot.lo >> shift);
-        sticky = (tot.lo << (64 - shift)) != 0ull;
-    } else {
-        shift = width - 64;  // <= 0
-        top = (width == 64) ? tot.lo : (tot.lo << (-shift));
-        sticky = false;
-    }
-    unsigned long long mant = top >> 11;
-    const unsigned long long rem = top & 0x7FFull;
-    if (rem > 0x400ull || (rem == 0x400ull && (sticky || (mant & 1ull)))) mant += 1ull;
-    return ldexp((double)mant, 11 + shift + 2 * (emax - 134) - 80);
+    for (int w = 1; w < kRouteWarps; w++) comp_merge(tot, s_acc[w]);
+    return comp_result(tot, mx);
 }
 
 // bf16(x * r * gamma) of one element: fp32 value, recomputed in fp64 when it
 // lies within its error bound (3 fp32 ulps; 8 used) of a bf16 rounding midpoint.
+// The fp64 evaluation sits in a function of its own: inlined, the compiler
+// may evaluate it for every element (fp64 throughput is a small fraction of
+// fp32 here) instead of branching to it for the rare uncertain one.
+__device__ __noinline__ uint32_t norm_elem_fp64(uint32_t xb, float gf, double r) {
+    return bf16_from_double_rne((double)__uint_as_float(xb << 16) * r * (double)gf);
+}
 __device__ __forceinline__ uint32_t norm_elem(uint32_t xb, float gf, float r32, double r) {
     const float xf = __uint_as_float(xb << 16);
     const float v32 = (xf * r32) * gf;
     const uint32_t low = __float_as_uint(v32) & 0xFFFFu;
     const bool safe =
         fabsf(v32) >= 0x1p-120f && fabsf(v32) < 0x1p126f && (low > 0x8000u + 8u || low + 8u < 0x8000u);
-    if (safe) {
+    if (__builtin_expect(safe, 1)) {
         __nv_bfloat16 bb = __float2bfloat16_rn(v32);
         return *reinterpret_cast<uint16_t *>(&bb);
     }
-    return bf16_from_double_rne((double)xf * r * (double)gf);
+    return norm_elem_fp64(xb, gf, r);
 }
 
 // 1/sqrt(m) in double: Newton steps from the fp32 seed (two steps take its
@@ -392,15 +407,18 @@ __device__ void topk_token(const float *l, const float *bd, const uint16_t *xh, 
 }
 
 // Bytes of shared memory the permutation needs (per-expert counters).
-__host__ __device__ constexpr size_t perm_smem_bytes(int E) { return (size_t)(5 * 264 + kRouteWarps * (E + 1)) * 4; }
+__host__ __device__ constexpr size_t perm_smem_bytes(int E, int warps = kRouteWarps) {
+    return (size_t)(5 * 264 + warps * (E + 1)) * 4;
+}
 
 // The token->expert permutation (goosedump gpt_oss.rs `mixture_of_experts_batch`:
 // routes appended per expert in token order): per-expert histogram, exclusive
 // prefix sums of counts and of tiles, stable scatter of (token, slot, weight),
-// the inverse map and the tile table.  Run by one CTA once every token's ids
-// are in global memory.
+// the inverse map and the tile table.  Run by one CTA (any multiple of 32
+// threads) once every token's ids are in global memory.
 __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int NTH = blockDim.x, NW = NTH >> 5;
     const int E = a.bp.E, K = a.bp.K;
     const int ns = a.bp.n_shared;
     const int EE = E + ns;
@@ -411,13 +429,13 @@ __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
     int32_t *run = offs + 264;
     int32_t *tcnt = run + 264;
     int32_t *toff = tcnt + 264;
-    int32_t *wcnt = toff + 264;  // [kRouteWarps][EE]
-    for (int e = tid; e < EE; e += kRouteThreads) {
+    int32_t *wcnt = toff + 264;  // [NW][EE]
+    for (int e = tid; e < EE; e += NTH) {
         cnt[e] = 0;
         run[e] = 0;
     }
     __syncthreads();
-    for (int r = tid; r < R; r += kRouteThreads) {
+    for (int r = tid; r < R; r += NTH) {
         int e = __ldcg(a.ws.ids + r);
         if ((unsigned)e >= (unsigned)E) {
             set_device_error(a.ws.status, MOE_DEV_BAD_ROUTE, r);
@@ -435,7 +453,7 @@ __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
         warp_exclusive_scan(tcnt, toff, EE, lane);
     }
     __syncthreads();
-    for (int e = tid; e < EE; e += kRouteThreads) {
+    for (int e = tid; e < EE; e += NTH) {
         if (e < E) a.ws.counts[e] = cnt[e];
         a.ws.offsets[e] = offs[e];
         const int n = tcnt[e], base = toff[e];
@@ -450,8 +468,8 @@ __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
         if (toff[EE] > a.ws.max_tiles) set_device_error(a.ws.status, MOE_DEV_BAD_ROUTE, -1);
     }
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int base = 0; base < R; base += kRouteThreads) {
-        for (int i = tid; i < kRouteWarps * EE; i += kRouteThreads) wcnt[i] = 0;
+    for (int base = 0; base < R; base += NTH) {
+        for (int i = tid; i < NW * EE; i += NTH) wcnt[i] = 0;
         __syncthreads();
         const int r = base + tid;
         int e = -1;
@@ -474,15 +492,15 @@ __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
             a.ws.loc[t * KK + s] = pos;
         }
         __syncthreads();
-        for (int x = tid; x < EE; x += kRouteThreads) {
+        for (int x = tid; x < EE; x += NTH) {
             int s = 0;
-            for (int w = 0; w < kRouteWarps; w++) s += wcnt[w * EE + x];
+            for (int w = 0; w < NW; w++) s += wcnt[w * EE + x];
             run[x] += s;
         }
         __syncthreads();
     }
     if (ns) {
-        for (int t = tid; t < a.T; t += kRouteThreads) {
+        for (int t = tid; t < a.T; t += NTH) {
             const int pos = offs[E] + t;
             a.ws.perm_token[pos] = t;
             a.ws.perm_slot[pos] = K;
@@ -570,6 +588,57 @@ __device__ __forceinline__ void router_logit(const uint16_t *wrow, const uint16_
     bound = 2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
 }
 
+// Router logits of one expert row (shared memory) for up to 8 x_hat rows
+// (shared memory, tokens g0, g0 + gstep, ...), by one warp: the arithmetic of
+// router_logit with the row's 16-byte chunks loaded once for all tokens.
+__device__ __forceinline__ void router_logits_tokens(const uint16_t *wrow, const uint16_t *xh, int H, int g0,
+                                                     int gstep, int nt, float b, int lane, float *lg_row,
+                                                     float *lb_row, int E) {
+    const int nchunk = H / 8, per_lane = (nchunk + 31) / 32, chain = 8 + per_lane + 6;
+    float acc[8], sab[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) acc[j] = sab[j] = 0.f;
+    for (int ch = lane; ch < nchunk; ch += 32) {
+        const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + 8 * ch);
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+        float wf[8];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            wf[2 * q] = __uint_as_float(ww[q] << 16);
+            wf[2 * q + 1] = __uint_as_float(ww[q] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const int g = g0 + j * gstep;
+            if (g >= nt) break;
+            const uint4 xq = *reinterpret_cast<const uint4 *>(xh + (size_t)g * H + 8 * ch);
+            const uint32_t xx[4] = {xq.x, xq.y, xq.z, xq.w};
+            float cs = 0.f, ab = sab[j];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const float x0 = __uint_as_float(xx[q] << 16), x1 = __uint_as_float(xx[q] & 0xFFFF0000u);
+                cs = fmaf(x0, wf[2 * q], cs);
+                cs = fmaf(x1, wf[2 * q + 1], cs);
+                ab = fmaf(fabsf(x0), fabsf(wf[2 * q]), ab);
+                ab = fmaf(fabsf(x1), fabsf(wf[2 * q + 1]), ab);
+            }
+            acc[j] += cs;
+            sab[j] = ab;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const int g = g0 + j * gstep;
+        if (g >= nt) break;
+        const float sm = warp_sum_f(acc[j]), ab = warp_sum_f(sab[j]);
+        if (lane == 0) {
+            const float l = sm + b;
+            lg_row[(size_t)g * E] = l;
+            lb_row[(size_t)g * E] = 2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
+        }
+    }
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -605,7 +674,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     float *lb = lg + E;
     double *exs = reinterpret_cast<double *>(smem + ((head + (size_t)H * 2 + 8 * (size_t)E + 7) & ~(size_t)7));
     __shared__ int s_maxexp[kRouteWarps];
-    __shared__ U128 s_acc[kRouteWarps];
+    __shared__ Comp s_acc[kRouteWarps];
     __shared__ double s_r;
     __shared__ int s_flag;
     __shared__ __align__(8) uint64_t wbar;
@@ -641,7 +710,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
         gm[j][0] = c < nchunk ? __ldg(g4) : make_float4(0.f, 0.f, 0.f, 0.f);
         gm[j][1] = c < nchunk ? __ldg(g4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const double ss = sumsq_exact(xv, lane, warp, s_maxexp, s_acc);
+    const double ss = sumsq_block(xv, lane, warp, s_maxexp, s_acc);
     MOE_PHASE_MARK(1);
     if (tid == 0) s_r = rsqrt_d(ss * a.inv_h + a.bp.eps);
     __syncthreads();
@@ -708,169 +777,163 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     MOE_PHASE_MARK(7);
 }
 
-// Larger batches: grid (token groups of G tokens) x (expert chunks of epc experts).
-template <int G>
-__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(RouteArgs a) {
+// Larger batches: one CTA of 8 warps per 8 tokens covers every expert.  Warp
+// w normalises token w (in its own x_hat row in shared memory); the
+// router rows stream through a double-buffered ring of RC rows (bulk copies);
+// warp w computes expert w % RC for the tokens g with g % (8/RC) == w / RC;
+// warp w then selects token w's top-k.  The permutation follows as a kernel
+// of its own.
+constexpr int kBatchTokens = kRouteWarps;
+
+__host__ __device__ inline size_t batch_rows_off(int H) { return (size_t)kBatchTokens * H * 2; }
+__host__ __device__ inline size_t batch_lg_off(int H, int RC) { return batch_rows_off(H) + (size_t)2 * RC * H * 2; }
+__host__ __device__ inline size_t batch_gm_off(int H, int E, int RC) {
+    return batch_lg_off(H, RC) + (size_t)kBatchTokens * E * 8;  // logits + bounds; exact logits reuse the ring
+}
+__host__ __device__ inline size_t batch_smem(int H, int E, int RC) { return batch_gm_off(H, E, RC) + (size_t)H * 4; }
+
+__global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArgs a, int RC) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int H = a.bp.H, E = a.bp.E;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int epc = a.epc;                                                        // experts per CTA
-    uint16_t *wsm = reinterpret_cast<uint16_t *>(smem);                           // [epc][H] router rows
-    uint16_t *xh = wsm + (size_t)epc * H;                                         // [G][H] x_hat
-    float *lg = reinterpret_cast<float *>(xh + (size_t)G * H);                    // [G][epc] logits
-    float *lb = lg + G * epc;                                                     // [G][epc] bounds
-    double *exs = reinterpret_cast<double *>(lb + G * epc) + (size_t)warp * E;  // [warps][E] exact logits
-    __shared__ int s_maxexp[kRouteWarps];
-    __shared__ U128 s_acc[kRouteWarps];
-    __shared__ double s_r;
-    __shared__ int s_flag;
-    __shared__ __align__(8) uint64_t wbar;
-
-    const int t0 = blockIdx.x * G;
-    const int nt = min(G, a.T - t0);
-    const int e0 = blockIdx.y * epc, ne = min(epc, E - e0);
-    const int nchunk = H / 8;  // 16-byte chunks per row
-
-    // router rows of this CTA's experts: one contiguous range, bulk-copied during the norm
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar)));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        const size_t bytes = (size_t)ne * H * 2;
-        asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(smem_u32(&wbar)),
-                     "r"((uint32_t)bytes)
+    const int t0 = blockIdx.x * kBatchTokens, nt = min(kBatchTokens, a.T - t0);
+    uint16_t *xh = reinterpret_cast<uint16_t *>(smem);                                  // [8][H]
+    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + batch_rows_off(H));            // [2][RC][H]
+    float *lg = reinterpret_cast<float *>(smem + batch_lg_off(H, RC));                  // [8][E]
+    float *lb = lg + kBatchTokens * E;                                                  // [8][E]
+    double *exs = reinterpret_cast<double *>(ring);                                     // [8][E] after the ring
+    __shared__ __align__(8) uint64_t wbar[2];
+    const int nchunk = (E + RC - 1) / RC;
+    const uint32_t slot_bytes = (uint32_t)RC * H * 2;
+    auto issue = [&](int c) {  // router rows of chunk c into ring slot c & 1
+        const int e0 = c * RC, ne = min(RC, E - e0);
+        const uint32_t bytes = (uint32_t)ne * H * 2;
+        uint64_t *bar = &wbar[c & 1];
+        asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(smem_u32(bar)),
+                     "r"(bytes)
                      : "memory");
         const unsigned char *src = reinterpret_cast<const unsigned char *>(a.router_w + (size_t)e0 * H);
-        for (size_t off = 0; off < bytes; off += 32768) {
-            const uint32_t n = (uint32_t)min((size_t)32768, bytes - off);
+        unsigned char *dst = reinterpret_cast<unsigned char *>(ring) + (size_t)(c & 1) * slot_bytes;
+        for (uint32_t off = 0; off < bytes; off += 32768) {
+            const uint32_t n = min(32768u, bytes - off);
             asm volatile(
                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_u32(reinterpret_cast<unsigned char *>(wsm) + off)),
-                "l"(src + off), "r"(n), "r"(smem_u32(&wbar))
+                    smem_u32(dst + off)),
+                "l"(src + off), "r"(n), "r"(smem_u32(bar))
                 : "memory");
-        }
-    }
-
-    // ---------------------------------------------------------------- norm
-    // x and gamma are read as 16-byte chunks held in registers: one round trip
-    // per row, issued ahead of use.
-    const bool store = blockIdx.y == 0;
-    float4 gm[kXC][2];
-#pragma unroll
-    for (int j = 0; j < kXC; j++) {
-        const int c = tid + kRouteThreads * j;
-        const float4 *g4 = reinterpret_cast<const float4 *>(a.gamma) + 2 * c;
-        gm[j][0] = c < nchunk ? __ldg(g4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        gm[j][1] = c < nchunk ? __ldg(g4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    uint4 xv[kXC], xnext[kXC];
-    auto load_row = [&](int t, uint4(&dst)[kXC]) {
-        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
-#pragma unroll
-        for (int j = 0; j < kXC; j++) {
-            const int c = tid + kRouteThreads * j;
-            dst[j] = c < nchunk ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
         }
     };
-    if (nt > 0) load_row(t0, xv);
-    for (int g = 0; g < nt; g++) {
-        const int t = t0 + g;
-        if (g + 1 < nt) load_row(t + 1, xnext);
-        const double ss = sumsq_exact(xv, lane, warp, s_maxexp, s_acc);
-        if (tid == 0) s_r = rsqrt_d(ss * a.inv_h + a.bp.eps);
-        __syncthreads();
-        normalise_row(a, xv, gm, t, s_r, xh + g * H, store);
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar[0])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar[1])));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        issue(0);
+        if (nchunk > 1) issue(1);
+    }
+    float *gsm = reinterpret_cast<float *>(smem + batch_gm_off(H, E, RC));  // gamma [H]
+    for (int c = tid; c < H / 4; c += kRouteThreads)
+        reinterpret_cast<float4 *>(gsm)[c] = __ldg(reinterpret_cast<const float4 *>(a.gamma) + c);
+    __syncthreads();
+    MOE_PHASE_MARK(0);
+    // ------------------------------------------------------- norm (warp per token)
+    if (warp < nt) {
+        const int t = t0 + warp;
+        uint16_t *row = xh + (size_t)warp * H;
+        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
+        for (int c = lane; c < H / 8; c += 32) reinterpret_cast<uint4 *>(row)[c] = __ldg(xr + c);
+        __syncwarp();
+        MOE_PHASE_MARK(4);
+        const double ssum = sumsq_row(row, H, lane);
+        MOE_PHASE_MARK(5);
+        const double r = rsqrt_d(ssum * a.inv_h + a.bp.eps);  // same in every lane
+        __syncwarp();
+        MOE_PHASE_MARK(6);
+        const float r32 = (float)r;
+        for (int c = lane; c < H / 8; c += 32) {
+            const uint4 xv = reinterpret_cast<const uint4 *>(row)[c];
+            const float4 g0 = reinterpret_cast<const float4 *>(gsm)[2 * c];
+            const float4 g1 = reinterpret_cast<const float4 *>(gsm)[2 * c + 1];
+            const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
+            const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            uint32_t hb[8];
 #pragma unroll
-        for (int j = 0; j < kXC; j++) xv[j] = xnext[j];
-        __syncthreads();
+            for (int q = 0; q < 8; q++) hb[q] = norm_elem((w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, gg[q], r32, r);
+            const uint4 nat = make_uint4(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16, hb[4] | hb[5] << 16,
+                                         hb[6] | hb[7] << 16);
+            reinterpret_cast<uint4 *>(row)[c] = nat;
+            const size_t go = (size_t)t * H + 8 * c;
+            *reinterpret_cast<uint4 *>(a.ws.xhat + go) = nat;
+            if (a.store_mma)
+                *reinterpret_cast<uint4 *>(a.ws.xhat_mma + go) = make_uint4(
+                    hb[0] | hb[4] << 16, hb[1] | hb[5] << 16, hb[2] | hb[6] << 16, hb[3] | hb[7] << 16);
+            uint32_t f[8];
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));
+                f[q] = *reinterpret_cast<uint16_t *>(&hh);
+            }
+            *reinterpret_cast<uint4 *>(a.ws.xhat16 + go) =
+                make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
+            if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + go) = nat;
+        }
     }
-
-    // -------------------------------------------------------------- router
-    {
-        uint32_t ok = 0;
-        uint64_t c0, c1;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c0));
-        for (;;) {
-            asm volatile(
-                "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0; selp.u32 %0, 1, 0, p; }"
-                : "=r"(ok)
-                : "r"(smem_u32(&wbar))
-                : "memory");
-            if (ok) break;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c1));
-            if (c1 - c0 > 2000000000ull) {
-                set_device_error(a.ws.status, MOE_DEV_WAIT_TIMEOUT, 70);
-                break;
+    __syncthreads();
+    MOE_PHASE_MARK(1);
+    // ------------------------------------------------------------------ router
+    const int split = kBatchTokens / RC;  // warps sharing one expert row
+    const int el = warp % RC, gsel = warp / RC;
+    bool ok = true;
+    for (int c = 0; c < nchunk; c++) {
+        if (ok) {
+            uint32_t done = 0;
+            uint64_t c0, c1;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c0));
+            for (;;) {
+                asm volatile(
+                    "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                    : "=r"(done)
+                    : "r"(smem_u32(&wbar[c & 1])), "r"((c >> 1) & 1)
+                    : "memory");
+                if (done) break;
+                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c1));
+                if (c1 - c0 > 2000000000ull) {
+                    set_device_error(a.ws.status, MOE_DEV_WAIT_TIMEOUT, 71);
+                    ok = false;
+                    break;
+                }
             }
         }
-        if (!ok) return;  // copies are reported lost; nothing else depends on this CTA
-    }
-    for (int el = warp; el < ne; el += kRouteWarps) {
-        const int e = e0 + el;
-        const uint16_t *wrow = wsm + (size_t)el * H;
-        for (int g = 0; g < nt; g++) {
-            float l, bd;
+        const int e = c * RC + el;
+        if (ok && e < E) {
+            const uint16_t *wrow = ring + (size_t)(c & 1) * RC * H + (size_t)el * H;
+            const float bias = a.router_b[e];
             if (!a.router_exact) {
-                router_logit<false>(wrow, xh + g * H, a.router_b[e], H, lane, l, bd);
+                router_logits_tokens(wrow, xh, H, gsel, split, nt, bias, lane, lg + e, lb + e, E);
             } else {
-                l = (float)exact_logit(xh + g * H, a.router_w, a.router_b, e, H, lane);
-                bd = 0.f;
-            }
-            if (lane == 0) {
-                lg[g * epc + el] = l;
-                lb[g * epc + el] = bd;
+                for (int g = gsel; g < nt; g += split) {
+                    const float l = (float)exact_logit(xh + (size_t)g * H, a.router_w, a.router_b, e, H, lane);
+                    if (lane == 0) {
+                        lg[g * E + e] = l;
+                        lb[g * E + e] = 0.f;
+                    }
+                }
             }
         }
+        __syncthreads();  // ring slot c & 1 is free again
+        if (tid == 0 && ok && c + 2 < nchunk) issue(c + 2);
     }
-    __syncthreads();
-
+    MOE_PHASE_MARK(2);
+    if (!ok) return;
     // ---------------------------------------------------------- top-k + softmax
-    if (gridDim.y == 1) {
-        // this CTA holds every logit of its tokens
-        for (int g = warp; g < nt; g += kRouteWarps)
-            topk_token<false>(lg + g * epc, lb + g * epc, xh + g * H, a, t0 + g, lane, exs);
-    } else {
-        for (int i = tid; i < nt * ne; i += kRouteThreads) {
-            const int g = i / ne, el = i - g * ne;
-            a.ws.logits[(size_t)(t0 + g) * E + e0 + el] = lg[g * epc + el];
-            a.ws.lbound[(size_t)(t0 + g) * E + e0 + el] = lb[g * epc + el];
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) s_flag = (atomicAdd(a.ws.tickets + 1 + blockIdx.x, 1u) == gridDim.y - 1);
-        __syncthreads();
-        if (!s_flag) return;
-        __threadfence();
-        for (int g = warp; g < nt; g += kRouteWarps)
-            topk_token<true>(a.ws.logits + (size_t)(t0 + g) * E, a.ws.lbound + (size_t)(t0 + g) * E, xh + g * H, a,
-                             t0 + g, lane, exs);
-        if (tid == 0) a.ws.tickets[1 + blockIdx.x] = 0u;  // re-arm the group ticket
-    }
-
-    // --------------------------------------------- last CTA of the grid: permutation
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_flag = (atomicAdd(a.ws.tickets, 1u) == gridDim.x - 1);
-    __syncthreads();
-    if (!s_flag) return;
-    __threadfence();
-    build_permutation(a, smem);  // reuses the router-row area
+    if (warp < nt) topk_token<false>(lg + warp * E, lb + warp * E, xh + (size_t)warp * H, a, t0 + warp, lane,
+                                     exs + (size_t)warp * E);
+    MOE_PHASE_MARK(3);
 }
 
-// Experts per CTA so that their router rows plus G x_hat rows fit in shared memory.
-int route_epc(int G, int H, int E) {
-    const size_t budget = 200 * 1024;
-    const size_t xbytes = (size_t)G * H * 2 + (size_t)kRouteWarps * E * 8 + 64;
-    int epc = (int)((budget - xbytes) / ((size_t)H * 2 + 8 * G));
-    if (epc > E) epc = E;
-    if (epc < 1) epc = 1;
-    return epc;
-}
-
-size_t route_smem_bytes(int G, int H, int E) {
-    const int epc = route_epc(G, H, E);
-    const size_t a = (size_t)epc * H * 2 + (size_t)G * H * 2 + (size_t)G * epc * 8 + (size_t)kRouteWarps * E * 8;
-    const size_t b = perm_smem_bytes(E);
-    return a > b ? a : b;
+// The permutation of a large batch, by one CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) moe_permute_kernel(RouteArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    build_permutation(a, smem);
 }
 
 // Small-batch geometry: C CTAs per token (a cluster, C <= cmax), epc experts each.
@@ -951,10 +1014,16 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
         MOE_CUDA_TRY(launch_small_geo(a, g, st));
         return cudaGetLastError();
     }
-    static bool done8 = false;
-    a.epc = route_epc(8, bp.H, bp.E);
-    MOE_CUDA_TRY(smem_optin_once(moe_route_kernel<8>, done8));
-    dim3 grid((T + 7) / 8, (bp.E + a.epc - 1) / a.epc);
-    moe_route_kernel<8><<<grid, kRouteThreads, route_smem_bytes(8, bp.H, bp.E), st>>>(a);
+    static bool doneb = false, donep = false;
+    int RC = kBatchTokens;
+    while (RC > 1 && batch_smem(bp.H, bp.E, RC) > 200 * 1024) RC >>= 1;
+    const size_t smb = batch_smem(bp.H, bp.E, RC);
+    if (smb > 200 * 1024 || (size_t)kBatchTokens * bp.E * 8 > (size_t)2 * RC * bp.H * 2)
+        return cudaErrorInvalidValue;  // the exact-logit scratch must fit in the ring
+    MOE_CUDA_TRY(smem_optin_once(moe_route_batch_kernel, doneb));
+    moe_route_batch_kernel<<<(T + kBatchTokens - 1) / kBatchTokens, kRouteThreads, smb, st>>>(a, RC);
+    MOE_CUDA_TRY(cudaGetLastError());
+    MOE_CUDA_TRY(smem_optin_once(moe_permute_kernel, donep));
+    moe_permute_kernel<<<1, 1024, perm_smem_bytes(bp.E + bp.n_shared, 32), st>>>(a);
     return cudaGetLastError();
 }
