@@ -34,6 +34,9 @@
 #ifndef MOE_PHASE_MARK
 #define MOE_PHASE_MARK(i)
 #endif
+#ifndef MOE_WARP_MARK
+#define MOE_WARP_MARK(i)
+#endif
 
 namespace {
 
@@ -88,27 +91,6 @@ __device__ __forceinline__ void warp_best(V &v, int &i) {
             i = j;
         }
     }
-}
-
-// Exact (fp64) router logit of expert e for an x_hat row in shared memory, by
-// one warp: 16-byte loads of the router row, products of two bf16 values are
-// exact in fp64, four independent accumulators per lane.
-__device__ double exact_logit(const uint16_t *xh, const uint16_t *router_w, const float *router_b, int e, int H,
-                              int lane) {
-    double acc[4] = {0.0, 0.0, 0.0, 0.0};
-    const uint4 *w = reinterpret_cast<const uint4 *>(router_w + (size_t)e * H);
-    const uint4 *x = reinterpret_cast<const uint4 *>(xh);
-    for (int c = lane; c < H / 8; c += 32) {
-        const uint4 wv = __ldg(w + c), xv = x[c];
-        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w}, xx[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            acc[q] += (double)__uint_as_float(xx[q] << 16) * (double)__uint_as_float(ww[q] << 16);
-            acc[q] += (double)__uint_as_float(xx[q] & 0xFFFF0000u) * (double)__uint_as_float(ww[q] & 0xFFFF0000u);
-        }
-    }
-    double s = warp_sum_d((acc[0] + acc[1]) + (acc[2] + acc[3]));
-    return s + (double)router_b[e];
 }
 
 // Exclusive scan by one warp over n <= 1024 ints (out[n] = total).
@@ -176,6 +158,32 @@ __device__ __forceinline__ void comp_add_pair(Comp &a, uint32_t w2, float sc) {
 }
 __device__ __forceinline__ double comp_result(const Comp &a, int emax) {
     return ldexp((double)a.s + (double)a.c, 2 * (emax - 127));
+}
+
+// Router logit of expert e for an x_hat row in shared memory, by one warp, to
+// ~2^-44 of Σ|products| (the reference's own double sum rounds at ~2^-50):
+// products of two bf16 are exact in fp32 and are summed with error-free
+// two-sums; equal rows give bit-identical results, so exact ties stay ties.
+// Used where the fp32 bounds cannot decide the top-k (and in the exact mode).
+__device__ double exact_logit(const uint16_t *xh, const uint16_t *router_w, const float *router_b, int e, int H,
+                              int lane) {
+    Comp acc[2] = {{0.f, 0.f}, {0.f, 0.f}};
+    const uint4 *w = reinterpret_cast<const uint4 *>(router_w + (size_t)e * H);
+    const uint4 *x = reinterpret_cast<const uint4 *>(xh);
+#pragma unroll 4  // several row loads in flight (the row is read from L2 or HBM)
+    for (int c = lane; c < H / 8; c += 32) {
+        const uint4 wv = __ldg(w + c), xv = x[c];
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w}, xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            comp_add(acc[q & 1], __fmul_rn(__uint_as_float(xx[q] << 16), __uint_as_float(ww[q] << 16)));
+            comp_add(acc[q & 1],
+                     __fmul_rn(__uint_as_float(xx[q] & 0xFFFF0000u), __uint_as_float(ww[q] & 0xFFFF0000u)));
+        }
+    }
+    comp_merge(acc[0], acc[1]);
+    const Comp t = comp_warp(acc[0]);
+    return ((double)t.s + (double)t.c) + (double)router_b[e];
 }
 
 // Σx² of one bf16 row (H elements, shared memory) by one warp; every lane gets it.
@@ -777,13 +785,13 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     MOE_PHASE_MARK(7);
 }
 
-// Larger batches: one CTA of 8 warps per 8 tokens covers every expert.  Warp
-// w normalises token w (in its own x_hat row in shared memory); the
-// router rows stream through a double-buffered ring of RC rows (bulk copies);
-// warp w computes expert w % RC for the tokens g with g % (8/RC) == w / RC;
-// warp w then selects token w's top-k.  The permutation follows as a kernel
-// of its own.
-constexpr int kBatchTokens = kRouteWarps;
+// Larger batches: one CTA of 8 warps per 4 tokens covers every expert.  Warp
+// w < 4 normalises token w (in its own x_hat row in shared memory); the router
+// rows stream through a double-buffered ring of RC rows (bulk copies); warp w
+// computes expert w % RC for the tokens g with g % (8/RC) == w / RC; warp w
+// < 4 then selects token w's top-k.  The permutation follows as a kernel of
+// its own.
+constexpr int kBatchTokens = 4;  // tokens per CTA (small CTAs: two fit an SM, more SMs busy)
 
 __host__ __device__ inline size_t batch_rows_off(int H) { return (size_t)kBatchTokens * H * 2; }
 __host__ __device__ inline size_t batch_lg_off(int H, int RC) { return batch_rows_off(H) + (size_t)2 * RC * H * 2; }
@@ -794,19 +802,23 @@ __host__ __device__ inline size_t batch_smem(int H, int E, int RC) { return batc
 
 __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArgs a, int RC) {
     extern __shared__ __align__(128) unsigned char smem[];
+    MOE_PHASE_MARK(7);
     const int H = a.bp.H, E = a.bp.E;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = blockIdx.x * kBatchTokens, nt = min(kBatchTokens, a.T - t0);
-    uint16_t *xh = reinterpret_cast<uint16_t *>(smem);                                  // [8][H]
+    uint16_t *xh = reinterpret_cast<uint16_t *>(smem);                                  // [4][H]
     uint16_t *ring = reinterpret_cast<uint16_t *>(smem + batch_rows_off(H));            // [2][RC][H]
-    float *lg = reinterpret_cast<float *>(smem + batch_lg_off(H, RC));                  // [8][E]
-    float *lb = lg + kBatchTokens * E;                                                  // [8][E]
-    double *exs = reinterpret_cast<double *>(ring);                                     // [8][E] after the ring
+    float *lg = reinterpret_cast<float *>(smem + batch_lg_off(H, RC));                  // [4][E]
+    float *lb = lg + kBatchTokens * E;                                                  // [4][E]
+    double *exs = reinterpret_cast<double *>(ring);                                     // [4][E] after the ring
     __shared__ __align__(8) uint64_t wbar[2];
     const int nchunk = (E + RC - 1) / RC;
     const uint32_t slot_bytes = (uint32_t)RC * H * 2;
-    auto issue = [&](int c) {  // router rows of chunk c into ring slot c & 1
-        const int e0 = c * RC, ne = min(RC, E - e0);
+    // CTAs walk the chunks from different starting points, so that they do
+    // not all read the same router rows (the same L2 lines) at the same time
+    const int rot = blockIdx.x % nchunk;
+    auto issue = [&](int c) {  // router rows of the c-th chunk of this CTA into ring slot c & 1
+        const int e0 = ((c + rot) % nchunk) * RC, ne = min(RC, E - e0);
         const uint32_t bytes = (uint32_t)ne * H * 2;
         uint64_t *bar = &wbar[c & 1];
         asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(smem_u32(bar)),
@@ -880,7 +892,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
     __syncthreads();
     MOE_PHASE_MARK(1);
     // ------------------------------------------------------------------ router
-    const int split = kBatchTokens / RC;  // warps sharing one expert row
+    const int split = kRouteWarps / RC;  // warps sharing one expert row
     const int el = warp % RC, gsel = warp / RC;
     bool ok = true;
     for (int c = 0; c < nchunk; c++) {
@@ -903,7 +915,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
                 }
             }
         }
-        const int e = c * RC + el;
+        const int e = ((c + rot) % nchunk) * RC + el;
         if (ok && e < E) {
             const uint16_t *wrow = ring + (size_t)(c & 1) * RC * H + (size_t)el * H;
             const float bias = a.router_b[e];
@@ -925,8 +937,10 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
     MOE_PHASE_MARK(2);
     if (!ok) return;
     // ---------------------------------------------------------- top-k + softmax
+    MOE_WARP_MARK(0);
     if (warp < nt) topk_token<false>(lg + warp * E, lb + warp * E, xh + (size_t)warp * H, a, t0 + warp, lane,
                                      exs + (size_t)warp * E);
+    MOE_WARP_MARK(1);
     MOE_PHASE_MARK(3);
 }
 
@@ -1015,8 +1029,9 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
         return cudaGetLastError();
     }
     static bool doneb = false, donep = false;
-    int RC = kBatchTokens;
-    while (RC > 1 && batch_smem(bp.H, bp.E, RC) > 200 * 1024) RC >>= 1;
+    // ring depth: as many rows as keep two CTAs on an SM (one row per warp at most)
+    int RC = kRouteWarps;
+    while (RC > 1 && batch_smem(bp.H, bp.E, RC) > 110 * 1024) RC >>= 1;
     const size_t smb = batch_smem(bp.H, bp.E, RC);
     if (smb > 200 * 1024 || (size_t)kBatchTokens * bp.E * 8 > (size_t)2 * RC * bp.H * 2)
         return cudaErrorInvalidValue;  // the exact-logit scratch must fit in the ring
