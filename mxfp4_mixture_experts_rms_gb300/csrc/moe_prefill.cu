@@ -15,11 +15,11 @@
 //   down kernel:    A = 128 rows of Wd, B = the tile's h rows;
 //                   epilogue: bias, times the route weight -> per-route fp32
 //
-// Warp roles (192 threads): warp 0 issues the TMA loads of the packed codes
+// Warp roles (320 threads): warp 0 issues the TMA loads of the packed codes
 // and of the B tile (128-byte swizzled, straight into the MMA layout; the
 // x_hat rows are first gathered into route order by moe_gather_kernel);
-// warp 1 owns TMEM and issues the MMAs (one elected lane); warps 2..5
-// dequantise A and run the epilogue.  A 4-stage mbarrier ring connects them.
+// warp 1 owns TMEM and issues the MMAs (one elected lane); warps 2..9
+// dequantise A (two threads per row) and warps 2..5 run the epilogue.  A 4-stage mbarrier ring connects them.
 // Activations use a 32-block pair order (x_hat_mma / h), and A is written in
 // that order straight from the nibble-pair dequantiser, so the K permutation
 // cancels in every dot product.
@@ -38,7 +38,8 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kBK = 64;            // K elements per stage (one 128-byte swizzle row of bf16)
 constexpr int kBN = 128;           // max routes per tile
-constexpr int kThreads = 192;
+constexpr int kDqWarps = 8;                   // dequantising warps (2 threads per A row)
+constexpr int kThreads = 64 + 32 * kDqWarps;
 constexpr int kABytes = 128 * 128;     // A stage: 128 rows x 128 B
 constexpr int kBBytes = kBN * 128;     // B stage
 constexpr int kFp4Bytes = 128 * 32;    // packed codes of one stage
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
             mbar_init(&full_fp4[s], 1);
-            mbar_init(&full_ab[s], 4);
+            mbar_init(&full_ab[s], kDqWarps);
             mbar_init(&full_b[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -245,8 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                 if (!ok) break;
                 // B: the tile's 128 activation rows (rows past the tile belong to other
                 // tiles or lie outside the tensor, read as zeros: their columns are ignored)
-                mbar_expect_tx(&full_b[s], kBBytes);
-                tma_load_2d(sB + s * kBBytes, &bmap, &full_b[s], kb * kBK, rstart);
+                // (in boxes of 32 rows, as many as the tile's routes need: the MMA
+                // reads only the first n_mma rows)
+                const int nbox = (rcount + 31) / 32;
+                mbar_expect_tx(&full_b[s], (uint32_t)nbox * 32 * 128);
+                for (int bx = 0; bx < nbox; bx++)
+                    tma_load_2d(sB + s * kBBytes + bx * 32 * 128, &bmap, &full_b[s], kb * kBK, rstart + 32 * bx);
                 mbar_expect_tx(&full_fp4[s], kFp4Bytes);
                 unsigned char *dst = sF + s * kFp4Bytes;
                 if (GATEUP) {
@@ -294,21 +299,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
             }
         }
     } else {
-        // ------------------------------------- dequant + B staging (warps 2..5)
-        const int t = threadIdx.x - 64;  // 0..127: A row of this thread
-        const MatPtrs &M = (GATEUP && t >= 64) ? a.A1 : a.A0;
-        int wrow;                        // weight row of A row t (may be >= rows for the last down tile)
+        // ----------------------------------------------- dequant (warps 2..9)
+        const int t = threadIdx.x - 64;  // 0..255
+        const int arow = t >> 1, half = t & 1;  // A row and which 32-element block of the stage
+        const MatPtrs &M = (GATEUP && arow >= 64) ? a.A1 : a.A0;
+        int wrow;                        // weight row of A row arow (may be >= rows for the last down tile)
         if (GATEUP)
-            wrow = mt * 64 + (t & 63);
+            wrow = mt * 64 + (arow & 63);
         else
-            wrow = mt * 128 + t;
+            wrow = mt * 128 + arow;
         const bool row_ok = wrow < a.rows;
-        const uint8_t *srow = mat_scales(M, e, E) + (size_t)(row_ok ? wrow : 0) * nb;
-        // this row's two scale bytes per k-block, loaded four k-blocks ahead
-        auto ldsc = [&](int k) -> uint32_t {
-            return (k < nkb && row_ok) ? ((uint32_t)__ldg(srow + 2 * k) | ((uint32_t)__ldg(srow + 2 * k + 1) << 8))
-                                       : 0x7F7Fu;
-        };
+        const uint8_t *srow = mat_scales(M, e, E) + (size_t)(row_ok ? wrow : 0) * nb + half;
+        // this thread's scale byte per k-block, loaded four k-blocks ahead
+        auto ldsc = [&](int k) -> uint32_t { return (k < nkb && row_ok) ? (uint32_t)__ldg(srow + 2 * k) : 127u; };
         uint32_t q0 = ldsc(0), q1 = ldsc(1), q2 = ldsc(2), q3 = ldsc(3);
         bool ok = true;
         for (int kb = 0; kb < nkb; kb++) {
@@ -317,31 +320,27 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                 ok = mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, status, 30);
                 if (!ok) break;
             }
-            const uint32_t sc0 = q0 & 0xFFu, sc1 = q0 >> 8;
+            const uint32_t sc = q0;
             q0 = q1;
             q1 = q2;
             q2 = q3;
             q3 = ldsc(kb + 4);
-            // A: wait for the packed codes, dequantise row t
+            // A: wait for the packed codes, dequantise half a row
             ok = mbar_wait(&full_fp4[s], (kb / kStages) & 1, status, 31);
             if (!ok) break;
-            const uint4 *src = reinterpret_cast<const uint4 *>(sF + s * kFp4Bytes + t * 32);
-            const uint4 c0 = src[0], c1 = src[1];
-            const bool big = (sc0 > 128u) || (sc1 > 128u);
-            const uint32_t l0 = scale_lo(sc0), h0 = scale_hi(sc0), l1 = scale_lo(sc1), h1 = scale_hi(sc1);
+            const uint4 c = *reinterpret_cast<const uint4 *>(sF + s * kFp4Bytes + arow * 32 + half * 16);
+            const bool big = sc > 128u;
+            const uint32_t l = scale_lo(sc), h = scale_hi(sc);
             unsigned char *adst = sA + s * kABytes;
-            *reinterpret_cast<uint4 *>(adst + sw128(t, 0)) = dequant8(c0.x, l0, h0, big);
-            *reinterpret_cast<uint4 *>(adst + sw128(t, 1)) = dequant8(c0.y, l0, h0, big);
-            *reinterpret_cast<uint4 *>(adst + sw128(t, 2)) = dequant8(c0.z, l0, h0, big);
-            *reinterpret_cast<uint4 *>(adst + sw128(t, 3)) = dequant8(c0.w, l0, h0, big);
-            *reinterpret_cast<uint4 *>(adst + sw128(t, 4)) = dequant8(c1.x, l1, h1, big);
-            *reinterpret_cast<uint4 *>(adst + sw128(t, 5)) = dequant8(c1.y, l1, h1, big);
-            *reinterpret_cast<uint4 *>(adst + sw128(t, 6)) = dequant8(c1.z, l1, h1, big);
-            *reinterpret_cast<uint4 *>(adst + sw128(t, 7)) = dequant8(c1.w, l1, h1, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 0)) = dequant8(c.x, l, h, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 1)) = dequant8(c.y, l, h, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 2)) = dequant8(c.z, l, h, big);
+            *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 3)) = dequant8(c.w, l, h, big);
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&full_ab[s]);
         }
+        if (warp < 6) {
         // ------------------------------------------------------------ epilogue
         if (ok) ok = mbar_wait(acc_full, 0, status, 40);
         ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
@@ -385,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                 }
             }
         }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -423,12 +423,13 @@ cudaError_t make_codes_map(CUtensorMap *m, const uint8_t *codes, size_t n_rows, 
 
 size_t prefill_smem_bytes() { return 1024 + kStages * (kABytes + kBBytes + kFp4Bytes) + 256; }
 
-// 2D map over a bf16 activation matrix [rows][K]: box 64 elements (128 B) x 128
-// rows, 128-byte swizzle (the K-major layout the MMA descriptors expect).
+// 2D map over a bf16 activation matrix [rows][K]: box 64 elements (128 B) x 32
+// rows, 128-byte swizzle (the K-major layout the MMA descriptors expect; a
+// 32-row box is four whole 8-row swizzle atoms).
 cudaError_t make_act_map(CUtensorMap *m, const uint16_t *base, int rows, int K) {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBN};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, 32};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
