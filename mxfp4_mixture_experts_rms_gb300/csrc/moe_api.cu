@@ -60,6 +60,8 @@ struct moe_plan {
     bool have_maps = false;
     // the decode GEMVs carry x_hat / h as fp16 unless these can leave its range
     bool x_bf16 = false, h_bf16 = false;
+    // the grouped GEMM takes fp16 operands (exponents in [104, 140], fp16-range activations)
+    bool pf_f16 = false;
     // kernel timing (profile option)
     static constexpr int kSlots = 4, kMaxRec = 4096 * kSlots;
     std::vector<cudaEvent_t> ev;     // 2 events per record
@@ -305,7 +307,7 @@ int moe_load_weights(moe_plan *p, const moe_weights *w) {
     if (e == cudaSuccess) e = cudaMemcpy(h, flag, 8, cudaMemcpyDeviceToHost);
     cudaFree(flag);
     if (e != cudaSuccess) return cuda_fail(e, "moe_load_weights scale scan");
-    if (h[0]) return fail(MOE_EINVAL, "an E8M0 scale holds the NaN code 0xFF");
+    if (h[0] & 1) return fail(MOE_EINVAL, "an E8M0 scale holds the NaN code 0xFF");
     float gmax;
     memcpy(&gmax, &h[1], 4);
     p->w = *w;
@@ -322,6 +324,7 @@ int moe_load_weights(moe_plan *p, const moe_weights *w) {
     const double hb = gb * (L + 1.0) * 1.01;
     p->x_bf16 = !(xb < 65504.0);
     p->h_bf16 = !(hb < 65504.0);
+    p->pf_f16 = !(h[0] & 2) && !p->x_bf16 && !p->h_bf16;
     p->have_w = true;
     return MOE_OK;
 }
@@ -361,15 +364,15 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     mark(0, false);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     mark(1, true);
-    if (!decode) e = launch_gather(b, p->ws, tokens, st);
+    if (!decode) e = launch_gather(b, p->ws, tokens, p->pf_f16, st);
     if (e == cudaSuccess)
         e = decode ? launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
-                   : launch_prefill_stage(b, p->ws, p->gate, p->up, true, tokens, p->maps.gateup, st);
+                   : launch_prefill_stage(b, p->ws, p->gate, p->up, true, tokens, p->maps.gateup, p->pf_f16, st);
     mark(1, false);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
     mark(2, true);
     e = decode ? launch_decode_stage(b, p->ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, st)
-               : launch_prefill_stage(b, p->ws, p->down, p->down, false, tokens, p->maps.down, st);
+               : launch_prefill_stage(b, p->ws, p->down, p->down, false, tokens, p->maps.down, p->pf_f16, st);
     mark(2, false);
     if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
     mark(3, true);
@@ -517,13 +520,13 @@ int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, 
     e = launch_route(b, ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, nullptr, nullptr,
                      tile_rows, p->router_exact, decode ? 0 : 1, st);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
-    if (!decode) e = launch_gather(b, ws, tokens, st);
+    if (!decode) e = launch_gather(b, ws, tokens, p->pf_f16, st);
     if (e == cudaSuccess)
         e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
-                   : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, st);
+                   : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, p->pf_f16, st);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
     e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, st)
-               : launch_prefill_stage(b, ws, p->down, p->down, false, tokens, p->maps.down, st);
+               : launch_prefill_stage(b, ws, p->down, p->down, false, tokens, p->maps.down, p->pf_f16, st);
     if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
     e = launch_combine(b, ws, x, tokens, out, st);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");

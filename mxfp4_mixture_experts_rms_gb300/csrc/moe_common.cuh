@@ -55,7 +55,7 @@ struct Workspace {
     uint16_t *h;           // [R][F] bf16 (decode: natural order, bf16-activation plans only; prefill: pair order)
     uint16_t *h16;         // [R][F] fp16 h of the decode GEMVs (natural order)
     float *y;              // [R][H] weighted expert outputs
-    uint16_t *xs;          // [R][H] x_hat rows in route order, pair order (grouped GEMM operand; aliases y,
+    uint16_t *xs;          // [R][H] x_hat rows in route order (grouped GEMM operand, fp16 or bf16; aliases y,
                            //         which is written only after the gate/up GEMM has read these)
     float *logits;         // [T][E] router logits (fp32) of the routing kernel
     float *lbound;         // [T][E] their rounding-error bounds
@@ -95,6 +95,19 @@ __device__ __forceinline__ uint16_t bf16_from_double_rne(double v) {
 
 __device__ __forceinline__ void set_device_error(int32_t *status, int code, int detail) {
     if (atomicCAS(status, 0, code) == 0) status[1] = detail;
+}
+
+// 8 E2M1 codes of one 32-bit word -> four f16x2 in natural order (hardware conversion)
+// (element 2i in the low half of h[i]), exact: byte i holds elements 2i, 2i+1.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t h[4]) {
+    asm("{ .reg .b8 a, b, c, d;\n"
+        "  mov.b32 {a, b, c, d}, %4;\n"
+        "  cvt.rn.f16x2.e2m1x2 %0, a;\n"
+        "  cvt.rn.f16x2.e2m1x2 %1, b;\n"
+        "  cvt.rn.f16x2.e2m1x2 %2, c;\n"
+        "  cvt.rn.f16x2.e2m1x2 %3, d; }"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
 }
 
 // Clamped SwiGLU (gate clamped from above, up to [-L, L]); NaN propagates.
@@ -178,10 +191,12 @@ struct PrefillMaps {
 };
 cudaError_t prefill_make_maps(const BlockParams &bp, const MatPtrs &gate, const MatPtrs &up, const MatPtrs &down,
                               PrefillMaps *out);
+// f16: the fp16-operand variant (E8M0 exponents in [104, 140], fp16-range activations).
 cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
-                                 const MatPtrs &a1, bool gateup, int T, const TmaMaps &maps, cudaStream_t st);
+                                 const MatPtrs &a1, bool gateup, int T, const TmaMaps &maps, bool f16,
+                                 cudaStream_t st);
 // x_hat rows gathered into route order (ws.xs) for the grouped GEMM.
-cudaError_t launch_gather(const BlockParams &bp, const Workspace &ws, int T, cudaStream_t st);
+cudaError_t launch_gather(const BlockParams &bp, const Workspace &ws, int T, bool f16, cudaStream_t st);
 int prefill_tile_rows();
 cudaError_t launch_dequant(const MatPtrs &m, int expert, int n_experts, float *out, cudaStream_t st);
 cudaError_t launch_scan_scales(const uint8_t *scales, size_t n, int32_t *flag, cudaStream_t st);

@@ -63,19 +63,6 @@ struct DecodeArgs {
     int h_bf16;      // gate/up: write h as bf16 (else fp16)
 };
 
-// 8 E2M1 codes of one 32-bit word -> four f16x2 in natural order
-// (element 2i in the low half of h[i]), exact: byte i holds elements 2i, 2i+1.
-__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t h[4]) {
-    asm("{ .reg .b8 a, b, c, d;\n"
-        "  mov.b32 {a, b, c, d}, %4;\n"
-        "  cvt.rn.f16x2.e2m1x2 %0, a;\n"
-        "  cvt.rn.f16x2.e2m1x2 %1, b;\n"
-        "  cvt.rn.f16x2.e2m1x2 %2, c;\n"
-        "  cvt.rn.f16x2.e2m1x2 %3, d; }"
-        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-        : "r"(w));
-}
-
 // f16x2 holding two E2M1 values (0, +-0.5 .. +-6) -> the same values as bf16x2.
 // Non-zero E2M1 magnitudes in fp16 are 0x3800..0x4600 (bit 13 or 14 set, low
 // byte zero); the bf16 pattern is (fp16 magnitude >> 3) + 0x3800.
@@ -505,12 +492,19 @@ __global__ void moe_dequant_kernel(MatPtrs m, int expert, int n_experts, float *
     }
 }
 
+// flag bit 0: an exponent holds the NaN code 0xFF; bit 1: an exponent lies
+// outside [104, 140] (where e2m1 * 2^(e-127) stops being exact in fp16)
 __global__ void moe_scan_scales_kernel(const uint8_t *s, size_t n, int32_t *flag) {
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     size_t stride = (size_t)gridDim.x * blockDim.x;
-    int bad = 0;
-    for (; i < n; i += stride) bad |= (s[i] == 0xFF);
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
+    int bad = 0, wide = 0;
+    for (; i < n; i += stride) {
+        bad |= (s[i] == 0xFF);
+        wide |= (s[i] < 104 || s[i] > 140);
+    }
+    bad = __syncthreads_or(bad);
+    wide = __syncthreads_or(wide);
+    if (threadIdx.x == 0 && (bad || wide)) atomicOr(flag, (bad ? 1 : 0) | (wide ? 2 : 0));
 }
 
 // max |v| over n floats (NaN counts as +inf), as the bit pattern of a

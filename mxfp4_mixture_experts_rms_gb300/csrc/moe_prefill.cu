@@ -15,14 +15,16 @@
 //   down kernel:    A = 128 rows of Wd, B = the tile's h rows;
 //                   epilogue: bias, times the route weight -> per-route fp32
 //
-// Warp roles (320 threads): warp 0 issues the TMA loads of the packed codes
-// and of the B tile (128-byte swizzled, straight into the MMA layout; the
-// x_hat rows are first gathered into route order by moe_gather_kernel);
-// warp 1 owns TMEM and issues the MMAs (one elected lane); warps 2..9
-// dequantise A (two threads per row) and warps 2..5 run the epilogue.  A 4-stage mbarrier ring connects them.
-// Activations use a 32-block pair order (x_hat_mma / h), and A is written in
-// that order straight from the nibble-pair dequantiser, so the K permutation
-// cancels in every dot product.
+// The kernel is persistent (one CTA per SM walking a static list of
+// (route tile, weight-row block) items) with warp roles: a TMA warp for the
+// packed codes, a TMA warp for the B tile (128-byte swizzled, straight into
+// the MMA layout; the x_hat rows are first gathered into route order by
+// moe_gather_kernel), an MMA warp that owns TMEM, eight dequantising warps
+// (two threads per A row) and four epilogue warps that drain one of two TMEM
+// accumulators while the MMA fills the other.  mbarrier rings connect them.
+// The bf16 variant keeps activations in a 32-block pair order (x_hat_mma / h)
+// and writes A in that order straight from the nibble-pair dequantiser, so
+// the K permutation cancels in every dot product.
 //
 // Every wait is bounded (about 2 s of %globaltimer); on a timeout the kernel
 // records MOE_DEV_WAIT_TIMEOUT in the status word, drains what it issued,
@@ -33,13 +35,28 @@
 
 #include "moe_common.cuh"
 
+// Timeline markers (no-ops unless an instrumented build defines them).
+#ifndef MOE_PF_MARK
+#define MOE_PF_MARK(slot)
+#endif
+#ifndef MOE_PF_KMARK
+#define MOE_PF_KMARK(kind, kb)
+#endif
+
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 5;          // A (dequantised) + B stages, consumed by the MMA
+constexpr int kCStages = 8;         // packed-code stages (prefetched further ahead)
 constexpr int kBK = 64;            // K elements per stage (one 128-byte swizzle row of bf16)
 constexpr int kBN = 128;           // max routes per tile
+constexpr int kWarpCodes = 0, kWarpMma = 1, kWarpB = 2, kWarpDq0 = 3;
 constexpr int kDqWarps = 8;                   // dequantising warps (2 threads per A row)
-constexpr int kThreads = 64 + 32 * kDqWarps;
+constexpr int kWarpEpi0 = kWarpDq0 + kDqWarps, kEpiWarps = 4;
+constexpr int kThreads = 32 * (kWarpEpi0 + kEpiWarps);
+constexpr int kAccCols = 128;                 // one fp32 accumulator: 128 lanes x N <= 128 columns
+constexpr int kTmemCols = 2 * kAccCols;       // two accumulators (MMA fills one, the epilogue drains the other)
+constexpr int kXchFloats = 2 * 64 * 17;       // gate/up epilogue exchange
+constexpr int kSmTiles = 256;                 // route tiles cached in shared memory
 constexpr int kABytes = 128 * 128;     // A stage: 128 rows x 128 B
 constexpr int kBBytes = kBN * 128;     // B stage
 constexpr int kFp4Bytes = 128 * 32;    // packed codes of one stage
@@ -99,6 +116,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int32_t 
     }
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Wait that ignores the status word (only the time limit ends it): used to let
+// copies or MMAs already issued land before the CTA's shared memory or TMEM goes.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t *b, uint32_t parity, int32_t *status) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try(b, parity))
+        if (globaltimer() - t0 > kWaitNs) {
+            set_device_error(status, MOE_DEV_WAIT_TIMEOUT, 90);
+            return;
+        }
+}
+// The last min(issued, n) copies of an n-stage ring have landed.
+__device__ __forceinline__ void drain_ring(uint64_t *full, int n, int issued, int32_t *status) {
+    for (int g = max(0, issued - n); g < issued; g++) mbar_wait_drain(&full[g % n], (g / n) & 1, status);
+}
+// Stage index and phase bit of a ring walked in order.  Consumers wait on a
+// full barrier with parity ph; producers wait on an empty barrier with parity
+// ph ^ 1, which a fresh barrier already satisfies (every stage starts free).
+struct Ring {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++s == n) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+};
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
     asm volatile(
@@ -118,9 +165,11 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
     d |= (uint64_t)2 << 61;              // SWIZZLE_128B
     return d;
 }
-// Instruction descriptor, kind::f16: D f32, A/B bf16, both K-major, M x N.
-__host__ __device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f16: D f32, A/B both bf16 (bf = true) or both
+// f16, both K-major, M x N.
+__host__ __device__ __forceinline__ uint32_t umma_idesc(int M, int N, bool bf) {
+    const uint32_t ab = bf ? 1u : 0u;
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __device__ __forceinline__ void umma_bf16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -182,199 +231,327 @@ __device__ __forceinline__ uint32_t scale_hi(uint32_t s) {
     uint32_t b = (s <= 128u) ? 0x3F80u : (s << 7);
     return b | (b << 16);
 }
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+// fp16 2^(s-127) in both halves for s in [104, 140] (subnormal below 113): the
+// product with an E2M1 value is then exact in fp16
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t s) {
+    const uint32_t b = (s >= 113u) ? ((s - 112u) << 10) : (1u << (s - 103u));
+    return b | (b << 16);
+}
+// 8 codes -> 8 fp16 values, natural order, times 2^(s-127) (fp16 variant)
+__device__ __forceinline__ uint4 dequant8_f16(uint32_t w, uint32_t sc2) {
+    uint32_t h[4];
+    e2m1x8_to_f16(w, h);
+    return make_uint4(hmul2_f16(h[0], sc2), hmul2_f16(h[1], sc2), hmul2_f16(h[2], sc2), hmul2_f16(h[3], sc2));
+}
+
 // byte offset of 16-byte chunk c of row r in a 128B-swizzled K-major tile
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <bool GATEUP>
+// Persistent grouped GEMM.  A launch covers n_tiles x mtiles work items, item
+// i = (route tile i / mtiles, weight-row block i % mtiles); CTA b takes items
+// b, b + gridDim.x, ...  Every role walks that same sequence with its own ring
+// counters, so the producers run ahead into the next item while the epilogue
+// drains the previous one from the other of two TMEM accumulators.
+//
+// Warps: 0 TMA for the packed codes, 1 MMA issue (and TMEM owner), 2 TMA for
+// the activation tile, 3..10 dequantisation (two threads per A row), 11..14
+// epilogue (one TMEM lane quarter each).  Each producer has a warp of its own:
+// a lane blocked in mbarrier.try_wait holds up every other lane of its warp.
+//
+// F16: the fp16 variant (every E8M0 exponent in [104, 140], activations in the
+// fp16 range): hardware e2m1 -> f16 conversion, natural K order, fp16 MMA
+// operands (x_hat16 / h16); otherwise the bf16 variant (any exponent,
+// nibble-pair order, bf16 operands x_hat_mma / h).
+template <bool GATEUP, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_constant__ PrefillArgs a,
                                                                     const __grid_constant__ TmaMaps maps,
                                                                     const __grid_constant__ CUtensorMap bmap) {
+    const int mtiles = GATEUP ? a.rows / 64 : (a.rows + 127) / 128;
+    const int n_tiles = *a.ws.n_tiles;
+    const int n_items = n_tiles * mtiles;
+    if ((int)blockIdx.x >= n_items) return;
+
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *sA = smem;                                   // [kStages][128 rows][128 B] swizzled
     unsigned char *sB = sA + kStages * kABytes;                 // [kStages][kBN rows][128 B] swizzled
-    unsigned char *sF = sB + kStages * kBBytes;                 // [kStages][128 rows][32 B] packed codes
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sF + kStages * kFp4Bytes);
-    uint64_t *full_fp4 = bars, *full_ab = bars + kStages, *empty = bars + 2 * kStages, *full_b = bars + 3 * kStages;
-    uint64_t *acc_full = bars + 4 * kStages, *drain = acc_full + 1;
+    unsigned char *sF = sB + kStages * kBBytes;                 // [kCStages][128 rows][32 B] packed codes
+    float *xch = reinterpret_cast<float *>(sF + kCStages * kFp4Bytes);  // gate/up exchange [2][64][17]
+    int4 *s_tiles = reinterpret_cast<int4 *>(xch + kXchFloats);          // [kSmTiles]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s_tiles + kSmTiles);
+    uint64_t *full_c = bars, *empty_c = bars + kCStages;                    // code ring
+    uint64_t *full_ab = bars + 2 * kCStages, *full_b = full_ab + kStages;   // A/B ring
+    uint64_t *empty = full_b + kStages;
+    uint64_t *acc_full = empty + kStages, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
-    const int tile_idx = blockIdx.x;
-    if (tile_idx >= *a.ws.n_tiles) return;
-    const int4 tile = a.ws.tiles[tile_idx];
-    const int e = tile.x, rstart = tile.y, rcount = tile.z;
+    MOE_PF_MARK(0);
     const int E = a.bp.E, K = a.Kdim, nb = K / 32, nkb = K / kBK;
-    const int mt = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_mma = max(16, (rcount + 15) & ~15);
     int32_t *status = a.ws.status;
 
+    for (int i = threadIdx.x; i < min(n_tiles, kSmTiles); i += blockDim.x) s_tiles[i] = a.ws.tiles[i];
     if (threadIdx.x == 0) {
+        for (int s = 0; s < kCStages; s++) {
+            mbar_init(&full_c[s], 1);
+            mbar_init(&empty_c[s], kDqWarps);
+        }
         for (int s = 0; s < kStages; s++) {
-            mbar_init(&full_fp4[s], 1);
             mbar_init(&full_ab[s], kDqWarps);
             mbar_init(&full_b[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(acc_full, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], kEpiWarps);
+        }
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(smem_u32(tmem_slot)));
+    if (warp == kWarpMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "n"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    auto tile_at = [&](int t) -> int4 { return t < kSmTiles ? s_tiles[t] : a.ws.tiles[t]; };
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer (codes)
+    if (warp == kWarpCodes) {
+        // ------------------------------------------------ packed codes (TMA)
         if (lane == 0) {
-            const bool shared_e = e >= E;
-            const CUtensorMap *m0 = shared_e ? &maps.m[2] : &maps.m[0];
-            const CUtensorMap *m1 = shared_e ? &maps.m[3] : &maps.m[1];
-            const int ebase = shared_e ? 0 : e;
-            int issued_upto = 0;
+            Ring r;
+            int issued = 0, g = 0;
             bool ok = true;
-            for (int kb = 0; kb < nkb && ok; kb++) {
-                const int s = kb % kStages;
-                if (kb >= kStages) ok = mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, status, 10);
-                if (!ok) break;
-                // B: the tile's 128 activation rows (rows past the tile belong to other
-                // tiles or lie outside the tensor, read as zeros: their columns are ignored)
-                // (in boxes of 32 rows, as many as the tile's routes need: the MMA
-                // reads only the first n_mma rows)
-                const int nbox = (rcount + 31) / 32;
-                mbar_expect_tx(&full_b[s], (uint32_t)nbox * 32 * 128);
-                for (int bx = 0; bx < nbox; bx++)
-                    tma_load_2d(sB + s * kBBytes + bx * 32 * 128, &bmap, &full_b[s], kb * kBK, rstart + 32 * bx);
-                mbar_expect_tx(&full_fp4[s], kFp4Bytes);
-                unsigned char *dst = sF + s * kFp4Bytes;
-                if (GATEUP) {
-                    const int y = ebase * a.rows + mt * 64;
-                    tma_load_2d(dst, m0, &full_fp4[s], kb * 32, y);
-                    tma_load_2d(dst + 64 * 32, m1, &full_fp4[s], kb * 32, y);
-                } else {
-                    tma_load_2d(dst, m0, &full_fp4[s], kb * 32, ebase * a.rows + mt * 128);
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const int tile = it / mtiles, mt = it - tile * mtiles;
+                const int e = tile_at(tile).x;
+                const bool shared_e = e >= E;
+                const CUtensorMap *m0 = shared_e ? &maps.m[2] : &maps.m[0];
+                const CUtensorMap *m1 = shared_e ? &maps.m[3] : &maps.m[1];
+                const int ebase = shared_e ? 0 : e;
+                for (int kb = 0; kb < nkb; kb++, g++) {
+                    if (!mbar_wait(&empty_c[r.s], r.ph ^ 1, status, 10)) {
+                        ok = false;
+                        break;
+                    }
+                    MOE_PF_KMARK(5, g);
+                    mbar_expect_tx(&full_c[r.s], kFp4Bytes);
+                    unsigned char *dst = sF + r.s * kFp4Bytes;
+                    if (GATEUP) {
+                        const int y = ebase * a.rows + mt * 64;
+                        tma_load_2d(dst, m0, &full_c[r.s], kb * 32, y);
+                        tma_load_2d(dst + 64 * 32, m1, &full_c[r.s], kb * 32, y);
+                    } else {
+                        tma_load_2d(dst, m0, &full_c[r.s], kb * 32, ebase * a.rows + mt * 128);
+                    }
+                    issued++;
+                    r.next(kCStages);
                 }
-                issued_upto = kb + 1;
             }
-            // make sure every copy this thread issued has landed before exiting
-            for (int kb = max(0, issued_upto - kStages); kb < issued_upto; kb++) {
-                mbar_wait(&full_fp4[kb % kStages], (kb / kStages) & 1, status, 11);
-                mbar_wait(&full_b[kb % kStages], (kb / kStages) & 1, status, 12);
-            }
+            drain_ring(full_c, kCStages, issued, status);
         }
-    } else if (warp == 1) {
+    } else if (warp == kWarpB) {
+        // ------------------------------- activation tile (TMA, 32-row boxes)
+        // as many boxes as the tile has routes; the MMA reads only the first
+        // n_mma rows, rows past the tile belong to other tiles or lie outside
+        // the tensor and read as zeros
+        if (lane == 0) {
+            Ring r;
+            int issued = 0, g = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const int4 tl = tile_at(it / mtiles);
+                const int rstart = tl.y, nbox = (tl.z + 31) / 32;
+                for (int kb = 0; kb < nkb; kb++, g++) {
+                    if (!mbar_wait(&empty[r.s], r.ph ^ 1, status, 13)) {
+                        ok = false;
+                        break;
+                    }
+                    MOE_PF_KMARK(4, g);
+                    mbar_expect_tx(&full_b[r.s], (uint32_t)nbox * 32 * 128);
+                    for (int bx = 0; bx < nbox; bx++)
+                        tma_load_2d(sB + r.s * kBBytes + bx * 32 * 128, &bmap, &full_b[r.s], kb * kBK,
+                                    rstart + 32 * bx);
+                    issued++;
+                    r.next(kStages);
+                }
+            }
+            drain_ring(full_b, kStages, issued, status);
+        }
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc_bf16(128, n_mma);
-            int done = 0;
+            Ring r;
             bool ok = true;
-            for (int kb = 0; kb < nkb; kb++) {
-                const int s = kb % kStages;
-                ok = mbar_wait(&full_ab[s], (kb / kStages) & 1, status, 20) &&
-                     mbar_wait(&full_b[s], (kb / kStages) & 1, status, 22);
+            int li = 0, g = 0;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, li++) {
+                const int rcount = tile_at(it / mtiles).z;
+                const uint32_t idesc = umma_idesc(128, max(16, (rcount + 15) & ~15), !F16);
+                const int ab = li & 1;
+                // the epilogue has read this accumulator out (free on its first use)
+                ok = mbar_wait(&acc_empty[ab], ((li >> 1) & 1) ^ 1, status, 23);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(sA + s * kABytes), b_addr = smem_u32(sB + s * kBBytes);
+                const uint32_t dt = tmem + (uint32_t)(ab * kAccCols);
+                for (int kb = 0; kb < nkb; kb++, g++) {
+                    ok = mbar_wait(&full_ab[r.s], r.ph, status, 20);
+                    MOE_PF_KMARK(0, g);
+                    ok = ok && mbar_wait(&full_b[r.s], r.ph, status, 22);
+                    if (!ok) break;
+                    tc_fence_after();
+                    MOE_PF_KMARK(3, g);
+                    const uint32_t a_addr = smem_u32(sA + r.s * kABytes), b_addr = smem_u32(sB + r.s * kBBytes);
 #pragma unroll
-                for (int k = 0; k < kBK / 16; k++) {
-                    umma_bf16(tmem, umma_desc_sw128(a_addr + 32 * k), umma_desc_sw128(b_addr + 32 * k), idesc,
-                              (kb | k) != 0);
+                    for (int k = 0; k < kBK / 16; k++)
+                        umma_bf16(dt, umma_desc_sw128(a_addr + 32 * k), umma_desc_sw128(b_addr + 32 * k), idesc,
+                                  (kb | k) != 0);
+                    umma_commit(&empty[r.s]);
+                    r.next(kStages);
                 }
-                umma_commit(&empty[s]);
-                done = kb + 1;
+                if (ok) umma_commit(&acc_full[ab]);
             }
-            if (ok && done == nkb) {
-                umma_commit(acc_full);
-            } else {
-                // drain the MMAs already issued before TMEM is released
+            if (!ok) {
+                // the MMAs already issued finish before TMEM is released
                 umma_commit(drain);
-                mbar_wait(drain, 0, status, 21);
+                mbar_wait_drain(drain, 0, status);
+            }
+        }
+    } else if (warp < kWarpEpi0) {
+        // ------------------------------------------ dequant (warps 3..10)
+        const int t = threadIdx.x - 32 * kWarpDq0;  // 0..255
+        const int arow = t >> 1, half = t & 1;      // A row and which 32-element block of the stage
+        // this thread's scale row in item it (nullptr: the row lies past the matrix)
+        auto scale_row = [&](int it) -> const uint8_t * {
+            if (it >= n_items) return nullptr;
+            const int tile = it / mtiles, mt = it - tile * mtiles;
+            const int e = tile_at(tile).x;
+            const MatPtrs &M = (GATEUP && arow >= 64) ? a.A1 : a.A0;
+            const int wrow = GATEUP ? mt * 64 + (arow & 63) : mt * 128 + arow;
+            return wrow < a.rows ? mat_scales(M, e, E) + (size_t)wrow * nb + half : nullptr;
+        };
+        // scale bytes are read four k-blocks ahead, across item boundaries
+        int la_it = blockIdx.x, la_kb = 0;
+        const uint8_t *la_p = scale_row(la_it);
+        auto next_scale = [&]() -> uint32_t {
+            const uint32_t v = la_p ? (uint32_t)__ldg(la_p + 2 * la_kb) : 127u;
+            if (++la_kb == nkb) {
+                la_kb = 0;
+                la_it += gridDim.x;
+                la_p = scale_row(la_it);
+            }
+            return v;
+        };
+        uint32_t q0 = next_scale(), q1 = next_scale(), q2 = next_scale(), q3 = next_scale();
+        Ring r, rc;
+        bool ok = true;
+        int g = 0;
+        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+            for (int kb = 0; kb < nkb; kb++, g++) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&empty[r.s], r.ph ^ 1, status, 30));
+                if (!ok) break;
+                const uint32_t sc = q0;
+                q0 = q1;
+                q1 = q2;
+                q2 = q3;
+                q3 = next_scale();
+                if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(1, g);
+                ok = __all_sync(0xffffffffu, mbar_wait(&full_c[rc.s], rc.ph, status, 31));
+                if (!ok) break;
+                if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(2, g);
+                const uint4 c = *reinterpret_cast<const uint4 *>(sF + rc.s * kFp4Bytes + arow * 32 + half * 16);
+                unsigned char *adst = sA + r.s * kABytes;
+                if (F16) {
+                    const uint32_t sc2 = scale_f16x2(sc);
+                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 0)) = dequant8_f16(c.x, sc2);
+                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 1)) = dequant8_f16(c.y, sc2);
+                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 2)) = dequant8_f16(c.z, sc2);
+                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 3)) = dequant8_f16(c.w, sc2);
+                } else {
+                    const bool big = sc > 128u;
+                    const uint32_t l = scale_lo(sc), h = scale_hi(sc);
+                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 0)) = dequant8(c.x, l, h, big);
+                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 1)) = dequant8(c.y, l, h, big);
+                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 2)) = dequant8(c.z, l, h, big);
+                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 3)) = dequant8(c.w, l, h, big);
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&full_ab[r.s]);
+                    mbar_arrive(&empty_c[rc.s]);
+                }
+                if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(6, g);
+                r.next(kStages);
+                rc.next(kCStages);
             }
         }
     } else {
-        // ----------------------------------------------- dequant (warps 2..9)
-        const int t = threadIdx.x - 64;  // 0..255
-        const int arow = t >> 1, half = t & 1;  // A row and which 32-element block of the stage
-        const MatPtrs &M = (GATEUP && arow >= 64) ? a.A1 : a.A0;
-        int wrow;                        // weight row of A row arow (may be >= rows for the last down tile)
-        if (GATEUP)
-            wrow = mt * 64 + (arow & 63);
-        else
-            wrow = mt * 128 + arow;
-        const bool row_ok = wrow < a.rows;
-        const uint8_t *srow = mat_scales(M, e, E) + (size_t)(row_ok ? wrow : 0) * nb + half;
-        // this thread's scale byte per k-block, loaded four k-blocks ahead
-        auto ldsc = [&](int k) -> uint32_t { return (k < nkb && row_ok) ? (uint32_t)__ldg(srow + 2 * k) : 127u; };
-        uint32_t q0 = ldsc(0), q1 = ldsc(1), q2 = ldsc(2), q3 = ldsc(3);
-        bool ok = true;
-        for (int kb = 0; kb < nkb; kb++) {
-            const int s = kb % kStages;
-            if (kb >= kStages) {
-                ok = mbar_wait(&empty[s], ((kb / kStages) - 1) & 1, status, 30);
-                if (!ok) break;
-            }
-            const uint32_t sc = q0;
-            q0 = q1;
-            q1 = q2;
-            q2 = q3;
-            q3 = ldsc(kb + 4);
-            // A: wait for the packed codes, dequantise half a row
-            ok = mbar_wait(&full_fp4[s], (kb / kStages) & 1, status, 31);
-            if (!ok) break;
-            const uint4 c = *reinterpret_cast<const uint4 *>(sF + s * kFp4Bytes + arow * 32 + half * 16);
-            const bool big = sc > 128u;
-            const uint32_t l = scale_lo(sc), h = scale_hi(sc);
-            unsigned char *adst = sA + s * kABytes;
-            *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 0)) = dequant8(c.x, l, h, big);
-            *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 1)) = dequant8(c.y, l, h, big);
-            *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 2)) = dequant8(c.z, l, h, big);
-            *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 3)) = dequant8(c.w, l, h, big);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full_ab[s]);
-        }
-        if (warp < 6) {
-        // ------------------------------------------------------------ epilogue
-        if (ok) ok = mbar_wait(acc_full, 0, status, 40);
-        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
-        tc_fence_after();
-        const int q = warp & 3;                  // TMEM lane quarter of this warp
-        const int lrow = q * 32 + lane;          // accumulator row (= A row)
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-        float *xch = reinterpret_cast<float *>(sA);  // [64][33] exchange buffer (stages are idle now)
-        for (int c0 = 0; c0 < n_mma; c0 += 32) {
-            float v[32];
-            if (ok) tmem_ld32(taddr + c0, v);
+        // ------------------------------------------ epilogue (warps 11..14)
+        const int q = warp & 3;  // TMEM lane quarter of this warp
+        int li = 0;
+        for (int it = blockIdx.x; it < n_items; it += gridDim.x, li++) {
+            const int tile = it / mtiles, mt = it - tile * mtiles;
+            const int4 tl = tile_at(tile);
+            const int e = tl.x, rstart = tl.y, rcount = tl.z;
+            const int ab = li & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[ab], (li >> 1) & 1, status, 40))) break;
+            if (it == (int)blockIdx.x && warp == kWarpEpi0 && lane == 0) MOE_PF_MARK(1);
+            tc_fence_after();
+            const uint32_t taddr = tmem + (uint32_t)(ab * kAccCols) + ((uint32_t)(q * 32) << 16);
             if (GATEUP) {
-                if (q >= 2) {
+                // gate row j sits in TMEM lane j, up row j in lane 64 + j: warps q and
+                // q + 2 hold the two halves of row j's pair and swap half of their
+                // columns through shared memory, so that each computes 16 of every 32
+                const int jl = (q & 1) * 32 + lane, j = mt * 64 + jl;
+                const bool gate_w = q < 2;
+                const float bg = mat_bias(a.A0, e, E)[j], bu = mat_bias(a.A1, e, E)[j];
+                const int pj = F16 ? j : mma_perm_pos(j);
+                uint16_t *hdst = (F16 ? a.ws.h16 : a.ws.h) + (size_t)rstart * a.bp.F + pj;
+                float *xg = xch + jl * 17, *xu = xch + 64 * 17 + jl * 17;
+                for (int c0 = 0; c0 < rcount; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c0, v);
 #pragma unroll
-                    for (int c = 0; c < 32; c++) xch[(lrow - 64) * 33 + c] = v[c];
-                }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (q < 2 && ok) {
-                    const int j = mt * 64 + lrow;
-                    const float bg = mat_bias(a.A0, e, E)[j], bu = mat_bias(a.A1, e, E)[j];
-                    const int pj = mma_perm_pos(j);
-#pragma unroll
-                    for (int c = 0; c < 32; c++) {
-                        if (c0 + c >= rcount) continue;
-                        const float hv = swiglu_clamped(v[c] + bg, xch[lrow * 33 + c] + bu, a.bp.alpha, a.bp.limit);
-                        __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                        a.ws.h[(size_t)(rstart + c0 + c) * a.bp.F + pj] = *reinterpret_cast<uint16_t *>(&hb);
+                    for (int c = 0; c < 16; c++) {
+                        if (gate_w)
+                            xg[c] = v[16 + c];
+                        else
+                            xu[c] = v[c];
                     }
+                    named_bar_sync(1 + (q & 1), 64);
+                    const int cb = c0 + (gate_w ? 0 : 16);
+#pragma unroll
+                    for (int c = 0; c < 16; c++) {
+                        if (cb + c >= rcount) continue;
+                        const float gv = gate_w ? v[c] : xg[c], uv = gate_w ? xu[c] : v[16 + c];
+                        const float hv = swiglu_clamped(gv + bg, uv + bu, a.bp.alpha, a.bp.limit);
+                        __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                        uint16_t bits = *reinterpret_cast<uint16_t *>(&hb);
+                        if (F16) {
+                            const __half hh = __float2half_rn(__bfloat162float(hb));  // exact in the fp16 range
+                            bits = *reinterpret_cast<const uint16_t *>(&hh);
+                        }
+                        hdst[(size_t)(cb + c) * a.bp.F] = bits;
+                    }
+                    named_bar_sync(1 + (q & 1), 64);
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-            } else if (ok) {
-                const int i = mt * 128 + lrow;
-                if (i < a.rows) {
-                    const float bd = mat_bias(a.A0, e, E)[i];
+            } else {
+                const int i = mt * 128 + q * 32 + lane;
+                const bool row_ok = i < a.rows;
+                const float bd = row_ok ? mat_bias(a.A0, e, E)[i] : 0.0f;
+                for (int c0 = 0; c0 < rcount; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c0, v);
+                    if (!row_ok) continue;
 #pragma unroll
                     for (int c = 0; c < 32; c++) {
                         if (c0 + c >= rcount) continue;
@@ -383,12 +560,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                     }
                 }
             }
+            // the accumulator may be overwritten once every lane's TMEM reads are done
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[ab]);
         }
-        }
+        if (warp == kWarpEpi0 && lane == 0) MOE_PF_MARK(2);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem));
+    MOE_PF_MARK(3);
+    if (warp == kWarpMma)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
 }
 
 // ------------------------------------------------------------------ host side
@@ -421,31 +604,35 @@ cudaError_t make_codes_map(CUtensorMap *m, const uint8_t *codes, size_t n_rows, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-size_t prefill_smem_bytes() { return 1024 + kStages * (kABytes + kBBytes + kFp4Bytes) + 256; }
+size_t prefill_smem_bytes() {
+    return 1024 + kStages * (kABytes + kBBytes) + kCStages * kFp4Bytes + kXchFloats * 4 + kSmTiles * 16 + 512;
+}
 
 // 2D map over a bf16 activation matrix [rows][K]: box 64 elements (128 B) x 32
 // rows, 128-byte swizzle (the K-major layout the MMA descriptors expect; a
 // 32-row box is four whole 8-row swizzle atoms).
-cudaError_t make_act_map(CUtensorMap *m, const uint16_t *base, int rows, int K) {
+cudaError_t make_act_map(CUtensorMap *m, const uint16_t *base, int rows, int K, bool f16) {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {(cuuint32_t)kBK, 32};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base), dims, strides, box,
+    CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<uint16_t *>(base), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// xs[pos] = x_hat_mma[perm_token[pos]] (16-byte chunks), pos < R.
-__global__ void __launch_bounds__(256) moe_gather_kernel(Workspace ws, int H, int R) {
+// xs[pos] = src[perm_token[pos]] (16-byte chunks), pos < R; src is x_hat16
+// (fp16 variant) or x_hat_mma (bf16 variant).
+__global__ void __launch_bounds__(256) moe_gather_kernel(Workspace ws, const uint16_t *src, int H, int R) {
     const int cpr = H / 8;  // 16-byte chunks per row
     const size_t n = (size_t)R * cpr;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const int pos = (int)(i / cpr), c = (int)(i - (size_t)pos * cpr);
         const int tok = ws.perm_token[pos];
         reinterpret_cast<uint4 *>(ws.xs + (size_t)pos * H)[c] =
-            reinterpret_cast<const uint4 *>(ws.xhat_mma + (size_t)tok * H)[c];
+            reinterpret_cast<const uint4 *>(src + (size_t)tok * H)[c];
     }
 }
 
@@ -469,32 +656,43 @@ cudaError_t prefill_make_maps(const BlockParams &bp, const MatPtrs &gate, const 
     return cudaSuccess;
 }
 
-cudaError_t launch_gather(const BlockParams &bp, const Workspace &ws, int T, cudaStream_t st) {
+cudaError_t launch_gather(const BlockParams &bp, const Workspace &ws, int T, bool f16, cudaStream_t st) {
     const int R = T * (bp.K + bp.n_shared);
     const size_t n = (size_t)R * (bp.H / 8);
     const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    moe_gather_kernel<<<blocks, 256, 0, st>>>(ws, bp.H, R);
+    moe_gather_kernel<<<blocks, 256, 0, st>>>(ws, f16 ? ws.xhat16 : ws.xhat_mma, bp.H, R);
+    return cudaGetLastError();
+}
+
+template <bool GATEUP, bool F16>
+cudaError_t launch_pf(const PrefillArgs &args, const TmaMaps &maps, const CUtensorMap &bmap, dim3 grid,
+                      cudaStream_t st) {
+    static bool done = false;
+    MOE_CUDA_TRY(smem_optin_once(moe_prefill_kernel<GATEUP, F16>, done));
+    moe_prefill_kernel<GATEUP, F16><<<grid, kThreads, prefill_smem_bytes(), st>>>(args, maps, bmap);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0, const MatPtrs &a1,
-                                 bool gateup, int T, const TmaMaps &maps, cudaStream_t st) {
+                                 bool gateup, int T, const TmaMaps &maps, bool f16, cudaStream_t st) {
     PrefillArgs args{bp, ws, a0, a1, gateup ? bp.H : bp.F, gateup ? bp.F : bp.H};
     const int R = T * (bp.K + bp.n_shared);
     CUtensorMap bmap;
     MOE_CUDA_TRY(get_encoder());
-    MOE_CUDA_TRY(make_act_map(&bmap, gateup ? ws.xs : ws.h, R, args.Kdim));
+    const uint16_t *bsrc = gateup ? ws.xs : (f16 ? ws.h16 : ws.h);
+    MOE_CUDA_TRY(make_act_map(&bmap, bsrc, R, args.Kdim, f16));
     int tiles = (R + kBN - 1) / kBN + bp.E + bp.n_shared;
     if (tiles > ws.max_tiles) tiles = ws.max_tiles;
     const int mtiles = gateup ? bp.F / 64 : (bp.H + 127) / 128;
-    const size_t sm = prefill_smem_bytes();
-    static bool done_gu = false, done_dn = false;
-    if (gateup) {
-        MOE_CUDA_TRY(smem_optin_once(moe_prefill_kernel<true>, done_gu));
-        moe_prefill_kernel<true><<<dim3(tiles, mtiles), kThreads, sm, st>>>(args, maps, bmap);
-    } else {
-        MOE_CUDA_TRY(smem_optin_once(moe_prefill_kernel<false>, done_dn));
-        moe_prefill_kernel<false><<<dim3(tiles, mtiles), kThreads, sm, st>>>(args, maps, bmap);
+    // persistent: one CTA per SM, or fewer when there are fewer work items
+    static int n_sm = 0;
+    if (!n_sm) {
+        int dev = 0;
+        MOE_CUDA_TRY(cudaGetDevice(&dev));
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
     }
-    return cudaGetLastError();
+    const long items = (long)tiles * mtiles;
+    const dim3 grid((unsigned)(items < n_sm ? items : n_sm));
+    if (gateup) return f16 ? launch_pf<true, true>(args, maps, bmap, grid, st) : launch_pf<true, false>(args, maps, bmap, grid, st);
+    return f16 ? launch_pf<false, true>(args, maps, bmap, grid, st) : launch_pf<false, false>(args, maps, bmap, grid, st);
 }

@@ -204,3 +204,16 @@ def test_block_parity_bf16_activation_gemvs(H, F, gamma_mul, limit, T):
     assert r["status"] == 0
     assert np.array_equal(r["ids"], ref["ids"])
     check_close(r["out"], ref["out"], x)
+
+
+@pytest.mark.parametrize("elo,ehi", [(118, 124), (90, 150)])
+def test_grouped_gemm_fp16_and_bf16_variants(elo, ehi):
+    # exponents inside [104, 140] take the fp16-operand grouped GEMM, wider ones the bf16 one
+    shape = synth.tiny_shape(128, 192, 6, 2)
+    blk = tiny_block(elo, shape, elo=elo, ehi=ehi)
+    x = synth.f32_to_bf16_bits(np.random.default_rng(elo).normal(0, 1, (45, 128)))
+    r, _, _ = run_gpu(blk, x, path=2)
+    ref = oracle.moe_forward(blk, x, nthreads=NTHREADS)
+    assert r["status"] == 0
+    assert np.array_equal(r["ids"], ref["ids"])
+    check_close(r["out"], ref["out"], x)
