@@ -58,6 +58,8 @@ struct moe_plan {
     MatPtrs gate{}, up{}, down{};
     PrefillMaps maps{};
     bool have_maps = false;
+    uint8_t *pf_scales = nullptr;    // owned: the scales repacked for the grouped GEMM
+    size_t pf_scales_bytes = 0;
     // the decode GEMVs carry x_hat / h as fp16 unless these can leave its range
     bool x_bf16 = false, h_bf16 = false;
     // the grouped GEMM takes fp16 operands (exponents in [104, 140], fp16-range activations)
@@ -202,6 +204,7 @@ moe_plan *moe_plan_create(int hidden, int expert_hidden, int n_experts, int top_
 void moe_plan_destroy(moe_plan *plan) {
     if (!plan) return;
     for (auto &e : plan->ev) cudaEventDestroy(e);
+    if (plan->pf_scales) cudaFree(plan->pf_scales);
     delete plan;
 }
 
@@ -314,8 +317,26 @@ int moe_load_weights(moe_plan *p, const moe_weights *w) {
     p->gate = mat_of(w->gate, w->sh_gate, b.F, b.H);
     p->up = mat_of(w->up, w->sh_up, b.F, b.H);
     p->down = mat_of(w->down, w->sh_down, b.H, b.F);
-    p->have_maps = (b.H % 64 == 0 && b.F % 64 == 0) &&
-                   prefill_make_maps(b, p->gate, p->up, p->down, &p->maps) == cudaSuccess;
+    p->have_maps = false;
+    if (b.H % 64 == 0 && b.F % 64 == 0 && prefill_make_maps(b, p->gate, p->up, p->down, &p->maps) == cudaSuccess) {
+        const size_t nbytes = prefill_scales_bytes(b);
+        if (p->pf_scales && p->pf_scales_bytes != nbytes) {
+            cudaFree(p->pf_scales);
+            p->pf_scales = nullptr;
+        }
+        if (!p->pf_scales) {
+            e = cudaMalloc(&p->pf_scales, nbytes);
+            if (e != cudaSuccess) {
+                p->pf_scales = nullptr;
+                return cuda_fail(e, "moe_load_weights (repacked scales)");
+            }
+            p->pf_scales_bytes = nbytes;
+        }
+        e = prefill_pack_scales(b, p->gate, p->up, p->down, p->pf_scales, &p->maps, 0);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_load_weights (repacked scales)");
+        p->have_maps = true;
+    }
     // fp16 holds the GEMV activations below 65504: |x_hat| <= sqrt(H) max|gamma|;
     // |h| <= max(|L|, 0.3/alpha) (|L| + 1), since x sigmoid(alpha x) >= -0.28/alpha
     const double xb = std::sqrt((double)b.H) * (double)gmax * 1.01;

@@ -182,15 +182,26 @@ cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, cons
                                 cudaStream_t st);
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T,
                            float *out, cudaStream_t st);
-// TMA descriptors of the packed codes: [0] routed A0, [1] routed A1, [2] shared A0, [3] shared A1.
+// What the grouped GEMM reads its weights through: TMA descriptors of the
+// packed codes and the scales repacked into 128-byte chunks (the two E8M0
+// bytes of one 64-element k-block for 64 consecutive rows, chunk (block b,
+// k-block kb) at byte ((b * nkb) + kb) * 128, b = expert * row_blocks + row / 64).
+// Index [0] routed A0, [1] routed A1, [2] shared A0, [3] shared A1.
 struct TmaMaps {
     CUtensorMap m[4];
+    const uint8_t *sc[4];
+    int row_blocks;     // 64-row blocks per expert matrix
 };
 struct PrefillMaps {
     TmaMaps gateup, down;
 };
 cudaError_t prefill_make_maps(const BlockParams &bp, const MatPtrs &gate, const MatPtrs &up, const MatPtrs &down,
                               PrefillMaps *out);
+// Bytes of the repacked scale buffer, and the repack itself (enqueued on st;
+// fills the sc / row_blocks fields of *out).
+size_t prefill_scales_bytes(const BlockParams &bp);
+cudaError_t prefill_pack_scales(const BlockParams &bp, const MatPtrs &gate, const MatPtrs &up, const MatPtrs &down,
+                                uint8_t *buf, PrefillMaps *out, cudaStream_t st);
 // f16: the fp16-operand variant (E8M0 exponents in [104, 140], fp16-range activations).
 cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
                                  const MatPtrs &a1, bool gateup, int T, const TmaMaps &maps, bool f16,

@@ -50,7 +50,9 @@ constexpr int kCStages = 8;         // packed-code stages (prefetched further ah
 constexpr int kBK = 64;            // K elements per stage (one 128-byte swizzle row of bf16)
 constexpr int kBN = 128;           // max routes per tile
 constexpr int kWarpCodes = 0, kWarpMma = 1, kWarpB = 2, kWarpDq0 = 3;
-constexpr int kDqWarps = 8;                   // dequantising warps (2 threads per A row)
+constexpr int kDqWarps = 8;                   // dequantising warps
+constexpr int kDqGroups = 4;                  // k-blocks are dealt round-robin to this many warp groups
+constexpr int kDqGroupWarps = kDqWarps / kDqGroups;
 constexpr int kWarpEpi0 = kWarpDq0 + kDqWarps, kEpiWarps = 4;
 constexpr int kThreads = 32 * (kWarpEpi0 + kEpiWarps);
 constexpr int kAccCols = 128;                 // one fp32 accumulator: 128 lanes x N <= 128 columns
@@ -60,6 +62,8 @@ constexpr int kSmTiles = 256;                 // route tiles cached in shared me
 constexpr int kABytes = 128 * 128;     // A stage: 128 rows x 128 B
 constexpr int kBBytes = kBN * 128;     // B stage
 constexpr int kFp4Bytes = 128 * 32;    // packed codes of one stage
+constexpr int kScBytes = 2 * 128;      // its scale bytes: two 128-byte chunks (64 rows x 2 blocks each)
+constexpr int kCStageBytes = kFp4Bytes + kScBytes;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct PrefillArgs {
@@ -153,6 +157,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         "[%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
+}
+
+// Untiled bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -281,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *sA = smem;                                   // [kStages][128 rows][128 B] swizzled
     unsigned char *sB = sA + kStages * kABytes;                 // [kStages][kBN rows][128 B] swizzled
-    unsigned char *sF = sB + kStages * kBBytes;                 // [kCStages][128 rows][32 B] packed codes
-    float *xch = reinterpret_cast<float *>(sF + kCStages * kFp4Bytes);  // gate/up exchange [2][64][17]
+    unsigned char *sF = sB + kStages * kBBytes;                 // [kCStages][codes 128 x 32 B, scales 2 x 128 B]
+    float *xch = reinterpret_cast<float *>(sF + kCStages * kCStageBytes);  // gate/up exchange [2][64][17]
     int4 *s_tiles = reinterpret_cast<int4 *>(xch + kXchFloats);          // [kSmTiles]
     uint64_t *bars = reinterpret_cast<uint64_t *>(s_tiles + kSmTiles);
     uint64_t *full_c = bars, *empty_c = bars + kCStages;                    // code ring
@@ -292,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
     MOE_PF_MARK(0);
-    const int E = a.bp.E, K = a.Kdim, nb = K / 32, nkb = K / kBK;
+    const int E = a.bp.E, K = a.Kdim, nkb = K / kBK;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = a.ws.status;
 
@@ -300,10 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
     if (threadIdx.x == 0) {
         for (int s = 0; s < kCStages; s++) {
             mbar_init(&full_c[s], 1);
-            mbar_init(&empty_c[s], kDqWarps);
+            mbar_init(&empty_c[s], kDqGroupWarps);
         }
         for (int s = 0; s < kStages; s++) {
-            mbar_init(&full_ab[s], kDqWarps);
+            mbar_init(&full_ab[s], kDqGroupWarps);
             mbar_init(&full_b[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -338,14 +350,25 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                 const CUtensorMap *m0 = shared_e ? &maps.m[2] : &maps.m[0];
                 const CUtensorMap *m1 = shared_e ? &maps.m[3] : &maps.m[1];
                 const int ebase = shared_e ? 0 : e;
+                // scale chunks of this item's two 64-row blocks (gate and up rows, or
+                // rows 128 mt .. 128 mt + 127), one per k-block
+                const size_t cb = (size_t)nkb * 128;
+                const uint8_t *sc0, *sc1;
+                if (GATEUP) {
+                    sc0 = maps.sc[shared_e ? 2 : 0] + (size_t)(ebase * maps.row_blocks + mt) * cb;
+                    sc1 = maps.sc[shared_e ? 3 : 1] + (size_t)(ebase * maps.row_blocks + mt) * cb;
+                } else {
+                    sc0 = maps.sc[shared_e ? 2 : 0] + (size_t)(ebase * maps.row_blocks + 2 * mt) * cb;
+                    sc1 = sc0 + cb;
+                }
                 for (int kb = 0; kb < nkb; kb++, g++) {
                     if (!mbar_wait(&empty_c[r.s], r.ph ^ 1, status, 10)) {
                         ok = false;
                         break;
                     }
                     MOE_PF_KMARK(5, g);
-                    mbar_expect_tx(&full_c[r.s], kFp4Bytes);
-                    unsigned char *dst = sF + r.s * kFp4Bytes;
+                    mbar_expect_tx(&full_c[r.s], kCStageBytes);
+                    unsigned char *dst = sF + r.s * kCStageBytes;
                     if (GATEUP) {
                         const int y = ebase * a.rows + mt * 64;
                         tma_load_2d(dst, m0, &full_c[r.s], kb * 32, y);
@@ -353,6 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                     } else {
                         tma_load_2d(dst, m0, &full_c[r.s], kb * 32, ebase * a.rows + mt * 128);
                     }
+                    bulk_load(dst + kFp4Bytes, sc0 + (size_t)kb * 128, 128, &full_c[r.s]);
+                    bulk_load(dst + kFp4Bytes + 128, sc1 + (size_t)kb * 128, 128, &full_c[r.s]);
                     issued++;
                     r.next(kCStages);
                 }
@@ -427,48 +452,28 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
         }
     } else if (warp < kWarpEpi0) {
         // ------------------------------------------ dequant (warps 3..10)
-        const int t = threadIdx.x - 32 * kWarpDq0;  // 0..255
-        const int arow = t >> 1, half = t & 1;      // A row and which 32-element block of the stage
-        // this thread's scale row in item it (nullptr: the row lies past the matrix)
-        auto scale_row = [&](int it) -> const uint8_t * {
-            if (it >= n_items) return nullptr;
-            const int tile = it / mtiles, mt = it - tile * mtiles;
-            const int e = tile_at(tile).x;
-            const MatPtrs &M = (GATEUP && arow >= 64) ? a.A1 : a.A0;
-            const int wrow = GATEUP ? mt * 64 + (arow & 63) : mt * 128 + arow;
-            return wrow < a.rows ? mat_scales(M, e, E) + (size_t)wrow * nb + half : nullptr;
-        };
-        // scale bytes are read four k-blocks ahead, across item boundaries
-        int la_it = blockIdx.x, la_kb = 0;
-        const uint8_t *la_p = scale_row(la_it);
-        auto next_scale = [&]() -> uint32_t {
-            const uint32_t v = la_p ? (uint32_t)__ldg(la_p + 2 * la_kb) : 127u;
-            if (++la_kb == nkb) {
-                la_kb = 0;
-                la_it += gridDim.x;
-                la_p = scale_row(la_it);
-            }
-            return v;
-        };
-        uint32_t q0 = next_scale(), q1 = next_scale(), q2 = next_scale(), q3 = next_scale();
-        Ring r, rc;
-        bool ok = true;
-        int g = 0;
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-            for (int kb = 0; kb < nkb; kb++, g++) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&empty[r.s], r.ph ^ 1, status, 30));
-                if (!ok) break;
-                const uint32_t sc = q0;
-                q0 = q1;
-                q1 = q2;
-                q2 = q3;
-                q3 = next_scale();
-                if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(1, g);
-                ok = __all_sync(0xffffffffu, mbar_wait(&full_c[rc.s], rc.ph, status, 31));
-                if (!ok) break;
-                if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(2, g);
-                const uint4 c = *reinterpret_cast<const uint4 *>(sF + rc.s * kFp4Bytes + arow * 32 + half * 16);
-                unsigned char *adst = sA + r.s * kABytes;
+        // Group grp (two warps) dequantises k-blocks g = grp, grp + 4, ... of the
+        // CTA's sequence, the whole 128 x 64 A stage each: a warp's fixed costs
+        // per stage (waits, proxy fence, arrivals) then overlap those of the
+        // other groups instead of adding up over every k-block.
+        const int grp = (warp - kWarpDq0) / kDqGroupWarps;
+        const int t = threadIdx.x - 32 * (kWarpDq0 + grp * kDqGroupWarps);  // 0..63
+        const int my_items = (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+        const int total = my_items * nkb;
+        for (int g = grp; g < total; g += kDqGroups) {
+            const int s = g % kStages, cs = g % kCStages;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, status, 30) &&
+                                                        mbar_wait(&full_c[cs], (g / kCStages) & 1, status, 31));
+            if (!ok) break;
+            if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(2, g);
+            const unsigned char *cst = sF + cs * kCStageBytes;
+            unsigned char *adst = sA + s * kABytes;
+            // unit u = (A row u / 2, 32-element half u % 2): 16 code bytes, one scale byte
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int u = t + 64 * i, arow = u >> 1, half = u & 1;
+                const uint4 c = *reinterpret_cast<const uint4 *>(cst + u * 16);
+                const uint32_t sc = cst[kFp4Bytes + u];
                 if (F16) {
                     const uint32_t sc2 = scale_f16x2(sc);
                     *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 0)) = dequant8_f16(c.x, sc2);
@@ -483,16 +488,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                     *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 2)) = dequant8(c.z, l, h, big);
                     *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 3)) = dequant8(c.w, l, h, big);
                 }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&full_ab[r.s]);
-                    mbar_arrive(&empty_c[rc.s]);
-                }
-                if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(6, g);
-                r.next(kStages);
-                rc.next(kCStages);
             }
+            if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(9, g);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&full_ab[s]);
+                mbar_arrive(&empty_c[cs]);
+            }
+            if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(6, g);
         }
     } else {
         // ------------------------------------------ epilogue (warps 11..14)
@@ -505,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
             const int ab = li & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[ab], (li >> 1) & 1, status, 40))) break;
             if (it == (int)blockIdx.x && warp == kWarpEpi0 && lane == 0) MOE_PF_MARK(1);
+            if (warp == kWarpEpi0 && lane == 0) MOE_PF_KMARK(7, li);
             tc_fence_after();
             const uint32_t taddr = tmem + (uint32_t)(ab * kAccCols) + ((uint32_t)(q * 32) << 16);
             if (GATEUP) {
@@ -564,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[ab]);
+            if (warp == kWarpEpi0 && lane == 0) MOE_PF_KMARK(8, li);
         }
         if (warp == kWarpEpi0 && lane == 0) MOE_PF_MARK(2);
     }
@@ -605,7 +611,7 @@ cudaError_t make_codes_map(CUtensorMap *m, const uint8_t *codes, size_t n_rows, 
 }
 
 size_t prefill_smem_bytes() {
-    return 1024 + kStages * (kABytes + kBBytes) + kCStages * kFp4Bytes + kXchFloats * 4 + kSmTiles * 16 + 512;
+    return 1024 + kStages * (kABytes + kBBytes) + kCStages * kCStageBytes + kXchFloats * 4 + kSmTiles * 16 + 512;
 }
 
 // 2D map over a bf16 activation matrix [rows][K]: box 64 elements (128 B) x 32
@@ -636,6 +642,27 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(Workspace ws, const uin
     }
 }
 
+// Scale repack: out chunk (block b, k-block kb) byte 2 r + h = scale of row
+// 64 (b % row_blocks) + r of expert b / row_blocks, 32-element block 2 kb + h;
+// rows past the matrix (and the trailing pad block) read 127, a scale of 1.
+__global__ void __launch_bounds__(256) moe_pack_scales_kernel(const uint8_t *in, uint8_t *out, int n_exp, int rows,
+                                                               int cols, size_t n_out) {
+    const int nb = cols / 32, nkb = cols / kBK, rb = (rows + 63) / 64;
+    const size_t per_block = (size_t)nkb * 128;
+    for (size_t o = (size_t)blockIdx.x * blockDim.x + threadIdx.x; o < n_out; o += (size_t)gridDim.x * blockDim.x) {
+        const size_t blk = o / per_block;
+        const int rem = (int)(o - blk * per_block);
+        const int kb = rem >> 7, r = (rem & 127) >> 1, h = rem & 1;
+        const int e = (int)(blk / rb), row = (int)(blk % rb) * 64 + r;
+        out[o] = (e < n_exp && row < rows) ? in[((size_t)e * rows + row) * nb + 2 * kb + h] : (uint8_t)127;
+    }
+}
+
+// bytes of one repacked matrix set: n_exp experts plus one pad block
+size_t packed_bytes(int n_exp, int rows, int cols) {
+    return (((size_t)n_exp * ((rows + 63) / 64) + 1) * (size_t)(cols / kBK) * 128 + 255) & ~(size_t)255;
+}
+
 }  // namespace
 
 int prefill_tile_rows() { return kBN; }
@@ -653,6 +680,41 @@ cudaError_t prefill_make_maps(const BlockParams &bp, const MatPtrs &gate, const 
     d.m[1] = d.m[0];
     MOE_CUDA_TRY(make_codes_map(&d.m[2], bp.n_shared ? down.sh_codes : nullptr, down.rows, down.cols, 128));
     d.m[3] = d.m[2];
+    return cudaSuccess;
+}
+
+size_t prefill_scales_bytes(const BlockParams &bp) {
+    const int ns = bp.n_shared ? 1 : 0;
+    return 2 * (packed_bytes(bp.E, bp.F, bp.H) + packed_bytes(ns, bp.F, bp.H)) + packed_bytes(bp.E, bp.H, bp.F) +
+           packed_bytes(ns, bp.H, bp.F);
+}
+
+cudaError_t prefill_pack_scales(const BlockParams &bp, const MatPtrs &gate, const MatPtrs &up, const MatPtrs &down,
+                                uint8_t *buf, PrefillMaps *out, cudaStream_t st) {
+    const MatPtrs *ms[3] = {&gate, &up, &down};
+    TmaMaps *tm[3] = {&out->gateup, &out->gateup, &out->down};
+    const int slot[3] = {0, 1, 0};
+    for (int i = 0; i < 3; i++) {
+        const MatPtrs &m = *ms[i];
+        for (int sh = 0; sh < 2; sh++) {
+            const int n_exp = sh ? (bp.n_shared ? 1 : 0) : bp.E;
+            const uint8_t *src = sh ? m.sh_scales : m.scales;
+            const size_t n = packed_bytes(n_exp, m.rows, m.cols);
+            const uint8_t *dst = nullptr;
+            if (n_exp) {
+                const size_t nout = ((size_t)n_exp * ((m.rows + 63) / 64) + 1) * (size_t)(m.cols / kBK) * 128;
+                const int blocks = (int)((nout + 255) / 256 < 8192 ? (nout + 255) / 256 : 8192);
+                moe_pack_scales_kernel<<<blocks, 256, 0, st>>>(src, buf, n_exp, m.rows, m.cols, nout);
+                MOE_CUDA_TRY(cudaGetLastError());
+                dst = buf;
+                buf += n;
+            }
+            tm[i]->sc[slot[i] + 2 * sh] = dst;
+        }
+        tm[i]->row_blocks = (m.rows + 63) / 64;
+    }
+    out->down.sc[1] = out->down.sc[0];
+    out->down.sc[3] = out->down.sc[2];
     return cudaSuccess;
 }
 
