@@ -11,7 +11,8 @@
 //  * one persistent CTA per SM: 14 consumer warps, 1 producer warp and 1
 //    epilogue warp (16 warps: 4 per SM sub-partition, up to 128 registers a
 //    thread);
-//  * work item = (tile of <= 8*NT routes of one expert, 16 weight rows); each
+//  * work item = (tile of <= 8*NT routes of one expert, 16 weight rows of gate
+//    and of up, or 32 rows of down -- about 46 KB of codes either way); each
 //    CTA walks a contiguous range of items;
 //  * the producer streams every item into a ring of S shared-memory stages
 //    (S = 2..8, as deep as shared memory allows), so that several items are in
@@ -173,16 +174,19 @@ struct DecGeom {
 // split-K partials: [2][kCW][NM][NT][16 rows][8 columns] fp32
 __host__ __device__ constexpr size_t dec_red_bytes(int NM, int NT) { return (size_t)2 * kCW * NM * NT * 128 * 4; }
 
-template <bool GATEUP, int NT, bool BF, int MP>
+// NM: matrices per item -- gate and up (gate/up), or for down 1 or 2 groups of
+// 16 consecutive rows (an item of 32 rows carries as many bytes as a gate/up item)
+template <bool GATEUP, int NT, bool BF, int MP, int NM>
 __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a) {
-    constexpr int NM = GATEUP ? 2 : 1;
+    static_assert(!GATEUP || NM == 2, "gate/up items hold both matrices");
+    constexpr int IR = GATEUP ? 16 : 16 * NM;  // output rows per item
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 4];
     uint64_t *full = bars, *empty = bars + kMaxStages, *redfull = bars + 2 * kMaxStages, *redempty = redfull + 2;
     const int K = a.Kdim, nb = K / 32, S = a.stages;
     const DecGeom geo(K, NM);
     float *red = reinterpret_cast<float *>(dsm + (size_t)S * geo.stage);
-    const int RB = a.rows / 16;
+    const int RB = a.rows / IR;
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; i++) {
             // one arrival with the codes' byte count + one per producer lane (its small copies)
@@ -216,7 +220,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
         auto issue = [&](int k) {
             const int s = k % S, item = begin + k;
             const int4 tile = a.ws.tiles[item / RB];
-            const int e = tile.x, j0 = (item % RB) * 16;
+            const int e = tile.x, j0 = (item % RB) * IR;
             unsigned char *st = dsm + (size_t)s * geo.stage;
             if (lane == 0) {
                 const uint32_t bytes = NM * 16 * (K / 2);
@@ -227,16 +231,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
 #pragma unroll
                 for (int m = 0; m < NM; m++) {
                     const MatPtrs &M = m == 0 ? a.A0 : a.A1;
-                    bulk_g2s(st + m * 16 * geo.rs, mat_codes(M, e, E) + (size_t)j0 * (K / 2), 16 * (K / 2), &full[s]);
+                    const int jm = GATEUP ? j0 : j0 + 16 * m;
+                    bulk_g2s(st + m * 16 * geo.rs, mat_codes(M, e, E) + (size_t)jm * (K / 2), 16 * (K / 2), &full[s]);
                 }
             }
 #pragma unroll
             for (int m = 0; m < NM; m++) {
                 const MatPtrs &M = m == 0 ? a.A0 : a.A1;
-                const uint8_t *scs = mat_scales(M, e, E) + (size_t)j0 * nb;
+                const int jm = GATEUP ? j0 : j0 + 16 * m;
+                const uint8_t *scs = mat_scales(M, e, E) + (size_t)jm * nb;
                 unsigned char *scd = st + NM * 16 * geo.rs + m * geo.scb;
                 for (int c = lane; c < nb; c += 32) cp_async16(scd + 16 * c, scs + 16 * c);
-                if (lane < 4) cp_async16(st + geo.bias + m * 64 + 16 * lane, mat_bias(M, e, E) + j0 + 4 * lane);
+                if (lane < 4) cp_async16(st + geo.bias + m * 64 + 16 * lane, mat_bias(M, e, E) + jm + 4 * lane);
             }
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&full[s])) : "memory");
             if (lane == 0) MOE_DEC_MARK(0, k);
@@ -256,14 +262,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
             // this item's biases, read before the stage may be refilled
             if (!dec_mbar_wait(&full[s], (k / S) & 1, status, 55)) break;
             const float *sb = reinterpret_cast<const float *>(dsm + (size_t)s * geo.stage + geo.bias);
-            const float b0 = sb[lane >> 1], b1 = GATEUP ? sb[16 + (lane >> 1)] : 0.f;
+            const float b0 = sb[lane >> 1], b1 = NM == 2 ? sb[16 + (lane >> 1)] : 0.f;
             asm volatile("" ::"f"(b0), "f"(b1));
             __syncwarp();
             if (lane == 0) dec_arrive(&empty[s]);
             if (!dec_mbar_wait(&redfull[r], (k >> 1) & 1, status, 54)) break;
             if (lane == 0) MOE_DEC_MARK(3, k);
             const int4 tile = a.ws.tiles[item / RB];
-            const int rstart = tile.y, rcount = tile.z, j0 = (item % RB) * 16;
+            const int rstart = tile.y, rcount = tile.z, j0 = (item % RB) * IR;
             // lane: row lane/2, columns 4*(lane&1) .. +3 of every column group nn
             const int row = lane >> 1, c0 = 4 * (lane & 1);
             const float *rr = red + (size_t)r * kCW * NM * NT * 128;
@@ -303,6 +309,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
                         }
                     } else {
                         a.ws.y[(size_t)route * a.bp.H + j] = a.ws.perm_w[route] * (s0[c] + b0);
+                    }
+                }
+                if (!GATEUP && NM == 2) {
+                    // the second group of 16 rows (a separate pass keeps the live ranges short)
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        const int col = nn * 8 + c0 + c;
+                        if (col >= rcount) continue;
+                        const int route = rstart + col;
+                        a.ws.y[(size_t)route * a.bp.H + j + 16] = a.ws.perm_w[route] * (s1[c] + b1);
                     }
                 }
             }
@@ -525,11 +541,10 @@ struct KernelInfo {
     int n_sm = 0, avail = 0;
 };
 
-template <bool GATEUP, int NT, bool BF, int MP>
+template <bool GATEUP, int NT, bool BF, int MP, int NM>
 static cudaError_t launch_one(DecodeArgs a, int n_items_max, cudaStream_t st) {
-    constexpr int NM = GATEUP ? 2 : 1;
     static KernelInfo ki;
-    auto kern = moe_decode_kernel<GATEUP, NT, BF, MP>;
+    auto kern = moe_decode_kernel<GATEUP, NT, BF, MP, NM>;
     if (!ki.done) {
         bool opt = false;
         MOE_CUDA_TRY(smem_optin_once(kern, opt));
@@ -556,16 +571,21 @@ static cudaError_t launch_one(DecodeArgs a, int n_items_max, cudaStream_t st) {
 
 // variant choice: bf16 activations, and the number of block pairs a warp covers
 // (fewer pairs, fewer registers for the activations of 8-route tiles)
-template <bool GATEUP, int NT, bool BF>
+template <bool GATEUP, int NT, bool BF, int NM>
 static cudaError_t launch_mp(const DecodeArgs &a, int n_items_max, cudaStream_t st) {
     const int ppw = ((a.Kdim / 32 + 1) / 2 + kCW - 1) / kCW;
-    if (ppw <= 3) return launch_one<GATEUP, NT, BF, 3>(a, n_items_max, st);
-    if (ppw <= 4) return launch_one<GATEUP, NT, BF, 4>(a, n_items_max, st);
-    return launch_one<GATEUP, NT, BF, kMaxPairs>(a, n_items_max, st);
+    if (ppw <= 3) return launch_one<GATEUP, NT, BF, 3, NM>(a, n_items_max, st);
+    if (ppw <= 4) return launch_one<GATEUP, NT, BF, 4, NM>(a, n_items_max, st);
+    return launch_one<GATEUP, NT, BF, kMaxPairs, NM>(a, n_items_max, st);
 }
-template <bool GATEUP, int NT>
+template <bool GATEUP, int NT, int NM>
 static cudaError_t launch_bf(const DecodeArgs &a, bool bf, int n_items_max, cudaStream_t st) {
-    return bf ? launch_mp<GATEUP, NT, true>(a, n_items_max, st) : launch_mp<GATEUP, NT, false>(a, n_items_max, st);
+    return bf ? launch_mp<GATEUP, NT, true, NM>(a, n_items_max, st)
+              : launch_mp<GATEUP, NT, false, NM>(a, n_items_max, st);
+}
+// down items of 32 rows when H allows it and two such stages fit beside the partials
+bool down_rows32(const BlockParams &bp) {
+    return bp.H % 32 == 0 && 2 * (size_t)DecGeom(bp.F, 2).stage + dec_red_bytes(2, 2) + 1024 <= 227 * 1024;
 }
 
 }  // namespace
@@ -588,11 +608,15 @@ cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, cons
     if (gateup) {
         DecodeArgs gu{bp, ws, a0, a1, bp.H, bp.F, 0, h_bf16 ? 1 : 0};
         const int items = tiles * (bp.F / 16);
-        return nt == 1 ? launch_bf<true, 1>(gu, x_bf16, items, st) : launch_bf<true, 2>(gu, x_bf16, items, st);
+        return nt == 1 ? launch_bf<true, 1, 2>(gu, x_bf16, items, st) : launch_bf<true, 2, 2>(gu, x_bf16, items, st);
     }
     DecodeArgs dn{bp, ws, a0, a0, bp.F, bp.H, 0, 0};
+    if (down_rows32(bp)) {
+        const int items = tiles * (bp.H / 32);
+        return nt == 1 ? launch_bf<false, 1, 2>(dn, h_bf16, items, st) : launch_bf<false, 2, 2>(dn, h_bf16, items, st);
+    }
     const int items = tiles * (bp.H / 16);
-    return nt == 1 ? launch_bf<false, 1>(dn, h_bf16, items, st) : launch_bf<false, 2>(dn, h_bf16, items, st);
+    return nt == 1 ? launch_bf<false, 1, 1>(dn, h_bf16, items, st) : launch_bf<false, 2, 1>(dn, h_bf16, items, st);
 }
 
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T, float *out,
