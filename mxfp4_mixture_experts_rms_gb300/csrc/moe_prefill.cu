@@ -1,29 +1,29 @@
 // moe_prefill.cu -- prefill path: grouped per-expert GEMMs on the 5th-gen
-// tensor cores (tcgen05.mma kind::f16, bf16 operands in shared memory, fp32
-// accumulators in TMEM), with MXFP4 weight tiles staged by TMA and
-// dequantised to bf16 in shared memory.
+// tensor cores (tcgen05.mma kind::f16, fp32 accumulators in TMEM), with MXFP4
+// weight tiles staged by TMA and dequantised by the SM into TMEM.
 //
 // goosedump gpt_oss.rs `expert_batch_output` gathers the routed rows of one
 // expert and runs `matrix_matrix_pair(gate, up)` + bias, `swiglu_inplace`,
 // `matrix_matrix(down)` + bias and the route weight; `mix_expert_outputs`
-// then sums each token's slots.  Here one CTA computes one (expert tile of
-// <= 128 routes) x (weight row tile) block:
+// then sums each token's slots.  Here a work item is one (expert tile of
+// <= 128 routes) x (weight row block) block:
 //
 //   gate/up kernel: A = [64 gate rows ; the same 64 up rows] (M = 128),
 //                   B = the tile's x_hat rows, D = TMEM [128 lanes][N];
-//                   epilogue: bias + clamped SwiGLU -> h (bf16)
+//                   epilogue: bias + clamped SwiGLU -> h
 //   down kernel:    A = 128 rows of Wd, B = the tile's h rows;
 //                   epilogue: bias, times the route weight -> per-route fp32
 //
-// The kernel is persistent (one CTA per SM walking a static list of
-// (route tile, weight-row block) items) with warp roles: a TMA warp for the
-// packed codes, a TMA warp for the B tile (128-byte swizzled, straight into
-// the MMA layout; the x_hat rows are first gathered into route order by
-// moe_gather_kernel), an MMA warp that owns TMEM, eight dequantising warps
-// (two threads per A row) and four epilogue warps that drain one of two TMEM
+// The kernel is persistent (one CTA per SM walking a static list of items)
+// with warp roles: a TMA warp for the packed codes and their scales, a TMA
+// warp for the B tile (128-byte swizzled, straight into the MMA layout; the
+// x_hat rows are first gathered into route order by moe_gather_kernel), an
+// MMA warp that owns all 512 TMEM columns, eight dequantising warps that
+// write A straight into TMEM (tcgen05.st; the MMA reads A from TMEM and B
+// from shared memory), and four epilogue warps that drain one of two TMEM
 // accumulators while the MMA fills the other.  mbarrier rings connect them.
 // The bf16 variant keeps activations in a 32-block pair order (x_hat_mma / h)
-// and writes A in that order straight from the nibble-pair dequantiser, so
+// and produces A in that order straight from the nibble-pair dequantiser, so
 // the K permutation cancels in every dot product.
 //
 // Every wait is bounded (about 2 s of %globaltimer); on a timeout the kernel
@@ -45,26 +45,36 @@
 
 namespace {
 
-constexpr int kStages = 5;          // A (dequantised) + B stages, consumed by the MMA
-constexpr int kCStages = 8;         // packed-code stages (prefetched further ahead)
+constexpr int kStages = 8;          // A (dequantised, in TMEM) + B (shared memory) stages, consumed by the MMA
+constexpr int kCK = 2;              // k-blocks per packed-code stage
+constexpr int kCStages = 6;         // packed-code stages (12 k-blocks ahead)
 constexpr int kBK = 64;            // K elements per stage (one 128-byte swizzle row of bf16)
 constexpr int kBN = 128;           // max routes per tile
 constexpr int kWarpCodes = 0, kWarpMma = 1, kWarpB = 2, kWarpDq0 = 3;
 constexpr int kDqWarps = 8;                   // dequantising warps
-constexpr int kDqGroups = 4;                  // k-blocks are dealt round-robin to this many warp groups
+constexpr int kDqGroups = 2;                  // k-blocks are dealt round-robin to this many warp groups
 constexpr int kDqGroupWarps = kDqWarps / kDqGroups;
+static_assert(kDqGroupWarps == 4, "a dequantising group covers the four TMEM lane quarters");
 constexpr int kWarpEpi0 = kWarpDq0 + kDqWarps, kEpiWarps = 4;
 constexpr int kThreads = 32 * (kWarpEpi0 + kEpiWarps);
 constexpr int kAccCols = 128;                 // one fp32 accumulator: 128 lanes x N <= 128 columns
-constexpr int kTmemCols = 2 * kAccCols;       // two accumulators (MMA fills one, the epilogue drains the other)
+constexpr int kACols = kBK / 2;               // one A stage in TMEM: 128 lanes x 64 16-bit values
+constexpr int kACol0 = 2 * kAccCols;          // A stages follow the two accumulators
+constexpr int kTmemCols = kACol0 + kStages * kACols;  // = 512, all of TMEM (one CTA per SM)
+static_assert(kTmemCols == 512, "TMEM budget");
 constexpr int kXchFloats = 2 * 64 * 17;       // gate/up epilogue exchange
 constexpr int kSmTiles = 256;                 // route tiles cached in shared memory
-constexpr int kABytes = 128 * 128;     // A stage: 128 rows x 128 B
 constexpr int kBBytes = kBN * 128;     // B stage
-constexpr int kFp4Bytes = 128 * 32;    // packed codes of one stage
-constexpr int kScBytes = 2 * 128;      // its scale bytes: two 128-byte chunks (64 rows x 2 blocks each)
-constexpr int kCStageBytes = kFp4Bytes + kScBytes;
+constexpr int kFp4Bytes = 128 * 32 * kCK;   // packed codes of one code stage: 128 rows x 64 B, 64-byte swizzle
+constexpr int kScBytes = 2 * 128 * kCK;     // its scale bytes: per 64-row block, kCK chunks of 128 B
+constexpr int kCStageBytes = kFp4Bytes + kScBytes;  // a multiple of 512 B (the 64-byte swizzle period)
 constexpr uint64_t kWaitNs = 2000000000ull;
+
+// TMA descriptors of the activation operand (B) with boxes of 32, 64 and 128
+// rows: one copy per k-block, the smallest box that covers the tile's routes.
+struct BMaps {
+    CUtensorMap m[3];
+};
 
 struct PrefillArgs {
     BlockParams bp;
@@ -88,6 +98,10 @@ __device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
     asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *b, uint32_t n) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0], %1; }" ::"r"(smem_u32(b)), "r"(n)
+                 : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
     asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(smem_u32(b)),
@@ -119,7 +133,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int32_t 
         }
     }
 }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // Wait that ignores the status word (only the time limit ends it): used to let
 // copies or MMAs already issued land before the CTA's shared memory or TMEM goes.
 __device__ __forceinline__ void mbar_wait_drain(uint64_t *b, uint32_t parity, int32_t *status) {
@@ -130,9 +143,17 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t *b, uint32_t parity, in
             return;
         }
 }
-// The last min(issued, n) copies of an n-stage ring have landed.
+// The last min(issued, n) copies of an n-stage ring have landed (one ~2 s
+// limit for all of them: a full barrier that also counts other arrivals may
+// never complete once the kernel is failing).
 __device__ __forceinline__ void drain_ring(uint64_t *full, int n, int issued, int32_t *status) {
-    for (int g = max(0, issued - n); g < issued; g++) mbar_wait_drain(&full[g % n], (g / n) & 1, status);
+    const uint64_t t0 = globaltimer();
+    for (int g = max(0, issued - n); g < issued; g++)
+        while (!mbar_try(&full[g % n], (g / n) & 1))
+            if (globaltimer() - t0 > kWaitNs) {
+                set_device_error(status, MOE_DEV_WAIT_TIMEOUT, 91);
+                return;
+            }
 }
 // Stage index and phase bit of a ring walked in order.  Consumers wait on a
 // full barrier with parity ph; producers wait on an empty barrier with parity
@@ -183,11 +204,12 @@ __host__ __device__ __forceinline__ uint32_t umma_idesc(int M, int N, bool bf) {
     const uint32_t ab = bf ? 1u : 0u;
     return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void umma_bf16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
+// D (TMEM) (+)= A (TMEM: lane = row, 2 16-bit K values per column) x B (shared memory)
+__device__ __forceinline__ void umma_ts(uint32_t dtmem, uint32_t atmem, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
     asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dtmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(dtmem),
+        "r"(atmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -211,6 +233,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
 #pragma unroll
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
+
+// 32 consecutive 32-bit columns of this warp's 32 TMEM lanes from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t v[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------- dequantisation
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
@@ -260,11 +295,6 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t w, uint32_t sc2) {
     return make_uint4(hmul2_f16(h[0], sc2), hmul2_f16(h[1], sc2), hmul2_f16(h[2], sc2), hmul2_f16(h[3], sc2));
 }
 
-// byte offset of 16-byte chunk c of row r in a 128B-swizzled K-major tile
-__device__ __forceinline__ uint32_t sw128(int r, int c) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
-
 // Persistent grouped GEMM.  A launch covers n_tiles x mtiles work items, item
 // i = (route tile i / mtiles, weight-row block i % mtiles); CTA b takes items
 // b, b + gridDim.x, ...  Every role walks that same sequence with its own ring
@@ -272,7 +302,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 // drains the previous one from the other of two TMEM accumulators.
 //
 // Warps: 0 TMA for the packed codes, 1 MMA issue (and TMEM owner), 2 TMA for
-// the activation tile, 3..10 dequantisation (two threads per A row), 11..14
+// the activation tile, 3..10 dequantisation into TMEM (one thread per A row), 11..14
 // epilogue (one TMEM lane quarter each).  Each producer has a warp of its own:
 // a lane blocked in mbarrier.try_wait holds up every other lane of its warp.
 //
@@ -283,7 +313,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 template <bool GATEUP, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_constant__ PrefillArgs a,
                                                                     const __grid_constant__ TmaMaps maps,
-                                                                    const __grid_constant__ CUtensorMap bmap) {
+                                                                    const __grid_constant__ BMaps bmaps) {
     const int mtiles = GATEUP ? a.rows / 64 : (a.rows + 127) / 128;
     const int n_tiles = *a.ws.n_tiles;
     const int n_items = n_tiles * mtiles;
@@ -291,15 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char *sA = smem;                                   // [kStages][128 rows][128 B] swizzled
-    unsigned char *sB = sA + kStages * kABytes;                 // [kStages][kBN rows][128 B] swizzled
-    unsigned char *sF = sB + kStages * kBBytes;                 // [kCStages][codes 128 x 32 B, scales 2 x 128 B]
+    unsigned char *sB = smem;                                   // [kStages][kBN rows][128 B] swizzled
+    unsigned char *sF = sB + kStages * kBBytes;                 // [kCStages][codes 128 x 64 B, scales 2 x 256 B]
     float *xch = reinterpret_cast<float *>(sF + kCStages * kCStageBytes);  // gate/up exchange [2][64][17]
     int4 *s_tiles = reinterpret_cast<int4 *>(xch + kXchFloats);          // [kSmTiles]
     uint64_t *bars = reinterpret_cast<uint64_t *>(s_tiles + kSmTiles);
     uint64_t *full_c = bars, *empty_c = bars + kCStages;                    // code ring
-    uint64_t *full_ab = bars + 2 * kCStages, *full_b = full_ab + kStages;   // A/B ring
-    uint64_t *empty = full_b + kStages;
+    uint64_t *full_ab = bars + 2 * kCStages;   // A/B ring: A from the dequantisers, B by TMA
+    uint64_t *empty = full_ab + kStages;
     uint64_t *acc_full = empty + kStages, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
@@ -312,11 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
     if (threadIdx.x == 0) {
         for (int s = 0; s < kCStages; s++) {
             mbar_init(&full_c[s], 1);
-            mbar_init(&empty_c[s], kDqGroupWarps);
+            mbar_init(&empty_c[s], kCK * kDqGroupWarps);
         }
         for (int s = 0; s < kStages; s++) {
-            mbar_init(&full_ab[s], kDqGroupWarps);
-            mbar_init(&full_b[s], 1);
+            mbar_init(&full_ab[s], kDqGroupWarps + 1);  // + the B copy's expect_tx arrival
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; b++) {
@@ -361,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                     sc0 = maps.sc[shared_e ? 2 : 0] + (size_t)(ebase * maps.row_blocks + 2 * mt) * cb;
                     sc1 = sc0 + cb;
                 }
-                for (int kb = 0; kb < nkb; kb++, g++) {
+                // kCK k-blocks per stage (past the end of K the box reads zeros,
+                // the scale chunks belong to the next block or the pad)
+                for (int kb = 0; kb < nkb; kb += kCK, g++) {
                     if (!mbar_wait(&empty_c[r.s], r.ph ^ 1, status, 10)) {
                         ok = false;
                         break;
@@ -372,12 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                     if (GATEUP) {
                         const int y = ebase * a.rows + mt * 64;
                         tma_load_2d(dst, m0, &full_c[r.s], kb * 32, y);
-                        tma_load_2d(dst + 64 * 32, m1, &full_c[r.s], kb * 32, y);
+                        tma_load_2d(dst + kFp4Bytes / 2, m1, &full_c[r.s], kb * 32, y);
                     } else {
                         tma_load_2d(dst, m0, &full_c[r.s], kb * 32, ebase * a.rows + mt * 128);
                     }
-                    bulk_load(dst + kFp4Bytes, sc0 + (size_t)kb * 128, 128, &full_c[r.s]);
-                    bulk_load(dst + kFp4Bytes + 128, sc1 + (size_t)kb * 128, 128, &full_c[r.s]);
+                    bulk_load(dst + kFp4Bytes, sc0 + (size_t)kb * 128, 128 * kCK, &full_c[r.s]);
+                    bulk_load(dst + kFp4Bytes + 128 * kCK, sc1 + (size_t)kb * 128, 128 * kCK, &full_c[r.s]);
                     issued++;
                     r.next(kCStages);
                 }
@@ -395,22 +425,22 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
             bool ok = true;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 const int4 tl = tile_at(it / mtiles);
-                const int rstart = tl.y, nbox = (tl.z + 31) / 32;
+                const int rstart = tl.y, mi = tl.z <= 32 ? 0 : (tl.z <= 64 ? 1 : 2);
+                const CUtensorMap *bm = &bmaps.m[mi];
+                const uint32_t bbytes = (uint32_t)(32 << mi) * 128;
                 for (int kb = 0; kb < nkb; kb++, g++) {
                     if (!mbar_wait(&empty[r.s], r.ph ^ 1, status, 13)) {
                         ok = false;
                         break;
                     }
                     MOE_PF_KMARK(4, g);
-                    mbar_expect_tx(&full_b[r.s], (uint32_t)nbox * 32 * 128);
-                    for (int bx = 0; bx < nbox; bx++)
-                        tma_load_2d(sB + r.s * kBBytes + bx * 32 * 128, &bmap, &full_b[r.s], kb * kBK,
-                                    rstart + 32 * bx);
+                    mbar_expect_tx(&full_ab[r.s], bbytes);
+                    tma_load_2d(sB + r.s * kBBytes, bm, &full_ab[r.s], kb * kBK, rstart);
                     issued++;
                     r.next(kStages);
                 }
             }
-            drain_ring(full_b, kStages, issued, status);
+            drain_ring(full_ab, kStages, issued, status);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------- MMA issuer
@@ -430,16 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                 for (int kb = 0; kb < nkb; kb++, g++) {
                     ok = mbar_wait(&full_ab[r.s], r.ph, status, 20);
                     MOE_PF_KMARK(0, g);
-                    ok = ok && mbar_wait(&full_b[r.s], r.ph, status, 22);
                     if (!ok) break;
                     tc_fence_after();
                     MOE_PF_KMARK(3, g);
-                    const uint32_t a_addr = smem_u32(sA + r.s * kABytes), b_addr = smem_u32(sB + r.s * kBBytes);
+                    const uint32_t a_col = tmem + (uint32_t)(kACol0 + r.s * kACols), b_addr = smem_u32(sB + r.s * kBBytes);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; k++)
-                        umma_bf16(dt, umma_desc_sw128(a_addr + 32 * k), umma_desc_sw128(b_addr + 32 * k), idesc,
-                                  (kb | k) != 0);
+                        umma_ts(dt, a_col + 8 * k, umma_desc_sw128(b_addr + 32 * k), idesc, (kb | k) != 0);
                     umma_commit(&empty[r.s]);
+                    MOE_PF_KMARK(1, g);
                     r.next(kStages);
                 }
                 if (ok) umma_commit(&acc_full[ab]);
@@ -452,49 +481,68 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
         }
     } else if (warp < kWarpEpi0) {
         // ------------------------------------------ dequant (warps 3..10)
-        // Group grp (two warps) dequantises k-blocks g = grp, grp + 4, ... of the
-        // CTA's sequence, the whole 128 x 64 A stage each: a warp's fixed costs
-        // per stage (waits, proxy fence, arrivals) then overlap those of the
-        // other groups instead of adding up over every k-block.
+        // Two groups of four warps; group grp dequantises k-blocks g = grp,
+        // grp + 2, ... of the CTA's sequence.  Thread = A row = TMEM lane (a warp
+        // may only touch its own lane quarter): it turns the row's 64 codes of
+        // the k-block into 32 columns of 16-bit pairs and stores them into the
+        // stage's TMEM columns with one tcgen05.st; no shared-memory copy of A.
         const int grp = (warp - kWarpDq0) / kDqGroupWarps;
-        const int t = threadIdx.x - 32 * (kWarpDq0 + grp * kDqGroupWarps);  // 0..63
+        const int q = warp & 3, arow = q * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+        const int swz = (arow >> 1) & 3;  // the code box's 64-byte swizzle for this row
         const int my_items = (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-        const int total = my_items * nkb;
+        const int total = my_items * nkb, ncs = (nkb + kCK - 1) / kCK;
         for (int g = grp; g < total; g += kDqGroups) {
-            const int s = g % kStages, cs = g % kCStages;
+            const int li = g / nkb, kb = g - li * nkb;
+            const int qq = li * ncs + kb / kCK;  // this CTA's code stage holding k-block kb
+            const int s = g % kStages, cs = qq % kCStages, kh = kb % kCK;
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, status, 30) &&
-                                                        mbar_wait(&full_c[cs], (g / kCStages) & 1, status, 31));
+                                                        mbar_wait(&full_c[cs], (qq / kCStages) & 1, status, 31));
             if (!ok) break;
+            tc_fence_after();  // the MMAs that read this A stage have completed
             if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(2, g);
             const unsigned char *cst = sF + cs * kCStageBytes;
-            unsigned char *adst = sA + s * kABytes;
-            // unit u = (A row u / 2, 32-element half u % 2): 16 code bytes, one scale byte
+            const uint4 c0 = *reinterpret_cast<const uint4 *>(cst + arow * 64 + (((2 * kh) ^ swz) << 4));
+            const uint4 c1 = *reinterpret_cast<const uint4 *>(cst + arow * 64 + (((2 * kh + 1) ^ swz) << 4));
+            const uint32_t sc2 =
+                *reinterpret_cast<const uint16_t *>(cst + kFp4Bytes + (arow >> 6) * 128 * kCK + kh * 128 + (arow & 63) * 2);
+            uint32_t v[32];
+            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const int u = t + 64 * i, arow = u >> 1, half = u & 1;
-                const uint4 c = *reinterpret_cast<const uint4 *>(cst + u * 16);
-                const uint32_t sc = cst[kFp4Bytes + u];
+            for (int hf = 0; hf < 2; hf++) {
+                const uint32_t sc = (sc2 >> (8 * hf)) & 0xFFu;
                 if (F16) {
-                    const uint32_t sc2 = scale_f16x2(sc);
-                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 0)) = dequant8_f16(c.x, sc2);
-                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 1)) = dequant8_f16(c.y, sc2);
-                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 2)) = dequant8_f16(c.z, sc2);
-                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 3)) = dequant8_f16(c.w, sc2);
+                    const uint32_t sx = scale_f16x2(sc);
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const uint4 d = dequant8_f16(w[4 * hf + j], sx);
+                        v[16 * hf + 4 * j + 0] = d.x;
+                        v[16 * hf + 4 * j + 1] = d.y;
+                        v[16 * hf + 4 * j + 2] = d.z;
+                        v[16 * hf + 4 * j + 3] = d.w;
+                    }
                 } else {
                     const bool big = sc > 128u;
                     const uint32_t l = scale_lo(sc), h = scale_hi(sc);
-                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 0)) = dequant8(c.x, l, h, big);
-                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 1)) = dequant8(c.y, l, h, big);
-                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 2)) = dequant8(c.z, l, h, big);
-                    *reinterpret_cast<uint4 *>(adst + sw128(arow, half * 4 + 3)) = dequant8(c.w, l, h, big);
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const uint4 d = dequant8(w[4 * hf + j], l, h, big);
+                        v[16 * hf + 4 * j + 0] = d.x;
+                        v[16 * hf + 4 * j + 1] = d.y;
+                        v[16 * hf + 4 * j + 2] = d.z;
+                        v[16 * hf + 4 * j + 3] = d.w;
+                    }
                 }
             }
+            tmem_st32(trow + (uint32_t)(kACol0 + s * kACols), v);
+            tmem_wait_st();
             if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(9, g);
-            fence_proxy_async();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&full_ab[s]);
-                mbar_arrive(&empty_c[cs]);
+                // the last stage of an item may hold fewer than kCK k-blocks: arrive for the missing ones too
+                mbar_arrive_n(&empty_c[cs], kb + 1 == nkb ? (uint32_t)(kCK - kh) : 1u);
             }
             if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(6, g);
         }
@@ -594,7 +642,7 @@ cudaError_t get_encoder() {
     return cudaSuccess;
 }
 
-// 2D map over packed codes: [n_rows][cols/2] bytes, box 32 bytes x box_rows.
+// 2D map over packed codes: [n_rows][cols/2] bytes, box 32 kCK bytes x box_rows, 64-byte swizzle.
 cudaError_t make_codes_map(CUtensorMap *m, const uint8_t *codes, size_t n_rows, int cols, int box_rows) {
     if (!codes) {
         memset(m, 0, sizeof *m);
@@ -602,25 +650,25 @@ cudaError_t make_codes_map(CUtensorMap *m, const uint8_t *codes, size_t n_rows, 
     }
     cuuint64_t dims[2] = {(cuuint64_t)(cols / 2), (cuuint64_t)n_rows};
     cuuint64_t strides[1] = {(cuuint64_t)(cols / 2)};
-    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {32 * kCK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 size_t prefill_smem_bytes() {
-    return 1024 + kStages * (kABytes + kBBytes) + kCStages * kCStageBytes + kXchFloats * 4 + kSmTiles * 16 + 512;
+    return 1024 + kStages * kBBytes + kCStages * kCStageBytes + kXchFloats * 4 + kSmTiles * 16 + 512;
 }
 
-// 2D map over a bf16 activation matrix [rows][K]: box 64 elements (128 B) x 32
-// rows, 128-byte swizzle (the K-major layout the MMA descriptors expect; a
-// 32-row box is four whole 8-row swizzle atoms).
-cudaError_t make_act_map(CUtensorMap *m, const uint16_t *base, int rows, int K, bool f16) {
+// 2D map over a bf16 activation matrix [rows][K]: box 64 elements (128 B) x
+// box_rows (32, 64, 128), 128-byte swizzle (the K-major layout the MMA
+// descriptors expect; the box is whole 8-row swizzle atoms).
+cudaError_t make_act_map(CUtensorMap *m, const uint16_t *base, int rows, int K, bool f16, int box_rows) {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, 32};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                           const_cast<uint16_t *>(base), dims, strides, box,
@@ -658,9 +706,11 @@ __global__ void __launch_bounds__(256) moe_pack_scales_kernel(const uint8_t *in,
     }
 }
 
-// bytes of one repacked matrix set: n_exp experts plus one pad block
+// blocks of one repacked matrix set: n_exp experts plus two pad blocks (a
+// code stage's chunk pair may start at the last chunk of the last real block)
+size_t packed_blocks(int n_exp, int rows) { return (size_t)n_exp * ((rows + 63) / 64) + 2; }
 size_t packed_bytes(int n_exp, int rows, int cols) {
-    return (((size_t)n_exp * ((rows + 63) / 64) + 1) * (size_t)(cols / kBK) * 128 + 255) & ~(size_t)255;
+    return (packed_blocks(n_exp, rows) * (size_t)(cols / kBK) * 128 + 255) & ~(size_t)255;
 }
 
 }  // namespace
@@ -702,7 +752,7 @@ cudaError_t prefill_pack_scales(const BlockParams &bp, const MatPtrs &gate, cons
             const size_t n = packed_bytes(n_exp, m.rows, m.cols);
             const uint8_t *dst = nullptr;
             if (n_exp) {
-                const size_t nout = ((size_t)n_exp * ((m.rows + 63) / 64) + 1) * (size_t)(m.cols / kBK) * 128;
+                const size_t nout = packed_blocks(n_exp, m.rows) * (size_t)(m.cols / kBK) * 128;
                 const int blocks = (int)((nout + 255) / 256 < 8192 ? (nout + 255) / 256 : 8192);
                 moe_pack_scales_kernel<<<blocks, 256, 0, st>>>(src, buf, n_exp, m.rows, m.cols, nout);
                 MOE_CUDA_TRY(cudaGetLastError());
@@ -727,11 +777,11 @@ cudaError_t launch_gather(const BlockParams &bp, const Workspace &ws, int T, boo
 }
 
 template <bool GATEUP, bool F16>
-cudaError_t launch_pf(const PrefillArgs &args, const TmaMaps &maps, const CUtensorMap &bmap, dim3 grid,
+cudaError_t launch_pf(const PrefillArgs &args, const TmaMaps &maps, const BMaps &bmaps, dim3 grid,
                       cudaStream_t st) {
     static bool done = false;
     MOE_CUDA_TRY(smem_optin_once(moe_prefill_kernel<GATEUP, F16>, done));
-    moe_prefill_kernel<GATEUP, F16><<<grid, kThreads, prefill_smem_bytes(), st>>>(args, maps, bmap);
+    moe_prefill_kernel<GATEUP, F16><<<grid, kThreads, prefill_smem_bytes(), st>>>(args, maps, bmaps);
     return cudaGetLastError();
 }
 
@@ -739,10 +789,10 @@ cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, con
                                  bool gateup, int T, const TmaMaps &maps, bool f16, cudaStream_t st) {
     PrefillArgs args{bp, ws, a0, a1, gateup ? bp.H : bp.F, gateup ? bp.F : bp.H};
     const int R = T * (bp.K + bp.n_shared);
-    CUtensorMap bmap;
+    BMaps bmaps;
     MOE_CUDA_TRY(get_encoder());
     const uint16_t *bsrc = gateup ? ws.xs : (f16 ? ws.h16 : ws.h);
-    MOE_CUDA_TRY(make_act_map(&bmap, bsrc, R, args.Kdim, f16));
+    for (int i = 0; i < 3; i++) MOE_CUDA_TRY(make_act_map(&bmaps.m[i], bsrc, R, args.Kdim, f16, 32 << i));
     int tiles = (R + kBN - 1) / kBN + bp.E + bp.n_shared;
     if (tiles > ws.max_tiles) tiles = ws.max_tiles;
     const int mtiles = gateup ? bp.F / 64 : (bp.H + 127) / 128;
@@ -755,6 +805,7 @@ cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, con
     }
     const long items = (long)tiles * mtiles;
     const dim3 grid((unsigned)(items < n_sm ? items : n_sm));
-    if (gateup) return f16 ? launch_pf<true, true>(args, maps, bmap, grid, st) : launch_pf<true, false>(args, maps, bmap, grid, st);
-    return f16 ? launch_pf<false, true>(args, maps, bmap, grid, st) : launch_pf<false, false>(args, maps, bmap, grid, st);
+    if (gateup)
+        return f16 ? launch_pf<true, true>(args, maps, bmaps, grid, st) : launch_pf<true, false>(args, maps, bmaps, grid, st);
+    return f16 ? launch_pf<false, true>(args, maps, bmaps, grid, st) : launch_pf<false, false>(args, maps, bmaps, grid, st);
 }
