@@ -8,23 +8,23 @@
 // then sums each token's slots.  Here a work item is one (expert tile of
 // <= 128 routes) x (weight row block) block:
 //
-//   gate/up kernel: A = [64 gate rows ; the same 64 up rows] (M = 128),
-//                   B = the tile's x_hat rows, D = TMEM [128 lanes][N];
+//   gate/up kernel: A = the tile's x_hat rows (M = 128 routes), B = [128 gate
+//                   rows ; the same 128 up rows] (N = 256), D = TMEM
+//                   [128 lanes = routes][256 columns];
 //                   epilogue: bias + clamped SwiGLU -> h
-//   down kernel:    A = 128 rows of Wd, B = the tile's h rows;
+//   down kernel:    A = the tile's h rows, B = 256 rows of Wd;
 //                   epilogue: bias, times the route weight -> per-route fp32
 //
 // The kernel is persistent (one CTA per SM walking a static list of items)
 // with warp roles: a TMA warp for the packed codes and their scales, a TMA
-// warp for the B tile (128-byte swizzled, straight into the MMA layout; the
+// warp for the activation tile, A (128-byte swizzled, straight into the MMA layout; the
 // x_hat rows are first gathered into route order by moe_gather_kernel), an
 // MMA warp that owns all 512 TMEM columns, eight dequantising warps that
-// write A straight into TMEM (tcgen05.st; the MMA reads A from TMEM and B
-// from shared memory), and four epilogue warps that drain one of two TMEM
-// accumulators while the MMA fills the other.  mbarrier rings connect them.
-// The bf16 variant keeps activations in a 32-block pair order (x_hat_mma / h)
-// and produces A in that order straight from the nibble-pair dequantiser, so
-// the K permutation cancels in every dot product.
+// write B into 128-byte-swizzled shared memory, and four epilogue warps that
+// drain one of two TMEM accumulators while the MMA fills the other.  mbarrier
+// rings connect them.  The bf16 variant keeps activations in a 32-block pair
+// order (x_hat_mma / h) and produces B in that order straight from the
+// nibble-pair dequantiser, so the K permutation cancels in every dot product.
 //
 // Every wait is bounded (about 2 s of %globaltimer); on a timeout the kernel
 // records MOE_DEV_WAIT_TIMEOUT in the status word, drains what it issued,
@@ -45,34 +45,35 @@
 
 namespace {
 
-constexpr int kStages = 8;          // A (dequantised, in TMEM) + B (shared memory) stages, consumed by the MMA
+constexpr int kStages = 3;          // A (activations, by TMA) + B (dequantised weights) stages, consumed by the MMA
 constexpr int kCK = 2;              // k-blocks per packed-code stage
-constexpr int kCStages = 6;         // packed-code stages (12 k-blocks ahead)
-constexpr int kBK = 64;            // K elements per stage (one 128-byte swizzle row of bf16)
-constexpr int kBN = 128;           // max routes per tile
-constexpr int kWarpCodes = 0, kWarpMma = 1, kWarpB = 2, kWarpDq0 = 3;
+constexpr int kCStages = 4;         // packed-code stages (8 k-blocks ahead)
+constexpr int kBK = 64;             // K elements per stage (one 128-byte swizzle row of 16-bit values)
+constexpr int kTM = 128;            // routes per tile (the MMA's M)
+constexpr int kWN = 256;            // weight rows per item (the MMA's N): 128 gate + 128 up rows, or 256 down rows
+constexpr int kWarpCodes = 0, kWarpMma = 1, kWarpA = 2, kWarpDq0 = 3;
 constexpr int kDqWarps = 8;                   // dequantising warps
 constexpr int kDqGroups = 2;                  // k-blocks are dealt round-robin to this many warp groups
 constexpr int kDqGroupWarps = kDqWarps / kDqGroups;
-static_assert(kDqGroupWarps == 4, "a dequantising group covers the four TMEM lane quarters");
 constexpr int kWarpEpi0 = kWarpDq0 + kDqWarps, kEpiWarps = 4;
 constexpr int kThreads = 32 * (kWarpEpi0 + kEpiWarps);
-constexpr int kAccCols = 128;                 // one fp32 accumulator: 128 lanes x N <= 128 columns
-constexpr int kACols = kBK / 2;               // one A stage in TMEM: 128 lanes x 64 16-bit values
-constexpr int kACol0 = 2 * kAccCols;          // A stages follow the two accumulators
-constexpr int kTmemCols = kACol0 + kStages * kACols;  // = 512, all of TMEM (one CTA per SM)
+constexpr int kAccCols = kWN;                 // one fp32 accumulator: 128 lanes (routes) x 256 columns (rows)
+constexpr int kTmemCols = 2 * kAccCols;       // two accumulators (MMA fills one, the epilogue drains the other)
 static_assert(kTmemCols == 512, "TMEM budget");
-constexpr int kXchFloats = 2 * 64 * 17;       // gate/up epilogue exchange
 constexpr int kSmTiles = 256;                 // route tiles cached in shared memory
-constexpr int kBBytes = kBN * 128;     // B stage
-constexpr int kFp4Bytes = 128 * 32 * kCK;   // packed codes of one code stage: 128 rows x 64 B, 64-byte swizzle
-constexpr int kScBytes = 2 * 128 * kCK;     // its scale bytes: per 64-row block, kCK chunks of 128 B
+constexpr int kBiasFloats = kWN;              // an epilogue warp's copy of the item's 256 biases
+constexpr int kABytes = kTM * 128;            // A stage: 128 route rows x 128 B
+constexpr int kBBytes = kWN * 128;            // B stage: 256 weight rows x 128 B
+constexpr int kFp4Bytes = kWN * 32 * kCK;     // packed codes of one code stage: 256 rows x 64 B, 64-byte swizzle
+constexpr int kScBytes = (kWN / 64) * 128 * kCK;  // its scale bytes: per 64-row block, kCK chunks of 128 B
 constexpr int kCStageBytes = kFp4Bytes + kScBytes;  // a multiple of 512 B (the 64-byte swizzle period)
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-// TMA descriptors of the activation operand (B) with boxes of 32, 64 and 128
-// rows: one copy per k-block, the smallest box that covers the tile's routes.
-struct BMaps {
+// TMA descriptors of the activation operand (A) with boxes of 32, 64 and 128
+// rows: one copy per k-block, the smallest box that covers the tile's routes
+// (the MMA reads all 128 rows; rows past the box are stale and only feed
+// accumulator lanes the epilogue skips).
+struct AMaps {
     CUtensorMap m[3];
 };
 
@@ -168,9 +169,6 @@ struct Ring {
         }
     }
 };
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
     asm volatile(
@@ -204,17 +202,18 @@ __host__ __device__ __forceinline__ uint32_t umma_idesc(int M, int N, bool bf) {
     const uint32_t ab = bf ? 1u : 0u;
     return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-// D (TMEM) (+)= A (TMEM: lane = row, 2 16-bit K values per column) x B (shared memory)
-__device__ __forceinline__ void umma_ts(uint32_t dtmem, uint32_t atmem, uint64_t bdesc, uint32_t idesc,
+// D (TMEM, fp32) (+)= A x B, both from shared memory (K-major, 128-byte swizzle)
+__device__ __forceinline__ void umma_ss(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
     asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(dtmem),
-        "r"(atmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dtmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
@@ -234,18 +233,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
-// 32 consecutive 32-bit columns of this warp's 32 TMEM lanes from registers.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t v[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------- dequantisation
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
@@ -295,16 +282,41 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t w, uint32_t sc2) {
     return make_uint4(hmul2_f16(h[0], sc2), hmul2_f16(h[1], sc2), hmul2_f16(h[2], sc2), hmul2_f16(h[3], sc2));
 }
 
+// Clamped SwiGLU with the hardware exponential and a fast divide: within a few
+// fp32 ulps of the correctly rounded form, far inside the bf16 rounding of h.
+// For α·g below about -87 the divide returns 0 where the exact value is a
+// normal below 1e-36 in magnitude.
+__device__ __forceinline__ float swiglu_fast(float g, float u, float alpha, float limit) {
+    const float gc = (g > limit) ? limit : g;
+    const float uc = (u > limit) ? limit : ((u < -limit) ? -limit : u);
+    return __fdividef(gc, 1.0f + __expf(-alpha * gc)) * (uc + 1.0f);
+}
+
+// byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
 // Persistent grouped GEMM.  A launch covers n_tiles x mtiles work items, item
 // i = (route tile i / mtiles, weight-row block i % mtiles); CTA b takes items
 // b, b + gridDim.x, ...  Every role walks that same sequence with its own ring
 // counters, so the producers run ahead into the next item while the epilogue
 // drains the previous one from the other of two TMEM accumulators.
 //
-// Warps: 0 TMA for the packed codes, 1 MMA issue (and TMEM owner), 2 TMA for
-// the activation tile, 3..10 dequantisation into TMEM (one thread per A row), 11..14
-// epilogue (one TMEM lane quarter each).  Each producer has a warp of its own:
-// a lane blocked in mbarrier.try_wait holds up every other lane of its warp.
+// Operands: A = the tile's activation rows (M = 128 routes, by TMA), B = 256
+// dequantised weight rows (N = 256): a tcgen05.mma of M = 128, K = 16 costs
+// the same issue slot whatever N is, so N is the weight dimension, always 256,
+// and the routes (often fewer than 128 per expert) take M.  D = TMEM [128
+// lanes = routes][256 columns = weight rows]; for gate/up the 256 rows are 128
+// gate rows then the same 128 up rows, so one thread holds both halves of its
+// route's SwiGLU inputs.
+//
+// Warps: 0 TMA for the packed codes and their scales, 1 MMA issue (and TMEM
+// owner), 2 TMA for the activation tile, 3..10 dequantisation into the
+// 128-byte-swizzled B stage (two groups of four warps, k-blocks dealt
+// round-robin, two weight rows per thread), 11..14 epilogue (one TMEM lane
+// quarter each).  Each producer has a warp of its own: a lane blocked in
+// mbarrier.try_wait holds up every other lane of its warp.
 //
 // F16: the fp16 variant (every E8M0 exponent in [104, 140], activations in the
 // fp16 range): hardware e2m1 -> f16 conversion, natural K order, fp16 MMA
@@ -313,21 +325,23 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t w, uint32_t sc2) {
 template <bool GATEUP, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_constant__ PrefillArgs a,
                                                                     const __grid_constant__ TmaMaps maps,
-                                                                    const __grid_constant__ BMaps bmaps) {
-    const int mtiles = GATEUP ? a.rows / 64 : (a.rows + 127) / 128;
+                                                                    const __grid_constant__ AMaps amaps) {
+    constexpr int RPI = GATEUP ? kWN / 2 : kWN;  // output rows per item
+    const int mtiles = (a.rows + RPI - 1) / RPI;
     const int n_tiles = *a.ws.n_tiles;
     const int n_items = n_tiles * mtiles;
     if ((int)blockIdx.x >= n_items) return;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char *sB = smem;                                   // [kStages][kBN rows][128 B] swizzled
-    unsigned char *sF = sB + kStages * kBBytes;                 // [kCStages][codes 128 x 64 B, scales 2 x 256 B]
-    float *xch = reinterpret_cast<float *>(sF + kCStages * kCStageBytes);  // gate/up exchange [2][64][17]
-    int4 *s_tiles = reinterpret_cast<int4 *>(xch + kXchFloats);          // [kSmTiles]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(s_tiles + kSmTiles);
-    uint64_t *full_c = bars, *empty_c = bars + kCStages;                    // code ring
-    uint64_t *full_ab = bars + 2 * kCStages;   // A/B ring: A from the dequantisers, B by TMA
+    unsigned char *sA = smem;                                   // [kStages][128 route rows][128 B] swizzled
+    unsigned char *sB = sA + kStages * kABytes;                 // [kStages][256 weight rows][128 B] swizzled
+    unsigned char *sF = sB + kStages * kBBytes;                 // [kCStages][codes 256 x 64 B, scales 4 x 256 B]
+    int4 *s_tiles = reinterpret_cast<int4 *>(sF + kCStages * kCStageBytes);  // [kSmTiles]
+    float *s_bias = reinterpret_cast<float *>(s_tiles + kSmTiles);           // [kEpiWarps][kBiasFloats]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s_bias + kEpiWarps * kBiasFloats);
+    uint64_t *full_c = bars, *empty_c = bars + kCStages;    // code ring
+    uint64_t *full_ab = empty_c + kCStages;                  // A/B ring: A by TMA, B from the dequantisers
     uint64_t *empty = full_ab + kStages;
     uint64_t *acc_full = empty + kStages, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -344,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
             mbar_init(&empty_c[s], kCK * kDqGroupWarps);
         }
         for (int s = 0; s < kStages; s++) {
-            mbar_init(&full_ab[s], kDqGroupWarps + 1);  // + the B copy's expect_tx arrival
+            mbar_init(&full_ab[s], kDqGroupWarps + 1);  // + the A copy's expect_tx arrival
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; b++) {
@@ -366,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
     auto tile_at = [&](int t) -> int4 { return t < kSmTiles ? s_tiles[t] : a.ws.tiles[t]; };
 
     if (warp == kWarpCodes) {
-        // ------------------------------------------------ packed codes (TMA)
+        // ------------------------------------------- packed codes + scales (TMA)
         if (lane == 0) {
             Ring r;
             int issued = 0, g = 0;
@@ -378,19 +392,22 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                 const CUtensorMap *m0 = shared_e ? &maps.m[2] : &maps.m[0];
                 const CUtensorMap *m1 = shared_e ? &maps.m[3] : &maps.m[1];
                 const int ebase = shared_e ? 0 : e;
-                // scale chunks of this item's two 64-row blocks (gate and up rows, or
-                // rows 128 mt .. 128 mt + 127), one per k-block
+                // the item's four 64-row scale blocks, kCK chunks per code stage
                 const size_t cb = (size_t)nkb * 128;
-                const uint8_t *sc0, *sc1;
+                const uint8_t *scp[4];
                 if (GATEUP) {
-                    sc0 = maps.sc[shared_e ? 2 : 0] + (size_t)(ebase * maps.row_blocks + mt) * cb;
-                    sc1 = maps.sc[shared_e ? 3 : 1] + (size_t)(ebase * maps.row_blocks + mt) * cb;
+                    const uint8_t *g0 = maps.sc[shared_e ? 2 : 0] + (size_t)(ebase * maps.row_blocks + 2 * mt) * cb;
+                    const uint8_t *u0 = maps.sc[shared_e ? 3 : 1] + (size_t)(ebase * maps.row_blocks + 2 * mt) * cb;
+                    scp[0] = g0;
+                    scp[1] = g0 + cb;
+                    scp[2] = u0;
+                    scp[3] = u0 + cb;
                 } else {
-                    sc0 = maps.sc[shared_e ? 2 : 0] + (size_t)(ebase * maps.row_blocks + 2 * mt) * cb;
-                    sc1 = sc0 + cb;
+                    const uint8_t *d0 = maps.sc[shared_e ? 2 : 0] + (size_t)(ebase * maps.row_blocks + 4 * mt) * cb;
+                    for (int j = 0; j < 4; j++) scp[j] = d0 + j * cb;
                 }
-                // kCK k-blocks per stage (past the end of K the box reads zeros,
-                // the scale chunks belong to the next block or the pad)
+                // past the end of K (or of the matrix) the boxes read zeros; the scale
+                // chunks there belong to the next block or the pad, and are never used
                 for (int kb = 0; kb < nkb; kb += kCK, g++) {
                     if (!mbar_wait(&empty_c[r.s], r.ph ^ 1, status, 10)) {
                         ok = false;
@@ -400,25 +417,23 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                     mbar_expect_tx(&full_c[r.s], kCStageBytes);
                     unsigned char *dst = sF + r.s * kCStageBytes;
                     if (GATEUP) {
-                        const int y = ebase * a.rows + mt * 64;
+                        const int y = ebase * a.rows + mt * RPI;
                         tma_load_2d(dst, m0, &full_c[r.s], kb * 32, y);
                         tma_load_2d(dst + kFp4Bytes / 2, m1, &full_c[r.s], kb * 32, y);
                     } else {
-                        tma_load_2d(dst, m0, &full_c[r.s], kb * 32, ebase * a.rows + mt * 128);
+                        tma_load_2d(dst, m0, &full_c[r.s], kb * 32, ebase * a.rows + mt * RPI);
                     }
-                    bulk_load(dst + kFp4Bytes, sc0 + (size_t)kb * 128, 128 * kCK, &full_c[r.s]);
-                    bulk_load(dst + kFp4Bytes + 128 * kCK, sc1 + (size_t)kb * 128, 128 * kCK, &full_c[r.s]);
+#pragma unroll
+                    for (int j = 0; j < 4; j++)
+                        bulk_load(dst + kFp4Bytes + j * 128 * kCK, scp[j] + (size_t)kb * 128, 128 * kCK, &full_c[r.s]);
                     issued++;
                     r.next(kCStages);
                 }
             }
             drain_ring(full_c, kCStages, issued, status);
         }
-    } else if (warp == kWarpB) {
-        // ------------------------------- activation tile (TMA, 32-row boxes)
-        // as many boxes as the tile has routes; the MMA reads only the first
-        // n_mma rows, rows past the tile belong to other tiles or lie outside
-        // the tensor and read as zeros
+    } else if (warp == kWarpA) {
+        // ------------------------------------- activation tile (TMA, A operand)
         if (lane == 0) {
             Ring r;
             int issued = 0, g = 0;
@@ -426,16 +441,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 const int4 tl = tile_at(it / mtiles);
                 const int rstart = tl.y, mi = tl.z <= 32 ? 0 : (tl.z <= 64 ? 1 : 2);
-                const CUtensorMap *bm = &bmaps.m[mi];
-                const uint32_t bbytes = (uint32_t)(32 << mi) * 128;
+                const CUtensorMap *am = &amaps.m[mi];
+                const uint32_t abytes = (uint32_t)(32 << mi) * 128;
                 for (int kb = 0; kb < nkb; kb++, g++) {
                     if (!mbar_wait(&empty[r.s], r.ph ^ 1, status, 13)) {
                         ok = false;
                         break;
                     }
                     MOE_PF_KMARK(4, g);
-                    mbar_expect_tx(&full_ab[r.s], bbytes);
-                    tma_load_2d(sB + r.s * kBBytes, bm, &full_ab[r.s], kb * kBK, rstart);
+                    mbar_expect_tx(&full_ab[r.s], abytes);
+                    tma_load_2d(sA + r.s * kABytes, am, &full_ab[r.s], kb * kBK, rstart);
                     issued++;
                     r.next(kStages);
                 }
@@ -445,12 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            const uint32_t idesc = umma_idesc(kTM, kWN, !F16);
             Ring r;
             bool ok = true;
             int li = 0, g = 0;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, li++) {
-                const int rcount = tile_at(it / mtiles).z;
-                const uint32_t idesc = umma_idesc(128, max(16, (rcount + 15) & ~15), !F16);
                 const int ab = li & 1;
                 // the epilogue has read this accumulator out (free on its first use)
                 ok = mbar_wait(&acc_empty[ab], ((li >> 1) & 1) ^ 1, status, 23);
@@ -463,10 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                     if (!ok) break;
                     tc_fence_after();
                     MOE_PF_KMARK(3, g);
-                    const uint32_t a_col = tmem + (uint32_t)(kACol0 + r.s * kACols), b_addr = smem_u32(sB + r.s * kBBytes);
+                    const uint32_t a_addr = smem_u32(sA + r.s * kABytes), b_addr = smem_u32(sB + r.s * kBBytes);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; k++)
-                        umma_ts(dt, a_col + 8 * k, umma_desc_sw128(b_addr + 32 * k), idesc, (kb | k) != 0);
+                        umma_ss(dt, umma_desc_sw128(a_addr + 32 * k), umma_desc_sw128(b_addr + 32 * k), idesc,
+                                (kb | k) != 0);
                     umma_commit(&empty[r.s]);
                     MOE_PF_KMARK(1, g);
                     r.next(kStages);
@@ -482,14 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
     } else if (warp < kWarpEpi0) {
         // ------------------------------------------ dequant (warps 3..10)
         // Two groups of four warps; group grp dequantises k-blocks g = grp,
-        // grp + 2, ... of the CTA's sequence.  Thread = A row = TMEM lane (a warp
-        // may only touch its own lane quarter): it turns the row's 64 codes of
-        // the k-block into 32 columns of 16-bit pairs and stores them into the
-        // stage's TMEM columns with one tcgen05.st; no shared-memory copy of A.
+        // grp + 2, ... of the CTA's sequence into the whole 256 x 64 B stage:
+        // thread t of the group handles weight rows t and t + 128.
         const int grp = (warp - kWarpDq0) / kDqGroupWarps;
-        const int q = warp & 3, arow = q * 32 + lane;
-        const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-        const int swz = (arow >> 1) & 3;  // the code box's 64-byte swizzle for this row
+        const int t = threadIdx.x - 32 * (kWarpDq0 + grp * kDqGroupWarps);  // 0..127
         const int my_items = (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
         const int total = my_items * nkb, ncs = (nkb + kCK - 1) / kCK;
         for (int g = grp; g < total; g += kDqGroups) {
@@ -499,45 +510,37 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, status, 30) &&
                                                         mbar_wait(&full_c[cs], (qq / kCStages) & 1, status, 31));
             if (!ok) break;
-            tc_fence_after();  // the MMAs that read this A stage have completed
             if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(2, g);
             const unsigned char *cst = sF + cs * kCStageBytes;
-            const uint4 c0 = *reinterpret_cast<const uint4 *>(cst + arow * 64 + (((2 * kh) ^ swz) << 4));
-            const uint4 c1 = *reinterpret_cast<const uint4 *>(cst + arow * 64 + (((2 * kh + 1) ^ swz) << 4));
-            const uint32_t sc2 =
-                *reinterpret_cast<const uint16_t *>(cst + kFp4Bytes + (arow >> 6) * 128 * kCK + kh * 128 + (arow & 63) * 2);
-            uint32_t v[32];
-            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            unsigned char *bdst = sB + s * kBBytes;
 #pragma unroll
-            for (int hf = 0; hf < 2; hf++) {
-                const uint32_t sc = (sc2 >> (8 * hf)) & 0xFFu;
-                if (F16) {
-                    const uint32_t sx = scale_f16x2(sc);
+            for (int rr = 0; rr < 2; rr++) {
+                const int row = t + 128 * rr;
+                const int swz = (row >> 1) & 3;  // the code box's 64-byte swizzle for this row
+                const uint4 c0 = *reinterpret_cast<const uint4 *>(cst + row * 64 + (((2 * kh) ^ swz) << 4));
+                const uint4 c1 = *reinterpret_cast<const uint4 *>(cst + row * 64 + (((2 * kh + 1) ^ swz) << 4));
+                const uint32_t sc2 = *reinterpret_cast<const uint16_t *>(cst + kFp4Bytes + (row >> 6) * 128 * kCK +
+                                                                          kh * 128 + (row & 63) * 2);
+                const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        const uint4 d = dequant8_f16(w[4 * hf + j], sx);
-                        v[16 * hf + 4 * j + 0] = d.x;
-                        v[16 * hf + 4 * j + 1] = d.y;
-                        v[16 * hf + 4 * j + 2] = d.z;
-                        v[16 * hf + 4 * j + 3] = d.w;
-                    }
-                } else {
-                    const bool big = sc > 128u;
-                    const uint32_t l = scale_lo(sc), h = scale_hi(sc);
+                for (int hf = 0; hf < 2; hf++) {
+                    const uint32_t sc = (sc2 >> (8 * hf)) & 0xFFu;
+                    if (F16) {
+                        const uint32_t sx = scale_f16x2(sc);
 #pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        const uint4 d = dequant8(w[4 * hf + j], l, h, big);
-                        v[16 * hf + 4 * j + 0] = d.x;
-                        v[16 * hf + 4 * j + 1] = d.y;
-                        v[16 * hf + 4 * j + 2] = d.z;
-                        v[16 * hf + 4 * j + 3] = d.w;
+                        for (int j = 0; j < 4; j++)
+                            *reinterpret_cast<uint4 *>(bdst + sw128(row, 4 * hf + j)) = dequant8_f16(w[4 * hf + j], sx);
+                    } else {
+                        const bool big = sc > 128u;
+                        const uint32_t l = scale_lo(sc), h = scale_hi(sc);
+#pragma unroll
+                        for (int j = 0; j < 4; j++)
+                            *reinterpret_cast<uint4 *>(bdst + sw128(row, 4 * hf + j)) = dequant8(w[4 * hf + j], l, h, big);
                     }
                 }
             }
-            tmem_st32(trow + (uint32_t)(kACol0 + s * kACols), v);
-            tmem_wait_st();
             if (warp == kWarpDq0 && lane == 0) MOE_PF_KMARK(9, g);
-            tc_fence_before();
+            fence_proxy_async();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&full_ab[s]);
@@ -548,7 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
         }
     } else {
         // ------------------------------------------ epilogue (warps 11..14)
-        const int q = warp & 3;  // TMEM lane quarter of this warp
+        // lane quarter q: routes 32 q .. 32 q + 31 of the tile, one per thread;
+        // a thread writes its route's row of h (or y) with 16-byte stores
+        const int q = warp & 3, lrow = q * 32 + lane;
         int li = 0;
         for (int it = blockIdx.x; it < n_items; it += gridDim.x, li++) {
             const int tile = it / mtiles, mt = it - tile * mtiles;
@@ -560,56 +565,67 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
             if (warp == kWarpEpi0 && lane == 0) MOE_PF_KMARK(7, li);
             tc_fence_after();
             const uint32_t taddr = tmem + (uint32_t)(ab * kAccCols) + ((uint32_t)(q * 32) << 16);
-            if (GATEUP) {
-                // gate row j sits in TMEM lane j, up row j in lane 64 + j: warps q and
-                // q + 2 hold the two halves of row j's pair and swap half of their
-                // columns through shared memory, so that each computes 16 of every 32
-                const int jl = (q & 1) * 32 + lane, j = mt * 64 + jl;
-                const bool gate_w = q < 2;
-                const float bg = mat_bias(a.A0, e, E)[j], bu = mat_bias(a.A1, e, E)[j];
-                const int pj = F16 ? j : mma_perm_pos(j);
-                uint16_t *hdst = (F16 ? a.ws.h16 : a.ws.h) + (size_t)rstart * a.bp.F + pj;
-                float *xg = xch + jl * 17, *xu = xch + 64 * 17 + jl * 17;
-                for (int c0 = 0; c0 < rcount; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(taddr + c0, v);
+            const bool mine = lrow < rcount;
+            if (q * 32 < rcount) {  // warp-uniform: the quarter holds routes of the tile
+                // the item's 256 biases (gate then up, or down), staged once per warp
+                float *bias = s_bias + (warp - kWarpEpi0) * kBiasFloats;
 #pragma unroll
-                    for (int c = 0; c < 16; c++) {
-                        if (gate_w)
-                            xg[c] = v[16 + c];
-                        else
-                            xu[c] = v[c];
-                    }
-                    named_bar_sync(1 + (q & 1), 64);
-                    const int cb = c0 + (gate_w ? 0 : 16);
-#pragma unroll
-                    for (int c = 0; c < 16; c++) {
-                        if (cb + c >= rcount) continue;
-                        const float gv = gate_w ? v[c] : xg[c], uv = gate_w ? xu[c] : v[16 + c];
-                        const float hv = swiglu_clamped(gv + bg, uv + bu, a.bp.alpha, a.bp.limit);
-                        __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-                        uint16_t bits = *reinterpret_cast<uint16_t *>(&hb);
-                        if (F16) {
-                            const __half hh = __float2half_rn(__bfloat162float(hb));  // exact in the fp16 range
-                            bits = *reinterpret_cast<const uint16_t *>(&hh);
-                        }
-                        hdst[(size_t)(cb + c) * a.bp.F] = bits;
-                    }
-                    named_bar_sync(1 + (q & 1), 64);
+                for (int i = lane; i < kWN; i += 32) {
+                    const int half = GATEUP ? i / RPI : 0, row = mt * RPI + (GATEUP ? i % RPI : i);
+                    bias[i] = row < a.rows ? __ldg(mat_bias(half ? a.A1 : a.A0, e, E) + row) : 0.0f;
                 }
-            } else {
-                const int i = mt * 128 + q * 32 + lane;
-                const bool row_ok = i < a.rows;
-                const float bd = row_ok ? mat_bias(a.A0, e, E)[i] : 0.0f;
-                for (int c0 = 0; c0 < rcount; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(taddr + c0, v);
-                    if (!row_ok) continue;
+                __syncwarp();
+                if (GATEUP) {
+                    uint16_t *hrow = (F16 ? a.ws.h16 : a.ws.h) + (size_t)(rstart + lrow) * a.bp.F;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < RPI; c0 += 32) {
+                        const int j0 = mt * RPI + c0;
+                        if (j0 >= a.rows) break;  // F is a multiple of 64: whole 32-column chunks
+                        float gv[32], uv[32];
+                        tmem_ld32(taddr + c0, gv);
+                        tmem_ld32(taddr + RPI + c0, uv);
+                        if (!mine) continue;
+                        uint32_t bits[32];
 #pragma unroll
-                    for (int c = 0; c < 32; c++) {
-                        if (c0 + c >= rcount) continue;
-                        const int route = rstart + c0 + c;
-                        a.ws.y[(size_t)route * a.bp.H + i] = a.ws.perm_w[route] * (v[c] + bd);
+                        for (int c = 0; c < 32; c++) {
+                            const float hv = swiglu_fast(gv[c] + bias[c0 + c], uv[c] + bias[RPI + c0 + c],
+                                                         a.bp.alpha, a.bp.limit);
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                            bits[c] = *reinterpret_cast<const uint16_t *>(&hb);
+                            if (F16) {
+                                const __half hh = __float2half_rn(__bfloat162float(hb));  // exact in the fp16 range
+                                bits[c] = *reinterpret_cast<const uint16_t *>(&hh);
+                            }
+                        }
+                        // fp16: natural order; bf16: the 32-block pair order (elements i and
+                        // i + 4 of every 8 share a word), as the next GEMM's B-side expects
+                        uint32_t wd[16];
+#pragma unroll
+                        for (int k = 0; k < 16; k++) {
+                            const int lo = F16 ? 2 * k : 8 * (k >> 2) + (k & 3), hi = F16 ? 2 * k + 1 : lo + 4;
+                            wd[k] = bits[lo] | (bits[hi] << 16);
+                        }
+                        uint4 *dst = reinterpret_cast<uint4 *>(hrow + j0);
+#pragma unroll
+                        for (int k = 0; k < 4; k++)
+                            dst[k] = make_uint4(wd[4 * k], wd[4 * k + 1], wd[4 * k + 2], wd[4 * k + 3]);
+                    }
+                } else {
+                    const float w = mine ? a.ws.perm_w[rstart + lrow] : 0.0f;
+                    float *yrow = a.ws.y + (size_t)(rstart + lrow) * a.bp.H;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < RPI; c0 += 32) {
+                        const int i0 = mt * RPI + c0;
+                        if (i0 >= a.rows) break;  // H is a multiple of 64: whole 32-column chunks
+                        float v[32];
+                        tmem_ld32(taddr + c0, v);
+                        if (!mine) continue;
+                        float4 *dst = reinterpret_cast<float4 *>(yrow + i0);
+#pragma unroll
+                        for (int k = 0; k < 8; k++)
+                            dst[k] = make_float4(w * (v[4 * k] + bias[c0 + 4 * k]), w * (v[4 * k + 1] + bias[c0 + 4 * k + 1]),
+                                                 w * (v[4 * k + 2] + bias[c0 + 4 * k + 2]),
+                                                 w * (v[4 * k + 3] + bias[c0 + 4 * k + 3]));
                     }
                 }
             }
@@ -659,12 +675,13 @@ cudaError_t make_codes_map(CUtensorMap *m, const uint8_t *codes, size_t n_rows, 
 }
 
 size_t prefill_smem_bytes() {
-    return 1024 + kStages * kBBytes + kCStages * kCStageBytes + kXchFloats * 4 + kSmTiles * 16 + 512;
+    return 1024 + kStages * (kABytes + kBBytes) + kCStages * kCStageBytes + kSmTiles * 16 +
+           kEpiWarps * kBiasFloats * 4 + 512;
 }
 
-// 2D map over a bf16 activation matrix [rows][K]: box 64 elements (128 B) x
-// box_rows (32, 64, 128), 128-byte swizzle (the K-major layout the MMA
-// descriptors expect; the box is whole 8-row swizzle atoms).
+// 2D map over a 16-bit activation matrix [rows][K] (the MMA's A operand): box
+// 64 elements (128 B) x box_rows (32, 64, 128), 128-byte swizzle (the K-major
+// layout the MMA descriptors expect; the box is whole 8-row swizzle atoms).
 cudaError_t make_act_map(CUtensorMap *m, const uint16_t *base, int rows, int K, bool f16, int box_rows) {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
@@ -706,29 +723,31 @@ __global__ void __launch_bounds__(256) moe_pack_scales_kernel(const uint8_t *in,
     }
 }
 
-// blocks of one repacked matrix set: n_exp experts plus two pad blocks (a
-// code stage's chunk pair may start at the last chunk of the last real block)
-size_t packed_blocks(int n_exp, int rows) { return (size_t)n_exp * ((rows + 63) / 64) + 2; }
+// blocks of one repacked matrix set: n_exp experts plus four pad blocks (a
+// down item's four blocks may run three past the last real one, and a code
+// stage's chunk pair one chunk further)
+size_t packed_blocks(int n_exp, int rows) { return (size_t)n_exp * ((rows + 63) / 64) + 4; }
 size_t packed_bytes(int n_exp, int rows, int cols) {
     return (packed_blocks(n_exp, rows) * (size_t)(cols / kBK) * 128 + 255) & ~(size_t)255;
 }
 
 }  // namespace
 
-int prefill_tile_rows() { return kBN; }
+int prefill_tile_rows() { return kTM; }
 
 cudaError_t prefill_make_maps(const BlockParams &bp, const MatPtrs &gate, const MatPtrs &up, const MatPtrs &down,
                               PrefillMaps *out) {
     MOE_CUDA_TRY(get_encoder());
     const int E = bp.E;
     TmaMaps &g = out->gateup, &d = out->down;
-    MOE_CUDA_TRY(make_codes_map(&g.m[0], gate.codes, (size_t)E * gate.rows, gate.cols, 64));
-    MOE_CUDA_TRY(make_codes_map(&g.m[1], up.codes, (size_t)E * up.rows, up.cols, 64));
-    MOE_CUDA_TRY(make_codes_map(&g.m[2], bp.n_shared ? gate.sh_codes : nullptr, gate.rows, gate.cols, 64));
-    MOE_CUDA_TRY(make_codes_map(&g.m[3], bp.n_shared ? up.sh_codes : nullptr, up.rows, up.cols, 64));
-    MOE_CUDA_TRY(make_codes_map(&d.m[0], down.codes, (size_t)E * down.rows, down.cols, 128));
+    // gate/up items: 128 gate rows + the same 128 up rows; down items: 256 rows
+    MOE_CUDA_TRY(make_codes_map(&g.m[0], gate.codes, (size_t)E * gate.rows, gate.cols, kWN / 2));
+    MOE_CUDA_TRY(make_codes_map(&g.m[1], up.codes, (size_t)E * up.rows, up.cols, kWN / 2));
+    MOE_CUDA_TRY(make_codes_map(&g.m[2], bp.n_shared ? gate.sh_codes : nullptr, gate.rows, gate.cols, kWN / 2));
+    MOE_CUDA_TRY(make_codes_map(&g.m[3], bp.n_shared ? up.sh_codes : nullptr, up.rows, up.cols, kWN / 2));
+    MOE_CUDA_TRY(make_codes_map(&d.m[0], down.codes, (size_t)E * down.rows, down.cols, kWN));
     d.m[1] = d.m[0];
-    MOE_CUDA_TRY(make_codes_map(&d.m[2], bp.n_shared ? down.sh_codes : nullptr, down.rows, down.cols, 128));
+    MOE_CUDA_TRY(make_codes_map(&d.m[2], bp.n_shared ? down.sh_codes : nullptr, down.rows, down.cols, kWN));
     d.m[3] = d.m[2];
     return cudaSuccess;
 }
@@ -777,11 +796,11 @@ cudaError_t launch_gather(const BlockParams &bp, const Workspace &ws, int T, boo
 }
 
 template <bool GATEUP, bool F16>
-cudaError_t launch_pf(const PrefillArgs &args, const TmaMaps &maps, const BMaps &bmaps, dim3 grid,
+cudaError_t launch_pf(const PrefillArgs &args, const TmaMaps &maps, const AMaps &amaps, dim3 grid,
                       cudaStream_t st) {
     static bool done = false;
     MOE_CUDA_TRY(smem_optin_once(moe_prefill_kernel<GATEUP, F16>, done));
-    moe_prefill_kernel<GATEUP, F16><<<grid, kThreads, prefill_smem_bytes(), st>>>(args, maps, bmaps);
+    moe_prefill_kernel<GATEUP, F16><<<grid, kThreads, prefill_smem_bytes(), st>>>(args, maps, amaps);
     return cudaGetLastError();
 }
 
@@ -789,13 +808,13 @@ cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, con
                                  bool gateup, int T, const TmaMaps &maps, bool f16, cudaStream_t st) {
     PrefillArgs args{bp, ws, a0, a1, gateup ? bp.H : bp.F, gateup ? bp.F : bp.H};
     const int R = T * (bp.K + bp.n_shared);
-    BMaps bmaps;
+    AMaps amaps;
     MOE_CUDA_TRY(get_encoder());
     const uint16_t *bsrc = gateup ? ws.xs : (f16 ? ws.h16 : ws.h);
-    for (int i = 0; i < 3; i++) MOE_CUDA_TRY(make_act_map(&bmaps.m[i], bsrc, R, args.Kdim, f16, 32 << i));
-    int tiles = (R + kBN - 1) / kBN + bp.E + bp.n_shared;
+    for (int i = 0; i < 3; i++) MOE_CUDA_TRY(make_act_map(&amaps.m[i], bsrc, R, args.Kdim, f16, 32 << i));
+    int tiles = (R + kTM - 1) / kTM + bp.E + bp.n_shared;
     if (tiles > ws.max_tiles) tiles = ws.max_tiles;
-    const int mtiles = gateup ? bp.F / 64 : (bp.H + 127) / 128;
+    const int mtiles = gateup ? (bp.F + kWN / 2 - 1) / (kWN / 2) : (bp.H + kWN - 1) / kWN;
     // persistent: one CTA per SM, or fewer when there are fewer work items
     static int n_sm = 0;
     if (!n_sm) {
@@ -806,6 +825,6 @@ cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, con
     const long items = (long)tiles * mtiles;
     const dim3 grid((unsigned)(items < n_sm ? items : n_sm));
     if (gateup)
-        return f16 ? launch_pf<true, true>(args, maps, bmaps, grid, st) : launch_pf<true, false>(args, maps, bmaps, grid, st);
-    return f16 ? launch_pf<false, true>(args, maps, bmaps, grid, st) : launch_pf<false, false>(args, maps, bmaps, grid, st);
+        return f16 ? launch_pf<true, true>(args, maps, amaps, grid, st) : launch_pf<true, false>(args, maps, amaps, grid, st);
+    return f16 ? launch_pf<false, true>(args, maps, amaps, grid, st) : launch_pf<false, false>(args, maps, amaps, grid, st);
 }
