@@ -278,11 +278,12 @@ def run_ours(args, rank, world, local):
     gu_bytes = sum(facts[i % len(sets)][0] for i in range(args.steps)) / args.steps
     dn_bytes = sum(facts[i % len(sets)][1] for i in range(args.steps)) / args.steps
     distinct = sum(facts[i % len(sets)][2] for i in range(args.steps)) / args.steps
-    hbm, _, peak_kind = peaks()
+    hbm, bf16_peak, peak_kind = peaks()
     dom = max(range(4), key=lambda k: tot[k])
     dom_bytes = {1: gu_bytes, 2: dn_bytes}.get(dom, gu_bytes)
     achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9 if avg_ms[dom] > 0 else 0.0
     tr = traffic_record(KERNEL_SLOTS[dom])
+    path = sets[0]["plan"].path_for(TOKENS)  # 1 GEMV decode path, 2 tensor-core grouped GEMM
     step_bytes = gu_bytes + dn_bytes
     step_gbs = step_bytes / (ms / args.steps / 1e3) / 1e9
     routes = TOKENS * (K + shape.n_shared)
@@ -336,15 +337,41 @@ def run_ours(args, rank, world, local):
                    "algorithmic_flops_per_step": step_flops, "step_tflops": step_tflops,
                    "step_tensor_frac_of_bf16_peak": step_tflops / peaks()[1],
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": KERNEL_SLOTS[dom], "achieved": achieved, "peak": hbm,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": tr["bytes_per_launch"] if tr else None,
-                     "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": avg_ms[dom]},
+        "roofline": roofline(path, dom, avg_ms[dom], achieved, hbm, bf16_peak, peak_kind, tr, dom_bytes,
+                             routes, H, shape.expert_hidden, TOKENS * shape.n_experts * H),
         "kernels": {KERNEL_SLOTS[k]: {"avg_us": 1e3 * avg_ms[k], "share": share[k], "launches": cnt[k]}
                     for k in range(4)},
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": int(sum(cnt)),
     }
     print(json.dumps(line), flush=True)
+
+
+# fp32 FMA peak of the SIMT router: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz
+# (the GB300's SM count and maximum SM clock)
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def roofline(path, dom, avg_ms, achieved_gbs, hbm, bf16_peak, peak_kind, tr, dom_bytes, routes, H, F, router_macs):
+    """Roofline of the dominant kernel: HBM for the GEMVs (decode path), the
+    bf16 tensor peak for the grouped GEMMs (prefill path), the fp32 FMA peak
+    when the SIMT routing kernel dominates a prefill step."""
+    if path == 2 and dom in (1, 2):
+        flops = 2.0 * routes * (2 * F if dom == 1 else F) * H
+        ach = flops / (avg_ms / 1e3) / 1e12 if avg_ms > 0 else 0.0
+        return {"bound": "tensor", "kernel": KERNEL_SLOTS[dom], "achieved": ach, "peak": bf16_peak,
+                "peak_kind": peak_kind, "unit": "TFLOP/s", "frac": ach / bf16_peak, "traffic": None,
+                "algorithmic_flops_per_launch": flops, "avg_launch_ms": avg_ms}
+    if path == 2 and dom == 0:
+        flops = 2.0 * router_macs
+        ach = flops / (avg_ms / 1e3) / 1e12 if avg_ms > 0 else 0.0
+        return {"bound": "alu", "kernel": KERNEL_SLOTS[dom], "achieved": ach, "peak": ALU_FP32_TFLOPS,
+                "peak_kind": "derived (SM count x fp32 lanes x 2 x max SM clock)", "unit": "TFLOP/s",
+                "frac": ach / ALU_FP32_TFLOPS, "traffic": None, "algorithmic_flops_per_launch": flops,
+                "avg_launch_ms": avg_ms}
+    return {"bound": "hbm", "kernel": KERNEL_SLOTS[dom], "achieved": achieved_gbs, "peak": hbm,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved_gbs / hbm,
+            "traffic": tr["bytes_per_launch"] if tr else None,
+            "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": avg_ms}
 
 
 def main():

@@ -89,7 +89,8 @@ void moe_plan_destroy(moe_plan *plan);
  *                       (ds4.c DS4_SHAPE_FLASH n_expert_shared)
  *   "max_tokens"        largest token count per forward (sizes the workspace)
  *   "decode_max_tokens" forwards with tokens <= this use the GEMV decode path,
- *                       larger ones the tensor-core grouped-GEMM path (default 16)
+ *                       larger ones the tensor-core grouped-GEMM path; -1
+ *                       (default): 60 for up to 64 experts, 8 above
  *   "path"              0 auto, 1 force decode, 2 force prefill (testing)
  *   "router_exact"      1: compute every router logit in fp64 (testing)
  *   "profile"           1: time each kernel launch with CUDA events (see
@@ -98,6 +99,13 @@ void moe_plan_destroy(moe_plan *plan);
 int moe_plan_set_i(moe_plan *plan, const char *key, long long value);
 /* Floating options: "rms_eps". */
 int moe_plan_set_f(moe_plan *plan, const char *key, double value);
+/* Which projection kernels a forward of `tokens` tokens would run: 1 the GEMV
+ * decode path, 2 the tensor-core grouped-GEMM path (the "path" and
+ * "decode_max_tokens" options and the shape decide; the choice also needs
+ * the weights loaded, since the grouped GEMM's tensor maps are built then).
+ * Negative status on error (NULL plan, weights not loaded, no path for the
+ * shape).  Host only; enqueues nothing. */
+int moe_plan_path_for(const moe_plan *plan, int tokens);
 
 /* Bytes of device workspace a forward of up to max_tokens tokens needs
  * (max_tokens <= 0: the plan's max_tokens).  0 on error. */

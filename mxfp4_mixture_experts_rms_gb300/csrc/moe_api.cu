@@ -46,7 +46,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 struct moe_plan {
     BlockParams bp;
     int max_tokens = 4096;
-    int decode_max_tokens = 16;
+    int decode_max_tokens = -1;  // -1: chosen from the shape (auto_decode_max)
     int path = 0;
     int router_exact = 0;
     void *ws_ptr = nullptr;
@@ -83,6 +83,12 @@ struct Carve {
     }
 };
 
+// Largest token count for which the GEMVs beat the grouped GEMM, measured on a
+// GB300: with 32 experts the GEMV path wins up to 56 tokens and ties at 64
+// (each expert tile then streams its weights with few routes per tile either
+// way); with 256 experts it wins up to 8 tokens, the grouped GEMM from 12.
+int auto_decode_max(const BlockParams &b) { return b.E <= 64 ? 60 : 8; }
+
 // Which projection kernels run for this token count: the GEMV (decode) path
 // or the tensor-core grouped GEMM (prefill) path.
 int choose_path(const moe_plan *p, int tokens, bool *decode, int *nt, int *tile_rows) {
@@ -93,7 +99,8 @@ int choose_path(const moe_plan *p, int tokens, bool *decode, int *nt, int *tile_
     const bool decode_ok = decode_supported(b);
     if (p->path == 2 && !prefill_ok) return fail(MOE_ESHAPE, "the prefill path needs H and F multiples of 64");
     if (p->path == 1 && !decode_ok) return fail(MOE_ESHAPE, "the decode path needs H and F <= 4800");
-    bool d = p->path == 1 || (p->path == 0 && (!prefill_ok || (decode_ok && tokens <= p->decode_max_tokens)));
+    const int dmax = p->decode_max_tokens >= 0 ? p->decode_max_tokens : auto_decode_max(b);
+    bool d = p->path == 1 || (p->path == 0 && (!prefill_ok || (decode_ok && tokens <= dmax)));
     if (d && !decode_ok) return fail(MOE_ESHAPE, "no kernel path for H=%d F=%d", b.H, b.F);
     *decode = d;
     *nt = tokens <= 8 ? 1 : 2;
@@ -220,7 +227,7 @@ int moe_plan_set_i(moe_plan *p, const char *key, long long v) {
         if (p->have_ws) return fail(MOE_EINVAL, "max_tokens must be set before moe_set_workspace");
         p->max_tokens = (int)v;
     } else if (!strcmp(key, "decode_max_tokens")) {
-        if (v < 0 || v > (1 << 20)) return fail(MOE_EINVAL, "decode_max_tokens out of range");
+        if (v < -1 || v > (1 << 20)) return fail(MOE_EINVAL, "decode_max_tokens out of range");
         p->decode_max_tokens = (int)v;
     } else if (!strcmp(key, "path")) {
         if (v < 0 || v > 2) return fail(MOE_EINVAL, "path must be 0, 1 or 2");
@@ -239,6 +246,16 @@ int moe_plan_set_i(moe_plan *p, const char *key, long long v) {
         return fail(MOE_EINVAL, "unknown integer option '%s'", key);
     }
     return MOE_OK;
+}
+
+int moe_plan_path_for(const moe_plan *p, int tokens) {
+    if (!p) return fail(MOE_EINVAL, "NULL plan");
+    if (!p->have_w) return fail(MOE_ENOTREADY, "moe_load_weights has not been called");
+    bool decode = false;
+    int nt = 1, tile_rows = 0;
+    const int rc = choose_path(p, tokens, &decode, &nt, &tile_rows);
+    if (rc != MOE_OK) return rc;
+    return decode ? 1 : 2;
 }
 
 int moe_plan_set_f(moe_plan *p, const char *key, double v) {

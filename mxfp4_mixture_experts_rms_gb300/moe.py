@@ -20,7 +20,8 @@ _STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ESHAPE", -3: "MOE_ENOTR
 
 _lib = None
 
-EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_plan_set_i", "moe_plan_set_f", "moe_workspace_bytes",
+EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_plan_set_i", "moe_plan_set_f", "moe_plan_path_for",
+           "moe_workspace_bytes",
            "moe_set_workspace", "moe_load_weights", "moe_forward", "moe_forward_ex", "moe_get_expert_counts",
            "moe_get_permutation", "moe_debug_dequant", "moe_profile_read", "moe_get_device_status",
            "moe_forward_noalloc", "moe_last_error"]
@@ -63,6 +64,7 @@ def load(build_if_missing: bool = True):
     L.moe_plan_destroy.argtypes = [P]
     L.moe_plan_set_i.argtypes = [P, C.c_char_p, LL]
     L.moe_plan_set_f.argtypes = [P, C.c_char_p, D]
+    L.moe_plan_path_for.argtypes = [P, I]
     L.moe_workspace_bytes.restype = SZ
     L.moe_workspace_bytes.argtypes = [P, I]
     L.moe_set_workspace.argtypes = [P, P, SZ]
@@ -162,6 +164,12 @@ class Plan:
 
     def set_f(self, key: str, v: float):
         _check(self.L.moe_plan_set_f(self.h, key.encode(), float(v)))
+
+    def path_for(self, tokens: int) -> int:
+        """1 if a forward of `tokens` tokens runs the GEMV decode path, 2 the grouped GEMM."""
+        rc = int(self.L.moe_plan_path_for(self.h, int(tokens)))
+        _check(min(rc, 0))
+        return rc
 
     def workspace_bytes(self, max_tokens: int = 0) -> int:
         return int(self.L.moe_workspace_bytes(self.h, max_tokens))

@@ -103,15 +103,18 @@ def test_routing_near_ties_are_resolved_exactly():
 
 
 # ------------------------------------------------------------------ full block
-@pytest.mark.parametrize("H,F,E,K,T,ns,scale", [
-    (64, 96, 5, 3, 1, 0, 1.0), (64, 96, 5, 3, 3, 0, 1.0), (96, 64, 5, 3, 9, 0, 1.0),
-    (64, 96, 5, 3, 17, 1, 1.5), (128, 64, 8, 2, 33, 0, 1.0), (32, 32, 4, 2, 40, 1, 2.5),
-    (64, 64, 1, 1, 5, 0, 1.0), (160, 96, 16, 8, 12, 0, 1.0)])
-def test_block_parity_ragged_shapes(H, F, E, K, T, ns, scale):
+@pytest.mark.parametrize("H,F,E,K,T,ns,scale,path", [
+    (64, 96, 5, 3, 1, 0, 1.0, 0), (64, 96, 5, 3, 3, 0, 1.0, 0), (96, 64, 5, 3, 9, 0, 1.0, 0),
+    (64, 96, 5, 3, 17, 1, 1.5, 0), (128, 64, 8, 2, 33, 0, 1.0, 0), (32, 32, 4, 2, 40, 1, 2.5, 0),
+    (64, 64, 1, 1, 5, 0, 1.0, 0), (160, 96, 16, 8, 12, 0, 1.0, 0),
+    # the grouped GEMM on ragged token counts, several route tiles, the shared expert
+    (128, 64, 8, 2, 33, 0, 1.0, 2), (64, 128, 6, 2, 50, 1, 1.5, 2), (128, 192, 5, 3, 70, 0, 1.0, 2),
+    (192, 320, 3, 2, 200, 0, 1.0, 2)])
+def test_block_parity_ragged_shapes(H, F, E, K, T, ns, scale, path):
     shape = synth.tiny_shape(H, F, E, K, n_shared=ns, weight_scale=scale)
     blk = tiny_block(H * 7 + T, shape)
     x = synth.f32_to_bf16_bits(np.random.default_rng(T).normal(0, 1, (T, H)))
-    r, _, _ = run_gpu(blk, x)
+    r, _, _ = run_gpu(blk, x, path=path)
     ref = oracle.moe_forward(blk, x, nthreads=NTHREADS)
     assert r["status"] == 0
     assert np.array_equal(r["ids"], ref["ids"])
