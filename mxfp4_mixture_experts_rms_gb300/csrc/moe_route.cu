@@ -592,15 +592,18 @@ __device__ __forceinline__ void router_logit(const uint16_t *wrow, const uint16_
 }
 
 // Router logits of one expert row (shared memory) for up to 8 x_hat rows
-// (shared memory, tokens g0, g0 + gstep, ...), by one warp: the arithmetic of
-// router_logit with the row's 16-byte chunks loaded once for all tokens.
+// (shared memory, tokens g0, g0 + gstep, ...), by one warp, with the summation
+// tree of router_logit.  The error bound uses sum|x_i w_i| <= |x| |w|
+// (Cauchy-Schwarz) instead of accumulating |x_i w_i|: xnorm[g] is an upper
+// bound of token g's |x_hat|, and |w| is accumulated here once for all tokens,
+// so each multiply-add costs one FMA.
 __device__ __forceinline__ void router_logits_tokens(const uint16_t *wrow, const uint16_t *xh, int H, int g0,
                                                      int gstep, int nt, float b, int lane, float *lg_row,
-                                                     float *lb_row, int E) {
+                                                     float *lb_row, int E, const float *xnorm) {
     const int nchunk = H / 8, per_lane = (nchunk + 31) / 32, chain = 8 + per_lane + 6;
-    float acc[8], sab[8];
+    float acc[8], sw = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; j++) acc[j] = sab[j] = 0.f;
+    for (int j = 0; j < 8; j++) acc[j] = 0.f;
     for (int ch = lane; ch < nchunk; ch += 32) {
         const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + 8 * ch);
         const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -611,33 +614,35 @@ __device__ __forceinline__ void router_logits_tokens(const uint16_t *wrow, const
             wf[2 * q + 1] = __uint_as_float(ww[q] & 0xFFFF0000u);
         }
 #pragma unroll
+        for (int q = 0; q < 8; q++) sw = fmaf(wf[q], wf[q], sw);
+#pragma unroll
         for (int j = 0; j < 8; j++) {
             const int g = g0 + j * gstep;
             if (g >= nt) break;
             const uint4 xq = *reinterpret_cast<const uint4 *>(xh + (size_t)g * H + 8 * ch);
             const uint32_t xx[4] = {xq.x, xq.y, xq.z, xq.w};
-            float cs = 0.f, ab = sab[j];
+            float cs = 0.f;
 #pragma unroll
             for (int q = 0; q < 4; q++) {
-                const float x0 = __uint_as_float(xx[q] << 16), x1 = __uint_as_float(xx[q] & 0xFFFF0000u);
-                cs = fmaf(x0, wf[2 * q], cs);
-                cs = fmaf(x1, wf[2 * q + 1], cs);
-                ab = fmaf(fabsf(x0), fabsf(wf[2 * q]), ab);
-                ab = fmaf(fabsf(x1), fabsf(wf[2 * q + 1]), ab);
+                cs = fmaf(__uint_as_float(xx[q] << 16), wf[2 * q], cs);
+                cs = fmaf(__uint_as_float(xx[q] & 0xFFFF0000u), wf[2 * q + 1], cs);
             }
             acc[j] += cs;
-            sab[j] = ab;
         }
     }
+    // |w|: a sum of squares (relative error below 2e-6 here), one correctly
+    // rounded square root, then a margin well above both
+    const float wn = sqrtf(warp_sum_f(sw)) * (1.0f + 0x1p-14f);
 #pragma unroll
     for (int j = 0; j < 8; j++) {
         const int g = g0 + j * gstep;
         if (g >= nt) break;
-        const float sm = warp_sum_f(acc[j]), ab = warp_sum_f(sab[j]);
+        const float sm = warp_sum_f(acc[j]);
         if (lane == 0) {
             const float l = sm + b;
             lg_row[(size_t)g * E] = l;
-            lb_row[(size_t)g * E] = 2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
+            lb_row[(size_t)g * E] =
+                2.0f * (float)chain * 0x1p-24f * (xnorm[g] * wn + fabsf(b) + fabsf(l)) + 1e-30f;
         }
     }
 }
@@ -786,27 +791,32 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
 // computes expert w % RC for the tokens g with g % (8/RC) == w / RC; warp w
 // < 4 then selects token w's top-k.  The permutation follows as a kernel of
 // its own.
-constexpr int kBatchTokens = 4;  // tokens per CTA (small CTAs: two fit an SM, more SMs busy)
+constexpr int kBatchTokensMax = 8;  // tokens per CTA: 4 (two CTAs per SM) or, for large batches, 8
 
-__host__ __device__ inline size_t batch_rows_off(int H) { return (size_t)kBatchTokens * H * 2; }
-__host__ __device__ inline size_t batch_lg_off(int H, int RC) { return batch_rows_off(H) + (size_t)2 * RC * H * 2; }
-__host__ __device__ inline size_t batch_gm_off(int H, int E, int RC) {
-    return batch_lg_off(H, RC) + (size_t)kBatchTokens * E * 8;  // logits + bounds; exact logits reuse the ring
+__host__ __device__ inline size_t batch_rows_off(int H, int TB) { return (size_t)TB * H * 2; }
+__host__ __device__ inline size_t batch_lg_off(int H, int RC, int TB) {
+    return batch_rows_off(H, TB) + (size_t)2 * RC * H * 2;
 }
-__host__ __device__ inline size_t batch_smem(int H, int E, int RC) { return batch_gm_off(H, E, RC) + (size_t)H * 4; }
+__host__ __device__ inline size_t batch_gm_off(int H, int E, int RC, int TB) {
+    return batch_lg_off(H, RC, TB) + (size_t)TB * E * 8;  // logits + bounds; exact logits reuse the ring
+}
+__host__ __device__ inline size_t batch_smem(int H, int E, int RC, int TB) {
+    return batch_gm_off(H, E, RC, TB) + (size_t)H * 4;
+}
 
-__global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArgs a, int RC) {
+__global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArgs a, int RC, int TB) {
     extern __shared__ __align__(128) unsigned char smem[];
     MOE_PHASE_MARK(7);
     const int H = a.bp.H, E = a.bp.E;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * kBatchTokens, nt = min(kBatchTokens, a.T - t0);
-    uint16_t *xh = reinterpret_cast<uint16_t *>(smem);                                  // [4][H]
-    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + batch_rows_off(H));            // [2][RC][H]
-    float *lg = reinterpret_cast<float *>(smem + batch_lg_off(H, RC));                  // [4][E]
-    float *lb = lg + kBatchTokens * E;                                                  // [4][E]
-    double *exs = reinterpret_cast<double *>(ring);                                     // [4][E] after the ring
+    const int t0 = blockIdx.x * TB, nt = min(TB, a.T - t0);
+    uint16_t *xh = reinterpret_cast<uint16_t *>(smem);                                  // [TB][H]
+    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + batch_rows_off(H, TB));        // [2][RC][H]
+    float *lg = reinterpret_cast<float *>(smem + batch_lg_off(H, RC, TB));              // [TB][E]
+    float *lb = lg + TB * E;                                                            // [TB][E]
+    double *exs = reinterpret_cast<double *>(ring);                                     // [TB][E] after the ring
     __shared__ __align__(8) uint64_t wbar[2];
+    __shared__ float xnorm[kBatchTokensMax];  // upper bounds of the tokens' |x_hat|
     const int nchunk = (E + RC - 1) / RC;
     const uint32_t slot_bytes = (uint32_t)RC * H * 2;
     // CTAs walk the chunks from different starting points, so that they do
@@ -837,7 +847,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
         issue(0);
         if (nchunk > 1) issue(1);
     }
-    float *gsm = reinterpret_cast<float *>(smem + batch_gm_off(H, E, RC));  // gamma [H]
+    float *gsm = reinterpret_cast<float *>(smem + batch_gm_off(H, E, RC, TB));  // gamma [H]
     for (int c = tid; c < H / 4; c += kRouteThreads)
         reinterpret_cast<float4 *>(gsm)[c] = __ldg(reinterpret_cast<const float4 *>(a.gamma) + c);
     __syncthreads();
@@ -856,6 +866,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
         __syncwarp();
         MOE_PHASE_MARK(6);
         const float r32 = (float)r;
+        float xs = 0.f;  // sum of x_hat^2 (for the router's error bound)
         for (int c = lane; c < H / 8; c += 32) {
             const uint4 xv = reinterpret_cast<const uint4 *>(row)[c];
             const float4 g0 = reinterpret_cast<const float4 *>(gsm)[2 * c];
@@ -865,6 +876,8 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
             uint32_t hb[8];
 #pragma unroll
             for (int q = 0; q < 8; q++) hb[q] = norm_elem((w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, gg[q], r32, r);
+#pragma unroll
+            for (int q = 0; q < 8; q++) xs = fmaf(__uint_as_float(hb[q] << 16), __uint_as_float(hb[q] << 16), xs);
             const uint4 nat = make_uint4(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16, hb[4] | hb[5] << 16,
                                          hb[6] | hb[7] << 16);
             reinterpret_cast<uint4 *>(row)[c] = nat;
@@ -883,6 +896,9 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
                 make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
             if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + go) = nat;
         }
+        // |x_hat| with a margin above the error of the sum (positive terms) and of the root
+        const float xn = sqrtf(warp_sum_f(xs)) * (1.0f + 0x1p-14f);
+        if (lane == 0) xnorm[warp] = xn;
     }
     __syncthreads();
     MOE_PHASE_MARK(1);
@@ -915,7 +931,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
             const uint16_t *wrow = ring + (size_t)(c & 1) * RC * H + (size_t)el * H;
             const float bias = a.router_b[e];
             if (!a.router_exact) {
-                router_logits_tokens(wrow, xh, H, gsel, split, nt, bias, lane, lg + e, lb + e, E);
+                router_logits_tokens(wrow, xh, H, gsel, split, nt, bias, lane, lg + e, lb + e, E, xnorm);
             } else {
                 for (int g = gsel; g < nt; g += split) {
                     const float l = (float)exact_logit(xh + (size_t)g * H, a.router_w, a.router_b, e, H, lane);
@@ -1024,14 +1040,25 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
         return cudaGetLastError();
     }
     static bool doneb = false, donep = false;
-    // ring depth: as many rows as keep two CTAs on an SM (one row per warp at most)
-    int RC = kRouteWarps;
-    while (RC > 1 && batch_smem(bp.H, bp.E, RC) > 110 * 1024) RC >>= 1;
-    const size_t smb = batch_smem(bp.H, bp.E, RC);
-    if (smb > 200 * 1024 || (size_t)kBatchTokens * bp.E * 8 > (size_t)2 * RC * bp.H * 2)
+    // Tokens per CTA: 4, with a ring as deep as keeps two CTAs on an SM (one
+    // row per warp at most); for batches that fill every SM with 8-token CTAs,
+    // 8 tokens and one CTA per SM, so that each staged router row serves twice
+    // the tokens.
+    int n_sm = 0, dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+    int TB = 4, RC = kRouteWarps;
+    size_t cap = 110 * 1024;
+    if ((T + kBatchTokensMax - 1) / kBatchTokensMax >= n_sm) {
+        TB = kBatchTokensMax;
+        cap = 220 * 1024;
+    }
+    while (RC > 1 && batch_smem(bp.H, bp.E, RC, TB) > cap) RC >>= 1;
+    const size_t smb = batch_smem(bp.H, bp.E, RC, TB);
+    if (smb > 224 * 1024 || (size_t)TB * bp.E * 8 > (size_t)2 * RC * bp.H * 2)
         return cudaErrorInvalidValue;  // the exact-logit scratch must fit in the ring
     MOE_CUDA_TRY(smem_optin_once(moe_route_batch_kernel, doneb));
-    moe_route_batch_kernel<<<(T + kBatchTokens - 1) / kBatchTokens, kRouteThreads, smb, st>>>(a, RC);
+    moe_route_batch_kernel<<<(T + TB - 1) / TB, kRouteThreads, smb, st>>>(a, RC, TB);
     MOE_CUDA_TRY(cudaGetLastError());
     MOE_CUDA_TRY(smem_optin_once(moe_permute_kernel, donep));
     moe_permute_kernel<<<1, 1024, perm_smem_bytes(bp.E + bp.n_shared, 32), st>>>(a);

@@ -65,7 +65,8 @@ def test_dequant_bitexact_workload_weights(cfg):
 
 
 # --------------------------------------------------------------------- routing
-@pytest.mark.parametrize("cfg,T", [(0, 1), (1, 8), (3, 128), (4, 40)])
+# 1300 / 1400 tokens: the large-batch routing configuration (8 tokens per CTA)
+@pytest.mark.parametrize("cfg,T", [(0, 1), (1, 8), (3, 128), (4, 40), (3, 1300), (4, 1400)])
 def test_routing_bitexact(cfg, T):
     blk = synth.make_block(cfg)
     x = synth.make_tokens(cfg, T, blk["shape"].hidden)
@@ -87,7 +88,8 @@ def test_router_exact_mode_gives_same_routes():
     np.testing.assert_allclose(a["route_w"], b["route_w"], rtol=2e-6)
 
 
-def test_routing_near_ties_are_resolved_exactly():
+@pytest.mark.parametrize("T", [33, 1300])
+def test_routing_near_ties_are_resolved_exactly(T):
     # two router rows identical except one tiny bf16 step: fp32 cannot order them
     # reliably, the certified path must fall back to exact logits
     shape = synth.tiny_shape(256, 64, 8, 2)
@@ -96,7 +98,7 @@ def test_routing_near_ties_are_resolved_exactly():
     blk["router_w"][1, 7] ^= 1
     blk["router_b"][:] = 0
     blk["router_b"][[0, 1]] = 5.0
-    x = synth.make_tokens(3, 33, 256)
+    x = synth.make_tokens(3, T, 256)
     r, _, _ = run_gpu(blk, x)
     ids, _, _ = oracle_routes(blk, x)
     assert np.array_equal(r["ids"], ids)
