@@ -794,11 +794,13 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
 constexpr int kBatchTokensMax = 8;  // tokens per CTA: 4 (two CTAs per SM) or, for large batches, 8
 
 __host__ __device__ inline size_t batch_rows_off(int H, int TB) { return (size_t)TB * H * 2; }
-__host__ __device__ inline size_t batch_lg_off(int H, int RC, int TB) {
-    return batch_rows_off(H, TB) + (size_t)2 * RC * H * 2;
+// ring slots: two (double buffer), or one when a single chunk holds every router row
+__host__ __device__ inline int batch_slots(int E, int RC) { return (E + RC - 1) / RC > 1 ? 2 : 1; }
+__host__ __device__ inline size_t batch_lg_off(int H, int E, int RC, int TB) {
+    return batch_rows_off(H, TB) + (size_t)batch_slots(E, RC) * RC * H * 2;
 }
 __host__ __device__ inline size_t batch_gm_off(int H, int E, int RC, int TB) {
-    return batch_lg_off(H, RC, TB) + (size_t)TB * E * 8;  // logits + bounds; exact logits reuse the ring
+    return batch_lg_off(H, E, RC, TB) + (size_t)TB * E * 8;  // logits + bounds; exact logits reuse the ring
 }
 __host__ __device__ inline size_t batch_smem(int H, int E, int RC, int TB) {
     return batch_gm_off(H, E, RC, TB) + (size_t)H * 4;
@@ -812,7 +814,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
     const int t0 = blockIdx.x * TB, nt = min(TB, a.T - t0);
     uint16_t *xh = reinterpret_cast<uint16_t *>(smem);                                  // [TB][H]
     uint16_t *ring = reinterpret_cast<uint16_t *>(smem + batch_rows_off(H, TB));        // [2][RC][H]
-    float *lg = reinterpret_cast<float *>(smem + batch_lg_off(H, RC, TB));              // [TB][E]
+    float *lg = reinterpret_cast<float *>(smem + batch_lg_off(H, E, RC, TB));           // [TB][E]
     float *lb = lg + TB * E;                                                            // [TB][E]
     double *exs = reinterpret_cast<double *>(ring);                                     // [TB][E] after the ring
     __shared__ __align__(8) uint64_t wbar[2];
@@ -903,8 +905,11 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
     __syncthreads();
     MOE_PHASE_MARK(1);
     // ------------------------------------------------------------------ router
-    const int split = kRouteWarps / RC;  // warps sharing one expert row
-    const int el = warp % RC, gsel = warp / RC;
+    // RC < 8: warps share a row (split of them, tokens gsel, gsel + split, ...);
+    // RC >= 8: each warp takes rows warp, warp + 8, ... for every token
+    const int split = RC >= kRouteWarps ? 1 : kRouteWarps / RC;
+    const int el0 = RC >= kRouteWarps ? warp : warp % RC, elstep = RC >= kRouteWarps ? kRouteWarps : RC;
+    const int gsel = RC >= kRouteWarps ? 0 : warp / RC;
     bool ok = true;
     for (int c = 0; c < nchunk; c++) {
         if (ok) {
@@ -926,6 +931,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
                 }
             }
         }
+        for (int el = el0; el < RC; el += elstep) {
         const int e = ((c + rot) % nchunk) * RC + el;
         if (ok && e < E) {
             const uint16_t *wrow = ring + (size_t)(c & 1) * RC * H + (size_t)el * H;
@@ -941,6 +947,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
                     }
                 }
             }
+        }
         }
         __syncthreads();  // ring slot c & 1 is free again
         if (tid == 0 && ok && c + 2 < nchunk) issue(c + 2);
@@ -1051,6 +1058,13 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
     size_t cap = 110 * 1024;
     if ((T + kBatchTokensMax - 1) / kBatchTokensMax >= n_sm) {
         TB = kBatchTokensMax;
+        cap = 220 * 1024;
+    }
+    const int rc_all = (bp.E + kRouteWarps - 1) / kRouteWarps * kRouteWarps;  // every row, whole warps
+    if (TB == 4 && batch_smem(bp.H, bp.E, rc_all, TB) <= 220 * 1024) {
+        // the whole router matrix fits beside the CTA's rows: one bulk round
+        // instead of a ring whose copy latency would be paid chunk by chunk
+        RC = rc_all;
         cap = 220 * 1024;
     }
     while (RC > 1 && batch_smem(bp.H, bp.E, RC, TB) > cap) RC >>= 1;
