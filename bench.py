@@ -62,8 +62,8 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def traffic_record(kernel: str):
-    """ncu DRAM bytes per launch of `kernel`, if taken on the current source."""
+def traffic_record(kernel: str, workload: str = ""):
+    """ncu DRAM bytes per launch of `kernel`, if taken on the current source and workload."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -72,6 +72,8 @@ def traffic_record(kernel: str):
         return None
     src = os.path.join(ROOT, rec["source"])
     if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["sha256"]:
+        return None
+    if rec.get("workload") and rec["workload"] != workload:
         return None
     return rec
 
@@ -282,7 +284,7 @@ def run_ours(args, rank, world, local):
     dom = max(range(4), key=lambda k: tot[k])
     dom_bytes = {1: gu_bytes, 2: dn_bytes}.get(dom, gu_bytes)
     achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9 if avg_ms[dom] > 0 else 0.0
-    tr = traffic_record(KERNEL_SLOTS[dom])
+    tr = traffic_record(KERNEL_SLOTS[dom], wl.name)
     path = sets[0]["plan"].path_for(TOKENS)  # 1 GEMV decode path, 2 tensor-core grouped GEMM
     step_bytes = gu_bytes + dn_bytes
     step_gbs = step_bytes / (ms / args.steps / 1e3) / 1e9

@@ -419,6 +419,9 @@ __host__ __device__ constexpr size_t perm_smem_bytes(int E, int warps = kRouteWa
 // prefix sums of counts and of tiles, stable scatter of (token, slot, weight),
 // the inverse map and the tile table.  Run by one CTA (any multiple of 32
 // threads) once every token's ids are in global memory.
+// CACHE: keep the first NTH routes' expert and weight in registers for the
+// scatter pass (the small-batch kernel: decode batches have no more routes)
+template <bool CACHE>
 __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NTH = blockDim.x, NW = NTH >> 5;
@@ -438,12 +441,18 @@ __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
         run[e] = 0;
     }
     __syncthreads();
+    // with CACHE, the first NTH routes' expert and weight stay in registers for
+    // the scatter pass, saving its round trips to L2
+    int e_first = -1;
+    float w_first = 0.f;
+    if (CACHE && tid < R) w_first = __ldcg(a.ws.route_w + tid);
     for (int r = tid; r < R; r += NTH) {
         int e = __ldcg(a.ws.ids + r);
         if ((unsigned)e >= (unsigned)E) {
             set_device_error(a.ws.status, MOE_DEV_BAD_ROUTE, r);
             e = 0;
         }
+        if (CACHE && r == tid) e_first = e;
         atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
@@ -477,8 +486,12 @@ __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
         const int r = base + tid;
         int e = -1;
         if (r < R) {
-            e = __ldcg(a.ws.ids + r);
-            if ((unsigned)e >= (unsigned)E) e = 0;
+            if (CACHE && base == 0) {
+                e = e_first;
+            } else {
+                e = __ldcg(a.ws.ids + r);
+                if ((unsigned)e >= (unsigned)E) e = 0;
+            }
         }
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int rank_w = __popc(peers & lt_mask);
@@ -491,7 +504,7 @@ __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
             const int t = r / K, s = r - t * K;
             a.ws.perm_token[pos] = t;
             a.ws.perm_slot[pos] = s;
-            a.ws.perm_w[pos] = __ldcg(a.ws.route_w + r);
+            a.ws.perm_w[pos] = (CACHE && base == 0) ? w_first : __ldcg(a.ws.route_w + r);
             a.ws.loc[t * KK + s] = pos;
         }
         __syncthreads();
@@ -781,7 +794,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     if (!s_flag) return;
     __threadfence();
     MOE_PHASE_MARK(6);
-    build_permutation(a, smem + rows_b);
+    build_permutation<true>(a, smem + rows_b);
     MOE_PHASE_MARK(7);
 }
 
@@ -965,7 +978,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArg
 // The permutation of a large batch, by one CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) moe_permute_kernel(RouteArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    build_permutation(a, smem);
+    build_permutation<false>(a, smem);
 }
 
 // Small-batch geometry: C CTAs per token (a cluster, C <= cmax), epc experts each.
