@@ -180,6 +180,26 @@ def cpu_baseline(blk, x):
             "sample": f"{n} tokens of one step (weight set 0), whole block per token, {el:.1f} s wall"}
 
 
+def cpu_baseline_stack(wl, x):
+    """The oracle through the whole stack (each layer's fp32 output cast to bf16
+    for the next), for as many of the step's tokens as there are cores."""
+    import oracle
+    from mxfp4_mixture_experts_rms_gb300 import synth
+    cores = os.cpu_count() or 1
+    n = min(x.shape[0], cores)
+    xs = x[:n]
+    el = 0.0
+    for l in range(wl.layers):
+        blk = synth.make_block(WORKLOAD, layer=l)
+        t0 = time.perf_counter()
+        out = oracle.moe_forward(blk, xs, nthreads=n)["out"]
+        el += time.perf_counter() - t0
+        xs = synth.f32_to_bf16_bits(out)
+        del blk
+    return {"value": n / el, "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "sample": f"{n} tokens through all {wl.layers} layers, {el:.1f} s of oracle time"}
+
+
 def run_ours(args, rank, world, local):
     import numpy as np
     import torch
@@ -193,7 +213,22 @@ def run_ours(args, rank, world, local):
     shape = wl.shape
     H, K = shape.hidden, shape.top_k
     sets = []
-    for s in range(args.sets):
+    if wl.layers > 1:
+        # a stack of independently seeded blocks: layer l's fp32 output, cast to
+        # bf16, is layer l+1's input; the stack itself (~10 GB) is far larger than L2
+        layers = []
+        for l in range(wl.layers):
+            blk = synth.make_block(WORKLOAD, layer=l + 100 * rank)
+            plan = moe.Plan(shape, max_tokens=TOKENS).alloc_workspace().load_weights(moe.DeviceBlock(blk))
+            layers.append(dict(plan=plan, x=torch.empty((TOKENS, H), dtype=torch.int16, device="cuda"),
+                               out=torch.empty((TOKENS, H), dtype=torch.float32, device="cuda"),
+                               ids=torch.empty((TOKENS, K), dtype=torch.int32, device="cuda")))
+            del blk
+        xb = synth.make_tokens(WORKLOAD, TOKENS, H, layer=100 * rank)
+        layers[0]["x"].copy_(torch.from_numpy(xb.view(np.int16)))
+        sets.append(dict(blk=None, xb=xb, plan=layers[0]["plan"], x=layers[0]["x"], out=layers[-1]["out"],
+                         ids=layers[-1]["ids"], layers=layers))
+    for s in range(args.sets if wl.layers == 1 else 0):
         layer = s + 100 * rank
         blk = synth.make_block(WORKLOAD, layer=layer)
         xb = synth.make_tokens(WORKLOAD, TOKENS, H, layer=layer)
@@ -203,9 +238,21 @@ def run_ours(args, rank, world, local):
         ids = torch.empty((TOKENS, K), dtype=torch.int32, device="cuda")
         sets.append(dict(blk=blk if s == 0 else None, xb=xb if s == 0 else None, plan=plan, x=x, out=out, ids=ids))
         del blk
+    def plans_of(d):
+        return [ly["plan"] for ly in d["layers"]] if "layers" in d else [d["plan"]]
+
+    def forward_set(d, stream):
+        if "layers" in d:
+            ls = d["layers"]
+            for l, ly in enumerate(ls):
+                ly["plan"].forward(ly["x"], ly["out"], ly["ids"], stream=stream)
+                if l + 1 < len(ls):
+                    moe.cast_f32_to_bf16(ly["out"], ls[l + 1]["x"], stream=stream)
+        else:
+            d["plan"].forward(d["x"], d["out"], d["ids"], stream=stream)
+
     def step(i, stream):
-        d = sets[i % len(sets)]
-        d["plan"].forward(d["x"], d["out"], d["ids"], stream=stream)
+        forward_set(sets[i % len(sets)], stream)
 
     def capture(n):
         """One CUDA graph holding n consecutive steps (launch overhead off the clock)."""
@@ -221,10 +268,14 @@ def run_ours(args, rank, world, local):
     facts = []
     for i, d in enumerate(sets):
         step(i, st)
-        c = torch.empty(shape.n_experts, dtype=torch.int32, device="cuda")
-        d["plan"].expert_counts(c)
-        torch.cuda.synchronize()
-        facts.append(algorithmic_bytes(shape, c.cpu().numpy(), TOKENS))
+        tot_f = [0, 0, 0]
+        for p in plans_of(d):
+            c = torch.empty(shape.n_experts, dtype=torch.int32, device="cuda")
+            p.expert_counts(c)
+            torch.cuda.synchronize()
+            tot_f = [a + b for a, b in zip(tot_f, algorithmic_bytes(shape, c.cpu().numpy(), TOKENS))]
+        facts.append(tuple(tot_f))
+    n_blocks = len(plans_of(sets[0]))  # blocks per step (the stack's layers)
     for i in range(args.warmup):
         step(i, st)
     torch.cuda.synchronize()
@@ -262,7 +313,8 @@ def run_ours(args, rank, world, local):
     # ---- kernel durations over the same K steps: CUDA events the library
     # records around each launch (captured into the graph as event nodes)
     for d in sets:
-        d["plan"].set_i("profile", 1)
+        for p in plans_of(d):
+            p.set_i("profile", 1)
     pgraph = capture(args.steps)
     torch.cuda.synchronize()
     pgraph.replay()
@@ -270,26 +322,28 @@ def run_ours(args, rank, world, local):
     tot = [0.0] * 4
     cnt = [0] * 4
     for d in sets:
-        m, c = d["plan"].profile_read()
-        tot = [a + b for a, b in zip(tot, m)]
-        cnt = [a + b for a, b in zip(cnt, c)]
-        d["plan"].set_i("profile", 0)
+        for p in plans_of(d):
+            m, c = p.profile_read()
+            tot = [a + b for a, b in zip(tot, m)]
+            cnt = [a + b for a, b in zip(cnt, c)]
+            p.set_i("profile", 0)
     del pgraph
     avg_ms = [t / c if c else 0.0 for t, c in zip(tot, cnt)]
     share = [t / sum(tot) for t in tot] if sum(tot) > 0 else [0.0] * 4
-    gu_bytes = sum(facts[i % len(sets)][0] for i in range(args.steps)) / args.steps
-    dn_bytes = sum(facts[i % len(sets)][1] for i in range(args.steps)) / args.steps
-    distinct = sum(facts[i % len(sets)][2] for i in range(args.steps)) / args.steps
+    # per launch of each kernel (a step launches each once per block)
+    gu_bytes = sum(facts[i % len(sets)][0] for i in range(args.steps)) / args.steps / n_blocks
+    dn_bytes = sum(facts[i % len(sets)][1] for i in range(args.steps)) / args.steps / n_blocks
+    distinct = sum(facts[i % len(sets)][2] for i in range(args.steps)) / args.steps / n_blocks
     hbm, bf16_peak, peak_kind = peaks()
     dom = max(range(4), key=lambda k: tot[k])
     dom_bytes = {1: gu_bytes, 2: dn_bytes}.get(dom, gu_bytes)
     achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9 if avg_ms[dom] > 0 else 0.0
     tr = traffic_record(KERNEL_SLOTS[dom], wl.name)
     path = sets[0]["plan"].path_for(TOKENS)  # 1 GEMV decode path, 2 tensor-core grouped GEMM
-    step_bytes = gu_bytes + dn_bytes
+    step_bytes = (gu_bytes + dn_bytes) * n_blocks
     step_gbs = step_bytes / (ms / args.steps / 1e3) / 1e9
     routes = TOKENS * (K + shape.n_shared)
-    step_flops = 6.0 * routes * H * shape.expert_hidden
+    step_flops = 6.0 * routes * H * shape.expert_hidden * n_blocks
     step_tflops = step_flops / (ms / args.steps / 1e3) / 1e12
 
     # ---- end to end through the public API with host buffers
@@ -301,7 +355,7 @@ def run_ours(args, rank, world, local):
         j = i % len(sets)
         d = sets[j]
         d["x"].copy_(hx[j], non_blocking=True)
-        d["plan"].forward(d["x"], d["out"], d["ids"], stream=st)
+        forward_set(d, st)
         hout[j].copy_(d["out"], non_blocking=True)
         hids[j].copy_(d["ids"], non_blocking=True)
 
@@ -326,15 +380,18 @@ def run_ours(args, rank, world, local):
         return
     cpu = None
     if not args.no_cpu_baseline and world >= 1:
-        cpu = cpu_baseline(sets[0]["blk"], sets[0]["xb"])
+        cpu = (cpu_baseline_stack(wl, sets[0]["xb"]) if n_blocks > 1
+               else cpu_baseline(sets[0]["blk"], sets[0]["xb"]))
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "tokens_per_step": TOKENS, "hidden": H, "n_experts": shape.n_experts,
                    "top_k": K, "expert_hidden": shape.expert_hidden, "weights": "mxfp4 (e2m1 + e8m0/32)",
-                   "weight_sets": len(sets), "l2": "inputs larger than L2: steps rotate over independently "
-                   "seeded weight sets", "distinct_experts_per_step": distinct,
+                   "weight_sets": len(sets), "layers": n_blocks,
+                   "l2": ("inputs larger than L2: a stack of independently seeded layers" if n_blocks > 1 else
+                          "inputs larger than L2: steps rotate over independently seeded weight sets"),
+                   "distinct_experts_per_block": distinct,
                    "algorithmic_bytes_per_step": step_bytes, "step_hbm_gbs": step_gbs,
                    "algorithmic_flops_per_step": step_flops, "step_tflops": step_tflops,
                    "step_tensor_frac_of_bf16_peak": step_tflops / peaks()[1],
@@ -343,7 +400,7 @@ def run_ours(args, rank, world, local):
                              routes, H, shape.expert_hidden, TOKENS * shape.n_experts * H),
         "kernels": {KERNEL_SLOTS[k]: {"avg_us": 1e3 * avg_ms[k], "share": share[k], "launches": cnt[k]}
                     for k in range(4)},
-        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": int(sum(cnt)),
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": int(sum(cnt)) + (n_blocks - 1) * args.steps,  # + the stack's casts between layers
     }
     print(json.dumps(line), flush=True)
 

@@ -175,6 +175,13 @@ int moe_get_device_status(moe_plan *plan, int *status, void *stream);
 int moe_forward_noalloc(moe_plan *plan, const uint16_t *x, int tokens, float *out,
                         int32_t *route_ids_out, void *stream);
 
+/* dst[i] = src[i] rounded to bf16 (nearest, ties to even), i < n, enqueued on
+ * `stream`: the residual stream between stacked blocks (a block's fp32 output
+ * becomes the next block's bf16 input).  src fp32 and dst uint16 are device
+ * pointers, 16-byte aligned, not overlapping.  NaN inputs give a quiet NaN.
+ * MOE_EINVAL on NULL/misaligned pointers, MOE_ECUDA on a launch error. */
+int moe_cast_f32_to_bf16(const float *src, uint16_t *dst, size_t n, void *stream);
+
 /* Text of the last failure on this thread ("" if none). */
 const char *moe_last_error(void);
 

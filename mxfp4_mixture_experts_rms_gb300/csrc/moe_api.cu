@@ -526,6 +526,16 @@ int noalloc_scratch(void **out) {
 }
 }  // namespace
 
+int moe_cast_f32_to_bf16(const float *src, uint16_t *dst, size_t n, void *stream) {
+    if (n == 0) return MOE_OK;
+    if (!src || !dst) return fail(MOE_EINVAL, "NULL src or dst");
+    if (!aligned16(src) || !aligned16(dst)) return fail(MOE_EINVAL, "src and dst must be 16-byte aligned");
+    const char *sb = reinterpret_cast<const char *>(src), *db = reinterpret_cast<const char *>(dst);
+    if (sb < db + n * 2 && db < sb + n * 4) return fail(MOE_EINVAL, "src and dst must not overlap");
+    const cudaError_t e = launch_cast_bf16(src, dst, n, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_cast_f32_to_bf16");
+}
+
 int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, int32_t *ids_out, void *stream) {
     if (!p) return fail(MOE_EINVAL, "NULL plan");
     if (tokens < 0) return fail(MOE_EINVAL, "tokens must be >= 0");

@@ -24,7 +24,7 @@ EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_plan_set_i", "moe_plan_se
            "moe_workspace_bytes",
            "moe_set_workspace", "moe_load_weights", "moe_forward", "moe_forward_ex", "moe_get_expert_counts",
            "moe_get_permutation", "moe_debug_dequant", "moe_profile_read", "moe_get_device_status",
-           "moe_forward_noalloc", "moe_last_error"]
+           "moe_forward_noalloc", "moe_cast_f32_to_bf16", "moe_last_error"]
 
 
 class MoeError(RuntimeError):
@@ -77,6 +77,7 @@ def load(build_if_missing: bool = True):
     L.moe_get_device_status.argtypes = [P, C.POINTER(I), P]
     L.moe_profile_read.argtypes = [P, C.POINTER(C.c_double), C.POINTER(I), I]
     L.moe_forward_noalloc.argtypes = [P, P, I, P, P, P]
+    L.moe_cast_f32_to_bf16.argtypes = [P, P, SZ, P]
     L.moe_last_error.restype = C.c_char_p
     L.moe_last_error.argtypes = []
     for name in EXPORTS:
@@ -102,6 +103,13 @@ def _stream_ptr(stream):
         import torch
         stream = torch.cuda.current_stream()
     return C.c_void_p(stream.cuda_stream)
+
+
+def cast_f32_to_bf16(src, dst, stream=None):
+    """dst (int16/uint16 bits, device) = bf16_rne(src (float32, device)); enqueued on `stream`."""
+    assert src.numel() == dst.numel()
+    _check(load().moe_cast_f32_to_bf16(C.c_void_p(_ptr(src)), C.c_void_p(_ptr(dst)), int(src.numel()),
+                                       _stream_ptr(stream)))
 
 
 class DeviceBlock:

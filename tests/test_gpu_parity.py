@@ -222,3 +222,59 @@ def test_grouped_gemm_fp16_and_bf16_variants(elo, ehi):
     assert r["status"] == 0
     assert np.array_equal(r["ids"], ref["ids"])
     check_close(r["out"], ref["out"], x)
+
+
+# ------------------------------------------------------------ stacked blocks
+def test_cast_f32_to_bf16_matches_round_to_nearest_even():
+    import torch
+    rng = np.random.default_rng(11)
+    v = rng.normal(0, 3, 4099).astype(np.float32)
+    # exact halfway cases (ties to even), both parities, signs, large and tiny values
+    v[:8] = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 3.0e38, -3.0e38, 1e-40, -1e-40, 0.0], np.float32)
+    src = torch.from_numpy(v).cuda()
+    dst = torch.empty(v.size, dtype=torch.int16, device="cuda")
+    moe.cast_f32_to_bf16(src, dst)
+    got = dst.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, synth.f32_to_bf16_bits(v))
+    nan = torch.full((5,), float("nan"), device="cuda")
+    out = torch.empty(5, dtype=torch.int16, device="cuda")
+    moe.cast_f32_to_bf16(nan, out)
+    b = out.cpu().numpy().view(np.uint16)
+    assert np.all((b & 0x7F80) == 0x7F80) and np.all(b & 0x7F)
+
+
+def test_stacked_blocks_residual_chain():
+    """Config 2's chain: layer l's fp32 output, cast to bf16, is layer l+1's
+    input.  Each layer is checked against the oracle fed the GPU's own input
+    (teacher-forced), and the last output against the oracle's own chain."""
+    import torch
+    cfg, T, n_layers = 2, 4, 4
+    shape = synth.WORKLOADS[cfg].shape
+    H = shape.hidden
+    x0 = synth.make_tokens(cfg, T, H)
+    x = torch.from_numpy(x0.view(np.int16)).cuda()
+    xr = x0
+    for layer in range(n_layers):
+        blk = synth.make_block(cfg, layer=layer)
+        plan = moe.Plan(shape, max_tokens=T).alloc_workspace().load_weights(moe.DeviceBlock(blk))
+        out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        plan.forward(x, out)
+        torch.cuda.synchronize()
+        xin = x.cpu().numpy().view(np.uint16)
+        ref = oracle.moe_forward(blk, xin, nthreads=NTHREADS)
+        check_close(out.cpu().numpy(), ref["out"], xin, what="layer %d (teacher-forced)" % layer)
+        xr = synth.f32_to_bf16_bits(oracle.moe_forward(blk, xr, nthreads=NTHREADS)["out"])
+        nxt = torch.empty((T, H), dtype=torch.int16, device="cuda")
+        moe.cast_f32_to_bf16(out, nxt)
+        x = nxt
+        plan.close()
+    torch.cuda.synchronize()
+    got = x.cpu().numpy().view(np.uint16)
+    # end to end: each layer adds its own rounding differences (within the
+    # per-block 1e-3) on top of what it inherits, so the chains may drift apart
+    # by up to about n_layers x 1e-3; a route chosen differently would show up
+    # as an error orders of magnitude larger
+    g = (got.astype(np.uint32) << 16).view(np.float32)
+    r = (xr.astype(np.uint32) << 16).view(np.float32)
+    rel = np.linalg.norm(g - r) / np.linalg.norm(r)
+    assert rel < n_layers * 1e-3, rel
