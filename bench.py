@@ -157,6 +157,25 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ our arm
+def max_over_ranks(x: float) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's);
+    x itself when there is no process group or a single rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, tokens: int, steps: int, ms: float) -> float:
+    """Tokens per second of the whole job: every rank processes `tokens` per step
+    (weak scaling), the job takes the slowest rank's `ms` for `steps` steps."""
+    return world * tokens * steps / (ms / 1e3)
+
+
 def algorithmic_bytes(shape, counts, T):
     """Bytes the gate/up and down kernels must move at least once per launch."""
     H, F = shape.hidden, shape.expert_hidden
@@ -299,11 +318,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * TOKENS * args.steps / (ms / 1e3)
+    ms = max_over_ranks(ms)
+    value = whole_job_rate(world, TOKENS, args.steps, ms)
     if args.quick:
         if rank == 0:
             print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "ms_per_step": ms / args.steps,
@@ -368,12 +384,8 @@ def run_ours(args, rank, world, local):
         e2e_step(i)
     e1.record(st)
     torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e = {"value": world * TOKENS * args.steps / (e_ms / 1e3), "unit": "tokens/s",
+    e_ms = max_over_ranks(e0.elapsed_time(e1))
+    e2e = {"value": whole_job_rate(world, TOKENS, args.steps, e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": TOKENS * H * 2, "d2h_bytes_per_step": TOKENS * H * 4 + TOKENS * K * 4}
 
     if rank != 0:
