@@ -619,33 +619,6 @@ cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, cons
     return nt == 1 ? launch_bf<false, 1, 1>(dn, h_bf16, items, st) : launch_bf<false, 2, 1>(dn, h_bf16, items, st);
 }
 
-namespace {
-// four elements per thread (one 16-byte load, one 8-byte store), the tail element-wise
-__global__ void __launch_bounds__(256) moe_cast_bf16_kernel(const float *src, uint16_t *dst, size_t n) {
-    const size_t n4 = n / 4;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-        const float4 v = reinterpret_cast<const float4 *>(src)[i];
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-        reinterpret_cast<uint2 *>(dst)[i] =
-            make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
-    }
-    const size_t t = 4 * n4 + (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t < n) {
-        const __nv_bfloat16 b = __float2bfloat16_rn(src[t]);
-        dst[t] = *reinterpret_cast<const uint16_t *>(&b);
-    }
-}
-}  // namespace
-
-cudaError_t launch_cast_bf16(const float *src, uint16_t *dst, size_t n, cudaStream_t st) {
-    const size_t n4 = n / 4;
-    size_t blocks = (n4 + 255) / 256;
-    if (blocks < 1) blocks = 1;
-    if (blocks > 4096) blocks = 4096;
-    moe_cast_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, dst, n);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T, float *out,
                            cudaStream_t st) {
     dim3 grid((bp.H / 4 + 255) / 256, T);
