@@ -62,20 +62,21 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def traffic_record(kernel: str, workload: str = ""):
-    """ncu DRAM bytes per launch of `kernel`, if taken on the current source and workload."""
+def traffic_record(kernel: str, workload: str = "", tokens: int = 0):
+    """ncu DRAM bytes per launch of `kernel`, if taken on the current source, on
+    this workload and token count."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    rec = json.load(open(p)).get(kernel)
-    if not rec:
-        return None
-    src = os.path.join(ROOT, rec["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["sha256"]:
-        return None
-    if rec.get("workload") and rec["workload"] != workload:
-        return None
-    return rec
+    recs = json.load(open(p)).get(kernel) or []
+    for rec in recs if isinstance(recs, list) else [recs]:
+        src = os.path.join(ROOT, rec["source"])
+        if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["sha256"]:
+            continue
+        if rec.get("workload", workload) != workload or rec.get("tokens", tokens) != tokens:
+            continue
+        return rec
+    return None
 
 
 class Clocks:
@@ -395,7 +396,7 @@ def run_ours(args, rank, world, local):
     dom = max(range(4), key=lambda k: tot[k])
     dom_bytes = {1: gu_bytes, 2: dn_bytes}.get(dom, gu_bytes)
     achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9 if avg_ms[dom] > 0 else 0.0
-    tr = traffic_record(KERNEL_SLOTS[dom], wl.name)
+    tr = traffic_record(KERNEL_SLOTS[dom], wl.name, TOKENS)
     path = sets[0]["plan"].path_for(TOKENS)  # 1 GEMV decode path, 2 tensor-core grouped GEMM
     step_bytes = (gu_bytes + dn_bytes) * n_blocks
     step_gbs = step_bytes / (ms / args.steps / 1e3) / 1e9
@@ -471,7 +472,8 @@ def roofline(path, dom, avg_ms, achieved_gbs, hbm, bf16_peak, peak_kind, tr, dom
         flops = 2.0 * routes * (2 * F if dom == 1 else F) * H
         ach = flops / (avg_ms / 1e3) / 1e12 if avg_ms > 0 else 0.0
         return {"bound": "tensor", "kernel": KERNEL_SLOTS[dom], "achieved": ach, "peak": bf16_peak,
-                "peak_kind": peak_kind, "unit": "TFLOP/s", "frac": ach / bf16_peak, "traffic": None,
+                "peak_kind": peak_kind, "unit": "TFLOP/s", "frac": ach / bf16_peak,
+                "traffic": tr["bytes_per_launch"] if tr else None,
                 "algorithmic_flops_per_launch": flops, "avg_launch_ms": avg_ms}
     if path == 2 and dom == 0:
         flops = 2.0 * router_macs
