@@ -78,6 +78,8 @@ def lib():
         L.oracle_expert_ffn.argtypes = [C.POINTER(Expert), C.c_int64, C.c_int64, P, C.c_double,
                                         C.c_double, P, P, P]
         L.oracle_permutation.argtypes = [P, C.c_int64, C.c_int32, C.c_int32, P, P, P, P, P]
+        L.oracle_mx_fp4_quantize.restype = C.c_int
+        L.oracle_mx_fp4_quantize.argtypes = [P, C.c_int64, C.c_int64, P, P]
         L.oracle_moe_forward.restype = C.c_int
         L.oracle_moe_forward.argtypes = [C.POINTER(Cfg), C.POINTER(Weights), P, C.c_int64, P, P,
                                          P, P, P, C.c_int]
@@ -124,6 +126,18 @@ def mxfp4_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     out = np.empty((rows, cols), np.float64)
     lib().oracle_mxfp4_dequant(_p(codes), _p(scales), rows, cols, _p(out))
     return out
+
+
+def mx_fp4_quantize(x: np.ndarray):
+    """float32 [rows][cols] (cols % 32 == 0) -> (codes uint8 [rows][cols/2],
+    E8M0 scales uint8 [rows][cols/32]): the FP4 activation encoding."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows, cols // 32), np.uint8)
+    if lib().oracle_mx_fp4_quantize(_p(x), rows, cols, _p(codes), _p(scales)) != 0:
+        raise ValueError("oracle_mx_fp4_quantize: bad arguments")
+    return codes, scales
 
 
 def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float):

@@ -11,6 +11,7 @@
  *                  `mixture_of_experts_batch`; `mix_expert_outputs`;
  *                  `top_experts`; tensor validation of the expert tensors)
  *   [ds4.c]       antirez ds4, ds4.c (`dsv4_e2m1fn_value_cpu`;
+ *                 `dsv4_e2m1fn_dequant_cpu`; `dsv4_fp4_act_quantize_row_inplace_cpu`;
  *                 `rms_norm_weight`; `DS4_SHAPE_FLASH` profile)
  *   [gptoss/mod]  turbospark-runtime 0.3.0, src/families/gptoss/mod.rs
  *                 (module doc comment: the per-layer formula)
@@ -55,6 +56,71 @@ void oracle_mxfp4_dequant(const uint8_t *codes, const uint8_t *scales, int64_t r
     for (int64_t r = 0; r < rows; r++)
         for (int64_t c = 0; c < cols; c++)
             out[r * cols + c] = oracle_mxfp4_element(codes, scales, cols, r, c);
+}
+
+/* [ds4.c] dsv4_e2m1fn_dequant_cpu: the index of the E2M1 magnitude nearest to
+ * |v| (|v| above 6, or NaN, is taken as 6), scanning the table upward and
+ * letting an equally near entry replace the current best only when it has an
+ * even index and the best so far has an odd one (ties to even). */
+static int e2m1_nearest_index(double av) {
+    if (!(av <= 6.0)) av = 6.0;
+    int best = 0;
+    double best_d = fabs(av - oracle_e2m1_value(0));
+    for (int i = 1; i < 8; i++) {
+        const double d = fabs(av - oracle_e2m1_value(i));
+        if (d < best_d || (d == best_d && (i & 1) == 0 && (best & 1) == 1)) {
+            best = i;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+/* [ds4.c] dsv4_fp4_act_quantize_row_inplace_cpu, returning the codes and the
+ * block exponents instead of the round-tripped floats.  The page takes the
+ * exponent as ceilf(log2f(amax / 6)); it is taken here exactly from q's
+ * binary exponent (frexp), the plain meaning of ceil(log2 q) for every float
+ * q, with no dependence on how a log2 routine rounds near powers of two. */
+int oracle_mx_fp4_quantize(const float *x, int64_t rows, int64_t cols, uint8_t *codes,
+                           uint8_t *scales) {
+    if (!x || !codes || !scales || rows < 0 || cols <= 0 || cols % 32 != 0) return -1;
+    const float amax_floor = 7.052966104933725e-38f; /* 6 * 2^-126: keeps q a normal float */
+    const int64_t nblk = cols / 32;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t b = 0; b < nblk; b++) {
+            const float *xb = x + r * cols + 32 * b;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; i++) {
+                const float a = fabsf(xb[i]);
+                if (a > amax) amax = a; /* false for NaN */
+            }
+            if (amax < amax_floor) amax = amax_floor;
+            const float q = amax / 6.0f; /* one float rounding */
+            int k;
+            if (isinf(q)) {
+                k = 127;
+            } else {
+                int ex;
+                const float m = frexpf(q, &ex); /* q = m * 2^ex, m in [0.5, 1) */
+                k = (m == 0.5f) ? ex - 1 : ex;
+            }
+            if (k > 127) k = 127;
+            scales[r * nblk + b] = (uint8_t)(k + 127);
+            const double scale = ldexp(1.0, k);
+            for (int i = 0; i < 32; i++) {
+                double v = (double)xb[i] / scale; /* exact: a power-of-two division in double */
+                if (v > 6.0) v = 6.0;
+                if (v < -6.0) v = -6.0;
+                const int nib = ((xb[i] < 0.0f) ? 8 : 0) | e2m1_nearest_index(fabs(v));
+                uint8_t *byte = codes + r * (cols / 2) + 16 * b + i / 2;
+                if (i & 1)
+                    *byte = (uint8_t)((*byte & 0x0F) | (nib << 4));
+                else
+                    *byte = (uint8_t)((*byte & 0xF0) | nib);
+            }
+        }
+    }
+    return 0;
 }
 
 /* bf16: 1 sign, 8 exponent, 7 fraction bits.  One rounding from double:

@@ -75,6 +75,23 @@ double oracle_mxfp4_element(const uint8_t *codes, const uint8_t *scales, int64_t
 void oracle_mxfp4_dequant(const uint8_t *codes, const uint8_t *scales, int64_t rows,
                           int64_t cols, double *out);
 
+/* MX FP4 encoding of activations in 32-element blocks along each row
+ * ([ds4.c] FP4 activation quantisation `dsv4_fp4_act_quantize_row_inplace_cpu`
+ * with its nearest-E2M1 step `dsv4_e2m1fn_dequant_cpu`).  Per block:
+ *   amax  = max |x_i| (NaN elements never raise it), at least 6 * 2^-126;
+ *   q     = amax / 6 rounded once to float;
+ *   k     = ceil(log2 q), taken exactly (q is a power of two -> its exponent);
+ *           k = 127 when q is infinite;
+ *   v_i   = x_i / 2^k clamped to [-6, 6]; NaN -> +6;
+ *   code  = nearest E2M1 magnitude index, ties to the even index, sign bit
+ *           set when x_i < 0 (so -0 and NaN encode as positive).
+ * x float [rows][cols], cols % 32 == 0 -> codes [rows][cols/2] (element 2i in
+ * the low nibble) and E8M0 scales [rows][cols/32] = k + 127, the canonical
+ * weight layout; decoding them gives the page's round-tripped values.
+ * Returns 0, or -1 on bad arguments. */
+int oracle_mx_fp4_quantize(const float *x, int64_t rows, int64_t cols, uint8_t *codes,
+                           uint8_t *scales);
+
 /* Round a double to bf16 (nearest, ties to even; one rounding); bf16 -> double. */
 uint16_t oracle_bf16_rne(double v);
 double oracle_bf16_to_double(uint16_t b);

@@ -425,3 +425,105 @@ def test_golden_constants_match_workload_shapes():
     shapes = {"gpt-oss": synth.GPT_OSS, "dsv4-flash": synth.DSV4_FLASH_SHAPE}
     for (name, key), v in want.items():
         assert float(getattr(shapes[name], key)) == v, (name, key)
+
+
+# ------------------------------------------------ FP4 activation encoding
+# ds4.c, FP4 activation quantisation: per 32-element block the scale is the
+# power of two 2^ceil(log2(amax / 6)) and each element is the nearest E2M1
+# value (ties to even) of x / scale, clamped to +-6.
+
+def _mx_blocks(rng, rows, cols, lo=-130, hi=120):
+    """float32 rows whose 32-element blocks each have their own magnitude."""
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    e = rng.integers(lo, hi, size=(rows, cols // 32))
+    return (x * np.repeat(np.exp2(e.astype(np.float64)), 32, axis=1)).astype(np.float32)
+
+
+def test_mx_fp4_scale_is_the_smallest_power_of_two_covering_amax_over_6():
+    rng = np.random.default_rng(11)
+    x = _mx_blocks(rng, 64, 256)
+    x[0, :32] = 0.0                       # all-zero block: the 6 * 2^-126 floor
+    x[1, :32] = np.float32(6.0)           # q = 1 exactly
+    x[2, 32:64] = np.float32(3.0) * np.float32(2.0) ** 20   # q a power of two
+    _, sc = oracle.mx_fp4_quantize(x)
+    amax = np.abs(x).reshape(64, 8, 32).max(axis=2)
+    amax = np.maximum(amax, np.float32(6.0 * 2.0 ** -126))
+    q = (amax / np.float32(6.0)).astype(np.float32)      # one float32 rounding
+    k = sc.astype(np.int64) - 127
+    for qi, ki in zip(q.ravel(), k.ravel()):
+        assert math.ldexp(1.0, int(ki) - 1) < float(qi) <= math.ldexp(1.0, int(ki))
+        lg = math.log2(float(qi))
+        if abs(lg - round(lg)) > 1e-4:
+            assert ki == math.ceil(lg)
+    assert sc[0, 0] == 1 and sc[1, 0] == 127 and sc[2, 1] == 127 + 19
+
+
+def _decode(codes, scales):
+    return oracle.mxfp4_dequant(codes, scales)
+
+
+def test_mx_fp4_codes_are_the_nearest_values_with_ties_to_even():
+    rng = np.random.default_rng(12)
+    x = _mx_blocks(rng, 32, 128, -20, 20)
+    # every tie of the E2M1 grid (midpoints) and the grid itself, scale 2^0
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1.0, 1.5, 2, 3, 4, 6], np.float32)
+    x[0, :14], x[0, 14:28] = mids, -mids
+    x[0, 28:32] = [6.0, 0.1, -0.2, 5.9]
+    codes, sc = oracle.mx_fp4_quantize(x)
+    nib = np.stack([codes & 15, codes >> 4], axis=2).reshape(x.shape).astype(np.int64)
+    k = np.repeat(sc.astype(np.int64) - 127, 32, axis=1)
+    cand_mag = np.array(TABLE)
+    for (r, c), xv in np.ndenumerate(x):
+        s = math.ldexp(1.0, int(k[r, c]))
+        xc = min(max(float(xv), -6 * s), 6 * s)
+        cands = np.concatenate([cand_mag, -cand_mag]) * s
+        dist = np.abs(cands - xc)
+        got = TABLE[nib[r, c] & 7] * s * (-1.0 if nib[r, c] & 8 else 1.0)
+        assert abs(got - xc) == dist.min(), (r, c, xv)
+        ties = {i % 8 for i in np.flatnonzero(dist == dist.min())}
+        if len(ties) > 1:
+            assert (nib[r, c] & 7) % 2 == 0, (r, c, xv)
+        assert bool(nib[r, c] & 8) == bool(xv < 0)
+
+
+def test_mx_fp4_worked_cases():
+    x = np.zeros((4, 32), np.float32)
+    x[0, :12] = [0.5, 6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -5, -0.0, -1e-30]
+    x[1, :2] = [12.0, -1.0]               # q = 2 -> k = 1
+    x[2, :2] = [np.nan, 1.0]              # NaN ignored by amax, encoded +6
+    x[3, :3] = [-np.inf, 1.0, 2.0 ** 120]
+    codes, sc = oracle.mx_fp4_quantize(x)
+    # scale 2^0: 0.5|6 -> 0x71, 0.25->0 | 0.75->1.0 -> 0x20, 1.25->1.0 | 1.75->2.0 -> 0x42,
+    # 2.5->2.0 | 3.5->4.0 -> 0x64, 5->4.0 | -5->-4.0 -> 0xE6, -0.0 -> +0 | -1e-30 -> -0 -> 0x80
+    assert sc[0, 0] == 127
+    assert codes[0, :8].tolist() == [0x71, 0x20, 0x42, 0x64, 0xE6, 0x80, 0, 0]
+    # 12 / 2 = 6 -> 7; -1 / 2 = -0.5 -> sign | 1
+    assert sc[1, 0] == 128 and codes[1, 0] == 0x97
+    # amax 1: q = 1/6 -> k = -2 (scale 2^-2); NaN -> +6 (7), 1 / 0.25 = 4 -> 6
+    assert sc[2, 0] == 125 and codes[2, 0] == 0x67
+    # an infinite element saturates the exponent at 127: -inf -> -6, the rest -> 0
+    assert sc[3, 0] == 254 and codes[3, 0] == 0x0F and codes[3, 1] == 0
+    with pytest.raises(ValueError):
+        oracle.mx_fp4_quantize(np.zeros((1, 48), np.float32))
+
+
+def test_mx_fp4_round_trip_is_idempotent_and_within_half_a_step():
+    rng = np.random.default_rng(13)
+    x = _mx_blocks(rng, 48, 320, -60, 60)
+    y = _decode(*oracle.mx_fp4_quantize(x))
+    y2 = _decode(*oracle.mx_fp4_quantize(y.astype(np.float32)))
+    np.testing.assert_array_equal(y2, y)
+    _, sc = oracle.mx_fp4_quantize(x)
+    s = np.exp2(np.repeat(sc.astype(np.float64) - 127, 32, axis=1))
+    v = np.abs(x.astype(np.float64)) / s
+    half_step = np.where(v < 2, 0.25, np.where(v < 4, 0.5, 1.0)) * s
+    assert np.all(np.abs(x - y) <= half_step)
+
+
+def test_mx_fp4_is_monotone_within_a_block():
+    rng = np.random.default_rng(14)
+    for _ in range(50):
+        b = np.sort(rng.uniform(-7.0, 7.0, 32)).astype(np.float32)
+        b[0], b[-1] = -7.5, 7.5          # fixed amax: one scale for the block
+        y = _decode(*oracle.mx_fp4_quantize(b[None, :]))[0]
+        assert np.all(np.diff(y) >= 0)
