@@ -44,6 +44,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only (no clock pre-roll, kernel timing, e2e or CPU baseline); for ncu")
+    ap.add_argument("--op", default="block", choices=["block", "mx_fp4_quantize"],
+                    help="block: the MoE block (the benchmark); mx_fp4_quantize: the FP4 activation "
+                         "encoder alone, on --rows x --cols bf16 activations")
+    ap.add_argument("--rows", type=int, default=14336, help="mx_fp4_quantize: rows (2048 tokens x 7 routes)")
+    ap.add_argument("--cols", type=int, default=2048, help="mx_fp4_quantize: columns (expert_hidden)")
     return ap.parse_args()
 
 
@@ -488,8 +493,64 @@ def roofline(path, dom, avg_ms, achieved_gbs, hbm, bf16_peak, peak_kind, tr, dom
             "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": avg_ms}
 
 
+def run_mx_fp4_quantize(args):
+    """The FP4 activation encoder alone: bf16 [rows][cols] -> MXFP4 codes + E8M0
+    scales, timed with CUDA events on the launching stream over input sets that
+    together exceed twice the L2, so every launch reads from HBM."""
+    import numpy as np
+    import torch
+    from mxfp4_mixture_experts_rms_gb300 import moe
+    moe.load()
+    R, Cc = args.rows, args.cols
+    n = R * Cc
+    algo = n * 2 + n // 2 + n // 32
+    n_sets = max(2, -(-2 * 129 * 2 ** 20 // algo) + 1)
+    g = torch.Generator(device="cuda").manual_seed(0x4D6F45)
+    xs = [(torch.randn((R, Cc), device="cuda", generator=g) * 4).to(torch.bfloat16).view(torch.int16)
+          for _ in range(n_sets)]
+    codes = [torch.empty(n // 2, dtype=torch.uint8, device="cuda") for _ in range(n_sets)]
+    scales = [torch.empty(n // 32, dtype=torch.uint8, device="cuda") for _ in range(n_sets)]
+    st = torch.cuda.current_stream()
+    for i in range(max(3, args.warmup)):
+        moe.mx_quantize_fp4(xs[i % n_sets], codes[i % n_sets], scales[i % n_sets], st)
+    torch.cuda.synchronize()
+    clk = Clocks(torch.cuda.current_device())
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < 1.0:   # clocks settle under load before the timed region
+        for i in range(n_sets):
+            moe.mx_quantize_fp4(xs[i], codes[i], scales[i], st)
+        torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for i in range(args.steps):
+        moe.mx_quantize_fp4(xs[i % n_sets], codes[i % n_sets], scales[i % n_sets], st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    hbm, _, peak_kind = peaks()
+    gbs = algo / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "op": "mx_fp4_quantize", "metric": "FP4 activation encoding bandwidth", "value": gbs, "unit": "GB/s",
+        "higher_is_better": True, "steps": args.steps, "ms_per_launch": ms, "dtype": "bf16->fp4",
+        "data": "synthetic", "gpu_launches": args.steps, "clocks": clocks,
+        "config": {"workload": f"FP4 activation encoding, {R} x {Cc} bf16", "rows": R, "cols": Cc,
+                   "l2": f"{n_sets} input sets rotated, {n_sets * algo / 1e6:.0f} MB > 2 x L2"},
+        "roofline": {"bound": "hbm", "kernel": "mx_fp4_quantize", "achieved": gbs, "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                     "algorithmic_bytes_per_launch": algo, "avg_launch_ms": ms}}))
+
+
 def main():
     args = parse()
+    if args.op == "mx_fp4_quantize":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": "mx_fp4_quantize",
+                              "unavailable": "the encoder is timed on the GPU only"}))
+            return
+        run_mx_fp4_quantize(args)
+        return
     from mxfp4_mixture_experts_rms_gb300 import synth
     global WORKLOAD, TOKENS
     WORKLOAD = args.workload

@@ -182,6 +182,27 @@ int moe_forward_noalloc(moe_plan *plan, const uint16_t *x, int tokens, float *ou
  * MOE_EINVAL on NULL/misaligned pointers, MOE_ECUDA on a launch error. */
 int moe_cast_f32_to_bf16(const float *src, uint16_t *dst, size_t n, void *stream);
 
+/* FP4 activation encoding (ds4.c, FP4 activation quantisation
+ * `dsv4_fp4_act_quantize_row_inplace_cpu` and its nearest-value step
+ * `dsv4_e2m1fn_dequant_cpu`): x bf16 [rows][cols] -> codes uint8
+ * [rows][cols/2] and E8M0 scales uint8 [rows][cols/32] in the canonical
+ * MXFP4 layout above, enqueued on `stream`.  Per 32-element block:
+ *   amax = max |x_i| over the block (NaN elements never raise it), at least
+ *          6 * 2^-126;
+ *   k    = ceil(log2(amax / 6)), the quotient rounded once to float and the
+ *          ceiling taken exactly (127 when the quotient is infinite);
+ *   scale byte = k + 127 (so 1..254: never the NaN code);
+ *   code = the E2M1 value nearest to x_i / 2^k clamped to [-6, 6], ties to
+ *          the even code; sign bit set when x_i < 0 (so -0 and NaN encode as
+ *          positive; NaN becomes +6).
+ * Decoding the result (E2M1 x 2^(scale-127)) gives the page's round-tripped
+ * activations.  x and codes are device pointers, 16-byte aligned; scales a
+ * device pointer; the three must not overlap.  rows = 0 is a no-op.
+ * MOE_ESHAPE when cols is not a positive multiple of 32; MOE_EINVAL on NULL,
+ * misaligned or overlapping pointers; MOE_ECUDA on a launch error. */
+int moe_mx_quantize_fp4(const uint16_t *x, size_t rows, size_t cols, uint8_t *codes, uint8_t *scales,
+                        void *stream);
+
 /* Text of the last failure on this thread ("" if none). */
 const char *moe_last_error(void);
 

@@ -536,6 +536,22 @@ int moe_cast_f32_to_bf16(const float *src, uint16_t *dst, size_t n, void *stream
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_cast_f32_to_bf16");
 }
 
+int moe_mx_quantize_fp4(const uint16_t *x, size_t rows, size_t cols, uint8_t *codes, uint8_t *scales,
+                        void *stream) {
+    if (rows == 0) return MOE_OK;
+    if (!x || !codes || !scales) return fail(MOE_EINVAL, "NULL x, codes or scales");
+    if (cols == 0 || cols % 32 != 0) return fail(MOE_ESHAPE, "cols must be a positive multiple of 32 (got %zu)", cols);
+    if (!aligned16(x) || !aligned16(codes)) return fail(MOE_EINVAL, "x and codes must be 16-byte aligned");
+    const size_t n = rows * cols;
+    const char *xb = reinterpret_cast<const char *>(x), *cb = reinterpret_cast<const char *>(codes),
+               *sb = reinterpret_cast<const char *>(scales);
+    const size_t xn = n * 2, cn = n / 2, sn = n / 32;
+    if ((xb < cb + cn && cb < xb + xn) || (xb < sb + sn && sb < xb + xn) || (cb < sb + sn && sb < cb + cn))
+        return fail(MOE_EINVAL, "x, codes and scales must not overlap");
+    const cudaError_t e = launch_mx_fp4_quantize(x, n / 32, codes, scales, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_mx_quantize_fp4");
+}
+
 int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, int32_t *ids_out, void *stream) {
     if (!p) return fail(MOE_EINVAL, "NULL plan");
     if (tokens < 0) return fail(MOE_EINVAL, "tokens must be >= 0");

@@ -182,6 +182,8 @@ cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, cons
                                 cudaStream_t st);
 // dst = bf16_rne(src), n elements (any n; 16-byte aligned pointers)
 cudaError_t launch_cast_bf16(const float *src, uint16_t *dst, size_t n, cudaStream_t st);
+cudaError_t launch_mx_fp4_quantize(const uint16_t *x, size_t n_blocks, uint8_t *codes, uint8_t *scales,
+                                   cudaStream_t st);
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T,
                            float *out, cudaStream_t st);
 // What the grouped GEMM reads its weights through: TMA descriptors of the

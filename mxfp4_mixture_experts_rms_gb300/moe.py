@@ -24,7 +24,7 @@ EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_plan_set_i", "moe_plan_se
            "moe_workspace_bytes",
            "moe_set_workspace", "moe_load_weights", "moe_forward", "moe_forward_ex", "moe_get_expert_counts",
            "moe_get_permutation", "moe_debug_dequant", "moe_profile_read", "moe_get_device_status",
-           "moe_forward_noalloc", "moe_cast_f32_to_bf16", "moe_last_error"]
+           "moe_forward_noalloc", "moe_cast_f32_to_bf16", "moe_mx_quantize_fp4", "moe_last_error"]
 
 
 class MoeError(RuntimeError):
@@ -78,6 +78,7 @@ def load(build_if_missing: bool = True):
     L.moe_profile_read.argtypes = [P, C.POINTER(C.c_double), C.POINTER(I), I]
     L.moe_forward_noalloc.argtypes = [P, P, I, P, P, P]
     L.moe_cast_f32_to_bf16.argtypes = [P, P, SZ, P]
+    L.moe_mx_quantize_fp4.argtypes = [P, SZ, SZ, P, P, P]
     L.moe_last_error.restype = C.c_char_p
     L.moe_last_error.argtypes = []
     for name in EXPORTS:
@@ -110,6 +111,16 @@ def cast_f32_to_bf16(src, dst, stream=None):
     assert src.numel() == dst.numel()
     _check(load().moe_cast_f32_to_bf16(C.c_void_p(_ptr(src)), C.c_void_p(_ptr(dst)), int(src.numel()),
                                        _stream_ptr(stream)))
+
+
+def mx_quantize_fp4(x, codes, scales, stream=None):
+    """FP4 activation encoding of x (bf16 bits as int16/uint16, device, [rows][cols])
+    into codes (uint8 [rows][cols/2]) and E8M0 scales (uint8 [rows][cols/32]),
+    both device tensors; enqueued on `stream`."""
+    rows, cols = x.shape
+    assert codes.numel() == rows * cols // 2 and scales.numel() == rows * cols // 32
+    _check(load().moe_mx_quantize_fp4(C.c_void_p(_ptr(x)), rows, cols, C.c_void_p(_ptr(codes)),
+                                      C.c_void_p(_ptr(scales)), _stream_ptr(stream)))
 
 
 class DeviceBlock:
