@@ -531,14 +531,17 @@ def run_mx_fp4_quantize(args):
     ms = e0.elapsed_time(e1) / args.steps
     hbm, _, peak_kind = peaks()
     gbs = algo / (ms / 1e3) / 1e9
+    workload = f"FP4 activation encoding, {R} x {Cc} bf16"
+    tr = traffic_record("mx_fp4_quantize", workload)
     print(json.dumps({
         "op": "mx_fp4_quantize", "metric": "FP4 activation encoding bandwidth", "value": gbs, "unit": "GB/s",
         "higher_is_better": True, "steps": args.steps, "ms_per_launch": ms, "dtype": "bf16->fp4",
         "data": "synthetic", "gpu_launches": args.steps, "clocks": clocks,
-        "config": {"workload": f"FP4 activation encoding, {R} x {Cc} bf16", "rows": R, "cols": Cc,
+        "config": {"workload": workload, "rows": R, "cols": Cc,
                    "l2": f"{n_sets} input sets rotated, {n_sets * algo / 1e6:.0f} MB > 2 x L2"},
         "roofline": {"bound": "hbm", "kernel": "mx_fp4_quantize", "achieved": gbs, "peak": hbm,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / hbm,
+                     "traffic": tr["bytes_per_launch"] if tr else None,
                      "algorithmic_bytes_per_launch": algo, "avg_launch_ms": ms}}))
 
 
