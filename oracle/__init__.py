@@ -40,7 +40,8 @@ def build(force: bool = False) -> str:
 class Cfg(C.Structure):
     _fields_ = [("hidden", C.c_int64), ("expert_hidden", C.c_int64), ("n_experts", C.c_int32),
                 ("top_k", C.c_int32), ("n_shared", C.c_int32), ("swiglu_alpha", C.c_double),
-                ("swiglu_limit", C.c_double), ("weight_scale", C.c_double), ("rms_eps", C.c_double)]
+                ("swiglu_limit", C.c_double), ("weight_scale", C.c_double), ("rms_eps", C.c_double),
+                ("act_fp4", C.c_int32)]
 
 
 class Expert(C.Structure):
@@ -213,18 +214,21 @@ def permutation(ids: np.ndarray, n_experts: int):
     return dict(counts=counts, offsets=offsets, perm_token=pt, perm_slot=ps, loc=loc)
 
 
-def _cfg(shape) -> Cfg:
+def _cfg(shape, act_fp4: bool = False) -> Cfg:
     return Cfg(shape.hidden, shape.expert_hidden, shape.n_experts, shape.top_k, shape.n_shared,
-               shape.swiglu_alpha, shape.swiglu_limit, shape.weight_scale, shape.rms_eps)
+               shape.swiglu_alpha, shape.swiglu_limit, shape.weight_scale, shape.rms_eps,
+               1 if act_fp4 else 0)
 
 
-def moe_forward(blk: dict, x: np.ndarray, nthreads: int = 1, shape=None):
+def moe_forward(blk: dict, x: np.ndarray, nthreads: int = 1, shape=None, act_fp4: bool = False):
     """Whole block on tokens ``x`` (bf16 bits [T][H]) with the weights of ``blk``.
+    act_fp4: every expert's inputs (x_hat, and h after its bf16 rounding) pass
+    through the FP4 activation encoding and back before their projections.
 
     Returns dict(out float64 [T][H], ids int32 [T][K], route_w float64 [T][K],
     xhat uint16 [T][H], logits float64 [T][E])."""
     shape = shape or blk["shape"]
-    cfg = _cfg(shape)
+    cfg = _cfg(shape, act_fp4)
     w = Weights()
     keep = []
 

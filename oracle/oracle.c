@@ -257,11 +257,33 @@ static double mxfp4_row_dot(const uint8_t *codes, const uint8_t *scales, int64_t
  * `matrix_vector` of down on the result, `add_bias`.  Expert tensors are
  * validated there as MXFP4; gate/up map hidden -> expert_hidden and down maps
  * back.  h is rounded to bf16 before the down projection (contract). */
+/* The FP4 activation mode's round trip of a vector of n (a multiple of 32)
+ * float values held in doubles: encode ([ds4.c] FP4 activation quantisation),
+ * then decode each element as E2M1 x 2^(e - 127). */
+static void fp4_round_trip(double *v, int64_t n) {
+    float *f = (float *)malloc(sizeof(float) * (size_t)n);
+    uint8_t *codes = (uint8_t *)calloc((size_t)n / 2, 1);
+    uint8_t *scales = (uint8_t *)malloc((size_t)n / 32);
+    for (int64_t i = 0; i < n; i++) f[i] = (float)v[i]; /* exact: v holds bf16 values */
+    oracle_mx_fp4_quantize(f, 1, n, codes, scales);
+    for (int64_t i = 0; i < n; i++) v[i] = oracle_mxfp4_element(codes, scales, n, 0, i);
+    free(f);
+    free(codes);
+    free(scales);
+}
+
 void oracle_expert_ffn(const oracle_expert *ex, int64_t H, int64_t F, const uint16_t *xhat,
                        double alpha, double limit, double *y, uint16_t *h_out, double *gu_out) {
+    oracle_expert_ffn_ex(ex, H, F, xhat, alpha, limit, 0, y, h_out, gu_out);
+}
+
+void oracle_expert_ffn_ex(const oracle_expert *ex, int64_t H, int64_t F, const uint16_t *xhat,
+                          double alpha, double limit, int act_fp4, double *y, uint16_t *h_out,
+                          double *gu_out) {
     double *xv = (double *)malloc(sizeof(double) * (size_t)H);
     double *hv = (double *)malloc(sizeof(double) * (size_t)F);
     for (int64_t i = 0; i < H; i++) xv[i] = oracle_bf16_to_double(xhat[i]);
+    if (act_fp4) fp4_round_trip(xv, H);
     for (int64_t j = 0; j < F; j++) {
         double g = mxfp4_row_dot(ex->codes[0], ex->scales[0], H, j, xv) + (double)ex->bias[0][j];
         double u = mxfp4_row_dot(ex->codes[1], ex->scales[1], H, j, xv) + (double)ex->bias[1][j];
@@ -273,6 +295,7 @@ void oracle_expert_ffn(const oracle_expert *ex, int64_t H, int64_t F, const uint
         if (h_out) h_out[j] = hb;
         hv[j] = oracle_bf16_to_double(hb);
     }
+    if (act_fp4) fp4_round_trip(hv, F);
     for (int64_t i = 0; i < H; i++)
         y[i] = mxfp4_row_dot(ex->codes[2], ex->scales[2], F, i, hv) + (double)ex->bias[2][i];
     free(xv);
@@ -334,7 +357,8 @@ static void token_forward(const oracle_cfg *cfg, const oracle_weights *w, const 
     oracle_route_weights(vals, K, cfg->weight_scale, rw);
     for (int32_t j = 0; j < K; j++) {
         oracle_expert ex = expert_at(w, cfg, ids[j]);
-        oracle_expert_ffn(&ex, H, F, xhat, cfg->swiglu_alpha, cfg->swiglu_limit, y, NULL, NULL);
+        oracle_expert_ffn_ex(&ex, H, F, xhat, cfg->swiglu_alpha, cfg->swiglu_limit, cfg->act_fp4, y, NULL,
+                             NULL);
         for (int64_t i = 0; i < H; i++) mix[i] += rw[j] * y[i];
     }
     if (cfg->n_shared) {
@@ -344,7 +368,8 @@ static void token_forward(const oracle_cfg *cfg, const oracle_weights *w, const 
             sh.scales[m] = w->sh_scales[m];
             sh.bias[m] = w->sh_bias[m];
         }
-        oracle_expert_ffn(&sh, H, F, xhat, cfg->swiglu_alpha, cfg->swiglu_limit, y, NULL, NULL);
+        oracle_expert_ffn_ex(&sh, H, F, xhat, cfg->swiglu_alpha, cfg->swiglu_limit, cfg->act_fp4, y, NULL,
+                             NULL);
         for (int64_t i = 0; i < H; i++) mix[i] += y[i];
     }
     for (int64_t i = 0; i < H; i++) out[i] = oracle_bf16_to_double(x[i]) + mix[i];

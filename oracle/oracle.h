@@ -43,6 +43,7 @@ typedef struct {
     double swiglu_limit;
     double weight_scale;   /* route weights = weight_scale * softmax */
     double rms_eps;
+    int32_t act_fp4;       /* 1: expert inputs pass through the FP4 activation encoding */
 } oracle_cfg;
 
 /* One expert's three matrices, already offset to that expert. */
@@ -115,6 +116,13 @@ double oracle_swiglu(double g, double u, double alpha, double limit);
  * y: [H]; h_out (optional): the bf16 bits of h, [F]; gu_out (optional): g then u, [2F]. */
 void oracle_expert_ffn(const oracle_expert *ex, int64_t H, int64_t F, const uint16_t *xhat,
                        double alpha, double limit, double *y, uint16_t *h_out, double *gu_out);
+/* oracle_expert_ffn with the FP4 activation mode: when act_fp4 is non-zero,
+ * x_hat (before gate/up) and h (after its bf16 rounding, before down) are each
+ * replaced by the decoded FP4 activation encoding of themselves, in 32-element
+ * blocks along the contracted dimension; h_out still returns the bf16 h. */
+void oracle_expert_ffn_ex(const oracle_expert *ex, int64_t H, int64_t F, const uint16_t *xhat,
+                          double alpha, double limit, int act_fp4, double *y, uint16_t *h_out,
+                          double *gu_out);
 /* Token -> expert grouping: counts[E], offsets[E+1] (exclusive prefix sum),
  * routes of each expert in ascending (token, slot) order: perm_token / perm_slot [T*K],
  * and the inverse map loc[t*K + s] = position of route (t, s). */

@@ -290,9 +290,17 @@ def _bf16_round_array(v):
     return np.array([oracle.bf16_to_double(oracle.bf16_rne(a)) for a in np.ravel(v)]).reshape(np.shape(v))
 
 
-def _dense_block(blk, x_bits):
+def _fp4_rows(v):
+    """Each row through the (separately pinned) FP4 activation encoding and back."""
+    c, s = oracle.mx_fp4_quantize(np.atleast_2d(v).astype(np.float32))   # exact: bf16 values
+    return oracle.mxfp4_dequant(c, s)
+
+
+def _dense_block(blk, x_bits, act_fp4=False):
     """Dense brute force: every expert on every token (numpy matmul on the test's
-    own dense matrices), then a top-k mask from a full stable sort, scipy softmax."""
+    own dense matrices), then a top-k mask from a full stable sort, scipy softmax.
+    act_fp4: the expert inputs (x_hat; h after its bf16 rounding) go through the
+    FP4 activation encoding row by row first."""
     import scipy.special as sp
     shape = blk["shape"]
     H, E, K = shape.hidden, shape.n_experts, shape.top_k
@@ -303,11 +311,15 @@ def _dense_block(blk, x_bits):
     logits = xh @ synth.bf16_bits_to_f32(blk["router_w"]).astype(np.float64).T + blk["router_b"]
 
     def ffn(d, b, xin):
+        if act_fp4:
+            xin = _fp4_rows(xin)
         gg = xin @ d["gate"].T + b["gate"]
         uu = xin @ d["up"].T + b["up"]
         gc = np.minimum(gg, shape.swiglu_limit)
         uc = np.clip(uu, -shape.swiglu_limit, shape.swiglu_limit)
         h = _bf16_round_array(gc * sp.expit(shape.swiglu_alpha * gc) * (uc + 1))
+        if act_fp4:
+            h = _fp4_rows(h)
         return h @ d["down"].T + b["down"]
 
     ys = np.stack([ffn({m: blk["dense"][m][e] for m in synth.MATS},
@@ -354,6 +366,37 @@ def test_tiny_block_rectangular_expert_hidden():
     want, ids, _ = _dense_block(blk, x)
     assert np.array_equal(r["ids"], ids)
     np.testing.assert_allclose(r["out"], want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("H,F,E,K,shared,scale", [(32, 32, 4, 2, 0, 1.0), (64, 32, 5, 3, 0, 1.0),
+                                                  (32, 64, 4, 2, 1, 1.5)])
+def test_fp4_activation_mode_matches_dense_brute_force(H, F, E, K, shared, scale):
+    """The FP4 activation mode of the block (expert inputs encoded as the ds4.c
+    FP4 activation quantisation does) against the dense formulation."""
+    pytest.importorskip("scipy")
+    rng = np.random.default_rng(31 + H + F + shared)
+    shape = synth.tiny_shape(H, F, E, K, n_shared=shared, weight_scale=scale)
+    blk = _tiny_block(rng, shape)
+    x = synth.f32_to_bf16_bits(rng.normal(0, 1, (7, H)))
+    r = oracle.moe_forward(blk, x, act_fp4=True)
+    want, ids, _ = _dense_block(blk, x, act_fp4=True)
+    assert np.array_equal(r["ids"], ids)
+    np.testing.assert_allclose(r["out"], want, rtol=1e-12, atol=1e-12)
+
+
+def test_fp4_activation_mode_changes_only_the_expert_outputs():
+    rng = np.random.default_rng(37)
+    shape = synth.tiny_shape(64, 64, 6, 2)
+    blk = _tiny_block(rng, shape)
+    x = synth.f32_to_bf16_bits(rng.normal(0, 1, (5, 64)))
+    r0 = oracle.moe_forward(blk, x)
+    r1 = oracle.moe_forward(blk, x, act_fp4=True)
+    for key in ("ids", "route_w", "xhat", "logits"):
+        assert np.array_equal(r0[key], r1[key]), key
+    d0, d1 = r0["out"] - synth.bf16_bits_to_f32(x), r1["out"] - synth.bf16_bits_to_f32(x)
+    assert not np.array_equal(d0, d1)
+    # E2M1 keeps ~2 significant bits of each activation: the deltas agree to tens of percent
+    assert np.linalg.norm(d1 - d0) < 0.5 * np.linalg.norm(d0)
 
 
 def test_identical_experts_collapse_to_one_expert():
