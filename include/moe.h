@@ -199,7 +199,8 @@ int moe_cast_f32_to_bf16(const float *src, uint16_t *dst, size_t n, void *stream
  * activations.  x and codes are device pointers, 16-byte aligned; scales a
  * device pointer; the three must not overlap.  rows = 0 is a no-op.
  * MOE_ESHAPE when cols is not a positive multiple of 32; MOE_EINVAL on NULL,
- * misaligned or overlapping pointers; MOE_ECUDA on a launch error. */
+ * misaligned or overlapping pointers or a rows x cols beyond the address
+ * space; MOE_ECUDA on a launch error. */
 int moe_mx_quantize_fp4(const uint16_t *x, size_t rows, size_t cols, uint8_t *codes, uint8_t *scales,
                         void *stream);
 

@@ -542,6 +542,7 @@ int moe_mx_quantize_fp4(const uint16_t *x, size_t rows, size_t cols, uint8_t *co
     if (!x || !codes || !scales) return fail(MOE_EINVAL, "NULL x, codes or scales");
     if (cols == 0 || cols % 32 != 0) return fail(MOE_ESHAPE, "cols must be a positive multiple of 32 (got %zu)", cols);
     if (!aligned16(x) || !aligned16(codes)) return fail(MOE_EINVAL, "x and codes must be 16-byte aligned");
+    if (rows > (SIZE_MAX / 2) / cols) return fail(MOE_EINVAL, "rows x cols overflows the address space");
     const size_t n = rows * cols;
     const char *xb = reinterpret_cast<const char *>(x), *cb = reinterpret_cast<const char *>(codes),
                *sb = reinterpret_cast<const char *>(scales);

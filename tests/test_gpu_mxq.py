@@ -2,9 +2,10 @@
 C-ABI) against the oracle: codes and E8M0 scales bit-exact, every byte.
 
 The encoding decides integers (a code, an exponent) from floating point; both
-sides take those decisions from exact quantities (|x| of bf16 values, one
-float32 rounding of amax / 6, a power-of-two division), so they must agree
-bit for bit on every input, NaN and infinity included.
+sides take those decisions from exact quantities (|x| of bf16 values; the
+exponent of amax / 6, from a float32 division in the oracle and from amax's
+bits on the GPU, equal for every bf16 amax; a power-of-two scaling), so they
+must agree bit for bit on every input, NaN and infinity included.
 """
 import numpy as np
 import pytest
@@ -115,5 +116,6 @@ def test_arguments_and_empty_input():
     assert L.moe_mx_quantize_fp4(p(x), 2, 32, p(codes, 4), p(scales), None) == moe.MOE_EINVAL
     assert L.moe_mx_quantize_fp4(p(x), 4, 64, p(x, 64), p(scales), None) == moe.MOE_EINVAL   # overlap
     assert L.moe_mx_quantize_fp4(None, 4, 64, p(codes), p(scales), None) == moe.MOE_EINVAL
+    assert L.moe_mx_quantize_fp4(p(x), 2 ** 62, 64, p(codes), p(scales), None) == moe.MOE_EINVAL
     torch.cuda.synchronize()
     assert codes.cpu().numpy().max() == 0 and scales.cpu().numpy().max() == 0   # nothing written
