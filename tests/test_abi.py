@@ -82,3 +82,23 @@ def test_generated_shapes_match_layout():
     assert blk["codes"]["gate"].shape == (32, 2880, 1440)
     assert blk["scales"]["down"].shape == (32, 2880, 90)
     assert synth.expert_bytes(synth.GPT_OSS) == 3 * (2880 * 1440 + 2880 * 90)
+
+
+def test_standalone_ops_reject_bad_arguments_before_touching_the_device(L):
+    """The encoder and the cast validate sizes, alignment and overlap on the
+    host; these addresses are never dereferenced."""
+    X, Cd, S = C.c_void_p(0x100000), C.c_void_p(0x200000), C.c_void_p(0x300000)
+    assert L.moe_mx_quantize_fp4(X, 0, 64, Cd, S, None) == moe.MOE_OK           # empty: no-op
+    assert L.moe_mx_quantize_fp4(X, 4, 48, Cd, S, None) == moe.MOE_ESHAPE
+    assert L.moe_mx_quantize_fp4(X, 4, 0, Cd, S, None) == moe.MOE_ESHAPE
+    assert L.moe_mx_quantize_fp4(None, 4, 64, Cd, S, None) == moe.MOE_EINVAL
+    assert L.moe_mx_quantize_fp4(C.c_void_p(0x100008), 4, 64, Cd, S, None) == moe.MOE_EINVAL
+    assert L.moe_mx_quantize_fp4(X, 4, 64, C.c_void_p(0x200004), S, None) == moe.MOE_EINVAL
+    assert L.moe_mx_quantize_fp4(X, 4, 64, C.c_void_p(0x100100), S, None) == moe.MOE_EINVAL  # inside x
+    assert L.moe_mx_quantize_fp4(X, 4, 64, Cd, C.c_void_p(0x200010), None) == moe.MOE_EINVAL  # inside codes
+    assert L.moe_mx_quantize_fp4(X, 2 ** 62, 64, Cd, S, None) == moe.MOE_EINVAL
+    assert b"overflow" in L.moe_last_error()
+    assert L.moe_cast_f32_to_bf16(X, Cd, 0, None) == moe.MOE_OK
+    assert L.moe_cast_f32_to_bf16(None, Cd, 16, None) == moe.MOE_EINVAL
+    assert L.moe_cast_f32_to_bf16(C.c_void_p(0x100004), Cd, 16, None) == moe.MOE_EINVAL
+    assert L.moe_cast_f32_to_bf16(X, C.c_void_p(0x100020), 16, None) == moe.MOE_EINVAL   # overlap
