@@ -120,13 +120,16 @@ int moe_set_workspace(moe_plan *plan, void *dev_ptr, size_t bytes);
 int moe_load_weights(moe_plan *plan, const moe_weights *w);
 
 /* out[T][H] (float) = x + MoE(x) for x bf16 [T][H]; route_ids_out int32
- * [T][top_k] (may be NULL) gets the selected experts of each token in
- * descending-logit order.  x and out must not alias.  tokens = 0 is a no-op.
+ * [T][top_k] (may be NULL; 4-byte aligned) gets the selected experts of each
+ * token in descending-logit order.  x and out (16-byte aligned) must not
+ * alias.  tokens = 0 is a no-op.  MOE_EINVAL on NULL, misaligned or aliasing
+ * pointers (checked before anything is enqueued).
  * Enqueue only; graph-capturable; stream is a cudaStream_t (NULL = legacy). */
 int moe_forward(moe_plan *plan, const uint16_t *x, int tokens, float *out,
                 int32_t *route_ids_out, void *stream);
-/* As moe_forward, also writing the route weights [T][top_k] (float) and the
- * normalised activations x_hat [T][H] (bf16) when those pointers are non-NULL. */
+/* As moe_forward, also writing the route weights [T][top_k] (float, 4-byte
+ * aligned) and the normalised activations x_hat [T][H] (bf16, 16-byte aligned,
+ * not overlapping x) when those pointers are non-NULL. */
 int moe_forward_ex(moe_plan *plan, const uint16_t *x, int tokens, float *out,
                    int32_t *route_ids_out, float *route_w_out, uint16_t *xhat_out, void *stream);
 

@@ -40,6 +40,7 @@ int cuda_fail(cudaError_t e, const char *what) {
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
 
 }  // namespace
 
@@ -156,6 +157,20 @@ MatPtrs mat_of(const moe_mxfp4_matrix &m, const moe_mxfp4_matrix &sh, int rows, 
     r.rows = rows;
     r.cols = cols;
     return r;
+}
+
+// The optional per-token outputs of a forward: the routing kernel writes ids
+// and route weights with 4-byte stores and x_hat with 16-byte stores, while it
+// still reads x.
+int check_outputs(const BlockParams &b, int tokens, const uint16_t *x, const int32_t *ids_out, const float *rw_out,
+                  const uint16_t *xhat_out) {
+    if (!aligned4(ids_out) || !aligned4(rw_out))
+        return fail(MOE_EINVAL, "ids and route-weight outputs must be 4-byte aligned");
+    if (!aligned16(xhat_out)) return fail(MOE_EINVAL, "the x_hat output must be 16-byte aligned");
+    const char *xb = reinterpret_cast<const char *>(x), *hb = reinterpret_cast<const char *>(xhat_out);
+    const size_t n = (size_t)tokens * b.H * 2;
+    if (hb && hb < xb + n && xb < hb + n) return fail(MOE_EINVAL, "the x_hat output must not overlap x");
+    return MOE_OK;
 }
 
 int check_matrix(const moe_mxfp4_matrix &m, const char *name) {
@@ -381,6 +396,7 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     const char *xb = reinterpret_cast<const char *>(x), *ob = reinterpret_cast<const char *>(out);
     if (xb < ob + (size_t)tokens * b.H * 4 && ob < xb + (size_t)tokens * b.H * 2)
         return fail(MOE_EINVAL, "x and out must not alias");
+    if (int rc = check_outputs(b, tokens, x, ids_out, rw_out, xhat_out)) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     bool decode = false;
     int nt = 1, tile_rows = 0;
@@ -564,6 +580,7 @@ int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, 
     const char *xb = reinterpret_cast<const char *>(x), *ob = reinterpret_cast<const char *>(out);
     if (xb < ob + (size_t)tokens * b.H * 4 && ob < xb + (size_t)tokens * b.H * 2)
         return fail(MOE_EINVAL, "x and out must not alias");
+    if (int rc0 = check_outputs(b, tokens, x, ids_out, nullptr, nullptr)) return rc0;
     const size_t need = carve(p, tokens, nullptr, nullptr);
     if (need > MOE_NOALLOC_SCRATCH_BYTES)
         return fail(MOE_ENOMEM, "moe_forward_noalloc: %d tokens need %zu bytes of scratch, the static array holds %u",

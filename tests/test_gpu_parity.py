@@ -160,6 +160,33 @@ def test_edge_token_counts():
     assert plan.device_status() == 0
 
 
+def test_misaligned_or_overlapping_outputs_rejected_before_launch():
+    """ids / route weights are written with 4-byte stores and x_hat with 16-byte
+    stores: misaligned output pointers are refused on the host, nothing runs."""
+    import ctypes as C
+    import torch
+    shape = synth.tiny_shape(64, 64, 4, 2)
+    blk = tiny_block(6, shape)
+    plan = moe.Plan(shape, max_tokens=4).alloc_workspace().load_weights(moe.DeviceBlock(blk))
+    x = torch.zeros((2, 64), dtype=torch.int16, device="cuda")
+    out = torch.empty((2, 64), dtype=torch.float32, device="cuda")
+    buf = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    P = lambda t, off=0: C.c_void_p(t.data_ptr() + off)  # noqa: E731
+    L, h, N = plan.L, plan.h, None
+    assert L.moe_forward_ex(h, P(x), 2, P(out), P(buf, 2), N, N, N) == moe.MOE_EINVAL
+    assert L.moe_forward_ex(h, P(x), 2, P(out), N, P(buf, 6), N, N) == moe.MOE_EINVAL
+    assert L.moe_forward_ex(h, P(x), 2, P(out), N, N, P(buf, 8), N) == moe.MOE_EINVAL
+    assert L.moe_forward_ex(h, P(x), 2, P(out), N, N, P(x, 16), N) == moe.MOE_EINVAL   # x_hat over x
+    assert L.moe_forward_noalloc(h, P(x), 2, P(out), P(buf, 1), N) == moe.MOE_EINVAL
+    torch.cuda.synchronize()
+    assert int(buf.sum()) == 0 and plan.device_status() == 0
+    plan.forward_ex(x, out, ids=torch.empty((2, 2), dtype=torch.int32, device="cuda"),
+                    route_w=torch.empty((2, 2), dtype=torch.float32, device="cuda"),
+                    xhat=torch.empty((2, 64), dtype=torch.int16, device="cuda"))
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+
+
 def test_nan_scale_rejected_at_load():
     shape = synth.tiny_shape(64, 64, 4, 2)
     blk = tiny_block(6, shape)
