@@ -135,10 +135,13 @@ int moe_forward_ex(moe_plan *plan, const uint16_t *x, int tokens, float *out,
 
 /* Per-expert token counts of the last forward: int32 [n_experts] (device), enqueued. */
 int moe_get_expert_counts(const moe_plan *plan, int32_t *dev_counts_out, void *stream);
-/* Token->expert grouping of the last forward (device outputs, enqueued):
- * offsets [n_experts + n_shared + 1] (exclusive prefix sums of the counts),
- * perm_token / perm_slot [tokens*(top_k + n_shared)]: the routes of each expert
- * in ascending (token, slot) order; the shared expert comes last with slot top_k. */
+/* Token->expert grouping of the last moe_forward / moe_forward_ex (device
+ * outputs, enqueued): offsets [n_experts + n_shared + 1] (exclusive prefix
+ * sums of the counts); perm_token / perm_slot: the routes of each expert in
+ * ascending (token, slot) order, the shared expert last with slot top_k.
+ * Both perm arrays must hold max_tokens * (top_k + n_shared) int32 entries
+ * (the plan's largest route count: that extent is copied); entries from
+ * offsets[n_experts + n_shared] on are unspecified. */
 int moe_get_permutation(const moe_plan *plan, int32_t *offsets, int32_t *perm_token,
                         int32_t *perm_slot, void *stream);
 /* Dequantise one expert matrix (which: 0 gate, 1 up, 2 down; expert = n_experts

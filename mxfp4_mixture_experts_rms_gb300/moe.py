@@ -221,6 +221,13 @@ class Plan:
         _check(self.L.moe_get_expert_counts(self.h, C.c_void_p(_ptr(out)), _stream_ptr(stream)))
 
     def permutation(self, offsets, perm_token, perm_slot, stream=None):
+        """offsets [E + n_shared + 1]; perm_token / perm_slot of at least
+        max_tokens * (top_k + n_shared) entries (the extent the library copies)."""
+        R = self.max_tokens * (self.shape.top_k + self.shape.n_shared)
+        if perm_token.numel() < R or perm_slot.numel() < R:
+            raise MoeError(MOE_EINVAL, f"perm_token / perm_slot need {R} entries")
+        if offsets.numel() < self.shape.n_experts + self.shape.n_shared + 1:
+            raise MoeError(MOE_EINVAL, "offsets needs n_experts + n_shared + 1 entries")
         _check(self.L.moe_get_permutation(self.h, C.c_void_p(_ptr(offsets)), C.c_void_p(_ptr(perm_token)),
                                           C.c_void_p(_ptr(perm_slot)), _stream_ptr(stream)))
 
