@@ -145,7 +145,8 @@ int moe_get_expert_counts(const moe_plan *plan, int32_t *dev_counts_out, void *s
 int moe_get_permutation(const moe_plan *plan, int32_t *offsets, int32_t *perm_token,
                         int32_t *perm_slot, void *stream);
 /* Dequantise one expert matrix (which: 0 gate, 1 up, 2 down; expert = n_experts
- * selects the shared expert) to float [rows][cols] on the device.  Test hook. */
+ * selects the shared expert) to float [rows][cols] on the device (dev_out
+ * 4-byte aligned, rows x cols floats).  Test hook. */
 int moe_debug_dequant(const moe_plan *plan, int expert, int which, float *dev_out, void *stream);
 
 /* Kernel timing for benchmarks.  After moe_plan_set_i(plan, "profile", 1)

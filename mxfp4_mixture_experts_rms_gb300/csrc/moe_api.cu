@@ -466,6 +466,7 @@ int moe_debug_dequant(const moe_plan *p, int expert, int which, float *dev_out, 
     if (!p || !dev_out) return fail(MOE_EINVAL, "NULL argument");
     if (!p->have_w) return fail(MOE_ENOTREADY, "moe_load_weights has not been called");
     if (which < 0 || which > 2) return fail(MOE_EINVAL, "which must be 0 (gate), 1 (up) or 2 (down)");
+    if (!aligned4(dev_out)) return fail(MOE_EINVAL, "dev_out must be 4-byte aligned");
     if (expert < 0 || expert > p->bp.E || (expert == p->bp.E && !p->bp.n_shared))
         return fail(MOE_EINVAL, "expert %d out of range", expert);
     const MatPtrs &m = which == 0 ? p->gate : which == 1 ? p->up : p->down;

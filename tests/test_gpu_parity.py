@@ -178,6 +178,7 @@ def test_misaligned_or_overlapping_outputs_rejected_before_launch():
     assert L.moe_forward_ex(h, P(x), 2, P(out), N, N, P(buf, 8), N) == moe.MOE_EINVAL
     assert L.moe_forward_ex(h, P(x), 2, P(out), N, N, P(x, 16), N) == moe.MOE_EINVAL   # x_hat over x
     assert L.moe_forward_noalloc(h, P(x), 2, P(out), P(buf, 1), N) == moe.MOE_EINVAL
+    assert L.moe_debug_dequant(h, 0, 0, P(buf, 2), N) == moe.MOE_EINVAL
     torch.cuda.synchronize()
     assert int(buf.sum()) == 0 and plan.device_status() == 0
     plan.forward_ex(x, out, ids=torch.empty((2, 2), dtype=torch.int32, device="cuda"),
