@@ -94,8 +94,12 @@ def _check(rc: int):
 
 
 def _ptr(t):
+    """Device address of a tensor the library reads or writes as one dense
+    row-major array; a strided view would be misread, so it is refused."""
     if t is None:
         return None
+    if not t.is_contiguous():
+        raise MoeError(MOE_EINVAL, "tensors passed to the library must be contiguous")
     return t.data_ptr()
 
 
