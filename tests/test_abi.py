@@ -102,3 +102,12 @@ def test_standalone_ops_reject_bad_arguments_before_touching_the_device(L):
     assert L.moe_cast_f32_to_bf16(None, Cd, 16, None) == moe.MOE_EINVAL
     assert L.moe_cast_f32_to_bf16(C.c_void_p(0x100004), Cd, 16, None) == moe.MOE_EINVAL
     assert L.moe_cast_f32_to_bf16(X, C.c_void_p(0x100020), 16, None) == moe.MOE_EINVAL   # overlap
+
+
+def test_binding_refuses_strided_tensors(L):
+    torch = pytest.importorskip("torch")
+    src = torch.zeros((8, 4), dtype=torch.float32).t()          # a transposed view
+    dst = torch.zeros((4, 8), dtype=torch.int16)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.cast_f32_to_bf16(src, dst)
+    assert ei.value.status == moe.MOE_EINVAL
