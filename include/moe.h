@@ -87,7 +87,8 @@ void moe_plan_destroy(moe_plan *plan);
 /* Integer options:
  *   "n_shared_experts"  0 or 1: an always-on expert added with weight 1
  *                       (ds4.c DS4_SHAPE_FLASH n_expert_shared)
- *   "max_tokens"        largest token count per forward (sizes the workspace)
+ *   "max_tokens"        largest token count per forward (sizes the workspace),
+ *                       1..65535
  *   "decode_max_tokens" forwards with tokens <= this use the GEMV decode path,
  *                       larger ones the tensor-core grouped-GEMM path; -1
  *                       (default): 60 for up to 64 experts, 8 above

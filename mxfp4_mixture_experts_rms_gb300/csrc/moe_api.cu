@@ -39,6 +39,8 @@ int cuda_fail(cudaError_t e, const char *what) {
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+constexpr int kMaxTokens = 65535;  // tokens per forward: one combine grid row each
+
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
 
@@ -238,7 +240,8 @@ int moe_plan_set_i(moe_plan *p, const char *key, long long v) {
         p->bp.n_shared = (int)v;
         p->have_w = false;
     } else if (!strcmp(key, "max_tokens")) {
-        if (v < 1 || v > (1 << 20)) return fail(MOE_EINVAL, "max_tokens must be in [1, 2^20]");
+        // the combine kernel takes one grid row per token (grid y <= 65535)
+        if (v < 1 || v > kMaxTokens) return fail(MOE_EINVAL, "max_tokens must be in [1, %d]", kMaxTokens);
         if (p->have_ws) return fail(MOE_EINVAL, "max_tokens must be set before moe_set_workspace");
         p->max_tokens = (int)v;
     } else if (!strcmp(key, "decode_max_tokens")) {
@@ -586,6 +589,7 @@ int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, 
     if (need > MOE_NOALLOC_SCRATCH_BYTES)
         return fail(MOE_ENOMEM, "moe_forward_noalloc: %d tokens need %zu bytes of scratch, the static array holds %u",
                     tokens, need, MOE_NOALLOC_SCRATCH_BYTES);
+    if (tokens > kMaxTokens) return fail(MOE_ENOMEM, "tokens %d > %d", tokens, kMaxTokens);
     void *base = nullptr;
     int rc = noalloc_scratch(&base);
     if (rc != MOE_OK) return rc;

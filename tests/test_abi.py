@@ -50,6 +50,8 @@ def test_options_and_workspace_sizing(L):
     assert L.moe_plan_set_i(h, b"n_shared_experts", 2) == moe.MOE_EINVAL
     assert L.moe_plan_set_i(h, b"no_such_key", 1) == moe.MOE_EINVAL
     assert L.moe_plan_set_f(h, b"rms_eps", -1.0) == moe.MOE_EINVAL
+    assert L.moe_plan_set_i(h, b"max_tokens", 65536) == moe.MOE_EINVAL   # one combine grid row per token
+    assert L.moe_plan_set_i(h, b"max_tokens", 0) == moe.MOE_EINVAL
     assert L.moe_plan_set_i(h, b"max_tokens", 8) == moe.MOE_OK
     small = L.moe_workspace_bytes(h, 0)
     assert L.moe_plan_set_i(h, b"max_tokens", 512) == moe.MOE_OK
