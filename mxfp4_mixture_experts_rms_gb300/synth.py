@@ -136,20 +136,28 @@ def expert_matrices(shape: BlockShape, n: int, config: int, layer: int, sub: int
     return out
 
 
-def make_block(config: int, layer: int = 0, shape: BlockShape | None = None,
-               skew: str | None = None) -> dict:
-    """All weights of one block of workload ``config`` (layer ``layer``)."""
+def make_router(config: int, layer: int = 0, shape: BlockShape | None = None,
+                skew: str | None = None) -> dict:
+    """The norm and router weights of one block (``make_block`` without the
+    experts; the same arrays)."""
     wl = WORKLOADS.get(config)
     shape = shape or wl.shape
     skew = skew if skew is not None else (wl.router_skew if wl else "none")
     H, E = shape.hidden, shape.n_experts
-    blk = {
+    return {
         "shape": shape,
         "gamma": (1.0 + _rng(config, layer, _T_GAMMA).normal(0.0, 0.1, size=H)).astype(np.float32),
         "router_w": f32_to_bf16_bits(_rng(config, layer, _T_RW).normal(0.0, 0.02, size=(E, H))),
         "router_b": router_bias(shape, skew, config, layer),
     }
-    blk.update(expert_matrices(shape, E, config, layer, 0))
+
+
+def make_block(config: int, layer: int = 0, shape: BlockShape | None = None,
+               skew: str | None = None) -> dict:
+    """All weights of one block of workload ``config`` (layer ``layer``)."""
+    blk = make_router(config, layer, shape, skew)
+    shape = blk["shape"]
+    blk.update(expert_matrices(shape, shape.n_experts, config, layer, 0))
     if shape.n_shared:
         sh = expert_matrices(shape, 1, config, layer, 1)
         blk["shared"] = sh
@@ -183,6 +191,6 @@ def distinct_uniform(E: int, K: int, T: int) -> float:
 
 __all__ = [
     "BlockShape", "Workload", "WORKLOADS", "GPT_OSS", "DSV4_FLASH_SHAPE", "MATS",
-    "make_block", "make_tokens", "tiny_shape", "f32_to_bf16_bits", "bf16_bits_to_f32",
+    "make_block", "make_router", "make_tokens", "tiny_shape", "f32_to_bf16_bits", "bf16_bits_to_f32",
     "expert_bytes", "expert_bias_bytes", "distinct_uniform",
 ]
