@@ -1,20 +1,32 @@
 #!/usr/bin/env python3
 """Throughput of the MXFP4 routed MoE block on GB300.
 
-One step = one forward of the whole block (norm + router + top-k + softmax,
+One step = one pass of the whole block (norm + router + top-k + softmax,
 permutation, MXFP4 gate/up + SwiGLU, MXFP4 down, weighted combine + residual)
-over one batch of the workload: the gpt-oss MoE block decoding a batch of 8
-tokens with two hot experts (hidden 2880, 32 experts, top-4, expert_hidden
-2880).  Weights are seeded synthetic MXFP4 tensors of that architecture.  The
-steps rotate over several independently seeded weight sets whose touched
-experts together exceed the 129 MB L2, so no step finds its weights in L2.
+over one batch of the workload.  The headline workload is the largest
+single-GPU one: the 24-layer stack of independently seeded gpt-oss MoE blocks
+(hidden 2880, 32 experts, top-4, expert_hidden 2880, ~10 GB of MXFP4 expert
+weights resident) decoding 16 tokens, each layer's fp32 output cast to bf16 as
+the next layer's input.  In the same run every other workload is measured too
+(1-token decode, the 8-token hot-2 batch, the stack at 1 and 4 tokens, prefill
+at 128 and 512 tokens, the DeepSeek-V4-Flash-shaped block at 1 and 2048
+tokens) and reported under "configs", each with its own rate, roofline and
+clock record.
+
+Weights: router, gamma and router bias are drawn exactly as the seeded recipe
+does on the host (they decide the routing, including the hot-2 and Zipf
+skews); the expert matrices, gigabytes of them, are drawn on the device from
+the same distributions.  Single-block workloads rotate over weight sets whose
+touched experts together exceed twice the 129 MB L2, so no step finds its
+weights in L2; the stack is itself ~10 GB.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
-bounded sample of the same workload instead.
+bounded sample of the headline workload instead.
 """
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -26,9 +38,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE block tokens/s; decode HBM GB/s and prefill TFLOP/s vs GB300 peak"
-WORKLOAD = 1
-TOKENS = 8
+HEADLINE = (2, 16)           # (workload, tokens): the 24-layer stack decoding 16 tokens
+EXTRAS = [(0, 1), (1, 8), (2, 1), (2, 4), (3, 128), (3, 512), (4, 1), (4, 2048)]
 KERNEL_SLOTS = ["route_permute", "gateup_swiglu", "down_weighted", "combine_residual"]
+L2_BYTES = 129 * 2 ** 20
 
 
 def parse():
@@ -37,13 +50,15 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--sets", type=int, default=4, help="weight sets rotated over the steps")
-    ap.add_argument("--workload", type=int, default=WORKLOAD,
-                    help="workload id of synth.WORKLOADS (default: the 8-token hot-2 decode batch)")
-    ap.add_argument("--tokens", type=int, default=0, help="tokens per step (default: the workload's largest)")
+    ap.add_argument("--workload", type=int, default=HEADLINE[0],
+                    help="workload id of synth.WORKLOADS for the headline (default: the 24-layer stack)")
+    ap.add_argument("--tokens", type=int, default=0, help="tokens per step (default: 16 for the stack, "
+                                                          "else the workload's largest)")
+    ap.add_argument("--no-extras", action="store_true", help="measure the headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
-                    help="timed region only (no clock pre-roll, kernel timing, e2e or CPU baseline); for ncu")
+                    help="timed region of the headline only (no clock pre-roll, kernel timing, e2e, CPU "
+                         "baseline or extras); for ncu")
     ap.add_argument("--op", default="block", choices=["block", "mx_fp4_quantize"],
                     help="block: the MoE block (the benchmark); mx_fp4_quantize: the FP4 activation "
                          "encoder alone, on --rows x --cols bf16 activations")
@@ -122,8 +137,20 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def workload_config(wl, tokens):
+    """The `config` object of a line: what the workload is, from its shape."""
+    sh = wl.shape
+    return {"workload": wl.name, "tokens_per_step": tokens, "layers": wl.layers, "hidden": sh.hidden,
+            "n_experts": sh.n_experts, "top_k": sh.top_k, "expert_hidden": sh.expert_hidden,
+            "n_shared_experts": sh.n_shared, "weight_scale": sh.weight_scale, "swiglu_limit": sh.swiglu_limit,
+            "routing": wl.router_skew, "weights": "mxfp4 (e2m1 + e8m0/32)"}
+
+
 # ------------------------------------------------------------------ reference arm
-def run_reference(args, rank, world):
+def run_reference(args, rank, world, wid, T):
+    """The oracle, as it stands, on the host cores: each step one bounded sample
+    of the step's tokens through the whole workload (every layer of the stack),
+    sized so that the whole run takes a few minutes."""
     if rank != 0:
         return
     import numpy as np
@@ -131,72 +158,38 @@ def run_reference(args, rank, world):
     import oracle
     from mxfp4_mixture_experts_rms_gb300 import synth
     cores = os.cpu_count() or 1
-    wl = synth.WORKLOADS[WORKLOAD]
-    if wl.layers > 1:
-        return run_reference_stack(args, world, wl, cores)
-    blk = synth.make_block(WORKLOAD)
-    x = synth.make_tokens(WORKLOAD, TOKENS, blk["shape"].hidden)
+    wl = synth.WORKLOADS[wid]
+    shape = wl.shape
+    n_steps = args.warmup + args.steps
+    blk = synth.make_block(wid, layer=0)
+    x = synth.make_tokens(wid, T, shape.hidden)
     oracle.moe_forward(blk, x[:1], nthreads=1)  # warm the library
     t0 = time.perf_counter()
     oracle.moe_forward(blk, x[:1], nthreads=1)
-    t_tok = time.perf_counter() - t0
-    # tokens per step so that the whole run takes about three minutes on all cores
-    budget = 180.0
-    per_step = max(1, min(TOKENS, int(budget * cores / max(1e-9, (args.steps + args.warmup) * t_tok))))
-    nthr = min(cores, per_step)
-    for i in range(args.warmup):
-        oracle.moe_forward(blk, np.ascontiguousarray(x[(i % TOKENS):(i % TOKENS) + 1].repeat(per_step, 0)), nthreads=nthr)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        xs = np.ascontiguousarray(np.roll(x, -i, axis=0)[:per_step]) if per_step <= TOKENS else x
-        oracle.moe_forward(blk, xs, nthreads=nthr)
-    el = time.perf_counter() - t0
-    value = per_step * args.steps / el
-    sample = f"{per_step} of the {TOKENS} tokens of each step (full block per token), {nthr} threads"
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": synth.WORKLOADS[WORKLOAD].name, "tokens_per_step": TOKENS,
-                       "hidden": 2880, "n_experts": 32, "top_k": 4, "expert_hidden": 2880},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthr, "kind": "oracle",
-                             "sample": sample},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
-
-
-def run_reference_stack(args, world, wl, cores):
-    """The oracle through the whole stack for a bounded sample of each step's
-    tokens; each layer's weights are regenerated from their seed off the clock
-    (the stack does not fit comfortably in host memory twice)."""
-    import numpy as np
-
-    import oracle
-    from mxfp4_mixture_experts_rms_gb300 import synth
-    shape = wl.shape
-    x = synth.make_tokens(WORKLOAD, TOKENS, shape.hidden)
-    per_step = min(TOKENS, cores)
+    t_tok = (time.perf_counter() - t0) * wl.layers   # one token through every layer
+    budget = 150.0
+    per_step = max(1, min(T, cores, int(budget * cores / max(1e-9, n_steps * t_tok))))
+    # each step's sample: per_step consecutive tokens of the batch, rotating
+    xs = [np.ascontiguousarray(np.roll(x, -(i * per_step) % T, axis=0)[:per_step]) for i in range(n_steps)]
     el = 0.0
-    for i in range(args.warmup + args.steps):
-        xs = np.ascontiguousarray(np.roll(x, -i, axis=0)[:per_step])
-        for l in range(wl.layers):
-            blk = synth.make_block(WORKLOAD, layer=l)
+    for layer in range(wl.layers):
+        if layer:
+            del blk
+            blk = synth.make_block(wid, layer=layer)          # weight generation off the clock
+        for i in range(n_steps):
             t0 = time.perf_counter()
-            out = oracle.moe_forward(blk, xs, nthreads=per_step)["out"]
+            out = oracle.moe_forward(blk, xs[i], nthreads=per_step)["out"]
             if i >= args.warmup:
                 el += time.perf_counter() - t0
-            xs = synth.f32_to_bf16_bits(out)
-            del blk
+            if layer + 1 < wl.layers:
+                xs[i] = synth.f32_to_bf16_bits(out)
     value = per_step * args.steps / el
-    sample = (f"{per_step} of the {TOKENS} tokens of each step through all {wl.layers} layers, "
-              f"{per_step} threads (weight generation off the clock)")
+    sample = (f"{per_step} of the {T} tokens of each step through all {wl.layers} layer(s), "
+              f"{per_step} threads, weight generation off the clock")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": wl.name, "tokens_per_step": TOKENS, "layers": wl.layers,
-                       "hidden": shape.hidden, "n_experts": shape.n_experts, "top_k": shape.top_k,
-                       "expert_hidden": shape.expert_hidden},
+            "data": "synthetic", "config": workload_config(wl, T),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": per_step, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -234,127 +227,134 @@ def algorithmic_bytes(shape, counts, T):
     return gateup, down, distinct
 
 
-def cpu_baseline(blk, x):
-    import oracle
-    cores = os.cpu_count() or 1
-    n = min(x.shape[0], cores)
-    oracle.moe_forward(blk, x[:1], nthreads=1)
-    t0 = time.perf_counter()
-    oracle.moe_forward(blk, x[:n], nthreads=n)
-    el = time.perf_counter() - t0
-    return {"value": n / el, "unit": "tokens/s", "cores": n, "kind": "oracle",
-            "sample": f"{n} tokens of one step (weight set 0), whole block per token, {el:.1f} s wall"}
+def launches_per_forward(path: int, T: int) -> int:
+    """Kernels one forward launches: routing (+ the permutation kernel above 32
+    tokens), the x_hat gather (grouped-GEMM path), gate/up, down, combine."""
+    return (1 if T <= 32 else 2) + (1 if path == 2 else 0) + 3
 
 
-def cpu_baseline_stack(wl, x):
-    """The oracle through the whole stack (each layer's fp32 output cast to bf16
-    for the next), for as many of the step's tokens as there are cores."""
-    import oracle
+def n_weight_sets(wid, T):
+    """Weight sets a single-block workload rotates over so that the experts
+    touched between two uses of a set exceed 2.5 x L2."""
     from mxfp4_mixture_experts_rms_gb300 import synth
-    cores = os.cpu_count() or 1
-    n = min(x.shape[0], cores)
-    xs = x[:n]
-    el = 0.0
-    for l in range(wl.layers):
-        blk = synth.make_block(WORKLOAD, layer=l)
-        t0 = time.perf_counter()
-        out = oracle.moe_forward(blk, xs, nthreads=n)["out"]
-        el += time.perf_counter() - t0
-        xs = synth.f32_to_bf16_bits(out)
-        del blk
-    return {"value": n / el, "unit": "tokens/s", "cores": n, "kind": "oracle",
-            "sample": f"{n} tokens through all {wl.layers} layers, {el:.1f} s of oracle time"}
+    wl = synth.WORKLOADS[wid]
+    sh = wl.shape
+    touched = (synth.distinct_uniform(sh.n_experts, sh.top_k, T) + sh.n_shared) * synth.expert_bytes(sh)
+    return max(2, min(8, 1 + math.ceil(2.5 * L2_BYTES / touched)))
 
 
-def run_ours(args, rank, world, local):
-    import numpy as np
-    import torch
+class Pool:
+    """Device weight sets shared by every workload of one shape (drawn once)."""
 
-    from mxfp4_mixture_experts_rms_gb300 import moe, synth
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    wl = synth.WORKLOADS[WORKLOAD]
-    shape = wl.shape
-    H, K = shape.hidden, shape.top_k
-    sets = []
-    if wl.layers > 1:
-        # a stack of independently seeded blocks: layer l's fp32 output, cast to
-        # bf16, is layer l+1's input; the stack itself (~10 GB) is far larger than L2
-        layers = []
-        for l in range(wl.layers):
-            blk = synth.make_block(WORKLOAD, layer=l + 100 * rank)
-            plan = moe.Plan(shape, max_tokens=TOKENS).alloc_workspace().load_weights(moe.DeviceBlock(blk))
-            layers.append(dict(plan=plan, x=torch.empty((TOKENS, H), dtype=torch.int16, device="cuda"),
-                               out=torch.empty((TOKENS, H), dtype=torch.float32, device="cuda"),
-                               ids=torch.empty((TOKENS, K), dtype=torch.int32, device="cuda")))
-            del blk
-        xb = synth.make_tokens(WORKLOAD, TOKENS, H, layer=100 * rank)
-        layers[0]["x"].copy_(torch.from_numpy(xb.view(np.int16)))
-        sets.append(dict(blk=None, xb=xb, plan=layers[0]["plan"], x=layers[0]["x"], out=layers[-1]["out"],
-                         ids=layers[-1]["ids"], layers=layers))
-    for s in range(args.sets if wl.layers == 1 else 0):
-        layer = s + 100 * rank
-        blk = synth.make_block(WORKLOAD, layer=layer)
-        xb = synth.make_tokens(WORKLOAD, TOKENS, H, layer=layer)
-        plan = moe.Plan(shape, max_tokens=TOKENS).alloc_workspace().load_weights(moe.DeviceBlock(blk))
-        x = torch.from_numpy(xb.view(np.int16)).cuda()
-        out = torch.empty((TOKENS, H), dtype=torch.float32, device="cuda")
-        ids = torch.empty((TOKENS, K), dtype=torch.int32, device="cuda")
-        sets.append(dict(blk=blk if s == 0 else None, xb=xb if s == 0 else None, plan=plan, x=x, out=out, ids=ids))
-        del blk
-    def plans_of(d):
-        return [ly["plan"] for ly in d["layers"]] if "layers" in d else [d["plan"]]
+    def __init__(self):
+        self.sets = {}
 
-    def forward_set(d, stream):
-        if "layers" in d:
-            ls = d["layers"]
-            for l, ly in enumerate(ls):
-                ly["plan"].forward(ly["x"], ly["out"], ly["ids"], stream=stream)
-                if l + 1 < len(ls):
-                    moe.cast_f32_to_bf16(ly["out"], ls[l + 1]["x"], stream=stream)
-        else:
-            d["plan"].forward(d["x"], d["out"], d["ids"], stream=stream)
+    def experts(self, shape, i):
+        from mxfp4_mixture_experts_rms_gb300 import synth
+        key = (shape, i)
+        if key not in self.sets:
+            seed = 0x4D6F45 + 1009 * i + (0 if shape == synth.GPT_OSS else 500009)
+            d = synth.expert_matrices_device(shape, shape.n_experts, seed)
+            if shape.n_shared:
+                d["shared"] = synth.expert_matrices_device(shape, 1, seed + 7919)
+            self.sets[key] = d
+        return self.sets[key]
 
-    def step(i, stream):
-        forward_set(sets[i % len(sets)], stream)
 
-    def capture(n):
+class Workload:
+    """Plans, inputs and buffers of one (workload, tokens) measurement."""
+
+    def __init__(self, wid, T, pool, rank):
+        import numpy as np
+        import torch
+
+        from mxfp4_mixture_experts_rms_gb300 import moe, synth
+        self.wid, self.T = wid, T
+        self.wl = wl = synth.WORKLOADS[wid]
+        self.shape = sh = wl.shape
+        H, K = sh.hidden, sh.top_k
+        self.layers = wl.layers
+        n_sets = 1 if wl.layers > 1 else n_weight_sets(wid, T)
+        self.sets = []
+        for s in range(n_sets):
+            chain = []
+            for layer in range(wl.layers):
+                li = layer if wl.layers > 1 else s
+                blk = synth.make_router(wid, layer=li + 100 * rank)
+                ex = pool.experts(sh, li + 30 * rank)
+                blk.update({k: ex[k] for k in ("codes", "scales", "bias")})
+                if sh.n_shared:
+                    blk["shared"] = ex["shared"]
+                plan = moe.Plan(sh, max_tokens=T).alloc_workspace().load_weights(moe.DeviceBlock(blk))
+                chain.append(dict(plan=plan, x=torch.empty((T, H), dtype=torch.int16, device="cuda"),
+                                  out=torch.empty((T, H), dtype=torch.float32, device="cuda"),
+                                  ids=torch.empty((T, K), dtype=torch.int32, device="cuda")))
+            xb = synth.make_tokens(wid, T, H, layer=s + 100 * rank)
+            chain[0]["x"].copy_(torch.from_numpy(xb.view(np.int16)))
+            self.sets.append(dict(chain=chain, xb=xb))
+        self.path = self.sets[0]["chain"][0]["plan"].path_for(T)
+
+    def plans(self, d):
+        return [ly["plan"] for ly in d["chain"]]
+
+    def forward_set(self, d, stream):
+        from mxfp4_mixture_experts_rms_gb300 import moe
+        ls = d["chain"]
+        for i, ly in enumerate(ls):
+            ly["plan"].forward(ly["x"], ly["out"], ly["ids"], stream=stream)
+            if i + 1 < len(ls):
+                moe.cast_f32_to_bf16(ly["out"], ls[i + 1]["x"], stream=stream)
+
+    def step(self, i, stream):
+        self.forward_set(self.sets[i % len(self.sets)], stream)
+
+    def capture(self, n):
         """One CUDA graph holding n consecutive steps (launch overhead off the clock)."""
+        import torch
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             cs = torch.cuda.current_stream()
             for i in range(n):
-                step(i, cs)
+                self.step(i, cs)
         return g
 
+    def close(self):
+        for d in self.sets:
+            for p in self.plans(d):
+                p.close()
+        self.sets = []
+
+
+def measure(w, args, world, local, preroll_s):
+    """Time exactly args.steps steps (one graph replay) between barriers and
+    device synchronisations, then the same steps again with per-kernel events;
+    returns the numbers of one line."""
+    import torch
     st = torch.cuda.current_stream()
-    # per-set routing facts for the algorithmic byte counts
+    sh, T = w.shape, w.T
     facts = []
-    for i, d in enumerate(sets):
-        step(i, st)
+    for i, d in enumerate(w.sets):
+        w.forward_set(d, st)
         tot_f = [0, 0, 0]
-        for p in plans_of(d):
-            c = torch.empty(shape.n_experts, dtype=torch.int32, device="cuda")
+        for p in w.plans(d):
+            c = torch.empty(sh.n_experts, dtype=torch.int32, device="cuda")
             p.expert_counts(c)
             torch.cuda.synchronize()
-            tot_f = [a + b for a, b in zip(tot_f, algorithmic_bytes(shape, c.cpu().numpy(), TOKENS))]
+            tot_f = [a + b for a, b in zip(tot_f, algorithmic_bytes(sh, c.cpu().numpy(), T))]
         facts.append(tuple(tot_f))
-    n_blocks = len(plans_of(sets[0]))  # blocks per step (the stack's layers)
+        for p in w.plans(d):
+            assert p.device_status() == 0
     for i in range(args.warmup):
-        step(i, st)
+        w.step(i, st)
     torch.cuda.synchronize()
-    graph = capture(args.steps)
+    graph = w.capture(args.steps)
     graph.replay()
     torch.cuda.synchronize()
-    # pre-roll so that the clock samples see this load for about a second
     clocks = Clocks(local)
-    t_end = time.perf_counter() + (0.0 if args.quick else 1.0)
-    while time.perf_counter() < t_end:
+    t_end = time.perf_counter() + preroll_s
+    while time.perf_counter() < t_end:      # clock samples see this load before and during the timed region
         graph.replay()
         torch.cuda.synchronize()
-    # ---- timed region: exactly K steps (one graph replay)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -366,102 +366,29 @@ def run_ours(args, rank, world, local):
     ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
     ms = max_over_ranks(ms)
-    value = whole_job_rate(world, TOKENS, args.steps, ms)
+    del graph
+    r = {"ms": ms, "clocks": clk, "facts": facts}
     if args.quick:
-        if rank == 0:
-            print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "ms_per_step": ms / args.steps,
-                              "quick": True}), flush=True)
-        return
-
-    # ---- kernel durations over the same K steps: CUDA events the library
-    # records around each launch (captured into the graph as event nodes)
-    for d in sets:
-        for p in plans_of(d):
+        return r
+    # kernel durations over the same K steps: CUDA events the library records
+    # around each launch on the launching stream (event nodes in the graph)
+    for d in w.sets:
+        for p in w.plans(d):
             p.set_i("profile", 1)
-    pgraph = capture(args.steps)
+    pgraph = w.capture(args.steps)
     torch.cuda.synchronize()
     pgraph.replay()
     torch.cuda.synchronize()
-    tot = [0.0] * 4
-    cnt = [0] * 4
-    for d in sets:
-        for p in plans_of(d):
+    tot, cnt = [0.0] * 4, [0] * 4
+    for d in w.sets:
+        for p in w.plans(d):
             m, c = p.profile_read()
             tot = [a + b for a, b in zip(tot, m)]
             cnt = [a + b for a, b in zip(cnt, c)]
             p.set_i("profile", 0)
     del pgraph
-    avg_ms = [t / c if c else 0.0 for t, c in zip(tot, cnt)]
-    share = [t / sum(tot) for t in tot] if sum(tot) > 0 else [0.0] * 4
-    # per launch of each kernel (a step launches each once per block)
-    gu_bytes = sum(facts[i % len(sets)][0] for i in range(args.steps)) / args.steps / n_blocks
-    dn_bytes = sum(facts[i % len(sets)][1] for i in range(args.steps)) / args.steps / n_blocks
-    distinct = sum(facts[i % len(sets)][2] for i in range(args.steps)) / args.steps / n_blocks
-    hbm, bf16_peak, peak_kind = peaks()
-    dom = max(range(4), key=lambda k: tot[k])
-    dom_bytes = {1: gu_bytes, 2: dn_bytes}.get(dom, gu_bytes)
-    achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9 if avg_ms[dom] > 0 else 0.0
-    tr = traffic_record(KERNEL_SLOTS[dom], wl.name, TOKENS)
-    path = sets[0]["plan"].path_for(TOKENS)  # 1 GEMV decode path, 2 tensor-core grouped GEMM
-    step_bytes = (gu_bytes + dn_bytes) * n_blocks
-    step_gbs = step_bytes / (ms / args.steps / 1e3) / 1e9
-    routes = TOKENS * (K + shape.n_shared)
-    step_flops = 6.0 * routes * H * shape.expert_hidden * n_blocks
-    step_tflops = step_flops / (ms / args.steps / 1e3) / 1e12
-
-    # ---- end to end through the public API with host buffers
-    hx = [d["x"].cpu().pin_memory() for d in sets]
-    hout = [torch.empty((TOKENS, H), dtype=torch.float32).pin_memory() for _ in sets]
-    hids = [torch.empty((TOKENS, K), dtype=torch.int32).pin_memory() for _ in sets]
-
-    def e2e_step(i):
-        j = i % len(sets)
-        d = sets[j]
-        d["x"].copy_(hx[j], non_blocking=True)
-        forward_set(d, st)
-        hout[j].copy_(d["out"], non_blocking=True)
-        hids[j].copy_(d["ids"], non_blocking=True)
-
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record(st)
-    torch.cuda.synchronize()
-    e_ms = max_over_ranks(e0.elapsed_time(e1))
-    e2e = {"value": whole_job_rate(world, TOKENS, args.steps, e_ms), "unit": "tokens/s",
-           "h2d_bytes_per_step": TOKENS * H * 2, "d2h_bytes_per_step": TOKENS * H * 4 + TOKENS * K * 4}
-
-    if rank != 0:
-        return
-    cpu = None
-    if not args.no_cpu_baseline and world >= 1:
-        cpu = (cpu_baseline_stack(wl, sets[0]["xb"]) if n_blocks > 1
-               else cpu_baseline(sets[0]["blk"], sets[0]["xb"]))
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "tokens_per_step": TOKENS, "hidden": H, "n_experts": shape.n_experts,
-                   "top_k": K, "expert_hidden": shape.expert_hidden, "weights": "mxfp4 (e2m1 + e8m0/32)",
-                   "weight_sets": len(sets), "layers": n_blocks,
-                   "l2": ("inputs larger than L2: a stack of independently seeded layers" if n_blocks > 1 else
-                          "inputs larger than L2: steps rotate over independently seeded weight sets"),
-                   "distinct_experts_per_block": distinct,
-                   "algorithmic_bytes_per_step": step_bytes, "step_hbm_gbs": step_gbs,
-                   "algorithmic_flops_per_step": step_flops, "step_tflops": step_tflops,
-                   "step_tensor_frac_of_bf16_peak": step_tflops / peaks()[1],
-                   "parallelism": f"replicas x{world}"},
-        "roofline": roofline(path, dom, avg_ms[dom], achieved, hbm, bf16_peak, peak_kind, tr, dom_bytes,
-                             routes, H, shape.expert_hidden, TOKENS * shape.n_experts * H),
-        "kernels": {KERNEL_SLOTS[k]: {"avg_us": 1e3 * avg_ms[k], "share": share[k], "launches": cnt[k]}
-                    for k in range(4)},
-        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": int(sum(cnt)) + (n_blocks - 1) * args.steps,  # + the stack's casts between layers
-    }
-    print(json.dumps(line), flush=True)
+    r.update(tot=tot, cnt=cnt)
+    return r
 
 
 # fp32 FMA peak of the SIMT router: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz
@@ -477,9 +404,10 @@ def roofline(path, dom, avg_ms, achieved_gbs, hbm, bf16_peak, peak_kind, tr, dom
         flops = 2.0 * routes * (2 * F if dom == 1 else F) * H
         ach = flops / (avg_ms / 1e3) / 1e12 if avg_ms > 0 else 0.0
         return {"bound": "tensor", "kernel": KERNEL_SLOTS[dom], "achieved": ach, "peak": bf16_peak,
-                "peak_kind": peak_kind, "unit": "TFLOP/s", "frac": ach / bf16_peak,
+                "peak_kind": peak_kind + " bf16 (burst)", "unit": "TFLOP/s", "frac": ach / bf16_peak,
                 "traffic": tr["bytes_per_launch"] if tr else None,
-                "algorithmic_flops_per_launch": flops, "avg_launch_ms": avg_ms}
+                "algorithmic_flops_per_launch": flops, "avg_launch_ms": avg_ms,
+                "hbm_frac_of_algorithmic_bytes": (dom_bytes / (avg_ms / 1e3) / 1e9 / hbm) if avg_ms > 0 else 0.0}
     if path == 2 and dom == 0:
         flops = 2.0 * router_macs
         ach = flops / (avg_ms / 1e3) / 1e12 if avg_ms > 0 else 0.0
@@ -493,18 +421,172 @@ def roofline(path, dom, avg_ms, achieved_gbs, hbm, bf16_peak, peak_kind, tr, dom
             "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": avg_ms}
 
 
+def summarise(w, r, args, world):
+    """value, roofline, kernels and step figures of one measurement."""
+    sh, T = w.shape, w.T
+    H, F, K = sh.hidden, sh.expert_hidden, sh.top_k
+    steps = args.steps
+    ms = r["ms"]
+    n_blocks = w.layers
+    facts = r["facts"]
+    gu_bytes = sum(facts[i % len(facts)][0] for i in range(steps)) / steps / n_blocks
+    dn_bytes = sum(facts[i % len(facts)][1] for i in range(steps)) / steps / n_blocks
+    distinct = sum(facts[i % len(facts)][2] for i in range(steps)) / steps / n_blocks
+    step_bytes = (gu_bytes + dn_bytes) * n_blocks
+    step_s = ms / steps / 1e3
+    routes = T * (K + sh.n_shared)
+    step_flops = 6.0 * routes * H * F * n_blocks
+    hbm, bf16_peak, peak_kind = peaks()
+    out = {"value": whole_job_rate(world, T, steps, ms), "unit": "tokens/s", "ms_per_step": ms / steps,
+           "path": "gemv" if w.path == 1 else "grouped_gemm",
+           "distinct_experts_per_block": distinct, "algorithmic_bytes_per_step": step_bytes,
+           "step_hbm_gbs": step_bytes / step_s / 1e9, "step_frac_of_hbm": step_bytes / step_s / 1e9 / hbm,
+           "algorithmic_flops_per_step": step_flops, "step_tflops": step_flops / step_s / 1e12,
+           "step_frac_of_bf16_peak": step_flops / step_s / 1e12 / bf16_peak,
+           "binding_roof_frac": max(step_bytes / (hbm * 1e9), step_flops / (bf16_peak * 1e12)) / step_s,
+           "clocks": r["clocks"],
+           "gpu_launches": (launches_per_forward(w.path, T) * n_blocks + (n_blocks - 1)) * steps}
+    if "tot" in r:
+        tot, cnt = r["tot"], r["cnt"]
+        avg_ms = [t / c if c else 0.0 for t, c in zip(tot, cnt)]
+        share = [t / sum(tot) for t in tot] if sum(tot) > 0 else [0.0] * 4
+        dom = max(range(4), key=lambda k: tot[k])
+        dom_bytes = {1: gu_bytes, 2: dn_bytes}.get(dom, gu_bytes)
+        achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9 if avg_ms[dom] > 0 else 0.0
+        tr = traffic_record(KERNEL_SLOTS[dom], w.wl.name, T)
+        out["roofline"] = roofline(w.path, dom, avg_ms[dom], achieved, hbm, bf16_peak, peak_kind, tr, dom_bytes,
+                                   routes, H, F, T * sh.n_experts * H)
+        out["kernels"] = {KERNEL_SLOTS[k]: {"avg_us": 1e3 * avg_ms[k], "share": share[k], "launches": cnt[k]}
+                          for k in range(4)}
+    return out
+
+
+def e2e_rate(w, args, world):
+    """The same metric through the public API with host buffers: every step
+    copies its inputs from pinned host memory and reads the outputs back."""
+    import torch
+    st = torch.cuda.current_stream()
+    T, H, K = w.T, w.shape.hidden, w.shape.top_k
+    hx = [d["chain"][0]["x"].cpu().pin_memory() for d in w.sets]
+    hout = [torch.empty((T, H), dtype=torch.float32).pin_memory() for _ in w.sets]
+    hids = [torch.empty((T, K), dtype=torch.int32).pin_memory() for _ in w.sets]
+
+    def e2e_step(i):
+        j = i % len(w.sets)
+        d = w.sets[j]
+        d["chain"][0]["x"].copy_(hx[j], non_blocking=True)
+        w.forward_set(d, st)
+        hout[j].copy_(d["chain"][-1]["out"], non_blocking=True)
+        hids[j].copy_(d["chain"][-1]["ids"], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(st)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(e0.elapsed_time(e1))
+    return {"value": whole_job_rate(world, T, args.steps, e_ms), "unit": "tokens/s",
+            "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4 + T * K * 4}
+
+
+def cpu_baseline(wid, T, w):
+    """The oracle, as it stands, timed on the host cores for a bounded sample of
+    the workload's tokens (about 10-30 s): as many tokens as there are cores
+    (at most the step's), through every layer, on the seeded host-drawn weights
+    of the same recipe (weight generation off the clock)."""
+    import oracle
+    from mxfp4_mixture_experts_rms_gb300 import synth
+    cores = os.cpu_count() or 1
+    wl = synth.WORKLOADS[wid]
+    n = min(T, cores)
+    xs = w.sets[0]["xb"][:n]
+    el = 0.0
+    for layer in range(wl.layers):
+        blk = synth.make_block(wid, layer=layer)
+        if layer == 0:
+            oracle.moe_forward(blk, xs[:1], nthreads=1)
+        t0 = time.perf_counter()
+        out = oracle.moe_forward(blk, xs, nthreads=n)["out"]
+        el += time.perf_counter() - t0
+        xs = synth.f32_to_bf16_bits(out)
+        del blk
+    return {"value": n / el, "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "sample": f"{n} of the {T} tokens of one step through all {wl.layers} layer(s), {el:.1f} s of oracle time"}
+
+
+def run_ours(args, rank, world, local, wid, T):
+    import torch
+
+    from mxfp4_mixture_experts_rms_gb300 import moe, synth
+    torch.cuda.set_device(local)
+    moe.load()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    pool = Pool()
+    wl = synth.WORKLOADS[wid]
+    w = Workload(wid, T, pool, rank)
+    r = measure(w, args, world, local, 0.0 if args.quick else 1.0)
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": whole_job_rate(world, T, args.steps, r["ms"]),
+                              "unit": "tokens/s", "ms_per_step": r["ms"] / args.steps, "quick": True,
+                              "config": {"workload": wl.name, "tokens_per_step": T}}), flush=True)
+        return
+    head = summarise(w, r, args, world)
+    e2e = e2e_rate(w, args, world)
+    extras = {}
+    if not args.no_extras:
+        for (ew, eT) in EXTRAS:
+            if (ew, eT) == (wid, T):
+                continue
+            x = Workload(ew, eT, pool, rank)
+            xr = measure(x, args, world, local, 0.5)
+            s = summarise(x, xr, args, world)
+            s["config"] = workload_config(x.wl, eT)
+            s["weight_sets"] = len(x.sets)
+            extras[f"{synth.WORKLOADS[ew].name} x{eT}"] = s
+            x.close()
+            torch.cuda.synchronize()
+    if rank != 0:
+        return
+    cpu = None if args.no_cpu_baseline else cpu_baseline(wid, T, w)
+    cfg = workload_config(wl, T)
+    cfg.update({"weight_sets": len(w.sets), "parallelism": f"replicas x{world}",
+                "l2": ("inputs larger than L2: a stack of independently seeded layers (~10 GB)" if w.layers > 1 else
+                       "inputs larger than L2: steps rotate over independently seeded weight sets "
+                       "(> 2.5 x L2 touched between two uses of a set)"),
+                "weights_drawn": "router/gamma/bias by the host recipe; expert matrices on the device, same "
+                                 "distributions"})
+    for k in ("distinct_experts_per_block", "algorithmic_bytes_per_step", "step_hbm_gbs", "step_frac_of_hbm",
+              "algorithmic_flops_per_step", "step_tflops", "step_frac_of_bf16_peak", "binding_roof_frac", "path"):
+        cfg[k] = head[k]
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "roofline": head.get("roofline"), "kernels": head.get("kernels"),
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": head["clocks"], "gpu_launches": head["gpu_launches"],
+        "configs": extras,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_mx_fp4_quantize(args):
     """The FP4 activation encoder alone: bf16 [rows][cols] -> MXFP4 codes + E8M0
     scales, timed with CUDA events on the launching stream over input sets that
     together exceed twice the L2, so every launch reads from HBM."""
-    import numpy as np
     import torch
     from mxfp4_mixture_experts_rms_gb300 import moe
     moe.load()
     R, Cc = args.rows, args.cols
     n = R * Cc
     algo = n * 2 + n // 2 + n // 32
-    n_sets = max(2, -(-2 * 129 * 2 ** 20 // algo) + 1)
+    n_sets = max(2, -(-2 * L2_BYTES // algo) + 1)
     g = torch.Generator(device="cuda").manual_seed(0x4D6F45)
     xs = [(torch.randn((R, Cc), device="cuda", generator=g) * 4).to(torch.bfloat16).view(torch.int16)
           for _ in range(n_sets)]
@@ -555,14 +637,13 @@ def main():
         run_mx_fp4_quantize(args)
         return
     from mxfp4_mixture_experts_rms_gb300 import synth
-    global WORKLOAD, TOKENS
-    WORKLOAD = args.workload
-    TOKENS = args.tokens or max(synth.WORKLOADS[WORKLOAD].tokens)
+    wid = args.workload
+    T = args.tokens or (HEADLINE[1] if wid == HEADLINE[0] else max(synth.WORKLOADS[wid].tokens))
     rank, world, local = dist_env()
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        run_reference(args, rank, world, wid, T)
         return
-    run_ours(args, rank, world, local)
+    run_ours(args, rank, world, local, wid, T)
 
 
 if __name__ == "__main__":

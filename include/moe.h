@@ -75,16 +75,21 @@ typedef struct {
                                                    read only when n_shared_experts = 1 */
 } moe_weights;
 
-/* Create a plan for one block shape.
+/* Create a plan for one block shape (goosedump gpt_oss.rs, constants block:
+ * HIDDEN, EXPERTS, EXPERTS_PER_TOKEN, EXPERT_HIDDEN, SWIGLU_ALPHA, SWIGLU_LIMIT;
+ * ds4.c DS4_SHAPE_FLASH `expert_weight_scale` for weight_scale).
  * hidden (H) and expert_hidden (F) must be positive multiples of 32;
  * 1 <= top_k <= min(n_experts, 8); 1 <= n_experts <= 256; swiglu_limit > 0.
  * Defaults: rms_eps 1e-5 (goosedump gpt_oss.rs EPSILON), no shared expert,
  * max_tokens 4096.  Returns NULL (see moe_last_error) on bad arguments. */
 moe_plan *moe_plan_create(int hidden, int expert_hidden, int n_experts, int top_k,
                           float swiglu_alpha, float swiglu_limit, float weight_scale);
+/* Free the plan and the scale copy it owns (see moe_load_weights); borrowed
+ * weights and workspace stay the caller's.  NULL is a no-op. */
 void moe_plan_destroy(moe_plan *plan);
 
-/* Integer options:
+/* Integer options (no passage of the pages defines these knobs; each names
+ * the passage its behaviour follows):
  *   "n_shared_experts"  0 or 1: an always-on expert added with weight 1
  *                       (ds4.c DS4_SHAPE_FLASH n_expert_shared)
  *   "max_tokens"        largest token count per forward (sizes the workspace),
@@ -92,16 +97,26 @@ void moe_plan_destroy(moe_plan *plan);
  *   "decode_max_tokens" forwards with tokens <= this use the GEMV decode path,
  *                       larger ones the tensor-core grouped-GEMM path; -1
  *                       (default): 60 for up to 64 experts, 8 above
+ *                       (goosedump gpt_oss.rs: `mixture_of_experts` for one
+ *                       token, `mixture_of_experts_batch` for a batch)
  *   "path"              0 auto, 1 force decode, 2 force prefill (testing)
  *   "router_exact"      1: compute every router logit in fp64 (testing)
+ *   "test_stall_wait"   1: test hook: the decode gate/up kernel first waits
+ *                       on a barrier nothing completes, so its bounded wait
+ *                       (about 2 s) runs out; the forward then reports
+ *                       MOE_EDEVICE through moe_get_device_status (detail 59)
+ *                       and its outputs are void.  0 (default): off
  *   "profile"           1: time each kernel launch with CUDA events (see
  *                       moe_profile_read); 0: off (default)
  * Options that change the workspace size must be set before moe_set_workspace. */
 int moe_plan_set_i(moe_plan *plan, const char *key, long long value);
-/* Floating options: "rms_eps". */
+/* Floating options: "rms_eps" (goosedump gpt_oss.rs EPSILON; ds4.c
+ * `rms_norm_weight` eps). */
 int moe_plan_set_f(moe_plan *plan, const char *key, double value);
 /* Which projection kernels a forward of `tokens` tokens would run: 1 the GEMV
- * decode path, 2 the tensor-core grouped-GEMM path (the "path" and
+ * decode path (goosedump gpt_oss.rs `mixture_of_experts`: one matvec pair per
+ * selected expert), 2 the tensor-core grouped-GEMM path (`expert_batch_output`:
+ * the routed rows of one expert as a matrix) (the "path" and
  * "decode_max_tokens" options and the shape decide; the choice also needs
  * the weights loaded, since the grouped GEMM's tensor maps are built then).
  * Negative status on error (NULL plan, weights not loaded, no path for the
@@ -109,18 +124,29 @@ int moe_plan_set_f(moe_plan *plan, const char *key, double value);
 int moe_plan_path_for(const moe_plan *plan, int tokens);
 
 /* Bytes of device workspace a forward of up to max_tokens tokens needs
- * (max_tokens <= 0: the plan's max_tokens).  0 on error. */
+ * (max_tokens <= 0: the plan's max_tokens; above 65535 refused).  0 on error.
+ * No passage of the pages corresponds: the pages allocate per call on the
+ * host; a caller-owned workspace keeps the forward allocation-free. */
 size_t moe_workspace_bytes(const moe_plan *plan, int max_tokens);
 /* Hand the plan a device buffer of at least moe_workspace_bytes() bytes,
- * 256-byte aligned.  The plan borrows it (the caller frees it). */
+ * 256-byte aligned.  The plan borrows it (the caller frees it).  No passage
+ * of the pages corresponds (see moe_workspace_bytes).  Synchronises the
+ * current device (it clears the status word and the routing tickets). */
 int moe_set_workspace(moe_plan *plan, void *dev_ptr, size_t bytes);
 
-/* Register the weights (device pointers, borrowed).  Checks pointer
- * alignment (16 bytes) and scans every scale tensor for the NaN code 0xFF
- * (this one call synchronises the current device).  Must precede moe_forward. */
+/* Register the weights (device pointers, borrowed), as goosedump gpt_oss.rs's
+ * expert tensor validation checks them (`ffn_{gate,up,down}_exps` Mxfp4 of
+ * dims [EXPERT_HIDDEN, HIDDEN, EXPERTS], biases F32, router F32 + bias): here
+ * pointer alignment (16 bytes) and every scale tensor scanned for the NaN
+ * code 0xFF (this one call synchronises the current device).  It also builds
+ * the plan's own copy of the scales repacked for the grouped GEMM (device
+ * memory the plan owns until moe_plan_destroy).  Must precede moe_forward. */
 int moe_load_weights(moe_plan *plan, const moe_weights *w);
 
-/* out[T][H] (float) = x + MoE(x) for x bf16 [T][H]; route_ids_out int32
+/* The block (turbospark-runtime gptoss/mod.rs, module doc comment; goosedump
+ * gpt_oss.rs `mixture_of_experts`, `mixture_of_experts_batch`,
+ * `mix_expert_outputs`, `top_experts`):
+ * out[T][H] (float) = x + MoE(x) for x bf16 [T][H]; route_ids_out int32
  * [T][top_k] (may be NULL; 4-byte aligned) gets the selected experts of each
  * token in descending-logit order.  x and out (16-byte aligned) must not
  * alias.  tokens = 0 is a no-op.  MOE_EINVAL on NULL, misaligned or aliasing
@@ -128,16 +154,24 @@ int moe_load_weights(moe_plan *plan, const moe_weights *w);
  * Enqueue only; graph-capturable; stream is a cudaStream_t (NULL = legacy). */
 int moe_forward(moe_plan *plan, const uint16_t *x, int tokens, float *out,
                 int32_t *route_ids_out, void *stream);
-/* As moe_forward, also writing the route weights [T][top_k] (float, 4-byte
+/* As moe_forward (same passages), also writing the route weights
+ * (goosedump gpt_oss.rs `softmax` over the selected logits) [T][top_k] (float, 4-byte
  * aligned) and the normalised activations x_hat [T][H] (bf16, 16-byte aligned,
  * not overlapping x) when those pointers are non-NULL. */
 int moe_forward_ex(moe_plan *plan, const uint16_t *x, int tokens, float *out,
                    int32_t *route_ids_out, float *route_w_out, uint16_t *xhat_out, void *stream);
 
-/* Per-expert token counts of the last forward: int32 [n_experts] (device), enqueued. */
+/* Per-expert token counts of the last moe_forward / moe_forward_ex on this
+ * plan (goosedump gpt_oss.rs ExpertRouteProfile `counts`, the per-layer
+ * selection histogram): int32 [n_experts] (device), enqueued.  Reads the
+ * plan's workspace: moe_forward_noalloc calls are not seen (their counts
+ * live in the shared static array and are not kept). */
 int moe_get_expert_counts(const moe_plan *plan, int32_t *dev_counts_out, void *stream);
-/* Token->expert grouping of the last moe_forward / moe_forward_ex (device
- * outputs, enqueued): offsets [n_experts + n_shared + 1] (exclusive prefix
+/* Token->expert grouping of the last moe_forward / moe_forward_ex (goosedump
+ * gpt_oss.rs `mixture_of_experts_batch`: `routes_by_expert`, routes appended
+ * per expert in token order; `route_output_index`: one location per route)
+ * (device outputs, enqueued; moe_forward_noalloc calls are not seen, as for
+ * moe_get_expert_counts): offsets [n_experts + n_shared + 1] (exclusive prefix
  * sums of the counts); perm_token / perm_slot: the routes of each expert in
  * ascending (token, slot) order, the shared expert last with slot top_k.
  * Both perm arrays must hold max_tokens * (top_k + n_shared) int32 entries
@@ -145,12 +179,15 @@ int moe_get_expert_counts(const moe_plan *plan, int32_t *dev_counts_out, void *s
  * offsets[n_experts + n_shared] on are unspecified. */
 int moe_get_permutation(const moe_plan *plan, int32_t *offsets, int32_t *perm_token,
                         int32_t *perm_slot, void *stream);
-/* Dequantise one expert matrix (which: 0 gate, 1 up, 2 down; expert = n_experts
+/* Dequantise one expert matrix (ds4.c `dsv4_e2m1fn_value_cpu`: the E2M1 table,
+ * times the block's E8M0 scale 2^(s-127)) (which: 0 gate, 1 up, 2 down; expert = n_experts
  * selects the shared expert) to float [rows][cols] on the device (dev_out
  * 4-byte aligned, rows x cols floats).  Test hook. */
 int moe_debug_dequant(const moe_plan *plan, int expert, int which, float *dev_out, void *stream);
 
-/* Kernel timing for benchmarks.  After moe_plan_set_i(plan, "profile", 1)
+/* Kernel timing for benchmarks (no passage of the pages corresponds; the
+ * pages' own timers are turbospark-runtime gptoss/mod.rs's per-phase GPU
+ * nanoseconds).  After moe_plan_set_i(plan, "profile", 1)
  * every forward records a CUDA event pair around each of its kernel launches,
  * on the forward's stream.  moe_profile_read synchronises on those events and
  * returns, per kernel slot (0 routing + permutation, 1 gate/up + SwiGLU,
@@ -160,7 +197,15 @@ int moe_debug_dequant(const moe_plan *plan, int expert, int which, float *dev_ou
 int moe_profile_read(moe_plan *plan, double *total_ms, int *launches, int n_slots);
 
 /* Synchronises the stream and returns the device-side status of the plan's
- * kernels in *status (0 = fine); clears it. */
+ * kernels in *status (0 = fine; 1 = a bounded wait ran out, 2 = a route out
+ * of range) and clears it: the plan's workspace word and, when this plan has
+ * called moe_forward_noalloc on the current device, the static array's word
+ * (shared by every no-alloc call on that device).  A status stays set until
+ * read here, and outputs of forwards run while it is set are void.
+ * MOE_EDEVICE when a word was set (message: status and detail), MOE_ENOTREADY
+ * when the plan has neither a workspace nor a no-alloc call on this device.
+ * (goosedump gpt_oss.rs `ensure!` checks: every violation is an error the
+ * caller sees, here also those found on the device.) */
 int moe_get_device_status(moe_plan *plan, int *status, void *stream);
 
 /* moe_forward without any device allocation, for callers that may not
@@ -178,6 +223,10 @@ int moe_get_device_status(moe_plan *plan, int *status, void *stream);
  *  - All calls share the array and it keeps the last call's contents; each
  *    call clears the parts that must start at zero.  Calls that overlap on
  *    the GPU (other streams, other plans, other threads) race on it.
+ *  - The kernels' status word is at the start of the array: read it with
+ *    moe_get_device_status (on this plan, this device current).
+ *    moe_get_expert_counts and moe_get_permutation do not see these calls.
+ *  - tokens above 65535 are rejected with MOE_ENOMEM.
  *  - Calls no cudaMalloc, cudaFree or allocating library routine; weights,
  *    x, out and route_ids_out are as for moe_forward. */
 int moe_forward_noalloc(moe_plan *plan, const uint16_t *x, int tokens, float *out,
@@ -185,7 +234,8 @@ int moe_forward_noalloc(moe_plan *plan, const uint16_t *x, int tokens, float *ou
 
 /* dst[i] = src[i] rounded to bf16 (nearest, ties to even), i < n, enqueued on
  * `stream`: the residual stream between stacked blocks (a block's fp32 output
- * becomes the next block's bf16 input).  src fp32 and dst uint16 are device
+ * becomes the next block's bf16 input; goosedump gpt_oss.rs `forward`, the
+ * layer loop's `vector_add` of the MoE output into the hidden state).  src fp32 and dst uint16 are device
  * pointers, 16-byte aligned, not overlapping.  NaN inputs give a quiet NaN.
  * MOE_EINVAL on NULL/misaligned pointers, MOE_ECUDA on a launch error. */
 int moe_cast_f32_to_bf16(const float *src, uint16_t *dst, size_t n, void *stream);
@@ -212,7 +262,8 @@ int moe_cast_f32_to_bf16(const float *src, uint16_t *dst, size_t n, void *stream
 int moe_mx_quantize_fp4(const uint16_t *x, size_t rows, size_t cols, uint8_t *codes, uint8_t *scales,
                         void *stream);
 
-/* Text of the last failure on this thread ("" if none). */
+/* Text of the last failure on this thread ("" if none) (goosedump gpt_oss.rs:
+ * every `ensure!` carries a message). */
 const char *moe_last_error(void);
 
 #ifdef __cplusplus

@@ -52,6 +52,8 @@ struct moe_plan {
     int decode_max_tokens = -1;  // -1: chosen from the shape (auto_decode_max)
     int path = 0;
     int router_exact = 0;
+    int stall_test = 0;              // test hook: the gate/up GEMV waits on a barrier nothing completes
+    int noalloc_dev = -1;            // device of this plan's last moe_forward_noalloc (-1: none)
     void *ws_ptr = nullptr;
     size_t ws_bytes = 0;
     Workspace ws{};
@@ -112,8 +114,9 @@ int choose_path(const moe_plan *p, int tokens, bool *decode, int *nt, int *tile_
 }
 
 int max_tiles_for(const moe_plan *p, int T) {
-    const int R = T * (p->bp.K + p->bp.n_shared);
-    return R / 8 + 2 * (p->bp.E + p->bp.n_shared) + 8;
+    // T <= kMaxTokens and K + n_shared <= 9 keep this far inside int
+    const size_t R = (size_t)T * (p->bp.K + p->bp.n_shared);
+    return (int)(R / 8 + 2 * (size_t)(p->bp.E + p->bp.n_shared) + 8);
 }
 
 // Lays the workspace out for T tokens; with base == nullptr only sizes it.
@@ -184,6 +187,40 @@ int check_matrix(const moe_mxfp4_matrix &m, const char *name) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Forward without any allocation: the workspace lives in a static device array.
+// Some callers cannot allocate device memory -- a runtime that owns every byte
+// of device memory through its own pool and forbids cudaMalloc, or code that
+// must not risk the implicit device synchronisation an allocation can cause.
+// For them the same kernels run on a fixed scratch array that every GPU
+// loading this library reserves once, at module load, until exit.  Its first
+// 256 bytes are the status word of the kernels run on it (read and cleared by
+// moe_get_device_status); the workspace is carved from the rest.
+#define MOE_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define MOE_NOALLOC_STATUS_BYTES 256u
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[256];  // device address of g_noalloc_scratch, per device ordinal
+
+// The device address of the static scratch array on device `dev`, looked up
+// once per device with that device current (in host code the array's name is
+// only a host-side stand-in, not a device address).
+int noalloc_scratch_addr(int dev, void **out) {
+    if (dev < 0 || dev >= 256) return fail(MOE_EINVAL, "moe_forward_noalloc: device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: cudaGetSymbolAddress");
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+}  // namespace
+
 extern "C" {
 
 const char *moe_last_error(void) { return g_err; }
@@ -252,6 +289,8 @@ int moe_plan_set_i(moe_plan *p, const char *key, long long v) {
         p->path = (int)v;
     } else if (!strcmp(key, "router_exact")) {
         p->router_exact = v ? 1 : 0;
+    } else if (!strcmp(key, "test_stall_wait")) {
+        p->stall_test = v ? 1 : 0;
     } else if (!strcmp(key, "profile")) {
         if (v && p->ev.empty()) {
             p->ev.resize(2 * moe_plan::kMaxRec);
@@ -293,6 +332,10 @@ size_t moe_workspace_bytes(const moe_plan *p, int max_tokens) {
         return 0;
     }
     int T = max_tokens > 0 ? max_tokens : p->max_tokens;
+    if (T > kMaxTokens) {
+        fail(MOE_EINVAL, "max_tokens %d > %d", T, kMaxTokens);
+        return 0;
+    }
     return carve(p, T, nullptr, nullptr);
 }
 
@@ -423,12 +466,12 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     mark(1, true);
     if (!decode) e = launch_gather(b, p->ws, tokens, p->pf_f16, st);
     if (e == cudaSuccess)
-        e = decode ? launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
+        e = decode ? launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, p->stall_test, st)
                    : launch_prefill_stage(b, p->ws, p->gate, p->up, true, tokens, p->maps.gateup, p->pf_f16, st);
     mark(1, false);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
     mark(2, true);
-    e = decode ? launch_decode_stage(b, p->ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, st)
+    e = decode ? launch_decode_stage(b, p->ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, 0, st)
                : launch_prefill_stage(b, p->ws, p->down, p->down, false, tokens, p->maps.down, p->pf_f16, st);
     mark(2, false);
     if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
@@ -500,51 +543,36 @@ int moe_profile_read(moe_plan *p, double *total_ms, int *launches, int n_slots) 
 
 int moe_get_device_status(moe_plan *p, int *status, void *stream) {
     if (!p || !status) return fail(MOE_EINVAL, "NULL argument");
-    if (!p->have_ws) return fail(MOE_ENOTREADY, "no workspace");
+    int32_t *words[2] = {nullptr, nullptr};
+    int nw = 0;
+    if (p->have_ws) words[nw++] = p->ws.status;
+    if (p->noalloc_dev >= 0) {
+        int dev = -1;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_get_device_status");
+        void *base = nullptr;
+        if (dev == p->noalloc_dev && noalloc_scratch_addr(dev, &base) == MOE_OK)
+            words[nw++] = static_cast<int32_t *>(base);  // the static array's status word
+    }
+    if (!nw) return fail(MOE_ENOTREADY, "no workspace and no moe_forward_noalloc on the current device");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int32_t h[4] = {0, 0, 0, 0};
-    cudaError_t e = cudaMemcpyAsync(h, p->ws.status, 16, cudaMemcpyDeviceToHost, st);
+    int32_t h[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < nw && e == cudaSuccess; i++) e = cudaMemcpyAsync(h[i], words[i], 16, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(p->ws.status, 0, 16, st);
+    for (int i = 0; i < nw && e == cudaSuccess; i++) e = cudaMemsetAsync(words[i], 0, 16, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "moe_get_device_status");
-    *status = h[0];
-    if (h[0]) return fail(MOE_EDEVICE, "device status %d (detail %d)", h[0], h[1]);
+    *status = 0;
+    for (int i = 0; i < nw; i++)
+        if (h[i][0]) {
+            *status = h[i][0];
+            return fail(MOE_EDEVICE, "device status %d (detail %d)%s", h[i][0], h[i][1],
+                        words[i] == p->ws.status && p->have_ws ? "" : " in moe_forward_noalloc");
+        }
     return MOE_OK;
 }
 
-// ---------------------------------------------------------------------------
-// Forward without any allocation: the workspace lives in a static device array.
-// Some callers cannot allocate device memory -- a runtime that owns every byte
-// of device memory through its own pool and forbids cudaMalloc, or code that
-// must not risk the implicit device synchronisation an allocation can cause.
-// For them the same kernels run on a fixed scratch array that every GPU
-// loading this library reserves once, at module load, until exit.
-#define MOE_NOALLOC_SCRATCH_BYTES (16u << 20)
-static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
-
-namespace {
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[256];  // device address of g_noalloc_scratch, per device ordinal
-
-// Once per device, with that device current: the device address of the array
-// (the name g_noalloc_scratch is only a host-side stand-in in host code).
-int noalloc_scratch(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: cudaGetDevice");
-    if (dev < 0 || dev >= 256) return fail(MOE_EINVAL, "moe_forward_noalloc: device ordinal %d out of range", dev);
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: cudaGetSymbolAddress");
-        g_noalloc_ptr[dev] = ptr;
-    }
-    *out = g_noalloc_ptr[dev];
-    return MOE_OK;
-}
-}  // namespace
 
 int moe_cast_f32_to_bf16(const float *src, uint16_t *dst, size_t n, void *stream) {
     if (n == 0) return MOE_OK;
@@ -580,39 +608,45 @@ int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, 
     if (!x || !out) return fail(MOE_EINVAL, "NULL x or out");
     if (!p->have_w) return fail(MOE_ENOTREADY, "moe_load_weights has not been called");
     if (!aligned16(x) || !aligned16(out)) return fail(MOE_EINVAL, "x and out must be 16-byte aligned");
+    if (tokens > kMaxTokens) return fail(MOE_ENOMEM, "moe_forward_noalloc: tokens %d > %d", tokens, kMaxTokens);
     const BlockParams &b = p->bp;
     const char *xb = reinterpret_cast<const char *>(x), *ob = reinterpret_cast<const char *>(out);
     if (xb < ob + (size_t)tokens * b.H * 4 && ob < xb + (size_t)tokens * b.H * 2)
         return fail(MOE_EINVAL, "x and out must not alias");
     if (int rc0 = check_outputs(b, tokens, x, ids_out, nullptr, nullptr)) return rc0;
     const size_t need = carve(p, tokens, nullptr, nullptr);
-    if (need > MOE_NOALLOC_SCRATCH_BYTES)
+    if (need > MOE_NOALLOC_SCRATCH_BYTES - MOE_NOALLOC_STATUS_BYTES)
         return fail(MOE_ENOMEM, "moe_forward_noalloc: %d tokens need %zu bytes of scratch, the static array holds %u",
-                    tokens, need, MOE_NOALLOC_SCRATCH_BYTES);
-    if (tokens > kMaxTokens) return fail(MOE_ENOMEM, "tokens %d > %d", tokens, kMaxTokens);
-    void *base = nullptr;
-    int rc = noalloc_scratch(&base);
-    if (rc != MOE_OK) return rc;
-    Workspace ws;
-    carve(p, tokens, static_cast<char *>(base), &ws);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // the array keeps the previous call's contents: the status word and the
-    // routing kernel's tickets must start at zero
-    cudaError_t e = cudaMemsetAsync(ws.status, 0, 16, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ws.tickets, 0, sizeof(uint32_t) * route_ticket_count(tokens), st);
-    if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: clearing scratch");
+                    tokens, need, MOE_NOALLOC_SCRATCH_BYTES - MOE_NOALLOC_STATUS_BYTES);
     bool decode = false;
     int nt = 1, tile_rows = 0;
     if (int rc2 = choose_path(p, tokens, &decode, &nt, &tile_rows)) return rc2;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: cudaGetDevice");
+    void *base = nullptr;
+    if (int rc = noalloc_scratch_addr(dev, &base)) return rc;
+    Workspace ws;
+    carve(p, tokens, static_cast<char *>(base) + MOE_NOALLOC_STATUS_BYTES, &ws);
+    // the status word sits at the start of the array, where moe_get_device_status
+    // finds it whatever the token count; like the workspace's, it is sticky
+    // until read (a failure stays visible, later results are void until then)
+    ws.status = static_cast<int32_t *>(base);
+    p->noalloc_dev = dev;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the array keeps the previous call's contents, and the routing kernel's
+    // tickets (whose place depends on the token count) must start at zero
+    e = cudaMemsetAsync(ws.tickets, 0, sizeof(uint32_t) * route_ticket_count(tokens), st);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: clearing scratch");
     e = launch_route(b, ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, nullptr, nullptr,
                      tile_rows, p->router_exact, decode ? 0 : 1, st);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     if (!decode) e = launch_gather(b, ws, tokens, p->pf_f16, st);
     if (e == cudaSuccess)
-        e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, st)
+        e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, p->stall_test, st)
                    : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, p->pf_f16, st);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
-    e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, st)
+    e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, 0, st)
                : launch_prefill_stage(b, ws, p->down, p->down, false, tokens, p->maps.down, p->pf_f16, st);
     if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
     e = launch_combine(b, ws, x, tokens, out, st);

@@ -177,9 +177,12 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
                          int T, int32_t *ids_out, float *rw_out, uint16_t *xhat_out, int tile_rows,
                          int router_exact, int store_mma, cudaStream_t st);
 // x_bf16 / h_bf16: the gate/up (down) GEMV reads bf16 activations instead of fp16.
+// stall (test hook, gate/up only): the consumers first wait on a barrier that
+// nothing completes, so the bounded wait runs out and the kernel reports
+// MOE_DEV_WAIT_TIMEOUT (detail 59) and drains.
 cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
                                 const MatPtrs &a1, bool gateup, int T, int nt, bool x_bf16, bool h_bf16,
-                                cudaStream_t st);
+                                int stall, cudaStream_t st);
 // dst = bf16_rne(src), n elements (any n; 16-byte aligned pointers)
 cudaError_t launch_cast_bf16(const float *src, uint16_t *dst, size_t n, cudaStream_t st);
 cudaError_t launch_mx_fp4_quantize(const uint16_t *x, size_t n_blocks, uint8_t *codes, uint8_t *scales,

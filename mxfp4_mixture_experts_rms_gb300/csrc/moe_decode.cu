@@ -62,6 +62,7 @@ struct DecodeArgs {
     int rows;        // output rows: F for gate/up, H for down
     int stages;      // shared-memory ring depth
     int h_bf16;      // gate/up: write h as bf16 (else fp16)
+    int stall;       // test hook: consumers first wait on a barrier nothing completes
 };
 
 // f16x2 holding two E2M1 values (0, +-0.5 .. +-6) -> the same values as bf16x2.
@@ -140,6 +141,22 @@ __device__ __forceinline__ bool dec_mbar_wait(uint64_t *b, uint32_t parity, int3
         }
     }
 }
+// Wait for copies already issued to land before the CTA's shared memory goes:
+// only the time limit ends it (a failure reported elsewhere does not).
+__device__ __forceinline__ void dec_mbar_drain(uint64_t *b, uint32_t parity, int32_t *status) {
+    if (dec_mbar_try(b, parity)) return;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (;;) {
+        if (dec_mbar_try(b, parity)) return;
+        uint64_t t1;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+        if (t1 - t0 > kDecWaitNs) {
+            set_device_error(status, MOE_DEV_WAIT_TIMEOUT, 58);
+            return;
+        }
+    }
+}
 __device__ __forceinline__ void dec_arrive(uint64_t *b) {
     asm volatile("{ .reg .b64 t; mbarrier.arrive.shared::cta.b64 t, [%0]; }" ::"r"(smem_addr(b)) : "memory");
 }
@@ -181,8 +198,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     static_assert(!GATEUP || NM == 2, "gate/up items hold both matrices");
     constexpr int IR = GATEUP ? 16 : 16 * NM;  // output rows per item
     extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 4];
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 5];
     uint64_t *full = bars, *empty = bars + kMaxStages, *redfull = bars + 2 * kMaxStages, *redempty = redfull + 2;
+    uint64_t *never = redempty + 2;  // completed by nobody (the stall test hook waits on it)
     const int K = a.Kdim, nb = K / 32, S = a.stages;
     const DecGeom geo(K, NM);
     float *red = reinterpret_cast<float *>(dsm + (size_t)S * geo.stage);
@@ -197,6 +215,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&redfull[i])), "r"(kCW));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&redempty[i])));
         }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(never)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -247,12 +266,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&full[s])) : "memory");
             if (lane == 0) MOE_DEC_MARK(0, k);
         };
+        int issued = 0;
         for (int k = 0; k < n; k++) {
             if (k >= S && !dec_mbar_wait(&empty[k % S], ((k / S) - 1) & 1, status, 51)) break;
             issue(k);
+            issued++;
         }
-        // the copies still in flight must land before this warp exits
-        for (int k = max(0, n - S); k < n; k++) dec_mbar_wait(&full[k % S], (k / S) & 1, status, 52);
+        // the copies still in flight must land before this warp exits: the
+        // last S issued (each earlier one was consumed before its stage was
+        // refilled), waited for even when the kernel is failing
+        for (int k = max(0, issued - S); k < issued; k++) dec_mbar_drain(&full[k % S], (k / S) & 1, status);
         return;
     }
     if (warp == kEpi) {
@@ -330,6 +353,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     }
 
     // -------------------------------------------------------------- consumers
+    // test hook: a bounded wait that runs out (nothing completes `never`); the
+    // status word then stops the producer and the epilogue, which drain and exit
+    if (GATEUP && a.stall && !dec_mbar_wait(never, 0, status, 59)) return;
     const int npairs = (nb + 1) >> 1;
     // activations of pair p = warp + kCW*i: block 2p+bb, token column nn*8 + g,
     // elements 8*t4 .. 8*t4+7 of the block (zero past the end of K or of the tile)
@@ -600,17 +626,17 @@ bool decode_supported(const BlockParams &bp) {
 }
 
 cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0, const MatPtrs &a1,
-                                bool gateup, int T, int nt, bool x_bf16, bool h_bf16, cudaStream_t st) {
+                                bool gateup, int T, int nt, bool x_bf16, bool h_bf16, int stall, cudaStream_t st) {
     const int R = T * (bp.K + bp.n_shared);
     // upper bound on the tile count: each expert's last tile may be partial
     int tiles = (R + 8 * nt - 1) / (8 * nt) + bp.E + bp.n_shared;
     if (tiles > ws.max_tiles) tiles = ws.max_tiles;
     if (gateup) {
-        DecodeArgs gu{bp, ws, a0, a1, bp.H, bp.F, 0, h_bf16 ? 1 : 0};
+        DecodeArgs gu{bp, ws, a0, a1, bp.H, bp.F, 0, h_bf16 ? 1 : 0, stall};
         const int items = tiles * (bp.F / 16);
         return nt == 1 ? launch_bf<true, 1, 2>(gu, x_bf16, items, st) : launch_bf<true, 2, 2>(gu, x_bf16, items, st);
     }
-    DecodeArgs dn{bp, ws, a0, a0, bp.F, bp.H, 0, 0};
+    DecodeArgs dn{bp, ws, a0, a0, bp.F, bp.H, 0, 0, 0};
     if (down_rows32(bp)) {
         const int items = tiles * (bp.H / 32);
         return nt == 1 ? launch_bf<false, 1, 2>(dn, h_bf16, items, st) : launch_bf<false, 2, 2>(dn, h_bf16, items, st);

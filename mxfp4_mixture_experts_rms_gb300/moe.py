@@ -136,6 +136,8 @@ class DeviceBlock:
         self.shape = shape
 
         def up(a, dt=None):
+            if isinstance(a, torch.Tensor):   # already a tensor (e.g. drawn on the device)
+                return a.to(device).contiguous()
             a = np.ascontiguousarray(a)
             t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
             return t.to(device)

@@ -164,6 +164,36 @@ def make_block(config: int, layer: int = 0, shape: BlockShape | None = None,
     return blk
 
 
+def expert_matrices_device(shape: BlockShape, n: int, seed: int, device="cuda") -> dict:
+    """The same recipe as ``expert_matrices`` drawn on the device with torch's
+    generator (another random stream: only the distributions are shared).
+    For benchmark weight sets too large to draw on the host in reasonable time;
+    nothing that is compared with the oracle uses these."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out = {"codes": {}, "scales": {}, "bias": {}}
+    for m in MATS:
+        rows, cols = shape.mat_shape(m)
+        out["codes"][m] = torch.randint(0, 256, (n, rows, cols // 2), dtype=torch.uint8, device=device, generator=g)
+        out["scales"][m] = torch.randint(118, 125, (n, rows, cols // 32), dtype=torch.uint8, device=device,
+                                         generator=g)
+        out["bias"][m] = torch.randn((n, rows), dtype=torch.float32, device=device, generator=g) * 0.02
+    return out
+
+
+def make_block_device(config: int, layer: int, expert_seed: int, device="cuda") -> dict:
+    """Norm and router weights of workload ``config`` (layer ``layer``) drawn
+    exactly as ``make_router`` does, with expert matrices from
+    ``expert_matrices_device`` (seeded by ``expert_seed``)."""
+    blk = make_router(config, layer)
+    shape = blk["shape"]
+    blk.update(expert_matrices_device(shape, shape.n_experts, expert_seed, device))
+    if shape.n_shared:
+        blk["shared"] = expert_matrices_device(shape, 1, expert_seed + 7919, device)
+    return blk
+
+
 def make_tokens(config: int, tokens: int, hidden: int, layer: int = 0, sub: int = 0) -> np.ndarray:
     """Input activations x ~ N(0,1) as bf16 bits ``[tokens][hidden]``."""
     return f32_to_bf16_bits(_rng(config, layer, _T_X, sub).normal(0.0, 1.0, size=(tokens, hidden)))
@@ -191,6 +221,6 @@ def distinct_uniform(E: int, K: int, T: int) -> float:
 
 __all__ = [
     "BlockShape", "Workload", "WORKLOADS", "GPT_OSS", "DSV4_FLASH_SHAPE", "MATS",
-    "make_block", "make_router", "make_tokens", "tiny_shape", "f32_to_bf16_bits", "bf16_bits_to_f32",
+    "make_block", "make_router", "make_tokens", "make_block_device", "expert_matrices_device", "tiny_shape", "f32_to_bf16_bits", "bf16_bits_to_f32",
     "expert_bytes", "expert_bias_bytes", "distinct_uniform",
 ]

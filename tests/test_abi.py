@@ -76,6 +76,21 @@ def test_forward_before_weights_is_not_ready(L):
     assert L.moe_load_weights(h, C.byref(w)) == moe.MOE_EINVAL
     assert L.moe_set_workspace(h, C.c_void_p(0x1008), 1 << 20) == moe.MOE_EINVAL  # misaligned
     assert L.moe_debug_dequant(h, 0, 0, C.c_void_p(256), None) == moe.MOE_ENOTREADY
+    # neither a workspace nor a no-alloc call: there is no status word to read
+    st = C.c_int(7)
+    assert L.moe_get_device_status(h, C.byref(st), None) == moe.MOE_ENOTREADY
+    assert L.moe_forward_noalloc(h, C.c_void_p(256), 1, C.c_void_p(4096), None, None) == moe.MOE_ENOTREADY
+    assert L.moe_plan_set_i(h, b"test_stall_wait", 1) == moe.MOE_OK
+    assert L.moe_plan_set_i(h, b"test_stall_wait", 0) == moe.MOE_OK
+    L.moe_plan_destroy(h)
+
+
+def test_token_counts_above_the_grid_limit_are_refused(L):
+    h = C.c_void_p(L.moe_plan_create(64, 64, 4, 2, 1.702, 7.0, 1.0))
+    assert L.moe_workspace_bytes(h, 65535) > 0
+    assert L.moe_workspace_bytes(h, 65536) == 0          # the combine grid's y extent
+    assert b"65535" in L.moe_last_error()
+    assert L.moe_workspace_bytes(h, 2 ** 31 - 1) == 0
     L.moe_plan_destroy(h)
 
 

@@ -306,3 +306,29 @@ def test_stacked_blocks_residual_chain():
     r = (xr.astype(np.uint32) << 16).view(np.float32)
     rel = np.linalg.norm(g - r) / np.linalg.norm(r)
     assert rel < n_layers * 1e-3, rel
+
+
+# ------------------------------------------------------- device-side failure
+def test_bounded_wait_timeout_is_reported_and_the_plan_recovers():
+    """The test hook makes the decode gate/up kernel wait on a barrier nothing
+    completes: the bounded wait (about 2 s) runs out, the kernel records
+    MOE_DEV_WAIT_TIMEOUT, lets the copies it issued land and exits; the host
+    reads the status (and clears it) and the next forward is correct."""
+    import torch
+    blk = synth.make_block(1)
+    x_bits = synth.make_tokens(1, 8, 2880)
+    ref, plan, dev = run_gpu(blk, x_bits)
+    assert ref["status"] == 0
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+    out = torch.empty((8, 2880), dtype=torch.float32, device="cuda")
+    ids = torch.empty((8, 4), dtype=torch.int32, device="cuda")
+    plan.set_i("test_stall_wait", 1)
+    plan.forward(x, out, ids)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 1            # MOE_DEV_WAIT_TIMEOUT
+    assert b"detail 59" in moe.load().moe_last_error()
+    assert plan.device_status() == 0            # cleared by the read
+    plan.set_i("test_stall_wait", 0)
+    again, _, _ = run_gpu(blk, x_bits, plan=plan, dev=dev)
+    assert again["status"] == 0
+    assert np.array_equal(again["ids"], ref["ids"]) and np.array_equal(again["out"], ref["out"])
