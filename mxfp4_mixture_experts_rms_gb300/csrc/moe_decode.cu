@@ -160,14 +160,26 @@ __device__ __forceinline__ void dec_mbar_drain(uint64_t *b, uint32_t parity, int
 __device__ __forceinline__ void dec_arrive(uint64_t *b) {
     asm volatile("{ .reg .b64 t; mbarrier.arrive.shared::cta.b64 t, [%0]; }" ::"r"(smem_addr(b)) : "memory");
 }
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_addr(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
-                 : "memory");
+// L2 policy for the weight stream: each weight byte is read once per
+// forward, so its lines go first when L2 needs room.  Everything else of a
+// forward (its activations and tables, and the kernels' own code) then stays
+// in L2 while gigabytes of weights pass through it; measured on a GB300 this
+// shortened the routing kernel's serial tail from 7.6 to 2.9 us at 16 tokens.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "l"(pol)
+                 : "memory");
 }
 __device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], const void *p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -236,6 +248,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
 
     if (warp == kProd) {
         // ---------------------------------------------------------- producer
+        const uint64_t pol = l2_evict_first();
         auto issue = [&](int k) {
             const int s = k % S, item = begin + k;
             const int4 tile = a.ws.tiles[item / RB];
@@ -251,7 +264,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
                 for (int m = 0; m < NM; m++) {
                     const MatPtrs &M = m == 0 ? a.A0 : a.A1;
                     const int jm = GATEUP ? j0 : j0 + 16 * m;
-                    bulk_g2s(st + m * 16 * geo.rs, mat_codes(M, e, E) + (size_t)jm * (K / 2), 16 * (K / 2), &full[s]);
+                    bulk_g2s(st + m * 16 * geo.rs, mat_codes(M, e, E) + (size_t)jm * (K / 2), 16 * (K / 2), &full[s], pol);
                 }
             }
 #pragma unroll
@@ -260,8 +273,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
                 const int jm = GATEUP ? j0 : j0 + 16 * m;
                 const uint8_t *scs = mat_scales(M, e, E) + (size_t)jm * nb;
                 unsigned char *scd = st + NM * 16 * geo.rs + m * geo.scb;
-                for (int c = lane; c < nb; c += 32) cp_async16(scd + 16 * c, scs + 16 * c);
-                if (lane < 4) cp_async16(st + geo.bias + m * 64 + 16 * lane, mat_bias(M, e, E) + jm + 4 * lane);
+                for (int c = lane; c < nb; c += 32) cp_async16(scd + 16 * c, scs + 16 * c, pol);
+                if (lane < 4) cp_async16(st + geo.bias + m * 64 + 16 * lane, mat_bias(M, e, E) + jm + 4 * lane, pol);
             }
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&full[s])) : "memory");
             if (lane == 0) MOE_DEC_MARK(0, k);

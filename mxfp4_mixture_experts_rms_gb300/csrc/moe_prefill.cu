@@ -178,12 +178,28 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// Untiled bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
+// The same for the weight stream, with an L2 evict-first policy (each weight
+// byte is read once per forward: its lines go first, the activation tiles
+// that every weight-row block re-reads stay).
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma_load_2d_ef(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y,
+                                               uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load_ef(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
 }
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -382,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
     if (warp == kWarpCodes) {
         // ------------------------------------------- packed codes + scales (TMA)
         if (lane == 0) {
+            const uint64_t pol = l2_evict_first();
             Ring r;
             int issued = 0, g = 0;
             bool ok = true;
@@ -418,14 +435,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_prefill_kernel(const __grid_c
                     unsigned char *dst = sF + r.s * kCStageBytes;
                     if (GATEUP) {
                         const int y = ebase * a.rows + mt * RPI;
-                        tma_load_2d(dst, m0, &full_c[r.s], kb * 32, y);
-                        tma_load_2d(dst + kFp4Bytes / 2, m1, &full_c[r.s], kb * 32, y);
+                        tma_load_2d_ef(dst, m0, &full_c[r.s], kb * 32, y, pol);
+                        tma_load_2d_ef(dst + kFp4Bytes / 2, m1, &full_c[r.s], kb * 32, y, pol);
                     } else {
-                        tma_load_2d(dst, m0, &full_c[r.s], kb * 32, ebase * a.rows + mt * RPI);
+                        tma_load_2d_ef(dst, m0, &full_c[r.s], kb * 32, ebase * a.rows + mt * RPI, pol);
                     }
 #pragma unroll
                     for (int j = 0; j < 4; j++)
-                        bulk_load(dst + kFp4Bytes + j * 128 * kCK, scp[j] + (size_t)kb * 128, 128 * kCK, &full_c[r.s]);
+                        bulk_load_ef(dst + kFp4Bytes + j * 128 * kCK, scp[j] + (size_t)kb * 128, 128 * kCK, &full_c[r.s],
+                                     pol);
                     issued++;
                     r.next(kCStages);
                 }
