@@ -39,7 +39,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE block tokens/s; decode HBM GB/s and prefill TFLOP/s vs GB300 peak"
 HEADLINE = (2, 16)           # (workload, tokens): the 24-layer stack decoding 16 tokens
-EXTRAS = [(0, 1), (1, 8), (2, 1), (2, 4), (3, 128), (3, 512), (4, 1), (4, 2048)]
+# (workload, tokens, plan options): the FP4 rows run the same workloads on the
+# block-scaled FP4 tensor-core path (activations FP4-encoded; its own oracle mode)
+EXTRAS = [(0, 1, {}), (1, 8, {}), (2, 1, {}), (2, 4, {}), (3, 128, {}), (3, 512, {}), (4, 1, {}), (4, 2048, {}),
+          (3, 128, {"act_fp4": 1}), (3, 512, {"act_fp4": 1}), (4, 2048, {"act_fp4": 1})]
 KERNEL_SLOTS = ["route_permute", "gateup_swiglu", "down_weighted", "combine_residual"]
 L2_BYTES = 129 * 2 ** 20
 
@@ -55,6 +58,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=0, help="tokens per step (default: 16 for the stack, "
                                                           "else the workload's largest)")
     ap.add_argument("--no-extras", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--act-fp4", action="store_true",
+                    help="run the headline workload on the block-scaled FP4 tensor-core path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="timed region of the headline only (no clock pre-roll, kernel timing, e2e, CPU "
@@ -216,21 +221,23 @@ def whole_job_rate(world: int, tokens: int, steps: int, ms: float) -> float:
     return world * tokens * steps / (ms / 1e3)
 
 
-def algorithmic_bytes(shape, counts, T):
-    """Bytes the gate/up and down kernels must move at least once per launch."""
+def algorithmic_bytes(shape, counts, T, fp4=False):
+    """Bytes the gate/up and down kernels must move at least once per launch
+    (fp4: activations as FP4 codes + E8M0 scales, 17/32 bytes an element)."""
     H, F = shape.hidden, shape.expert_hidden
     distinct = int((counts > 0).sum()) + shape.n_shared
     routes = int(counts.sum()) + shape.n_shared * T
     mat = F * H // 2 + F * H // 32
-    gateup = distinct * (2 * mat + 2 * F * 4) + T * H * 2 + routes * F * 2
-    down = distinct * (mat + H * 4) + routes * F * 2 + routes * H * 4
+    act = 17 / 32 if fp4 else 2
+    gateup = distinct * (2 * mat + 2 * F * 4) + (routes if fp4 else T) * H * act + routes * F * act
+    down = distinct * (mat + H * 4) + routes * F * act + routes * H * 4
     return gateup, down, distinct
 
 
 def launches_per_forward(path: int, T: int) -> int:
     """Kernels one forward launches: routing (+ the permutation kernel above 32
     tokens), the x_hat gather (grouped-GEMM path), gate/up, down, combine."""
-    return (1 if T <= 32 else 2) + (1 if path == 2 else 0) + 3
+    return (1 if T <= 32 else 2) + (1 if path in (2, 3) else 0) + 3
 
 
 def n_weight_sets(wid, T):
@@ -264,12 +271,13 @@ class Pool:
 class Workload:
     """Plans, inputs and buffers of one (workload, tokens) measurement."""
 
-    def __init__(self, wid, T, pool, rank):
+    def __init__(self, wid, T, pool, rank, opts=None):
         import numpy as np
         import torch
 
         from mxfp4_mixture_experts_rms_gb300 import moe, synth
         self.wid, self.T = wid, T
+        self.opts = dict(opts or {})
         self.wl = wl = synth.WORKLOADS[wid]
         self.shape = sh = wl.shape
         H, K = sh.hidden, sh.top_k
@@ -285,7 +293,7 @@ class Workload:
                 blk.update({k: ex[k] for k in ("codes", "scales", "bias")})
                 if sh.n_shared:
                     blk["shared"] = ex["shared"]
-                plan = moe.Plan(sh, max_tokens=T).alloc_workspace().load_weights(moe.DeviceBlock(blk))
+                plan = moe.Plan(sh, max_tokens=T, **self.opts).alloc_workspace().load_weights(moe.DeviceBlock(blk))
                 chain.append(dict(plan=plan, x=torch.empty((T, H), dtype=torch.int16, device="cuda"),
                                   out=torch.empty((T, H), dtype=torch.float32, device="cuda"),
                                   ids=torch.empty((T, K), dtype=torch.int32, device="cuda")))
@@ -340,7 +348,7 @@ def measure(w, args, world, local, preroll_s):
             c = torch.empty(sh.n_experts, dtype=torch.int32, device="cuda")
             p.expert_counts(c)
             torch.cuda.synchronize()
-            tot_f = [a + b for a, b in zip(tot_f, algorithmic_bytes(sh, c.cpu().numpy(), T))]
+            tot_f = [a + b for a, b in zip(tot_f, algorithmic_bytes(sh, c.cpu().numpy(), T, w.path == 3))]
         facts.append(tuple(tot_f))
         for p in w.plans(d):
             assert p.device_status() == 0
@@ -394,12 +402,24 @@ def measure(w, args, world, local, preroll_s):
 # fp32 FMA peak of the SIMT router: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz
 # (the GB300's SM count and maximum SM clock)
 ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+# dense FP4 tensor peak taken as the measured bf16 peak x the nominal ratio (13.5 / 2.25)
+FP4_OVER_BF16 = 13.5 / 2.25
 
 
 def roofline(path, dom, avg_ms, achieved_gbs, hbm, bf16_peak, peak_kind, tr, dom_bytes, routes, H, F, router_macs):
     """Roofline of the dominant kernel: HBM for the GEMVs (decode path), the
     bf16 tensor peak for the grouped GEMMs (prefill path), the fp32 FMA peak
     when the SIMT routing kernel dominates a prefill step."""
+    if path == 3 and dom in (1, 2):
+        # the block-scaled FP4 GEMMs: far below the FP4 ridge (~1700 flop/B), so HBM binds
+        flops = 2.0 * routes * (2 * F if dom == 1 else F) * H
+        tf = flops / (avg_ms / 1e3) / 1e12 if avg_ms > 0 else 0.0
+        fp4_peak = bf16_peak * FP4_OVER_BF16
+        return {"bound": "hbm", "kernel": KERNEL_SLOTS[dom], "achieved": achieved_gbs, "peak": hbm,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved_gbs / hbm,
+                "traffic": tr["bytes_per_launch"] if tr else None, "algorithmic_bytes_per_launch": dom_bytes,
+                "avg_launch_ms": avg_ms, "tensor_tflops": tf, "fp4_peak_tflops": fp4_peak,
+                "fp4_peak_kind": peak_kind + " bf16 x nominal fp4/bf16 ratio 6", "tensor_frac_of_fp4_peak": tf / fp4_peak}
     if path == 2 and dom in (1, 2):
         flops = 2.0 * routes * (2 * F if dom == 1 else F) * H
         ach = flops / (avg_ms / 1e3) / 1e12 if avg_ms > 0 else 0.0
@@ -408,7 +428,7 @@ def roofline(path, dom, avg_ms, achieved_gbs, hbm, bf16_peak, peak_kind, tr, dom
                 "traffic": tr["bytes_per_launch"] if tr else None,
                 "algorithmic_flops_per_launch": flops, "avg_launch_ms": avg_ms,
                 "hbm_frac_of_algorithmic_bytes": (dom_bytes / (avg_ms / 1e3) / 1e9 / hbm) if avg_ms > 0 else 0.0}
-    if path == 2 and dom == 0:
+    if path in (2, 3) and dom == 0:
         flops = 2.0 * router_macs
         ach = flops / (avg_ms / 1e3) / 1e12 if avg_ms > 0 else 0.0
         return {"bound": "alu", "kernel": KERNEL_SLOTS[dom], "achieved": ach, "peak": ALU_FP32_TFLOPS,
@@ -438,7 +458,7 @@ def summarise(w, r, args, world):
     step_flops = 6.0 * routes * H * F * n_blocks
     hbm, bf16_peak, peak_kind = peaks()
     out = {"value": whole_job_rate(world, T, steps, ms), "unit": "tokens/s", "ms_per_step": ms / steps,
-           "path": "gemv" if w.path == 1 else "grouped_gemm",
+           "path": {1: "gemv", 2: "grouped_gemm", 3: "fp4_grouped_gemm"}[w.path],
            "distinct_experts_per_block": distinct, "algorithmic_bytes_per_step": step_bytes,
            "step_hbm_gbs": step_bytes / step_s / 1e9, "step_frac_of_hbm": step_bytes / step_s / 1e9 / hbm,
            "algorithmic_flops_per_step": step_flops, "step_tflops": step_flops / step_s / 1e12,
@@ -529,7 +549,7 @@ def run_ours(args, rank, world, local, wid, T):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     pool = Pool()
     wl = synth.WORKLOADS[wid]
-    w = Workload(wid, T, pool, rank)
+    w = Workload(wid, T, pool, rank, {"act_fp4": 1} if args.act_fp4 else None)
     r = measure(w, args, world, local, 0.0 if args.quick else 1.0)
     if args.quick:
         if rank == 0:
@@ -541,15 +561,17 @@ def run_ours(args, rank, world, local, wid, T):
     e2e = e2e_rate(w, args, world)
     extras = {}
     if not args.no_extras:
-        for (ew, eT) in EXTRAS:
-            if (ew, eT) == (wid, T):
+        for (ew, eT, eo) in EXTRAS:
+            if (ew, eT) == (wid, T) and not eo:
                 continue
-            x = Workload(ew, eT, pool, rank)
+            x = Workload(ew, eT, pool, rank, eo)
             xr = measure(x, args, world, local, 0.5)
             s = summarise(x, xr, args, world)
             s["config"] = workload_config(x.wl, eT)
+            if eo.get("act_fp4"):
+                s["config"]["activations"] = "fp4 (e2m1 + e8m0/32, the FP4 activation encoding)"
             s["weight_sets"] = len(x.sets)
-            extras[f"{synth.WORKLOADS[ew].name} x{eT}"] = s
+            extras[f"{synth.WORKLOADS[ew].name} x{eT}" + (" fp4" if eo.get("act_fp4") else "")] = s
             x.close()
             torch.cuda.synchronize()
     if rank != 0:

@@ -69,6 +69,12 @@ struct moe_plan {
     bool x_bf16 = false, h_bf16 = false;
     // the grouped GEMM takes fp16 operands (exponents in [104, 140], fp16-range activations)
     bool pf_f16 = false;
+    // FP4 activations: the grouped GEMM on the block-scaled FP4 tensor cores (kind::mxf4)
+    bool act_fp4 = false;
+    Mxf4Weights mxf4{};
+    bool have_mxf4 = false;
+    uint8_t *mxf4_scales = nullptr;  // owned: weight scales repacked into the kernel's atoms
+    size_t mxf4_scales_bytes = 0;
     // kernel timing (profile option)
     static constexpr int kSlots = 4, kMaxRec = 4096 * kSlots;
     std::vector<cudaEvent_t> ev;     // 2 events per record
@@ -98,6 +104,14 @@ int auto_decode_max(const BlockParams &b) { return b.E <= 64 ? 60 : 8; }
 // or the tensor-core grouped GEMM (prefill) path.
 int choose_path(const moe_plan *p, int tokens, bool *decode, int *nt, int *tile_rows) {
     const BlockParams &b = p->bp;
+    if (p->act_fp4) {
+        // FP4 activations: the block-scaled FP4 grouped GEMM at every token count
+        if (!p->have_mxf4) return fail(MOE_ESHAPE, "the FP4-activation path needs H and F multiples of 64, H <= 4096");
+        *decode = false;
+        *nt = 1;
+        *tile_rows = prefill_tile_rows();
+        return MOE_OK;
+    }
     // the grouped GEMM needs H and F in whole 64-element stages; the GEMVs need
     // H, F <= 4800 (register-resident activations)
     const bool prefill_ok = b.H % 64 == 0 && b.F % 64 == 0 && p->have_maps;
@@ -151,6 +165,16 @@ size_t carve(const moe_plan *p, int T, char *base, Workspace *ws) {
     w.lbound = c.take<float>(base, (size_t)T * b.E);
     w.status = c.take<int32_t>(base, 4);
     w.tickets = c.take<uint32_t>(base, route_ticket_count(T));
+    if (p->act_fp4) {
+        // FP4 operands: codes alias buffers the FP4 path does not otherwise use
+        // (x_hat codes are dead before y is written; h16 is the bf16 paths');
+        // scale atoms per 128-route tile
+        w.xq = reinterpret_cast<uint8_t *>(w.y);
+        w.hq = reinterpret_cast<uint8_t *>(w.h16);
+        const size_t tiles = R / 128 + (size_t)(b.E + b.n_shared) + 2;
+        w.xsf = c.take<uint8_t>(base, tiles * mxf4_nqe(b.H) * 512);
+        w.hsf = c.take<uint8_t>(base, tiles * mxf4_nqe(b.F) * 512);
+    }
     if (ws) *ws = w;
     return c.off;
 }
@@ -223,6 +247,48 @@ int noalloc_scratch_addr(int dev, void **out) {
     *out = g_noalloc_ptr[dev];
     return MOE_OK;
 }
+// The launch sequence of one forward on workspace ws: routing (+ permutation),
+// gate/up, down, combine.  mark(slot, begin) brackets each kernel slot (the
+// profile option's events; a no-op otherwise).
+template <class Mark>
+int enqueue_forward(moe_plan *p, const Workspace &ws, const uint16_t *x, int tokens, float *out, int32_t *ids_out,
+                    float *rw_out, uint16_t *xhat_out, cudaStream_t st, Mark &&mark) {
+    const BlockParams &b = p->bp;
+    bool decode = false;
+    int nt = 1, tile_rows = 0;
+    if (int rc = choose_path(p, tokens, &decode, &nt, &tile_rows)) return rc;
+    mark(0, true);
+    cudaError_t e = launch_route(b, ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, rw_out,
+                                 xhat_out, tile_rows, p->router_exact, (decode || p->act_fp4) ? 0 : 1, st);
+    mark(0, false);
+    if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
+    mark(1, true);
+    if (p->act_fp4) {
+        e = launch_mxf4_stage(b, ws, p->gate, p->up, p->down, p->mxf4, tokens, true, st);
+    } else {
+        if (!decode) e = launch_gather(b, ws, tokens, p->pf_f16, st);
+        if (e == cudaSuccess)
+            e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16,
+                                             p->stall_test, st)
+                       : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, p->pf_f16, st);
+    }
+    mark(1, false);
+    if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
+    mark(2, true);
+    if (p->act_fp4)
+        e = launch_mxf4_stage(b, ws, p->gate, p->up, p->down, p->mxf4, tokens, false, st);
+    else
+        e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, 0, st)
+                   : launch_prefill_stage(b, ws, p->down, p->down, false, tokens, p->maps.down, p->pf_f16, st);
+    mark(2, false);
+    if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
+    mark(3, true);
+    e = launch_combine(b, ws, x, tokens, out, st);
+    mark(3, false);
+    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -270,6 +336,7 @@ void moe_plan_destroy(moe_plan *plan) {
     if (!plan) return;
     for (auto &e : plan->ev) cudaEventDestroy(e);
     if (plan->pf_scales) cudaFree(plan->pf_scales);
+    if (plan->mxf4_scales) cudaFree(plan->mxf4_scales);
     delete plan;
 }
 
@@ -293,6 +360,10 @@ int moe_plan_set_i(moe_plan *p, const char *key, long long v) {
         p->path = (int)v;
     } else if (!strcmp(key, "router_exact")) {
         p->router_exact = v ? 1 : 0;
+    } else if (!strcmp(key, "act_fp4")) {
+        if (p->have_ws) return fail(MOE_EINVAL, "act_fp4 must be set before moe_set_workspace");
+        p->act_fp4 = v != 0;
+        p->have_w = false;  // the weights are prepared for the path at load
     } else if (!strcmp(key, "test_stall_wait")) {
         p->stall_test = v ? 1 : 0;
     } else if (!strcmp(key, "profile")) {
@@ -316,7 +387,7 @@ int moe_plan_path_for(const moe_plan *p, int tokens) {
     int nt = 1, tile_rows = 0;
     const int rc = choose_path(p, tokens, &decode, &nt, &tile_rows);
     if (rc != MOE_OK) return rc;
-    return decode ? 1 : 2;
+    return p->act_fp4 ? 3 : decode ? 1 : 2;
 }
 
 int moe_plan_set_f(moe_plan *p, const char *key, double v) {
@@ -419,6 +490,26 @@ int moe_load_weights(moe_plan *p, const moe_weights *w) {
         if (e != cudaSuccess) return cuda_fail(e, "moe_load_weights (repacked scales)");
         p->have_maps = true;
     }
+    p->have_mxf4 = false;
+    if (p->act_fp4 && b.H % 64 == 0 && b.F % 64 == 0 && b.H <= 4096) {
+        const size_t nbytes = mxf4_scales_bytes(b);
+        if (p->mxf4_scales && p->mxf4_scales_bytes != nbytes) {
+            cudaFree(p->mxf4_scales);
+            p->mxf4_scales = nullptr;
+        }
+        if (!p->mxf4_scales) {
+            e = cudaMalloc(&p->mxf4_scales, nbytes);
+            if (e != cudaSuccess) {
+                p->mxf4_scales = nullptr;
+                return cuda_fail(e, "moe_load_weights (FP4 scale atoms)");
+            }
+            p->mxf4_scales_bytes = nbytes;
+        }
+        e = mxf4_prepare(b, p->gate, p->up, p->down, p->mxf4_scales, &p->mxf4, 0);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_load_weights (FP4 scale atoms)");
+        p->have_mxf4 = true;
+    }
     // fp16 holds the GEMV activations below 65504: |x_hat| <= sqrt(H) max|gamma|;
     // |h| <= max(|L|, 0.3/alpha) (|L| + 1), since x sigmoid(alpha x) >= -0.28/alpha
     const double xb = std::sqrt((double)b.H) * (double)gmax * 1.01;
@@ -448,9 +539,6 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
         return fail(MOE_EINVAL, "x and out must not alias");
     if (int rc = check_outputs(b, tokens, x, ids_out, rw_out, xhat_out)) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    bool decode = false;
-    int nt = 1, tile_rows = 0;
-    if (int rc = choose_path(p, tokens, &decode, &nt, &tile_rows)) return rc;
     auto mark = [&](int slot, bool begin) {
         if (!p->profile) return;
         if (begin) {
@@ -462,28 +550,7 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
             cudaEventRecordWithFlags(p->ev[2 * (p->rec_slot.size() - 1) + 1], st, cudaEventRecordExternal);
         }
     };
-    mark(0, true);
-    cudaError_t e = launch_route(b, p->ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, rw_out,
-                                 xhat_out, tile_rows, p->router_exact, decode ? 0 : 1, st);
-    mark(0, false);
-    if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
-    mark(1, true);
-    if (!decode) e = launch_gather(b, p->ws, tokens, p->pf_f16, st);
-    if (e == cudaSuccess)
-        e = decode ? launch_decode_stage(b, p->ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, p->stall_test, st)
-                   : launch_prefill_stage(b, p->ws, p->gate, p->up, true, tokens, p->maps.gateup, p->pf_f16, st);
-    mark(1, false);
-    if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
-    mark(2, true);
-    e = decode ? launch_decode_stage(b, p->ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, 0, st)
-               : launch_prefill_stage(b, p->ws, p->down, p->down, false, tokens, p->maps.down, p->pf_f16, st);
-    mark(2, false);
-    if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
-    mark(3, true);
-    e = launch_combine(b, p->ws, x, tokens, out, st);
-    mark(3, false);
-    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
-    return MOE_OK;
+    return enqueue_forward(p, p->ws, x, tokens, out, ids_out, rw_out, xhat_out, st, mark);
 }
 
 int moe_forward(moe_plan *p, const uint16_t *x, int tokens, float *out, int32_t *ids_out, void *stream) {
@@ -622,9 +689,11 @@ int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, 
     if (need > MOE_NOALLOC_SCRATCH_BYTES - MOE_NOALLOC_STATUS_BYTES)
         return fail(MOE_ENOMEM, "moe_forward_noalloc: %d tokens need %zu bytes of scratch, the static array holds %u",
                     tokens, need, MOE_NOALLOC_SCRATCH_BYTES - MOE_NOALLOC_STATUS_BYTES);
-    bool decode = false;
-    int nt = 1, tile_rows = 0;
-    if (int rc2 = choose_path(p, tokens, &decode, &nt, &tile_rows)) return rc2;
+    {
+        bool decode = false;
+        int nt = 1, tile_rows = 0;
+        if (int rc2 = choose_path(p, tokens, &decode, &nt, &tile_rows)) return rc2;
+    }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: cudaGetDevice");
@@ -642,20 +711,7 @@ int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, 
     // tickets (whose place depends on the token count) must start at zero
     e = cudaMemsetAsync(ws.tickets, 0, sizeof(uint32_t) * route_ticket_count(tokens), st);
     if (e != cudaSuccess) return cuda_fail(e, "moe_forward_noalloc: clearing scratch");
-    e = launch_route(b, ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, nullptr, nullptr,
-                     tile_rows, p->router_exact, decode ? 0 : 1, st);
-    if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
-    if (!decode) e = launch_gather(b, ws, tokens, p->pf_f16, st);
-    if (e == cudaSuccess)
-        e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16, p->stall_test, st)
-                   : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, p->pf_f16, st);
-    if (e != cudaSuccess) return cuda_fail(e, "gate/up kernel launch");
-    e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, 0, st)
-               : launch_prefill_stage(b, ws, p->down, p->down, false, tokens, p->maps.down, p->pf_f16, st);
-    if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
-    e = launch_combine(b, ws, x, tokens, out, st);
-    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
-    return MOE_OK;
+    return enqueue_forward(p, ws, x, tokens, out, ids_out, nullptr, nullptr, st, [](int, bool) {});
 }
 
 }  // extern "C"

@@ -61,6 +61,11 @@ struct Workspace {
     float *lbound;         // [T][E] their rounding-error bounds
     int32_t *status;       // [4] device error flag + detail
     uint32_t *tickets;     // [T + 1] last-CTA counters of the routing kernel (grid, token groups)
+    // FP4-activation grouped GEMM (plans with act_fp4 only)
+    uint8_t *xq;           // [R][H/2] FP4 codes of the routes' x_hat rows (aliases y, like xs)
+    uint8_t *hq;           // [R][F/2] FP4 codes of h (aliases h16)
+    uint8_t *xsf;          // [tiles][nqe(H)][512] scale atoms of xq, per route tile
+    uint8_t *hsf;          // [tiles][nqe(F)][512] scale atoms of hq
     int max_tiles;
 };
 
@@ -108,6 +113,57 @@ __device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t h[4]) {
         "  cvt.rn.f16x2.e2m1x2 %3, d; }"
         : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
         : "r"(w));
+}
+
+// FP4 activation encoding of one 32-element block (ds4.c, FP4 activation
+// quantisation `dsv4_fp4_act_quantize_row_inplace_cpu`, nearest value as in
+// `dsv4_e2m1fn_dequant_cpu`): scale 2^k with k = ceil(log2(amax / 6)), amax at
+// least 6 * 2^-126.  For a bf16-valued amax = m * 2^e (m in [1, 2)), k = e - 2
+// + (m > 1.5), exactly the ceiling of the float quotient (no division).
+// mxq_exponent takes amax (a bf16 value held in a float; NaN elements never
+// raise it) and returns k in [-126, 127] (127 for an infinite amax).
+__device__ __forceinline__ int mxq_exponent(float amax) {
+    const uint32_t ab = max(__float_as_uint(amax) >> 16, 0x01C0u);
+    return ab >= 0x7F80u ? 127 : (int)(ab >> 7) - 129 + ((ab & 0x7Fu) > 0x40u ? 1 : 0);
+}
+// 2^-k as float for k in [-126, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float mxq_inv_scale(int k) {
+    return k <= 126 ? __uint_as_float((uint32_t)(127 - k) << 23) : __uint_as_float(0x00400000u);
+}
+// Four floats -> four E2M1 codes in bits 0..15 (x0 in bits 0..3, x1 in 4..7,
+// x2 in 8..11, x3 in 12..15): round to nearest even, magnitudes above 6 (and
+// infinities) saturated to 6.  The conversion puts its first source operand
+// in the high nibble of its byte.
+__device__ __forceinline__ uint32_t e2m1x4(float x0, float x1, float x2, float x3) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "mov.b32 %0, {b0, b1, 0, 0};\n\t}"
+        : "=r"(r)
+        : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+    return r;
+}
+// One whole 32-element block held by one thread -> 16 bytes of codes (element
+// 2i in the low nibble of byte i) and the E8M0 scale byte k + 127.  Each
+// element goes in as fmin(x * 2^-k + 0, 6): exact scaling; +0 turns -0 into +0
+// and fmin turns NaN into 6, as the page's sign test and clamp do.
+__device__ __forceinline__ uint4 mxq_encode_block(const float (&x)[32], uint32_t &scale_byte) {
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; i++) am = fmaxf(am, fabsf(x[i]));
+    const int k = mxq_exponent(am);
+    const float inv = mxq_inv_scale(k);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) f[i] = fminf(fmaf(x[8 * q + i], inv, 0.0f), 6.0f);
+        w[q] = e2m1x4(f[0], f[1], f[2], f[3]) | (e2m1x4(f[4], f[5], f[6], f[7]) << 16);
+    }
+    scale_byte = (uint32_t)(k + 127);
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Clamped SwiGLU (gate clamped from above, up to [-L, L]); NaN propagates.
@@ -217,4 +273,28 @@ cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, con
 cudaError_t launch_gather(const BlockParams &bp, const Workspace &ws, int T, bool f16, cudaStream_t st);
 int prefill_tile_rows();
 cudaError_t launch_dequant(const MatPtrs &m, int expert, int n_experts, float *out, cudaStream_t st);
+
+// Block-scaled FP4 grouped GEMM (tcgen05.mma kind::mxf4).  Per matrix side
+// (gate/up, down): TMA maps of the weight codes with 128-byte boxes and the
+// weight scales repacked into the 512-byte atoms the kernel copies into
+// tensor memory.
+struct Mxf4Side {
+    CUtensorMap b[4];       // [0] routed gate (or down), [1] routed up, [2] shared gate (or down), [3] shared up
+    const uint8_t *bsf;     // routed scale atoms [E][row blocks][nqe][512]
+    const uint8_t *bsf_sh;  // the shared expert's
+    int row_blocks;         // item row blocks per expert matrix (64 gate/up rows, or 128 down rows)
+    int nqe;                // 128-element scale groups per row, rounded up to even
+};
+struct Mxf4Weights {
+    Mxf4Side gu, dn;
+};
+int mxf4_nqe(int K);
+size_t mxf4_scales_bytes(const BlockParams &bp);
+// Builds the maps and repacks the scales into buf (mxf4_scales_bytes bytes), enqueued on st.
+cudaError_t mxf4_prepare(const BlockParams &bp, const MatPtrs &gate, const MatPtrs &up, const MatPtrs &down,
+                         uint8_t *buf, Mxf4Weights *out, cudaStream_t st);
+// gateup: x_hat FP4 encoding into route order + the gate/up GEMM (bias, SwiGLU, h's bf16 rounding and FP4
+// encoding in the epilogue); otherwise the down GEMM (bias x route weight -> y).
+cudaError_t launch_mxf4_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &gate, const MatPtrs &up,
+                              const MatPtrs &down, const Mxf4Weights &w, int T, bool gateup, cudaStream_t st);
 cudaError_t launch_scan_scales(const uint8_t *scales, size_t n, int32_t *flag, cudaStream_t st);

@@ -19,21 +19,6 @@
 
 namespace {
 
-// Four floats -> four E2M1 codes in bits 0..15 (x0 in bits 0..3, x1 in 4..7,
-// x2 in 8..11, x3 in 12..15): round to nearest even, magnitudes above 6 (and
-// infinities) saturated to 6.  The conversion puts its first source operand
-// in the high nibble of its byte.
-__device__ __forceinline__ uint32_t e2m1x4(float x0, float x1, float x2, float x3) {
-    uint32_t r;
-    asm("{\n\t.reg .b8 b0, b1;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-        "mov.b32 %0, {b0, b1, 0, 0};\n\t}"
-        : "=r"(r)
-        : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
-    return r;
-}
-
 // Encode 16-byte chunk u of x (elements 8u..8u+7 of block u / 4: rows are
 // contiguous, so blocks are numbered straight through the matrix) into the
 // 32-bit code word u; the four lanes of a block meet by shuffles, so the whole
@@ -53,12 +38,8 @@ __device__ __forceinline__ void encode_chunk(const uint4 v, size_t u, bool activ
     for (int i = 0; i < 8; i++) am = fmaxf(am, fabsf(xf[i]));
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-    // amax as bf16 magnitude bits, at least 6 * 2^-126 (0x01C0: 1.5 * 2^-124);
-    // k = e - 2 + (m > 1.5), 127 for an infinite amax
-    const uint32_t ab = max(__float_as_uint(am) >> 16, 0x01C0u);
-    const int k = ab >= 0x7F80u ? 127 : (int)(ab >> 7) - 129 + ((ab & 0x7Fu) > 0x40u ? 1 : 0);
-    // 2^-k for k in [-126, 127]; 2^-127 is the subnormal 0x00400000
-    const float inv = k <= 126 ? __uint_as_float((uint32_t)(127 - k) << 23) : __uint_as_float(0x00400000u);
+    const int k = mxq_exponent(am);
+    const float inv = mxq_inv_scale(k);
     float f[8];
 #pragma unroll
     for (int i = 0; i < 8; i++) f[i] = fminf(fmaf(xf[i], inv, 0.0f), 6.0f);  // exact scaling

@@ -191,7 +191,8 @@ class Plan:
         _check(self.L.moe_plan_set_f(self.h, key.encode(), float(v)))
 
     def path_for(self, tokens: int) -> int:
-        """1 if a forward of `tokens` tokens runs the GEMV decode path, 2 the grouped GEMM."""
+        """1 if a forward of `tokens` tokens runs the GEMV decode path, 2 the
+        grouped GEMM, 3 the block-scaled FP4 grouped GEMM (act_fp4 plans)."""
         rc = int(self.L.moe_plan_path_for(self.h, int(tokens)))
         _check(min(rc, 0))
         return rc
