@@ -235,9 +235,10 @@ def algorithmic_bytes(shape, counts, T, fp4=False):
 
 
 def launches_per_forward(path: int, T: int) -> int:
-    """Kernels one forward launches: routing (+ the permutation kernel above 32
-    tokens), the x_hat gather (grouped-GEMM path), gate/up, down, combine."""
-    return (1 if T <= 32 else 2) + (1 if path in (2, 3) else 0) + 3
+    """Kernels one forward launches: routing (one kernel up to 32 tokens; above,
+    norm, logits GEMM, top-k and the permutation), the x_hat gather (grouped-GEMM
+    paths), gate/up, down, combine."""
+    return (1 if T <= 32 else 4) + (1 if path in (2, 3) else 0) + 3
 
 
 def n_weight_sets(wid, T):

@@ -163,6 +163,8 @@ size_t carve(const moe_plan *p, int T, char *base, Workspace *ws) {
     w.xs = reinterpret_cast<uint16_t *>(w.y);
     w.logits = c.take<float>(base, (size_t)T * b.E);
     w.lbound = c.take<float>(base, (size_t)T * b.E);
+    w.xnorm = c.take<float>(base, (size_t)T);
+    w.wnorm = c.take<float>(base, (size_t)b.E);
     w.status = c.take<int32_t>(base, 4);
     w.tickets = c.take<uint32_t>(base, route_ticket_count(T));
     if (p->act_fp4) {

@@ -59,6 +59,8 @@ struct Workspace {
                            //         which is written only after the gate/up GEMM has read these)
     float *logits;         // [T][E] router logits (fp32) of the routing kernel
     float *lbound;         // [T][E] their rounding-error bounds
+    float *xnorm;          // [T] upper bounds of |x_hat| (large-batch routing)
+    float *wnorm;          // [E] upper bounds of the router rows' |w| (large-batch routing)
     int32_t *status;       // [4] device error flag + detail
     uint32_t *tickets;     // [T + 1] last-CTA counters of the routing kernel (grid, token groups)
     // FP4-activation grouped GEMM (plans with act_fp4 only)

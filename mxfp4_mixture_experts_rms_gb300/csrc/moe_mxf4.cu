@@ -153,13 +153,6 @@ __device__ __forceinline__ void q_tma(void *dst, const CUtensorMap *map, uint64_
         "l"(reinterpret_cast<uint64_t>(map)), "r"(q_smem(bar)), "r"(x), "r"(y)
         : "memory");
 }
-__device__ __forceinline__ void q_tma_ef(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
-        "{%3, %4}], [%2], %5;" ::"r"(q_smem(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(q_smem(bar)), "r"(x), "r"(y), "l"(pol)
-        : "memory");
-}
 __device__ __forceinline__ void q_tma3_ef(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z,
                                           uint64_t pol) {
     asm volatile(

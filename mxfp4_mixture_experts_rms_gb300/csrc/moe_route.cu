@@ -604,62 +604,6 @@ __device__ __forceinline__ void router_logit(const uint16_t *wrow, const uint16_
     bound = 2.0f * (float)chain * 0x1p-24f * (ab + fabsf(b) + fabsf(l)) + 1e-30f;
 }
 
-// Router logits of one expert row (shared memory) for up to 8 x_hat rows
-// (shared memory, tokens g0, g0 + gstep, ...), by one warp, with the summation
-// tree of router_logit.  The error bound uses sum|x_i w_i| <= |x| |w|
-// (Cauchy-Schwarz) instead of accumulating |x_i w_i|: xnorm[g] is an upper
-// bound of token g's |x_hat|, and |w| is accumulated here once for all tokens,
-// so each multiply-add costs one FMA.
-__device__ __forceinline__ void router_logits_tokens(const uint16_t *wrow, const uint16_t *xh, int H, int g0,
-                                                     int gstep, int nt, float b, int lane, float *lg_row,
-                                                     float *lb_row, int E, const float *xnorm) {
-    const int nchunk = H / 8, per_lane = (nchunk + 31) / 32, chain = 8 + per_lane + 6;
-    float acc[8], sw = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; j++) acc[j] = 0.f;
-    for (int ch = lane; ch < nchunk; ch += 32) {
-        const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + 8 * ch);
-        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-        float wf[8];
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            wf[2 * q] = __uint_as_float(ww[q] << 16);
-            wf[2 * q + 1] = __uint_as_float(ww[q] & 0xFFFF0000u);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; q++) sw = fmaf(wf[q], wf[q], sw);
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const int g = g0 + j * gstep;
-            if (g >= nt) break;
-            const uint4 xq = *reinterpret_cast<const uint4 *>(xh + (size_t)g * H + 8 * ch);
-            const uint32_t xx[4] = {xq.x, xq.y, xq.z, xq.w};
-            float cs = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                cs = fmaf(__uint_as_float(xx[q] << 16), wf[2 * q], cs);
-                cs = fmaf(__uint_as_float(xx[q] & 0xFFFF0000u), wf[2 * q + 1], cs);
-            }
-            acc[j] += cs;
-        }
-    }
-    // |w|: a sum of squares (relative error below 2e-6 here), one correctly
-    // rounded square root, then a margin well above both
-    const float wn = sqrtf(warp_sum_f(sw)) * (1.0f + 0x1p-14f);
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-        const int g = g0 + j * gstep;
-        if (g >= nt) break;
-        const float sm = warp_sum_f(acc[j]);
-        if (lane == 0) {
-            const float l = sm + b;
-            lg_row[(size_t)g * E] = l;
-            lb_row[(size_t)g * E] =
-                2.0f * (float)chain * 0x1p-24f * (xnorm[g] * wn + fabsf(b) + fabsf(l)) + 1e-30f;
-        }
-    }
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -798,186 +742,226 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     MOE_PHASE_MARK(7);
 }
 
-// Larger batches: one CTA of 8 warps per 4 tokens covers every expert.  Warp
-// w < 4 normalises token w (in its own x_hat row in shared memory); the router
-// rows stream through a double-buffered ring of RC rows (bulk copies); warp w
-// computes expert w % RC for the tokens g with g % (8/RC) == w / RC; warp w
-// < 4 then selects token w's top-k.  The permutation follows as a kernel of
-// its own.
-constexpr int kBatchTokensMax = 8;  // tokens per CTA: 4 (two CTAs per SM) or, for large batches, 8
+// Larger batches (T > 32): three kernels.
+//  * moe_route_norm_kernel: a warp per token normalises it (x_hat in its
+//    three forms) and records an upper bound of |x_hat|; a warp per router
+//    row records an upper bound of |w|.
+//  * moe_router_gemm_kernel: the logits as a register-tiled SIMT GEMM over
+//    64-token x 64-expert tiles (4 x 4 per thread), K split over grid.z when
+//    the tiles alone do not fill the GPU.  Products of two bf16 are exact in
+//    fp32; each thread sums 32 of them (one k-chunk, 32 roundings) and adds
+//    the chunk sum to a compensated (Kahan) running total, whose error stays
+//    within 2u of the sum of |chunk sums| whatever the number of chunks; the
+//    K-split partials and the bias add one rounding each.
+//  * moe_route_topk_kernel: a warp per token sums the K-split partials in a
+//    fixed order, adds the bias and the rigorous bound 2 gamma_n (|x_hat| |w| +
+//    |b| + |l|) (Cauchy-Schwarz bounds sum |x_i w_i|), and selects the top-k,
+//    recomputing exactly whatever the bounds cannot order.
+constexpr int kGT = 64, kGE = 64, kGK = 32;  // GEMM tile: tokens x experts, k-chunk
+constexpr int kGPad = 68;                    // padded row of the transposed tiles (floats; 16-byte aligned)
+constexpr int kNormRows = 8;                 // tokens (or router rows) per CTA of the norm kernel
+constexpr int kMaxKSplit = 16;               // K splits of the logits GEMM
 
-__host__ __device__ inline size_t batch_rows_off(int H, int TB) { return (size_t)TB * H * 2; }
-// ring slots: two (double buffer), or one when a single chunk holds every router row
-__host__ __device__ inline int batch_slots(int E, int RC) { return (E + RC - 1) / RC > 1 ? 2 : 1; }
-__host__ __device__ inline size_t batch_lg_off(int H, int E, int RC, int TB) {
-    return batch_rows_off(H, TB) + (size_t)batch_slots(E, RC) * RC * H * 2;
-}
-__host__ __device__ inline size_t batch_gm_off(int H, int E, int RC, int TB) {
-    return batch_lg_off(H, E, RC, TB) + (size_t)TB * E * 8;  // logits + bounds; exact logits reuse the ring
-}
-__host__ __device__ inline size_t batch_smem(int H, int E, int RC, int TB) {
-    return batch_gm_off(H, E, RC, TB) + (size_t)H * 4;
-}
+// Roundings a product can pass through in the large-batch logits, with a
+// margin: the chunk's FMAs, the compensated total (2, and its second-order
+// term, counted as 4 more), the K-split partials, the bias.
+__device__ __forceinline__ int router_chain(int ks) { return kGK + 6 + ks + 2; }
 
-__global__ void __launch_bounds__(kRouteThreads) moe_route_batch_kernel(RouteArgs a, int RC, int TB) {
+__global__ void __launch_bounds__(kRouteThreads) moe_route_norm_kernel(RouteArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    MOE_PHASE_MARK(7);
     const int H = a.bp.H, E = a.bp.E;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * TB, nt = min(TB, a.T - t0);
-    uint16_t *xh = reinterpret_cast<uint16_t *>(smem);                                  // [TB][H]
-    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + batch_rows_off(H, TB));        // [2][RC][H]
-    float *lg = reinterpret_cast<float *>(smem + batch_lg_off(H, E, RC, TB));           // [TB][E]
-    float *lb = lg + TB * E;                                                            // [TB][E]
-    double *exs = reinterpret_cast<double *>(ring);                                     // [TB][E] after the ring
-    __shared__ __align__(8) uint64_t wbar[2];
-    __shared__ float xnorm[kBatchTokensMax];  // upper bounds of the tokens' |x_hat|
-    const int nchunk = (E + RC - 1) / RC;
-    const uint32_t slot_bytes = (uint32_t)RC * H * 2;
-    // CTAs walk the chunks from different starting points, so that they do
-    // not all read the same router rows (the same L2 lines) at the same time
-    const int rot = blockIdx.x % nchunk;
-    auto issue = [&](int c) {  // router rows of the c-th chunk of this CTA into ring slot c & 1
-        const int e0 = ((c + rot) % nchunk) * RC, ne = min(RC, E - e0);
-        const uint32_t bytes = (uint32_t)ne * H * 2;
-        uint64_t *bar = &wbar[c & 1];
-        asm volatile("{ .reg .b64 t; mbarrier.arrive.expect_tx.shared::cta.b64 t, [%0], %1; }" ::"r"(smem_u32(bar)),
-                     "r"(bytes)
-                     : "memory");
-        const unsigned char *src = reinterpret_cast<const unsigned char *>(a.router_w + (size_t)e0 * H);
-        unsigned char *dst = reinterpret_cast<unsigned char *>(ring) + (size_t)(c & 1) * slot_bytes;
-        for (uint32_t off = 0; off < bytes; off += 32768) {
-            const uint32_t n = min(32768u, bytes - off);
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_u32(dst + off)),
-                "l"(src + off), "r"(n), "r"(smem_u32(bar))
-                : "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int tok_blocks = (a.T + kNormRows - 1) / kNormRows;
+    if ((int)blockIdx.x >= tok_blocks) {
+        // |w| of router rows: a sum of squares (relative error below 2e-6), one
+        // correctly rounded square root, then a margin well above both
+        const int e = ((int)blockIdx.x - tok_blocks) * kNormRows + warp;
+        if (e >= E) return;
+        const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)e * H);
+        float sw = 0.f;
+        for (int c = lane; c < H / 8; c += 32) {
+            const uint4 v = __ldg(wr + c);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
+                sw = fmaf(lo, lo, fmaf(hi, hi, sw));
+            }
         }
-    };
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar[0])));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar[1])));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        issue(0);
-        if (nchunk > 1) issue(1);
+        const float wn = sqrtf(warp_sum_f(sw)) * (1.0f + 0x1p-14f);
+        if (lane == 0) a.ws.wnorm[e] = wn;
+        return;
     }
-    float *gsm = reinterpret_cast<float *>(smem + batch_gm_off(H, E, RC, TB));  // gamma [H]
+    uint16_t *row = reinterpret_cast<uint16_t *>(smem) + (size_t)warp * H;   // [8][H]
+    float *gsm = reinterpret_cast<float *>(smem + (size_t)kNormRows * H * 2);  // gamma [H]
     for (int c = tid; c < H / 4; c += kRouteThreads)
         reinterpret_cast<float4 *>(gsm)[c] = __ldg(reinterpret_cast<const float4 *>(a.gamma) + c);
     __syncthreads();
-    MOE_PHASE_MARK(0);
-    // ------------------------------------------------------- norm (warp per token)
-    if (warp < nt) {
-        const int t = t0 + warp;
-        uint16_t *row = xh + (size_t)warp * H;
-        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
-        for (int c = lane; c < H / 8; c += 32) reinterpret_cast<uint4 *>(row)[c] = __ldg(xr + c);
-        __syncwarp();
-        MOE_PHASE_MARK(4);
-        const double ssum = sumsq_row(row, H, lane);
-        MOE_PHASE_MARK(5);
-        const double r = rsqrt_d(ssum * a.inv_h + a.bp.eps);  // same in every lane
-        __syncwarp();
-        MOE_PHASE_MARK(6);
-        const float r32 = (float)r;
-        float xs = 0.f;  // sum of x_hat^2 (for the router's error bound)
-        for (int c = lane; c < H / 8; c += 32) {
-            const uint4 xv = reinterpret_cast<const uint4 *>(row)[c];
-            const float4 g0 = reinterpret_cast<const float4 *>(gsm)[2 * c];
-            const float4 g1 = reinterpret_cast<const float4 *>(gsm)[2 * c + 1];
-            const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
-            const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            uint32_t hb[8];
+    const int t = blockIdx.x * kNormRows + warp;
+    if (t >= a.T) return;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
+    for (int c = lane; c < H / 8; c += 32) reinterpret_cast<uint4 *>(row)[c] = __ldg(xr + c);
+    __syncwarp();
+    const double ssum = sumsq_row(row, H, lane);
+    const double r = rsqrt_d(ssum * a.inv_h + a.bp.eps);  // same in every lane
+    const float r32 = (float)r;
+    float xs = 0.f;  // sum of x_hat^2 (for the router's error bound)
+    for (int c = lane; c < H / 8; c += 32) {
+        const uint4 xv = reinterpret_cast<const uint4 *>(row)[c];
+        const float4 g0 = reinterpret_cast<const float4 *>(gsm)[2 * c];
+        const float4 g1 = reinterpret_cast<const float4 *>(gsm)[2 * c + 1];
+        const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
+        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        uint32_t hb[8];
 #pragma unroll
-            for (int q = 0; q < 8; q++) hb[q] = norm_elem((w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, gg[q], r32, r);
+        for (int q = 0; q < 8; q++) hb[q] = norm_elem((w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, gg[q], r32, r);
 #pragma unroll
-            for (int q = 0; q < 8; q++) xs = fmaf(__uint_as_float(hb[q] << 16), __uint_as_float(hb[q] << 16), xs);
-            const uint4 nat = make_uint4(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16, hb[4] | hb[5] << 16,
-                                         hb[6] | hb[7] << 16);
-            reinterpret_cast<uint4 *>(row)[c] = nat;
-            const size_t go = (size_t)t * H + 8 * c;
-            *reinterpret_cast<uint4 *>(a.ws.xhat + go) = nat;
-            if (a.store_mma)
-                *reinterpret_cast<uint4 *>(a.ws.xhat_mma + go) = make_uint4(
-                    hb[0] | hb[4] << 16, hb[1] | hb[5] << 16, hb[2] | hb[6] << 16, hb[3] | hb[7] << 16);
-            uint32_t f[8];
+        for (int q = 0; q < 8; q++) xs = fmaf(__uint_as_float(hb[q] << 16), __uint_as_float(hb[q] << 16), xs);
+        const uint4 nat = make_uint4(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16, hb[4] | hb[5] << 16,
+                                     hb[6] | hb[7] << 16);
+        const size_t go = (size_t)t * H + 8 * c;
+        *reinterpret_cast<uint4 *>(a.ws.xhat + go) = nat;
+        if (a.store_mma)
+            *reinterpret_cast<uint4 *>(a.ws.xhat_mma + go) =
+                make_uint4(hb[0] | hb[4] << 16, hb[1] | hb[5] << 16, hb[2] | hb[6] << 16, hb[3] | hb[7] << 16);
+        uint32_t f[8];
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));
-                f[q] = *reinterpret_cast<uint16_t *>(&hh);
-            }
-            *reinterpret_cast<uint4 *>(a.ws.xhat16 + go) =
-                make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
-            if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + go) = nat;
+        for (int q = 0; q < 8; q++) {
+            __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));
+            f[q] = *reinterpret_cast<uint16_t *>(&hh);
         }
-        // |x_hat| with a margin above the error of the sum (positive terms) and of the root
-        const float xn = sqrtf(warp_sum_f(xs)) * (1.0f + 0x1p-14f);
-        if (lane == 0) xnorm[warp] = xn;
+        *reinterpret_cast<uint4 *>(a.ws.xhat16 + go) =
+            make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
+        if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + go) = nat;
+    }
+    // |x_hat| with a margin above the error of the sum (positive terms) and of the root
+    const float xn = sqrtf(warp_sum_f(xs)) * (1.0f + 0x1p-14f);
+    if (lane == 0) a.ws.xnorm[t] = xn;
+}
+
+// lpart[kz][t][e] = sum over the kz-th K range of x_hat[t][k] * W[e][k].
+// Thread (tx, ty) = (tid % 16, tid / 16) owns tokens 4 ty .. 4 ty + 3 and
+// experts 4 tx .. 4 tx + 3 of the tile; the tile's operands pass through
+// shared memory as fp32, transposed to [k][row], a chunk of 32 k at a time
+// (the next chunk's loads in flight during the current chunk's FMAs).
+__global__ void __launch_bounds__(256) moe_router_gemm_kernel(const uint16_t *xhat, const uint16_t *w, int T, int E,
+                                                              int H, int kc_per_split, float *lpart) {
+    __shared__ __align__(16) float sx[2][kGK][kGPad];
+    __shared__ __align__(16) float sw[2][kGK][kGPad];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // x_hat comes from the norm kernel
+    const int t0 = blockIdx.x * kGT, e0 = blockIdx.y * kGE, kz = blockIdx.z;
+    const int nkc = (H + kGK - 1) / kGK;
+    const int kc0 = kz * kc_per_split, kc1 = min(nkc, kc0 + kc_per_split);
+    // loader: row (tid % 64) of the tile, 8 consecutive k at 8 (tid / 64)
+    const int lr = tid & 63, lk = (tid >> 6) * 8;
+    const bool xok = t0 + lr < T, wok = e0 + lr < E;
+    const uint16_t *xrow = xhat + (size_t)(t0 + lr) * H, *wrow = w + (size_t)(e0 + lr) * H;
+    auto fetch = [&](int kc, uint4 &xv, uint4 &wv) {
+        const int k = kc * kGK + lk;
+        const bool kin = k < H;  // H is a multiple of 32: whole groups of 8
+        xv = (xok && kin) ? __ldg(reinterpret_cast<const uint4 *>(xrow + k)) : make_uint4(0, 0, 0, 0);
+        wv = (wok && kin) ? __ldg(reinterpret_cast<const uint4 *>(wrow + k)) : make_uint4(0, 0, 0, 0);
+    };
+    auto stash = [&](int buf, const uint4 &xv, const uint4 &wv) {
+        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ws4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            sx[buf][lk + 2 * q][lr] = __uint_as_float(xs[q] << 16);
+            sx[buf][lk + 2 * q + 1][lr] = __uint_as_float(xs[q] & 0xFFFF0000u);
+            sw[buf][lk + 2 * q][lr] = __uint_as_float(ws4[q] << 16);
+            sw[buf][lk + 2 * q + 1][lr] = __uint_as_float(ws4[q] & 0xFFFF0000u);
+        }
+    };
+    float tot[4][4], cmp[4][4];  // compensated running totals
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) tot[i][j] = cmp[i][j] = 0.f;
+    uint4 xv, wv;
+    if (kc0 < kc1) {
+        fetch(kc0, xv, wv);
+        stash(0, xv, wv);
     }
     __syncthreads();
-    MOE_PHASE_MARK(1);
-    // ------------------------------------------------------------------ router
-    // RC < 8: warps share a row (split of them, tokens gsel, gsel + split, ...);
-    // RC >= 8: each warp takes rows warp, warp + 8, ... for every token
-    const int split = RC >= kRouteWarps ? 1 : kRouteWarps / RC;
-    const int el0 = RC >= kRouteWarps ? warp : warp % RC, elstep = RC >= kRouteWarps ? kRouteWarps : RC;
-    const int gsel = RC >= kRouteWarps ? 0 : warp / RC;
-    bool ok = true;
-    for (int c = 0; c < nchunk; c++) {
-        if (ok) {
-            uint32_t done = 0;
-            uint64_t c0, c1;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c0));
-            for (;;) {
-                asm volatile(
-                    "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-                    : "=r"(done)
-                    : "r"(smem_u32(&wbar[c & 1])), "r"((c >> 1) & 1)
-                    : "memory");
-                if (done) break;
-                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(c1));
-                if (c1 - c0 > 2000000000ull) {
-                    set_device_error(a.ws.status, MOE_DEV_WAIT_TIMEOUT, 71);
-                    ok = false;
-                    break;
-                }
+    for (int kc = kc0; kc < kc1; kc++) {
+        const int buf = (kc - kc0) & 1;
+        if (kc + 1 < kc1) fetch(kc + 1, xv, wv);
+        float part[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) part[i][j] = 0.f;
+#pragma unroll 8
+        for (int kk = 0; kk < kGK; kk++) {
+            const float4 av = *reinterpret_cast<const float4 *>(&sx[buf][kk][4 * ty]);
+            const float4 bv = *reinterpret_cast<const float4 *>(&sw[buf][kk][4 * tx]);
+            const float ai[4] = {av.x, av.y, av.z, av.w}, bj[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int j = 0; j < 4; j++) part[i][j] = fmaf(ai[i], bj[j], part[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) {  // Kahan: tot + cmp carries the sum of the chunk sums
+                const float y = part[i][j] - cmp[i][j];
+                const float tn = tot[i][j] + y;
+                cmp[i][j] = (tn - tot[i][j]) - y;
+                tot[i][j] = tn;
             }
-        }
-        for (int el = el0; el < RC; el += elstep) {
-        const int e = ((c + rot) % nchunk) * RC + el;
-        if (ok && e < E) {
-            const uint16_t *wrow = ring + (size_t)(c & 1) * RC * H + (size_t)el * H;
-            const float bias = a.router_b[e];
-            if (!a.router_exact) {
-                router_logits_tokens(wrow, xh, H, gsel, split, nt, bias, lane, lg + e, lb + e, E, xnorm);
-            } else {
-                for (int g = gsel; g < nt; g += split) {
-                    const float l = (float)exact_logit(xh + (size_t)g * H, a.router_w, a.router_b, e, H, lane);
-                    if (lane == 0) {
-                        lg[g * E + e] = l;
-                        lb[g * E + e] = 0.f;
-                    }
-                }
-            }
-        }
-        }
-        __syncthreads();  // ring slot c & 1 is free again
-        if (tid == 0 && ok && c + 2 < nchunk) issue(c + 2);
+        if (kc + 1 < kc1) stash(buf ^ 1, xv, wv);
+        __syncthreads();
     }
-    MOE_PHASE_MARK(2);
-    if (!ok) return;
-    // ---------------------------------------------------------- top-k + softmax
-    MOE_WARP_MARK(0);
-    if (warp < nt) topk_token<false>(lg + warp * E, lb + warp * E, xh + (size_t)warp * H, a, t0 + warp, lane,
-                                     exs + (size_t)warp * E);
-    MOE_WARP_MARK(1);
-    MOE_PHASE_MARK(3);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int t = t0 + 4 * ty + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int e = e0 + 4 * tx + j;
+            if (e < E) lpart[((size_t)kz * T + t) * E + e] = tot[i][j];
+        }
+    }
+}
+
+// A warp per token: logits and bounds into shared memory, then top-k + softmax.
+__global__ void __launch_bounds__(kRouteThreads) moe_route_topk_kernel(RouteArgs a, const float *lpart, int ks) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int E = a.bp.E, H = a.bp.H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // partials from the GEMM, norms from the norm kernel
+    const int t = blockIdx.x * kRouteWarps + warp;
+    if (t >= a.T) return;
+    double *exs = reinterpret_cast<double *>(smem) + (size_t)warp * E;                       // [8][E]
+    float *lg = reinterpret_cast<float *>(smem + (size_t)kRouteWarps * E * 8) + (size_t)warp * 2 * E;  // [8][2][E]
+    float *lb = lg + E;
+    const float chain = (float)router_chain(ks), xn = a.ws.xnorm[t];
+    for (int e = lane; e < E; e += 32) {
+        // every partial's load in flight before the sum (in K order)
+        float pv[kMaxKSplit];
+#pragma unroll
+        for (int kz = 0; kz < kMaxKSplit; kz++) pv[kz] = kz < ks ? __ldcg(lpart + ((size_t)kz * a.T + t) * E + e) : 0.f;
+        float s = 0.f;
+#pragma unroll
+        for (int kz = 0; kz < kMaxKSplit; kz++)
+            if (kz < ks) s += pv[kz];
+        const float b = a.router_b[e], l = s + b;
+        lg[e] = l;
+        lb[e] = 2.0f * chain * 0x1p-24f * (xn * a.ws.wnorm[e] + fabsf(b) + fabsf(l)) + 1e-30f;
+    }
+    __syncwarp();
+    topk_token<false>(lg, lb, a.ws.xhat + (size_t)t * H, a, t, lane, exs);
 }
 
 // The permutation of a large batch, by one CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) moe_permute_kernel(RouteArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the routing result of the previous kernel
     build_permutation<false>(a, smem);
 }
 
@@ -1059,35 +1043,34 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
         MOE_CUDA_TRY(launch_small_geo(a, g, st));
         return cudaGetLastError();
     }
-    static bool doneb = false, donep = false;
-    // Tokens per CTA: 4, with a ring as deep as keeps two CTAs on an SM (one
-    // row per warp at most); for batches that fill every SM with 8-token CTAs,
-    // 8 tokens and one CTA per SM, so that each staged router row serves twice
-    // the tokens.
+    static bool donen = false, donep = false, donet = false;
     int n_sm = 0, dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
-    int TB = 4, RC = kRouteWarps;
-    size_t cap = 110 * 1024;
-    if ((T + kBatchTokensMax - 1) / kBatchTokensMax >= n_sm) {
-        TB = kBatchTokensMax;
-        cap = 220 * 1024;
-    }
-    const int rc_all = (bp.E + kRouteWarps - 1) / kRouteWarps * kRouteWarps;  // every row, whole warps
-    if (TB == 4 && batch_smem(bp.H, bp.E, rc_all, TB) <= 220 * 1024) {
-        // the whole router matrix fits beside the CTA's rows: one bulk round
-        // instead of a ring whose copy latency would be paid chunk by chunk
-        RC = rc_all;
-        cap = 220 * 1024;
-    }
-    while (RC > 1 && batch_smem(bp.H, bp.E, RC, TB) > cap) RC >>= 1;
-    const size_t smb = batch_smem(bp.H, bp.E, RC, TB);
-    if (smb > 224 * 1024 || (size_t)TB * bp.E * 8 > (size_t)2 * RC * bp.H * 2)
-        return cudaErrorInvalidValue;  // the exact-logit scratch must fit in the ring
-    MOE_CUDA_TRY(smem_optin_once(moe_route_batch_kernel, doneb));
-    moe_route_batch_kernel<<<(T + TB - 1) / TB, kRouteThreads, smb, st>>>(a, RC, TB);
+    // norm (+ the router rows' norms)
+    const int nblk = (T + kNormRows - 1) / kNormRows + (bp.E + kNormRows - 1) / kNormRows;
+    const size_t nsm = (size_t)kNormRows * bp.H * 2 + (size_t)bp.H * 4;
+    if (nsm > 224 * 1024) return cudaErrorInvalidValue;
+    MOE_CUDA_TRY(smem_optin_once(moe_route_norm_kernel, donen));
+    moe_route_norm_kernel<<<nblk, kRouteThreads, nsm, st>>>(a);
     MOE_CUDA_TRY(cudaGetLastError());
+    // logits: split K while the tiles alone leave SMs idle (partials live in y,
+    // which is free until the down projection)
+    const int tiles = ((T + kGT - 1) / kGT) * ((bp.E + kGE - 1) / kGE);
+    const int nkc = (bp.H + kGK - 1) / kGK;
+    int ks = (6 * n_sm + tiles - 1) / tiles;  // about six GEMM CTAs per SM: waves end close together
+    ks = ks < 1 ? 1 : (ks > kMaxKSplit ? kMaxKSplit : ks);
+    if (ks > nkc / 4) ks = nkc / 4 > 0 ? nkc / 4 : 1;
+    while (ks > 1 && (size_t)ks * bp.E > (size_t)(bp.K + bp.n_shared) * bp.H) ks--;
+    const int kc_per = (nkc + ks - 1) / ks;
+    ks = (nkc + kc_per - 1) / kc_per;
+    MOE_CUDA_TRY(launch_pdl(moe_router_gemm_kernel, dim3((T + kGT - 1) / kGT, (bp.E + kGE - 1) / kGE, ks), dim3(256),
+                            0, st, (const uint16_t *)ws.xhat, router_w, T, bp.E, bp.H, kc_per, ws.y));
+    // top-k + softmax, a warp per token
+    const size_t tsm = (size_t)kRouteWarps * bp.E * (8 + 8);
+    MOE_CUDA_TRY(smem_optin_once(moe_route_topk_kernel, donet));
+    MOE_CUDA_TRY(launch_pdl(moe_route_topk_kernel, dim3((T + kRouteWarps - 1) / kRouteWarps), dim3(kRouteThreads), tsm,
+                            st, a, (const float *)ws.y, ks));
     MOE_CUDA_TRY(smem_optin_once(moe_permute_kernel, donep));
-    moe_permute_kernel<<<1, 1024, perm_smem_bytes(bp.E + bp.n_shared, 32), st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(moe_permute_kernel, dim3(1), dim3(1024), perm_smem_bytes(bp.E + bp.n_shared, 32), st, a);
 }
