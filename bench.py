@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=0, help="tokens per step (default: 16 for the stack, "
                                                           "else the workload's largest)")
     ap.add_argument("--no-extras", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers of the stack workload (default: all 24); fewer only to keep an ncu capture small")
     ap.add_argument("--act-fp4", action="store_true",
                     help="run the headline workload on the block-scaled FP4 tensor-core path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -272,7 +274,7 @@ class Pool:
 class Workload:
     """Plans, inputs and buffers of one (workload, tokens) measurement."""
 
-    def __init__(self, wid, T, pool, rank, opts=None):
+    def __init__(self, wid, T, pool, rank, opts=None, layers=0):
         import numpy as np
         import torch
 
@@ -282,12 +284,12 @@ class Workload:
         self.wl = wl = synth.WORKLOADS[wid]
         self.shape = sh = wl.shape
         H, K = sh.hidden, sh.top_k
-        self.layers = wl.layers
+        self.layers = min(layers, wl.layers) if layers else wl.layers
         n_sets = 1 if wl.layers > 1 else n_weight_sets(wid, T)
         self.sets = []
         for s in range(n_sets):
             chain = []
-            for layer in range(wl.layers):
+            for layer in range(self.layers):
                 li = layer if wl.layers > 1 else s
                 blk = synth.make_router(wid, layer=li + 100 * rank)
                 ex = pool.experts(sh, li + 30 * rank)
@@ -550,7 +552,7 @@ def run_ours(args, rank, world, local, wid, T):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     pool = Pool()
     wl = synth.WORKLOADS[wid]
-    w = Workload(wid, T, pool, rank, {"act_fp4": 1} if args.act_fp4 else None)
+    w = Workload(wid, T, pool, rank, {"act_fp4": 1} if args.act_fp4 else None, args.layers)
     r = measure(w, args, world, local, 0.0 if args.quick else 1.0)
     if args.quick:
         if rank == 0:

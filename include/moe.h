@@ -101,6 +101,21 @@ void moe_plan_destroy(moe_plan *plan);
  *                       token, `mixture_of_experts_batch` for a batch)
  *   "path"              0 auto, 1 force decode, 2 force prefill (testing)
  *   "router_exact"      1: compute every router logit in fp64 (testing)
+ *   "act_fp4"           1: run both expert projections as block-scaled FP4
+ *                       tensor-core GEMMs at every token count: the
+ *                       normalised input x_hat and the SwiGLU output h are
+ *                       themselves encoded as MXFP4 along the contracted
+ *                       dimension (E2M1 codes, one E8M0 scale per 32 values,
+ *                       ds4.c `dsv4_fp4_act_quantize_row_inplace_cpu`: scale
+ *                       exponent ceil(log2(amax / 6)), codes rounded to
+ *                       nearest even); needs H and F multiples of 64 and
+ *                       H <= 4096 (else moe_load_weights leaves the plan
+ *                       without this path and forwards fail with MOE_ESHAPE).
+ *                       The result is the block with FP4 activations, not
+ *                       the bf16 one: compare it with a reference that
+ *                       encodes the activations the same way.  Must be set
+ *                       before moe_set_workspace and before
+ *                       moe_load_weights.  0 (default): off
  *   "test_stall_wait"   1: test hook: the decode gate/up kernel first waits
  *                       on a barrier nothing completes, so its bounded wait
  *                       (about 2 s) runs out; the forward then reports
@@ -116,7 +131,8 @@ int moe_plan_set_f(moe_plan *plan, const char *key, double value);
 /* Which projection kernels a forward of `tokens` tokens would run: 1 the GEMV
  * decode path (goosedump gpt_oss.rs `mixture_of_experts`: one matvec pair per
  * selected expert), 2 the tensor-core grouped-GEMM path (`expert_batch_output`:
- * the routed rows of one expert as a matrix) (the "path" and
+ * the routed rows of one expert as a matrix), 3 the block-scaled FP4 grouped
+ * GEMM of the "act_fp4" option (the same grouping, FP4 activations) (the "path" and
  * "decode_max_tokens" options and the shape decide; the choice also needs
  * the weights loaded, since the grouped GEMM's tensor maps are built then).
  * Negative status on error (NULL plan, weights not loaded, no path for the
