@@ -110,6 +110,7 @@ __device__ void warp_exclusive_scan(const int32_t *in, int32_t *out, int n, int 
 }
 
 constexpr int kXC = 2;  // 16-byte chunks of one x row per thread (H <= 8 * 256 * kXC)
+constexpr int kRowChunks = kRouteThreads * kXC / 32;  // 16-byte chunks of one row per lane of a warp
 
 // Σx² of a bf16 row, to ~2^-44 relative (the reference statistic is itself a
 // double sum whose rounding is of that order).  Every value is scaled by
@@ -162,13 +163,23 @@ __device__ __forceinline__ double comp_result(const Comp &a, int emax) {
 // Used where the fp32 bounds cannot decide the top-k (and in the exact mode).
 __device__ double exact_logit(const uint16_t *xh, const uint16_t *router_w, const float *router_b, int e, int H,
                               int lane) {
-    Comp acc[2] = {{0.f, 0.f}, {0.f, 0.f}};
+    // every load of both rows issued before the first product: one memory
+    // latency per logit, not one per chunk
+    const int nch = H / 8;
     const uint4 *w = reinterpret_cast<const uint4 *>(router_w + (size_t)e * H);
     const uint4 *x = reinterpret_cast<const uint4 *>(xh);
-#pragma unroll 4  // several row loads in flight (the row is read from L2 or HBM)
-    for (int c = lane; c < H / 8; c += 32) {
-        const uint4 wv = __ldg(w + c), xv = x[c];
-        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w}, xx[4] = {xv.x, xv.y, xv.z, xv.w};
+    uint4 wv[kRowChunks], xv[kRowChunks];
+#pragma unroll
+    for (int i = 0; i < kRowChunks; i++) {
+        const int c = lane + 32 * i;
+        wv[i] = c < nch ? __ldg(w + c) : make_uint4(0, 0, 0, 0);
+        xv[i] = c < nch ? x[c] : make_uint4(0, 0, 0, 0);
+    }
+    Comp acc[2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+    for (int i = 0; i < kRowChunks; i++) {
+        if (lane + 32 * i >= nch) break;
+        const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w}, xx[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             comp_add(acc[q & 1], __fmul_rn(__uint_as_float(xx[q] << 16), __uint_as_float(ww[q] << 16)));
@@ -274,17 +285,21 @@ __device__ __forceinline__ double rsqrt_d(double m) {
 constexpr int kInvalid = 0x7fffffff;
 
 // Top-k + softmax of one token by one warp (goosedump gpt_oss.rs
-// `top_experts` and `softmax`).  The logits l[0..E) and their error bounds
-// come from shared (GLOBAL = false) or global memory; lane j holds experts
-// j, j+32, ...; the r-th selection ends in lane r's registers.  The fp32
-// selection stands when consecutive selected values are further apart than
-// twice the largest bound; otherwise every candidate within reach of the k-th
-// value is recomputed exactly in fp64 (into exs[0..E), shared memory) and the
-// selection is redone on those.
+// `top_experts` and `softmax`), in three steps so that the exact logits a
+// token may need are computed by every warp of the CTA at once:
+//  * topk_select: the fp32 selection from the logits l[0..E) and their error
+//    bounds (shared or global memory; lane j holds experts j, j+32, ...; the
+//    r-th selection ends in lane r's registers).  It stands when consecutive
+//    selected values are further apart than twice the largest bound;
+//    otherwise every expert within reach of the k-th value is listed as a
+//    candidate (cand[0..*ncand)) and exs[0..E) is set to -inf;
+//  * exact_candidates: the listed candidates' exact logits into exs;
+//  * topk_finish: the selection redone on the exact logits where needed, the
+//    softmax over the selected raw logits times the weight scale, the stores.
 template <bool GLOBAL>
-__device__ void topk_token(const float *l, const float *bd, const uint16_t *xh, const RouteArgs &a, int t,
-                           int lane, double *exs) {
-    const int E = a.bp.E, K = a.bp.K, H = a.bp.H;
+__device__ bool topk_select(const float *l, const float *bd, const RouteArgs &a, int lane, float &my_v, int &my_i,
+                            double *exs, uint16_t *cand, int *ncand) {
+    const int E = a.bp.E, K = a.bp.K;
     const bool exact_mode = a.router_exact != 0;
     auto ld = [&](const float *p) { return GLOBAL ? __ldcg(p) : *p; };
     constexpr int NQ = MOE_MAX_EXPERTS / 32;
@@ -299,8 +314,8 @@ __device__ void topk_token(const float *l, const float *bd, const uint16_t *xh, 
 #pragma unroll
     for (int o = 16; o; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
     uint32_t taken = 0;
-    float my_v = -INFINITY;
-    int my_i = kInvalid;
+    my_v = -INFINITY;
+    my_i = kInvalid;
     if (E <= 32) {
         // one logit per lane: its rank among the selectable ones (NaN and -inf
         // never are) by 32 independent comparisons, then selection r moves to lane r
@@ -349,21 +364,53 @@ __device__ void topk_token(const float *l, const float *bd, const uint16_t *xh, 
     const int nx_i = __shfl_down_sync(0xffffffffu, my_i, 1);
     bool ok = true;
     if (lane < K && my_i != kInvalid) ok = my_v - (nx_i == kInvalid ? -INFINITY : nx_v) > 2.0f * dmax;
-    const bool certain = !exact_mode && __all_sync(0xffffffffu, ok);
-    double my_d = 0.0;
-    bool have_exact = false;
-    if (!certain) {
-        const float kv = __shfl_sync(0xffffffffu, my_v, K - 1);
-        const int ki = __shfl_sync(0xffffffffu, my_i, K - 1);
-        const float thr = (exact_mode || ki == kInvalid) ? -INFINITY : kv - 2.0f * dmax;
-        for (int j = 0; j < E; j++) {  // warp-uniform
-            const float v = ld(l + j);
-            double ex = -INFINITY;
-            if (v > -INFINITY && !(v < thr)) ex = exact_logit(xh, a.router_w, a.router_b, j, H, lane);
-            if (lane == 0) exs[j] = ex;
+    if (!exact_mode && __all_sync(0xffffffffu, ok)) {
+        if (lane == 0) *ncand = 0;
+        return false;
+    }
+    const float kv = __shfl_sync(0xffffffffu, my_v, K - 1);
+    const int ki = __shfl_sync(0xffffffffu, my_i, K - 1);
+    const float thr = (exact_mode || ki == kInvalid) ? -INFINITY : kv - 2.0f * dmax;
+    int n = 0;
+    for (int base = 0; base < E; base += 32) {  // candidates listed in expert order
+        const int j = base + lane;
+        const float v = j < E ? ld(l + j) : -INFINITY;
+        const bool c = v > -INFINITY && !(v < thr);
+        const uint32_t m = __ballot_sync(0xffffffffu, c);
+        if (c) cand[n + __popc(m & ((1u << lane) - 1u))] = (uint16_t)j;
+        n += __popc(m);
+        if (j < E) exs[j] = -INFINITY;
+    }
+    if (lane == 0) *ncand = n;
+    return true;
+}
+
+// Exact logits of the candidates listed by topk_select for W tokens (token w:
+// x_hat row xbase + w * xstride, candidates cand[w * E ..], count ncand[w],
+// results into exs[w * E + j]), one candidate per warp of the CTA at a time.
+__device__ void exact_candidates(const RouteArgs &a, const uint16_t *xbase, size_t xstride, const uint16_t *cand,
+                                 const int *ncand, int W, double *exs, int warp, int nwarps, int lane) {
+    const int E = a.bp.E;
+    int total = 0;
+    for (int w = 0; w < W; w++) total += ncand[w];
+    for (int p = warp; p < total; p += nwarps) {
+        int w = 0, q = p;
+        while (q >= ncand[w]) {
+            q -= ncand[w];
+            w++;
         }
-        __syncwarp();
-        taken = 0;
+        const int j = cand[w * E + q];
+        const double ex = exact_logit(xbase + (size_t)w * xstride, a.router_w, a.router_b, j, a.bp.H, lane);
+        if (lane == 0) exs[w * E + j] = ex;
+    }
+}
+
+__device__ void topk_finish(const RouteArgs &a, int t, int lane, bool need, const double *exs, float my_v, int my_i) {
+    const int E = a.bp.E, K = a.bp.K;
+    constexpr int NQ = MOE_MAX_EXPERTS / 32;
+    double my_d = 0.0;
+    if (need) {
+        uint32_t taken = 0;
         my_i = kInvalid;
         my_d = -INFINITY;
         for (int r = 0; r < K; r++) {
@@ -388,14 +435,13 @@ __device__ void topk_token(const float *l, const float *bd, const uint16_t *xh, 
             }
             if (bi != kInvalid && (bi & 31) == lane) taken |= 1u << (bi >> 5);
         }
-        have_exact = true;
     }
     // softmax over the selected raw logits, times the weight scale; lane r owns slot r
     const float m = __shfl_sync(0xffffffffu, my_v, 0);
     const double md = __shfl_sync(0xffffffffu, my_d, 0);
     const bool valid = lane < K && my_i != kInvalid;
     float ew = 0.f;
-    if (valid) ew = expf(have_exact ? (float)(my_d - md) : (my_v - m));
+    if (valid) ew = expf(need ? (float)(my_d - md) : (my_v - m));
     float ssum = ew;
 #pragma unroll
     for (int o = 16; o; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
@@ -631,6 +677,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     const uint32_t rank = cluster_ctarank();
     const int epc = a.epc, e0 = (int)rank * epc, ne = max(0, min(epc, E - e0));
     // layout: [router rows] [permutation counters] [x_hat row] [logits E] [bounds E] [exact logits E]
+    // [candidates E]
     const size_t rows_b = STAGED ? (size_t)epc * H * 2 : 0;
     const size_t head = (rows_b + perm_smem_bytes(E) + 127) & ~(size_t)127;  // rows, then counters
     uint16_t *wsm = reinterpret_cast<uint16_t *>(smem);
@@ -638,6 +685,8 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     float *lg = reinterpret_cast<float *>(smem + head + (size_t)H * 2);
     float *lb = lg + E;
     double *exs = reinterpret_cast<double *>(smem + ((head + (size_t)H * 2 + 8 * (size_t)E + 7) & ~(size_t)7));
+    uint16_t *cand = reinterpret_cast<uint16_t *>(exs + E);
+    __shared__ int s_ncand;
     __shared__ int s_maxexp[kRouteWarps];
     __shared__ Comp s_acc[kRouteWarps];
     __shared__ double s_r;
@@ -728,7 +777,16 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     MOE_PHASE_MARK(4);
     if (rank != 0) return;
     // ---------------------------------------------------------- top-k + softmax
-    if (warp == 0) topk_token<false>(lg, lb, xh, a, t, lane, exs);
+    // warp 0 selects; the candidates it cannot order are recomputed exactly by
+    // all warps of the CTA
+    float my_v = -INFINITY;
+    int my_i = kInvalid;
+    bool need = false;
+    if (warp == 0) need = topk_select<false>(lg, lb, a, lane, my_v, my_i, exs, cand, &s_ncand);
+    __syncthreads();
+    if (s_ncand) exact_candidates(a, xh, 0, cand, &s_ncand, 1, exs, warp, kRouteWarps, lane);
+    __syncthreads();
+    if (warp == 0) topk_finish(a, t, lane, need, exs, my_v, my_i);
     MOE_PHASE_MARK(5);
     // ---------------------------------- last token to finish: permutation
     __threadfence();
@@ -742,7 +800,8 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     MOE_PHASE_MARK(7);
 }
 
-// Larger batches (T > 32): three kernels.
+// Larger batches (T > 32): four kernels chained by programmatic dependent
+// launch.
 //  * moe_route_norm_kernel: a warp per token normalises it (x_hat in its
 //    three forms) and records an upper bound of |x_hat|; a warp per router
 //    row records an upper bound of |w|.
@@ -757,6 +816,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
 //    fixed order, adds the bias and the rigorous bound 2 gamma_n (|x_hat| |w| +
 //    |b| + |l|) (Cauchy-Schwarz bounds sum |x_i w_i|), and selects the top-k,
 //    recomputing exactly whatever the bounds cannot order.
+//  * moe_permute_kernel: the token->expert permutation, a CTA per expert.
 constexpr int kGT = 64, kGE = 64, kGK = 32;  // GEMM tile: tokens x experts, k-chunk
 constexpr int kGPad = 68;                    // padded row of the transposed tiles (floats; 16-byte aligned)
 constexpr int kNormRows = 8;                 // tokens (or router rows) per CTA of the norm kernel
@@ -779,9 +839,16 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_norm_kernel(RouteArgs
         const int e = ((int)blockIdx.x - tok_blocks) * kNormRows + warp;
         if (e >= E) return;
         const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)e * H);
+        uint4 wv[kRowChunks];  // the whole row's loads in flight at once
+#pragma unroll
+        for (int i = 0; i < kRowChunks; i++) {
+            const int c = lane + 32 * i;
+            wv[i] = c < H / 8 ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
+        }
         float sw = 0.f;
-        for (int c = lane; c < H / 8; c += 32) {
-            const uint4 v = __ldg(wr + c);
+#pragma unroll
+        for (int i = 0; i < kRowChunks; i++) {
+            const uint4 v = wv[i];
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int q = 0; q < 4; q++) {
@@ -795,13 +862,35 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_norm_kernel(RouteArgs
     }
     uint16_t *row = reinterpret_cast<uint16_t *>(smem) + (size_t)warp * H;   // [8][H]
     float *gsm = reinterpret_cast<float *>(smem + (size_t)kNormRows * H * 2);  // gamma [H]
-    for (int c = tid; c < H / 4; c += kRouteThreads)
-        reinterpret_cast<float4 *>(gsm)[c] = __ldg(reinterpret_cast<const float4 *>(a.gamma) + c);
-    __syncthreads();
+    // gamma and the token row: every load issued before the first use
+    float4 gv[kXC * 2];
+#pragma unroll
+    for (int i = 0; i < kXC * 2; i++) {
+        const int c = tid + kRouteThreads * i;
+        gv[i] = c < H / 4 ? __ldg(reinterpret_cast<const float4 *>(a.gamma) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const int t = blockIdx.x * kNormRows + warp;
+    uint4 xv[kRowChunks];
+    if (t < a.T) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
+#pragma unroll
+        for (int i = 0; i < kRowChunks; i++) {
+            const int c = lane + 32 * i;
+            xv[i] = c < H / 8 ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kXC * 2; i++) {
+        const int c = tid + kRouteThreads * i;
+        if (c < H / 4) reinterpret_cast<float4 *>(gsm)[c] = gv[i];
+    }
+    __syncthreads();
     if (t >= a.T) return;
-    const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
-    for (int c = lane; c < H / 8; c += 32) reinterpret_cast<uint4 *>(row)[c] = __ldg(xr + c);
+#pragma unroll
+    for (int i = 0; i < kRowChunks; i++) {
+        const int c = lane + 32 * i;
+        if (c < H / 8) reinterpret_cast<uint4 *>(row)[c] = xv[i];
+    }
     __syncwarp();
     const double ssum = sumsq_row(row, H, lane);
     const double r = rsqrt_d(ssum * a.inv_h + a.bp.eps);  // same in every lane
@@ -841,46 +930,56 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_norm_kernel(RouteArgs
 }
 
 // lpart[kz][t][e] = sum over the kz-th K range of x_hat[t][k] * W[e][k].
-// Thread (tx, ty) = (tid % 16, tid / 16) owns tokens 4 ty .. 4 ty + 3 and
-// experts 4 tx .. 4 tx + 3 of the tile; the tile's operands pass through
-// shared memory as fp32, transposed to [k][row], a chunk of 32 k at a time
-// (the next chunk's loads in flight during the current chunk's FMAs).
-__global__ void __launch_bounds__(256) moe_router_gemm_kernel(const uint16_t *xhat, const uint16_t *w, int T, int E,
-                                                              int H, int kc_per_split, float *lpart) {
+// Thread (tx, ty) = (tid % 8, tid / 8) owns tokens 4 ty .. 4 ty + 3 and
+// experts 4 tx .. 4 tx + 3 and 32 + 4 tx .. 32 + 4 tx + 3 of the 64 x 64 tile
+// (32 products per three 16-byte shared-memory reads, each read one
+// wavefront for the warp); the tile's operands pass through shared memory as
+// fp32, transposed to [k][row], a chunk of 32 k at a time (the next chunk's
+// loads in flight during the current chunk's FMAs).
+constexpr int kGThreads = 128;
+__global__ void __launch_bounds__(kGThreads) moe_router_gemm_kernel(const uint16_t *xhat, const uint16_t *w, int T,
+                                                                    int E, int H, int kc_per_split, float *lpart) {
     __shared__ __align__(16) float sx[2][kGK][kGPad];
     __shared__ __align__(16) float sw[2][kGK][kGPad];
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int tid = threadIdx.x, tx = tid & 7, ty = tid >> 3;
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // x_hat comes from the norm kernel
     const int t0 = blockIdx.x * kGT, e0 = blockIdx.y * kGE, kz = blockIdx.z;
     const int nkc = (H + kGK - 1) / kGK;
     const int kc0 = kz * kc_per_split, kc1 = min(nkc, kc0 + kc_per_split);
-    // loader: row (tid % 64) of the tile, 8 consecutive k at 8 (tid / 64)
-    const int lr = tid & 63, lk = (tid >> 6) * 8;
+    // loader: row (tid % 64) of the tile, 16 consecutive k at 16 (tid / 64)
+    const int lr = tid & 63, lk = (tid >> 6) * 16;
     const bool xok = t0 + lr < T, wok = e0 + lr < E;
     const uint16_t *xrow = xhat + (size_t)(t0 + lr) * H, *wrow = w + (size_t)(e0 + lr) * H;
-    auto fetch = [&](int kc, uint4 &xv, uint4 &wv) {
-        const int k = kc * kGK + lk;
-        const bool kin = k < H;  // H is a multiple of 32: whole groups of 8
-        xv = (xok && kin) ? __ldg(reinterpret_cast<const uint4 *>(xrow + k)) : make_uint4(0, 0, 0, 0);
-        wv = (wok && kin) ? __ldg(reinterpret_cast<const uint4 *>(wrow + k)) : make_uint4(0, 0, 0, 0);
-    };
-    auto stash = [&](int buf, const uint4 &xv, const uint4 &wv) {
-        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ws4[4] = {wv.x, wv.y, wv.z, wv.w};
+    auto fetch = [&](int kc, uint4 (&xv)[2], uint4 (&wv)[2]) {
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            sx[buf][lk + 2 * q][lr] = __uint_as_float(xs[q] << 16);
-            sx[buf][lk + 2 * q + 1][lr] = __uint_as_float(xs[q] & 0xFFFF0000u);
-            sw[buf][lk + 2 * q][lr] = __uint_as_float(ws4[q] << 16);
-            sw[buf][lk + 2 * q + 1][lr] = __uint_as_float(ws4[q] & 0xFFFF0000u);
+        for (int h = 0; h < 2; h++) {
+            const int k = kc * kGK + lk + 8 * h;
+            const bool kin = k < H;  // H is a multiple of 32: whole groups of 8
+            xv[h] = (xok && kin) ? __ldg(reinterpret_cast<const uint4 *>(xrow + k)) : make_uint4(0, 0, 0, 0);
+            wv[h] = (wok && kin) ? __ldg(reinterpret_cast<const uint4 *>(wrow + k)) : make_uint4(0, 0, 0, 0);
         }
     };
-    float tot[4][4], cmp[4][4];  // compensated running totals
+    auto stash = [&](int buf, const uint4 (&xv)[2], const uint4 (&wv)[2]) {
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const uint32_t xs[4] = {xv[h].x, xv[h].y, xv[h].z, xv[h].w}, ws4[4] = {wv[h].x, wv[h].y, wv[h].z, wv[h].w};
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int k = lk + 8 * h + 2 * q;
+                sx[buf][k][lr] = __uint_as_float(xs[q] << 16);
+                sx[buf][k + 1][lr] = __uint_as_float(xs[q] & 0xFFFF0000u);
+                sw[buf][k][lr] = __uint_as_float(ws4[q] << 16);
+                sw[buf][k + 1][lr] = __uint_as_float(ws4[q] & 0xFFFF0000u);
+            }
+        }
+    };
+    float tot[4][8], cmp[4][8];  // compensated running totals
 #pragma unroll
     for (int i = 0; i < 4; i++)
 #pragma unroll
-        for (int j = 0; j < 4; j++) tot[i][j] = cmp[i][j] = 0.f;
-    uint4 xv, wv;
+        for (int j = 0; j < 8; j++) tot[i][j] = cmp[i][j] = 0.f;
+    uint4 xv[2], wv[2];
     if (kc0 < kc1) {
         fetch(kc0, xv, wv);
         stash(0, xv, wv);
@@ -889,25 +988,27 @@ __global__ void __launch_bounds__(256) moe_router_gemm_kernel(const uint16_t *xh
     for (int kc = kc0; kc < kc1; kc++) {
         const int buf = (kc - kc0) & 1;
         if (kc + 1 < kc1) fetch(kc + 1, xv, wv);
-        float part[4][4];
+        float part[4][8];
 #pragma unroll
         for (int i = 0; i < 4; i++)
 #pragma unroll
-            for (int j = 0; j < 4; j++) part[i][j] = 0.f;
+            for (int j = 0; j < 8; j++) part[i][j] = 0.f;
 #pragma unroll 8
         for (int kk = 0; kk < kGK; kk++) {
             const float4 av = *reinterpret_cast<const float4 *>(&sx[buf][kk][4 * ty]);
-            const float4 bv = *reinterpret_cast<const float4 *>(&sw[buf][kk][4 * tx]);
-            const float ai[4] = {av.x, av.y, av.z, av.w}, bj[4] = {bv.x, bv.y, bv.z, bv.w};
+            const float4 b0 = *reinterpret_cast<const float4 *>(&sw[buf][kk][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&sw[buf][kk][32 + 4 * tx]);
+            const float ai[4] = {av.x, av.y, av.z, av.w};
+            const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int i = 0; i < 4; i++)
 #pragma unroll
-                for (int j = 0; j < 4; j++) part[i][j] = fmaf(ai[i], bj[j], part[i][j]);
+                for (int j = 0; j < 8; j++) part[i][j] = fmaf(ai[i], bj[j], part[i][j]);
         }
 #pragma unroll
         for (int i = 0; i < 4; i++)
 #pragma unroll
-            for (int j = 0; j < 4; j++) {  // Kahan: tot + cmp carries the sum of the chunk sums
+            for (int j = 0; j < 8; j++) {  // Kahan: tot + cmp carries the sum of the chunk sums
                 const float y = part[i][j] - cmp[i][j];
                 const float tn = tot[i][j] + y;
                 cmp[i][j] = (tn - tot[i][j]) - y;
@@ -921,48 +1022,188 @@ __global__ void __launch_bounds__(256) moe_router_gemm_kernel(const uint16_t *xh
         const int t = t0 + 4 * ty + i;
         if (t >= T) continue;
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int e = e0 + 4 * tx + j;
+        for (int j = 0; j < 8; j++) {
+            const int e = e0 + (j < 4 ? 4 * tx + j : 32 + 4 * tx + j - 4);
             if (e < E) lpart[((size_t)kz * T + t) * E + e] = tot[i][j];
         }
     }
 }
 
-// A warp per token: logits and bounds into shared memory, then top-k + softmax.
+// A warp per token: logits and bounds into shared memory, then top-k + softmax
+// (the exact logits of uncertain tokens by all warps of the CTA).
 __global__ void __launch_bounds__(kRouteThreads) moe_route_topk_kernel(RouteArgs a, const float *lpart, int ks) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int E = a.bp.E, H = a.bp.H;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // partials from the GEMM, norms from the norm kernel
-    const int t = blockIdx.x * kRouteWarps + warp;
-    if (t >= a.T) return;
-    double *exs = reinterpret_cast<double *>(smem) + (size_t)warp * E;                       // [8][E]
+    const int t0 = blockIdx.x * kRouteWarps, t = t0 + warp;
+    double *exs = reinterpret_cast<double *>(smem);                                    // [8][E]
     float *lg = reinterpret_cast<float *>(smem + (size_t)kRouteWarps * E * 8) + (size_t)warp * 2 * E;  // [8][2][E]
     float *lb = lg + E;
-    const float chain = (float)router_chain(ks), xn = a.ws.xnorm[t];
-    for (int e = lane; e < E; e += 32) {
-        // every partial's load in flight before the sum (in K order)
-        float pv[kMaxKSplit];
+    uint16_t *cand = reinterpret_cast<uint16_t *>(smem + (size_t)kRouteWarps * E * 16);  // [8][E]
+    __shared__ int s_ncand[kRouteWarps];
+    float my_v = -INFINITY;
+    int my_i = kInvalid;
+    bool need = false;
+    if (t < a.T) {
+        const float chain = (float)router_chain(ks), xn = a.ws.xnorm[t];
+        for (int e = lane; e < E; e += 32) {
+            // every partial's load in flight before the sum (in K order)
+            float pv[kMaxKSplit];
 #pragma unroll
-        for (int kz = 0; kz < kMaxKSplit; kz++) pv[kz] = kz < ks ? __ldcg(lpart + ((size_t)kz * a.T + t) * E + e) : 0.f;
-        float s = 0.f;
+            for (int kz = 0; kz < kMaxKSplit; kz++)
+                pv[kz] = kz < ks ? __ldcg(lpart + ((size_t)kz * a.T + t) * E + e) : 0.f;
+            float s = 0.f;
 #pragma unroll
-        for (int kz = 0; kz < kMaxKSplit; kz++)
-            if (kz < ks) s += pv[kz];
-        const float b = a.router_b[e], l = s + b;
-        lg[e] = l;
-        lb[e] = 2.0f * chain * 0x1p-24f * (xn * a.ws.wnorm[e] + fabsf(b) + fabsf(l)) + 1e-30f;
+            for (int kz = 0; kz < kMaxKSplit; kz++)
+                if (kz < ks) s += pv[kz];
+            const float b = a.router_b[e], l = s + b;
+            lg[e] = l;
+            lb[e] = 2.0f * chain * 0x1p-24f * (xn * a.ws.wnorm[e] + fabsf(b) + fabsf(l)) + 1e-30f;
+        }
+        __syncwarp();
+        need = topk_select<false>(lg, lb, a, lane, my_v, my_i, exs + (size_t)warp * E, cand + (size_t)warp * E,
+                                  &s_ncand[warp]);
+    } else if (lane == 0) {
+        s_ncand[warp] = 0;
     }
-    __syncwarp();
-    topk_token<false>(lg, lb, a.ws.xhat + (size_t)t * H, a, t, lane, exs);
+    __syncthreads();
+    exact_candidates(a, a.ws.xhat + (size_t)t0 * H, (size_t)H, cand, s_ncand, kRouteWarps, exs, warp, kRouteWarps,
+                     lane);
+    __syncthreads();
+    if (t < a.T) topk_finish(a, t, lane, need, exs + (size_t)warp * E, my_v, my_i);
 }
 
-// The permutation of a large batch, by one CTA of 1024 threads.
-__global__ void __launch_bounds__(1024) moe_permute_kernel(RouteArgs a) {
+// The permutation of a large batch (the same result as build_permutation),
+// one CTA per expert (and one for the shared expert).  Every CTA counts the
+// routes of all experts (a shared-memory histogram), scans the counts and the
+// tile counts, then collects its own expert's routes in route order: warp w
+// owns the w-th contiguous segment of the routes; a first pass counts each
+// warp's routes of the expert, a scan over warps places the segments, a
+// second pass writes the entries (token, slot, weight), the inverse map and
+// the expert's tiles.
+constexpr int kPermThreads = 512;
+constexpr int kPermWarps = kPermThreads / 32;
+constexpr int kPermPer = 16;  // route ids per lane in flight
+__host__ __device__ constexpr size_t perm_expert_smem_bytes(int EE) { return (size_t)(4 * (EE + 1) + 2 * 32) * 4; }
+
+__global__ void __launch_bounds__(kPermThreads) moe_permute_kernel(RouteArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the routing result of the previous kernel
-    build_permutation<false>(a, smem);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = a.bp.E, K = a.bp.K, ns = a.bp.n_shared, EE = E + ns, KK = K + ns;
+    const int R = a.T * K;
+    const int me = blockIdx.x;  // this CTA's expert (E: the shared expert)
+    int32_t *cnt = reinterpret_cast<int32_t *>(smem);  // [EE + 1]
+    int32_t *offs = cnt + (EE + 1);                     // [EE + 1]
+    int32_t *tcnt = offs + (EE + 1);                    // [EE + 1]
+    int32_t *toff = tcnt + (EE + 1);                    // [EE + 1]
+    int32_t *wn = toff + (EE + 1);                      // [32] this expert's routes per warp segment
+    int32_t *wo = wn + 32;                              // [32] their exclusive prefix
+    for (int e = tid; e <= EE; e += kPermThreads) cnt[e] = 0;
+    __syncthreads();
+    const int seg = (R + kPermWarps - 1) / kPermWarps;
+    const int r0 = min(R, warp * seg), r1 = min(R, r0 + seg);
+    auto expert_of = [&](int r) {
+        const int e = __ldcg(a.ws.ids + r);
+        return (unsigned)e < (unsigned)E ? e : 0;  // out of range: counted as expert 0 (reported below)
+    };
+    // pass 1: histogram of every expert, and this warp's routes of `me`
+    int mine = 0;
+    for (int b = r0; b < r1; b += 32 * kPermPer) {
+        int ev[kPermPer];
+#pragma unroll
+        for (int i = 0; i < kPermPer; i++) {
+            const int r = b + 32 * i + lane;
+            ev[i] = r < r1 ? expert_of(r) : -1;
+        }
+#pragma unroll
+        for (int i = 0; i < kPermPer; i++) {
+            if (ev[i] >= 0) atomicAdd(&cnt[ev[i]], 1);
+            mine += __popc(__ballot_sync(0xffffffffu, ev[i] == me));
+        }
+    }
+    if (lane == 0) wn[warp] = mine;
+    __syncthreads();
+    if (ns && tid == 0) cnt[E] = a.T;
+    __syncthreads();
+    if (warp == 0) warp_exclusive_scan(cnt, offs, EE, lane);
+    if (warp == 1) {
+        for (int e = lane; e < EE; e += 32) tcnt[e] = (cnt[e] + a.tile_rows - 1) / a.tile_rows;
+        __syncwarp();
+        warp_exclusive_scan(tcnt, toff, EE, lane);
+    }
+    if (warp == 2) {
+        const int v = lane < kPermWarps ? wn[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        wo[lane] = incl - v;
+    }
+    __syncthreads();
+    // counts, offsets and tiles of this expert; the totals by CTA 0
+    if (tid == 0) {
+        if (me < E) a.ws.counts[me] = cnt[me];
+        a.ws.offsets[me] = offs[me];
+    }
+    {
+        const int n = tcnt[me], base = toff[me];
+        for (int k = tid; k < n && base + k < a.ws.max_tiles; k += kPermThreads) {
+            const int st = k * a.tile_rows;
+            a.ws.tiles[base + k] = make_int4(me, offs[me] + st, min(a.tile_rows, cnt[me] - st), 0);
+        }
+    }
+    if (me == 0 && tid == 0) {
+        a.ws.offsets[EE] = offs[EE];
+        *a.ws.n_tiles = min(toff[EE], a.ws.max_tiles);
+        if (toff[EE] > a.ws.max_tiles) set_device_error(a.ws.status, MOE_DEV_BAD_ROUTE, -1);
+        a.ws.tickets[0] = 0u;  // kept re-armed for the small-batch kernel
+    }
+    if (me == E) {  // the shared expert: every token, slot K, weight 1
+        for (int t = tid; t < a.T; t += kPermThreads) {
+            const int pos = offs[E] + t;
+            a.ws.perm_token[pos] = t;
+            a.ws.perm_slot[pos] = K;
+            a.ws.perm_w[pos] = 1.0f;
+            a.ws.loc[t * KK + K] = pos;
+        }
+        return;
+    }
+    // pass 2: this expert's routes in route order
+    int pos = offs[me] + wo[warp];
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int b = r0; b < r1; b += 32 * kPermPer) {
+        int ev[kPermPer];
+#pragma unroll
+        for (int i = 0; i < kPermPer; i++) {
+            const int r = b + 32 * i + lane;
+            ev[i] = r < r1 ? __ldcg(a.ws.ids + r) : -1;
+        }
+#pragma unroll
+        for (int i = 0; i < kPermPer; i++) {
+            const int r = b + 32 * i + lane;
+            int e = ev[i];
+            if (r < r1 && (unsigned)e >= (unsigned)E) {
+                if (me == 0) set_device_error(a.ws.status, MOE_DEV_BAD_ROUTE, r);
+                e = 0;
+            }
+            const bool hit = r < r1 && e == me;
+            const uint32_t m = __ballot_sync(0xffffffffu, hit);
+            if (hit) {
+                const int p = pos + __popc(m & lt);
+                const int t = r / K, sl = r - t * K;
+                a.ws.perm_token[p] = t;
+                a.ws.perm_slot[p] = sl;
+                a.ws.perm_w[p] = __ldcg(a.ws.route_w + r);
+                a.ws.loc[t * KK + sl] = p;
+            }
+            pos += __popc(m);
+        }
+    }
 }
 
 // Small-batch geometry: C CTAs per token (a cluster, C <= cmax), epc experts each.
@@ -978,7 +1219,7 @@ SmallGeo small_geo(int H, int E, int cmax) {
     g.staged = (size_t)g.epc * H * 2 <= 160 * 1024;
     const size_t rows_b = g.staged ? (size_t)g.epc * H * 2 : 0;
     const size_t head = (rows_b + perm_smem_bytes(E) + 127) & ~(size_t)127;
-    g.smem = ((head + (size_t)H * 2 + 8 * (size_t)E + 7) & ~(size_t)7) + 8 * (size_t)E;
+    g.smem = ((head + (size_t)H * 2 + 8 * (size_t)E + 7) & ~(size_t)7) + 8 * (size_t)E + 2 * (size_t)E;
     return g;
 }
 
@@ -1043,7 +1284,7 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
         MOE_CUDA_TRY(launch_small_geo(a, g, st));
         return cudaGetLastError();
     }
-    static bool donen = false, donep = false, donet = false;
+    static bool donen = false, donet = false;
     int n_sm = 0, dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
@@ -1064,13 +1305,13 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
     while (ks > 1 && (size_t)ks * bp.E > (size_t)(bp.K + bp.n_shared) * bp.H) ks--;
     const int kc_per = (nkc + ks - 1) / ks;
     ks = (nkc + kc_per - 1) / kc_per;
-    MOE_CUDA_TRY(launch_pdl(moe_router_gemm_kernel, dim3((T + kGT - 1) / kGT, (bp.E + kGE - 1) / kGE, ks), dim3(256),
+    MOE_CUDA_TRY(launch_pdl(moe_router_gemm_kernel, dim3((T + kGT - 1) / kGT, (bp.E + kGE - 1) / kGE, ks), dim3(kGThreads),
                             0, st, (const uint16_t *)ws.xhat, router_w, T, bp.E, bp.H, kc_per, ws.y));
     // top-k + softmax, a warp per token
-    const size_t tsm = (size_t)kRouteWarps * bp.E * (8 + 8);
+    const size_t tsm = (size_t)kRouteWarps * bp.E * (8 + 8 + 2);
     MOE_CUDA_TRY(smem_optin_once(moe_route_topk_kernel, donet));
     MOE_CUDA_TRY(launch_pdl(moe_route_topk_kernel, dim3((T + kRouteWarps - 1) / kRouteWarps), dim3(kRouteThreads), tsm,
                             st, a, (const float *)ws.y, ks));
-    MOE_CUDA_TRY(smem_optin_once(moe_permute_kernel, donep));
-    return launch_pdl(moe_permute_kernel, dim3(1), dim3(1024), perm_smem_bytes(bp.E + bp.n_shared, 32), st, a);
+    return launch_pdl(moe_permute_kernel, dim3(bp.E + bp.n_shared), dim3(kPermThreads),
+                      perm_expert_smem_bytes(bp.E + bp.n_shared), st, a);
 }
