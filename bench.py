@@ -89,9 +89,9 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def traffic_record(kernel: str, workload: str = "", tokens: int = 0):
+def traffic_record(kernel: str, workload: str = "", tokens: int = 0, path: int = 0):
     """ncu DRAM bytes per launch of `kernel`, if taken on the current source, on
-    this workload and token count."""
+    this workload, token count and projection path."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -101,6 +101,8 @@ def traffic_record(kernel: str, workload: str = "", tokens: int = 0):
         if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["sha256"]:
             continue
         if rec.get("workload", workload) != workload or rec.get("tokens", tokens) != tokens:
+            continue
+        if path and rec.get("path", path) != path:
             continue
         return rec
     return None
@@ -476,7 +478,7 @@ def summarise(w, r, args, world):
         dom = max(range(4), key=lambda k: tot[k])
         dom_bytes = {1: gu_bytes, 2: dn_bytes}.get(dom, gu_bytes)
         achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9 if avg_ms[dom] > 0 else 0.0
-        tr = traffic_record(KERNEL_SLOTS[dom], w.wl.name, T)
+        tr = traffic_record(KERNEL_SLOTS[dom], w.wl.name, T, w.path)
         out["roofline"] = roofline(w.path, dom, avg_ms[dom], achieved, hbm, bf16_peak, peak_kind, tr, dom_bytes,
                                    routes, H, F, T * sh.n_experts * H)
         out["kernels"] = {KERNEL_SLOTS[k]: {"avg_us": 1e3 * avg_ms[k], "share": share[k], "launches": cnt[k]}

@@ -116,11 +116,14 @@ void moe_plan_destroy(moe_plan *plan);
  *                       encodes the activations the same way.  Must be set
  *                       before moe_set_workspace and before
  *                       moe_load_weights.  0 (default): off
- *   "test_stall_wait"   1: test hook: the decode gate/up kernel first waits
- *                       on a barrier nothing completes, so its bounded wait
- *                       (about 2 s) runs out; the forward then reports
- *                       MOE_EDEVICE through moe_get_device_status (detail 59)
- *                       and its outputs are void.  0 (default): off
+ *   "test_stall_wait"   1: test hook: the decode gate/up kernel's consumer
+ *                       warps first wait on a barrier nothing completes, so a
+ *                       bounded wait (about 2 s) runs out: theirs (detail 59)
+ *                       or the epilogue warp's wait for their partial sums
+ *                       (detail 54), whichever expires first; the forward
+ *                       then reports MOE_EDEVICE through
+ *                       moe_get_device_status and its outputs are void.
+ *                       0 (default): off
  *   "profile"           1: time each kernel launch with CUDA events (see
  *                       moe_profile_read); 0: off (default)
  * Options that change the workspace size must be set before moe_set_workspace. */

@@ -260,8 +260,9 @@ int enqueue_forward(moe_plan *p, const Workspace &ws, const uint16_t *x, int tok
     int nt = 1, tile_rows = 0;
     if (int rc = choose_path(p, tokens, &decode, &nt, &tile_rows)) return rc;
     mark(0, true);
+    const int forms = p->act_fp4 ? 0 : decode ? (p->x_bf16 ? 0 : kFormF16) : (p->pf_f16 ? kFormF16 : kFormMma);
     cudaError_t e = launch_route(b, ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, rw_out,
-                                 xhat_out, tile_rows, p->router_exact, (decode || p->act_fp4) ? 0 : 1, st);
+                                 xhat_out, tile_rows, p->router_exact, forms, st);
     mark(0, false);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     mark(1, true);

@@ -228,12 +228,17 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
         if (_e != cudaSuccess) return _e;                   \
     } while (0)
 
+// x_hat copies the routing kernels write besides the natural bf16 one, as
+// the expert kernels of the chosen path read them.
+constexpr int kFormF16 = 1;  // fp16 (the GEMVs, the fp16 grouped GEMM)
+constexpr int kFormMma = 2;  // bf16 in the grouped GEMM's pair order (its bf16 variant)
+
 // Launchers implemented in the .cu files (host side).
 int route_ticket_count(int T);
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x,
                          const float *gamma, const uint16_t *router_w, const float *router_b,
                          int T, int32_t *ids_out, float *rw_out, uint16_t *xhat_out, int tile_rows,
-                         int router_exact, int store_mma, cudaStream_t st);
+                         int router_exact, int forms, cudaStream_t st);
 // x_bf16 / h_bf16: the gate/up (down) GEMV reads bf16 activations instead of fp16.
 // stall (test hook, gate/up only): the consumers first wait on a barrier that
 // nothing completes, so the bounded wait runs out and the kernel reports

@@ -238,6 +238,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     // for gate/up's results.
     if (GATEUP || threadIdx.x < kCW * 32 || threadIdx.x >= kEpi * 32) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    // the producer's lanes fetch the first 64 tile-table entries together with
+    // the tile count, so that the first copy waits for one round trip, not two
+    int4 tpre[2] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};
+    if ((threadIdx.x >> 5) == kProd) {
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            const int ti = (threadIdx.x & 31) + 32 * h;
+            if (ti < a.ws.max_tiles) tpre[h] = __ldcg(a.ws.tiles + ti);
+        }
+    }
     const int n_items = *a.ws.n_tiles * RB;
     const int per = (n_items + gridDim.x - 1) / gridDim.x;
     const int begin = blockIdx.x * per, end = min(n_items, begin + per);
@@ -249,9 +259,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     if (warp == kProd) {
         // ---------------------------------------------------------- producer
         const uint64_t pol = l2_evict_first();
+        auto tile_of = [&](int ti) {  // warp-uniform ti
+            if (ti >= 64) return a.ws.tiles[ti];
+            const int4 v = ti < 32 ? tpre[0] : tpre[1];
+            const int src = ti & 31;
+            return make_int4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
+                             __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
+        };
         auto issue = [&](int k) {
             const int s = k % S, item = begin + k;
-            const int4 tile = a.ws.tiles[item / RB];
+            const int4 tile = tile_of(item / RB);
             const int e = tile.x, j0 = (item % RB) * IR;
             unsigned char *st = dsm + (size_t)s * geo.stage;
             if (lane == 0) {

@@ -57,7 +57,7 @@ struct RouteArgs {
     int tile_rows;
     int router_exact;
     int epc;        // experts per CTA (router rows staged in shared memory)
-    int store_mma;  // also write x_hat in the grouped GEMM's pair order
+    int forms;      // x_hat copies the expert kernels read besides the natural one (kFormF16 | kFormMma)
     double inv_h;   // 1 / H
 };
 
@@ -163,28 +163,32 @@ __device__ __forceinline__ double comp_result(const Comp &a, int emax) {
 // Used where the fp32 bounds cannot decide the top-k (and in the exact mode).
 __device__ double exact_logit(const uint16_t *xh, const uint16_t *router_w, const float *router_b, int e, int H,
                               int lane) {
-    // every load of both rows issued before the first product: one memory
-    // latency per logit, not one per chunk
+    // the loads of both rows issued in two rounds of eight 16-byte chunks per
+    // lane: two memory latencies per logit, not one per chunk
+    constexpr int kRound = kRowChunks / 2;
     const int nch = H / 8;
     const uint4 *w = reinterpret_cast<const uint4 *>(router_w + (size_t)e * H);
     const uint4 *x = reinterpret_cast<const uint4 *>(xh);
-    uint4 wv[kRowChunks], xv[kRowChunks];
-#pragma unroll
-    for (int i = 0; i < kRowChunks; i++) {
-        const int c = lane + 32 * i;
-        wv[i] = c < nch ? __ldg(w + c) : make_uint4(0, 0, 0, 0);
-        xv[i] = c < nch ? x[c] : make_uint4(0, 0, 0, 0);
-    }
     Comp acc[2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll 1
+    for (int i0 = 0; i0 < kRowChunks && lane + 32 * i0 < nch; i0 += kRound) {
+        uint4 wv[kRound], xv[kRound];
 #pragma unroll
-    for (int i = 0; i < kRowChunks; i++) {
-        if (lane + 32 * i >= nch) break;
-        const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w}, xx[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+        for (int i = 0; i < kRound; i++) {
+            const int c = lane + 32 * (i0 + i);
+            wv[i] = c < nch ? __ldg(w + c) : make_uint4(0, 0, 0, 0);
+            xv[i] = c < nch ? x[c] : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            comp_add(acc[q & 1], __fmul_rn(__uint_as_float(xx[q] << 16), __uint_as_float(ww[q] << 16)));
-            comp_add(acc[q & 1],
-                     __fmul_rn(__uint_as_float(xx[q] & 0xFFFF0000u), __uint_as_float(ww[q] & 0xFFFF0000u)));
+        for (int i = 0; i < kRound; i++) {
+            if (lane + 32 * (i0 + i) >= nch) break;
+            const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w}, xx[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                comp_add(acc[q & 1], __fmul_rn(__uint_as_float(xx[q] << 16), __uint_as_float(ww[q] << 16)));
+                comp_add(acc[q & 1],
+                         __fmul_rn(__uint_as_float(xx[q] & 0xFFFF0000u), __uint_as_float(ww[q] & 0xFFFF0000u)));
+            }
         }
     }
     comp_merge(acc[0], acc[1]);
@@ -192,37 +196,13 @@ __device__ double exact_logit(const uint16_t *xh, const uint16_t *router_w, cons
     return ((double)t.s + (double)t.c) + (double)router_b[e];
 }
 
-// Σx² of one bf16 row (H elements, shared memory) by one warp; every lane gets it.
-__device__ double sumsq_row(const uint16_t *row, int H, int lane) {
-    const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
-    int mx = 1;
-    for (int c = lane; c < H / 8; c += 32) {
-        const uint4 v = r4[c];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; q++) mx = max(mx, max(bf16_exp(w[q]), bf16_exp(w[q] >> 16)));
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float sc = exp_scale(mx);
-    Comp acc[2] = {{0.f, 0.f}, {0.f, 0.f}};  // two independent chains
-    for (int c = lane; c < H / 8; c += 32) {
-        const uint4 v = r4[c];
-        comp_add_pair(acc[0], v.x, sc);
-        comp_add_pair(acc[1], v.y, sc);
-        comp_add_pair(acc[0], v.z, sc);
-        comp_add_pair(acc[1], v.w, sc);
-    }
-    comp_merge(acc[0], acc[1]);
-    return comp_result(comp_warp(acc[0]), mx);
-}
-
-// Σx² of one bf16 row held in registers by the whole CTA (kXC chunks of 8 per
-// thread); every thread gets it.
-__device__ double sumsq_block(const uint4 (&xv)[kXC], int lane, int warp, int *s_maxexp, Comp *s_acc) {
+// Σx² of one bf16 row held in registers by the whole CTA of NTH threads (XC
+// chunks of 8 per thread); every thread gets it.
+template <int NTH, int XC>
+__device__ double sumsq_block(const uint4 (&xv)[XC], int lane, int warp, int *s_maxexp, Comp *s_acc) {
     int mx = 1;
 #pragma unroll
-    for (int j = 0; j < kXC; j++) {
+    for (int j = 0; j < XC; j++) {
         const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
         for (int q = 0; q < 4; q++) mx = max(mx, max(bf16_exp(w[q]), bf16_exp(w[q] >> 16)));
@@ -232,11 +212,11 @@ __device__ double sumsq_block(const uint4 (&xv)[kXC], int lane, int warp, int *s
     if (lane == 0) s_maxexp[warp] = mx;
     __syncthreads();
 #pragma unroll
-    for (int w = 0; w < kRouteWarps; w++) mx = max(mx, s_maxexp[w]);
+    for (int w = 0; w < NTH / 32; w++) mx = max(mx, s_maxexp[w]);
     const float sc = exp_scale(mx);
     Comp acc{0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < kXC; j++) {
+    for (int j = 0; j < XC; j++) {
         comp_add_pair(acc, xv[j].x, sc);
         comp_add_pair(acc, xv[j].y, sc);
         comp_add_pair(acc, xv[j].z, sc);
@@ -247,7 +227,7 @@ __device__ double sumsq_block(const uint4 (&xv)[kXC], int lane, int warp, int *s
     __syncthreads();
     Comp tot = s_acc[0];
 #pragma unroll
-    for (int w = 1; w < kRouteWarps; w++) comp_merge(tot, s_acc[w]);
+    for (int w = 1; w < NTH / 32; w++) comp_merge(tot, s_acc[w]);
     return comp_result(tot, mx);
 }
 
@@ -405,7 +385,7 @@ __device__ void exact_candidates(const RouteArgs &a, const uint16_t *xbase, size
     }
 }
 
-__device__ void topk_finish(const RouteArgs &a, int t, int lane, bool need, const double *exs, float my_v, int my_i) {
+__device__ int topk_finish(const RouteArgs &a, int t, int lane, bool need, const double *exs, float my_v, int my_i) {
     const int E = a.bp.E, K = a.bp.K;
     constexpr int NQ = MOE_MAX_EXPERTS / 32;
     double my_d = 0.0;
@@ -445,14 +425,15 @@ __device__ void topk_finish(const RouteArgs &a, int t, int lane, bool need, cons
     float ssum = ew;
 #pragma unroll
     for (int o = 16; o; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+    const int id = valid ? my_i : 0;  // unfilled slot: expert 0, weight 0
     if (lane < K) {
-        const int id = valid ? my_i : 0;  // unfilled slot: expert 0, weight 0
         const float w = (valid && ssum > 0.f) ? a.bp.wscale * (ew / ssum) : 0.f;
         a.ws.ids[t * K + lane] = id;
         a.ws.route_w[t * K + lane] = w;
         if (a.ids_out) a.ids_out[t * K + lane] = id;
         if (a.rw_out) a.rw_out[t * K + lane] = w;
     }
+    return id;  // lane r: slot r's expert
 }
 
 // Bytes of shared memory the permutation needs (per-expert counters).
@@ -573,16 +554,20 @@ __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
     if (tid == 0) a.ws.tickets[0] = 0u;  // re-arm for the next launch
 }
 
-// Normalise one token row held in registers into xh (shared) and, if `store`,
-// into the workspace copies: bf16 natural order, fp16, and (store_mma) the
-// grouped GEMM's pair order.
-__device__ __forceinline__ void normalise_row(const RouteArgs &a, const uint4 (&xv)[kXC], const float4 (&gm)[kXC][2],
-                                              int t, double r, uint16_t *xh, bool store) {
+// Normalise one token row held in registers (XC chunks of 8 per thread) into
+// xh (shared memory; skipped when null) and, if `store`, into the workspace
+// copies: bf16 natural order, and as a.forms asks, fp16 (the GEMV and the fp16
+// grouped GEMM) and the grouped GEMM's pair order (its bf16 variant).  Returns
+// this thread's sum of x_hat^2.
+template <int NTH, int XC>
+__device__ __forceinline__ float normalise_row(const RouteArgs &a, const uint4 (&xv)[XC], const float4 (&gm)[XC][2],
+                                               int t, double r, uint16_t *xh, bool store) {
     const int H = a.bp.H, nchunk = H / 8;
     const float r32 = (float)r;
+    float xs = 0.f;
 #pragma unroll
-    for (int j = 0; j < kXC; j++) {
-        const int c = threadIdx.x + kRouteThreads * j;
+    for (int j = 0; j < XC; j++) {
+        const int c = threadIdx.x + NTH * j;
         if (c >= nchunk) continue;
         const uint32_t w4[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
         const float gg[8] = {gm[j][0].x, gm[j][0].y, gm[j][0].z, gm[j][0].w,
@@ -590,28 +575,33 @@ __device__ __forceinline__ void normalise_row(const RouteArgs &a, const uint4 (&
         uint32_t hb[8];
 #pragma unroll
         for (int q = 0; q < 8; q++) hb[q] = norm_elem((w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, gg[q], r32, r);
+#pragma unroll
+        for (int q = 0; q < 8; q++) xs = fmaf(__uint_as_float(hb[q] << 16), __uint_as_float(hb[q] << 16), xs);
         const uint4 nat = make_uint4(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16, hb[4] | hb[5] << 16,
                                      hb[6] | hb[7] << 16);
-        *reinterpret_cast<uint4 *>(xh + 8 * c) = nat;
+        if (xh) *reinterpret_cast<uint4 *>(xh + 8 * c) = nat;
         if (store) {
             const size_t go = (size_t)t * H + 8 * c;
             *reinterpret_cast<uint4 *>(a.ws.xhat + go) = nat;
-            if (a.store_mma) {
+            if (a.forms & kFormMma) {
                 // pair order inside each 8-element chunk: (e0,e4),(e1,e5),(e2,e6),(e3,e7)
                 *reinterpret_cast<uint4 *>(a.ws.xhat_mma + go) = make_uint4(
                     hb[0] | hb[4] << 16, hb[1] | hb[5] << 16, hb[2] | hb[6] << 16, hb[3] | hb[7] << 16);
             }
-            uint32_t f[8];
+            if (a.forms & kFormF16) {
+                uint32_t f[8];
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));  // exact for |x_hat| >= 2^-17
-                f[q] = *reinterpret_cast<uint16_t *>(&hh);
+                for (int q = 0; q < 8; q++) {
+                    __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));  // exact for |x_hat| >= 2^-17
+                    f[q] = *reinterpret_cast<uint16_t *>(&hh);
+                }
+                *reinterpret_cast<uint4 *>(a.ws.xhat16 + go) =
+                    make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
             }
-            *reinterpret_cast<uint4 *>(a.ws.xhat16 + go) =
-                make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
             if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + go) = nat;
         }
     }
+    return xs;
 }
 
 // Router logit of expert e (row w, shared or global memory) for one x_hat row
@@ -676,6 +666,9 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     const int t = blockIdx.x;
     const uint32_t rank = cluster_ctarank();
     const int epc = a.epc, e0 = (int)rank * epc, ne = max(0, min(epc, E - e0));
+    // the gate/up GEMV (one persistent CTA per SM, waiting for this grid's
+    // results) may take the SMs this kernel leaves free and set itself up
+    asm volatile("griddepcontrol.launch_dependents;");
     // layout: [router rows] [permutation counters] [x_hat row] [logits E] [bounds E] [exact logits E]
     // [candidates E]
     const size_t rows_b = STAGED ? (size_t)epc * H * 2 : 0;
@@ -724,12 +717,12 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
         gm[j][0] = c < nchunk ? __ldg(g4) : make_float4(0.f, 0.f, 0.f, 0.f);
         gm[j][1] = c < nchunk ? __ldg(g4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const double ss = sumsq_block(xv, lane, warp, s_maxexp, s_acc);
+    const double ss = sumsq_block<kRouteThreads, kXC>(xv, lane, warp, s_maxexp, s_acc);
     MOE_PHASE_MARK(1);
     if (tid == 0) s_r = rsqrt_d(ss * a.inv_h + a.bp.eps);
     __syncthreads();
     MOE_PHASE_MARK(2);
-    normalise_row(a, xv, gm, t, s_r, xh, rank == 0);
+    normalise_row<kRouteThreads, kXC>(a, xv, gm, t, s_r, xh, rank == 0);
     __syncthreads();
     MOE_PHASE_MARK(3);
     // -------------------------------------------------------------- router
@@ -802,9 +795,10 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
 
 // Larger batches (T > 32): four kernels chained by programmatic dependent
 // launch.
-//  * moe_route_norm_kernel: a warp per token normalises it (x_hat in its
-//    three forms) and records an upper bound of |x_hat|; a warp per router
-//    row records an upper bound of |w|.
+//  * moe_route_norm_kernel: a CTA per token normalises it (x_hat in the forms
+//    the expert kernels read) and records an upper bound of |x_hat|; a warp
+//    per router row records an upper bound of |w|; the expert counts are
+//    zeroed for the top-k kernel.
 //  * moe_router_gemm_kernel: the logits as a register-tiled SIMT GEMM over
 //    64-token x 64-expert tiles (4 x 4 per thread), K split over grid.z when
 //    the tiles alone do not fill the GPU.  Products of two bf16 are exact in
@@ -815,11 +809,11 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
 //  * moe_route_topk_kernel: a warp per token sums the K-split partials in a
 //    fixed order, adds the bias and the rigorous bound 2 gamma_n (|x_hat| |w| +
 //    |b| + |l|) (Cauchy-Schwarz bounds sum |x_i w_i|), and selects the top-k,
-//    recomputing exactly whatever the bounds cannot order.
+//    recomputing exactly whatever the bounds cannot order; it adds its routes
+//    to the expert counts.
 //  * moe_permute_kernel: the token->expert permutation, a CTA per expert.
 constexpr int kGT = 64, kGE = 64, kGK = 32;  // GEMM tile: tokens x experts, k-chunk
 constexpr int kGPad = 68;                    // padded row of the transposed tiles (floats; 16-byte aligned)
-constexpr int kNormRows = 8;                 // tokens (or router rows) per CTA of the norm kernel
 constexpr int kMaxKSplit = 16;               // K splits of the logits GEMM
 
 // Roundings a product can pass through in the large-batch logits, with a
@@ -827,106 +821,78 @@ constexpr int kMaxKSplit = 16;               // K splits of the logits GEMM
 // term, counted as 4 more), the K-split partials, the bias.
 __device__ __forceinline__ int router_chain(int ks) { return kGK + 6 + ks + 2; }
 
-__global__ void __launch_bounds__(kRouteThreads) moe_route_norm_kernel(RouteArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
+constexpr int kNormThreads = 128;                          // one token per CTA of the norm kernel
+constexpr int kNormXC = kRouteThreads * kXC / kNormThreads;  // 16-byte chunks of the row per thread
+
+__global__ void __launch_bounds__(kNormThreads) moe_route_norm_kernel(RouteArgs a) {
     const int H = a.bp.H, E = a.bp.E;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    asm volatile("griddepcontrol.launch_dependents;");
-    const int tok_blocks = (a.T + kNormRows - 1) / kNormRows;
-    if ((int)blockIdx.x >= tok_blocks) {
-        // |w| of router rows: a sum of squares (relative error below 2e-6), one
-        // correctly rounded square root, then a margin well above both
-        const int e = ((int)blockIdx.x - tok_blocks) * kNormRows + warp;
-        if (e >= E) return;
-        const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)e * H);
-        uint4 wv[kRowChunks];  // the whole row's loads in flight at once
+    if ((int)blockIdx.x >= a.T) {
+        // |w| of router rows, a warp per row: a sum of squares (relative error
+        // below 2e-6), one correctly rounded square root, then a margin well
+        // above both
+        const int e = ((int)blockIdx.x - a.T) * (kNormThreads / 32) + warp;
+        if (e < E) {
+            const uint4 *wr = reinterpret_cast<const uint4 *>(a.router_w + (size_t)e * H);
+            uint4 wv[kRowChunks];  // the whole row's loads in flight at once
 #pragma unroll
-        for (int i = 0; i < kRowChunks; i++) {
-            const int c = lane + 32 * i;
-            wv[i] = c < H / 8 ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
-        }
-        float sw = 0.f;
-#pragma unroll
-        for (int i = 0; i < kRowChunks; i++) {
-            const uint4 v = wv[i];
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
-                sw = fmaf(lo, lo, fmaf(hi, hi, sw));
+            for (int i = 0; i < kRowChunks; i++) {
+                const int c = lane + 32 * i;
+                wv[i] = c < H / 8 ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
             }
+            float sw = 0.f;
+#pragma unroll
+            for (int i = 0; i < kRowChunks; i++) {
+                const uint4 v = wv[i];
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
+                    sw = fmaf(lo, lo, fmaf(hi, hi, sw));
+                }
+            }
+            const float wn = sqrtf(warp_sum_f(sw)) * (1.0f + 0x1p-14f);
+            if (lane == 0) a.ws.wnorm[e] = wn;
         }
-        const float wn = sqrtf(warp_sum_f(sw)) * (1.0f + 0x1p-14f);
-        if (lane == 0) a.ws.wnorm[e] = wn;
+        asm volatile("griddepcontrol.launch_dependents;");
         return;
     }
-    uint16_t *row = reinterpret_cast<uint16_t *>(smem) + (size_t)warp * H;   // [8][H]
-    float *gsm = reinterpret_cast<float *>(smem + (size_t)kNormRows * H * 2);  // gamma [H]
-    // gamma and the token row: every load issued before the first use
-    float4 gv[kXC * 2];
+    // one token per CTA: the row and gamma in registers (kNormXC chunks of 8 per thread)
+    __shared__ int s_maxexp[kNormThreads / 32];
+    __shared__ Comp s_acc[kNormThreads / 32];
+    __shared__ float s_xs[kNormThreads / 32];
+    __shared__ double s_r;
+    const int t = blockIdx.x, nchunk = H / 8;
+    if (t == 0)  // expert counts start from zero; the top-k kernel adds its routes
+        for (int e = tid; e <= E; e += kNormThreads) a.ws.counts[e] = 0;
+    float4 gm[kNormXC][2];
+    uint4 xv[kNormXC];
+    const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
 #pragma unroll
-    for (int i = 0; i < kXC * 2; i++) {
-        const int c = tid + kRouteThreads * i;
-        gv[i] = c < H / 4 ? __ldg(reinterpret_cast<const float4 *>(a.gamma) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < kNormXC; j++) {
+        const int c = tid + kNormThreads * j;
+        const float4 *g4 = reinterpret_cast<const float4 *>(a.gamma) + 2 * c;
+        xv[j] = c < nchunk ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        gm[j][0] = c < nchunk ? __ldg(g4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        gm[j][1] = c < nchunk ? __ldg(g4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const int t = blockIdx.x * kNormRows + warp;
-    uint4 xv[kRowChunks];
-    if (t < a.T) {
-        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H);
-#pragma unroll
-        for (int i = 0; i < kRowChunks; i++) {
-            const int c = lane + 32 * i;
-            xv[i] = c < H / 8 ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < kXC * 2; i++) {
-        const int c = tid + kRouteThreads * i;
-        if (c < H / 4) reinterpret_cast<float4 *>(gsm)[c] = gv[i];
-    }
+    const double ss = sumsq_block<kNormThreads, kNormXC>(xv, lane, warp, s_maxexp, s_acc);
+    if (tid == 0) s_r = rsqrt_d(ss * a.inv_h + a.bp.eps);
     __syncthreads();
-    if (t >= a.T) return;
+    const float xs = warp_sum_f(normalise_row<kNormThreads, kNormXC>(a, xv, gm, t, s_r, nullptr, true));
+    if (lane == 0) s_xs[warp] = xs;
+    __syncthreads();
+    if (tid == 0) {
+        float tot = 0.f;
 #pragma unroll
-    for (int i = 0; i < kRowChunks; i++) {
-        const int c = lane + 32 * i;
-        if (c < H / 8) reinterpret_cast<uint4 *>(row)[c] = xv[i];
+        for (int w = 0; w < kNormThreads / 32; w++) tot += s_xs[w];
+        // |x_hat| with a margin above the error of the sum (positive terms) and of the root
+        a.ws.xnorm[t] = sqrtf(tot) * (1.0f + 0x1p-14f);
     }
-    __syncwarp();
-    const double ssum = sumsq_row(row, H, lane);
-    const double r = rsqrt_d(ssum * a.inv_h + a.bp.eps);  // same in every lane
-    const float r32 = (float)r;
-    float xs = 0.f;  // sum of x_hat^2 (for the router's error bound)
-    for (int c = lane; c < H / 8; c += 32) {
-        const uint4 xv = reinterpret_cast<const uint4 *>(row)[c];
-        const float4 g0 = reinterpret_cast<const float4 *>(gsm)[2 * c];
-        const float4 g1 = reinterpret_cast<const float4 *>(gsm)[2 * c + 1];
-        const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
-        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        uint32_t hb[8];
-#pragma unroll
-        for (int q = 0; q < 8; q++) hb[q] = norm_elem((w4[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, gg[q], r32, r);
-#pragma unroll
-        for (int q = 0; q < 8; q++) xs = fmaf(__uint_as_float(hb[q] << 16), __uint_as_float(hb[q] << 16), xs);
-        const uint4 nat = make_uint4(hb[0] | hb[1] << 16, hb[2] | hb[3] << 16, hb[4] | hb[5] << 16,
-                                     hb[6] | hb[7] << 16);
-        const size_t go = (size_t)t * H + 8 * c;
-        *reinterpret_cast<uint4 *>(a.ws.xhat + go) = nat;
-        if (a.store_mma)
-            *reinterpret_cast<uint4 *>(a.ws.xhat_mma + go) =
-                make_uint4(hb[0] | hb[4] << 16, hb[1] | hb[5] << 16, hb[2] | hb[6] << 16, hb[3] | hb[7] << 16);
-        uint32_t f[8];
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            __half hh = __float2half_rn(__uint_as_float(hb[q] << 16));
-            f[q] = *reinterpret_cast<uint16_t *>(&hh);
-        }
-        *reinterpret_cast<uint4 *>(a.ws.xhat16 + go) =
-            make_uint4(f[0] | f[1] << 16, f[2] | f[3] << 16, f[4] | f[5] << 16, f[6] | f[7] << 16);
-        if (a.xhat_out) *reinterpret_cast<uint4 *>(a.xhat_out + go) = nat;
-    }
-    // |x_hat| with a margin above the error of the sum (positive terms) and of the root
-    const float xn = sqrtf(warp_sum_f(xs)) * (1.0f + 0x1p-14f);
-    if (lane == 0) a.ws.xnorm[t] = xn;
+    // the logits GEMM may launch once every CTA is here: launched earlier, its
+    // CTAs would take SM slots as the norm CTAs happen to leave them, not
+    // evenly, and some SMs would run several of its equal-sized CTAs
+    asm volatile("griddepcontrol.launch_dependents;");
 }
 
 // lpart[kz][t][e] = sum over the kz-th K range of x_hat[t][k] * W[e][k].
@@ -942,7 +908,6 @@ __global__ void __launch_bounds__(kGThreads) moe_router_gemm_kernel(const uint16
     __shared__ __align__(16) float sx[2][kGK][kGPad];
     __shared__ __align__(16) float sw[2][kGK][kGPad];
     const int tid = threadIdx.x, tx = tid & 7, ty = tid >> 3;
-    asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // x_hat comes from the norm kernel
     const int t0 = blockIdx.x * kGT, e0 = blockIdx.y * kGE, kz = blockIdx.z;
     const int nkc = (H + kGK - 1) / kGK;
@@ -1017,6 +982,8 @@ __global__ void __launch_bounds__(kGThreads) moe_router_gemm_kernel(const uint16
         if (kc + 1 < kc1) stash(buf ^ 1, xv, wv);
         __syncthreads();
     }
+    // the top-k kernel may launch now (its CTAs then find the SMs free and spread evenly)
+    asm volatile("griddepcontrol.launch_dependents;");
 #pragma unroll
     for (int i = 0; i < 4; i++) {
         const int t = t0 + 4 * ty + i;
@@ -1030,37 +997,80 @@ __global__ void __launch_bounds__(kGThreads) moe_router_gemm_kernel(const uint16
 }
 
 // A warp per token: logits and bounds into shared memory, then top-k + softmax
-// (the exact logits of uncertain tokens by all warps of the CTA).
-__global__ void __launch_bounds__(kRouteThreads) moe_route_topk_kernel(RouteArgs a, const float *lpart, int ks) {
+// (the exact logits of uncertain tokens by all warps of the CTA); the CTA's
+// routes are counted per expert in shared memory and added to the expert
+// counts.
+__global__ void __launch_bounds__(kRouteThreads, 2) moe_route_topk_kernel(RouteArgs a, const float *lpart, int ks) {
     extern __shared__ __align__(128) unsigned char smem[];
-    const int E = a.bp.E, H = a.bp.H;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    asm volatile("griddepcontrol.launch_dependents;");
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // partials from the GEMM, norms from the norm kernel
-    const int t0 = blockIdx.x * kRouteWarps, t = t0 + warp;
+    const int E = a.bp.E, H = a.bp.H, K = a.bp.K;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     double *exs = reinterpret_cast<double *>(smem);                                    // [8][E]
     float *lg = reinterpret_cast<float *>(smem + (size_t)kRouteWarps * E * 8) + (size_t)warp * 2 * E;  // [8][2][E]
     float *lb = lg + E;
     uint16_t *cand = reinterpret_cast<uint16_t *>(smem + (size_t)kRouteWarps * E * 16);  // [8][E]
     __shared__ int s_ncand[kRouteWarps];
+    __shared__ int s_hist[MOE_MAX_EXPERTS];
+    for (int e = tid; e < E; e += kRouteThreads) s_hist[e] = 0;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // partials from the GEMM, norms from the norm kernel
+    const int t0 = blockIdx.x * kRouteWarps, t = t0 + warp;
     float my_v = -INFINITY;
     int my_i = kInvalid;
     bool need = false;
     if (t < a.T) {
-        const float chain = (float)router_chain(ks), xn = a.ws.xnorm[t];
-        for (int e = lane; e < E; e += 32) {
-            // every partial's load in flight before the sum (in K order)
+        const float chain = (float)router_chain(ks), xn = __ldcg(a.ws.xnorm + t);
+        // the K-split partials of each logit summed in K order (into lg), their
+        // loads issued ahead: all splits at once for up to 32 experts (one per
+        // lane), 16-byte loads of eight splits at a time for wider rows
+        if (E <= 32) {
             float pv[kMaxKSplit];
 #pragma unroll
             for (int kz = 0; kz < kMaxKSplit; kz++)
-                pv[kz] = kz < ks ? __ldcg(lpart + ((size_t)kz * a.T + t) * E + e) : 0.f;
-            float s = 0.f;
+                pv[kz] = (kz < ks && lane < E) ? __ldcg(lpart + ((size_t)kz * a.T + t) * E + lane) : 0.f;
+            float sum = 0.f;
 #pragma unroll
             for (int kz = 0; kz < kMaxKSplit; kz++)
-                if (kz < ks) s += pv[kz];
-            const float b = a.router_b[e], l = s + b;
+                if (kz < ks) sum += pv[kz];
+            if (lane < E) lg[lane] = sum;
+        } else if (E % 4 == 0) {
+            const int nv = E / 4;  // float4 per partial row: lane owns float4 lane and lane + 32
+            float4 sum[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+            for (int k0 = 0; k0 < ks; k0 += 8) {
+                float4 pv[8][2];
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const int v = lane + 32 * h;
+                        pv[i][h] = (k0 + i < ks && v < nv)
+                                       ? __ldcg(reinterpret_cast<const float4 *>(lpart + ((size_t)(k0 + i) * a.T + t) * E) + v)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+                    if (k0 + i < ks)
+#pragma unroll
+                        for (int h = 0; h < 2; h++) {
+                            sum[h].x += pv[i][h].x;
+                            sum[h].y += pv[i][h].y;
+                            sum[h].z += pv[i][h].z;
+                            sum[h].w += pv[i][h].w;
+                        }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; h++)
+                if (lane + 32 * h < nv) reinterpret_cast<float4 *>(lg)[lane + 32 * h] = sum[h];
+        } else {
+            for (int e = lane; e < E; e += 32) {
+                float sum = 0.f;
+                for (int kz = 0; kz < ks; kz++) sum += __ldcg(lpart + ((size_t)kz * a.T + t) * E + e);
+                lg[e] = sum;
+            }
+        }
+        __syncwarp();
+        for (int e = lane; e < E; e += 32) {
+            const float b = a.router_b[e], l = lg[e] + b;
             lg[e] = l;
-            lb[e] = 2.0f * chain * 0x1p-24f * (xn * a.ws.wnorm[e] + fabsf(b) + fabsf(l)) + 1e-30f;
+            lb[e] = 2.0f * chain * 0x1p-24f * (xn * __ldcg(a.ws.wnorm + e) + fabsf(b) + fabsf(l)) + 1e-30f;
         }
         __syncwarp();
         need = topk_select<false>(lg, lb, a, lane, my_v, my_i, exs + (size_t)warp * E, cand + (size_t)warp * E,
@@ -1072,17 +1082,23 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_topk_kernel(RouteArgs
     exact_candidates(a, a.ws.xhat + (size_t)t0 * H, (size_t)H, cand, s_ncand, kRouteWarps, exs, warp, kRouteWarps,
                      lane);
     __syncthreads();
-    if (t < a.T) topk_finish(a, t, lane, need, exs + (size_t)warp * E, my_v, my_i);
+    if (t < a.T) {
+        const int id = topk_finish(a, t, lane, need, exs + (size_t)warp * E, my_v, my_i);
+        if (lane < K) atomicAdd(&s_hist[id], 1);
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kRouteThreads)
+        if (s_hist[e]) atomicAdd(a.ws.counts + e, s_hist[e]);
+    asm volatile("griddepcontrol.launch_dependents;");
 }
 
 // The permutation of a large batch (the same result as build_permutation),
-// one CTA per expert (and one for the shared expert).  Every CTA counts the
-// routes of all experts (a shared-memory histogram), scans the counts and the
-// tile counts, then collects its own expert's routes in route order: warp w
-// owns the w-th contiguous segment of the routes; a first pass counts each
-// warp's routes of the expert, a scan over warps places the segments, a
-// second pass writes the entries (token, slot, weight), the inverse map and
-// the expert's tiles.
+// one CTA per expert (and one for the shared expert).  Every CTA scans the
+// expert counts (added up by the top-k kernel) and the tile counts, then
+// collects its own expert's routes in route order: warp w owns the w-th
+// contiguous segment of the routes; a first pass counts each warp's routes of
+// the expert, a scan over warps places the segments, a second pass writes the
+// entries (token, slot, weight), the inverse map and the expert's tiles.
 constexpr int kPermThreads = 512;
 constexpr int kPermWarps = kPermThreads / 32;
 constexpr int kPermPer = 16;  // route ids per lane in flight
@@ -1101,32 +1117,27 @@ __global__ void __launch_bounds__(kPermThreads) moe_permute_kernel(RouteArgs a) 
     int32_t *toff = tcnt + (EE + 1);                    // [EE + 1]
     int32_t *wn = toff + (EE + 1);                      // [32] this expert's routes per warp segment
     int32_t *wo = wn + 32;                              // [32] their exclusive prefix
-    for (int e = tid; e <= EE; e += kPermThreads) cnt[e] = 0;
-    __syncthreads();
+    for (int e = tid; e < EE; e += kPermThreads) cnt[e] = e < E ? __ldcg(a.ws.counts + e) : a.T;
     const int seg = (R + kPermWarps - 1) / kPermWarps;
     const int r0 = min(R, warp * seg), r1 = min(R, r0 + seg);
-    auto expert_of = [&](int r) {
-        const int e = __ldcg(a.ws.ids + r);
-        return (unsigned)e < (unsigned)E ? e : 0;  // out of range: counted as expert 0 (reported below)
-    };
-    // pass 1: histogram of every expert, and this warp's routes of `me`
+    // pass 1: this warp's routes of `me` (ids out of range count as expert 0,
+    // as the top-k kernel never writes one)
     int mine = 0;
     for (int b = r0; b < r1; b += 32 * kPermPer) {
         int ev[kPermPer];
 #pragma unroll
         for (int i = 0; i < kPermPer; i++) {
             const int r = b + 32 * i + lane;
-            ev[i] = r < r1 ? expert_of(r) : -1;
+            ev[i] = r < r1 ? __ldcg(a.ws.ids + r) : -1;
         }
 #pragma unroll
         for (int i = 0; i < kPermPer; i++) {
-            if (ev[i] >= 0) atomicAdd(&cnt[ev[i]], 1);
-            mine += __popc(__ballot_sync(0xffffffffu, ev[i] == me));
+            const int r = b + 32 * i + lane;
+            const int e = (r < r1 && (unsigned)ev[i] >= (unsigned)E) ? 0 : ev[i];
+            mine += __popc(__ballot_sync(0xffffffffu, e == me));
         }
     }
     if (lane == 0) wn[warp] = mine;
-    __syncthreads();
-    if (ns && tid == 0) cnt[E] = a.T;
     __syncthreads();
     if (warp == 0) warp_exclusive_scan(cnt, offs, EE, lane);
     if (warp == 1) {
@@ -1146,10 +1157,7 @@ __global__ void __launch_bounds__(kPermThreads) moe_permute_kernel(RouteArgs a) 
     }
     __syncthreads();
     // counts, offsets and tiles of this expert; the totals by CTA 0
-    if (tid == 0) {
-        if (me < E) a.ws.counts[me] = cnt[me];
-        a.ws.offsets[me] = offs[me];
-    }
+    if (tid == 0) a.ws.offsets[me] = offs[me];
     {
         const int n = tcnt[me], base = toff[me];
         for (int k = tid; k < n && base + k < a.ws.max_tiles; k += kPermThreads) {
@@ -1173,15 +1181,17 @@ __global__ void __launch_bounds__(kPermThreads) moe_permute_kernel(RouteArgs a) 
         }
         return;
     }
-    // pass 2: this expert's routes in route order
+    // pass 2: this expert's routes in route order (ids and weights loaded ahead)
     int pos = offs[me] + wo[warp];
     const uint32_t lt = (1u << lane) - 1u;
     for (int b = r0; b < r1; b += 32 * kPermPer) {
         int ev[kPermPer];
+        float wv[kPermPer];
 #pragma unroll
         for (int i = 0; i < kPermPer; i++) {
             const int r = b + 32 * i + lane;
             ev[i] = r < r1 ? __ldcg(a.ws.ids + r) : -1;
+            wv[i] = r < r1 ? __ldcg(a.ws.route_w + r) : 0.f;
         }
 #pragma unroll
         for (int i = 0; i < kPermPer; i++) {
@@ -1198,7 +1208,7 @@ __global__ void __launch_bounds__(kPermThreads) moe_permute_kernel(RouteArgs a) 
                 const int t = r / K, sl = r - t * K;
                 a.ws.perm_token[p] = t;
                 a.ws.perm_slot[p] = sl;
-                a.ws.perm_w[p] = __ldcg(a.ws.route_w + r);
+                a.ws.perm_w[p] = wv[i];
                 a.ws.loc[t * KK + sl] = p;
             }
             pos += __popc(m);
@@ -1257,10 +1267,10 @@ int route_ticket_count(int T) { return T + 1; }
 
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x, const float *gamma,
                          const uint16_t *router_w, const float *router_b, int T, int32_t *ids_out, float *rw_out,
-                         uint16_t *xhat_out, int tile_rows, int router_exact, int store_mma, cudaStream_t st) {
+                         uint16_t *xhat_out, int tile_rows, int router_exact, int forms, cudaStream_t st) {
     if (bp.H / 8 > kRouteThreads * kXC) return cudaErrorInvalidValue;
     RouteArgs a{bp, ws, x, gamma, router_w, router_b, T, ids_out, rw_out, xhat_out, tile_rows, router_exact, 0,
-                store_mma, 1.0 / (double)bp.H};
+                forms, 1.0 / (double)bp.H};
     if (T <= 32) {
         // many experts: 16-CTA clusters (a non-portable size) keep every CTA's
         // router rows in shared memory; where such a cluster cannot be
@@ -1284,27 +1294,36 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
         MOE_CUDA_TRY(launch_small_geo(a, g, st));
         return cudaGetLastError();
     }
-    static bool donen = false, donet = false;
+    static bool donet = false;
     int n_sm = 0, dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
-    // norm (+ the router rows' norms)
-    const int nblk = (T + kNormRows - 1) / kNormRows + (bp.E + kNormRows - 1) / kNormRows;
-    const size_t nsm = (size_t)kNormRows * bp.H * 2 + (size_t)bp.H * 4;
-    if (nsm > 224 * 1024) return cudaErrorInvalidValue;
-    MOE_CUDA_TRY(smem_optin_once(moe_route_norm_kernel, donen));
-    moe_route_norm_kernel<<<nblk, kRouteThreads, nsm, st>>>(a);
+    // norm, a CTA per token (+ the router rows' norms, a warp per row)
+    moe_route_norm_kernel<<<T + (bp.E + kNormThreads / 32 - 1) / (kNormThreads / 32), kNormThreads, 0, st>>>(a);
     MOE_CUDA_TRY(cudaGetLastError());
-    // logits: split K while the tiles alone leave SMs idle (partials live in y,
-    // which is free until the down projection)
+    // logits: K split so that the CTAs' waves times their chunks is least (the
+    // partials live in y, which is free until the down projection; fewer
+    // splits on a tie, since each split adds a rounding to the bound)
+    static int gemm_per_sm = 0;
+    if (!gemm_per_sm) {
+        MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&gemm_per_sm, moe_router_gemm_kernel, kGThreads, 0));
+        if (gemm_per_sm < 1) gemm_per_sm = 1;
+    }
     const int tiles = ((T + kGT - 1) / kGT) * ((bp.E + kGE - 1) / kGE);
     const int nkc = (bp.H + kGK - 1) / kGK;
-    int ks = (6 * n_sm + tiles - 1) / tiles;  // about six GEMM CTAs per SM: waves end close together
-    ks = ks < 1 ? 1 : (ks > kMaxKSplit ? kMaxKSplit : ks);
-    if (ks > nkc / 4) ks = nkc / 4 > 0 ? nkc / 4 : 1;
-    while (ks > 1 && (size_t)ks * bp.E > (size_t)(bp.K + bp.n_shared) * bp.H) ks--;
-    const int kc_per = (nkc + ks - 1) / ks;
-    ks = (nkc + kc_per - 1) / kc_per;
+    const long long slots = (long long)gemm_per_sm * n_sm;
+    int ks = 1, kc_per = nkc;
+    long long best = -1;
+    for (int k = 1; k <= kMaxKSplit && k <= (nkc / 4 > 0 ? nkc / 4 : 1); k++) {
+        const int per = (nkc + k - 1) / k, kk = (nkc + per - 1) / per;
+        if (kk > 1 && (size_t)kk * bp.E > (size_t)(bp.K + bp.n_shared) * bp.H) break;
+        const long long cost = ((tiles * (long long)kk + slots - 1) / slots) * per;
+        if (best < 0 || cost < best) {
+            best = cost;
+            ks = kk;
+            kc_per = per;
+        }
+    }
     MOE_CUDA_TRY(launch_pdl(moe_router_gemm_kernel, dim3((T + kGT - 1) / kGT, (bp.E + kGE - 1) / kGE, ks), dim3(kGThreads),
                             0, st, (const uint16_t *)ws.xhat, router_w, T, bp.E, bp.H, kc_per, ws.y));
     // top-k + softmax, a warp per token
