@@ -6,8 +6,9 @@ permutation, MXFP4 gate/up + SwiGLU, MXFP4 down, weighted combine + residual)
 over one batch of the workload.  The headline workload is the largest
 single-GPU one: the 24-layer stack of independently seeded gpt-oss MoE blocks
 (hidden 2880, 32 experts, top-4, expert_hidden 2880, ~10 GB of MXFP4 expert
-weights resident) decoding 16 tokens, each layer's fp32 output cast to bf16 as
-the next layer's input.  In the same run every other workload is measured too
+weights resident) decoding 16 tokens, each layer's output rounded to bf16 as
+the next layer's input (written so by the layer itself, the "out_bf16" plan
+option).  In the same run every other workload is measured too
 (1-token decode, the 8-token hot-2 batch, the stack at 1 and 4 tokens, prefill
 at 128 and 512 tokens, the DeepSeek-V4-Flash-shaped block at 1 and 2048
 tokens) and reported under "configs", each with its own rate, roofline and
@@ -298,9 +299,12 @@ class Workload:
                 blk.update({k: ex[k] for k in ("codes", "scales", "bias")})
                 if sh.n_shared:
                     blk["shared"] = ex["shared"]
-                plan = moe.Plan(sh, max_tokens=T, **self.opts).alloc_workspace().load_weights(moe.DeviceBlock(blk))
+                # every layer but the last writes its output as the next layer's bf16 input
+                last = layer == self.layers - 1
+                plan = moe.Plan(sh, max_tokens=T, **self.opts, **({} if last else {"out_bf16": 1}))
+                plan.alloc_workspace().load_weights(moe.DeviceBlock(blk))
                 chain.append(dict(plan=plan, x=torch.empty((T, H), dtype=torch.int16, device="cuda"),
-                                  out=torch.empty((T, H), dtype=torch.float32, device="cuda"),
+                                  out=torch.empty((T, H), dtype=torch.float32, device="cuda") if last else None,
                                   ids=torch.empty((T, K), dtype=torch.int32, device="cuda")))
             xb = synth.make_tokens(wid, T, H, layer=s + 100 * rank)
             chain[0]["x"].copy_(torch.from_numpy(xb.view(np.int16)))
@@ -311,12 +315,10 @@ class Workload:
         return [ly["plan"] for ly in d["chain"]]
 
     def forward_set(self, d, stream):
-        from mxfp4_mixture_experts_rms_gb300 import moe
         ls = d["chain"]
         for i, ly in enumerate(ls):
-            ly["plan"].forward(ly["x"], ly["out"], ly["ids"], stream=stream)
-            if i + 1 < len(ls):
-                moe.cast_f32_to_bf16(ly["out"], ls[i + 1]["x"], stream=stream)
+            out = ly["out"] if i + 1 == len(ls) else ls[i + 1]["x"]
+            ly["plan"].forward(ly["x"], out, ly["ids"], stream=stream)
 
     def step(self, i, stream):
         self.forward_set(self.sets[i % len(self.sets)], stream)
@@ -470,7 +472,7 @@ def summarise(w, r, args, world):
            "step_frac_of_bf16_peak": step_flops / step_s / 1e12 / bf16_peak,
            "binding_roof_frac": max(step_bytes / (hbm * 1e9), step_flops / (bf16_peak * 1e12)) / step_s,
            "clocks": r["clocks"],
-           "gpu_launches": (launches_per_forward(w.path, T) * n_blocks + (n_blocks - 1)) * steps}
+           "gpu_launches": launches_per_forward(w.path, T) * n_blocks * steps}
     if "tot" in r:
         tot, cnt = r["tot"], r["cnt"]
         avg_ms = [t / c if c else 0.0 for t, c in zip(tot, cnt)]

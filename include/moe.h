@@ -124,6 +124,15 @@ void moe_plan_destroy(moe_plan *plan);
  *                       then reports MOE_EDEVICE through
  *                       moe_get_device_status and its outputs are void.
  *                       0 (default): off
+ *   "out_bf16"          1: the forwards write `out` as bf16 [T][hidden] --
+ *                       x + the block's output rounded to nearest (ties to
+ *                       even), exactly what moe_cast_f32_to_bf16 makes of
+ *                       the fp32 output -- so that a stack of blocks passes
+ *                       each block's out to the next as its x (the residual
+ *                       stream between layers, goosedump gpt_oss.rs `forward`:
+ *                       `vector_add(&mut hidden, &mixture)` per layer) with
+ *                       no separate cast; `out` then needs T * hidden * 2
+ *                       bytes.  0 (default): fp32 out
  *   "profile"           1: time each kernel launch with CUDA events (see
  *                       moe_profile_read); 0: off (default)
  * Options that change the workspace size must be set before moe_set_workspace. */
@@ -165,7 +174,8 @@ int moe_load_weights(moe_plan *plan, const moe_weights *w);
 /* The block (turbospark-runtime gptoss/mod.rs, module doc comment; goosedump
  * gpt_oss.rs `mixture_of_experts`, `mixture_of_experts_batch`,
  * `mix_expert_outputs`, `top_experts`):
- * out[T][H] (float) = x + MoE(x) for x bf16 [T][H]; route_ids_out int32
+ * out[T][H] (float; bf16 with the "out_bf16" option) = x + MoE(x) for x bf16
+ * [T][H]; route_ids_out int32
  * [T][top_k] (may be NULL; 4-byte aligned) gets the selected experts of each
  * token in descending-logit order.  x and out (16-byte aligned) must not
  * alias.  tokens = 0 is a no-op.  MOE_EINVAL on NULL, misaligned or aliasing

@@ -71,6 +71,7 @@ struct moe_plan {
     bool pf_f16 = false;
     // FP4 activations: the grouped GEMM on the block-scaled FP4 tensor cores (kind::mxf4)
     bool act_fp4 = false;
+    bool out_bf16 = false;  // out receives bf16 (the next stacked block's input) instead of fp32
     Mxf4Weights mxf4{};
     bool have_mxf4 = false;
     uint8_t *mxf4_scales = nullptr;  // owned: weight scales repacked into the kernel's atoms
@@ -286,7 +287,7 @@ int enqueue_forward(moe_plan *p, const Workspace &ws, const uint16_t *x, int tok
     mark(2, false);
     if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
     mark(3, true);
-    e = launch_combine(b, ws, x, tokens, out, st);
+    e = launch_combine(b, ws, x, tokens, out, p->out_bf16 ? 1 : 0, st);
     mark(3, false);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     return MOE_OK;
@@ -363,6 +364,8 @@ int moe_plan_set_i(moe_plan *p, const char *key, long long v) {
         p->path = (int)v;
     } else if (!strcmp(key, "router_exact")) {
         p->router_exact = v ? 1 : 0;
+    } else if (!strcmp(key, "out_bf16")) {
+        p->out_bf16 = v != 0;
     } else if (!strcmp(key, "act_fp4")) {
         if (p->have_ws) return fail(MOE_EINVAL, "act_fp4 must be set before moe_set_workspace");
         p->act_fp4 = v != 0;
@@ -538,7 +541,7 @@ int moe_forward_ex(moe_plan *p, const uint16_t *x, int tokens, float *out, int32
     if (!aligned16(x) || !aligned16(out)) return fail(MOE_EINVAL, "x and out must be 16-byte aligned");
     const BlockParams &b = p->bp;
     const char *xb = reinterpret_cast<const char *>(x), *ob = reinterpret_cast<const char *>(out);
-    if (xb < ob + (size_t)tokens * b.H * 4 && ob < xb + (size_t)tokens * b.H * 2)
+    if (xb < ob + (size_t)tokens * b.H * (p->out_bf16 ? 2 : 4) && ob < xb + (size_t)tokens * b.H * 2)
         return fail(MOE_EINVAL, "x and out must not alias");
     if (int rc = check_outputs(b, tokens, x, ids_out, rw_out, xhat_out)) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -685,7 +688,7 @@ int moe_forward_noalloc(moe_plan *p, const uint16_t *x, int tokens, float *out, 
     if (tokens > kMaxTokens) return fail(MOE_ENOMEM, "moe_forward_noalloc: tokens %d > %d", tokens, kMaxTokens);
     const BlockParams &b = p->bp;
     const char *xb = reinterpret_cast<const char *>(x), *ob = reinterpret_cast<const char *>(out);
-    if (xb < ob + (size_t)tokens * b.H * 4 && ob < xb + (size_t)tokens * b.H * 2)
+    if (xb < ob + (size_t)tokens * b.H * (p->out_bf16 ? 2 : 4) && ob < xb + (size_t)tokens * b.H * 2)
         return fail(MOE_EINVAL, "x and out must not alias");
     if (int rc0 = check_outputs(b, tokens, x, ids_out, nullptr, nullptr)) return rc0;
     const size_t need = carve(p, tokens, nullptr, nullptr);

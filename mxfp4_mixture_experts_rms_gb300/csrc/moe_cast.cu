@@ -3,8 +3,12 @@
 #include "moe_common.cuh"
 
 namespace {
-// four elements per thread (one 16-byte load, one 8-byte store), the tail element-wise
+// Four elements per thread (one 16-byte load, one 8-byte store), the tail
+// element-wise.  Launched as a programmatic dependent of whatever precedes it
+// on the stream: it waits for that grid (complete, its writes visible) before
+// reading src.
 __global__ void __launch_bounds__(256) moe_cast_bf16_kernel(const float *src, uint16_t *dst, size_t n) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t n4 = n / 4;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         const float4 v = reinterpret_cast<const float4 *>(src)[i];
@@ -25,6 +29,5 @@ cudaError_t launch_cast_bf16(const float *src, uint16_t *dst, size_t n, cudaStre
     size_t blocks = (n4 + 255) / 256;
     if (blocks < 1) blocks = 1;
     if (blocks > 4096) blocks = 4096;
-    moe_cast_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, dst, n);
-    return cudaGetLastError();
+    return launch_pdl(moe_cast_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, st, src, dst, n);
 }

@@ -251,7 +251,7 @@ cudaError_t launch_cast_bf16(const float *src, uint16_t *dst, size_t n, cudaStre
 cudaError_t launch_mx_fp4_quantize(const uint16_t *x, size_t n_blocks, uint8_t *codes, uint8_t *scales,
                                    cudaStream_t st);
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T,
-                           float *out, cudaStream_t st);
+                           void *out, int out_bf16, cudaStream_t st);
 // What the grouped GEMM reads its weights through: TMA descriptors of the
 // packed codes and the scales repacked into 128-byte chunks (the two E8M0
 // bytes of one 64-element k-block for 64 consecutive rows, chunk (block b,

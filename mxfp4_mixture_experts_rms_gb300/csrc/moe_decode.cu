@@ -514,10 +514,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     }
 }
 
-// out[t] = x[t] + Σ_slot y[loc[t][slot]] (slot order; the shared expert last)
-__global__ void __launch_bounds__(256) moe_combine_kernel(BlockParams bp, Workspace ws, const uint16_t *x,
-                                                          float *out, int T) {
+// out[t] = x[t] + Σ_slot y[loc[t][slot]] (slot order; the shared expert last),
+// as fp32, or (BF16OUT) rounded to bf16 (nearest, ties to even): the input of
+// a next stacked block, written here instead of by a separate cast.
+template <bool BF16OUT>
+__global__ void __launch_bounds__(256) moe_combine_kernel(BlockParams bp, Workspace ws, const uint16_t *x, void *out,
+                                                          int T) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");  // a following cast may set itself up
     const int t = blockIdx.y;
     const int KK = bp.K + bp.n_shared;
     const int H = bp.H;
@@ -538,7 +542,13 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(BlockParams bp, Worksp
     o.y = __uint_as_float(xv.x & 0xFFFF0000u) + m.y;
     o.z = __uint_as_float(xv.y << 16) + m.z;
     o.w = __uint_as_float(xv.y & 0xFFFF0000u) + m.w;
-    *reinterpret_cast<float4 *>(out + (size_t)t * H + i4 * 4) = o;
+    if (BF16OUT) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+        reinterpret_cast<uint2 *>(out)[((size_t)t * H + i4 * 4) / 4] =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+    } else {
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + (size_t)t * H + i4 * 4) = o;
+    }
 }
 
 // One thread per 32-element block: the GEMV's element converter (E2M1 -> fp16,
@@ -675,10 +685,11 @@ cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, cons
     return nt == 1 ? launch_bf<false, 1, 1>(dn, h_bf16, items, st) : launch_bf<false, 2, 1>(dn, h_bf16, items, st);
 }
 
-cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T, float *out,
-                           cudaStream_t st) {
+cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T, void *out,
+                           int out_bf16, cudaStream_t st) {
     dim3 grid((bp.H / 4 + 255) / 256, T);
-    return launch_pdl(moe_combine_kernel, grid, dim3(256), 0, st, bp, ws, x, out, T);
+    return out_bf16 ? launch_pdl(moe_combine_kernel<true>, grid, dim3(256), 0, st, bp, ws, x, out, T)
+                    : launch_pdl(moe_combine_kernel<false>, grid, dim3(256), 0, st, bp, ws, x, out, T);
 }
 
 cudaError_t launch_dequant(const MatPtrs &m, int expert, int n_experts, float *out, cudaStream_t st) {

@@ -82,6 +82,8 @@ def test_forward_before_weights_is_not_ready(L):
     assert L.moe_forward_noalloc(h, C.c_void_p(256), 1, C.c_void_p(4096), None, None) == moe.MOE_ENOTREADY
     assert L.moe_plan_set_i(h, b"test_stall_wait", 1) == moe.MOE_OK
     assert L.moe_plan_set_i(h, b"test_stall_wait", 0) == moe.MOE_OK
+    assert L.moe_plan_set_i(h, b"out_bf16", 1) == moe.MOE_OK      # out written as bf16
+    assert L.moe_plan_set_i(h, b"out_bf16", 0) == moe.MOE_OK
     L.moe_plan_destroy(h)
 
 

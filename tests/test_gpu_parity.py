@@ -335,3 +335,36 @@ def test_bounded_wait_timeout_is_reported_and_the_plan_recovers():
     again, _, _ = run_gpu(blk, x_bits, plan=plan, dev=dev)
     assert again["status"] == 0
     assert np.array_equal(again["ids"], ref["ids"]) and np.array_equal(again["out"], ref["out"])
+
+
+# ------------------------------------------------------------ bf16 output
+@pytest.mark.parametrize("cfg,T", [(1, 8), (3, 128)])
+def test_out_bf16_is_the_rounded_fp32_output(cfg, T):
+    """With the out_bf16 option the forward writes x + MoE(x) rounded to bf16:
+    bit for bit what moe_cast_f32_to_bf16 makes of the fp32 output (GEMV and
+    grouped-GEMM paths), and the no-alloc forward does the same."""
+    import torch
+    blk = synth.make_block(cfg)
+    shape = blk["shape"]
+    H = shape.hidden
+    x_bits = synth.make_tokens(cfg, T, H)
+    ref, plan, dev = run_gpu(blk, x_bits)
+    want = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    moe.cast_f32_to_bf16(torch.from_numpy(ref["out"]).cuda(), want)
+    p16 = moe.Plan(shape, max_tokens=T, out_bf16=1).alloc_workspace().load_weights(dev)
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+    got = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    p16.forward(x, got)
+    torch.cuda.synchronize()
+    assert p16.device_status() == 0
+    assert torch.equal(got, want)
+    got.zero_()
+    L = moe.load()
+    import ctypes as C
+    st = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert L.moe_forward_noalloc(p16.h, C.c_void_p(x.data_ptr()), T, C.c_void_p(got.data_ptr()), None,
+                                 st) == moe.MOE_OK
+    torch.cuda.synchronize()
+    assert p16.device_status() == 0
+    assert torch.equal(got, want)
+    p16.close()
