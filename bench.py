@@ -67,9 +67,10 @@ def parse():
     ap.add_argument("--quick", action="store_true",
                     help="timed region of the headline only (no clock pre-roll, kernel timing, e2e, CPU "
                          "baseline or extras); for ncu")
-    ap.add_argument("--op", default="block", choices=["block", "mx_fp4_quantize"],
+    ap.add_argument("--op", default="block", choices=["block", "mx_fp4_quantize", "attention"],
                     help="block: the MoE block (the benchmark); mx_fp4_quantize: the FP4 activation "
-                         "encoder alone, on --rows x --cols bf16 activations")
+                         "encoder alone, on --rows x --cols bf16 activations; attention: the gpt-oss "
+                         "attention decode step alone")
     ap.add_argument("--rows", type=int, default=14336, help="mx_fp4_quantize: rows (2048 tokens x 7 routes)")
     ap.add_argument("--cols", type=int, default=2048, help="mx_fp4_quantize: columns (expert_hidden)")
     return ap.parse_args()
@@ -520,6 +521,124 @@ def e2e_rate(w, args, world):
             "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4 + T * K * 4}
 
 
+def attention_bench(args, seqs: int = 16, ctx: int = 4096):
+    """The attention half of the gpt-oss layer (moe_attn_decode), decode step:
+    `seqs` sequences with ctx - 1 cached tokens each, one sliding-window layer
+    (128 tokens) and one full-attention layer as in gpt-oss's alternation.
+    Timed in a CUDA graph of the two steps; the roofline is HBM: both layers'
+    projection weights once, the visible keys and values, activations."""
+    import numpy as np
+    import torch
+    from mxfp4_mixture_experts_rms_gb300 import moe, synth
+    A = synth.ATTN_GPT_OSS
+    H, QH, KVH, D, window = A["hidden"], A["q_heads"], A["kv_heads"], A["head_dim"], A["window"]
+    plans = []
+    for layer, win in enumerate((window, 0)):
+        w = synth.make_attention(200 + layer, H, QH, KVH)
+        p = moe.AttnPlan(H, QH, KVH, seqs, ctx, sliding_window=win)
+        p.load_weights({k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda()
+                        for k, v in w.items()})
+        kh, vh = synth.make_kv_history(200 + layer, seqs, ctx, KVH)
+        p.k_cache.copy_(torch.from_numpy(kh))
+        p.v_cache.copy_(torch.from_numpy(vh))
+        plans.append(p)
+    x = torch.from_numpy(synth.f32_to_bf16_bits(np.random.default_rng(0).normal(0, 1, (seqs, H))).view(np.int16)).cuda()
+    pos = torch.full((seqs,), ctx - 1, dtype=torch.int32, device="cuda")
+    out = torch.empty((seqs, H), dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        for p in plans:
+            p.decode(x, pos, out, stream=st)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    reps = max(1, min(args.steps, 100))
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            for p in plans:
+                p.decode(x, pos, out, stream=torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / reps
+    weights = 2 * ((QH * D + 2 * KVH * D) * H * 2 + H * QH * D * 2 + 4 * (QH * D + 2 * KVH * D + 2 * H + QH))
+    kv = seqs * (min(ctx, window) + ctx) * KVH * D * 2 * 2
+    act = 2 * seqs * (H * 2 + H * 4 + 2 * KVH * D * 2)
+    hbm, _, kind = peaks()
+    gbs = (weights + kv + act) / (ms / 1e3) / 1e9
+    for p in plans:
+        p.close()
+    del g
+    return {"value": seqs / (ms / 1e3), "unit": "tokens/s (one sliding + one full attention layer)",
+            "ms_per_step": ms, "path": "attention decode",
+            "config": {"workload": f"gpt-oss attention decode, {seqs} sequences x {ctx - 1} cached tokens, "
+                                   "one sliding-window (128) and one full layer",
+                       "hidden": H, "q_heads": QH, "kv_heads": KVH, "head_dim": D, "weights": "bf16 (synthetic)",
+                       "kv_cache": "fp16"},
+            "algorithmic_bytes_per_step": weights + kv + act,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "peak_kind": kind, "unit": "GB/s",
+                         "frac": gbs / hbm, "traffic": None},
+            "clocks": clk, "gpu_launches": 2 * 5 * reps}
+
+
+def locality_stats(w, steps: int = 16):
+    """Expert-locality statistics of the stack's routing (the library's
+    profiler attached to every layer; untimed, outside the measured steps):
+    steps of the workload's tokens as consecutive positions, per-capacity hit
+    rates of least-recently-used expert caches, the overlap of consecutive
+    tokens' expert sets, and the recording cost per layer and step."""
+    import torch
+    from mxfp4_mixture_experts_rms_gb300 import moe
+    sh = w.shape
+    caps = [4, 8, 12, 16, 24]
+    prof = moe.Locality(w.layers, sh.n_experts, sh.top_k, caps)
+    d = w.sets[0]
+    plans = w.plans(d)
+    for i, p in enumerate(plans):
+        prof.attach(p, i)
+    st = torch.cuda.current_stream()
+    for _ in range(steps):
+        w.forward_set(d, st)
+    torch.cuda.synchronize()
+    got = prof.read()
+    for p in plans:
+        moe.load().moe_locality_attach(p.h, None, 0)
+    # the recording alone (every layer's routes of the last step), in a CUDA
+    # graph so that host launch costs stay off the clock
+    wts = torch.zeros((w.T, sh.top_k), dtype=torch.float32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i, ly in enumerate(d["chain"]):
+            prof.record(i, ly["ids"], wts, 0, stream=torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(10):
+        g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    rec_us = 1e3 * e0.elapsed_time(e1) / (10 * len(plans))
+    del g
+    sel = float(got["hist"].sum())
+    wsum = float(got["weight_hist"].sum())
+    pairs = float(got["adjacent_pairs"].sum())
+    prof.close()
+    return {"tokens": int(steps * w.T), "layers": w.layers, "caps": [int(c) for c in got["caps"]],
+            "hit_rate": [float(h) / sel for h in got["cache_hits"].sum(axis=1)],
+            "weighted_hit_rate": [float(h) / wsum for h in got["cache_weight_hits"].sum(axis=1)],
+            "adjacent_overlap": float(got["overlap_sum"].sum()) / pairs if pairs else None,
+            "adjacent_jaccard": float(got["jaccard_sum"].sum()) / pairs if pairs else None,
+            "unique_experts_per_layer": float((got["hist"] > 0).sum(axis=1).mean()),
+            "record_us_per_layer_step": rec_us,
+            "note": "synthetic router weights: the statistics show the profiler working, not a model's locality"}
+
+
 def cpu_baseline(wid, T, w):
     """The oracle, as it stands, timed on the host cores for a bounded sample of
     the workload's tokens (about 10-30 s): as many tokens as there are cores
@@ -566,6 +685,7 @@ def run_ours(args, rank, world, local, wid, T):
         return
     head = summarise(w, r, args, world)
     e2e = e2e_rate(w, args, world)
+    loc = locality_stats(w) if w.layers > 1 else None
     extras = {}
     if not args.no_extras:
         for (ew, eT, eo) in EXTRAS:
@@ -581,6 +701,8 @@ def run_ours(args, rank, world, local, wid, T):
             extras[f"{synth.WORKLOADS[ew].name} x{eT}" + (" fp4" if eo.get("act_fp4") else "")] = s
             x.close()
             torch.cuda.synchronize()
+        att = attention_bench(args)
+        extras[att["config"]["workload"]] = att
     if rank != 0:
         return
     cpu = None if args.no_cpu_baseline else cpu_baseline(wid, T, w)
@@ -602,6 +724,8 @@ def run_ours(args, rank, world, local, wid, T):
         "cpu_baseline": cpu, "e2e": e2e, "clocks": head["clocks"], "gpu_launches": head["gpu_launches"],
         "configs": extras,
     }
+    if loc:
+        line["locality"] = loc
     print(json.dumps(line), flush=True)
 
 
@@ -664,6 +788,16 @@ def main():
                               "unavailable": "the encoder is timed on the GPU only"}))
             return
         run_mx_fp4_quantize(args)
+        return
+    if args.op == "attention":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": "attention",
+                              "unavailable": "the attention step is timed on the GPU only"}))
+            return
+        import torch
+        from mxfp4_mixture_experts_rms_gb300 import moe
+        moe.load()
+        print(json.dumps(attention_bench(args)), flush=True)
         return
     from mxfp4_mixture_experts_rms_gb300 import synth
     wid = args.workload

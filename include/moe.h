@@ -291,6 +291,131 @@ int moe_cast_f32_to_bf16(const float *src, uint16_t *dst, size_t n, void *stream
 int moe_mx_quantize_fp4(const uint16_t *x, size_t rows, size_t cols, uint8_t *codes, uint8_t *scales,
                         void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Expert-locality statistics (antirez ds4, ds4.c, the expert locality
+ * profiler: `ds4_expert_profile_record`, `ds4_expert_profile_cache_use`,
+ * `ds4_expert_profile_write_cache_summary`; its per-layer selection histogram
+ * is goosedump gpt_oss.rs `ExpertRouteProfile::record`).  A profiler holds,
+ * in device memory, per layer: the selections and the summed route weight of
+ * each expert, the number of recorded tokens, the overlap of the expert sets
+ * of tokens at consecutive positions, and for each cache capacity the hits
+ * (and hit weight) a least-recently-used cache of that many of the layer's
+ * experts would see.  Recording runs on the device, in stream order, after
+ * the forward that produced the routes; one warp takes a layer's selections
+ * in (token, slot) order for the cache statistics, so recording a batch of T
+ * tokens costs about T * top_k dependent steps (microseconds for decode
+ * batches, about half a millisecond for 12 K selections).
+ */
+typedef struct moe_locality moe_locality;
+
+/* Host arrays a read fills (each may be NULL): hist and weight_hist
+ * [n_layers][n_experts]; layer_records, adjacent_pairs, overlap_sum (sum over
+ * adjacent pairs of intersection / top_k) and jaccard_sum (of intersection /
+ * union) [n_layers]; cache_hits and cache_weight_hits [n_caps][n_layers];
+ * caps [n_caps] the capacities kept.  n_caps is set by the read. */
+typedef struct {
+    uint64_t *hist;
+    double *weight_hist;
+    uint64_t *layer_records;
+    uint64_t *adjacent_pairs;
+    double *overlap_sum;
+    double *jaccard_sum;
+    uint64_t *cache_hits;
+    double *cache_weight_hits;
+    int *caps;
+    int n_caps;
+} moe_locality_stats;
+
+/* A profiler for n_layers layers (1..4096) of n_experts experts (1..256) with
+ * top_k slots (1..min(8, n_experts)) and up to 16 cache capacities; as the
+ * page does, capacities outside 1..n_experts are left out.  Allocates its
+ * device state (zeroed; this call synchronises).  NULL on bad arguments or
+ * allocation failure (moe_last_error says which). */
+moe_locality *moe_locality_create(int n_layers, int n_experts, int top_k, const int *caps, int n_caps);
+/* Record `tokens` tokens of layer `layer` at sequence positions first_pos,
+ * first_pos + 1, ...: ids int32 [tokens][top_k] and route_w float
+ * [tokens][top_k], device pointers (4-byte aligned) as moe_forward_ex writes
+ * them; experts outside [0, n_experts) are skipped, as on the page.  A token
+ * is compared with the layer's previous recorded token when that one sat at
+ * the position just before.  Enqueue only. */
+int moe_locality_record(moe_locality *prof, int layer, const int32_t *ids, const float *route_w, int tokens,
+                        long long first_pos, void *stream);
+/* Record every later forward of `plan` (moe_forward, moe_forward_ex,
+ * moe_forward_noalloc) into layer `layer` of prof, each forward's tokens at
+ * the positions after the previous forward's, from 0 (goosedump gpt_oss.rs:
+ * `forward` / `prefill` take an optional route profile).  prof NULL
+ * detaches.  The profiler must outlive the attachment. */
+int moe_locality_attach(moe_plan *plan, moe_locality *prof, int layer);
+/* Synchronise the device and copy the statistics into *out. */
+int moe_locality_read(const moe_locality *prof, moe_locality_stats *out);
+/* Zero every statistic and forget every layer's previous token (synchronises stream). */
+int moe_locality_reset(moe_locality *prof, void *stream);
+/* Free the device state.  NULL is a no-op. */
+void moe_locality_destroy(moe_locality *prof);
+
+/* ---------------------------------------------------------------------------
+ * The attention half of the gpt-oss layer, one decode step for a batch of
+ * sequences (goosedump gpt_oss.rs `forward`: the attention norm, the query,
+ * key and value projections with biases, `apply_rope` with `Rope::new`'s
+ * YaRN tables, `LayerCache::append`, `causal_gqa` / `attention_head` with the
+ * per-head sink logit and `attention_window`, the output projection with its
+ * bias and the residual add; turbospark-runtime gptoss/mod.rs module doc
+ * comment).  For each sequence b with its new token at position pos[b] (the
+ * number of tokens its cache already holds):
+ *   x_hat = bf16(rms_norm(x[b]) * gamma)              (as in the MoE block)
+ *   q, k, v = Wq x_hat + bq, Wk x_hat + bk, Wv x_hat + bv   (fp32)
+ *   q, k rotated per head: dims d and d + 32 form pair d, by the angle
+ *     pos[b] * f_d, f_d the RoPE base frequency blended toward f_d / factor
+ *     between the YaRN correction dimensions of beta_fast and beta_slow;
+ *     cosine and sine scaled by 0.1 ln(factor) + 1
+ *   k, v stored (fp16, nearest) at cache row pos[b] of sequence b
+ *   per query head h (kv head h / (q_heads / kv_heads)): softmax over the
+ *     scores q_h . k_t / 8 of the visible tokens (the last sliding_window of
+ *     them, or all) and the head's sink logit; o_h = sum_t p_t v_t
+ *   out[b] = x[b] + Wo bf16(o) + bo   (fp32, or bf16 with "out_bf16")
+ * Weights: gamma f32 [H]; wq bf16 [q_heads * 64][H], wk and wv bf16
+ * [kv_heads * 64][H], wo bf16 [H][q_heads * 64]; bq, bk, bv, bo f32 of the
+ * matching lengths; sinks f32 [q_heads]; all device pointers, 16-byte
+ * aligned, borrowed.  Caches: fp16 [max_seqs][max_ctx][kv_heads][64] for
+ * keys and for values, device memory the caller owns.
+ */
+typedef struct moe_attn moe_attn;
+typedef struct {
+    const float *gamma;
+    const uint16_t *wq, *wk, *wv, *wo;
+    const float *bq, *bk, *bv, *bo;
+    const float *sinks;
+} moe_attn_weights;
+
+/* A plan for one layer: hidden a multiple of 32 up to 4096, head_dim 64 (the
+ * page's constant), q_heads a multiple of kv_heads with at most 16 per kv
+ * head, up to 32 sequences per step, up to 65536 context tokens.  Defaults:
+ * full attention, rms_eps 1e-5, the page's RoPE constants (base 150000,
+ * factor 32, original context 4096, beta_fast 32, beta_slow 1).  NULL on bad
+ * arguments. */
+moe_attn *moe_attn_create(int hidden, int q_heads, int kv_heads, int head_dim, int max_seqs, int max_ctx);
+/* "sliding_window": 0 (full attention) or the number of most recent tokens a
+ * query sees (the page: 128 on even layers); "out_bf16": 1 writes out as bf16. */
+int moe_attn_set_i(moe_attn *plan, const char *key, long long value);
+/* "rms_eps", "rope_base", "rope_factor", "rope_original_context",
+ * "rope_beta_fast", "rope_beta_slow" (positive, finite). */
+int moe_attn_set_f(moe_attn *plan, const char *key, double value);
+/* Device workspace a step needs (x_hat, q, the chunk partials, o): caller-owned,
+ * 256-byte aligned, borrowed by moe_attn_set_workspace. */
+size_t moe_attn_workspace_bytes(const moe_attn *plan);
+int moe_attn_set_workspace(moe_attn *plan, void *dev_ptr, size_t bytes);
+/* The key and value caches (fp16, layout above; borrowed). */
+int moe_attn_set_cache(moe_attn *plan, void *k_cache, void *v_cache);
+int moe_attn_load_weights(moe_attn *plan, const moe_attn_weights *w);
+/* One decode step for n_seqs sequences (0..max_seqs): x bf16 [n_seqs][H]
+ * (16-byte aligned), positions int32 [n_seqs] on the device (each in
+ * 0..max_ctx-1; a sequence whose position is outside is skipped and its out
+ * row undefined), out [n_seqs][H] (16-byte aligned, not overlapping x).
+ * Writes the new tokens' keys and values into the caches.  Enqueue only. */
+int moe_attn_decode(moe_attn *plan, const uint16_t *x, int n_seqs, const int32_t *positions, void *out,
+                    void *stream);
+void moe_attn_destroy(moe_attn *plan);
+
 /* Text of the last failure on this thread ("" if none) (goosedump gpt_oss.rs:
  * every `ensure!` carries a message). */
 const char *moe_last_error(void);

@@ -37,6 +37,25 @@ int cuda_fail(cudaError_t e, const char *what) {
     return fail(MOE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+}  // namespace
+
+// The thread's last-error message, for the other translation units.
+int moe_fail_status(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+void moe_set_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+}
+
+namespace {
+
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 constexpr int kMaxTokens = 65535;  // tokens per forward: one combine grid row each
@@ -72,6 +91,9 @@ struct moe_plan {
     // FP4 activations: the grouped GEMM on the block-scaled FP4 tensor cores (kind::mxf4)
     bool act_fp4 = false;
     bool out_bf16 = false;  // out receives bf16 (the next stacked block's input) instead of fp32
+    moe_locality *loc = nullptr;  // attached locality profiler: every forward's routes are recorded
+    int loc_layer = 0;
+    long long loc_pos = 0;        // position of the next forward's first token
     Mxf4Weights mxf4{};
     bool have_mxf4 = false;
     uint8_t *mxf4_scales = nullptr;  // owned: weight scales repacked into the kernel's atoms
@@ -290,6 +312,11 @@ int enqueue_forward(moe_plan *p, const Workspace &ws, const uint16_t *x, int tok
     e = launch_combine(b, ws, x, tokens, out, p->out_bf16 ? 1 : 0, st);
     mark(3, false);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    if (p->loc) {
+        e = locality_enqueue(p->loc, p->loc_layer, ws.ids, ws.route_w, tokens, p->loc_pos, st);
+        if (e != cudaSuccess) return cuda_fail(e, "locality profiler launch");
+        p->loc_pos += tokens;
+    }
     return MOE_OK;
 }
 
@@ -298,6 +325,15 @@ int enqueue_forward(moe_plan *p, const Workspace &ws, const uint16_t *x, int tok
 extern "C" {
 
 const char *moe_last_error(void) { return g_err; }
+
+int moe_locality_attach(moe_plan *p, moe_locality *prof, int layer) {
+    if (!p) return fail(MOE_EINVAL, "NULL plan");
+    if (prof && layer < 0) return fail(MOE_EINVAL, "layer must be >= 0");
+    p->loc = prof;
+    p->loc_layer = layer;
+    p->loc_pos = 0;
+    return MOE_OK;
+}
 
 moe_plan *moe_plan_create(int hidden, int expert_hidden, int n_experts, int top_k, float swiglu_alpha,
                           float swiglu_limit, float weight_scale) {

@@ -233,8 +233,18 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 constexpr int kFormF16 = 1;  // fp16 (the GEMVs, the fp16 grouped GEMM)
 constexpr int kFormMma = 2;  // bf16 in the grouped GEMM's pair order (its bf16 variant)
 
+// The thread's last-error message (moe_last_error), set from any translation unit.
+int moe_fail_status(int code, const char *fmt, ...);
+void moe_set_error(const char *fmt, ...);
+// Enqueue the recording of T tokens' routes of one layer into a locality profiler.
+struct moe_locality;
+cudaError_t locality_enqueue(moe_locality *p, int layer, const int32_t *ids, const float *w, int T,
+                             long long first_pos, cudaStream_t st);
+
 // Launchers implemented in the .cu files (host side).
 int route_ticket_count(int T);
+cudaError_t launch_rms_norm_rows(const uint16_t *x, const float *gamma, int T, int H, double eps, uint16_t *xhat,
+                                 float *xnorm_scratch, int32_t *count_scratch, cudaStream_t st);
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x,
                          const float *gamma, const uint16_t *router_w, const float *router_b,
                          int T, int32_t *ids_out, float *rw_out, uint16_t *xhat_out, int tile_rows,

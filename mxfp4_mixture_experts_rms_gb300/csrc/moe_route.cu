@@ -1265,6 +1265,24 @@ cudaError_t launch_small_geo(const RouteArgs &a, const SmallGeo &g, cudaStream_t
 
 int route_ticket_count(int T) { return T + 1; }
 
+// x_hat = bf16(rms_norm(x) * gamma) for T rows of H, by the routing's norm
+// kernel alone (no router): the attention block's input norm.  xnorm_scratch
+// [T] floats and count_scratch [1] int are the kernel's side outputs.
+cudaError_t launch_rms_norm_rows(const uint16_t *x, const float *gamma, int T, int H, double eps, uint16_t *xhat,
+                                 float *xnorm_scratch, int32_t *count_scratch, cudaStream_t st) {
+    if (H <= 0 || H % 32 != 0 || H / 8 > kRouteThreads * kXC) return cudaErrorInvalidValue;
+    BlockParams bp{};
+    bp.H = H;
+    bp.eps = eps;
+    Workspace ws{};
+    ws.xhat = xhat;
+    ws.xnorm = xnorm_scratch;
+    ws.counts = count_scratch;
+    RouteArgs a{bp, ws, x, gamma, nullptr, nullptr, T, nullptr, nullptr, nullptr, 0, 0, 0, 0, 1.0 / (double)H};
+    moe_route_norm_kernel<<<T, kNormThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x, const float *gamma,
                          const uint16_t *router_w, const float *router_b, int T, int32_t *ids_out, float *rw_out,
                          uint16_t *xhat_out, int tile_rows, int router_exact, int forms, cudaStream_t st) {

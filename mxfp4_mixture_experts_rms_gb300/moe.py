@@ -24,7 +24,24 @@ EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_plan_set_i", "moe_plan_se
            "moe_workspace_bytes",
            "moe_set_workspace", "moe_load_weights", "moe_forward", "moe_forward_ex", "moe_get_expert_counts",
            "moe_get_permutation", "moe_debug_dequant", "moe_profile_read", "moe_get_device_status",
-           "moe_forward_noalloc", "moe_cast_f32_to_bf16", "moe_mx_quantize_fp4", "moe_last_error"]
+           "moe_forward_noalloc", "moe_cast_f32_to_bf16", "moe_mx_quantize_fp4", "moe_locality_create",
+           "moe_locality_record", "moe_locality_attach", "moe_locality_read", "moe_locality_reset",
+           "moe_locality_destroy", "moe_attn_create", "moe_attn_set_i", "moe_attn_set_f", "moe_attn_workspace_bytes",
+           "moe_attn_set_workspace", "moe_attn_set_cache", "moe_attn_load_weights", "moe_attn_decode",
+           "moe_attn_destroy", "moe_last_error"]
+
+
+class LocalityStats(C.Structure):
+    _fields_ = [("hist", C.c_void_p), ("weight_hist", C.c_void_p), ("layer_records", C.c_void_p),
+                ("adjacent_pairs", C.c_void_p), ("overlap_sum", C.c_void_p), ("jaccard_sum", C.c_void_p),
+                ("cache_hits", C.c_void_p), ("cache_weight_hits", C.c_void_p), ("caps", C.c_void_p),
+                ("n_caps", C.c_int)]
+
+
+class AttnWeights(C.Structure):
+    _fields_ = [("gamma", C.c_void_p), ("wq", C.c_void_p), ("wk", C.c_void_p), ("wv", C.c_void_p),
+                ("wo", C.c_void_p), ("bq", C.c_void_p), ("bk", C.c_void_p), ("bv", C.c_void_p),
+                ("bo", C.c_void_p), ("sinks", C.c_void_p)]
 
 
 class MoeError(RuntimeError):
@@ -79,10 +96,32 @@ def load(build_if_missing: bool = True):
     L.moe_forward_noalloc.argtypes = [P, P, I, P, P, P]
     L.moe_cast_f32_to_bf16.argtypes = [P, P, SZ, P]
     L.moe_mx_quantize_fp4.argtypes = [P, SZ, SZ, P, P, P]
+    L.moe_locality_create.restype = P
+    L.moe_locality_create.argtypes = [I, I, I, P, I]
+    L.moe_locality_record.argtypes = [P, I, P, P, I, LL, P]
+    L.moe_locality_attach.argtypes = [P, P, I]
+    L.moe_locality_read.argtypes = [P, C.POINTER(LocalityStats)]
+    L.moe_locality_reset.argtypes = [P, P]
+    L.moe_locality_destroy.restype = None
+    L.moe_locality_destroy.argtypes = [P]
+    L.moe_attn_create.restype = P
+    L.moe_attn_create.argtypes = [I, I, I, I, I, I]
+    L.moe_attn_set_i.argtypes = [P, C.c_char_p, LL]
+    L.moe_attn_set_f.argtypes = [P, C.c_char_p, D]
+    L.moe_attn_workspace_bytes.restype = SZ
+    L.moe_attn_workspace_bytes.argtypes = [P]
+    L.moe_attn_set_workspace.argtypes = [P, P, SZ]
+    L.moe_attn_set_cache.argtypes = [P, P, P]
+    L.moe_attn_load_weights.argtypes = [P, C.POINTER(AttnWeights)]
+    L.moe_attn_decode.argtypes = [P, P, I, P, P, P]
+    L.moe_attn_destroy.restype = None
+    L.moe_attn_destroy.argtypes = [P]
     L.moe_last_error.restype = C.c_char_p
     L.moe_last_error.argtypes = []
     for name in EXPORTS:
-        if name not in ("moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_last_error"):
+        if name not in ("moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_last_error",
+                        "moe_locality_create", "moe_locality_destroy", "moe_attn_create", "moe_attn_destroy",
+                        "moe_attn_workspace_bytes"):
             getattr(L, name).restype = C.c_int
     _lib = L
     return L
@@ -258,6 +297,110 @@ class Plan:
     def close(self):
         if getattr(self, "h", None):
             self.L.moe_plan_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Locality:
+    """Expert-locality statistics of the routing (ds4.c expert locality
+    profiler; goosedump gpt_oss.rs ExpertRouteProfile), kept on the device."""
+
+    def __init__(self, n_layers: int, n_experts: int, top_k: int, caps=()):
+        import numpy as np
+        self.L = load()
+        self.n_layers, self.n_experts, self.top_k = n_layers, n_experts, top_k
+        arr = (C.c_int * max(len(caps), 1))(*[int(c) for c in caps])
+        h = self.L.moe_locality_create(n_layers, n_experts, top_k, arr, len(caps))
+        if not h:
+            raise MoeError(MOE_EINVAL, self.L.moe_last_error().decode())
+        self.h = C.c_void_p(h)
+        self._np = np
+
+    def record(self, layer: int, ids, route_w, first_pos: int, stream=None):
+        _check(self.L.moe_locality_record(self.h, int(layer), C.c_void_p(_ptr(ids)), C.c_void_p(_ptr(route_w)),
+                                          int(ids.shape[0]), int(first_pos), _stream_ptr(stream)))
+
+    def attach(self, plan, layer: int):
+        _check(self.L.moe_locality_attach(plan.h, self.h, int(layer)))
+
+    def reset(self, stream=None):
+        _check(self.L.moe_locality_reset(self.h, _stream_ptr(stream)))
+
+    def read(self) -> dict:
+        np = self._np
+        L, E = self.n_layers, self.n_experts
+        out = dict(hist=np.zeros((L, E), np.uint64), weight_hist=np.zeros((L, E), np.float64),
+                   layer_records=np.zeros(L, np.uint64), adjacent_pairs=np.zeros(L, np.uint64),
+                   overlap_sum=np.zeros(L, np.float64), jaccard_sum=np.zeros(L, np.float64),
+                   cache_hits=np.zeros((16, L), np.uint64), cache_weight_hits=np.zeros((16, L), np.float64),
+                   caps=np.zeros(16, np.int32))
+        st = LocalityStats(*[out[k].ctypes.data for k in ("hist", "weight_hist", "layer_records", "adjacent_pairs",
+                                                          "overlap_sum", "jaccard_sum", "cache_hits",
+                                                          "cache_weight_hits", "caps")], 0)
+        _check(self.L.moe_locality_read(self.h, C.byref(st)))
+        n = st.n_caps
+        out["caps"] = out["caps"][:n].copy()
+        out["cache_hits"] = out["cache_hits"][:n].copy()
+        out["cache_weight_hits"] = out["cache_weight_hits"][:n].copy()
+        return out
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.L.moe_locality_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class AttnPlan:
+    """One layer's attention decode step (moe_attn_*): the plan, a torch-allocated
+    workspace and fp16 key/value caches [max_seqs][max_ctx][kv_heads][64]."""
+
+    def __init__(self, hidden: int, q_heads: int, kv_heads: int, max_seqs: int, max_ctx: int, head_dim: int = 64,
+                 sliding_window: int = 0, out_bf16: bool = False, device="cuda"):
+        import torch
+        self.L = load()
+        h = self.L.moe_attn_create(hidden, q_heads, kv_heads, head_dim, max_seqs, max_ctx)
+        if not h:
+            raise MoeError(MOE_EINVAL, self.L.moe_last_error().decode())
+        self.h = C.c_void_p(h)
+        self.hidden, self.q_heads, self.kv_heads, self.max_seqs, self.max_ctx = hidden, q_heads, kv_heads, max_seqs, max_ctx
+        _check(self.L.moe_attn_set_i(self.h, b"sliding_window", int(sliding_window)))
+        _check(self.L.moe_attn_set_i(self.h, b"out_bf16", int(out_bf16)))
+        n = int(self.L.moe_attn_workspace_bytes(self.h))
+        self.ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+        off = (-self.ws.data_ptr()) % 256
+        _check(self.L.moe_attn_set_workspace(self.h, C.c_void_p(self.ws.data_ptr() + off), n))
+        self.k_cache = torch.zeros((max_seqs, max_ctx, kv_heads, head_dim), dtype=torch.float16, device=device)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        _check(self.L.moe_attn_set_cache(self.h, C.c_void_p(self.k_cache.data_ptr()),
+                                         C.c_void_p(self.v_cache.data_ptr())))
+        self.weights = None
+
+    def load_weights(self, wts: dict):
+        """wts: device tensors gamma, wq, wk, wv, wo (bf16 bits as int16), bq, bk, bv, bo, sinks (float32)."""
+        self.weights = wts
+        self._w = AttnWeights(*[_ptr(wts[k]) for k in ("gamma", "wq", "wk", "wv", "wo", "bq", "bk", "bv", "bo",
+                                                        "sinks")])
+        _check(self.L.moe_attn_load_weights(self.h, C.byref(self._w)))
+        return self
+
+    def decode(self, x, positions, out, stream=None):
+        _check(self.L.moe_attn_decode(self.h, C.c_void_p(_ptr(x)), int(x.shape[0]), C.c_void_p(_ptr(positions)),
+                                      C.c_void_p(_ptr(out)), _stream_ptr(stream)))
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.L.moe_attn_destroy(self.h)
             self.h = None
 
     def __del__(self):

@@ -194,6 +194,38 @@ def make_block_device(config: int, layer: int, expert_seed: int, device="cuda") 
     return blk
 
 
+# The attention half of the gpt-oss layer (goosedump gpt_oss.rs constants block:
+# 64 query heads, 8 key/value heads, head dimension 64).
+_T_ATTN = 40
+ATTN_GPT_OSS = dict(hidden=2880, q_heads=64, kv_heads=8, head_dim=64, window=128)
+
+
+def make_attention(seed: int, hidden: int = 2880, q_heads: int = 64, kv_heads: int = 8, head_dim: int = 64) -> dict:
+    """Seeded attention weights: gamma = 1 + N(0, 0.1) (f32); Wq, Wk, Wv, Wo ~
+    N(0, 0.02) as bf16 bits (Wq [q_heads*64][H], Wk/Wv [kv_heads*64][H],
+    Wo [H][q_heads*64]); biases N(0, 0.02) (f32); sinks N(0, 1) (f32)."""
+    r = lambda t: _rng(_T_ATTN, seed, t)  # noqa: E731
+    QD, KD = q_heads * head_dim, kv_heads * head_dim
+    return dict(gamma=(1.0 + r(0).normal(0.0, 0.1, hidden)).astype(np.float32),
+                wq=f32_to_bf16_bits(r(1).normal(0.0, 0.02, (QD, hidden))),
+                wk=f32_to_bf16_bits(r(2).normal(0.0, 0.02, (KD, hidden))),
+                wv=f32_to_bf16_bits(r(3).normal(0.0, 0.02, (KD, hidden))),
+                wo=f32_to_bf16_bits(r(4).normal(0.0, 0.02, (hidden, QD))),
+                bq=r(5).normal(0.0, 0.02, QD).astype(np.float32),
+                bk=r(6).normal(0.0, 0.02, KD).astype(np.float32),
+                bv=r(7).normal(0.0, 0.02, KD).astype(np.float32),
+                bo=r(8).normal(0.0, 0.02, hidden).astype(np.float32),
+                sinks=r(9).normal(0.0, 1.0, q_heads).astype(np.float32))
+
+
+def make_kv_history(seed: int, seqs: int, ctx: int, kv_heads: int = 8, head_dim: int = 64) -> tuple:
+    """Cached keys and values of earlier tokens: N(0, 1) rounded to fp16,
+    [seqs][ctx][kv_heads][head_dim] each."""
+    k = _rng(_T_ATTN, seed, 20).normal(0.0, 1.0, (seqs, ctx, kv_heads, head_dim)).astype(np.float16)
+    v = _rng(_T_ATTN, seed, 21).normal(0.0, 1.0, (seqs, ctx, kv_heads, head_dim)).astype(np.float16)
+    return k, v
+
+
 def make_tokens(config: int, tokens: int, hidden: int, layer: int = 0, sub: int = 0) -> np.ndarray:
     """Input activations x ~ N(0,1) as bf16 bits ``[tokens][hidden]``."""
     return f32_to_bf16_bits(_rng(config, layer, _T_X, sub).normal(0.0, 1.0, size=(tokens, hidden)))
@@ -220,7 +252,8 @@ def distinct_uniform(E: int, K: int, T: int) -> float:
 
 
 __all__ = [
-    "BlockShape", "Workload", "WORKLOADS", "GPT_OSS", "DSV4_FLASH_SHAPE", "MATS",
+    "BlockShape", "Workload", "WORKLOADS", "GPT_OSS", "DSV4_FLASH_SHAPE", "MATS", "ATTN_GPT_OSS", "make_attention",
+    "make_kv_history",
     "make_block", "make_router", "make_tokens", "make_block_device", "expert_matrices_device", "tiny_shape", "f32_to_bf16_bits", "bf16_bits_to_f32",
     "expert_bytes", "expert_bias_bytes", "distinct_uniform",
 ]

@@ -130,3 +130,21 @@ def test_binding_refuses_strided_tensors(L):
     with pytest.raises(moe.MoeError) as ei:
         moe.cast_f32_to_bf16(src, dst)
     assert ei.value.status == moe.MOE_EINVAL
+
+
+def test_locality_profiler_refuses_bad_arguments(L):
+    """Refusals happen on the host before any device memory is touched."""
+    import ctypes as C
+    caps = (C.c_int * 2)(4, 8)
+    assert not L.moe_locality_create(0, 32, 4, caps, 2)            # no layer
+    assert b"bad arguments" in L.moe_last_error()
+    assert not L.moe_locality_create(2, 300, 4, caps, 2)           # too many experts
+    assert not L.moe_locality_create(2, 32, 9, caps, 2)            # top_k above 8
+    assert not L.moe_locality_create(2, 4, 5, caps, 2)             # top_k above n_experts
+    assert not L.moe_locality_create(2, 32, 4, None, 2)            # capacities missing
+    assert not L.moe_locality_create(2, 32, 4, caps, 17)           # too many capacities
+    assert L.moe_locality_record(None, 0, None, None, 1, 0, None) == moe.MOE_EINVAL
+    assert L.moe_locality_attach(None, None, 0) == moe.MOE_EINVAL
+    assert L.moe_locality_read(None, None) == moe.MOE_EINVAL
+    assert L.moe_locality_reset(None, None) == moe.MOE_EINVAL
+    L.moe_locality_destroy(None)                                    # no-op

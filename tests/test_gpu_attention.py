@@ -1,0 +1,113 @@
+"""GPU parity of the attention decode step (moe_attn_decode) against the
+oracle's plain float64 restatement of goosedump gpt_oss.rs (`forward`'s
+attention step: norm, projections, YaRN RoPE, fp16 cache append, grouped
+attention with sinks over the full or the sliding window, output projection,
+residual).  Outputs within the block tolerance (relative L2 <= 1e-3, max abs
+<= 2e-3 max|ref|, on the output and on the attention's own contribution);
+the appended cache rows within one fp16 rounding of the oracle's; cache rows
+the step must not touch unchanged."""
+import numpy as np
+import pytest
+
+from oracle import attention as A
+from mxfp4_mixture_experts_rms_gb300 import moe, synth
+
+from gpu_helpers import check_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.load()
+
+
+def _as64(bits):
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def _run(H, QH, KVH, positions, max_ctx, window, seed, out_bf16=False):
+    import torch
+    B = len(positions)
+    w = synth.make_attention(seed, H, QH, KVH)
+    kh, vh = synth.make_kv_history(seed, B, max_ctx, KVH)
+    x = synth.f32_to_bf16_bits(np.random.default_rng(seed).normal(0.0, 1.0, (B, H)))
+    plan = moe.AttnPlan(H, QH, KVH, B, max_ctx, sliding_window=window, out_bf16=out_bf16)
+    dev = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda() for k, v in w.items()}
+    plan.load_weights(dev)
+    plan.k_cache.copy_(torch.from_numpy(kh))
+    plan.v_cache.copy_(torch.from_numpy(vh))
+    pos = torch.tensor(positions, dtype=torch.int32, device="cuda")
+    xd = torch.from_numpy(x.view(np.int16)).cuda()
+    out = torch.empty((B, H), dtype=torch.int16 if out_bf16 else torch.float32, device="cuda")
+    plan.decode(xd, pos, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    kc, vc = plan.k_cache.cpu().numpy(), plan.v_cache.cpu().numpy()
+    wts = dict(gamma=w["gamma"], wq=_as64(w["wq"]), wk=_as64(w["wk"]), wv=_as64(w["wv"]), wo=_as64(w["wo"]),
+               bq=w["bq"].astype(np.float64), bk=w["bk"].astype(np.float64), bv=w["bv"].astype(np.float64),
+               bo=w["bo"].astype(np.float64), sinks=w["sinks"].astype(np.float64))
+    refs = []
+    for b, p in enumerate(positions):
+        kr = kh[b, :p + 1].astype(np.float64)
+        vr = vh[b, :p + 1].astype(np.float64)
+        out_r, _, _ = A.decode_step(wts, x[b], kr, vr, p, q_heads=QH, kv_heads=KVH, head_dim=64,
+                                    sliding=window > 0, window=window or 1, eps=1e-5)
+        refs.append((out_r, kr[p], vr[p]))
+        # the appended rows: within one fp16 rounding of the oracle's, beyond
+        # the fp32 accumulation error of the projection (1e-5 of the row's
+        # largest entry: entries near zero come from cancelling sums)
+        for got_row, ref_row in ((kc[b, p], kr[p]), (vc[b, p], vr[p])):
+            g = got_row.astype(np.float64)
+            assert np.all(np.abs(g - ref_row) <= 2.0 ** -10 * np.abs(ref_row) + 1e-5 * np.abs(ref_row).max()), (b, p)
+        # every other row as it was
+        others = np.ones(max_ctx, bool)
+        others[p] = False
+        assert np.array_equal(kc[b, others], kh[b, others]) and np.array_equal(vc[b, others], vh[b, others])
+    ref = np.stack([r[0] for r in refs])
+    if out_bf16:
+        want = synth.f32_to_bf16_bits(ref.astype(np.float32))
+        gotf = synth.bf16_bits_to_f32(got.view(np.uint16)).astype(np.float64)
+        check_close(gotf, synth.bf16_bits_to_f32(want).astype(np.float64), what="bf16 out")
+    else:
+        check_close(got, ref, x, what=f"attention out (window {window})")
+    plan.close()
+
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_gpt_oss_attention_decode(window):
+    """gpt-oss shape (2880 hidden, 64 query heads over 8 kv heads): an empty
+    cache, short contexts, contexts across the 256-token chunk boundary and
+    beyond the 128-token window, and a position near the end of the cache."""
+    _run(2880, 64, 8, [0, 5, 127, 128, 255, 256, 300, 1022], 1024, window, seed=1 + window)
+
+
+def test_ragged_batch_sizes_and_small_shapes():
+    """Every MMA column tile count (1..32 sequences), a smaller head layout
+    (4 query heads per kv head), the bf16 output."""
+    _run(256, 8, 2, [3], 64, 0, seed=5)
+    _run(256, 8, 2, list(range(9)), 64, 16, seed=6)
+    _run(512, 16, 4, [i * 7 % 300 for i in range(17)], 320, 0, seed=7)
+    _run(512, 16, 1, [i * 13 % 300 for i in range(32)], 320, 100, seed=8)
+    _run(2880, 64, 8, [10, 700], 768, 128, seed=9, out_bf16=True)
+
+
+def test_position_outside_the_cache_is_skipped():
+    """A position at or beyond max_ctx writes nothing into the caches."""
+    import torch
+    H, QH, KVH, ctx = 256, 8, 2, 32
+    w = synth.make_attention(3, H, QH, KVH)
+    plan = moe.AttnPlan(H, QH, KVH, 2, ctx)
+    plan.load_weights({k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda()
+                       for k, v in w.items()})
+    x = torch.from_numpy(synth.f32_to_bf16_bits(np.ones((2, H))).view(np.int16)).cuda()
+    out = torch.empty((2, H), dtype=torch.float32, device="cuda")
+    plan.decode(x, torch.tensor([ctx, 4], dtype=torch.int32, device="cuda"), out)
+    torch.cuda.synchronize()
+    kc = plan.k_cache.cpu().numpy()
+    assert not kc[0].any()                      # sequence 0 untouched
+    assert kc[1, 4].any() and not kc[1, :4].any() and not kc[1, 5:].any()
+    plan.close()
