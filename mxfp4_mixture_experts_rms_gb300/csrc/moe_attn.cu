@@ -36,7 +36,7 @@
 namespace {
 
 constexpr int kHeadDim = 64;
-constexpr int kGemvWarps = 4;
+constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kMaxSeqs = 32;      // tokens per decode step (4 MMA column tiles of 8)
 constexpr int kChunk = 256;       // context tokens per attention CTA
@@ -179,15 +179,19 @@ __device__ __forceinline__ void visible_range(const AttnDims &d, int p, int &fir
 }
 
 // Partials per (sequence, query head, chunk): max score, sum of exp(s - max),
-// and the exp-weighted value sums [64].
-__global__ void __launch_bounds__(256) moe_attn_chunk_kernel(AttnDims d, const float *q, const int32_t *pos,
+// and the exp-weighted value sums [64].  Shared memory: the G query rows
+// (fp32), the chunk's scores [G][256] and its value rows [256][64] (fp16),
+// staged once for the G heads that read them.
+__global__ void __launch_bounds__(256, 3) moe_attn_chunk_kernel(AttnDims d, const float *q, const int32_t *pos,
                                                              const __half *kc, const __half *vc, float *pm, float *pl,
                                                              float *pacc, int n_chunks) {
-    __shared__ float sq[kMaxQPerKV][kHeadDim];
-    __shared__ float ss[kMaxQPerKV][kChunk];
+    extern __shared__ __align__(16) unsigned char smem[];
     const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = d.QH / d.KVH;
+    float *sq = reinterpret_cast<float *>(smem);             // [G][64]
+    float *ss = sq + G * kHeadDim;                            // [G][256]
+    __half *sv = reinterpret_cast<__half *>(ss + G * kChunk);  // [256][64]
     const int p = pos[b];
     if (p < 0 || p >= d.max_ctx) return;
     int first, count;
@@ -197,43 +201,60 @@ __global__ void __launch_bounds__(256) moe_attn_chunk_kernel(AttnDims d, const f
     if (nt <= 0) return;
     const float scale = rsqrtf((float)kHeadDim);
     for (int i = tid; i < G * kHeadDim; i += 256)
-        sq[i / kHeadDim][i % kHeadDim] = q[(size_t)b * d.QH * kHeadDim + (size_t)(j * G) * kHeadDim + i];
-    __syncthreads();
+        sq[i] = q[(size_t)b * d.QH * kHeadDim + (size_t)(j * G) * kHeadDim + i];
     const size_t row0 = ((size_t)b * d.max_ctx) * d.KVH * kHeadDim + (size_t)j * kHeadDim;
     const size_t rstride = (size_t)d.KVH * kHeadDim;
-    // scores: thread t <-> token t0 + t
+    // thread t <-> token t0 + t: its key row to registers (fp16 pairs), its
+    // value row to shared memory
+    uint4 kr4[kHeadDim / 8];
     if (tid < nt) {
         const uint4 *kr = reinterpret_cast<const uint4 *>(kc + row0 + (size_t)(t0 + tid) * rstride);
-        float kf[kHeadDim];
+        const __half *vr = vc + row0 + (size_t)(t0 + tid) * rstride;
 #pragma unroll
         for (int v = 0; v < kHeadDim / 8; v++) {
-            const uint4 u = kr[v];
-            const uint32_t h4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h4[e]));
-                kf[8 * v + 2 * e] = f.x;
-                kf[8 * v + 2 * e + 1] = f.y;
-            }
+            const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(sv + (size_t)tid * kHeadDim + 8 * v));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(vr + 8 * v) : "memory");
         }
+#pragma unroll
+        for (int v = 0; v < kHeadDim / 8; v++) kr4[v] = kr[v];
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (tid < nt) {
         for (int h = 0; h < G; h++) {
+            const float4 *q4 = reinterpret_cast<const float4 *>(sq + h * kHeadDim);
             float s = 0.f;
 #pragma unroll
-            for (int e = 0; e < kHeadDim; e++) s = fmaf(sq[h][e], kf[e], s);
-            ss[h][tid] = s * scale;
+            for (int v = 0; v < kHeadDim / 8; v++) {
+                const uint32_t h4[4] = {kr4[v].x, kr4[v].y, kr4[v].z, kr4[v].w};
+                const float4 qa = q4[2 * v], qb = q4[2 * v + 1];
+                const float2 k0 = __half22float2(*reinterpret_cast<const __half2 *>(&h4[0]));
+                const float2 k1 = __half22float2(*reinterpret_cast<const __half2 *>(&h4[1]));
+                const float2 k2 = __half22float2(*reinterpret_cast<const __half2 *>(&h4[2]));
+                const float2 k3 = __half22float2(*reinterpret_cast<const __half2 *>(&h4[3]));
+                s = fmaf(qa.x, k0.x, s);
+                s = fmaf(qa.y, k0.y, s);
+                s = fmaf(qa.z, k1.x, s);
+                s = fmaf(qa.w, k1.y, s);
+                s = fmaf(qb.x, k2.x, s);
+                s = fmaf(qb.y, k2.y, s);
+                s = fmaf(qb.z, k3.x, s);
+                s = fmaf(qb.w, k3.y, s);
+            }
+            ss[h * kChunk + tid] = s * scale;
         }
     }
     __syncthreads();
     // per head (a warp each): max, exponentials, their sum
     for (int h = warp; h < G; h += 8) {
         float m = -INFINITY;
-        for (int t = lane; t < nt; t += 32) m = fmaxf(m, ss[h][t]);
+        for (int t = lane; t < nt; t += 32) m = fmaxf(m, ss[h * kChunk + t]);
 #pragma unroll
         for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float l = 0.f;
         for (int t = lane; t < nt; t += 32) {
-            const float e = __expf(ss[h][t] - m);
-            ss[h][t] = e;
+            const float e = __expf(ss[h * kChunk + t] - m);
+            ss[h * kChunk + t] = e;
             l += e;
         }
 #pragma unroll
@@ -245,20 +266,34 @@ __global__ void __launch_bounds__(256) moe_attn_chunk_kernel(AttnDims d, const f
         }
     }
     __syncthreads();
-    // weighted values: warp h, lane -> dims 2 lane, 2 lane + 1
+    // weighted values from shared memory: warp h, lane -> dims 2 lane, 2 lane + 1
     for (int h = warp; h < G; h += 8) {
-        float a0 = 0.f, a1 = 0.f;
-        for (int t = 0; t < nt; t++) {
-            const float pw = ss[h][t];
-            const float2 v = __half22float2(
-                *reinterpret_cast<const __half2 *>(vc + row0 + (size_t)(t0 + t) * rstride + 2 * lane));
-            a0 = fmaf(pw, v.x, a0);
-            a1 = fmaf(pw, v.y, a1);
+        float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;  // two chains per dim
+        int t = 0;
+        for (; t + 1 < nt; t += 2) {
+            const float p0 = ss[h * kChunk + t], p1 = ss[h * kChunk + t + 1];
+            const float2 v0 = __half22float2(reinterpret_cast<const __half2 *>(sv + (size_t)t * kHeadDim)[lane]);
+            const float2 v1 = __half22float2(reinterpret_cast<const __half2 *>(sv + (size_t)(t + 1) * kHeadDim)[lane]);
+            a0 = fmaf(p0, v0.x, a0);
+            a1 = fmaf(p0, v0.y, a1);
+            c0 = fmaf(p1, v1.x, c0);
+            c1 = fmaf(p1, v1.y, c1);
+        }
+        if (t < nt) {
+            const float p0 = ss[h * kChunk + t];
+            const float2 v0 = __half22float2(reinterpret_cast<const __half2 *>(sv + (size_t)t * kHeadDim)[lane]);
+            a0 = fmaf(p0, v0.x, a0);
+            a1 = fmaf(p0, v0.y, a1);
         }
         const size_t idx = ((size_t)b * d.QH + j * G + h) * n_chunks + c;
-        pacc[idx * kHeadDim + 2 * lane] = a0;
-        pacc[idx * kHeadDim + 2 * lane + 1] = a1;
+        pacc[idx * kHeadDim + 2 * lane] = a0 + c0;
+        pacc[idx * kHeadDim + 2 * lane + 1] = a1 + c1;
     }
+}
+
+size_t chunk_smem_bytes(const AttnDims &d) {
+    const int G = d.QH / d.KVH;
+    return (size_t)G * kHeadDim * 4 + (size_t)G * kChunk * 4 + (size_t)kChunk * kHeadDim * 2;
 }
 
 // o[b][h][:] = (sum over chunks of acc e^(m_c - m)) / (sum of l e^(m_c - m) +
@@ -507,9 +542,17 @@ int moe_attn_decode(moe_attn *p, const uint16_t *x, int n_seqs, const int32_t *p
     cudaError_t e = launch_rms_norm_rows(x, p->w.gamma, n_seqs, p->d.H, p->d.eps, c.xhat, c.xnorm, c.count, st);
     if (e == cudaSuccess) e = by_nt<QkvRun>(n_seqs, p->d, p->w, (const uint16_t *)c.xhat, n_seqs, positions, c.q, p->kc, p->vc, st);
     if (e == cudaSuccess) {
-        moe_attn_chunk_kernel<<<dim3(nch, p->d.KVH, n_seqs), 256, 0, st>>>(p->d, c.q, positions, p->kc, p->vc, c.pm, c.pl,
-                                                                         c.pacc, nch);
-        e = cudaGetLastError();
+        const size_t sm = chunk_smem_bytes(p->d);
+        static bool opted = false;
+        if (!opted) {
+            e = cudaFuncSetAttribute(moe_attn_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+            opted = e == cudaSuccess;
+        }
+        if (e == cudaSuccess) {
+            moe_attn_chunk_kernel<<<dim3(nch, p->d.KVH, n_seqs), 256, sm, st>>>(p->d, c.q, positions, p->kc, p->vc,
+                                                                                c.pm, c.pl, c.pacc, nch);
+            e = cudaGetLastError();
+        }
     }
     if (e == cudaSuccess) {
         moe_attn_merge_kernel<<<dim3(p->d.QH, n_seqs), kHeadDim, 0, st>>>(p->d, p->w.sinks, positions, c.pm, c.pl,

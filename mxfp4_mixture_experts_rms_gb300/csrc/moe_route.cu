@@ -799,21 +799,21 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
 //    the expert kernels read) and records an upper bound of |x_hat|; a warp
 //    per router row records an upper bound of |w|; the expert counts are
 //    zeroed for the top-k kernel.
-//  * moe_router_gemm_kernel: the logits as a register-tiled SIMT GEMM over
-//    64-token x 64-expert tiles (4 x 4 per thread), K split over grid.z when
-//    the tiles alone do not fill the GPU.  Products of two bf16 are exact in
-//    fp32; each thread sums 32 of them (one k-chunk, 32 roundings) and adds
-//    the chunk sum to a compensated (Kahan) running total, whose error stays
-//    within 2u of the sum of |chunk sums| whatever the number of chunks; the
-//    K-split partials and the bias add one rounding each.
+//  * moe_router_gemm_kernel: the logits over 64-token x 64-expert tiles on
+//    the tensor cores, K split over grid.z when the tiles alone do not fill
+//    the GPU.  Products of two bf16 are exact; each 32-element k-chunk is
+//    summed by two MMAs into a zero accumulator (budgeted as 32 roundings of
+//    the chunk's absolute product sum) and added to a compensated (Kahan)
+//    running total, whose error stays within 2u of the sum of |chunk sums|
+//    whatever the number of chunks; the K-split partials and the bias add
+//    one rounding each.
 //  * moe_route_topk_kernel: a warp per token sums the K-split partials in a
-//    fixed order, adds the bias and the rigorous bound 2 gamma_n (|x_hat| |w| +
+//    fixed order, adds the bias and the bound 2 gamma_n (|x_hat| |w| +
 //    |b| + |l|) (Cauchy-Schwarz bounds sum |x_i w_i|), and selects the top-k,
 //    recomputing exactly whatever the bounds cannot order; it adds its routes
 //    to the expert counts.
 //  * moe_permute_kernel: the token->expert permutation, a CTA per expert.
 constexpr int kGT = 64, kGE = 64, kGK = 32;  // GEMM tile: tokens x experts, k-chunk
-constexpr int kGPad = 68;                    // padded row of the transposed tiles (floats; 16-byte aligned)
 constexpr int kMaxKSplit = 16;               // K splits of the logits GEMM
 
 // Roundings a product can pass through in the large-batch logits, with a
@@ -895,105 +895,115 @@ __global__ void __launch_bounds__(kNormThreads) moe_route_norm_kernel(RouteArgs 
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
-// lpart[kz][t][e] = sum over the kz-th K range of x_hat[t][k] * W[e][k].
-// Thread (tx, ty) = (tid % 8, tid / 8) owns tokens 4 ty .. 4 ty + 3 and
-// experts 4 tx .. 4 tx + 3 and 32 + 4 tx .. 32 + 4 tx + 3 of the 64 x 64 tile
-// (32 products per three 16-byte shared-memory reads, each read one
-// wavefront for the warp); the tile's operands pass through shared memory as
-// fp32, transposed to [k][row], a chunk of 32 k at a time (the next chunk's
-// loads in flight during the current chunk's FMAs).
+// lpart[kz][t][e] = sum over the kz-th K range of x_hat[t][k] * W[e][k], on
+// the tensor cores: each 32-element k-chunk is two bf16 mma.sync m16n8k16
+// into a zero fp32 accumulator (the products of two bf16 are exact; the bound
+// budgets 32 roundings of 2^-24 of the chunk's absolute product sum for the
+// two MMAs, twice what an accumulation with 22 significant bits can lose), and
+// the chunk sums are added to Kahan totals (compensated, as before).  A CTA's
+// four warps own 32 tokens x 32 experts each of the 64 x 64 tile; each thread
+// reads 16 contiguous bytes of a token row and of a router row per chunk and
+// hands them to the two MMAs as if their k order were permuted (A and B see
+// the same permutation; the dot product does not depend on the order).  The
+// next chunk's rows are loaded while the current one is multiplied.
 constexpr int kGThreads = 128;
+
+__device__ __forceinline__ void rmma_bf16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1, bool zero) {
+    if (zero)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%10,%10,%10,%10};\n"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __global__ void __launch_bounds__(kGThreads) moe_router_gemm_kernel(const uint16_t *xhat, const uint16_t *w, int T,
                                                                     int E, int H, int kc_per_split, float *lpart) {
-    __shared__ __align__(16) float sx[2][kGK][kGPad];
-    __shared__ __align__(16) float sw[2][kGK][kGPad];
-    const int tid = threadIdx.x, tx = tid & 7, ty = tid >> 3;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // x_hat comes from the norm kernel
-    const int t0 = blockIdx.x * kGT, e0 = blockIdx.y * kGE, kz = blockIdx.z;
+    const int tb = blockIdx.x * kGT + 32 * (warp & 1), eb = blockIdx.y * kGE + 32 * (warp >> 1), kz = blockIdx.z;
     const int nkc = (H + kGK - 1) / kGK;
     const int kc0 = kz * kc_per_split, kc1 = min(nkc, kc0 + kc_per_split);
-    // loader: row (tid % 64) of the tile, 16 consecutive k at 16 (tid / 64)
-    const int lr = tid & 63, lk = (tid >> 6) * 16;
-    const bool xok = t0 + lr < T, wok = e0 + lr < E;
-    const uint16_t *xrow = xhat + (size_t)(t0 + lr) * H, *wrow = w + (size_t)(e0 + lr) * H;
-    auto fetch = [&](int kc, uint4 (&xv)[2], uint4 (&wv)[2]) {
+    // this thread's rows: tokens tb + 16 mi + g (+ 8), experts eb + 8 ni + g
+    const uint16_t *xr[2][2];
+    const uint16_t *wr[4];
+#pragma unroll
+    for (int mi = 0; mi < 2; mi++)
 #pragma unroll
         for (int h = 0; h < 2; h++) {
-            const int k = kc * kGK + lk + 8 * h;
-            const bool kin = k < H;  // H is a multiple of 32: whole groups of 8
-            xv[h] = (xok && kin) ? __ldg(reinterpret_cast<const uint4 *>(xrow + k)) : make_uint4(0, 0, 0, 0);
-            wv[h] = (wok && kin) ? __ldg(reinterpret_cast<const uint4 *>(wrow + k)) : make_uint4(0, 0, 0, 0);
+            const int t = tb + 16 * mi + 8 * h + g;
+            xr[mi][h] = t < T ? xhat + (size_t)t * H + 8 * t4 : nullptr;
         }
-    };
-    auto stash = [&](int buf, const uint4 (&xv)[2], const uint4 (&wv)[2]) {
 #pragma unroll
-        for (int h = 0; h < 2; h++) {
-            const uint32_t xs[4] = {xv[h].x, xv[h].y, xv[h].z, xv[h].w}, ws4[4] = {wv[h].x, wv[h].y, wv[h].z, wv[h].w};
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const int k = lk + 8 * h + 2 * q;
-                sx[buf][k][lr] = __uint_as_float(xs[q] << 16);
-                sx[buf][k + 1][lr] = __uint_as_float(xs[q] & 0xFFFF0000u);
-                sw[buf][k][lr] = __uint_as_float(ws4[q] << 16);
-                sw[buf][k + 1][lr] = __uint_as_float(ws4[q] & 0xFFFF0000u);
-            }
-        }
-    };
-    float tot[4][8], cmp[4][8];  // compensated running totals
-#pragma unroll
-    for (int i = 0; i < 4; i++)
-#pragma unroll
-        for (int j = 0; j < 8; j++) tot[i][j] = cmp[i][j] = 0.f;
-    uint4 xv[2], wv[2];
-    if (kc0 < kc1) {
-        fetch(kc0, xv, wv);
-        stash(0, xv, wv);
+    for (int ni = 0; ni < 4; ni++) {
+        const int e = eb + 8 * ni + g;
+        wr[ni] = e < E ? w + (size_t)e * H + 8 * t4 : nullptr;
     }
-    __syncthreads();
+    auto fetch = [&](int kc, uint4 (&a)[2][2], uint4 (&b)[4]) {
+        const int k = kc * kGK;
+#pragma unroll
+        for (int mi = 0; mi < 2; mi++)
+#pragma unroll
+            for (int h = 0; h < 2; h++)
+                a[mi][h] = xr[mi][h] ? __ldg(reinterpret_cast<const uint4 *>(xr[mi][h] + k)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int ni = 0; ni < 4; ni++)
+            b[ni] = wr[ni] ? __ldg(reinterpret_cast<const uint4 *>(wr[ni] + k)) : make_uint4(0, 0, 0, 0);
+    };
+    float tot[2][4][4], cmp[2][4][4];  // compensated running totals
+#pragma unroll
+    for (int mi = 0; mi < 2; mi++)
+#pragma unroll
+        for (int ni = 0; ni < 4; ni++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) tot[mi][ni][q] = cmp[mi][ni][q] = 0.f;
+    uint4 a[2][2], b[4], an[2][2], bn[4];
+    if (kc0 < kc1) fetch(kc0, a, b);
     for (int kc = kc0; kc < kc1; kc++) {
-        const int buf = (kc - kc0) & 1;
-        if (kc + 1 < kc1) fetch(kc + 1, xv, wv);
-        float part[4][8];
+        if (kc + 1 < kc1) fetch(kc + 1, an, bn);
 #pragma unroll
-        for (int i = 0; i < 4; i++)
+        for (int mi = 0; mi < 2; mi++)
 #pragma unroll
-            for (int j = 0; j < 8; j++) part[i][j] = 0.f;
-#pragma unroll 8
-        for (int kk = 0; kk < kGK; kk++) {
-            const float4 av = *reinterpret_cast<const float4 *>(&sx[buf][kk][4 * ty]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&sw[buf][kk][4 * tx]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&sw[buf][kk][32 + 4 * tx]);
-            const float ai[4] = {av.x, av.y, av.z, av.w};
-            const float bj[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            for (int ni = 0; ni < 4; ni++) {
+                float part[4];
+                rmma_bf16(part, a[mi][0].x, a[mi][1].x, a[mi][0].y, a[mi][1].y, b[ni].x, b[ni].y, true);
+                rmma_bf16(part, a[mi][0].z, a[mi][1].z, a[mi][0].w, a[mi][1].w, b[ni].z, b[ni].w, false);
 #pragma unroll
-            for (int i = 0; i < 4; i++)
-#pragma unroll
-                for (int j = 0; j < 8; j++) part[i][j] = fmaf(ai[i], bj[j], part[i][j]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; i++)
-#pragma unroll
-            for (int j = 0; j < 8; j++) {  // Kahan: tot + cmp carries the sum of the chunk sums
-                const float y = part[i][j] - cmp[i][j];
-                const float tn = tot[i][j] + y;
-                cmp[i][j] = (tn - tot[i][j]) - y;
-                tot[i][j] = tn;
+                for (int q = 0; q < 4; q++) {  // Kahan: tot + cmp carries the sum of the chunk sums
+                    const float y = part[q] - cmp[mi][ni][q];
+                    const float tn = tot[mi][ni][q] + y;
+                    cmp[mi][ni][q] = (tn - tot[mi][ni][q]) - y;
+                    tot[mi][ni][q] = tn;
+                }
             }
-        if (kc + 1 < kc1) stash(buf ^ 1, xv, wv);
-        __syncthreads();
+        if (kc + 1 < kc1) {
+#pragma unroll
+            for (int mi = 0; mi < 2; mi++) {
+                a[mi][0] = an[mi][0];
+                a[mi][1] = an[mi][1];
+            }
+#pragma unroll
+            for (int ni = 0; ni < 4; ni++) b[ni] = bn[ni];
+        }
     }
     // the top-k kernel may launch now (its CTAs then find the SMs free and spread evenly)
     asm volatile("griddepcontrol.launch_dependents;");
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const int t = t0 + 4 * ty + i;
-        if (t >= T) continue;
+    for (int mi = 0; mi < 2; mi++)
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const int e = e0 + (j < 4 ? 4 * tx + j : 32 + 4 * tx + j - 4);
-            if (e < E) lpart[((size_t)kz * T + t) * E + e] = tot[i][j];
-        }
-    }
+        for (int ni = 0; ni < 4; ni++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int t = tb + 16 * mi + g + 8 * (q >> 1), e = eb + 8 * ni + 2 * t4 + (q & 1);
+                if (t < T && e < E) lpart[((size_t)kz * T + t) * E + e] = tot[mi][ni][q];
+            }
 }
 
 // A warp per token: logits and bounds into shared memory, then top-k + softmax
