@@ -16,8 +16,11 @@
 //    exact angle, evaluated in double), then q to the workspace (fp32) and k,
 //    v into the caller's fp16 cache at the token's position;
 //  * moe_attn_chunk_kernel: one CTA per (256-token chunk of the visible
-//    context, kv head, sequence): the scores of the kv head's query heads,
-//    the chunk's softmax statistics and weighted value sums;
+//    context, kv head, sequence): the scores of the kv head's query heads and
+//    their weighted value sums on the tensor cores (mma.sync m16n8k16 f16,
+//    the query heads as the MMA's rows; fp32 q and probabilities split into
+//    fp16 high and low parts, keys and values fp16 as cached), the chunk's
+//    softmax statistics;
 //  * moe_attn_merge_kernel: the chunks and the head's sink logit combined
 //    into o, rounded to bf16;
 //  * moe_attn_out_kernel: out = x + Wo o + bo with the same GEMV core.
@@ -40,7 +43,7 @@ constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kMaxSeqs = 32;      // tokens per decode step (4 MMA column tiles of 8)
 constexpr int kChunk = 256;       // context tokens per attention CTA
-constexpr int kMaxQPerKV = 16;    // query heads sharing one kv head
+constexpr int kMaxQPerKV = 16;    // query heads sharing one kv head (the attention MMA's 16 rows)
 
 struct AttnDims {
     int H, QH, KVH;
@@ -178,20 +181,45 @@ __device__ __forceinline__ void visible_range(const AttnDims &d, int p, int &fir
     count = n - first;
 }
 
+// fp16 pair (x, y) rounded from fp32, and the pair of what that rounding left
+// (so hi + lo carries about 22 significant bits of each value).
+__device__ __forceinline__ void split_half2(float x, float y, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(x, y);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+__device__ __forceinline__ void mma_f16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+constexpr int kVPad = kHeadDim + 8;  // value row in shared memory (halves): ldmatrix rows on distinct banks
+
 // Partials per (sequence, query head, chunk): max score, sum of exp(s - max),
-// and the exp-weighted value sums [64].  Shared memory: the G query rows
-// (fp32), the chunk's scores [G][256] and its value rows [256][64] (fp16),
-// staged once for the G heads that read them.
-__global__ void __launch_bounds__(256, 3) moe_attn_chunk_kernel(AttnDims d, const float *q, const int32_t *pos,
+// and the exp-weighted value sums [64], on the tensor cores (up to 16 query
+// heads per kv head as the MMA's 16 rows).  Scores: q (split into fp16 high
+// and low parts, about 22 significant bits together) against the fp16 keys
+// (exact), warp w taking tokens 32 w .. 32 w + 31, each thread reading 16
+// contiguous bytes of a key row per 32 dims and the matching slice of q (the
+// MMA sees both in the same permuted k order).  Weighted values: the
+// probabilities (split the same way) against the value rows staged in shared
+// memory (transposed by ldmatrix), warp w taking dims 8 w .. 8 w + 7.
+__global__ void __launch_bounds__(256) moe_attn_chunk_kernel(AttnDims d, const float *q, const int32_t *pos,
                                                              const __half *kc, const __half *vc, float *pm, float *pl,
                                                              float *pacc, int n_chunks) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
     const int G = d.QH / d.KVH;
-    float *sq = reinterpret_cast<float *>(smem);             // [G][64]
-    float *ss = sq + G * kHeadDim;                            // [G][256]
-    __half *sv = reinterpret_cast<__half *>(ss + G * kChunk);  // [256][64]
+    float *ss = reinterpret_cast<float *>(smem);                 // [16][256] scores, then probabilities
+    __half *sv = reinterpret_cast<__half *>(ss + 16 * kChunk);  // [256][kVPad] value rows
     const int p = pos[b];
     if (p < 0 || p >= d.max_ctx) return;
     int first, count;
@@ -199,61 +227,75 @@ __global__ void __launch_bounds__(256, 3) moe_attn_chunk_kernel(AttnDims d, cons
     const int t0 = first + c * kChunk;
     const int nt = min(kChunk, first + count - t0);
     if (nt <= 0) return;
-    const float scale = rsqrtf((float)kHeadDim);
-    for (int i = tid; i < G * kHeadDim; i += 256)
-        sq[i] = q[(size_t)b * d.QH * kHeadDim + (size_t)(j * G) * kHeadDim + i];
     const size_t row0 = ((size_t)b * d.max_ctx) * d.KVH * kHeadDim + (size_t)j * kHeadDim;
     const size_t rstride = (size_t)d.KVH * kHeadDim;
-    // thread t <-> token t0 + t: its key row to registers (fp16 pairs), its
-    // value row to shared memory
-    uint4 kr4[kHeadDim / 8];
-    if (tid < nt) {
-        const uint4 *kr = reinterpret_cast<const uint4 *>(kc + row0 + (size_t)(t0 + tid) * rstride);
-        const __half *vr = vc + row0 + (size_t)(t0 + tid) * rstride;
+    // value rows of the chunk into shared memory (rows past the chunk: zeros)
+    {
+        const int t = tid;  // one row per thread
+        uint4 *dst = reinterpret_cast<uint4 *>(sv + (size_t)t * kVPad);
+        if (t < nt) {
+            const __half *vr = vc + row0 + (size_t)(t0 + t) * rstride;
 #pragma unroll
-        for (int v = 0; v < kHeadDim / 8; v++) {
-            const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(sv + (size_t)tid * kHeadDim + 8 * v));
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(vr + 8 * v) : "memory");
+            for (int v = 0; v < kHeadDim / 8; v++) {
+                const uint32_t da = static_cast<uint32_t>(__cvta_generic_to_shared(dst + v));
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(da), "l"(vr + 8 * v) : "memory");
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < kHeadDim / 8; v++) dst[v] = make_uint4(0, 0, 0, 0);
         }
+    }
+    // q slices of heads g and g + 8 (zero rows past G), split high / low
+    const float *qb = q + (size_t)b * d.QH * kHeadDim + (size_t)(j * G) * kHeadDim;
+    uint32_t qh[2][2][4], ql[2][2][4];  // [row g / g+8][32-dim block][pair]
 #pragma unroll
-        for (int v = 0; v < kHeadDim / 8; v++) kr4[v] = kr[v];
+    for (int r = 0; r < 2; r++)
+#pragma unroll
+        for (int db = 0; db < 2; db++) {
+            const int h = g + 8 * r;
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) v[e] = h < G ? qb[(size_t)h * kHeadDim + 32 * db + 8 * t4 + e] : 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; e++) split_half2(v[2 * e], v[2 * e + 1], qh[r][db][e], ql[r][db][e]);
+        }
+    // scores of this warp's 32 tokens (4 column tiles of 8)
+    const float scale = rsqrtf((float)kHeadDim);
+#pragma unroll
+    for (int ni = 0; ni < 4; ni++) {
+        const int tt = 32 * warp + 8 * ni + g;  // this thread's key row
+        uint4 kv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (tt < nt) {
+            const uint4 *kr = reinterpret_cast<const uint4 *>(kc + row0 + (size_t)(t0 + tt) * rstride);
+            kv[0] = kr[t4];
+            kv[1] = kr[4 + t4];
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int db = 0; db < 2; db++) {
+            mma_f16(acc, qh[0][db][0], qh[1][db][0], qh[0][db][1], qh[1][db][1], kv[db].x, kv[db].y);
+            mma_f16(acc, qh[0][db][2], qh[1][db][2], qh[0][db][3], qh[1][db][3], kv[db].z, kv[db].w);
+            mma_f16(acc, ql[0][db][0], ql[1][db][0], ql[0][db][1], ql[1][db][1], kv[db].x, kv[db].y);
+            mma_f16(acc, ql[0][db][2], ql[1][db][2], ql[0][db][3], ql[1][db][3], kv[db].z, kv[db].w);
+        }
+        // acc[0..1]: head g, tokens 2 t4, 2 t4 + 1 of the tile; acc[2..3]: head g + 8
+#pragma unroll
+        for (int qd = 0; qd < 4; qd++) {
+            const int h = g + 8 * (qd >> 1), t = 32 * warp + 8 * ni + 2 * t4 + (qd & 1);
+            if (h < G) ss[h * kChunk + t] = t < nt ? acc[qd] * scale : -INFINITY;
+        }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    if (tid < nt) {
-        for (int h = 0; h < G; h++) {
-            const float4 *q4 = reinterpret_cast<const float4 *>(sq + h * kHeadDim);
-            float s = 0.f;
-#pragma unroll
-            for (int v = 0; v < kHeadDim / 8; v++) {
-                const uint32_t h4[4] = {kr4[v].x, kr4[v].y, kr4[v].z, kr4[v].w};
-                const float4 qa = q4[2 * v], qb = q4[2 * v + 1];
-                const float2 k0 = __half22float2(*reinterpret_cast<const __half2 *>(&h4[0]));
-                const float2 k1 = __half22float2(*reinterpret_cast<const __half2 *>(&h4[1]));
-                const float2 k2 = __half22float2(*reinterpret_cast<const __half2 *>(&h4[2]));
-                const float2 k3 = __half22float2(*reinterpret_cast<const __half2 *>(&h4[3]));
-                s = fmaf(qa.x, k0.x, s);
-                s = fmaf(qa.y, k0.y, s);
-                s = fmaf(qa.z, k1.x, s);
-                s = fmaf(qa.w, k1.y, s);
-                s = fmaf(qb.x, k2.x, s);
-                s = fmaf(qb.y, k2.y, s);
-                s = fmaf(qb.z, k3.x, s);
-                s = fmaf(qb.w, k3.y, s);
-            }
-            ss[h * kChunk + tid] = s * scale;
-        }
-    }
-    __syncthreads();
-    // per head (a warp each): max, exponentials, their sum
+    // per head (a warp each): max, exponentials (0 past the chunk), their sum
     for (int h = warp; h < G; h += 8) {
         float m = -INFINITY;
         for (int t = lane; t < nt; t += 32) m = fmaxf(m, ss[h * kChunk + t]);
 #pragma unroll
         for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float l = 0.f;
-        for (int t = lane; t < nt; t += 32) {
-            const float e = __expf(ss[h * kChunk + t] - m);
+        for (int t = lane; t < kChunk; t += 32) {
+            const float e = t < nt ? __expf(ss[h * kChunk + t] - m) : 0.f;
             ss[h * kChunk + t] = e;
             l += e;
         }
@@ -266,34 +308,45 @@ __global__ void __launch_bounds__(256, 3) moe_attn_chunk_kernel(AttnDims d, cons
         }
     }
     __syncthreads();
-    // weighted values from shared memory: warp h, lane -> dims 2 lane, 2 lane + 1
-    for (int h = warp; h < G; h += 8) {
-        float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;  // two chains per dim
-        int t = 0;
-        for (; t + 1 < nt; t += 2) {
-            const float p0 = ss[h * kChunk + t], p1 = ss[h * kChunk + t + 1];
-            const float2 v0 = __half22float2(reinterpret_cast<const __half2 *>(sv + (size_t)t * kHeadDim)[lane]);
-            const float2 v1 = __half22float2(reinterpret_cast<const __half2 *>(sv + (size_t)(t + 1) * kHeadDim)[lane]);
-            a0 = fmaf(p0, v0.x, a0);
-            a1 = fmaf(p0, v0.y, a1);
-            c0 = fmaf(p1, v1.x, c0);
-            c1 = fmaf(p1, v1.y, c1);
+    // weighted values: this warp's 8 dims, the chunk's tokens 16 at a time
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    const int ksteps = (nt + 15) / 16;
+    for (int ks = 0; ks < ksteps; ks++) {
+        const int kt = 16 * ks;
+        uint32_t ph[4], plo[4];
+        {
+            const float *r0 = ss + (size_t)g * kChunk + kt + 2 * t4;        // head g
+            const float *r1 = ss + (size_t)(g + 8) * kChunk + kt + 2 * t4;  // head g + 8
+            const bool h1 = g + 8 < G;
+            const bool h0 = g < G;
+            split_half2(h0 ? r0[0] : 0.f, h0 ? r0[1] : 0.f, ph[0], plo[0]);
+            split_half2(h1 ? r1[0] : 0.f, h1 ? r1[1] : 0.f, ph[1], plo[1]);
+            split_half2(h0 ? r0[8] : 0.f, h0 ? r0[9] : 0.f, ph[2], plo[2]);
+            split_half2(h1 ? r1[8] : 0.f, h1 ? r1[9] : 0.f, ph[3], plo[3]);
         }
-        if (t < nt) {
-            const float p0 = ss[h * kChunk + t];
-            const float2 v0 = __half22float2(reinterpret_cast<const __half2 *>(sv + (size_t)t * kHeadDim)[lane]);
-            a0 = fmaf(p0, v0.x, a0);
-            a1 = fmaf(p0, v0.y, a1);
+        uint32_t b0, b1;
+        {
+            const __half *rowp = sv + (size_t)(kt + (lane & 15)) * kVPad + 8 * warp;
+            const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(rowp));
+            asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                         : "=r"(b0), "=r"(b1)
+                         : "r"(addr));
         }
+        mma_f16(o, ph[0], ph[1], ph[2], ph[3], b0, b1);
+        mma_f16(o, plo[0], plo[1], plo[2], plo[3], b0, b1);
+    }
+    // o[0..1]: head g, dims 8 w + 2 t4, + 1; o[2..3]: head g + 8
+#pragma unroll
+    for (int qd = 0; qd < 4; qd++) {
+        const int h = g + 8 * (qd >> 1);
+        if (h >= G) continue;
         const size_t idx = ((size_t)b * d.QH + j * G + h) * n_chunks + c;
-        pacc[idx * kHeadDim + 2 * lane] = a0 + c0;
-        pacc[idx * kHeadDim + 2 * lane + 1] = a1 + c1;
+        pacc[idx * kHeadDim + 8 * warp + 2 * t4 + (qd & 1)] = o[qd];
     }
 }
 
-size_t chunk_smem_bytes(const AttnDims &d) {
-    const int G = d.QH / d.KVH;
-    return (size_t)G * kHeadDim * 4 + (size_t)G * kChunk * 4 + (size_t)kChunk * kHeadDim * 2;
+size_t chunk_smem_bytes(const AttnDims &) {
+    return (size_t)16 * kChunk * 4 + (size_t)kChunk * kVPad * 2;
 }
 
 // o[b][h][:] = (sum over chunks of acc e^(m_c - m)) / (sum of l e^(m_c - m) +
