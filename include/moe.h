@@ -400,8 +400,9 @@ int moe_attn_set_i(moe_attn *plan, const char *key, long long value);
 /* "rms_eps", "rope_base", "rope_factor", "rope_original_context",
  * "rope_beta_fast", "rope_beta_slow" (positive, finite). */
 int moe_attn_set_f(moe_attn *plan, const char *key, double value);
-/* Device workspace a step needs (x_hat, q, the chunk partials, o): caller-owned,
- * 256-byte aligned, borrowed by moe_attn_set_workspace. */
+/* Device workspace a step needs (x_hat; q, k, v before RoPE; the RoPE table;
+ * the chunk partials; o): caller-owned, 256-byte aligned, borrowed by
+ * moe_attn_set_workspace. */
 size_t moe_attn_workspace_bytes(const moe_attn *plan);
 int moe_attn_set_workspace(moe_attn *plan, void *dev_ptr, size_t bytes);
 /* The key and value caches (fp16, layout above; borrowed). */

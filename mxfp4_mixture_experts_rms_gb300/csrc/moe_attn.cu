@@ -6,28 +6,27 @@
 // with bias and the residual add; turbospark-runtime gptoss/mod.rs module doc
 // comment).
 //
-// Kernels, in stream order:
+// Kernels, in stream order (each after the first launched as a programmatic
+// dependent of the one before):
 //  * the routing's norm kernel: x_hat = bf16(rms_norm(x) * gamma), exact;
-//  * moe_attn_qkv_kernel: the three projections as one GEMV over 16-row tiles
-//    (mma.sync m16n8k16, bf16 weights and x_hat, fp32 accumulation; four
-//    warps split K and add their partials in a fixed order).  A q or k tile
-//    holds dims d and d + 32 of one head in its upper and lower eight rows, so
-//    that each RoPE pair sits in one thread; biases, RoPE (cos and sin of the
-//    exact angle, evaluated in double), then q to the workspace (fp32) and k,
-//    v into the caller's fp16 cache at the token's position;
+//  * moe_attn_proj_kernel<., 0>: q, k, v = W x_hat + b as one GEMV over
+//    16-row tiles of the concatenated weights (mma.sync m16n8k16, bf16
+//    weights and x_hat, fp32 accumulation; eight warps split K and add their
+//    partials in a fixed order), fp32 to the workspace, and the RoPE table of
+//    each sequence's position (cos and sin per pair, from the angle reduced
+//    in double);
 //  * moe_attn_chunk_kernel: one CTA per (256-token chunk of the visible
-//    context, kv head, sequence): the scores of the kv head's query heads and
-//    their weighted value sums on the tensor cores (mma.sync m16n8k16 f16,
-//    the query heads as the MMA's rows; fp32 q and probabilities split into
-//    fp16 high and low parts, keys and values fp16 as cached), the chunk's
-//    softmax statistics;
+//    context, kv head, sequence); the chunk holding the new token first
+//    appends its rotated key and its value to the caller's fp16 cache.  Each
+//    warp takes 32 of the chunk's tokens: the scores of the kv head's query
+//    heads (q rotated as it is read) and their weighted value sums on the
+//    tensor cores (mma.sync m16n8k16 f16, the query heads as the MMA's rows;
+//    fp32 q and probabilities split into fp16 high and low parts, keys and
+//    values fp16 as cached; the probabilities stay in registers), the warps'
+//    softmax statistics combined in warp order;
 //  * moe_attn_merge_kernel: the chunks and the head's sink logit combined
 //    into o, rounded to bf16;
-//  * moe_attn_out_kernel: out = x + Wo o + bo with the same GEMV core.
-// In the GEMV core each thread reads 16 contiguous bytes of a weight row and
-// of an activation row per 32-element block, and hands them to two MMAs as
-// if their k order were permuted: the dot product does not depend on the
-// order of k, and A and B see the same permutation.
+//  * moe_attn_proj_kernel<., 1>: out = x + Wo o + bo with the same GEMV core.
 #include "moe_common.cuh"
 #include "../../include/moe.h"
 
@@ -39,8 +38,6 @@
 namespace {
 
 constexpr int kHeadDim = 64;
-constexpr int kGemvWarps = 8;
-constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kMaxSeqs = 32;      // tokens per decode step (4 MMA column tiles of 8)
 constexpr int kChunk = 256;       // context tokens per attention CTA
 constexpr int kMaxQPerKV = 16;    // query heads sharing one kv head (the attention MMA's 16 rows)
@@ -69,10 +66,40 @@ __device__ __forceinline__ void mma_bf16(float d[4], uint32_t a0, uint32_t a1, u
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---- the projections ----
+// One CTA per 16 weight rows (8 warps split K).  Each thread reads 16
+// contiguous bytes of a weight row and of an activation row per 32-element
+// block and hands them to two MMAs (mma.sync m16n8k16, bf16, fp32
+// accumulate) as if their k order were permuted: the dot product does not
+// depend on the order of k, and A and B see the same permutation.
+constexpr double kTwoPi = 6.283185307179586476925;
+constexpr double kInvTwoPi = 0.159154943091895335769;
+
+struct ProjArgs {
+    AttnDims d;
+    int rows, K;           // weight rows, reduction length
+    const uint16_t *w[3];  // Q/K/V: wq, wk, wv (rows in that order); output: Wo
+    const float *bias[3];
+    int r1, r2;            // first row of the second and the third matrix
+    const uint16_t *x;     // activations [B][K]
+    int B;
+    // Q/K/V: q, k, v with biases, fp32 [B][rows]; the RoPE table (cos, sin)
+    // x attention factor [B][32]
+    float *raw;
+    float2 *rope;
+    const int32_t *pos;
+    // output: out = res + Wo o + bo
+    const uint16_t *res;
+    void *out;
+    int out_bf16;
+};
+
+__device__ __forceinline__ int proj_mat(const ProjArgs &a, int row) { return row < a.r1 ? 0 : row < a.r2 ? 1 : 2; }
+
 // acc[nt][0..1]: row lo, tokens 8 nt + 2 t4, + 1; acc[nt][2..3]: row hi.
 // Rows lo and hi (16-byte aligned row pointers, K elements each) against
 // activation rows X[b] (K elements, 16-byte aligned rows, b < B), over the
-// warp's share of the 32-element blocks; then the four warps' partials are
+// warp's share of the 32-element blocks; then the eight warps' partials are
 // added in warp order (result valid in warp 0).
 template <int NT>
 __device__ void gemv_tile(const uint16_t *wlo, const uint16_t *whi, const uint16_t *X, int B, int K, float (*red)[4],
@@ -80,7 +107,7 @@ __device__ void gemv_tile(const uint16_t *wlo, const uint16_t *whi, const uint16
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    const int nblk = K / 32, per = (nblk + kGemvWarps - 1) / kGemvWarps;
+    const int nblk = K / 32, per = (nblk + 8 - 1) / 8;
     const int b0 = warp * per, b1 = min(nblk, b0 + per);
     const uint16_t *xrow[NT];
 #pragma unroll
@@ -105,73 +132,72 @@ __device__ void gemv_tile(const uint16_t *wlo, const uint16_t *whi, const uint16
             for (int q = 0; q < 4; q++) red[((warp - 1) * NT + nt) * 32 + lane][q] = acc[nt][q];
     __syncthreads();
     if (warp == 0)
-        for (int w = 1; w < kGemvWarps; w++)
+        for (int w = 1; w < 8; w++)
 #pragma unroll
             for (int nt = 0; nt < NT; nt++)
 #pragma unroll
                 for (int q = 0; q < 4; q++) acc[nt][q] += red[((w - 1) * NT + nt) * 32 + lane][q];
 }
 
-// Tiles 0 .. QH*4-1: q (head ti/4, dims 8(ti%4) + g and + 32); then KVH*4 k
-// tiles the same way; then KVH*4 v tiles of 16 consecutive rows.
-template <int NT>
-__global__ void __launch_bounds__(kGemvThreads) moe_attn_qkv_kernel(AttnDims d, AttnWeights w, const uint16_t *xhat,
-                                                                    int B, const int32_t *pos, float *q,
-                                                                    __half *kc, __half *vc) {
-    __shared__ float red[(kGemvWarps - 1) * NT * 32][4];
+
+// 16 rows per CTA: Q/K/V (raw: biases added, RoPE later) or the output
+// (with the residual, fp32 or bf16).  The Q/K/V kernel also writes the RoPE
+// table: per sequence and pair, the angle pos f in double less the nearest
+// whole number of turns (exact to about 1e-11 at any position), then its
+// cosine and sine in float, times the attention factor.
+template <int NT, int KIND>
+__global__ void __launch_bounds__(256) moe_attn_proj_kernel(const __grid_constant__ ProjArgs a) {
+    __shared__ float red[7 * NT * 32][4];
     const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-    const int ti = blockIdx.x, H = d.H;
-    const int nq = d.QH * 4, nk = d.KVH * 4;
-    int kind, head, sub;  // 0 q, 1 k, 2 v
-    if (ti < nq) {
-        kind = 0, head = ti / 4, sub = ti % 4;
-    } else if (ti < nq + nk) {
-        kind = 1, head = (ti - nq) / 4, sub = (ti - nq) % 4;
-    } else {
-        kind = 2, head = (ti - nq - nk) / 4, sub = (ti - nq - nk) % 4;
-    }
-    int rlo, rhi;  // rows within the matrix
-    if (kind < 2) {
-        rlo = head * kHeadDim + 8 * sub + g;
-        rhi = rlo + 32;
-    } else {
-        rlo = head * kHeadDim + 16 * sub + g;
-        rhi = rlo + 8;
-    }
-    const uint16_t *W = kind == 0 ? w.wq : kind == 1 ? w.wk : w.wv;
-    const float *bias = kind == 0 ? w.bq : kind == 1 ? w.bk : w.bv;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the activations come from the previous kernel
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int rlo = blockIdx.x * 16 + g, rhi = rlo + 8;
+    const int m = proj_mat(a, rlo), base = m == 0 ? 0 : m == 1 ? a.r1 : a.r2;
     float acc[NT][4];
-    gemv_tile<NT>(W + (size_t)rlo * H, W + (size_t)rhi * H, xhat, B, H, red, acc);
+    gemv_tile<NT>(a.w[m] + (size_t)(rlo - base) * a.K, a.w[m] + (size_t)(rhi - base) * a.K, a.x, a.B, a.K, red, acc);
     if ((threadIdx.x >> 5) != 0) return;
-    const float blo = bias[rlo], bhi = bias[rhi];
+    const float blo = a.bias[m][rlo - base], bhi = a.bias[m][rhi - base];
 #pragma unroll
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
         for (int c = 0; c < 2; c++) {
             const int b = nt * 8 + 2 * t4 + c;
-            if (b >= B) continue;
-            float lo = acc[nt][c] + blo, hi = acc[nt][2 + c] + bhi;
-            const int p = pos[b];
-            if (p < 0 || p >= d.max_ctx) continue;  // outside the cache: the sequence is skipped
-            if (kind < 2) {
-                // RoPE pair 8 sub + g of the head: l cos - r sin, l sin + r cos
-                double sn, cs;
-                sincos((double)p * d.freq[8 * sub + g], &sn, &cs);
-                const float cf = (float)(cs * d.rope_af), sf = (float)(sn * d.rope_af);
-                const float l = lo, r = hi;
-                lo = l * cf - r * sf;
-                hi = l * sf + r * cf;
-            }
-            if (kind == 0) {
-                q[(size_t)b * d.QH * kHeadDim + rlo] = lo;
-                q[(size_t)b * d.QH * kHeadDim + rhi] = hi;
+            if (b >= a.B) continue;
+            const size_t ol = (size_t)b * a.rows + rlo, oh = (size_t)b * a.rows + rhi;
+            const float lo = acc[nt][c] + blo, hi = acc[nt][2 + c] + bhi;
+            if (KIND == 0) {
+                a.raw[ol] = lo;
+                a.raw[oh] = hi;
             } else {
-                __half *cache = kind == 1 ? kc : vc;
-                const size_t base = ((size_t)b * d.max_ctx + p) * d.KVH * kHeadDim;
-                cache[base + rlo] = __float2half_rn(lo);
-                cache[base + rhi] = __float2half_rn(hi);
+                const float yl = bf16_to_f32(a.res[ol]) + lo, yh = bf16_to_f32(a.res[oh]) + hi;
+                if (a.out_bf16) {
+                    const __nv_bfloat16 l = __float2bfloat16_rn(yl), h = __float2bfloat16_rn(yh);
+                    static_cast<uint16_t *>(a.out)[ol] = *reinterpret_cast<const uint16_t *>(&l);
+                    static_cast<uint16_t *>(a.out)[oh] = *reinterpret_cast<const uint16_t *>(&h);
+                } else {
+                    static_cast<float *>(a.out)[ol] = yl;
+                    static_cast<float *>(a.out)[oh] = yh;
+                }
             }
         }
+    if (KIND == 0)
+        for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+            const double ang = (double)a.pos[b] * a.d.freq[lane];
+            const float r = (float)fma(-rint(ang * kInvTwoPi), kTwoPi, ang);
+            float sn, cs;
+            sincosf(r, &sn, &cs);
+            a.rope[(size_t)b * 32 + lane] = make_float2(cs * (float)a.d.rope_af, sn * (float)a.d.rope_af);
+        }
+}
+
+template <int KIND>
+cudaError_t proj_launch(const ProjArgs &a, cudaStream_t st) {
+    const dim3 grid(a.rows / 16), block(256);
+    const int nt = (a.B + 7) / 8;
+    if (nt == 1) return launch_pdl(moe_attn_proj_kernel<1, KIND>, grid, block, 0, st, a);
+    if (nt == 2) return launch_pdl(moe_attn_proj_kernel<2, KIND>, grid, block, 0, st, a);
+    if (nt == 3) return launch_pdl(moe_attn_proj_kernel<3, KIND>, grid, block, 0, st, a);
+    return launch_pdl(moe_attn_proj_kernel<4, KIND>, grid, block, 0, st, a);
 }
 
 // Visible context of sequence b (its new token at position p is the last).
@@ -201,25 +227,39 @@ __device__ __forceinline__ void mma_f16(float d[4], uint32_t a0, uint32_t a1, ui
 }
 
 constexpr int kVPad = kHeadDim + 8;  // value row in shared memory (halves): ldmatrix rows on distinct banks
+constexpr int kOPad = kHeadDim + 8;  // a warp's weighted sums per head (floats): 64-bit stores on distinct banks
+constexpr int kChunkWarps = kChunk / 32;
+static_assert(kHeadDim == 64, "the chunk kernel's fragments assume 64-dim heads");
+static_assert(kChunkWarps * kMaxQPerKV * kOPad * 4 <= kChunk * kVPad * 2, "the sums reuse the value rows' space");
 
 // Partials per (sequence, query head, chunk): max score, sum of exp(s - max),
-// and the exp-weighted value sums [64], on the tensor cores (up to 16 query
-// heads per kv head as the MMA's 16 rows).  Scores: q (split into fp16 high
-// and low parts, about 22 significant bits together) against the fp16 keys
-// (exact), warp w taking tokens 32 w .. 32 w + 31, each thread reading 16
-// contiguous bytes of a key row per 32 dims and the matching slice of q (the
-// MMA sees both in the same permuted k order).  Weighted values: the
-// probabilities (split the same way) against the value rows staged in shared
-// memory (transposed by ldmatrix), warp w taking dims 8 w .. 8 w + 7.
-__global__ void __launch_bounds__(256) moe_attn_chunk_kernel(AttnDims d, const float *q, const int32_t *pos,
-                                                             const __half *kc, const __half *vc, float *pm, float *pl,
-                                                             float *pacc, int n_chunks) {
-    extern __shared__ __align__(16) unsigned char smem[];
+// and the exp-weighted value sums [64], on the tensor cores with the query
+// heads of the kv head as the MMA's 16 rows.  Warp w takes the chunk's tokens
+// 32 w .. 32 w + 31 by itself:
+//  * scores: q (fp32, split into fp16 high and low parts, about 22
+//    significant bits together) against the fp16 keys (exact), each thread
+//    reading 16 contiguous bytes of a key row per 32 dims and the matching
+//    slice of q (the MMA sees both in the same permuted k order);
+//  * the warp's own maximum per head and exp(s - max): the score fragments
+//    are, element for element, the A fragments of the weighted sum (rows the
+//    heads, k the tokens), so the probabilities (split the same way) never
+//    leave the registers;
+//  * weighted values: against the warp's 32 value rows, staged in shared
+//    memory by asynchronous copies and transposed by ldmatrix.
+// Then the eight warps' results are combined in warp order: the chunk's
+// maximum per head, each warp's sums rescaled by exp(its max - chunk max).
+__global__ void __launch_bounds__(256, 2) moe_attn_chunk_kernel(AttnDims d, const float *raw, const float2 *rope,
+                                                                const int32_t *pos, __half *kc, __half *vc, float *pm,
+                                                                float *pl, float *pacc, int n_chunks) {
+    __shared__ __align__(16) unsigned char smem[kChunk * kVPad * 2];
+    __shared__ float sml[kChunkWarps][kMaxQPerKV][2];  // per warp and head: max, sum
+    __half *sv = reinterpret_cast<__half *>(smem);     // [256][kVPad] value rows
+    float *so = reinterpret_cast<float *>(smem);       // [8][16][kOPad] rescaled sums (after the products)
     const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
     const int G = d.QH / d.KVH;
-    float *ss = reinterpret_cast<float *>(smem);                 // [16][256] scores, then probabilities
-    __half *sv = reinterpret_cast<__half *>(ss + 16 * kChunk);  // [256][kVPad] value rows
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // q, k, v and the RoPE table
+    asm volatile("griddepcontrol.launch_dependents;");
     const int p = pos[b];
     if (p < 0 || p >= d.max_ctx) return;
     int first, count;
@@ -229,124 +269,198 @@ __global__ void __launch_bounds__(256) moe_attn_chunk_kernel(AttnDims d, const f
     if (nt <= 0) return;
     const size_t row0 = ((size_t)b * d.max_ctx) * d.KVH * kHeadDim + (size_t)j * kHeadDim;
     const size_t rstride = (size_t)d.KVH * kHeadDim;
-    // value rows of the chunk into shared memory (rows past the chunk: zeros)
-    {
-        const int t = tid;  // one row per thread
-        uint4 *dst = reinterpret_cast<uint4 *>(sv + (size_t)t * kVPad);
-        if (t < nt) {
-            const __half *vr = vc + row0 + (size_t)(t0 + t) * rstride;
+    const int RW = (d.QH + 2 * d.KVH) * kHeadDim;
+    const float *rq = raw + (size_t)b * RW;
+    const float2 *rt = rope + (size_t)b * 32;
+    if (t0 + nt - 1 == p) {
+        // the chunk holding the new token appends its key (rotated: pair i is
+        // dims i and i + 32) and value to the cache, as fp16, before reading it
+        if (tid < 32) {
+            const float l = rq[(d.QH + j) * kHeadDim + tid], r = rq[(d.QH + j) * kHeadDim + tid + 32];
+            const float2 cs = rt[tid];
+            kc[row0 + (size_t)p * rstride + tid] = __float2half_rn(l * cs.x - r * cs.y);
+            kc[row0 + (size_t)p * rstride + tid + 32] = __float2half_rn(l * cs.y + r * cs.x);
+        } else if (tid < 32 + kHeadDim) {
+            const int e = tid - 32;
+            vc[row0 + (size_t)p * rstride + e] = __float2half_rn(rq[(d.QH + d.KVH + j) * kHeadDim + e]);
+        }
+        __syncthreads();
+    }
+    const int w0 = 32 * warp;  // the warp's first token in the chunk
+    float o[8][4];             // [dim tile][fragment]: rows g, g + 8; dims 8 nd + 2 t4, + 1
 #pragma unroll
-            for (int v = 0; v < kHeadDim / 8; v++) {
-                const uint32_t da = static_cast<uint32_t>(__cvta_generic_to_shared(dst + v));
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(da), "l"(vr + 8 * v) : "memory");
+    for (int nd = 0; nd < 8; nd++) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};  // heads g, g + 8
+    if (w0 < nt) {
+        {   // this lane's value row (zeros past the chunk's tokens)
+            const int t = w0 + lane;
+            uint4 *dst = reinterpret_cast<uint4 *>(sv + (size_t)t * kVPad);
+            if (t < nt) {
+                const __half *vr = vc + row0 + (size_t)(t0 + t) * rstride;
+#pragma unroll
+                for (int v = 0; v < kHeadDim / 8; v++) {
+                    const uint32_t da = static_cast<uint32_t>(__cvta_generic_to_shared(dst + v));
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(da), "l"(vr + 8 * v) : "memory");
+                }
+            } else {
+#pragma unroll
+                for (int v = 0; v < kHeadDim / 8; v++) dst[v] = make_uint4(0, 0, 0, 0);
             }
-        } else {
-#pragma unroll
-            for (int v = 0; v < kHeadDim / 8; v++) dst[v] = make_uint4(0, 0, 0, 0);
         }
-    }
-    // q slices of heads g and g + 8 (zero rows past G), split high / low
-    const float *qb = q + (size_t)b * d.QH * kHeadDim + (size_t)(j * G) * kHeadDim;
-    uint32_t qh[2][2][4], ql[2][2][4];  // [row g / g+8][32-dim block][pair]
+        uint4 kv[4][2];  // key rows w0 + 8 ni + g: dims 8 t4 .. + 7 and 32 + 8 t4 .. + 7
 #pragma unroll
-    for (int r = 0; r < 2; r++)
+        for (int ni = 0; ni < 4; ni++) {
+            const int tt = w0 + 8 * ni + g;
+            if (tt < nt) {
+                const uint4 *kr = reinterpret_cast<const uint4 *>(kc + row0 + (size_t)(t0 + tt) * rstride);
+                kv[ni][0] = kr[t4];
+                kv[ni][1] = kr[4 + t4];
+            } else {
+                kv[ni][0] = kv[ni][1] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        // q slices of heads g and g + 8 (zero rows past G): dims 8 t4 .. + 7
+        // and their RoPE partners 32 + 8 t4 .. + 7, rotated, split high / low
+        const float *qb = rq + (size_t)(j * G) * kHeadDim;
+        float2 cs[8];
 #pragma unroll
-        for (int db = 0; db < 2; db++) {
+        for (int e = 0; e < 8; e++) cs[e] = rt[8 * t4 + e];
+        uint32_t qh[2][2][4], ql[2][2][4];  // [row g / g+8][32-dim block][pair]
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
             const int h = g + 8 * r;
-            float v[8];
+            float lo[8], hi[8];
 #pragma unroll
-            for (int e = 0; e < 8; e++) v[e] = h < G ? qb[(size_t)h * kHeadDim + 32 * db + 8 * t4 + e] : 0.f;
+            for (int e = 0; e < 8; e++) lo[e] = hi[e] = 0.f;
+            if (h < G) {
+                const float4 *q0 = reinterpret_cast<const float4 *>(qb + (size_t)h * kHeadDim + 8 * t4);
+                const float4 *q1 = reinterpret_cast<const float4 *>(qb + (size_t)h * kHeadDim + 32 + 8 * t4);
+                const float4 a0 = q0[0], a1 = q0[1], b0 = q1[0], b1 = q1[1];
+                const float l[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float rr[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int e = 0; e < 4; e++) split_half2(v[2 * e], v[2 * e + 1], qh[r][db][e], ql[r][db][e]);
+                for (int e = 0; e < 8; e++) {
+                    lo[e] = l[e] * cs[e].x - rr[e] * cs[e].y;
+                    hi[e] = l[e] * cs[e].y + rr[e] * cs[e].x;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                split_half2(lo[2 * e], lo[2 * e + 1], qh[r][0][e], ql[r][0][e]);
+                split_half2(hi[2 * e], hi[2 * e + 1], qh[r][1][e], ql[r][1][e]);
+            }
         }
-    // scores of this warp's 32 tokens (4 column tiles of 8)
-    const float scale = rsqrtf((float)kHeadDim);
+        // scores: s[ni][0..1] head g, tokens w0 + 8 ni + 2 t4, + 1; s[ni][2..3] head g + 8
+        float sc[4][4];
 #pragma unroll
-    for (int ni = 0; ni < 4; ni++) {
-        const int tt = 32 * warp + 8 * ni + g;  // this thread's key row
-        uint4 kv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-        if (tt < nt) {
-            const uint4 *kr = reinterpret_cast<const uint4 *>(kc + row0 + (size_t)(t0 + tt) * rstride);
-            kv[0] = kr[t4];
-            kv[1] = kr[4 + t4];
-        }
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int ni = 0; ni < 4; ni++) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int db = 0; db < 2; db++) {
-            mma_f16(acc, qh[0][db][0], qh[1][db][0], qh[0][db][1], qh[1][db][1], kv[db].x, kv[db].y);
-            mma_f16(acc, qh[0][db][2], qh[1][db][2], qh[0][db][3], qh[1][db][3], kv[db].z, kv[db].w);
-            mma_f16(acc, ql[0][db][0], ql[1][db][0], ql[0][db][1], ql[1][db][1], kv[db].x, kv[db].y);
-            mma_f16(acc, ql[0][db][2], ql[1][db][2], ql[0][db][3], ql[1][db][3], kv[db].z, kv[db].w);
-        }
-        // acc[0..1]: head g, tokens 2 t4, 2 t4 + 1 of the tile; acc[2..3]: head g + 8
+            for (int db = 0; db < 2; db++) {
+                const uint4 k4 = kv[ni][db];
+                mma_f16(acc, qh[0][db][0], qh[1][db][0], qh[0][db][1], qh[1][db][1], k4.x, k4.y);
+                mma_f16(acc, qh[0][db][2], qh[1][db][2], qh[0][db][3], qh[1][db][3], k4.z, k4.w);
+                mma_f16(acc, ql[0][db][0], ql[1][db][0], ql[0][db][1], ql[1][db][1], k4.x, k4.y);
+                mma_f16(acc, ql[0][db][2], ql[1][db][2], ql[0][db][3], ql[1][db][3], k4.z, k4.w);
+            }
 #pragma unroll
-        for (int qd = 0; qd < 4; qd++) {
-            const int h = g + 8 * (qd >> 1), t = 32 * warp + 8 * ni + 2 * t4 + (qd & 1);
-            if (h < G) ss[h * kChunk + t] = t < nt ? acc[qd] * scale : -INFINITY;
+            for (int qd = 0; qd < 4; qd++) {
+                const int t = w0 + 8 * ni + 2 * t4 + (qd & 1);
+                sc[ni][qd] = t < nt ? acc[qd] * 0.125f : -INFINITY;  // 1 / sqrt(64)
+            }
         }
+        // the warp's maximum per head (the four lanes of a row hold its 32 tokens)
+#pragma unroll
+        for (int ni = 0; ni < 4; ni++) {
+            mrow[0] = fmaxf(mrow[0], fmaxf(sc[ni][0], sc[ni][1]));
+            mrow[1] = fmaxf(mrow[1], fmaxf(sc[ni][2], sc[ni][3]));
+        }
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            mrow[r] = fmaxf(mrow[r], __shfl_xor_sync(0xffffffffu, mrow[r], 1));
+            mrow[r] = fmaxf(mrow[r], __shfl_xor_sync(0xffffffffu, mrow[r], 2));
+        }
+        // exponentials into the A fragments of the products (k step ks: tokens
+        // w0 + 16 ks .. + 15 = score tiles 2 ks and 2 ks + 1)
+        uint32_t ph[2][4], plo[2][4];
+#pragma unroll
+        for (int ks = 0; ks < 2; ks++) {
+            float e[2][4];
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++)
+#pragma unroll
+                for (int qd = 0; qd < 4; qd++) {
+                    e[hh][qd] = __expf(sc[2 * ks + hh][qd] - mrow[qd >> 1]);
+                    lrow[qd >> 1] += e[hh][qd];
+                }
+            split_half2(e[0][0], e[0][1], ph[ks][0], plo[ks][0]);  // head g, tokens 2 t4, + 1
+            split_half2(e[0][2], e[0][3], ph[ks][1], plo[ks][1]);  // head g + 8
+            split_half2(e[1][0], e[1][1], ph[ks][2], plo[ks][2]);  // head g, tokens 8 + 2 t4, + 1
+            split_half2(e[1][2], e[1][3], ph[ks][3], plo[ks][3]);  // head g + 8
+        }
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
+            lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncwarp();
+        // weighted values: two dim tiles per ldmatrix (rows: the k step's 16
+        // tokens; lanes 16..31 address the second tile)
+#pragma unroll
+        for (int ks = 0; ks < 2; ks++)
+#pragma unroll
+            for (int nd = 0; nd < 8; nd += 2) {
+                const __half *rowp = sv + (size_t)(w0 + 16 * ks + (lane & 15)) * kVPad + 8 * nd + 8 * (lane >> 4);
+                const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(rowp));
+                uint32_t v0, v1, v2, v3;
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                             : "r"(addr));
+                mma_f16(o[nd], ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3], v0, v1);
+                mma_f16(o[nd + 1], ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3], v2, v3);
+                mma_f16(o[nd], plo[ks][0], plo[ks][1], plo[ks][2], plo[ks][3], v0, v1);
+                mma_f16(o[nd + 1], plo[ks][0], plo[ks][1], plo[ks][2], plo[ks][3], v2, v3);
+            }
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (t4 == 0) {
+        sml[warp][g][0] = mrow[0];
+        sml[warp][g][1] = lrow[0];
+        sml[warp][g + 8][0] = mrow[1];
+        sml[warp][g + 8][1] = lrow[1];
+    }
+    __syncthreads();  // every warp is done with the value rows; maxima and sums visible
+    // the chunk's maximum per head and this warp's sums rescaled to it
+#pragma unroll
+    for (int r = 0; r < 2; r++) {
+        const int h = g + 8 * r;
+        float M = -INFINITY;
+        for (int w = 0; w < kChunkWarps; w++) M = fmaxf(M, sml[w][h][0]);
+        const float f = mrow[r] == -INFINITY ? 0.f : __expf(mrow[r] - M);
+#pragma unroll
+        for (int nd = 0; nd < 8; nd++)
+            *reinterpret_cast<float2 *>(so + ((size_t)warp * kMaxQPerKV + h) * kOPad + 8 * nd + 2 * t4) =
+                make_float2(o[nd][2 * r] * f, o[nd][2 * r + 1] * f);
+    }
     __syncthreads();
-    // per head (a warp each): max, exponentials (0 past the chunk), their sum
-    for (int h = warp; h < G; h += 8) {
-        float m = -INFINITY;
-        for (int t = lane; t < nt; t += 32) m = fmaxf(m, ss[h * kChunk + t]);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float l = 0.f;
-        for (int t = lane; t < kChunk; t += 32) {
-            const float e = t < nt ? __expf(ss[h * kChunk + t] - m) : 0.f;
-            ss[h * kChunk + t] = e;
-            l += e;
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) {
-            const size_t idx = ((size_t)b * d.QH + j * G + h) * n_chunks + c;
-            pm[idx] = m;
-            pl[idx] = l;
-        }
-    }
-    __syncthreads();
-    // weighted values: this warp's 8 dims, the chunk's tokens 16 at a time
-    float o[4] = {0.f, 0.f, 0.f, 0.f};
-    const int ksteps = (nt + 15) / 16;
-    for (int ks = 0; ks < ksteps; ks++) {
-        const int kt = 16 * ks;
-        uint32_t ph[4], plo[4];
-        {
-            const float *r0 = ss + (size_t)g * kChunk + kt + 2 * t4;        // head g
-            const float *r1 = ss + (size_t)(g + 8) * kChunk + kt + 2 * t4;  // head g + 8
-            const bool h1 = g + 8 < G;
-            const bool h0 = g < G;
-            split_half2(h0 ? r0[0] : 0.f, h0 ? r0[1] : 0.f, ph[0], plo[0]);
-            split_half2(h1 ? r1[0] : 0.f, h1 ? r1[1] : 0.f, ph[1], plo[1]);
-            split_half2(h0 ? r0[8] : 0.f, h0 ? r0[9] : 0.f, ph[2], plo[2]);
-            split_half2(h1 ? r1[8] : 0.f, h1 ? r1[9] : 0.f, ph[3], plo[3]);
-        }
-        uint32_t b0, b1;
-        {
-            const __half *rowp = sv + (size_t)(kt + (lane & 15)) * kVPad + 8 * warp;
-            const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(rowp));
-            asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
-                         : "=r"(b0), "=r"(b1)
-                         : "r"(addr));
-        }
-        mma_f16(o, ph[0], ph[1], ph[2], ph[3], b0, b1);
-        mma_f16(o, plo[0], plo[1], plo[2], plo[3], b0, b1);
-    }
-    // o[0..1]: head g, dims 8 w + 2 t4, + 1; o[2..3]: head g + 8
-#pragma unroll
-    for (int qd = 0; qd < 4; qd++) {
-        const int h = g + 8 * (qd >> 1);
-        if (h >= G) continue;
+    for (int i = tid; i < G * kHeadDim; i += 256) {
+        const int h = i / kHeadDim, dd = i % kHeadDim;
+        float acc = 0.f;
+        for (int w = 0; w < kChunkWarps; w++) acc += so[((size_t)w * kMaxQPerKV + h) * kOPad + dd];
         const size_t idx = ((size_t)b * d.QH + j * G + h) * n_chunks + c;
-        pacc[idx * kHeadDim + 8 * warp + 2 * t4 + (qd & 1)] = o[qd];
+        pacc[idx * kHeadDim + dd] = acc;
     }
-}
-
-size_t chunk_smem_bytes(const AttnDims &) {
-    return (size_t)16 * kChunk * 4 + (size_t)kChunk * kVPad * 2;
+    if (tid < G) {
+        const int h = tid;
+        float M = -INFINITY;
+        for (int w = 0; w < kChunkWarps; w++) M = fmaxf(M, sml[w][h][0]);
+        float l = 0.f;
+        for (int w = 0; w < kChunkWarps; w++)
+            if (sml[w][h][0] != -INFINITY) l += __expf(sml[w][h][0] - M) * sml[w][h][1];
+        const size_t idx = ((size_t)b * d.QH + j * G + h) * n_chunks + c;
+        pm[idx] = M;
+        pl[idx] = l;
+    }
 }
 
 // o[b][h][:] = (sum over chunks of acc e^(m_c - m)) / (sum of l e^(m_c - m) +
@@ -354,6 +468,8 @@ size_t chunk_smem_bytes(const AttnDims &) {
 __global__ void moe_attn_merge_kernel(AttnDims d, const float *sinks, const int32_t *pos, const float *pm,
                                       const float *pl, const float *pacc, int n_chunks, uint16_t *o) {
     const int h = blockIdx.x, b = blockIdx.y, e = threadIdx.x;  // 64 threads
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunks' partials
+    asm volatile("griddepcontrol.launch_dependents;");
     const int p = pos[b];
     int first = 0, count = 0;
     if (p >= 0 && p < d.max_ctx) visible_range(d, p, first, count);
@@ -372,44 +488,6 @@ __global__ void moe_attn_merge_kernel(AttnDims d, const float *sinks, const int3
     o[((size_t)b * d.QH + h) * kHeadDim + e] = *reinterpret_cast<const uint16_t *>(&r);
 }
 
-// out[b][r] = x[b][r] + (Wo o[b])[r] + bo[r], 16 consecutive rows per CTA.
-template <int NT>
-__global__ void __launch_bounds__(kGemvThreads) moe_attn_out_kernel(AttnDims d, AttnWeights w, const uint16_t *o,
-                                                                    int B, const uint16_t *x, void *out, int out_bf16) {
-    __shared__ float red[(kGemvWarps - 1) * NT * 32][4];
-    const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-    const int K = d.QH * kHeadDim, H = d.H;
-    const int rlo = blockIdx.x * 16 + g, rhi = rlo + 8;
-    float acc[NT][4];
-    gemv_tile<NT>(w.wo + (size_t)rlo * K, w.wo + (size_t)rhi * K, o, B, K, red, acc);
-    if ((threadIdx.x >> 5) != 0) return;
-    const float blo = w.bo[rlo], bhi = w.bo[rhi];
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-        for (int c = 0; c < 2; c++) {
-            const int b = nt * 8 + 2 * t4 + c;
-            if (b >= B) continue;
-            const float lo = bf16_to_f32(x[(size_t)b * H + rlo]) + (acc[nt][c] + blo);
-            const float hi = bf16_to_f32(x[(size_t)b * H + rhi]) + (acc[nt][2 + c] + bhi);
-            if (out_bf16) {
-                const __nv_bfloat16 l = __float2bfloat16_rn(lo), h = __float2bfloat16_rn(hi);
-                static_cast<uint16_t *>(out)[(size_t)b * H + rlo] = *reinterpret_cast<const uint16_t *>(&l);
-                static_cast<uint16_t *>(out)[(size_t)b * H + rhi] = *reinterpret_cast<const uint16_t *>(&h);
-            } else {
-                static_cast<float *>(out)[(size_t)b * H + rlo] = lo;
-                static_cast<float *>(out)[(size_t)b * H + rhi] = hi;
-            }
-        }
-}
-
-template <template <int> class F, typename... A>
-cudaError_t by_nt(int B, A... args) {
-    if (B <= 8) return F<1>::run(args...);
-    if (B <= 16) return F<2>::run(args...);
-    if (B <= 24) return F<3>::run(args...);
-    return F<4>::run(args...);
-}
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -446,7 +524,8 @@ struct Carve {
     uint16_t *xhat;
     float *xnorm;
     int32_t *count;
-    float *q;
+    float *raw;       // q, k, v with biases (before RoPE), fp32 [seq][(QH + 2 KVH) 64]
+    float2 *rope;     // [seq][32] (cos, sin) x attention factor
     float *pm, *pl, *pacc;
     uint16_t *o;
 };
@@ -462,7 +541,8 @@ size_t attn_carve(const AttnDims &d, unsigned char *base, Carve *c) {
     t.xhat = reinterpret_cast<uint16_t *>(take(S * d.H * 2));
     t.xnorm = reinterpret_cast<float *>(take(S * 4));
     t.count = reinterpret_cast<int32_t *>(take(4));
-    t.q = reinterpret_cast<float *>(take(S * QD * 4));
+    t.raw = reinterpret_cast<float *>(take(S * (QD + 2 * (size_t)d.KVH * kHeadDim) * 4));
+    t.rope = reinterpret_cast<float2 *>(take(S * 32 * 8));
     t.pm = reinterpret_cast<float *>(take(S * d.QH * nch * 4));
     t.pl = reinterpret_cast<float *>(take(S * d.QH * nch * 4));
     t.pacc = reinterpret_cast<float *>(take(S * d.QH * nch * kHeadDim * 4));
@@ -470,24 +550,6 @@ size_t attn_carve(const AttnDims &d, unsigned char *base, Carve *c) {
     if (c) *c = t;
     return off;
 }
-
-template <int NT>
-struct QkvRun {
-    static cudaError_t run(const AttnDims &d, const AttnWeights &w, const uint16_t *xh, int B, const int32_t *pos,
-                           float *q, __half *kc, __half *vc, cudaStream_t st) {
-        const int tiles = d.QH * 4 + 2 * d.KVH * 4;
-        moe_attn_qkv_kernel<NT><<<tiles, kGemvThreads, 0, st>>>(d, w, xh, B, pos, q, kc, vc);
-        return cudaGetLastError();
-    }
-};
-template <int NT>
-struct OutRun {
-    static cudaError_t run(const AttnDims &d, const AttnWeights &w, const uint16_t *o, int B, const uint16_t *x,
-                           void *out, int out_bf16, cudaStream_t st) {
-        moe_attn_out_kernel<NT><<<d.H / 16, kGemvThreads, 0, st>>>(d, w, o, B, x, out, out_bf16);
-        return cudaGetLastError();
-    }
-};
 
 }  // namespace
 
@@ -515,6 +577,7 @@ moe_attn *moe_attn_create(int hidden, int q_heads, int kv_heads, int head_dim, i
 }
 
 void moe_attn_destroy(moe_attn *p) { delete p; }
+
 
 int moe_attn_set_i(moe_attn *p, const char *key, long long v) {
     if (!p || !key) return moe_fail_status(MOE_EINVAL, "NULL argument");
@@ -550,6 +613,8 @@ int moe_attn_set_workspace(moe_attn *p, void *dev, size_t bytes) {
     if (((uintptr_t)dev & 255u) != 0) return moe_fail_status(MOE_EINVAL, "the workspace must be 256-byte aligned");
     if (bytes < attn_carve(p->d, nullptr, nullptr))
         return moe_fail_status(MOE_ENOMEM, "workspace of %zu bytes, %zu needed", bytes, attn_carve(p->d, nullptr, nullptr));
+    Carve c;
+    attn_carve(p->d, static_cast<unsigned char *>(dev), &c);
     p->ws = static_cast<unsigned char *>(dev);
     p->ws_bytes = bytes;
     return MOE_OK;
@@ -593,27 +658,42 @@ int moe_attn_decode(moe_attn *p, const uint16_t *x, int n_seqs, const int32_t *p
     attn_carve(p->d, p->ws, &c);
     const int nch = (p->d.max_ctx + kChunk - 1) / kChunk;
     cudaError_t e = launch_rms_norm_rows(x, p->w.gamma, n_seqs, p->d.H, p->d.eps, c.xhat, c.xnorm, c.count, st);
-    if (e == cudaSuccess) e = by_nt<QkvRun>(n_seqs, p->d, p->w, (const uint16_t *)c.xhat, n_seqs, positions, c.q, p->kc, p->vc, st);
+    const int RW = (p->d.QH + 2 * p->d.KVH) * kHeadDim, QD = p->d.QH * kHeadDim;
+    ProjArgs a{};
+    a.d = p->d;
+    a.B = n_seqs;
     if (e == cudaSuccess) {
-        const size_t sm = chunk_smem_bytes(p->d);
-        static bool opted = false;
-        if (!opted) {
-            e = cudaFuncSetAttribute(moe_attn_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-            opted = e == cudaSuccess;
-        }
-        if (e == cudaSuccess) {
-            moe_attn_chunk_kernel<<<dim3(nch, p->d.KVH, n_seqs), 256, sm, st>>>(p->d, c.q, positions, p->kc, p->vc,
-                                                                                c.pm, c.pl, c.pacc, nch);
-            e = cudaGetLastError();
-        }
-    }
-    if (e == cudaSuccess) {
-        moe_attn_merge_kernel<<<dim3(p->d.QH, n_seqs), kHeadDim, 0, st>>>(p->d, p->w.sinks, positions, c.pm, c.pl,
-                                                                          c.pacc, nch, c.o);
-        e = cudaGetLastError();
+        a.rows = RW;
+        a.K = p->d.H;
+        a.w[0] = p->w.wq, a.w[1] = p->w.wk, a.w[2] = p->w.wv;
+        a.bias[0] = p->w.bq, a.bias[1] = p->w.bk, a.bias[2] = p->w.bv;
+        a.r1 = QD;
+        a.r2 = QD + p->d.KVH * kHeadDim;
+        a.x = c.xhat;
+        a.raw = c.raw;
+        a.rope = c.rope;
+        a.pos = positions;
+        e = proj_launch<0>(a, st);
     }
     if (e == cudaSuccess)
-        e = by_nt<OutRun>(n_seqs, p->d, p->w, (const uint16_t *)c.o, n_seqs, x, out, p->out_bf16 ? 1 : 0, st);
+        e = launch_pdl(moe_attn_chunk_kernel, dim3(nch, p->d.KVH, n_seqs), dim3(256), 0, st, p->d, (const float *)c.raw,
+                       (const float2 *)c.rope, positions, p->kc, p->vc, c.pm, c.pl, c.pacc, nch);
+    if (e == cudaSuccess)
+        e = launch_pdl(moe_attn_merge_kernel, dim3(p->d.QH, n_seqs), dim3(kHeadDim), 0, st, p->d,
+                       (const float *)p->w.sinks, positions, (const float *)c.pm, (const float *)c.pl,
+                       (const float *)c.pacc, nch, c.o);
+    if (e == cudaSuccess) {
+        a.rows = p->d.H;
+        a.K = QD;
+        a.w[0] = a.w[1] = a.w[2] = p->w.wo;
+        a.bias[0] = a.bias[1] = a.bias[2] = p->w.bo;
+        a.r1 = a.r2 = p->d.H;
+        a.x = c.o;
+        a.res = x;
+        a.out = out;
+        a.out_bf16 = p->out_bf16 ? 1 : 0;
+        e = proj_launch<1>(a, st);
+    }
     return e == cudaSuccess ? MOE_OK : moe_fail_status(MOE_ECUDA, "moe_attn_decode: %s", cudaGetErrorString(e));
 }
 

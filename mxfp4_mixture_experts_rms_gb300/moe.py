@@ -398,6 +398,9 @@ class AttnPlan:
         _check(self.L.moe_attn_decode(self.h, C.c_void_p(_ptr(x)), int(x.shape[0]), C.c_void_p(_ptr(positions)),
                                       C.c_void_p(_ptr(out)), _stream_ptr(stream)))
 
+    def set_i(self, key: str, value: int):
+        _check(self.L.moe_attn_set_i(self.h, key.encode(), int(value)))
+
     def close(self):
         if getattr(self, "h", None):
             self.L.moe_attn_destroy(self.h)

@@ -122,3 +122,30 @@ def test_position_outside_the_cache_is_skipped():
     assert not kc[0].any()                      # sequence 0 untouched
     assert kc[1, 4].any() and not kc[1, :4].any() and not kc[1, 5:].any()
     plan.close()
+
+
+def test_repeated_steps_are_bitwise_identical():
+    """The same step three times on one plan (the cache row it appends is
+    rewritten with the same values): identical outputs, so the projections'
+    cross-CTA partial sums are added in a fixed order and their tickets come
+    back to zero after every launch.  Shapes whose tiles are shared by two,
+    three and four CTAs."""
+    import torch
+    for H, QH, KVH, B in [(2880, 64, 8, 16), (512, 16, 4, 5), (256, 8, 2, 32)]:
+        w = synth.make_attention(21, H, QH, KVH)
+        kh, vh = synth.make_kv_history(21, B, 300, KVH)
+        plan = moe.AttnPlan(H, QH, KVH, B, 300, sliding_window=0)
+        plan.load_weights({k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda()
+                           for k, v in w.items()})
+        plan.k_cache.copy_(torch.from_numpy(kh))
+        plan.v_cache.copy_(torch.from_numpy(vh))
+        x = torch.from_numpy(synth.f32_to_bf16_bits(np.random.default_rng(2).normal(0, 1, (B, H))).view(np.int16)).cuda()
+        pos = torch.tensor([(37 * i) % 300 for i in range(B)], dtype=torch.int32, device="cuda")
+        outs = []
+        for _ in range(3):
+            out = torch.empty((B, H), dtype=torch.float32, device="cuda")
+            plan.decode(x, pos, out)
+            outs.append(out.cpu().numpy())
+        assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+        plan.close()
+
