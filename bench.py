@@ -586,6 +586,82 @@ def attention_bench(args, seqs: int = 16, ctx: int = 4096):
             "clocks": clk, "gpu_launches": 2 * 5 * reps}
 
 
+def decoder_bench(args, w, ctx: int = 4096):
+    """The whole gpt-oss decoder stack's decode step: per layer the attention
+    half (moe_attn_decode: sliding window of 128 on even layers, full
+    attention on odd ones; the workload's tokens as that many sequences, each
+    with ctx - 1 cached tokens) writing bf16 into the MoE block of the same
+    layer (the stack workload's plans), whose bf16 output is the next layer's
+    input.  Timed in one CUDA graph of K steps; HBM roofline of the step's
+    algorithmic bytes (the MoE stack's, plus every layer's attention weights
+    and visible keys and values)."""
+    import torch
+    from mxfp4_mixture_experts_rms_gb300 import moe, synth
+    A = synth.ATTN_GPT_OSS
+    H, QH, KVH, D, window = A["hidden"], A["q_heads"], A["kv_heads"], A["head_dim"], A["window"]
+    T, d = w.T, w.sets[0]
+    chain = d["chain"]
+    L = len(chain)
+    att = []
+    for i in range(L):
+        p = moe.AttnPlan(H, QH, KVH, T, ctx, sliding_window=window if i % 2 == 0 else 0, out_bf16=True)
+        p.load_weights(synth.attention_device(7000 + i, H, QH, KVH, D))
+        synth.kv_history_device(9000 + i, p.k_cache, p.v_cache)
+        att.append(p)
+    hs = [chain[0]["x"].clone()] + [torch.empty((T, H), dtype=torch.int16, device="cuda") for _ in range(L - 1)]
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    pos = torch.full((T,), ctx - 1, dtype=torch.int32, device="cuda")
+
+    def step(st):
+        for i in range(L):
+            att[i].decode(hs[i], pos, chain[i]["x"], stream=st)
+            chain[i]["plan"].forward(chain[i]["x"], out if i + 1 == L else hs[i + 1], chain[i]["ids"], stream=st)
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        step(st)
+    torch.cuda.synchronize()
+    reps = max(1, min(args.steps, 50))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            step(torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / reps
+    # algorithmic bytes: the MoE stack's (from its own measurement) and, per
+    # layer, the attention weights once and the visible keys and values
+    aw = (QH * D + 2 * KVH * D) * H * 2 + H * QH * D * 2 + 4 * (QH * D + 2 * KVH * D + 2 * H + QH)
+    kv = sum(T * (min(ctx, window) if i % 2 == 0 else ctx) * KVH * D * 2 * 2 for i in range(L))
+    hbm, _, kind = peaks()
+    moe_bytes = 0
+    for ly in chain:  # the MoE blocks' bytes from this run's own routing (the last step's counts)
+        c = torch.empty(w.shape.n_experts, dtype=torch.int32, device="cuda")
+        ly["plan"].expert_counts(c)
+        torch.cuda.synchronize()
+        gu, dn, _ = algorithmic_bytes(w.shape, c.cpu().numpy(), T)
+        moe_bytes += gu + dn
+    total = moe_bytes + L * aw + kv
+    for p in att:
+        p.close()
+    del g
+    return {"value": T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "path": "attention decode + MoE GEMV",
+            "config": {"workload": f"{L}-layer gpt-oss decoder stack decode (attention + MoE), {T} sequences x "
+                                   f"{ctx - 1} cached tokens", "layers": L, "sequences": T, "context": ctx,
+                       "attention": "sliding window 128 on even layers, full on odd; bf16 weights (synthetic); "
+                                    "fp16 caches", "moe": "the 24-layer stack workload's blocks"},
+            "algorithmic_bytes_per_step": total,
+            "roofline": {"bound": "hbm", "achieved": total / (ms / 1e3) / 1e9, "peak": hbm, "peak_kind": kind,
+                         "unit": "GB/s", "frac": total / (ms / 1e3) / 1e9 / hbm, "traffic": None},
+            "clocks": clk, "gpu_launches": reps * L * 9}
+
+
 def locality_stats(w, steps: int = 16):
     """Expert-locality statistics of the stack's routing (the library's
     profiler attached to every layer; untimed, outside the measured steps):
@@ -686,6 +762,7 @@ def run_ours(args, rank, world, local, wid, T):
     head = summarise(w, r, args, world)
     e2e = e2e_rate(w, args, world)
     loc = locality_stats(w) if w.layers > 1 else None
+    dec = decoder_bench(args, w) if w.layers > 1 and not args.no_extras else None
     extras = {}
     if not args.no_extras:
         for (ew, eT, eo) in EXTRAS:
@@ -703,6 +780,8 @@ def run_ours(args, rank, world, local, wid, T):
             torch.cuda.synchronize()
         att = attention_bench(args)
         extras[att["config"]["workload"]] = att
+        if dec:
+            extras[dec["config"]["workload"]] = dec
     if rank != 0:
         return
     cpu = None if args.no_cpu_baseline else cpu_baseline(wid, T, w)

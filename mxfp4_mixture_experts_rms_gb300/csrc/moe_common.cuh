@@ -186,14 +186,29 @@ __device__ __forceinline__ int mma_perm_pos(int j) {
     return b + (q << 3) + (i << 1) + hh;
 }
 
+// Host-side setup done once per device (kernel attributes and device
+// properties belong to a device, not to the process): the current device's
+// slot in a PerDevice table.
+constexpr int kMaxDevices = 64;
+template <class T>
+struct PerDevice {
+    T v[kMaxDevices]{};
+};
+inline cudaError_t current_device_slot(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e == cudaSuccess && (*dev < 0 || *dev >= kMaxDevices)) e = cudaErrorInvalidDevice;
+    return e;
+}
+
 // Raise a kernel's dynamic shared memory limit to the device maximum, once per
-// process (host-side setup; kept out of the per-forward launch sequence).
+// device (host-side setup; kept out of the per-forward launch sequence).
 template <class F>
-inline cudaError_t smem_optin_once(F *kernel, bool &done) {
-    if (done) return cudaSuccess;
+inline cudaError_t smem_optin_once(F *kernel, PerDevice<bool> &flag) {
     int dev = 0, optin = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaError_t e = current_device_slot(&dev);
+    if (e != cudaSuccess || flag.v[dev]) return e;
+    bool &done = flag.v[dev];
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     cudaFuncAttributes fa;
     if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
     if (e == cudaSuccess)

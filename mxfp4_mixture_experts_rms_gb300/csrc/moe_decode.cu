@@ -609,13 +609,15 @@ struct KernelInfo {
 
 template <bool GATEUP, int NT, bool BF, int MP, int NM>
 static cudaError_t launch_one(DecodeArgs a, int n_items_max, cudaStream_t st) {
-    static KernelInfo ki;
+    static PerDevice<KernelInfo> kis;
+    static PerDevice<bool> opt;
     auto kern = moe_decode_kernel<GATEUP, NT, BF, MP, NM>;
+    int dev = 0;
+    MOE_CUDA_TRY(current_device_slot(&dev));
+    KernelInfo &ki = kis.v[dev];
     if (!ki.done) {
-        bool opt = false;
         MOE_CUDA_TRY(smem_optin_once(kern, opt));
-        int dev = 0, optin = 0;
-        MOE_CUDA_TRY(cudaGetDevice(&dev));
+        int optin = 0;
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&ki.n_sm, cudaDevAttrMultiProcessorCount, dev));
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
         cudaFuncAttributes fa;

@@ -662,14 +662,13 @@ cudaError_t mxf4_prepare(const BlockParams &bp, const MatPtrs &gate, const MatPt
 cudaError_t launch_mxf4_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &gate, const MatPtrs &up,
                               const MatPtrs &down, const Mxf4Weights &w, int T, bool gateup, cudaStream_t st) {
     MOE_CUDA_TRY(q_get_encoder());
-    static int n_sm = 0;
-    if (!n_sm) {
-        int dev = 0;
-        MOE_CUDA_TRY(cudaGetDevice(&dev));
-        MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
-    }
-    static bool done_g = false, done_d = false;
-    bool &done = gateup ? done_g : done_d;
+    static PerDevice<int> sms;
+    static PerDevice<bool> done_g, done_d;
+    int dev = 0;
+    MOE_CUDA_TRY(current_device_slot(&dev));
+    int &n_sm = sms.v[dev];
+    if (!n_sm) MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+    bool &done = (gateup ? done_g : done_d).v[dev];
     if (!done) {
         MOE_CUDA_TRY(cudaFuncSetAttribute(gateup ? moe_mxf4_kernel<true> : moe_mxf4_kernel<false>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)q_smem_bytes()));

@@ -816,7 +816,7 @@ cudaError_t launch_gather(const BlockParams &bp, const Workspace &ws, int T, boo
 template <bool GATEUP, bool F16>
 cudaError_t launch_pf(const PrefillArgs &args, const TmaMaps &maps, const AMaps &amaps, dim3 grid,
                       cudaStream_t st) {
-    static bool done = false;
+    static PerDevice<bool> done;
     MOE_CUDA_TRY(smem_optin_once(moe_prefill_kernel<GATEUP, F16>, done));
     moe_prefill_kernel<GATEUP, F16><<<grid, kThreads, prefill_smem_bytes(), st>>>(args, maps, amaps);
     return cudaGetLastError();
@@ -834,12 +834,11 @@ cudaError_t launch_prefill_stage(const BlockParams &bp, const Workspace &ws, con
     if (tiles > ws.max_tiles) tiles = ws.max_tiles;
     const int mtiles = gateup ? (bp.F + kWN / 2 - 1) / (kWN / 2) : (bp.H + kWN - 1) / kWN;
     // persistent: one CTA per SM, or fewer when there are fewer work items
-    static int n_sm = 0;
-    if (!n_sm) {
-        int dev = 0;
-        MOE_CUDA_TRY(cudaGetDevice(&dev));
-        MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
-    }
+    static PerDevice<int> sms;
+    int dev = 0;
+    MOE_CUDA_TRY(current_device_slot(&dev));
+    int &n_sm = sms.v[dev];
+    if (!n_sm) MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
     const long items = (long)tiles * mtiles;
     const dim3 grid((unsigned)(items < n_sm ? items : n_sm));
     if (gateup)

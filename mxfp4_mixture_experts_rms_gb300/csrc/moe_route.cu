@@ -1245,12 +1245,14 @@ SmallGeo small_geo(int H, int E, int cmax) {
 
 template <bool STAGED>
 cudaError_t launch_small(const RouteArgs &a, const SmallGeo &g, cudaStream_t st) {
-    static bool done = false, nonportable = false;
+    static PerDevice<bool> done, nonportable;
     MOE_CUDA_TRY(smem_optin_once(moe_route_small_kernel<STAGED>, done));
-    if (g.C > 8 && !nonportable) {
+    int dev = 0;
+    MOE_CUDA_TRY(current_device_slot(&dev));
+    if (g.C > 8 && !nonportable.v[dev]) {
         MOE_CUDA_TRY(cudaFuncSetAttribute(moe_route_small_kernel<STAGED>,
                                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-        nonportable = true;
+        nonportable.v[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.T, g.C);
@@ -1303,9 +1305,12 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
         // many experts: 16-CTA clusters (a non-portable size) keep every CTA's
         // router rows in shared memory; where such a cluster cannot be
         // launched, 8-CTA clusters read the rows from global memory
-        static int use16 = -1;
+        static PerDevice<int> use16s;  // 0: not tried, 1: launches, 2: cannot launch here
+        int dev = 0;
+        MOE_CUDA_TRY(current_device_slot(&dev));
+        int &use16 = use16s.v[dev];
         SmallGeo g = small_geo(bp.H, bp.E, 8);
-        if (!g.staged && use16 != 0) {
+        if (!g.staged && use16 != 2) {
             const SmallGeo g16 = small_geo(bp.H, bp.E, 16);
             if (g16.staged) {
                 a.epc = g16.epc;
@@ -1315,16 +1320,16 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
                     return cudaSuccess;
                 }
                 cudaGetLastError();  // a launch-configuration error is not sticky
-                use16 = 0;
+                use16 = 2;
             }
         }
         a.epc = g.epc;
         MOE_CUDA_TRY(launch_small_geo(a, g, st));
         return cudaGetLastError();
     }
-    static bool donet = false;
+    static PerDevice<bool> donet;
     int n_sm = 0, dev = 0;
-    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    MOE_CUDA_TRY(current_device_slot(&dev));
     MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
     // norm, a CTA per token (+ the router rows' norms, a warp per row)
     moe_route_norm_kernel<<<T + (bp.E + kNormThreads / 32 - 1) / (kNormThreads / 32), kNormThreads, 0, st>>>(a);
@@ -1332,7 +1337,8 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
     // logits: K split so that the CTAs' waves times their chunks is least (the
     // partials live in y, which is free until the down projection; fewer
     // splits on a tie, since each split adds a rounding to the bound)
-    static int gemm_per_sm = 0;
+    static PerDevice<int> gemm_per_sms;
+    int &gemm_per_sm = gemm_per_sms.v[dev];
     if (!gemm_per_sm) {
         MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&gemm_per_sm, moe_router_gemm_kernel, kGThreads, 0));
         if (gemm_per_sm < 1) gemm_per_sm = 1;

@@ -226,6 +226,36 @@ def make_kv_history(seed: int, seqs: int, ctx: int, kv_heads: int = 8, head_dim:
     return k, v
 
 
+def attention_device(seed: int, hidden: int = 2880, q_heads: int = 64, kv_heads: int = 8, head_dim: int = 64,
+                     device="cuda") -> dict:
+    """The ``make_attention`` recipe drawn on the device with torch's generator
+    (another random stream: only the distributions are shared), bf16 bits as
+    int16.  For benchmark stacks; nothing compared with the oracle uses it."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    QD, KD = q_heads * head_dim, kv_heads * head_dim
+
+    def n(shape, s):
+        return torch.randn(shape, dtype=torch.float32, device=device, generator=g) * s
+
+    def bf(shape):
+        return n(shape, 0.02).to(torch.bfloat16).view(torch.int16)
+    return dict(gamma=1.0 + n(hidden, 0.1), wq=bf((QD, hidden)), wk=bf((KD, hidden)), wv=bf((KD, hidden)),
+                wo=bf((hidden, QD)), bq=n(QD, 0.02), bk=n(KD, 0.02), bv=n(KD, 0.02), bo=n(hidden, 0.02),
+                sinks=n(q_heads, 1.0))
+
+
+def kv_history_device(seed: int, k_cache, v_cache) -> None:
+    """Fill a plan's key and value caches with N(0, 1) rounded to fp16 on the
+    device (the ``make_kv_history`` distributions, torch's generator)."""
+    import torch
+    g = torch.Generator(device=k_cache.device)
+    g.manual_seed(int(seed))
+    for c in (k_cache, v_cache):
+        c.copy_(torch.randn(c.shape, dtype=torch.float32, device=c.device, generator=g).to(torch.float16))
+
+
 def make_tokens(config: int, tokens: int, hidden: int, layer: int = 0, sub: int = 0) -> np.ndarray:
     """Input activations x ~ N(0,1) as bf16 bits ``[tokens][hidden]``."""
     return f32_to_bf16_bits(_rng(config, layer, _T_X, sub).normal(0.0, 1.0, size=(tokens, hidden)))
