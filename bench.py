@@ -67,10 +67,10 @@ def parse():
     ap.add_argument("--quick", action="store_true",
                     help="timed region of the headline only (no clock pre-roll, kernel timing, e2e, CPU "
                          "baseline or extras); for ncu")
-    ap.add_argument("--op", default="block", choices=["block", "mx_fp4_quantize", "attention"],
+    ap.add_argument("--op", default="block", choices=["block", "mx_fp4_quantize", "attention", "attention_prefill"],
                     help="block: the MoE block (the benchmark); mx_fp4_quantize: the FP4 activation "
                          "encoder alone, on --rows x --cols bf16 activations; attention: the gpt-oss "
-                         "attention decode step alone")
+                         "attention decode step alone; attention_prefill: its prefill of one 512-token prompt")
     ap.add_argument("--rows", type=int, default=14336, help="mx_fp4_quantize: rows (2048 tokens x 7 routes)")
     ap.add_argument("--cols", type=int, default=2048, help="mx_fp4_quantize: columns (expert_hidden)")
     return ap.parse_args()
@@ -586,6 +586,67 @@ def attention_bench(args, seqs: int = 16, ctx: int = 4096):
             "clocks": clk, "gpu_launches": 2 * 5 * reps}
 
 
+def attention_prefill_bench(args, n: int = 512, ctx: int = 4096):
+    """Prefill of the attention half (moe_attn_prefill): an n-token prompt into
+    the empty cache of one sequence, one sliding-window (128) layer and one
+    full-attention layer (blocks of 32 rows, each appended, then attended).
+    Timed in a CUDA graph; HBM roofline of the algorithmic bytes (both layers'
+    projection weights once, the keys and values each row sees, activations)."""
+    import numpy as np
+    import torch
+    from mxfp4_mixture_experts_rms_gb300 import moe, synth
+    A = synth.ATTN_GPT_OSS
+    H, QH, KVH, D, window = A["hidden"], A["q_heads"], A["kv_heads"], A["head_dim"], A["window"]
+    plans = []
+    for layer, win in enumerate((window, 0)):
+        p = moe.AttnPlan(H, QH, KVH, 32, ctx, sliding_window=win)
+        p.load_weights(synth.attention_device(300 + layer, H, QH, KVH, D))
+        plans.append(p)
+    x = torch.from_numpy(synth.f32_to_bf16_bits(np.random.default_rng(1).normal(0, 1, (n, H))).view(np.int16)).cuda()
+    out = torch.empty((n, H), dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        for p in plans:
+            p.prefill(x, 0, 0, out, stream=st)
+    torch.cuda.synchronize()
+    reps = max(1, min(args.steps, 20))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            for p in plans:
+                p.prefill(x, 0, 0, out, stream=torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / reps
+    weights = 2 * ((QH * D + 2 * KVH * D) * H * 2 + H * QH * D * 2)
+    seen = sum(min(r + 1, window) for r in range(n)) + sum(r + 1 for r in range(n))
+    kv = seen * KVH * D * 2 * 2
+    act = 2 * n * (H * 2 + H * 4 + 2 * KVH * D * 2)
+    hbm, _, kind = peaks()
+    total = weights + kv + act
+    for p in plans:
+        p.close()
+    del g
+    return {"value": n / (ms / 1e3), "unit": "tokens/s (one sliding + one full attention layer)", "ms_per_step": ms,
+            "path": "attention prefill (blocks of 32 rows)",
+            "config": {"workload": f"gpt-oss attention prefill, one {n}-token prompt into an empty cache, one "
+                                   "sliding-window (128) and one full layer", "hidden": H, "q_heads": QH,
+                       "kv_heads": KVH, "head_dim": D, "rows_per_block": 32, "weights": "bf16 (synthetic)",
+                       "kv_cache": "fp16"},
+            "algorithmic_bytes_per_step": total,
+            "roofline": {"bound": "hbm", "achieved": total / (ms / 1e3) / 1e9, "peak": hbm, "peak_kind": kind,
+                         "unit": "GB/s", "frac": total / (ms / 1e3) / 1e9 / hbm, "traffic": None},
+            "note": "each 32-row block reads the projection weights again (16 blocks: 16 x their bytes)",
+            "clocks": clk, "gpu_launches": reps * 2 * ((n + 31) // 32) * 6}
+
+
 def decoder_bench(args, w, ctx: int = 4096):
     """The whole gpt-oss decoder stack's decode step: per layer the attention
     half (moe_attn_decode: sliding window of 128 on even layers, full
@@ -780,6 +841,8 @@ def run_ours(args, rank, world, local, wid, T):
             torch.cuda.synchronize()
         att = attention_bench(args)
         extras[att["config"]["workload"]] = att
+        apf = attention_prefill_bench(args)
+        extras[apf["config"]["workload"]] = apf
         if dec:
             extras[dec["config"]["workload"]] = dec
     if rank != 0:
@@ -868,15 +931,16 @@ def main():
             return
         run_mx_fp4_quantize(args)
         return
-    if args.op == "attention":
+    if args.op in ("attention", "attention_prefill"):
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "op": "attention",
+            print(json.dumps({"impl": "reference", "op": args.op,
                               "unavailable": "the attention step is timed on the GPU only"}))
             return
         import torch
         from mxfp4_mixture_experts_rms_gb300 import moe
         moe.load()
-        print(json.dumps(attention_bench(args)), flush=True)
+        fn = attention_bench if args.op == "attention" else attention_prefill_bench
+        print(json.dumps(fn(args)), flush=True)
         return
     from mxfp4_mixture_experts_rms_gb300 import synth
     wid = args.workload

@@ -415,6 +415,17 @@ int moe_attn_load_weights(moe_attn *plan, const moe_attn_weights *w);
  * Writes the new tokens' keys and values into the caches.  Enqueue only. */
 int moe_attn_decode(moe_attn *plan, const uint16_t *x, int n_seqs, const int32_t *positions, void *out,
                     void *stream);
+/* Prefill (goosedump gpt_oss.rs `prefill_attention_layer` / `causal_gqa_batch`):
+ * n_tokens consecutive new tokens of cache sequence seq (0..max_seqs-1) at
+ * positions pos0 .. pos0 + n_tokens - 1 (pos0 = the tokens its cache already
+ * holds; the last position at most max_ctx - 1).  Token r sees the cached
+ * tokens and the new tokens up to itself (the last sliding_window of them on
+ * sliding layers), as a decode step at position pos0 + r would.  Processed in
+ * blocks of max_seqs rows, each block's keys and values appended before its
+ * attention.  x bf16 [n_tokens][H], out [n_tokens][H] (16-byte aligned, not
+ * overlapping); writes cache rows pos0 .. pos0 + n_tokens - 1 of sequence
+ * seq and no others.  Enqueue only. */
+int moe_attn_prefill(moe_attn *plan, const uint16_t *x, int n_tokens, int seq, int pos0, void *out, void *stream);
 void moe_attn_destroy(moe_attn *plan);
 
 /* Text of the last failure on this thread ("" if none) (goosedump gpt_oss.rs:

@@ -57,6 +57,16 @@ struct AttnWeights {
     const float *bq, *bk, *bv, *bo, *sinks;
 };
 
+// Row b of a step: decode, one new token per cache sequence (sequence b, its
+// position pos[b]); prefill, consecutive new tokens of one sequence (sequence
+// seq, position pos0 + b).
+struct RowMap {
+    const int32_t *pos;  // decode: [rows] on the device; prefill: null
+    int pos0, seq;       // prefill: first position, cache sequence (seq < 0: decode)
+};
+__device__ __forceinline__ int row_pos(const RowMap &m, int b) { return m.pos ? m.pos[b] : m.pos0 + b; }
+__device__ __forceinline__ int row_seq(const RowMap &m, int b) { return m.seq >= 0 ? m.seq : b; }
+
 __device__ __forceinline__ void mma_bf16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
     asm volatile(
@@ -87,7 +97,7 @@ struct ProjArgs {
     // x attention factor [B][32]
     float *raw;
     float2 *rope;
-    const int32_t *pos;
+    RowMap rows_of;
     // output: out = res + Wo o + bo
     const uint16_t *res;
     void *out;
@@ -182,7 +192,7 @@ __global__ void __launch_bounds__(256) moe_attn_proj_kernel(const __grid_constan
         }
     if (KIND == 0)
         for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-            const double ang = (double)a.pos[b] * a.d.freq[lane];
+            const double ang = (double)row_pos(a.rows_of, b) * a.d.freq[lane];
             const float r = (float)fma(-rint(ang * kInvTwoPi), kTwoPi, ang);
             float sn, cs;
             sincosf(r, &sn, &cs);
@@ -249,7 +259,7 @@ static_assert(kChunkWarps * kMaxQPerKV * kOPad * 4 <= kChunk * kVPad * 2, "the s
 // Then the eight warps' results are combined in warp order: the chunk's
 // maximum per head, each warp's sums rescaled by exp(its max - chunk max).
 __global__ void __launch_bounds__(256, 2) moe_attn_chunk_kernel(AttnDims d, const float *raw, const float2 *rope,
-                                                                const int32_t *pos, __half *kc, __half *vc, float *pm,
+                                                                RowMap rm, __half *kc, __half *vc, float *pm,
                                                                 float *pl, float *pacc, int n_chunks) {
     __shared__ __align__(16) unsigned char smem[kChunk * kVPad * 2];
     __shared__ float sml[kChunkWarps][kMaxQPerKV][2];  // per warp and head: max, sum
@@ -258,23 +268,24 @@ __global__ void __launch_bounds__(256, 2) moe_attn_chunk_kernel(AttnDims d, cons
     const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
     const int G = d.QH / d.KVH;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // q, k, v and the RoPE table
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // q, k, v and the RoPE table (prefill: the cache rows)
     asm volatile("griddepcontrol.launch_dependents;");
-    const int p = pos[b];
+    const int p = row_pos(rm, b);
     if (p < 0 || p >= d.max_ctx) return;
     int first, count;
     visible_range(d, p, first, count);
     const int t0 = first + c * kChunk;
     const int nt = min(kChunk, first + count - t0);
     if (nt <= 0) return;
-    const size_t row0 = ((size_t)b * d.max_ctx) * d.KVH * kHeadDim + (size_t)j * kHeadDim;
+    const size_t row0 = ((size_t)row_seq(rm, b) * d.max_ctx) * d.KVH * kHeadDim + (size_t)j * kHeadDim;
     const size_t rstride = (size_t)d.KVH * kHeadDim;
     const int RW = (d.QH + 2 * d.KVH) * kHeadDim;
     const float *rq = raw + (size_t)b * RW;
     const float2 *rt = rope + (size_t)b * 32;
-    if (t0 + nt - 1 == p) {
-        // the chunk holding the new token appends its key (rotated: pair i is
-        // dims i and i + 32) and value to the cache, as fp16, before reading it
+    if (rm.seq < 0 && t0 + nt - 1 == p) {
+        // decode: the chunk holding the new token appends its key (rotated:
+        // pair i is dims i and i + 32) and value to the cache, as fp16, before
+        // reading it (prefill: the append kernel did it for every row)
         if (tid < 32) {
             const float l = rq[(d.QH + j) * kHeadDim + tid], r = rq[(d.QH + j) * kHeadDim + tid + 32];
             const float2 cs = rt[tid];
@@ -463,14 +474,37 @@ __global__ void __launch_bounds__(256, 2) moe_attn_chunk_kernel(AttnDims d, cons
     }
 }
 
+// Prefill: every new row's key (rotated with its row of the RoPE table) and
+// value into the cache of sequence seq at position pos0 + b, as fp16 (goosedump
+// gpt_oss.rs prefill_attention_layer: the batch is appended before its
+// attention).  One CTA per (row, kv head), 64 threads.
+__global__ void moe_attn_append_kernel(AttnDims d, const float *raw, const float2 *rope, RowMap rm, __half *kc,
+                                       __half *vc) {
+    const int b = blockIdx.x, j = blockIdx.y, e = threadIdx.x;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // k, v and the RoPE table
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int p = row_pos(rm, b);
+    if (p < 0 || p >= d.max_ctx) return;
+    const int RW = (d.QH + 2 * d.KVH) * kHeadDim;
+    const float *rq = raw + (size_t)b * RW;
+    const size_t at = (((size_t)row_seq(rm, b) * d.max_ctx + p) * d.KVH + j) * kHeadDim;
+    if (e < 32) {
+        const float l = rq[(d.QH + j) * kHeadDim + e], r = rq[(d.QH + j) * kHeadDim + e + 32];
+        const float2 cs = rope[(size_t)b * 32 + e];
+        kc[at + e] = __float2half_rn(l * cs.x - r * cs.y);
+        kc[at + e + 32] = __float2half_rn(l * cs.y + r * cs.x);
+    }
+    vc[at + e] = __float2half_rn(rq[(d.QH + d.KVH + j) * kHeadDim + e]);
+}
+
 // o[b][h][:] = (sum over chunks of acc e^(m_c - m)) / (sum of l e^(m_c - m) +
 // e^(sink - m)), m the largest of the chunk maxima and the sink; rounded to bf16.
-__global__ void moe_attn_merge_kernel(AttnDims d, const float *sinks, const int32_t *pos, const float *pm,
+__global__ void moe_attn_merge_kernel(AttnDims d, const float *sinks, RowMap rm, const float *pm,
                                       const float *pl, const float *pacc, int n_chunks, uint16_t *o) {
     const int h = blockIdx.x, b = blockIdx.y, e = threadIdx.x;  // 64 threads
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunks' partials
     asm volatile("griddepcontrol.launch_dependents;");
-    const int p = pos[b];
+    const int p = row_pos(rm, b);
     int first = 0, count = 0;
     if (p >= 0 && p < d.max_ctx) visible_range(d, p, first, count);
     const int nc = (count + kChunk - 1) / kChunk;
@@ -549,6 +583,54 @@ size_t attn_carve(const AttnDims &d, unsigned char *base, Carve *c) {
     t.o = reinterpret_cast<uint16_t *>(take(S * QD * 2));
     if (c) *c = t;
     return off;
+}
+
+// One step over n rows: norm, Q/K/V + RoPE table, (prefill: the append), the
+// chunked attention, merge, output projection + residual.
+cudaError_t attn_step(moe_attn *p, const uint16_t *x, int n, RowMap rm, void *out, cudaStream_t st) {
+    Carve c;
+    attn_carve(p->d, p->ws, &c);
+    const int nch = (p->d.max_ctx + kChunk - 1) / kChunk;
+    cudaError_t e = launch_rms_norm_rows(x, p->w.gamma, n, p->d.H, p->d.eps, c.xhat, c.xnorm, c.count, st);
+    const int RW = (p->d.QH + 2 * p->d.KVH) * kHeadDim, QD = p->d.QH * kHeadDim;
+    ProjArgs a{};
+    a.d = p->d;
+    a.B = n;
+    if (e == cudaSuccess) {
+        a.rows = RW;
+        a.K = p->d.H;
+        a.w[0] = p->w.wq, a.w[1] = p->w.wk, a.w[2] = p->w.wv;
+        a.bias[0] = p->w.bq, a.bias[1] = p->w.bk, a.bias[2] = p->w.bv;
+        a.r1 = QD;
+        a.r2 = QD + p->d.KVH * kHeadDim;
+        a.x = c.xhat;
+        a.raw = c.raw;
+        a.rope = c.rope;
+        a.rows_of = rm;
+        e = proj_launch<0>(a, st);
+    }
+    if (e == cudaSuccess && rm.seq >= 0)
+        e = launch_pdl(moe_attn_append_kernel, dim3(n, p->d.KVH), dim3(kHeadDim), 0, st, p->d, (const float *)c.raw,
+                       (const float2 *)c.rope, rm, p->kc, p->vc);
+    if (e == cudaSuccess)
+        e = launch_pdl(moe_attn_chunk_kernel, dim3(nch, p->d.KVH, n), dim3(256), 0, st, p->d, (const float *)c.raw,
+                       (const float2 *)c.rope, rm, p->kc, p->vc, c.pm, c.pl, c.pacc, nch);
+    if (e == cudaSuccess)
+        e = launch_pdl(moe_attn_merge_kernel, dim3(p->d.QH, n), dim3(kHeadDim), 0, st, p->d, (const float *)p->w.sinks,
+                       rm, (const float *)c.pm, (const float *)c.pl, (const float *)c.pacc, nch, c.o);
+    if (e == cudaSuccess) {
+        a.rows = p->d.H;
+        a.K = QD;
+        a.w[0] = a.w[1] = a.w[2] = p->w.wo;
+        a.bias[0] = a.bias[1] = a.bias[2] = p->w.bo;
+        a.r1 = a.r2 = p->d.H;
+        a.x = c.o;
+        a.res = x;
+        a.out = out;
+        a.out_bf16 = p->out_bf16 ? 1 : 0;
+        e = proj_launch<1>(a, st);
+    }
+    return e;
 }
 
 }  // namespace
@@ -653,48 +735,37 @@ int moe_attn_decode(moe_attn *p, const uint16_t *x, int n_seqs, const int32_t *p
     const size_t xb = (size_t)n_seqs * p->d.H * 2, ob = (size_t)n_seqs * p->d.H * (p->out_bf16 ? 2 : 4);
     const char *xc = reinterpret_cast<const char *>(x), *oc = static_cast<const char *>(out);
     if (xc < oc + ob && oc < xc + xb) return moe_fail_status(MOE_EINVAL, "x and out must not overlap");
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    Carve c;
-    attn_carve(p->d, p->ws, &c);
-    const int nch = (p->d.max_ctx + kChunk - 1) / kChunk;
-    cudaError_t e = launch_rms_norm_rows(x, p->w.gamma, n_seqs, p->d.H, p->d.eps, c.xhat, c.xnorm, c.count, st);
-    const int RW = (p->d.QH + 2 * p->d.KVH) * kHeadDim, QD = p->d.QH * kHeadDim;
-    ProjArgs a{};
-    a.d = p->d;
-    a.B = n_seqs;
-    if (e == cudaSuccess) {
-        a.rows = RW;
-        a.K = p->d.H;
-        a.w[0] = p->w.wq, a.w[1] = p->w.wk, a.w[2] = p->w.wv;
-        a.bias[0] = p->w.bq, a.bias[1] = p->w.bk, a.bias[2] = p->w.bv;
-        a.r1 = QD;
-        a.r2 = QD + p->d.KVH * kHeadDim;
-        a.x = c.xhat;
-        a.raw = c.raw;
-        a.rope = c.rope;
-        a.pos = positions;
-        e = proj_launch<0>(a, st);
-    }
-    if (e == cudaSuccess)
-        e = launch_pdl(moe_attn_chunk_kernel, dim3(nch, p->d.KVH, n_seqs), dim3(256), 0, st, p->d, (const float *)c.raw,
-                       (const float2 *)c.rope, positions, p->kc, p->vc, c.pm, c.pl, c.pacc, nch);
-    if (e == cudaSuccess)
-        e = launch_pdl(moe_attn_merge_kernel, dim3(p->d.QH, n_seqs), dim3(kHeadDim), 0, st, p->d,
-                       (const float *)p->w.sinks, positions, (const float *)c.pm, (const float *)c.pl,
-                       (const float *)c.pacc, nch, c.o);
-    if (e == cudaSuccess) {
-        a.rows = p->d.H;
-        a.K = QD;
-        a.w[0] = a.w[1] = a.w[2] = p->w.wo;
-        a.bias[0] = a.bias[1] = a.bias[2] = p->w.bo;
-        a.r1 = a.r2 = p->d.H;
-        a.x = c.o;
-        a.res = x;
-        a.out = out;
-        a.out_bf16 = p->out_bf16 ? 1 : 0;
-        e = proj_launch<1>(a, st);
-    }
+    const cudaError_t e = attn_step(p, x, n_seqs, RowMap{positions, 0, -1}, out, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : moe_fail_status(MOE_ECUDA, "moe_attn_decode: %s", cudaGetErrorString(e));
+}
+
+int moe_attn_prefill(moe_attn *p, const uint16_t *x, int n_tokens, int seq, int pos0, void *out, void *stream) {
+    if (!p) return moe_fail_status(MOE_EINVAL, "NULL plan");
+    if (!p->have_w) return moe_fail_status(MOE_ENOTREADY, "moe_attn_load_weights has not been called");
+    if (!p->ws) return moe_fail_status(MOE_ENOTREADY, "moe_attn_set_workspace has not been called");
+    if (!p->kc) return moe_fail_status(MOE_ENOTREADY, "moe_attn_set_cache has not been called");
+    if (n_tokens < 0) return moe_fail_status(MOE_EINVAL, "n_tokens must be >= 0");
+    if (n_tokens == 0) return MOE_OK;
+    if (seq < 0 || seq >= p->d.max_seq) return moe_fail_status(MOE_EINVAL, "seq must be 0..%d", p->d.max_seq - 1);
+    if (pos0 < 0 || (long long)pos0 + n_tokens > p->d.max_ctx)
+        return moe_fail_status(MOE_EINVAL, "positions %d .. %lld outside the cache's %d rows", pos0,
+                               (long long)pos0 + n_tokens - 1, p->d.max_ctx);
+    if (!x || !out) return moe_fail_status(MOE_EINVAL, "NULL x or out");
+    if (!aligned16(x) || !aligned16(out)) return moe_fail_status(MOE_EINVAL, "x and out must be 16-byte aligned");
+    const size_t xb = (size_t)n_tokens * p->d.H * 2, ob = (size_t)n_tokens * p->d.H * (p->out_bf16 ? 2 : 4);
+    const char *xc = reinterpret_cast<const char *>(x), *oc = static_cast<const char *>(out);
+    if (xc < oc + ob && oc < xc + xb) return moe_fail_status(MOE_EINVAL, "x and out must not overlap");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // blocks of up to max_seqs rows (goosedump gpt_oss.rs prefill_attention_layer:
+    // batches of PREFILL_BATCH_SIZE rows, each appended, then attended)
+    const size_t osz = p->out_bf16 ? 2 : 4;
+    cudaError_t e = cudaSuccess;
+    for (int r0 = 0; r0 < n_tokens && e == cudaSuccess; r0 += p->d.max_seq) {
+        const int nb = std::min(p->d.max_seq, n_tokens - r0);
+        e = attn_step(p, x + (size_t)r0 * p->d.H, nb, RowMap{nullptr, pos0 + r0, seq},
+                      static_cast<char *>(out) + (size_t)r0 * p->d.H * osz, st);
+    }
+    return e == cudaSuccess ? MOE_OK : moe_fail_status(MOE_ECUDA, "moe_attn_prefill: %s", cudaGetErrorString(e));
 }
 
 }  // extern "C"

@@ -27,7 +27,7 @@ EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_plan_set_i", "moe_plan_se
            "moe_forward_noalloc", "moe_cast_f32_to_bf16", "moe_mx_quantize_fp4", "moe_locality_create",
            "moe_locality_record", "moe_locality_attach", "moe_locality_read", "moe_locality_reset",
            "moe_locality_destroy", "moe_attn_create", "moe_attn_set_i", "moe_attn_set_f", "moe_attn_workspace_bytes",
-           "moe_attn_set_workspace", "moe_attn_set_cache", "moe_attn_load_weights", "moe_attn_decode",
+           "moe_attn_set_workspace", "moe_attn_set_cache", "moe_attn_load_weights", "moe_attn_decode", "moe_attn_prefill",
            "moe_attn_destroy", "moe_last_error"]
 
 
@@ -114,6 +114,7 @@ def load(build_if_missing: bool = True):
     L.moe_attn_set_cache.argtypes = [P, P, P]
     L.moe_attn_load_weights.argtypes = [P, C.POINTER(AttnWeights)]
     L.moe_attn_decode.argtypes = [P, P, I, P, P, P]
+    L.moe_attn_prefill.argtypes = [P, P, I, I, I, P, P]
     L.moe_attn_destroy.restype = None
     L.moe_attn_destroy.argtypes = [P]
     L.moe_last_error.restype = C.c_char_p
@@ -397,6 +398,11 @@ class AttnPlan:
     def decode(self, x, positions, out, stream=None):
         _check(self.L.moe_attn_decode(self.h, C.c_void_p(_ptr(x)), int(x.shape[0]), C.c_void_p(_ptr(positions)),
                                       C.c_void_p(_ptr(out)), _stream_ptr(stream)))
+
+    def prefill(self, x, seq: int, pos0: int, out, stream=None):
+        """x: bf16 bits [n][hidden] (n new tokens of cache sequence seq at positions pos0 ..)."""
+        _check(self.L.moe_attn_prefill(self.h, C.c_void_p(_ptr(x)), int(x.shape[0]), int(seq), int(pos0),
+                                       C.c_void_p(_ptr(out)), _stream_ptr(stream)))
 
     def set_i(self, key: str, value: int):
         _check(self.L.moe_attn_set_i(self.h, key.encode(), int(value)))

@@ -135,3 +135,21 @@ def decode_step(wts: dict, x_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.
     ob = bf16_round(o)
     out = x + wts["wo"] @ ob + wts["bo"]
     return out, q, ob
+
+
+def prefill(wts: dict, x_rows: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, pos0: int, *,
+            q_heads: int, kv_heads: int, head_dim: int, sliding: bool, window: int, eps: float):
+    """goosedump gpt_oss.rs `prefill_attention_layer` with `causal_gqa_batch`:
+    new tokens x_rows (bf16 bits [n][H]) of one sequence whose cache holds
+    pos0 tokens.  Every new token's k and v go to the cache; token r attends
+    over the tokens 0 .. pos0 + r (the last `window` of them on sliding
+    layers) and the sink -- the same as n decode steps in order, which is how
+    this restates it.  k_cache, v_cache: float64 [pos0 + n][kv_heads][64]
+    (rows pos0 .. receive the new keys and values).  Returns the outputs
+    [n][H]."""
+    out = []
+    for r in range(x_rows.shape[0]):
+        o, _, _ = decode_step(wts, x_rows[r], k_cache, v_cache, pos0 + r, q_heads=q_heads, kv_heads=kv_heads,
+                              head_dim=head_dim, sliding=sliding, window=window, eps=eps)
+        out.append(o)
+    return np.stack(out)

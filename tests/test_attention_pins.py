@@ -144,3 +144,54 @@ def test_heads_of_one_group_read_the_same_keys():
     for h in (1, 2, 3):
         assert np.array_equal(o[h], o[0])
     assert not np.array_equal(o[4], o[0])
+
+
+def test_prefill_equals_masked_attention_written_as_matrices():
+    """The oracle's prefill of n tokens (sequential decode steps) against a
+    restatement with matrices: all new tokens' q, k, v at once, one score
+    matrix per head with the causal mask (and, on a sliding layer, the
+    window) applied as -inf, the sink as an extra column."""
+    rng = np.random.default_rng(7)
+    H, QH, KVH, n, pos0 = 64, 8, 2, 7, 5
+    for sliding, window in ((False, 128), (True, 4)):
+        wts = _weights(rng, H, QH, KVH, sink=0.3)
+        x = synth.f32_to_bf16_bits(rng.normal(size=(n, H)))
+        kc, vc = _cache(rng, pos0 + n - 1, KVH)
+        kc1, vc1 = kc.copy(), vc.copy()
+        got = A.prefill(wts, x, kc1, vc1, pos0, q_heads=QH, kv_heads=KVH, head_dim=D, sliding=sliding,
+                        window=window, eps=1e-5)
+        # the matrix form
+        import oracle as O
+        xs = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        xh = np.stack([(O.rmsnorm(x[r], wts["gamma"], 1e-5)[0].astype(np.uint32) << 16).view(np.float32)
+                       for r in range(n)]).astype(np.float64)
+        q = xh @ wts["wq"].T + wts["bq"]
+        k = xh @ wts["wk"].T + wts["bk"]
+        v = xh @ wts["wv"].T + wts["bv"]
+        for r in range(n):
+            c, s_ = A.rope_tables(pos0 + r, D)
+            q[r] = A.apply_rope(q[r], c, s_)
+            k[r] = A.apply_rope(k[r], c, s_)
+        keys = kc.copy()
+        vals = vc.copy()
+        keys[pos0:] = A.to_fp16(k).reshape(n, KVH, D)
+        vals[pos0:] = A.to_fp16(v).reshape(n, KVH, D)
+        assert np.array_equal(keys, kc1) and np.array_equal(vals, vc1)
+        T = pos0 + n
+        t = np.arange(T)
+        o = np.zeros((n, QH * D))
+        for h in range(QH):
+            g = h // (QH // KVH)
+            sc = q[:, h * D:(h + 1) * D] @ keys[:, g, :].T / math.sqrt(D)        # [n][T]
+            pos = pos0 + np.arange(n)[:, None]
+            mask = t[None, :] <= pos
+            if sliding:
+                mask &= t[None, :] > pos - window
+            sc = np.where(mask, sc, -np.inf)
+            full = np.concatenate([sc, np.full((n, 1), wts["sinks"][h])], axis=1)
+            p = np.exp(full - full.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            o[:, h * D:(h + 1) * D] = p[:, :T] @ vals[:, g, :]
+        ob = A.bf16_round(o)
+        want = xs + ob @ wts["wo"].T + wts["bo"]
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)

@@ -149,3 +149,45 @@ def test_repeated_steps_are_bitwise_identical():
         assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
         plan.close()
 
+
+
+@pytest.mark.parametrize("window", [0, 16])
+def test_prefill_matches_the_oracle(window):
+    """Prefill (goosedump gpt_oss.rs prefill_attention_layer): 40 new tokens
+    of sequence 1 in blocks of the plan's 16 rows, after 300 cached tokens
+    (across the first 256-token chunk's end), then 9 more from position 340;
+    and a first prompt of 5 tokens into the empty sequence 2.  Outputs within the block tolerance; the new cache rows
+    within one fp16 rounding; every other cache row unchanged."""
+    import torch
+    H, QH, KVH, S, ctx = 512, 16, 4, 16, 600
+    w = synth.make_attention(51 + window, H, QH, KVH)
+    kh, vh = synth.make_kv_history(51, S, ctx, KVH)
+    dev = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda() for k, v in w.items()}
+    plan = moe.AttnPlan(H, QH, KVH, S, ctx, sliding_window=window)
+    plan.load_weights(dev)
+    plan.k_cache.copy_(torch.from_numpy(kh))
+    plan.v_cache.copy_(torch.from_numpy(vh))
+    wts = dict(gamma=w["gamma"], wq=_as64(w["wq"]), wk=_as64(w["wk"]), wv=_as64(w["wv"]), wo=_as64(w["wo"]),
+               bq=w["bq"].astype(np.float64), bk=w["bk"].astype(np.float64), bv=w["bv"].astype(np.float64),
+               bo=w["bo"].astype(np.float64), sinks=w["sinks"].astype(np.float64))
+    kref, vref = kh.astype(np.float64), vh.astype(np.float64)
+    rng = np.random.default_rng(4)
+    for seq, pos0, n in [(1, 300, 40), (1, 340, 9), (2, 0, 5)]:
+        x = synth.f32_to_bf16_bits(rng.normal(0.0, 1.0, (n, H)))
+        out = torch.empty((n, H), dtype=torch.float32, device="cuda")
+        plan.prefill(torch.from_numpy(x.view(np.int16)).cuda(), seq, pos0, out)
+        torch.cuda.synchronize()
+        kseq, vseq = kref[seq, :pos0 + n].copy(), vref[seq, :pos0 + n].copy()
+        ref = A.prefill(wts, x, kseq, vseq, pos0, q_heads=QH, kv_heads=KVH, head_dim=64, sliding=window > 0,
+                        window=window or 1, eps=1e-5)
+        check_close(out.cpu().numpy(), ref, x, what=f"prefill seq {seq} from {pos0}")
+        kc, vc = plan.k_cache.cpu().numpy(), plan.v_cache.cpu().numpy()
+        for got_c, ref_rows in ((kc, kseq), (vc, vseq)):
+            g = got_c[seq, pos0:pos0 + n].astype(np.float64)
+            r = ref_rows[pos0:pos0 + n]
+            assert np.all(np.abs(g - r) <= 2.0 ** -10 * np.abs(r) + 1e-5 * np.abs(r).max())
+        # the oracle continues from the GPU's appended rows; nothing else moved
+        kref[seq, pos0:pos0 + n] = kc[seq, pos0:pos0 + n]
+        vref[seq, pos0:pos0 + n] = vc[seq, pos0:pos0 + n]
+        assert np.array_equal(kc, kref.astype(np.float16)) and np.array_equal(vc, vref.astype(np.float16))
+    plan.close()
