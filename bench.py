@@ -589,7 +589,7 @@ def attention_bench(args, seqs: int = 16, ctx: int = 4096):
 def attention_prefill_bench(args, n: int = 512, ctx: int = 4096):
     """Prefill of the attention half (moe_attn_prefill): an n-token prompt into
     the empty cache of one sequence, one sliding-window (128) layer and one
-    full-attention layer (blocks of 32 rows, each appended, then attended).
+    full-attention layer (one block of n rows: appended, then attended).
     Timed in a CUDA graph; HBM roofline of the algorithmic bytes (both layers'
     projection weights once, the keys and values each row sees, activations)."""
     import numpy as np
@@ -599,7 +599,7 @@ def attention_prefill_bench(args, n: int = 512, ctx: int = 4096):
     H, QH, KVH, D, window = A["hidden"], A["q_heads"], A["kv_heads"], A["head_dim"], A["window"]
     plans = []
     for layer, win in enumerate((window, 0)):
-        p = moe.AttnPlan(H, QH, KVH, 32, ctx, sliding_window=win)
+        p = moe.AttnPlan(H, QH, KVH, 32, ctx, sliding_window=win, prefill_rows=n)
         p.load_weights(synth.attention_device(300 + layer, H, QH, KVH, D))
         plans.append(p)
     x = torch.from_numpy(synth.f32_to_bf16_bits(np.random.default_rng(1).normal(0, 1, (n, H))).view(np.int16)).cuda()
@@ -635,16 +635,17 @@ def attention_prefill_bench(args, n: int = 512, ctx: int = 4096):
         p.close()
     del g
     return {"value": n / (ms / 1e3), "unit": "tokens/s (one sliding + one full attention layer)", "ms_per_step": ms,
-            "path": "attention prefill (blocks of 32 rows)",
+            "path": "attention prefill (one block of the prompt's rows)",
             "config": {"workload": f"gpt-oss attention prefill, one {n}-token prompt into an empty cache, one "
                                    "sliding-window (128) and one full layer", "hidden": H, "q_heads": QH,
-                       "kv_heads": KVH, "head_dim": D, "rows_per_block": 32, "weights": "bf16 (synthetic)",
+                       "kv_heads": KVH, "head_dim": D, "rows_per_block": n, "weights": "bf16 (synthetic)",
                        "kv_cache": "fp16"},
             "algorithmic_bytes_per_step": total,
             "roofline": {"bound": "hbm", "achieved": total / (ms / 1e3) / 1e9, "peak": hbm, "peak_kind": kind,
                          "unit": "GB/s", "frac": total / (ms / 1e3) / 1e9 / hbm, "traffic": None},
-            "note": "each 32-row block reads the projection weights again (16 blocks: 16 x their bytes)",
-            "clocks": clk, "gpu_launches": reps * 2 * ((n + 31) // 32) * 6}
+            "note": "the projections take the tokens 32 at a time: their weights come from HBM once and from "
+                    "L2 for the other token blocks",
+            "clocks": clk, "gpu_launches": reps * 2 * 6}
 
 
 def decoder_bench(args, w, ctx: int = 4096):

@@ -395,7 +395,10 @@ typedef struct {
  * arguments. */
 moe_attn *moe_attn_create(int hidden, int q_heads, int kv_heads, int head_dim, int max_seqs, int max_ctx);
 /* "sliding_window": 0 (full attention) or the number of most recent tokens a
- * query sees (the page: 128 on even layers); "out_bf16": 1 writes out as bf16. */
+ * query sees (the page: 128 on even layers); "out_bf16": 1 writes out as bf16;
+ * "prefill_rows": rows of one prefill block, 1..4096 (default and minimum:
+ * max_seqs); it sizes the workspace, so set it before moe_attn_set_workspace
+ * (setting it to a new value unsets the workspace). */
 int moe_attn_set_i(moe_attn *plan, const char *key, long long value);
 /* "rms_eps", "rope_base", "rope_factor", "rope_original_context",
  * "rope_beta_fast", "rope_beta_slow" (positive, finite). */
@@ -421,8 +424,8 @@ int moe_attn_decode(moe_attn *plan, const uint16_t *x, int n_seqs, const int32_t
  * holds; the last position at most max_ctx - 1).  Token r sees the cached
  * tokens and the new tokens up to itself (the last sliding_window of them on
  * sliding layers), as a decode step at position pos0 + r would.  Processed in
- * blocks of max_seqs rows, each block's keys and values appended before its
- * attention.  x bf16 [n_tokens][H], out [n_tokens][H] (16-byte aligned, not
+ * blocks of max(max_seqs, prefill_rows) rows, each block's keys and values
+ * appended before its attention.  x bf16 [n_tokens][H], out [n_tokens][H] (16-byte aligned, not
  * overlapping); writes cache rows pos0 .. pos0 + n_tokens - 1 of sequence
  * seq and no others.  Enqueue only. */
 int moe_attn_prefill(moe_attn *plan, const uint16_t *x, int n_tokens, int seq, int pos0, void *out, void *stream);

@@ -41,11 +41,13 @@ constexpr int kHeadDim = 64;
 constexpr int kMaxSeqs = 32;      // tokens per decode step (4 MMA column tiles of 8)
 constexpr int kChunk = 256;       // context tokens per attention CTA
 constexpr int kMaxQPerKV = 16;    // query heads sharing one kv head (the attention MMA's 16 rows)
+constexpr int kMaxPrefillRows = 4096;  // prefill rows per block (workspace rows)
 
 struct AttnDims {
     int H, QH, KVH;
     int window;       // 0: full causal attention; else the last `window` tokens
     int max_seq, max_ctx;
+    int rows;         // rows a step holds in the workspace: max(max_seq, prefill rows)
     double eps;
     double rope_af;   // attention factor 0.1 ln(factor) + 1
     double freq[kHeadDim / 2];
@@ -163,15 +165,17 @@ __global__ void __launch_bounds__(256) moe_attn_proj_kernel(const __grid_constan
     asm volatile("griddepcontrol.launch_dependents;");
     const int rlo = blockIdx.x * 16 + g, rhi = rlo + 8;
     const int m = proj_mat(a, rlo), base = m == 0 ? 0 : m == 1 ? a.r1 : a.r2;
+    const int tb = blockIdx.y * 8 * NT, B = min(8 * NT, a.B - tb);  // this CTA's tokens: tb .. tb + B - 1
     float acc[NT][4];
-    gemv_tile<NT>(a.w[m] + (size_t)(rlo - base) * a.K, a.w[m] + (size_t)(rhi - base) * a.K, a.x, a.B, a.K, red, acc);
+    gemv_tile<NT>(a.w[m] + (size_t)(rlo - base) * a.K, a.w[m] + (size_t)(rhi - base) * a.K, a.x + (size_t)tb * a.K, B,
+                  a.K, red, acc);
     if ((threadIdx.x >> 5) != 0) return;
     const float blo = a.bias[m][rlo - base], bhi = a.bias[m][rhi - base];
 #pragma unroll
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
         for (int c = 0; c < 2; c++) {
-            const int b = nt * 8 + 2 * t4 + c;
+            const int b = tb + nt * 8 + 2 * t4 + c;
             if (b >= a.B) continue;
             const size_t ol = (size_t)b * a.rows + rlo, oh = (size_t)b * a.rows + rhi;
             const float lo = acc[nt][c] + blo, hi = acc[nt][2 + c] + bhi;
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(256) moe_attn_proj_kernel(const __grid_constan
                 }
             }
         }
-    if (KIND == 0)
+    if (KIND == 0 && blockIdx.y == 0)
         for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
             const double ang = (double)row_pos(a.rows_of, b) * a.d.freq[lane];
             const float r = (float)fma(-rint(ang * kInvTwoPi), kTwoPi, ang);
@@ -202,8 +206,8 @@ __global__ void __launch_bounds__(256) moe_attn_proj_kernel(const __grid_constan
 
 template <int KIND>
 cudaError_t proj_launch(const ProjArgs &a, cudaStream_t st) {
-    const dim3 grid(a.rows / 16), block(256);
-    const int nt = (a.B + 7) / 8;
+    const dim3 grid(a.rows / 16, (a.B + 31) / 32), block(256);  // above 32 tokens: blocks of 32 on grid.y
+    const int nt = a.B > 32 ? 4 : (a.B + 7) / 8;
     if (nt == 1) return launch_pdl(moe_attn_proj_kernel<1, KIND>, grid, block, 0, st, a);
     if (nt == 2) return launch_pdl(moe_attn_proj_kernel<2, KIND>, grid, block, 0, st, a);
     if (nt == 3) return launch_pdl(moe_attn_proj_kernel<3, KIND>, grid, block, 0, st, a);
@@ -570,7 +574,7 @@ size_t attn_carve(const AttnDims &d, unsigned char *base, Carve *c) {
         off = (off + bytes + 255) & ~(size_t)255;
         return q;
     };
-    const size_t S = d.max_seq, nch = (d.max_ctx + kChunk - 1) / kChunk, QD = (size_t)d.QH * kHeadDim;
+    const size_t S = d.rows, nch = (d.max_ctx + kChunk - 1) / kChunk, QD = (size_t)d.QH * kHeadDim;
     Carve t;
     t.xhat = reinterpret_cast<uint16_t *>(take(S * d.H * 2));
     t.xnorm = reinterpret_cast<float *>(take(S * 4));
@@ -653,6 +657,7 @@ moe_attn *moe_attn_create(int hidden, int q_heads, int kv_heads, int head_dim, i
     p->d.window = 0;
     p->d.max_seq = max_seqs;
     p->d.max_ctx = max_ctx;
+    p->d.rows = max_seqs;
     p->d.eps = 1e-5;
     attn_rope(p);
     return p;
@@ -668,6 +673,15 @@ int moe_attn_set_i(moe_attn *p, const char *key, long long v) {
         p->d.window = (int)v;
     } else if (!strcmp(key, "out_bf16")) {
         p->out_bf16 = v != 0;
+    } else if (!strcmp(key, "prefill_rows")) {
+        if (v < 1 || v > kMaxPrefillRows)
+            return moe_fail_status(MOE_EINVAL, "prefill_rows must be 1..%d", kMaxPrefillRows);
+        const int rows = std::max(p->d.max_seq, (int)v);
+        if (rows != p->d.rows) {
+            p->d.rows = rows;
+            p->ws = nullptr;  // the workspace is sized by the rows: set it again
+            p->ws_bytes = 0;
+        }
     } else {
         return moe_fail_status(MOE_EINVAL, "unknown integer option '%s'", key);
     }
@@ -756,12 +770,13 @@ int moe_attn_prefill(moe_attn *p, const uint16_t *x, int n_tokens, int seq, int 
     const char *xc = reinterpret_cast<const char *>(x), *oc = static_cast<const char *>(out);
     if (xc < oc + ob && oc < xc + xb) return moe_fail_status(MOE_EINVAL, "x and out must not overlap");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // blocks of up to max_seqs rows (goosedump gpt_oss.rs prefill_attention_layer:
-    // batches of PREFILL_BATCH_SIZE rows, each appended, then attended)
+    // blocks of up to max(max_seqs, prefill_rows) rows (goosedump gpt_oss.rs
+    // prefill_attention_layer: batches of PREFILL_BATCH_SIZE rows, each
+    // appended, then attended)
     const size_t osz = p->out_bf16 ? 2 : 4;
     cudaError_t e = cudaSuccess;
-    for (int r0 = 0; r0 < n_tokens && e == cudaSuccess; r0 += p->d.max_seq) {
-        const int nb = std::min(p->d.max_seq, n_tokens - r0);
+    for (int r0 = 0; r0 < n_tokens && e == cudaSuccess; r0 += p->d.rows) {
+        const int nb = std::min(p->d.rows, n_tokens - r0);
         e = attn_step(p, x + (size_t)r0 * p->d.H, nb, RowMap{nullptr, pos0 + r0, seq},
                       static_cast<char *>(out) + (size_t)r0 * p->d.H * osz, st);
     }

@@ -367,7 +367,7 @@ class AttnPlan:
     workspace and fp16 key/value caches [max_seqs][max_ctx][kv_heads][64]."""
 
     def __init__(self, hidden: int, q_heads: int, kv_heads: int, max_seqs: int, max_ctx: int, head_dim: int = 64,
-                 sliding_window: int = 0, out_bf16: bool = False, device="cuda"):
+                 sliding_window: int = 0, out_bf16: bool = False, prefill_rows: int = 0, device="cuda"):
         import torch
         self.L = load()
         h = self.L.moe_attn_create(hidden, q_heads, kv_heads, head_dim, max_seqs, max_ctx)
@@ -377,6 +377,8 @@ class AttnPlan:
         self.hidden, self.q_heads, self.kv_heads, self.max_seqs, self.max_ctx = hidden, q_heads, kv_heads, max_seqs, max_ctx
         _check(self.L.moe_attn_set_i(self.h, b"sliding_window", int(sliding_window)))
         _check(self.L.moe_attn_set_i(self.h, b"out_bf16", int(out_bf16)))
+        if prefill_rows:
+            _check(self.L.moe_attn_set_i(self.h, b"prefill_rows", int(prefill_rows)))
         n = int(self.L.moe_attn_workspace_bytes(self.h))
         self.ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
         off = (-self.ws.data_ptr()) % 256

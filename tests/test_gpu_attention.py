@@ -151,10 +151,12 @@ def test_repeated_steps_are_bitwise_identical():
 
 
 
-@pytest.mark.parametrize("window", [0, 16])
-def test_prefill_matches_the_oracle(window):
+@pytest.mark.parametrize("window,prefill_rows", [(0, 0), (16, 0), (16, 64), (0, 33)])
+def test_prefill_matches_the_oracle(window, prefill_rows):
     """Prefill (goosedump gpt_oss.rs prefill_attention_layer): 40 new tokens
-    of sequence 1 in blocks of the plan's 16 rows, after 300 cached tokens
+    of sequence 1 in blocks of the plan's 16 rows (or 64 or 33: one block, a
+    ragged one; the projections then take the tokens 32 at a time on their
+    grid's second axis), after 300 cached tokens
     (across the first 256-token chunk's end), then 9 more from position 340;
     and a first prompt of 5 tokens into the empty sequence 2.  Outputs within the block tolerance; the new cache rows
     within one fp16 rounding; every other cache row unchanged."""
@@ -163,7 +165,7 @@ def test_prefill_matches_the_oracle(window):
     w = synth.make_attention(51 + window, H, QH, KVH)
     kh, vh = synth.make_kv_history(51, S, ctx, KVH)
     dev = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda() for k, v in w.items()}
-    plan = moe.AttnPlan(H, QH, KVH, S, ctx, sliding_window=window)
+    plan = moe.AttnPlan(H, QH, KVH, S, ctx, sliding_window=window, prefill_rows=prefill_rows)
     plan.load_weights(dev)
     plan.k_cache.copy_(torch.from_numpy(kh))
     plan.v_cache.copy_(torch.from_numpy(vh))
