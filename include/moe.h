@@ -403,9 +403,9 @@ int moe_attn_set_i(moe_attn *plan, const char *key, long long value);
 /* "rms_eps", "rope_base", "rope_factor", "rope_original_context",
  * "rope_beta_fast", "rope_beta_slow" (positive, finite). */
 int moe_attn_set_f(moe_attn *plan, const char *key, double value);
-/* Device workspace a step needs (x_hat; q, k, v before RoPE; the RoPE table;
- * the chunk partials; o): caller-owned, 256-byte aligned, borrowed by
- * moe_attn_set_workspace. */
+/* Device workspace a step needs (the status word; x_hat; q, k, v before RoPE;
+ * the RoPE table; the chunk partials; o): caller-owned, 256-byte aligned,
+ * borrowed by moe_attn_set_workspace (which zeroes the status word). */
 size_t moe_attn_workspace_bytes(const moe_attn *plan);
 int moe_attn_set_workspace(moe_attn *plan, void *dev_ptr, size_t bytes);
 /* The key and value caches (fp16, layout above; borrowed). */
@@ -429,6 +429,11 @@ int moe_attn_decode(moe_attn *plan, const uint16_t *x, int n_seqs, const int32_t
  * overlapping); writes cache rows pos0 .. pos0 + n_tokens - 1 of sequence
  * seq and no others.  Enqueue only. */
 int moe_attn_prefill(moe_attn *plan, const uint16_t *x, int n_tokens, int seq, int pos0, void *out, void *stream);
+/* Synchronises the stream and returns the device-side status of the plan's
+ * kernels in *status (0 = fine; 1 = a bounded wait of the prefill's tensor-core
+ * projections gave up), then clears it; MOE_EDEVICE when it was set (message:
+ * status and detail). */
+int moe_attn_get_device_status(moe_attn *plan, int *status, void *stream);
 void moe_attn_destroy(moe_attn *plan);
 
 /* Text of the last failure on this thread ("" if none) (goosedump gpt_oss.rs:

@@ -478,6 +478,22 @@ __global__ void __launch_bounds__(256, 2) moe_attn_chunk_kernel(AttnDims d, cons
     }
 }
 
+// The RoPE table of rows 0 .. n - 1 (as the Q/K/V GEMV writes it): per row
+// and pair, the angle pos f in double less the nearest whole number of turns,
+// then its cosine and sine in float, times the attention factor.  One warp
+// per row.
+__global__ void moe_attn_rope_kernel(AttnDims d, RowMap rm, int n, float2 *rope) {
+    const int b = blockIdx.x, lane = threadIdx.x;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (b >= n) return;
+    const double ang = (double)row_pos(rm, b) * d.freq[lane];
+    const float r = (float)fma(-rint(ang * kInvTwoPi), kTwoPi, ang);
+    float sn, cs;
+    sincosf(r, &sn, &cs);
+    rope[(size_t)b * 32 + lane] = make_float2(cs * (float)d.rope_af, sn * (float)d.rope_af);
+}
+
 // Prefill: every new row's key (rotated with its row of the RoPE table) and
 // value into the cache of sequence seq at position pos0 + b, as fp16 (goosedump
 // gpt_oss.rs prefill_attention_layer: the batch is appended before its
@@ -559,6 +575,7 @@ void attn_rope(moe_attn *p) {
 }
 
 struct Carve {
+    int32_t *status;  // the device status word and its detail (the prefill GEMM's bounded waits)
     uint16_t *xhat;
     float *xnorm;
     int32_t *count;
@@ -576,6 +593,7 @@ size_t attn_carve(const AttnDims &d, unsigned char *base, Carve *c) {
     };
     const size_t S = d.rows, nch = (d.max_ctx + kChunk - 1) / kChunk, QD = (size_t)d.QH * kHeadDim;
     Carve t;
+    t.status = reinterpret_cast<int32_t *>(take(16));
     t.xhat = reinterpret_cast<uint16_t *>(take(S * d.H * 2));
     t.xnorm = reinterpret_cast<float *>(take(S * 4));
     t.count = reinterpret_cast<int32_t *>(take(4));
@@ -600,7 +618,20 @@ cudaError_t attn_step(moe_attn *p, const uint16_t *x, int n, RowMap rm, void *ou
     ProjArgs a{};
     a.d = p->d;
     a.B = n;
-    if (e == cudaSuccess) {
+    // above 32 rows (a prefill block) the projections run as tensor-core GEMMs
+    const bool gemm = n > 32 && attn_gemm_supported(p->d.H, RW) && attn_gemm_supported(QD, p->d.H);
+    if (e == cudaSuccess && gemm) {
+        AttnGemm gq{};
+        gq.n = n, gq.K = p->d.H, gq.rows = RW, gq.r1 = QD, gq.r2 = QD + p->d.KVH * kHeadDim;
+        gq.x = c.xhat;
+        gq.w[0] = p->w.wq, gq.w[1] = p->w.wk, gq.w[2] = p->w.wv;
+        gq.bias[0] = p->w.bq, gq.bias[1] = p->w.bk, gq.bias[2] = p->w.bv;
+        gq.kind = 0;
+        gq.raw = c.raw;
+        gq.status = c.status;
+        e = launch_attn_gemm(gq, st);
+        if (e == cudaSuccess) e = launch_pdl(moe_attn_rope_kernel, dim3(n), dim3(32), 0, st, p->d, rm, n, c.rope);
+    } else if (e == cudaSuccess) {
         a.rows = RW;
         a.K = p->d.H;
         a.w[0] = p->w.wq, a.w[1] = p->w.wk, a.w[2] = p->w.wv;
@@ -622,7 +653,19 @@ cudaError_t attn_step(moe_attn *p, const uint16_t *x, int n, RowMap rm, void *ou
     if (e == cudaSuccess)
         e = launch_pdl(moe_attn_merge_kernel, dim3(p->d.QH, n), dim3(kHeadDim), 0, st, p->d, (const float *)p->w.sinks,
                        rm, (const float *)c.pm, (const float *)c.pl, (const float *)c.pacc, nch, c.o);
-    if (e == cudaSuccess) {
+    if (e == cudaSuccess && gemm) {
+        AttnGemm go{};
+        go.n = n, go.K = QD, go.rows = p->d.H, go.r1 = go.r2 = p->d.H;
+        go.x = c.o;
+        go.w[0] = go.w[1] = go.w[2] = p->w.wo;
+        go.bias[0] = go.bias[1] = go.bias[2] = p->w.bo;
+        go.kind = 1;
+        go.res = x;
+        go.out = out;
+        go.out_bf16 = p->out_bf16 ? 1 : 0;
+        go.status = c.status;
+        e = launch_attn_gemm(go, st);
+    } else if (e == cudaSuccess) {
         a.rows = p->d.H;
         a.K = QD;
         a.w[0] = a.w[1] = a.w[2] = p->w.wo;
@@ -664,6 +707,22 @@ moe_attn *moe_attn_create(int hidden, int q_heads, int kv_heads, int head_dim, i
 }
 
 void moe_attn_destroy(moe_attn *p) { delete p; }
+
+int moe_attn_get_device_status(moe_attn *p, int *status, void *stream) {
+    if (!p || !status) return moe_fail_status(MOE_EINVAL, "NULL argument");
+    if (!p->ws) return moe_fail_status(MOE_ENOTREADY, "moe_attn_set_workspace has not been called");
+    Carve c;
+    attn_carve(p->d, p->ws, &c);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t h[4] = {0, 0, 0, 0};
+    cudaError_t e = cudaMemcpyAsync(h, c.status, 16, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c.status, 0, 16, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return moe_fail_status(MOE_ECUDA, "moe_attn_get_device_status: %s", cudaGetErrorString(e));
+    *status = h[0];
+    if (h[0]) return moe_fail_status(MOE_EDEVICE, "device status %d (detail %d)", h[0], h[1]);
+    return MOE_OK;
+}
 
 
 int moe_attn_set_i(moe_attn *p, const char *key, long long v) {
@@ -711,6 +770,8 @@ int moe_attn_set_workspace(moe_attn *p, void *dev, size_t bytes) {
         return moe_fail_status(MOE_ENOMEM, "workspace of %zu bytes, %zu needed", bytes, attn_carve(p->d, nullptr, nullptr));
     Carve c;
     attn_carve(p->d, static_cast<unsigned char *>(dev), &c);
+    const cudaError_t e = cudaMemset(c.status, 0, 16);
+    if (e != cudaSuccess) return moe_fail_status(MOE_ECUDA, "moe_attn_set_workspace: %s", cudaGetErrorString(e));
     p->ws = static_cast<unsigned char *>(dev);
     p->ws_bytes = bytes;
     return MOE_OK;

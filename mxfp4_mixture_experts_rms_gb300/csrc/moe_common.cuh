@@ -252,6 +252,26 @@ constexpr int kFormMma = 2;  // bf16 in the grouped GEMM's pair order (its bf16 
 int moe_fail_status(int code, const char *fmt, ...);
 void moe_set_error(const char *fmt, ...);
 // Enqueue the recording of T tokens' routes of one layer into a locality profiler.
+// Dense bf16 GEMM on the tensor cores for the attention projections of a
+// prefill block (csrc/moe_attn_gemm.cu): for each token t < n and row r of up
+// to three matrices laid end to end (w[0] rows [0, r1), w[1] [r1, r2), w[2]
+// [r2, rows)), y = sum_k x[t][k] w[r][k] + bias[r]; kind 0 writes y to
+// raw[t][r] (fp32), kind 1 writes res[t][r] + y to out[t][r] (fp32, or bf16).
+struct AttnGemm {
+    int n, K, rows, r1, r2;
+    const uint16_t *x;  // [n][K] bf16, 16-byte aligned rows
+    const uint16_t *w[3];
+    const float *bias[3];
+    int kind;
+    float *raw;
+    const uint16_t *res;
+    void *out;
+    int out_bf16;
+    int32_t *status;  // bounded waits that gave up
+};
+bool attn_gemm_supported(int K, int rows);
+cudaError_t launch_attn_gemm(const AttnGemm &g, cudaStream_t st);
+
 struct moe_locality;
 cudaError_t locality_enqueue(moe_locality *p, int layer, const int32_t *ids, const float *w, int T,
                              long long first_pos, cudaStream_t st);

@@ -28,7 +28,7 @@ EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_plan_set_i", "moe_plan_se
            "moe_locality_record", "moe_locality_attach", "moe_locality_read", "moe_locality_reset",
            "moe_locality_destroy", "moe_attn_create", "moe_attn_set_i", "moe_attn_set_f", "moe_attn_workspace_bytes",
            "moe_attn_set_workspace", "moe_attn_set_cache", "moe_attn_load_weights", "moe_attn_decode", "moe_attn_prefill",
-           "moe_attn_destroy", "moe_last_error"]
+           "moe_attn_destroy", "moe_attn_get_device_status", "moe_last_error"]
 
 
 class LocalityStats(C.Structure):
@@ -115,6 +115,7 @@ def load(build_if_missing: bool = True):
     L.moe_attn_load_weights.argtypes = [P, C.POINTER(AttnWeights)]
     L.moe_attn_decode.argtypes = [P, P, I, P, P, P]
     L.moe_attn_prefill.argtypes = [P, P, I, I, I, P, P]
+    L.moe_attn_get_device_status.argtypes = [P, C.POINTER(I), P]
     L.moe_attn_destroy.restype = None
     L.moe_attn_destroy.argtypes = [P]
     L.moe_last_error.restype = C.c_char_p
@@ -408,6 +409,13 @@ class AttnPlan:
 
     def set_i(self, key: str, value: int):
         _check(self.L.moe_attn_set_i(self.h, key.encode(), int(value)))
+
+    def device_status(self, stream=None) -> int:
+        s = C.c_int(0)
+        rc = self.L.moe_attn_get_device_status(self.h, C.byref(s), _stream_ptr(stream))
+        if rc not in (MOE_OK, MOE_EDEVICE):
+            _check(rc)
+        return s.value
 
     def close(self):
         if getattr(self, "h", None):

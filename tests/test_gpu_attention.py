@@ -188,8 +188,38 @@ def test_prefill_matches_the_oracle(window, prefill_rows):
             g = got_c[seq, pos0:pos0 + n].astype(np.float64)
             r = ref_rows[pos0:pos0 + n]
             assert np.all(np.abs(g - r) <= 2.0 ** -10 * np.abs(r) + 1e-5 * np.abs(r).max())
+        assert plan.device_status() == 0
         # the oracle continues from the GPU's appended rows; nothing else moved
         kref[seq, pos0:pos0 + n] = kc[seq, pos0:pos0 + n]
         vref[seq, pos0:pos0 + n] = vc[seq, pos0:pos0 + n]
         assert np.array_equal(kc, kref.astype(np.float16)) and np.array_equal(vc, vref.astype(np.float16))
+    plan.close()
+
+
+def test_prefill_gpt_oss_shape_tensor_core_projections():
+    """A 150-token prompt at gpt-oss shapes in one block (the projections as
+    tensor-core GEMMs over two 128-token tiles), after 100 cached tokens, on
+    a sliding layer: every output row within the block tolerance."""
+    import torch
+    a = synth.ATTN_GPT_OSS
+    H, QH, KVH, S, ctx, pos0, n = a["hidden"], a["q_heads"], a["kv_heads"], 2, 512, 100, 150
+    w = synth.make_attention(61, H, QH, KVH)
+    kh, vh = synth.make_kv_history(61, S, ctx, KVH)
+    dev = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda() for k, v in w.items()}
+    plan = moe.AttnPlan(H, QH, KVH, S, ctx, sliding_window=a["window"], prefill_rows=160)
+    plan.load_weights(dev)
+    plan.k_cache.copy_(torch.from_numpy(kh))
+    plan.v_cache.copy_(torch.from_numpy(vh))
+    x = synth.f32_to_bf16_bits(np.random.default_rng(8).normal(0.0, 1.0, (n, H)))
+    out = torch.empty((n, H), dtype=torch.float32, device="cuda")
+    plan.prefill(torch.from_numpy(x.view(np.int16)).cuda(), 1, pos0, out)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    wts = dict(gamma=w["gamma"], wq=_as64(w["wq"]), wk=_as64(w["wk"]), wv=_as64(w["wv"]), wo=_as64(w["wo"]),
+               bq=w["bq"].astype(np.float64), bk=w["bk"].astype(np.float64), bv=w["bv"].astype(np.float64),
+               bo=w["bo"].astype(np.float64), sinks=w["sinks"].astype(np.float64))
+    kseq, vseq = kh[1, :pos0 + n].astype(np.float64), vh[1, :pos0 + n].astype(np.float64)
+    ref = A.prefill(wts, x, kseq, vseq, pos0, q_heads=QH, kv_heads=KVH, head_dim=64, sliding=True,
+                    window=a["window"], eps=1e-5)
+    check_close(out.cpu().numpy(), ref, x, what="prefill at gpt-oss shapes")
     plan.close()
