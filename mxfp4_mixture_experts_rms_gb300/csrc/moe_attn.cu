@@ -519,11 +519,13 @@ __global__ void moe_attn_append_kernel(AttnDims d, const float *raw, const float
 
 // o[b][h][:] = (sum over chunks of acc e^(m_c - m)) / (sum of l e^(m_c - m) +
 // e^(sink - m)), m the largest of the chunk maxima and the sink; rounded to bf16.
+constexpr int kMergeHeads = 4;  // query heads per merge CTA (64 threads each)
 __global__ void moe_attn_merge_kernel(AttnDims d, const float *sinks, RowMap rm, const float *pm,
                                       const float *pl, const float *pacc, int n_chunks, uint16_t *o) {
-    const int h = blockIdx.x, b = blockIdx.y, e = threadIdx.x;  // 64 threads
+    const int h = blockIdx.x * kMergeHeads + (threadIdx.x >> 6), b = blockIdx.y, e = threadIdx.x & 63;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunks' partials
     asm volatile("griddepcontrol.launch_dependents;");
+    if (h >= d.QH) return;
     const int p = row_pos(rm, b);
     int first = 0, count = 0;
     if (p >= 0 && p < d.max_ctx) visible_range(d, p, first, count);
@@ -612,7 +614,13 @@ size_t attn_carve(const AttnDims &d, unsigned char *base, Carve *c) {
 cudaError_t attn_step(moe_attn *p, const uint16_t *x, int n, RowMap rm, void *out, cudaStream_t st) {
     Carve c;
     attn_carve(p->d, p->ws, &c);
-    const int nch = (p->d.max_ctx + kChunk - 1) / kChunk;
+    // chunks a row can need: a sliding layer's window, a prefill block's last
+    // row's context, else the whole cache (launched CTAs past a row's
+    // context exit at once, but each still costs a launch slot)
+    int most = p->d.max_ctx;
+    if (p->d.window > 0) most = std::min(most, p->d.window);
+    if (rm.seq >= 0) most = std::min(most, rm.pos0 + n);
+    const int nch = (most + kChunk - 1) / kChunk;
     cudaError_t e = launch_rms_norm_rows(x, p->w.gamma, n, p->d.H, p->d.eps, c.xhat, c.xnorm, c.count, st);
     const int RW = (p->d.QH + 2 * p->d.KVH) * kHeadDim, QD = p->d.QH * kHeadDim;
     ProjArgs a{};
@@ -651,7 +659,8 @@ cudaError_t attn_step(moe_attn *p, const uint16_t *x, int n, RowMap rm, void *ou
         e = launch_pdl(moe_attn_chunk_kernel, dim3(nch, p->d.KVH, n), dim3(256), 0, st, p->d, (const float *)c.raw,
                        (const float2 *)c.rope, rm, p->kc, p->vc, c.pm, c.pl, c.pacc, nch);
     if (e == cudaSuccess)
-        e = launch_pdl(moe_attn_merge_kernel, dim3(p->d.QH, n), dim3(kHeadDim), 0, st, p->d, (const float *)p->w.sinks,
+        e = launch_pdl(moe_attn_merge_kernel, dim3((p->d.QH + kMergeHeads - 1) / kMergeHeads, n),
+                       dim3(kMergeHeads * kHeadDim), 0, st, p->d, (const float *)p->w.sinks,
                        rm, (const float *)c.pm, (const float *)c.pl, (const float *)c.pacc, nch, c.o);
     if (e == cudaSuccess && gemm) {
         AttnGemm go{};
