@@ -517,6 +517,212 @@ __global__ void moe_attn_append_kernel(AttnDims d, const float *raw, const float
     vc[at + e] = __float2half_rn(rq[(d.QH + d.KVH + j) * kHeadDim + e]);
 }
 
+// Prefill attention, flash style (goosedump gpt_oss.rs causal_gqa_batch): one
+// CTA per (16 consecutive new tokens, kv head), warp w the kv head's query
+// head w, the 16 tokens the MMA's rows.  The keys and values the block can
+// see stream once through a two-stage shared-memory ring of 64-key chunks
+// (asynchronous copies) shared by all the warps; per chunk each warp forms
+// its 16 x 64 scores (q rotated as it is read, fp32 split into fp16 high and
+// low parts, against the fp16 keys transposed by ldmatrix), masks them
+// causally (and to the window), keeps a running maximum and sum per token,
+// rescales its running value sums, and adds the chunk's exponentials (split
+// the same way) times the values.  At the end the sink logit joins the
+// maximum and the denominator, and o is written (bf16).  Requires the block's
+// keys and values already in the cache (the append kernel).
+constexpr int kFChunk = 64;                  // keys per stage
+constexpr int kFPitch = kHeadDim + 8;        // shared row pitch (halves): ldmatrix rows on distinct banks
+constexpr int kFStage = 2 * kFChunk * kFPitch;  // halves per stage: keys then values
+
+template <int NTHR>  // 32 x the query heads of a kv head at most: 256 or 512
+__global__ void __launch_bounds__(NTHR) moe_attn_flash_kernel(AttnDims d, const float *raw, const float2 *rope,
+                                                             RowMap rm, int n, const __half *kc, const __half *vc,
+                                                             const float *sinks, uint16_t *o) {
+    __shared__ __align__(16) __half sm[2 * kFStage];
+    const int T0 = blockIdx.x * 16, j = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, t4 = lane & 3;
+    const int G = d.QH / d.KVH, h = j * G + w, nthr = blockDim.x;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the appended rows, q and the RoPE table
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int nb = min(16, n - T0);  // tokens of this block
+    const int P0 = row_pos(rm, T0), P1 = row_pos(rm, T0 + nb - 1);  // first and last position
+    // keys the block can see: from the first token's window start to the last token
+    const int kstart = (d.window > 0 && P0 + 1 > d.window) ? P0 + 1 - d.window : 0, kend = P1;
+    const size_t seqbase = (size_t)row_seq(rm, T0) * d.max_ctx * d.KVH * kHeadDim + (size_t)j * kHeadDim;
+    const size_t rstride = (size_t)d.KVH * kHeadDim;
+    auto load_chunk = [&](int k0, int st) {
+        __half *dst = sm + st * kFStage;
+        for (int i = tid; i < 2 * kFChunk * 8; i += nthr) {
+            const int v = i >= kFChunk * 8, r = (i >> 3) & (kFChunk - 1), pc = i & 7;
+            __half *dp = dst + (v * kFChunk + r) * kFPitch + 8 * pc;
+            const int t = k0 + r;
+            if (t <= kend) {
+                const __half *src = (v ? vc : kc) + seqbase + (size_t)t * rstride + 8 * pc;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                                 __cvta_generic_to_shared(dp))),
+                             "l"(src)
+                             : "memory");
+            } else {
+                *reinterpret_cast<uint4 *>(dp) = make_uint4(0, 0, 0, 0);  // past the block: zeros
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    load_chunk(kstart, 0);
+    // q of tokens g and g + 8 (rows past the block: zeros), rotated; A
+    // fragments of the four 16-dim steps, high and low parts
+    uint32_t qh[4][4], ql[4][4];
+    {
+        float q[2][16];  // [token g / g+8][dims 16 s + 2 t4 + {0, 1, 8, 9}, s = 0..3]
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            const int tb = T0 + g + 8 * r;
+            const bool ok = g + 8 * r < nb && w < G;
+            const float *qr = raw + (size_t)tb * (d.QH + 2 * d.KVH) * kHeadDim + (size_t)h * kHeadDim;
+            const float2 *rt = rope + (size_t)tb * 32;
+#pragma unroll
+            for (int sp = 0; sp < 2; sp++)  // dims 16 sp + .. and their partners 32 + 16 sp + ..
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int dd = 16 * sp + 2 * t4 + (e & 1) + 8 * (e >> 1);
+                    float l = 0.f, rr = 0.f;
+                    float2 cs = make_float2(0.f, 0.f);
+                    if (ok) {
+                        l = qr[dd];
+                        rr = qr[dd + 32];
+                        cs = rt[dd];
+                    }
+                    q[r][4 * sp + e] = l * cs.x - rr * cs.y;
+                    q[r][4 * (sp + 2) + e] = l * cs.y + rr * cs.x;
+                }
+        }
+#pragma unroll
+        for (int s4 = 0; s4 < 4; s4++) {
+            split_half2(q[0][4 * s4], q[0][4 * s4 + 1], qh[s4][0], ql[s4][0]);      // token g, 2 t4 .. + 1
+            split_half2(q[1][4 * s4], q[1][4 * s4 + 1], qh[s4][1], ql[s4][1]);      // token g + 8
+            split_half2(q[0][4 * s4 + 2], q[0][4 * s4 + 3], qh[s4][2], ql[s4][2]);  // token g, 2 t4 + 8 .. + 9
+            split_half2(q[1][4 * s4 + 2], q[1][4 * s4 + 3], qh[s4][3], ql[s4][3]);
+        }
+    }
+    float oacc[8][4];
+#pragma unroll
+    for (int dt = 0; dt < 8; dt++) oacc[dt][0] = oacc[dt][1] = oacc[dt][2] = oacc[dt][3] = 0.f;
+    float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
+    const int tok[2] = {P0 + g, P0 + g + 8};  // positions of tokens g and g + 8
+    int first[2];
+#pragma unroll
+    for (int r = 0; r < 2; r++) first[r] = (d.window > 0 && tok[r] + 1 > d.window) ? tok[r] + 1 - d.window : 0;
+    int st = 0;
+    for (int k0 = kstart; k0 <= kend; k0 += kFChunk, st ^= 1) {
+        if (k0 + kFChunk <= kend) {
+            load_chunk(k0 + kFChunk, st ^ 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        const __half *sk = sm + st * kFStage, *sv = sk + kFChunk * kFPitch;
+        if (w < G) {
+            // scores: 8 key tiles of 8
+            float sc[8][4];
+#pragma unroll
+            for (int nt = 0; nt < 8; nt++) {
+                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < 4; s2 += 2) {  // two 16-dim steps per ldmatrix.x4
+                    const __half *rowp = sk + (size_t)(8 * nt + (lane & 7)) * kFPitch + 16 * s2 + 8 * (lane >> 3);
+                    uint32_t b0, b1, b2, b3;
+                    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(rowp))));
+                    mma_f16(sc[nt], qh[s2][0], qh[s2][1], qh[s2][2], qh[s2][3], b0, b1);
+                    mma_f16(sc[nt], ql[s2][0], ql[s2][1], ql[s2][2], ql[s2][3], b0, b1);
+                    mma_f16(sc[nt], qh[s2 + 1][0], qh[s2 + 1][1], qh[s2 + 1][2], qh[s2 + 1][3], b2, b3);
+                    mma_f16(sc[nt], ql[s2 + 1][0], ql[s2 + 1][1], ql[s2 + 1][2], ql[s2 + 1][3], b2, b3);
+                }
+            }
+            // mask (causal, window, past the block's last key), chunk maximum per token
+            float cm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const int r = c >> 1, t = k0 + 8 * nt + 2 * t4 + (c & 1);
+                    const bool ok = t >= first[r] && t <= tok[r] && t <= kend;
+                    sc[nt][c] = ok ? sc[nt][c] * 0.125f : -INFINITY;  // 1 / sqrt(64)
+                    cm[r] = fmaxf(cm[r], sc[nt][c]);
+                }
+            float scale[2];
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                cm[r] = fmaxf(cm[r], __shfl_xor_sync(0xffffffffu, cm[r], 1));
+                cm[r] = fmaxf(cm[r], __shfl_xor_sync(0xffffffffu, cm[r], 2));
+                const float mn = fmaxf(mrun[r], cm[r]);
+                scale[r] = mrun[r] == -INFINITY ? 0.f : __expf(mrun[r] - mn);
+                mrun[r] = mn;
+                lrun[r] *= scale[r];
+            }
+#pragma unroll
+            for (int dt = 0; dt < 8; dt++) {
+                oacc[dt][0] *= scale[0], oacc[dt][1] *= scale[0];
+                oacc[dt][2] *= scale[1], oacc[dt][3] *= scale[1];
+            }
+            // exponentials into the A fragments of the value products; sums
+#pragma unroll
+            for (int ks = 0; ks < 4; ks++) {  // keys 16 ks .. + 15 = key tiles 2 ks, 2 ks + 1
+                float e[2][4];
+#pragma unroll
+                for (int hh = 0; hh < 2; hh++)
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        const float v = sc[2 * ks + hh][c];
+                        e[hh][c] = v == -INFINITY ? 0.f : __expf(v - mrun[c >> 1]);
+                        lrun[c >> 1] += e[hh][c];
+                    }
+                uint32_t ph[4], pl[4];
+                split_half2(e[0][0], e[0][1], ph[0], pl[0]);
+                split_half2(e[0][2], e[0][3], ph[1], pl[1]);
+                split_half2(e[1][0], e[1][1], ph[2], pl[2]);
+                split_half2(e[1][2], e[1][3], ph[3], pl[3]);
+#pragma unroll
+                for (int dt = 0; dt < 8; dt += 2) {
+                    const __half *rowp = sv + (size_t)(16 * ks + (lane & 15)) * kFPitch + 8 * dt + 8 * (lane >> 4);
+                    uint32_t v0, v1, v2, v3;
+                    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(rowp))));
+                    mma_f16(oacc[dt], ph[0], ph[1], ph[2], ph[3], v0, v1);
+                    mma_f16(oacc[dt + 1], ph[0], ph[1], ph[2], ph[3], v2, v3);
+                    mma_f16(oacc[dt], pl[0], pl[1], pl[2], pl[3], v0, v1);
+                    mma_f16(oacc[dt + 1], pl[0], pl[1], pl[2], pl[3], v2, v3);
+                }
+            }
+        }
+        __syncthreads();  // every warp is done with this stage before it is refilled
+    }
+    if (w >= G) return;
+    // the sink, and o
+    const float sink = sinks[h];
+#pragma unroll
+    for (int r = 0; r < 2; r++) {
+        lrun[r] += __shfl_xor_sync(0xffffffffu, lrun[r], 1);
+        lrun[r] += __shfl_xor_sync(0xffffffffu, lrun[r], 2);
+        const int b = T0 + g + 8 * r;
+        const float mf = fmaxf(mrun[r], sink);
+        const float f = mrun[r] == -INFINITY ? 0.f : __expf(mrun[r] - mf);
+        const float inv = f / (lrun[r] * f + __expf(sink - mf));
+        if (g + 8 * r >= nb) continue;
+        uint16_t *orow = o + ((size_t)b * d.QH + h) * kHeadDim;
+#pragma unroll
+        for (int dt = 0; dt < 8; dt++) {
+            const __nv_bfloat16 a0 = __float2bfloat16_rn(oacc[dt][2 * r] * inv);
+            const __nv_bfloat16 a1 = __float2bfloat16_rn(oacc[dt][2 * r + 1] * inv);
+            const uint32_t pr = (uint32_t)*reinterpret_cast<const uint16_t *>(&a0) |
+                                ((uint32_t)*reinterpret_cast<const uint16_t *>(&a1) << 16);
+            *reinterpret_cast<uint32_t *>(orow + 8 * dt + 2 * t4) = pr;
+        }
+    }
+}
+
 // o[b][h][:] = (sum over chunks of acc e^(m_c - m)) / (sum of l e^(m_c - m) +
 // e^(sink - m)), m the largest of the chunk maxima and the sink; rounded to bf16.
 constexpr int kMergeHeads = 4;  // query heads per merge CTA (64 threads each)
@@ -655,13 +861,22 @@ cudaError_t attn_step(moe_attn *p, const uint16_t *x, int n, RowMap rm, void *ou
     if (e == cudaSuccess && rm.seq >= 0)
         e = launch_pdl(moe_attn_append_kernel, dim3(n, p->d.KVH), dim3(kHeadDim), 0, st, p->d, (const float *)c.raw,
                        (const float2 *)c.rope, rm, p->kc, p->vc);
-    if (e == cudaSuccess)
-        e = launch_pdl(moe_attn_chunk_kernel, dim3(nch, p->d.KVH, n), dim3(256), 0, st, p->d, (const float *)c.raw,
-                       (const float2 *)c.rope, rm, p->kc, p->vc, c.pm, c.pl, c.pacc, nch);
-    if (e == cudaSuccess)
-        e = launch_pdl(moe_attn_merge_kernel, dim3((p->d.QH + kMergeHeads - 1) / kMergeHeads, n),
-                       dim3(kMergeHeads * kHeadDim), 0, st, p->d, (const float *)p->w.sinks,
-                       rm, (const float *)c.pm, (const float *)c.pl, (const float *)c.pacc, nch, c.o);
+    if (e == cudaSuccess && rm.seq >= 0) {
+        // prefill: the flash kernel over blocks of 16 tokens (a warp per query head)
+        const int G = p->d.QH / p->d.KVH;
+        e = launch_pdl(G <= 8 ? moe_attn_flash_kernel<256> : moe_attn_flash_kernel<512>,
+                       dim3((n + 15) / 16, p->d.KVH), dim3(32 * G), 0, st, p->d, (const float *)c.raw,
+                       (const float2 *)c.rope, rm, n, (const __half *)p->kc, (const __half *)p->vc,
+                       (const float *)p->w.sinks, c.o);
+    } else {
+        if (e == cudaSuccess)
+            e = launch_pdl(moe_attn_chunk_kernel, dim3(nch, p->d.KVH, n), dim3(256), 0, st, p->d,
+                           (const float *)c.raw, (const float2 *)c.rope, rm, p->kc, p->vc, c.pm, c.pl, c.pacc, nch);
+        if (e == cudaSuccess)
+            e = launch_pdl(moe_attn_merge_kernel, dim3((p->d.QH + kMergeHeads - 1) / kMergeHeads, n),
+                           dim3(kMergeHeads * kHeadDim), 0, st, p->d, (const float *)p->w.sinks,
+                           rm, (const float *)c.pm, (const float *)c.pl, (const float *)c.pacc, nch, c.o);
+    }
     if (e == cudaSuccess && gemm) {
         AttnGemm go{};
         go.n = n, go.K = QD, go.rows = p->d.H, go.r1 = go.r2 = p->d.H;

@@ -223,3 +223,30 @@ def test_prefill_gpt_oss_shape_tensor_core_projections():
                     window=a["window"], eps=1e-5)
     check_close(out.cpu().numpy(), ref, x, what="prefill at gpt-oss shapes")
     plan.close()
+
+
+def test_prefill_sixteen_query_heads_per_kv_head():
+    """16 query heads on one kv head (the flash kernel's 512-thread form):
+    a 40-token prompt after 20 cached tokens, full and sliding (24)."""
+    import torch
+    H, QH, KVH, S, ctx, pos0, n = 256, 16, 1, 2, 96, 20, 40
+    for window in (0, 24):
+        w = synth.make_attention(71 + window, H, QH, KVH)
+        kh, vh = synth.make_kv_history(71, S, ctx, KVH)
+        dev = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda() for k, v in w.items()}
+        plan = moe.AttnPlan(H, QH, KVH, S, ctx, sliding_window=window, prefill_rows=64)
+        plan.load_weights(dev)
+        plan.k_cache.copy_(torch.from_numpy(kh))
+        plan.v_cache.copy_(torch.from_numpy(vh))
+        x = synth.f32_to_bf16_bits(np.random.default_rng(9).normal(0.0, 1.0, (n, H)))
+        out = torch.empty((n, H), dtype=torch.float32, device="cuda")
+        plan.prefill(torch.from_numpy(x.view(np.int16)).cuda(), 0, pos0, out)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        wts = dict(gamma=w["gamma"], wq=_as64(w["wq"]), wk=_as64(w["wk"]), wv=_as64(w["wv"]), wo=_as64(w["wo"]),
+                   bq=w["bq"].astype(np.float64), bk=w["bk"].astype(np.float64), bv=w["bv"].astype(np.float64),
+                   bo=w["bo"].astype(np.float64), sinks=w["sinks"].astype(np.float64))
+        ref = A.prefill(wts, x, kh[0, :pos0 + n].astype(np.float64), vh[0, :pos0 + n].astype(np.float64), pos0,
+                        q_heads=QH, kv_heads=KVH, head_dim=64, sliding=window > 0, window=window or 1, eps=1e-5)
+        check_close(out.cpu().numpy(), ref, x, what=f"prefill, 16 heads per kv head, window {window}")
+        plan.close()
