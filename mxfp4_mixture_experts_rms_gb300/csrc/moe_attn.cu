@@ -1,10 +1,11 @@
-// moe_attn.cu -- the attention half of the gpt-oss layer, one decode step for a
-// batch of sequences (goosedump gpt_oss.rs `forward`: attention norm, the
-// query/key/value projections with biases, `apply_rope` with `Rope::new`'s
-// YaRN tables, `LayerCache::append` (fp16), `causal_gqa` / `attention_head`
-// with the per-head sink logit and `attention_window`, the output projection
-// with bias and the residual add; turbospark-runtime gptoss/mod.rs module doc
-// comment).
+// moe_attn.cu -- the attention half of the gpt-oss layer: one decode step for
+// a batch of sequences, or the prefill of a prompt (goosedump gpt_oss.rs
+// `forward` and `prefill_attention_layer`: attention norm, the query/key/value
+// projections with biases, `apply_rope` with `Rope::new`'s YaRN tables,
+// `LayerCache::append` (fp16), `causal_gqa` / `causal_gqa_batch` /
+// `attention_head` with the per-head sink logit and `attention_window`, the
+// output projection with bias and the residual add; turbospark-runtime
+// gptoss/mod.rs module doc comment).
 //
 // Kernels, in stream order (each after the first launched as a programmatic
 // dependent of the one before):
@@ -13,22 +14,26 @@
 //    16-row tiles of the concatenated weights (mma.sync m16n8k16, bf16
 //    weights and x_hat, fp32 accumulation; eight warps split K and add their
 //    partials in a fixed order), fp32 to the workspace, and the RoPE table of
-//    each sequence's position (cos and sin per pair, from the angle reduced
-//    in double);
-//  * moe_attn_chunk_kernel: one CTA per (256-token chunk of the visible
-//    context, kv head, sequence); the chunk holding the new token first
-//    appends its rotated key and its value to the caller's fp16 cache.  Each
-//    warp takes 32 of the chunk's tokens: the scores of the kv head's query
-//    heads (q rotated as it is read) and their weighted value sums on the
-//    tensor cores (mma.sync m16n8k16 f16, the query heads as the MMA's rows;
-//    fp32 q and probabilities split into fp16 high and low parts, keys and
-//    values fp16 as cached; the probabilities stay in registers), the warps'
-//    softmax statistics combined in warp order;
-//  * moe_attn_merge_kernel: the chunks and the head's sink logit combined
+//    each row's position (cos and sin per pair, from the angle reduced in
+//    double); a prefill block of more than 32 rows uses the tensor-core GEMM
+//    (moe_attn_gemm.cu) and moe_attn_rope_kernel instead;
+//  * moe_attn_append_kernel: every row's rotated key and its value into the
+//    caller's fp16 cache;
+//  * decode: moe_attn_stream_kernel, one CTA per (split of the visible
+//    context, kv head, sequence), the split's 64-key chunks through a TMA
+//    ring; the kv head's query heads are the MMA's rows (mma.sync m16n8k16
+//    f16; fp32 q and probabilities split into fp16 high and low parts, keys
+//    and values fp16 as cached; the probabilities stay in registers); then
+//    moe_attn_merge_kernel: the splits and the head's sink logit combined
 //    into o, rounded to bf16;
-//  * moe_attn_proj_kernel<., 1>: out = x + Wo o + bo with the same GEMV core.
+//  * prefill: moe_attn_flash_kernel, one CTA per (16 rows, kv head), o
+//    directly;
+//  * moe_attn_proj_kernel<., 1> (or the GEMM): out = x + Wo o + bo.
 #include "moe_common.cuh"
 #include "../../include/moe.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cmath>
@@ -240,243 +245,7 @@ __device__ __forceinline__ void mma_f16(float d[4], uint32_t a0, uint32_t a1, ui
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-constexpr int kVPad = kHeadDim + 8;  // value row in shared memory (halves): ldmatrix rows on distinct banks
 constexpr int kOPad = kHeadDim + 8;  // a warp's weighted sums per head (floats): 64-bit stores on distinct banks
-constexpr int kChunkWarps = kChunk / 32;
-static_assert(kHeadDim == 64, "the chunk kernel's fragments assume 64-dim heads");
-static_assert(kChunkWarps * kMaxQPerKV * kOPad * 4 <= kChunk * kVPad * 2, "the sums reuse the value rows' space");
-
-// Partials per (sequence, query head, chunk): max score, sum of exp(s - max),
-// and the exp-weighted value sums [64], on the tensor cores with the query
-// heads of the kv head as the MMA's 16 rows.  Warp w takes the chunk's tokens
-// 32 w .. 32 w + 31 by itself:
-//  * scores: q (fp32, split into fp16 high and low parts, about 22
-//    significant bits together) against the fp16 keys (exact), each thread
-//    reading 16 contiguous bytes of a key row per 32 dims and the matching
-//    slice of q (the MMA sees both in the same permuted k order);
-//  * the warp's own maximum per head and exp(s - max): the score fragments
-//    are, element for element, the A fragments of the weighted sum (rows the
-//    heads, k the tokens), so the probabilities (split the same way) never
-//    leave the registers;
-//  * weighted values: against the warp's 32 value rows, staged in shared
-//    memory by asynchronous copies and transposed by ldmatrix.
-// Then the eight warps' results are combined in warp order: the chunk's
-// maximum per head, each warp's sums rescaled by exp(its max - chunk max).
-__global__ void __launch_bounds__(256, 2) moe_attn_chunk_kernel(AttnDims d, const float *raw, const float2 *rope,
-                                                                RowMap rm, __half *kc, __half *vc, float *pm,
-                                                                float *pl, float *pacc, int n_chunks) {
-    __shared__ __align__(16) unsigned char smem[kChunk * kVPad * 2];
-    __shared__ float sml[kChunkWarps][kMaxQPerKV][2];  // per warp and head: max, sum
-    __half *sv = reinterpret_cast<__half *>(smem);     // [256][kVPad] value rows
-    float *so = reinterpret_cast<float *>(smem);       // [8][16][kOPad] rescaled sums (after the products)
-    const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
-    const int G = d.QH / d.KVH;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // q, k, v and the RoPE table (prefill: the cache rows)
-    asm volatile("griddepcontrol.launch_dependents;");
-    const int p = row_pos(rm, b);
-    if (p < 0 || p >= d.max_ctx) return;
-    int first, count;
-    visible_range(d, p, first, count);
-    const int t0 = first + c * kChunk;
-    const int nt = min(kChunk, first + count - t0);
-    if (nt <= 0) return;
-    const size_t row0 = ((size_t)row_seq(rm, b) * d.max_ctx) * d.KVH * kHeadDim + (size_t)j * kHeadDim;
-    const size_t rstride = (size_t)d.KVH * kHeadDim;
-    const int RW = (d.QH + 2 * d.KVH) * kHeadDim;
-    const float *rq = raw + (size_t)b * RW;
-    const float2 *rt = rope + (size_t)b * 32;
-    if (rm.seq < 0 && t0 + nt - 1 == p) {
-        // decode: the chunk holding the new token appends its key (rotated:
-        // pair i is dims i and i + 32) and value to the cache, as fp16, before
-        // reading it (prefill: the append kernel did it for every row)
-        if (tid < 32) {
-            const float l = rq[(d.QH + j) * kHeadDim + tid], r = rq[(d.QH + j) * kHeadDim + tid + 32];
-            const float2 cs = rt[tid];
-            kc[row0 + (size_t)p * rstride + tid] = __float2half_rn(l * cs.x - r * cs.y);
-            kc[row0 + (size_t)p * rstride + tid + 32] = __float2half_rn(l * cs.y + r * cs.x);
-        } else if (tid < 32 + kHeadDim) {
-            const int e = tid - 32;
-            vc[row0 + (size_t)p * rstride + e] = __float2half_rn(rq[(d.QH + d.KVH + j) * kHeadDim + e]);
-        }
-        __syncthreads();
-    }
-    const int w0 = 32 * warp;  // the warp's first token in the chunk
-    float o[8][4];             // [dim tile][fragment]: rows g, g + 8; dims 8 nd + 2 t4, + 1
-#pragma unroll
-    for (int nd = 0; nd < 8; nd++) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};  // heads g, g + 8
-    if (w0 < nt) {
-        {   // this lane's value row (zeros past the chunk's tokens)
-            const int t = w0 + lane;
-            uint4 *dst = reinterpret_cast<uint4 *>(sv + (size_t)t * kVPad);
-            if (t < nt) {
-                const __half *vr = vc + row0 + (size_t)(t0 + t) * rstride;
-#pragma unroll
-                for (int v = 0; v < kHeadDim / 8; v++) {
-                    const uint32_t da = static_cast<uint32_t>(__cvta_generic_to_shared(dst + v));
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(da), "l"(vr + 8 * v) : "memory");
-                }
-            } else {
-#pragma unroll
-                for (int v = 0; v < kHeadDim / 8; v++) dst[v] = make_uint4(0, 0, 0, 0);
-            }
-        }
-        uint4 kv[4][2];  // key rows w0 + 8 ni + g: dims 8 t4 .. + 7 and 32 + 8 t4 .. + 7
-#pragma unroll
-        for (int ni = 0; ni < 4; ni++) {
-            const int tt = w0 + 8 * ni + g;
-            if (tt < nt) {
-                const uint4 *kr = reinterpret_cast<const uint4 *>(kc + row0 + (size_t)(t0 + tt) * rstride);
-                kv[ni][0] = kr[t4];
-                kv[ni][1] = kr[4 + t4];
-            } else {
-                kv[ni][0] = kv[ni][1] = make_uint4(0, 0, 0, 0);
-            }
-        }
-        // q slices of heads g and g + 8 (zero rows past G): dims 8 t4 .. + 7
-        // and their RoPE partners 32 + 8 t4 .. + 7, rotated, split high / low
-        const float *qb = rq + (size_t)(j * G) * kHeadDim;
-        float2 cs[8];
-#pragma unroll
-        for (int e = 0; e < 8; e++) cs[e] = rt[8 * t4 + e];
-        uint32_t qh[2][2][4], ql[2][2][4];  // [row g / g+8][32-dim block][pair]
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            const int h = g + 8 * r;
-            float lo[8], hi[8];
-#pragma unroll
-            for (int e = 0; e < 8; e++) lo[e] = hi[e] = 0.f;
-            if (h < G) {
-                const float4 *q0 = reinterpret_cast<const float4 *>(qb + (size_t)h * kHeadDim + 8 * t4);
-                const float4 *q1 = reinterpret_cast<const float4 *>(qb + (size_t)h * kHeadDim + 32 + 8 * t4);
-                const float4 a0 = q0[0], a1 = q0[1], b0 = q1[0], b1 = q1[1];
-                const float l[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float rr[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    lo[e] = l[e] * cs[e].x - rr[e] * cs[e].y;
-                    hi[e] = l[e] * cs[e].y + rr[e] * cs[e].x;
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                split_half2(lo[2 * e], lo[2 * e + 1], qh[r][0][e], ql[r][0][e]);
-                split_half2(hi[2 * e], hi[2 * e + 1], qh[r][1][e], ql[r][1][e]);
-            }
-        }
-        // scores: s[ni][0..1] head g, tokens w0 + 8 ni + 2 t4, + 1; s[ni][2..3] head g + 8
-        float sc[4][4];
-#pragma unroll
-        for (int ni = 0; ni < 4; ni++) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int db = 0; db < 2; db++) {
-                const uint4 k4 = kv[ni][db];
-                mma_f16(acc, qh[0][db][0], qh[1][db][0], qh[0][db][1], qh[1][db][1], k4.x, k4.y);
-                mma_f16(acc, qh[0][db][2], qh[1][db][2], qh[0][db][3], qh[1][db][3], k4.z, k4.w);
-                mma_f16(acc, ql[0][db][0], ql[1][db][0], ql[0][db][1], ql[1][db][1], k4.x, k4.y);
-                mma_f16(acc, ql[0][db][2], ql[1][db][2], ql[0][db][3], ql[1][db][3], k4.z, k4.w);
-            }
-#pragma unroll
-            for (int qd = 0; qd < 4; qd++) {
-                const int t = w0 + 8 * ni + 2 * t4 + (qd & 1);
-                sc[ni][qd] = t < nt ? acc[qd] * 0.125f : -INFINITY;  // 1 / sqrt(64)
-            }
-        }
-        // the warp's maximum per head (the four lanes of a row hold its 32 tokens)
-#pragma unroll
-        for (int ni = 0; ni < 4; ni++) {
-            mrow[0] = fmaxf(mrow[0], fmaxf(sc[ni][0], sc[ni][1]));
-            mrow[1] = fmaxf(mrow[1], fmaxf(sc[ni][2], sc[ni][3]));
-        }
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            mrow[r] = fmaxf(mrow[r], __shfl_xor_sync(0xffffffffu, mrow[r], 1));
-            mrow[r] = fmaxf(mrow[r], __shfl_xor_sync(0xffffffffu, mrow[r], 2));
-        }
-        // exponentials into the A fragments of the products (k step ks: tokens
-        // w0 + 16 ks .. + 15 = score tiles 2 ks and 2 ks + 1)
-        uint32_t ph[2][4], plo[2][4];
-#pragma unroll
-        for (int ks = 0; ks < 2; ks++) {
-            float e[2][4];
-#pragma unroll
-            for (int hh = 0; hh < 2; hh++)
-#pragma unroll
-                for (int qd = 0; qd < 4; qd++) {
-                    e[hh][qd] = __expf(sc[2 * ks + hh][qd] - mrow[qd >> 1]);
-                    lrow[qd >> 1] += e[hh][qd];
-                }
-            split_half2(e[0][0], e[0][1], ph[ks][0], plo[ks][0]);  // head g, tokens 2 t4, + 1
-            split_half2(e[0][2], e[0][3], ph[ks][1], plo[ks][1]);  // head g + 8
-            split_half2(e[1][0], e[1][1], ph[ks][2], plo[ks][2]);  // head g, tokens 8 + 2 t4, + 1
-            split_half2(e[1][2], e[1][3], ph[ks][3], plo[ks][3]);  // head g + 8
-        }
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-            lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-        }
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        __syncwarp();
-        // weighted values: two dim tiles per ldmatrix (rows: the k step's 16
-        // tokens; lanes 16..31 address the second tile)
-#pragma unroll
-        for (int ks = 0; ks < 2; ks++)
-#pragma unroll
-            for (int nd = 0; nd < 8; nd += 2) {
-                const __half *rowp = sv + (size_t)(w0 + 16 * ks + (lane & 15)) * kVPad + 8 * nd + 8 * (lane >> 4);
-                const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(rowp));
-                uint32_t v0, v1, v2, v3;
-                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
-                             : "r"(addr));
-                mma_f16(o[nd], ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3], v0, v1);
-                mma_f16(o[nd + 1], ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3], v2, v3);
-                mma_f16(o[nd], plo[ks][0], plo[ks][1], plo[ks][2], plo[ks][3], v0, v1);
-                mma_f16(o[nd + 1], plo[ks][0], plo[ks][1], plo[ks][2], plo[ks][3], v2, v3);
-            }
-    }
-    if (t4 == 0) {
-        sml[warp][g][0] = mrow[0];
-        sml[warp][g][1] = lrow[0];
-        sml[warp][g + 8][0] = mrow[1];
-        sml[warp][g + 8][1] = lrow[1];
-    }
-    __syncthreads();  // every warp is done with the value rows; maxima and sums visible
-    // the chunk's maximum per head and this warp's sums rescaled to it
-#pragma unroll
-    for (int r = 0; r < 2; r++) {
-        const int h = g + 8 * r;
-        float M = -INFINITY;
-        for (int w = 0; w < kChunkWarps; w++) M = fmaxf(M, sml[w][h][0]);
-        const float f = mrow[r] == -INFINITY ? 0.f : __expf(mrow[r] - M);
-#pragma unroll
-        for (int nd = 0; nd < 8; nd++)
-            *reinterpret_cast<float2 *>(so + ((size_t)warp * kMaxQPerKV + h) * kOPad + 8 * nd + 2 * t4) =
-                make_float2(o[nd][2 * r] * f, o[nd][2 * r + 1] * f);
-    }
-    __syncthreads();
-    for (int i = tid; i < G * kHeadDim; i += 256) {
-        const int h = i / kHeadDim, dd = i % kHeadDim;
-        float acc = 0.f;
-        for (int w = 0; w < kChunkWarps; w++) acc += so[((size_t)w * kMaxQPerKV + h) * kOPad + dd];
-        const size_t idx = ((size_t)b * d.QH + j * G + h) * n_chunks + c;
-        pacc[idx * kHeadDim + dd] = acc;
-    }
-    if (tid < G) {
-        const int h = tid;
-        float M = -INFINITY;
-        for (int w = 0; w < kChunkWarps; w++) M = fmaxf(M, sml[w][h][0]);
-        float l = 0.f;
-        for (int w = 0; w < kChunkWarps; w++)
-            if (sml[w][h][0] != -INFINITY) l += __expf(sml[w][h][0] - M) * sml[w][h][1];
-        const size_t idx = ((size_t)b * d.QH + j * G + h) * n_chunks + c;
-        pm[idx] = M;
-        pl[idx] = l;
-    }
-}
 
 // The RoPE table of rows 0 .. n - 1 (as the Q/K/V GEMV writes it): per row
 // and pair, the angle pos f in double less the nearest whole number of turns,
@@ -515,6 +284,310 @@ __global__ void moe_attn_append_kernel(AttnDims d, const float *raw, const float
         kc[at + e + 32] = __float2half_rn(l * cs.y + r * cs.x);
     }
     vc[at + e] = __float2half_rn(rq[(d.QH + d.KVH + j) * kHeadDim + e]);
+}
+
+// Decode attention, streamed (goosedump gpt_oss.rs causal_gqa /
+// attention_head): one CTA per (split of the visible context, kv head,
+// sequence).  A producer warp copies the split's 64-key chunks of keys and
+// values by TMA (2-D maps over the caches, 128-byte swizzle) into a 4-stage
+// ring; four consumer warps take 16 keys of each chunk apiece, with the kv
+// head's query heads as the MMA's 16 rows: scores (q rotated as it is read,
+// fp32 split into fp16 high and low parts, keys by ldmatrix), a running
+// maximum and sum per head, the value sums rescaled and the chunk's
+// exponentials (split the same way) times the values (ldmatrix.trans).  The
+// four warps' results are combined in warp order into the split's partials
+// (max, sum, value sums), which the merge kernel combines with the sink.  The
+// new token's key and value are in the cache already (the append kernel).
+constexpr int kSKeys = 64;                        // keys per stage
+constexpr int kSStages = 4;
+constexpr int kSWarps = 4;                        // consumers; warp kSWarps is the producer
+constexpr int kSStage = 2 * kSKeys * 128;         // bytes: keys then values, 128-byte rows
+constexpr int kSSmem = 1024 + kSStages * kSStage;
+constexpr uint64_t kSWaitNs = 2000000000ull;
+
+struct KvMaps {
+    CUtensorMap k, v;  // [max_seq * max_ctx rows][KVH * 64] fp16, box 64 x 64, 128-byte swizzle
+};
+
+__device__ __forceinline__ uint32_t s_smem(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ bool s_try(uint64_t *b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(s_smem(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: false (and the status word set) after about 2 s, or when a
+// failure was reported elsewhere first; drain: only the time limit ends it.
+__device__ bool s_wait(uint64_t *b, uint32_t parity, int32_t *status, int where, bool drain = false) {
+    if (s_try(b, parity)) return true;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (uint32_t i = 0;; i++) {
+        if (s_try(b, parity)) return true;
+        if ((i & 63) == 63) {
+            if (!drain && *(volatile int32_t *)status != 0) return false;
+            uint64_t t1;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+            if (t1 - t0 > kSWaitNs) {
+                set_device_error(status, MOE_DEV_WAIT_TIMEOUT, where);
+                return false;
+            }
+        }
+    }
+}
+
+// Keys per split of a visible context of `count` tokens cut into `splits`:
+// whole 64-key chunks (the merge kernel uses the same cut).
+__device__ __forceinline__ int split_len(int count, int splits) {
+    return ((count + splits - 1) / splits + kSKeys - 1) / kSKeys * kSKeys;
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+__global__ void __launch_bounds__((kSWarps + 1) * 32) moe_attn_stream_kernel(
+    AttnDims d, const float *raw, const float2 *rope, RowMap rm, float *pm, float *pl, float *pacc, int n_splits,
+    int32_t *status, const __grid_constant__ KvMaps maps) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ __align__(8) uint64_t full[kSStages], empty[kSStages];
+    __shared__ float sml[kSWarps][kMaxQPerKV][2];
+    const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
+    const int G = d.QH / d.KVH;
+    if (tid == 0) {
+        for (int s = 0; s < kSStages; s++) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_smem(&full[s])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s_smem(&empty[s])), "r"(kSWarps));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // q, the RoPE table and the appended rows
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int p = row_pos(rm, b);
+    if (p < 0 || p >= d.max_ctx) return;
+    int first, count;
+    visible_range(d, p, first, count);
+    const int per = split_len(count, n_splits);
+    const int k_beg = first + c * per, k_end = min(first + count, k_beg + per);  // keys [k_beg, k_end)
+    if (k_beg >= k_end) return;
+    const int nst = (k_end - k_beg + kSKeys - 1) / kSKeys;  // chunks of this split
+    const int seqrow = row_seq(rm, b) * d.max_ctx;
+    if (warp == kSWarps) {
+        // producer: one lane issues the two copies of each chunk
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nst; i++) {
+                const int s = i % kSStages;
+                if (i >= kSStages && !s_wait(&empty[s], ((i / kSStages) - 1) & 1, status, 80)) break;
+                unsigned char *dst = smem + s * kSStage;
+                asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(
+                                 s_smem(&full[s])),
+                             "r"(kSStage)
+                             : "memory");
+#pragma unroll
+                for (int kv = 0; kv < 2; kv++)
+                    asm volatile(
+                        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+                        "{%3, %4}], [%2];" ::"r"(s_smem(dst + kv * kSKeys * 128)),
+                        "l"(reinterpret_cast<uint64_t>(kv ? &maps.v : &maps.k)), "r"(s_smem(&full[s])),
+                        "r"(j * kHeadDim), "r"(seqrow + k_beg + i * kSKeys)
+                        : "memory");
+                issued++;
+            }
+            // copies still in flight land before the CTA's shared memory goes
+            uint64_t t0;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+            for (int i = max(0, issued - kSStages); i < issued; i++)
+                while (!s_try(&full[i % kSStages], (i / kSStages) & 1)) {
+                    uint64_t t1;
+                    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+                    if (t1 - t0 > kSWaitNs) {
+                        set_device_error(status, MOE_DEV_WAIT_TIMEOUT, 81);
+                        i = issued;
+                        break;
+                    }
+                }
+        }
+    }
+    float o[8][4];  // [dim tile][fragment]: heads g, g + 8; dims 8 dt + 2 t4, + 1
+#pragma unroll
+    for (int dt = 0; dt < 8; dt++) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+    float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
+    if (warp < kSWarps) {
+        // q of heads g and g + 8 (zero rows past G), rotated: A fragments of
+        // the four 16-dim steps (dims 16 s + 2 t4 + {0, 1, 8, 9})
+        const int RW = (d.QH + 2 * d.KVH) * kHeadDim;
+        const float *qb = raw + (size_t)b * RW + (size_t)(j * G) * kHeadDim;
+        const float2 *rt = rope + (size_t)b * 32;
+        uint32_t qh[4][4], ql[4][4];
+        {
+            float q[2][16];
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                const int h = g + 8 * r;
+#pragma unroll
+                for (int sp = 0; sp < 2; sp++)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int dd = 16 * sp + 2 * t4 + (e & 1) + 8 * (e >> 1);
+                        float l = 0.f, rr = 0.f;
+                        float2 cs = make_float2(0.f, 0.f);
+                        if (h < G) {
+                            l = qb[(size_t)h * kHeadDim + dd];
+                            rr = qb[(size_t)h * kHeadDim + dd + 32];
+                            cs = rt[dd];
+                        }
+                        q[r][4 * sp + e] = l * cs.x - rr * cs.y;
+                        q[r][4 * (sp + 2) + e] = l * cs.y + rr * cs.x;
+                    }
+            }
+#pragma unroll
+            for (int s4 = 0; s4 < 4; s4++) {
+                split_half2(q[0][4 * s4], q[0][4 * s4 + 1], qh[s4][0], ql[s4][0]);
+                split_half2(q[1][4 * s4], q[1][4 * s4 + 1], qh[s4][1], ql[s4][1]);
+                split_half2(q[0][4 * s4 + 2], q[0][4 * s4 + 3], qh[s4][2], ql[s4][2]);
+                split_half2(q[1][4 * s4 + 2], q[1][4 * s4 + 3], qh[s4][3], ql[s4][3]);
+            }
+        }
+        for (int i = 0; i < nst; i++) {
+            const int s = i % kSStages, k0 = k_beg + i * kSKeys;
+            if (!s_wait(&full[s], (i / kSStages) & 1, status, 82)) break;
+            unsigned char *sk = smem + s * kSStage, *sv = sk + kSKeys * 128;
+            const int r0 = 16 * warp;  // this warp's rows of the chunk
+            if (k0 + r0 + 16 > k_end) {
+                // rows past the split: zero values (their weights are zero, but
+                // what the copy brought there need not be finite)
+                for (int r = r0 + (lane >> 3); r < r0 + 16; r += 4)
+                    if (k0 + r >= k_end) *reinterpret_cast<uint4 *>(sv + r * 128 + (lane & 7) * 16) = make_uint4(0, 0, 0, 0);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // before a copy refills the stage
+                __syncwarp();
+            }
+            // scores of keys r0 .. r0 + 15: two key tiles of 8
+            float sc[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++) {
+                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < 4; s2 += 2) {
+                    const int row = r0 + 8 * nt + (lane & 7);
+                    uint32_t b0, b1, b2, b3;
+                    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                                 : "r"(s_smem(sk) + sw128(row, 2 * s2 + (lane >> 3))));
+                    mma_f16(sc[nt], qh[s2][0], qh[s2][1], qh[s2][2], qh[s2][3], b0, b1);
+                    mma_f16(sc[nt], ql[s2][0], ql[s2][1], ql[s2][2], ql[s2][3], b0, b1);
+                    mma_f16(sc[nt], qh[s2 + 1][0], qh[s2 + 1][1], qh[s2 + 1][2], qh[s2 + 1][3], b2, b3);
+                    mma_f16(sc[nt], ql[s2 + 1][0], ql[s2 + 1][1], ql[s2 + 1][2], ql[s2 + 1][3], b2, b3);
+                }
+            }
+            float cm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+                for (int qd = 0; qd < 4; qd++) {
+                    const int t = k0 + r0 + 8 * nt + 2 * t4 + (qd & 1);
+                    sc[nt][qd] = t < k_end ? sc[nt][qd] * 0.125f : -INFINITY;  // 1 / sqrt(64)
+                    cm[qd >> 1] = fmaxf(cm[qd >> 1], sc[nt][qd]);
+                }
+            float scale[2];
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                cm[r] = fmaxf(cm[r], __shfl_xor_sync(0xffffffffu, cm[r], 1));
+                cm[r] = fmaxf(cm[r], __shfl_xor_sync(0xffffffffu, cm[r], 2));
+                const float mn = fmaxf(mrun[r], cm[r]);
+                scale[r] = mrun[r] == -INFINITY ? 0.f : __expf(mrun[r] - mn);
+                mrun[r] = mn;
+                lrun[r] *= scale[r];
+            }
+#pragma unroll
+            for (int dt = 0; dt < 8; dt++) {
+                o[dt][0] *= scale[0], o[dt][1] *= scale[0];
+                o[dt][2] *= scale[1], o[dt][3] *= scale[1];
+            }
+            float e[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+                for (int qd = 0; qd < 4; qd++) {
+                    const float v = sc[nt][qd];
+                    e[nt][qd] = v == -INFINITY ? 0.f : __expf(v - mrun[qd >> 1]);
+                    lrun[qd >> 1] += e[nt][qd];
+                }
+            uint32_t ph[4], plo[4];
+            split_half2(e[0][0], e[0][1], ph[0], plo[0]);
+            split_half2(e[0][2], e[0][3], ph[1], plo[1]);
+            split_half2(e[1][0], e[1][1], ph[2], plo[2]);
+            split_half2(e[1][2], e[1][3], ph[3], plo[3]);
+#pragma unroll
+            for (int dt = 0; dt < 8; dt += 2) {
+                const int row = r0 + (lane & 15);
+                uint32_t v0, v1, v2, v3;
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                             : "r"(s_smem(sv) + sw128(row, dt + (lane >> 4))));
+                mma_f16(o[dt], ph[0], ph[1], ph[2], ph[3], v0, v1);
+                mma_f16(o[dt + 1], ph[0], ph[1], ph[2], ph[3], v2, v3);
+                mma_f16(o[dt], plo[0], plo[1], plo[2], plo[3], v0, v1);
+                mma_f16(o[dt + 1], plo[0], plo[1], plo[2], plo[3], v2, v3);
+            }
+            __syncwarp();
+            if (lane == 0) asm volatile("{ .reg .b64 t; mbarrier.arrive.shared::cta.b64 t, [%0]; }" ::"r"(
+                                            s_smem(&empty[s]))
+                                        : "memory");
+        }
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            lrun[r] += __shfl_xor_sync(0xffffffffu, lrun[r], 1);
+            lrun[r] += __shfl_xor_sync(0xffffffffu, lrun[r], 2);
+        }
+        if (t4 == 0) {
+            sml[warp][g][0] = mrun[0];
+            sml[warp][g][1] = lrun[0];
+            sml[warp][g + 8][0] = mrun[1];
+            sml[warp][g + 8][1] = lrun[1];
+        }
+    }
+    __syncthreads();  // every stage is consumed and every copy has landed (the producer drained)
+    // the split's maximum per head and each warp's sums rescaled to it, then
+    // added in warp order
+    float *so = reinterpret_cast<float *>(smem);  // [4][16][kOPad]
+    if (warp < kSWarps) {
+#pragma unroll
+        for (int r = 0; r < 2; r++) {
+            const int h = g + 8 * r;
+            float M = -INFINITY;
+            for (int w = 0; w < kSWarps; w++) M = fmaxf(M, sml[w][h][0]);
+            const float f = mrun[r] == -INFINITY ? 0.f : __expf(mrun[r] - M);
+#pragma unroll
+            for (int dt = 0; dt < 8; dt++)
+                *reinterpret_cast<float2 *>(so + ((size_t)warp * kMaxQPerKV + h) * kOPad + 8 * dt + 2 * t4) =
+                    make_float2(o[dt][2 * r] * f, o[dt][2 * r + 1] * f);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < G * kHeadDim; i += blockDim.x) {
+        const int h = i / kHeadDim, dd = i % kHeadDim;
+        float acc = 0.f;
+        for (int w = 0; w < kSWarps; w++) acc += so[((size_t)w * kMaxQPerKV + h) * kOPad + dd];
+        const size_t idx = ((size_t)b * d.QH + j * G + h) * n_splits + c;
+        pacc[idx * kHeadDim + dd] = acc;
+    }
+    if (tid < G) {
+        const int h = tid;
+        float M = -INFINITY;
+        for (int w = 0; w < kSWarps; w++) M = fmaxf(M, sml[w][h][0]);
+        float l = 0.f;
+        for (int w = 0; w < kSWarps; w++)
+            if (sml[w][h][0] != -INFINITY) l += __expf(sml[w][h][0] - M) * sml[w][h][1];
+        const size_t idx = ((size_t)b * d.QH + j * G + h) * n_splits + c;
+        pm[idx] = M;
+        pl[idx] = l;
+    }
 }
 
 // Prefill attention, flash style (goosedump gpt_oss.rs causal_gqa_batch): one
@@ -735,7 +808,8 @@ __global__ void moe_attn_merge_kernel(AttnDims d, const float *sinks, RowMap rm,
     const int p = row_pos(rm, b);
     int first = 0, count = 0;
     if (p >= 0 && p < d.max_ctx) visible_range(d, p, first, count);
-    const int nc = (count + kChunk - 1) / kChunk;
+    const int per = split_len(count, n_chunks);
+    const int nc = count > 0 ? (count + per - 1) / per : 0;  // the splits that hold keys
     const size_t base = ((size_t)b * d.QH + h) * n_chunks;
     const float sink = sinks[h];
     float m = sink;
@@ -763,6 +837,7 @@ struct moe_attn {
     unsigned char *ws = nullptr;
     size_t ws_bytes = 0;
     bool out_bf16 = false;
+    KvMaps kv{};  // the caches as TMA maps (set with the caches)
     double rope_base = 150000.0, rope_factor = 32.0, rope_orig = 4096.0, beta_fast = 32.0, beta_slow = 1.0;
 };
 
@@ -815,6 +890,35 @@ size_t attn_carve(const AttnDims &d, unsigned char *base, Carve *c) {
     return off;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 g_kv_encode = nullptr;
+
+cudaError_t kv_encoder() {
+    if (g_kv_encode) return cudaSuccess;
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_kv_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+// Splits of each row's context for the streamed decode attention: about
+// three CTAs per SM over the (kv head, row) pairs, whole 64-key chunks, no
+// more than the workspace's partials hold.
+cudaError_t stream_splits(const AttnDims &d, int n, int most, int *splits) {
+    static PerDevice<int> sms;
+    int dev = 0;
+    cudaError_t e = current_device_slot(&dev);
+    if (e != cudaSuccess) return e;
+    int &n_sm = sms.v[dev];
+    if (!n_sm) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int pairs = d.KVH * n, cap = (d.max_ctx + kChunk - 1) / kChunk, chunks = (most + kSKeys - 1) / kSKeys;
+    *splits = std::max(1, std::min({3 * n_sm / pairs, cap, chunks}));  // one wave: no partial second one
+    return cudaSuccess;
+}
+
 // One step over n rows: norm, Q/K/V + RoPE table, (prefill: the append), the
 // chunked attention, merge, output projection + residual.
 cudaError_t attn_step(moe_attn *p, const uint16_t *x, int n, RowMap rm, void *out, cudaStream_t st) {
@@ -826,7 +930,6 @@ cudaError_t attn_step(moe_attn *p, const uint16_t *x, int n, RowMap rm, void *ou
     int most = p->d.max_ctx;
     if (p->d.window > 0) most = std::min(most, p->d.window);
     if (rm.seq >= 0) most = std::min(most, rm.pos0 + n);
-    const int nch = (most + kChunk - 1) / kChunk;
     cudaError_t e = launch_rms_norm_rows(x, p->w.gamma, n, p->d.H, p->d.eps, c.xhat, c.xnorm, c.count, st);
     const int RW = (p->d.QH + 2 * p->d.KVH) * kHeadDim, QD = p->d.QH * kHeadDim;
     ProjArgs a{};
@@ -869,13 +972,30 @@ cudaError_t attn_step(moe_attn *p, const uint16_t *x, int n, RowMap rm, void *ou
                        (const float2 *)c.rope, rm, n, (const __half *)p->kc, (const __half *)p->vc,
                        (const float *)p->w.sinks, c.o);
     } else {
+        // decode: the new rows into the cache, the streamed attention over
+        // splits of each row's context, the merge
+        int splits = 1;
         if (e == cudaSuccess)
-            e = launch_pdl(moe_attn_chunk_kernel, dim3(nch, p->d.KVH, n), dim3(256), 0, st, p->d,
-                           (const float *)c.raw, (const float2 *)c.rope, rm, p->kc, p->vc, c.pm, c.pl, c.pacc, nch);
+            e = launch_pdl(moe_attn_append_kernel, dim3(n, p->d.KVH), dim3(kHeadDim), 0, st, p->d,
+                           (const float *)c.raw, (const float2 *)c.rope, rm, p->kc, p->vc);
+        if (e == cudaSuccess) e = stream_splits(p->d, n, most, &splits);
+        if (e == cudaSuccess) {
+            static PerDevice<bool> opted;
+            int dev = 0;
+            e = current_device_slot(&dev);
+            if (e == cudaSuccess && !opted.v[dev]) {
+                e = cudaFuncSetAttribute(moe_attn_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSSmem);
+                if (e == cudaSuccess) opted.v[dev] = true;
+            }
+        }
+        if (e == cudaSuccess)
+            e = launch_pdl(moe_attn_stream_kernel, dim3(splits, p->d.KVH, n), dim3((kSWarps + 1) * 32),
+                           (size_t)kSSmem, st, p->d, (const float *)c.raw, (const float2 *)c.rope, rm, c.pm, c.pl,
+                           c.pacc, splits, c.status, p->kv);
         if (e == cudaSuccess)
             e = launch_pdl(moe_attn_merge_kernel, dim3((p->d.QH + kMergeHeads - 1) / kMergeHeads, n),
                            dim3(kMergeHeads * kHeadDim), 0, st, p->d, (const float *)p->w.sinks,
-                           rm, (const float *)c.pm, (const float *)c.pl, (const float *)c.pacc, nch, c.o);
+                           rm, (const float *)c.pm, (const float *)c.pl, (const float *)c.pacc, splits, c.o);
     }
     if (e == cudaSuccess && gemm) {
         AttnGemm go{};
@@ -1004,6 +1124,19 @@ int moe_attn_set_workspace(moe_attn *p, void *dev, size_t bytes) {
 int moe_attn_set_cache(moe_attn *p, void *k_cache, void *v_cache) {
     if (!p || !k_cache || !v_cache) return moe_fail_status(MOE_EINVAL, "NULL argument");
     if (!aligned16(k_cache) || !aligned16(v_cache)) return moe_fail_status(MOE_EINVAL, "caches must be 16-byte aligned");
+    cudaError_t e = kv_encoder();
+    for (int i = 0; i < 2 && e == cudaSuccess; i++) {
+        cuuint64_t dims[2] = {(cuuint64_t)p->d.KVH * kHeadDim, (cuuint64_t)p->d.max_seq * p->d.max_ctx};
+        cuuint64_t strides[1] = {(cuuint64_t)p->d.KVH * kHeadDim * 2};
+        cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)kSKeys};
+        cuuint32_t estr[2] = {1, 1};
+        const CUresult r = g_kv_encode(i ? &p->kv.v : &p->kv.k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, i ? v_cache : k_cache,
+                                       dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) e = cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return moe_fail_status(MOE_ECUDA, "moe_attn_set_cache: tensor maps: %s", cudaGetErrorString(e));
     p->kc = static_cast<__half *>(k_cache);
     p->vc = static_cast<__half *>(v_cache);
     return MOE_OK;
