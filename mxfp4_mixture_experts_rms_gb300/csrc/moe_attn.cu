@@ -166,10 +166,16 @@ template <int NT, int KIND>
 __global__ void __launch_bounds__(256) moe_attn_proj_kernel(const __grid_constant__ ProjArgs a) {
     __shared__ float red[7 * NT * 32][4];
     const int lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the activations come from the previous kernel
-    asm volatile("griddepcontrol.launch_dependents;");
     const int rlo = blockIdx.x * 16 + g, rhi = rlo + 8;
     const int m = proj_mat(a, rlo), base = m == 0 ? 0 : m == 1 ? a.r1 : a.r2;
+    if (threadIdx.x == 0 && blockIdx.y == 0) {
+        // the tile's 16 weight rows (contiguous) into L2 while the previous
+        // kernel finishes: they do not depend on it
+        const uint16_t *w0 = a.w[m] + (size_t)(blockIdx.x * 16 - base) * a.K;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(w0), "r"((uint32_t)(16 * a.K * 2)) : "memory");
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the activations come from the previous kernel
+    asm volatile("griddepcontrol.launch_dependents;");
     const int tb = blockIdx.y * 8 * NT, B = min(8 * NT, a.B - tb);  // this CTA's tokens: tb .. tb + B - 1
     float acc[NT][4];
     gemv_tile<NT>(a.w[m] + (size_t)(rlo - base) * a.K, a.w[m] + (size_t)(rhi - base) * a.K, a.x + (size_t)tb * a.K, B,

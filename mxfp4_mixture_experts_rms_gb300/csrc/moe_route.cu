@@ -827,6 +827,11 @@ constexpr int kNormXC = kRouteThreads * kXC / kNormThreads;  // 16-byte chunks o
 __global__ void __launch_bounds__(kNormThreads) moe_route_norm_kernel(RouteArgs a) {
     const int H = a.bp.H, E = a.bp.E;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // launched as a programmatic dependent (rows only, no router: the
+    // attention's norm) it waits for the previous kernel, whose output x is,
+    // and lets its dependent launch at once (it prefetches weights meanwhile)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!a.router_w) asm volatile("griddepcontrol.launch_dependents;");
     if ((int)blockIdx.x >= a.T) {
         // |w| of router rows, a warp per row: a sum of squares (relative error
         // below 2e-6), one correctly rounded square root, then a margin well
@@ -1291,8 +1296,7 @@ cudaError_t launch_rms_norm_rows(const uint16_t *x, const float *gamma, int T, i
     ws.xnorm = xnorm_scratch;
     ws.counts = count_scratch;
     RouteArgs a{bp, ws, x, gamma, nullptr, nullptr, T, nullptr, nullptr, nullptr, 0, 0, 0, 0, 1.0 / (double)H};
-    moe_route_norm_kernel<<<T, kNormThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(moe_route_norm_kernel, dim3(T), dim3(kNormThreads), 0, st, a);
 }
 
 cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint16_t *x, const float *gamma,
