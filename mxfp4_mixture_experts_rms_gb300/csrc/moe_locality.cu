@@ -104,17 +104,19 @@ __device__ void adjacent(const LocState &s, const LocDims &d, int layer, const i
 // histograms (atomics) and the adjacent-token overlaps.
 __global__ void __launch_bounds__(kLocThreads) moe_locality_kernel(LocState s, LocDims d, int layer, const int32_t *ids,
                                                                  const float *w, int T, long long first_pos) {
-    __shared__ unsigned long long s_last[MOE_MAX_EXPERTS];
     __shared__ int s_ids[kLocChunk];
     __shared__ float s_w[kLocChunk];
     __shared__ int s_dist[kLocChunk];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = d.E, K = d.K, n = T * K;
     if (warp == 0) {
+        // expert e's last use lives in lane e % 32, register slot e / 32
+        constexpr int kSlots = MOE_MAX_EXPERTS / 32;
         unsigned long long *last = s.last_use + (size_t)layer * E;
-        for (int e = lane; e < E; e += 32) s_last[e] = last[e];
+        unsigned long long lr[kSlots];
+#pragma unroll
+        for (int k = 0; k < kSlots; k++) lr[k] = 32 * k + lane < E ? last[32 * k + lane] : 0ull;
         unsigned long long clk = s.clock[layer];
-        __syncwarp();
         unsigned long long hits[kLocMaxCaps];  // registers: every index below is a constant
         double whits[kLocMaxCaps];
 #pragma unroll
@@ -132,25 +134,34 @@ __global__ void __launch_bounds__(kLocThreads) moe_locality_kernel(LocState s, L
             __syncwarp();
             // in access order: each selection's count of experts used since the
             // expert's last use (a hit for every larger capacity; never used
-            // before or skipped: a hit for none), integer work only
+            // before or skipped: a hit for none), integer work only, in registers
             for (int i = 0; i < m; i++) {
                 const int e = s_ids[i];
                 int dist = 0x7fffffff;
                 if (e >= 0 && e < E) {
-                    const unsigned long long lu = s_last[e];
+                    const int slot = e >> 5, owner = e & 31;
+                    unsigned long long mine = 0;
+#pragma unroll
+                    for (int k = 0; k < kSlots; k++)
+                        if (k == slot) mine = lr[k];
+                    const unsigned long long lu = __shfl_sync(0xffffffffu, mine, owner);
                     if (lu) {
                         int later = 0;
-                        for (int j = lane; j < E; j += 32) later += s_last[j] > lu;
 #pragma unroll
-                        for (int o = 16; o; o >>= 1) later += __shfl_xor_sync(0xffffffffu, later, o);
+                        for (int k = 0; k < kSlots; k++)
+                            if (32 * k < E) later += __popc(__ballot_sync(0xffffffffu, lr[k] > lu));
                         dist = later;
                     }
-                    __syncwarp();
-                    if (lane == 0) s_last[e] = ++clk;
+                    ++clk;
+                    if (lane == owner) {
+#pragma unroll
+                        for (int k = 0; k < kSlots; k++)
+                            if (k == slot) lr[k] = clk;
+                    }
                 }
                 if (lane == 0) s_dist[i] = dist;
-                __syncwarp();
             }
+            __syncwarp();
             // hits and hit weights per capacity, the lanes over the chunk's selections
 #pragma unroll
             for (int c = 0; c < kLocMaxCaps; c++) {
@@ -172,7 +183,9 @@ __global__ void __launch_bounds__(kLocThreads) moe_locality_kernel(LocState s, L
             }
             __syncwarp();
         }
-        for (int e = lane; e < E; e += 32) last[e] = s_last[e];
+#pragma unroll
+        for (int k = 0; k < kSlots; k++)
+            if (32 * k + lane < E) last[32 * k + lane] = lr[k];
         if (lane == 0) {
             s.clock[layer] = clk;
 #pragma unroll
