@@ -612,8 +612,8 @@ constexpr int kFChunk = 64;                  // keys per stage
 constexpr int kFPitch = kHeadDim + 8;        // shared row pitch (halves): ldmatrix rows on distinct banks
 constexpr int kFStage = 2 * kFChunk * kFPitch;  // halves per stage: keys then values
 
-template <int NTHR>  // 32 x the query heads of a kv head at most: 256 or 512
-__global__ void __launch_bounds__(NTHR) moe_attn_flash_kernel(AttnDims d, const float *raw, const float2 *rope,
+template <int NTHR>  // 32 x the query heads of a kv head at most: 256 (two CTAs an SM) or 512
+__global__ void __launch_bounds__(NTHR, 512 / NTHR) moe_attn_flash_kernel(AttnDims d, const float *raw, const float2 *rope,
                                                              RowMap rm, int n, const __half *kc, const __half *vc,
                                                              const float *sinks, uint16_t *o) {
     __shared__ __align__(16) __half sm[2 * kFStage];
