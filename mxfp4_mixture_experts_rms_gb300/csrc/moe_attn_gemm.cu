@@ -5,12 +5,13 @@
 //
 // y[t][r] = sum_k x[t][k] W[r][k] + b[r] for the block's tokens t and the rows
 // r of up to three matrices laid end to end (Wq, Wk, Wv; or Wo alone).  One
-// CTA per (256 weight rows, 128 tokens) tile:
+// CTA per (TN weight rows, 128 tokens) tile, TN = 256, or 128 when twice the
+// tiles still make one wave:
 //  * warp 0 (one lane): per 64-element k-block, one TMA copy of the tokens'
-//    activations (128 rows x 128 B) and one of the weight rows (256 rows x
+//    activations (128 rows x 128 B) and one of the weight rows (TN rows x
 //    128 B), both 128-byte swizzled, into a 4-stage ring;
-//  * warp 1 (one lane; it owns the 256 TMEM columns): four
-//    tcgen05.mma.cta_group::1.kind::f16 (M = 128 tokens, N = 256 rows,
+//  * warp 1 (one lane; it owns the TN TMEM columns): four
+//    tcgen05.mma.cta_group::1.kind::f16 (M = 128 tokens, N = TN rows,
 //    K = 16, bf16 operands, fp32 accumulator in TMEM) per k-block, each
 //    stage released by tcgen05.commit;
 //  * warps 2..5: the epilogue, one TMEM lane quarter (32 tokens) each:
@@ -26,11 +27,11 @@
 namespace {
 
 constexpr int kGM = 128;                 // tokens per tile (TMEM lanes)
-constexpr int kGN = 256;                 // weight rows per tile (TMEM columns)
+constexpr int kGN = 256;                 // weight rows per tile (TMEM columns): 256, or 128 when that fills more SMs
 constexpr int kGK = 64;                  // elements per k-block: one 128-byte swizzle row
 constexpr int kGStages = 4;
 constexpr int kGABytes = kGM * kGK * 2;  // 16 KB
-constexpr int kGBBytes = kGN * kGK * 2;  // 32 KB
+constexpr int kGBBytes = kGN * kGK * 2;  // 32 KB (the stage's room; an N = 128 tile uses half)
 constexpr int kGThreads = 6 * 32;
 constexpr uint64_t kGWaitNs = 2000000000ull;
 
@@ -125,8 +126,9 @@ __device__ __forceinline__ void g_ld32(uint32_t taddr, float v[32]) {
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
-// Tile blockIdx.x over the matrices' 256-row tiles (a tile never spans two
+// Tile blockIdx.x over the matrices' TN-row tiles (a tile never spans two
 // matrices), tokens 128 blockIdx.y .. + 127.
+template <int TN>
 __global__ void __launch_bounds__(kGThreads, 1) moe_attn_gemm_kernel(const __grid_constant__ AttnGemm g,
                                                                       const __grid_constant__ GemmMaps maps) {
     extern __shared__ unsigned char smem_raw[];
@@ -139,11 +141,11 @@ __global__ void __launch_bounds__(kGThreads, 1) moe_attn_gemm_kernel(const __gri
     const int starts[3] = {0, g.r1, g.r2}, ends[3] = {g.r1, g.r2, g.rows};
     int m = 0, t = blockIdx.x;
     for (; m < 2; m++) {
-        const int nt = (ends[m] - starts[m] + kGN - 1) / kGN;
+        const int nt = (ends[m] - starts[m] + TN - 1) / TN;
         if (t < nt) break;
         t -= nt;
     }
-    const int n0 = t * kGN, mrows = ends[m] - starts[m], m0 = blockIdx.y * kGM;
+    const int n0 = t * TN, mrows = ends[m] - starts[m], m0 = blockIdx.y * kGM;
     const int nkb = (g.K + kGK - 1) / kGK;
     int32_t *status = g.status;
     if (threadIdx.x == 0) {
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kGThreads, 1) moe_attn_gemm_kernel(const __gri
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(g_smem(&tmem_slot)),
-                     "n"(kGN));
+                     "n"(TN));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     g_fence_before();
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kGThreads, 1) moe_attn_gemm_kernel(const __gri
             for (int kb = 0; kb < nkb; kb++) {
                 const int s = kb % kGStages;
                 if (kb >= kGStages && !g_wait(&empty[s], ((kb / kGStages) - 1) & 1, status, 70)) break;
-                g_expect(&full[s], kGABytes + kGBBytes);
+                g_expect(&full[s], kGABytes + TN * kGK * 2);
                 g_tma(sA + s * kGABytes, &maps.a, &full[s], kb * kGK, m0, 0ull);
                 g_tma(sB + s * kGBBytes, &maps.b[m], &full[s], kb * kGK, n0, pol);
                 issued++;
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kGThreads, 1) moe_attn_gemm_kernel(const __gri
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = g_idesc(kGM, kGN);
+            constexpr uint32_t idesc = g_idesc(kGM, TN);
             bool ok = true;
             for (int kb = 0; kb < nkb; kb++) {
                 const int s = kb % kGStages;
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(kGThreads, 1) moe_attn_gemm_kernel(const __gri
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
             const float *bias = g.bias[m];
 #pragma unroll 1
-            for (int c0 = 0; c0 < kGN; c0 += 32) {
+            for (int c0 = 0; c0 < TN; c0 += 32) {
                 if (n0 + c0 >= mrows) break;  // past the matrix (whole 32-row chunks: rows are multiples of 32)
                 float v[32];
                 g_ld32(taddr + c0, v);
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(kGThreads, 1) moe_attn_gemm_kernel(const __gri
     }
     g_fence_before();
     __syncthreads();
-    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kGN));
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(TN));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -311,25 +313,36 @@ bool attn_gemm_supported(int K, int rows) {
 
 cudaError_t launch_attn_gemm(const AttnGemm &g, cudaStream_t st) {
     static PerDevice<bool> opted;
+    static PerDevice<int> sms;
     int dev = 0;
     MOE_CUDA_TRY(current_device_slot(&dev));
     const int smem = 1024 + kGStages * (kGABytes + kGBBytes);
     if (!opted.v[dev]) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(moe_attn_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        MOE_CUDA_TRY(cudaFuncSetAttribute(moe_attn_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        MOE_CUDA_TRY(cudaFuncSetAttribute(moe_attn_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms.v[dev], cudaDevAttrMultiProcessorCount, dev));
         opted.v[dev] = true;
     }
     MOE_CUDA_TRY(gemm_encoder());
-    GemmMaps maps;
-    memset(&maps, 0, sizeof maps);
-    MOE_CUDA_TRY(gemm_map(&maps.a, g.x, g.n, g.K, kGM));
     const int starts[3] = {0, g.r1, g.r2}, ends[3] = {g.r1, g.r2, g.rows};
-    int tiles = 0;
+    const int mt = (g.n + kGM - 1) / kGM;
+    // 256-row tiles, or 128-row ones when twice as many tiles still make one wave
+    int tiles256 = 0, tiles128 = 0;
     for (int i = 0; i < 3; i++) {
         const int rows = ends[i] - starts[i];
         if (rows <= 0) continue;
-        MOE_CUDA_TRY(gemm_map(&maps.b[i], g.w[i], rows, g.K, kGN));
-        tiles += (rows + kGN - 1) / kGN;
+        tiles256 += (rows + 255) / 256;
+        tiles128 += (rows + 127) / 128;
     }
-    const dim3 grid(tiles, (g.n + kGM - 1) / kGM);
-    return launch_pdl(moe_attn_gemm_kernel, grid, dim3(kGThreads), (size_t)smem, st, g, maps);
+    const int tn = tiles128 * mt <= sms.v[dev] ? 128 : 256;
+    GemmMaps maps;
+    memset(&maps, 0, sizeof maps);
+    MOE_CUDA_TRY(gemm_map(&maps.a, g.x, g.n, g.K, kGM));
+    for (int i = 0; i < 3; i++) {
+        const int rows = ends[i] - starts[i];
+        if (rows > 0) MOE_CUDA_TRY(gemm_map(&maps.b[i], g.w[i], rows, g.K, tn));
+    }
+    const dim3 grid(tn == 128 ? tiles128 : tiles256, mt);
+    if (tn == 128) return launch_pdl(moe_attn_gemm_kernel<128>, grid, dim3(kGThreads), (size_t)smem, st, g, maps);
+    return launch_pdl(moe_attn_gemm_kernel<256>, grid, dim3(kGThreads), (size_t)smem, st, g, maps);
 }

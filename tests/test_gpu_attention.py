@@ -196,17 +196,20 @@ def test_prefill_matches_the_oracle(window, prefill_rows):
     plan.close()
 
 
-def test_prefill_gpt_oss_shape_tensor_core_projections():
-    """A 150-token prompt at gpt-oss shapes in one block (the projections as
-    tensor-core GEMMs over two 128-token tiles), after 100 cached tokens, on
-    a sliding layer: every output row within the block tolerance."""
+@pytest.mark.parametrize("pos0,n", [(100, 150), (0, 400)])
+def test_prefill_gpt_oss_shape_tensor_core_projections(pos0, n):
+    """Prompts at gpt-oss shapes in one block, the projections as tensor-core
+    GEMMs: 150 tokens after 100 cached ones (two 128-token tiles, 128-row
+    weight tiles), and 400 tokens into an empty cache (four token tiles: the
+    Q/K/V GEMM takes 256-row weight tiles), on a sliding layer: every output
+    row within the block tolerance."""
     import torch
     a = synth.ATTN_GPT_OSS
-    H, QH, KVH, S, ctx, pos0, n = a["hidden"], a["q_heads"], a["kv_heads"], 2, 512, 100, 150
+    H, QH, KVH, S, ctx = a["hidden"], a["q_heads"], a["kv_heads"], 2, 512
     w = synth.make_attention(61, H, QH, KVH)
     kh, vh = synth.make_kv_history(61, S, ctx, KVH)
     dev = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda() for k, v in w.items()}
-    plan = moe.AttnPlan(H, QH, KVH, S, ctx, sliding_window=a["window"], prefill_rows=160)
+    plan = moe.AttnPlan(H, QH, KVH, S, ctx, sliding_window=a["window"], prefill_rows=n)
     plan.load_weights(dev)
     plan.k_cache.copy_(torch.from_numpy(kh))
     plan.v_cache.copy_(torch.from_numpy(vh))
