@@ -703,6 +703,9 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
                 : "memory");
         }
     }
+    // launched as a programmatic dependent of the previous forward's last
+    // kernel: the router rows (constant) are on their way; x is its output
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     MOE_PHASE_MARK(0);
     // ---------------------------------------------------------------- norm
     const int nchunk = H / 8;
@@ -1264,13 +1267,15 @@ cudaError_t launch_small(const RouteArgs &a, const SmallGeo &g, cudaStream_t st)
     cfg.blockDim = dim3(kRouteThreads);
     cfg.dynamicSmemBytes = g.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = g.C;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, moe_route_small_kernel<STAGED>, a);
 }
 
