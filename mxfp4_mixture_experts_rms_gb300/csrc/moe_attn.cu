@@ -612,14 +612,15 @@ constexpr int kFChunk = 64;                  // keys per stage
 constexpr int kFPitch = kHeadDim + 8;        // shared row pitch (halves): ldmatrix rows on distinct banks
 constexpr int kFStage = 2 * kFChunk * kFPitch;  // halves per stage: keys then values
 
-template <int NTHR>  // 32 x the query heads of a kv head at most: 256 (two CTAs an SM) or 512
-__global__ void __launch_bounds__(NTHR, 512 / NTHR) moe_attn_flash_kernel(AttnDims d, const float *raw, const float2 *rope,
+__global__ void __launch_bounds__(256) moe_attn_flash_kernel(AttnDims d, const float *raw, const float2 *rope,
                                                              RowMap rm, int n, const __half *kc, const __half *vc,
                                                              const float *sinks, uint16_t *o) {
     __shared__ __align__(16) __half sm[2 * kFStage];
     const int T0 = blockIdx.x * 16, j = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, g = lane >> 2, t4 = lane & 3;
-    const int G = d.QH / d.KVH, h = j * G + w, nthr = blockDim.x;
+    // warp w: query head 8 blockIdx.z + w of the kv head (more than 8 heads
+    // per kv head take further CTAs on grid.z)
+    const int G = d.QH / d.KVH, hw = 8 * blockIdx.z + w, h = j * G + hw, nthr = blockDim.x;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the appended rows, q and the RoPE table
     asm volatile("griddepcontrol.launch_dependents;");
     const int nb = min(16, n - T0);  // tokens of this block
@@ -655,7 +656,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR) moe_attn_flash_kernel(AttnDi
 #pragma unroll
         for (int r = 0; r < 2; r++) {
             const int tb = T0 + g + 8 * r;
-            const bool ok = g + 8 * r < nb && w < G;
+            const bool ok = g + 8 * r < nb && hw < G;
             const float *qr = raw + (size_t)tb * (d.QH + 2 * d.KVH) * kHeadDim + (size_t)h * kHeadDim;
             const float2 *rt = rope + (size_t)tb * 32;
 #pragma unroll
@@ -700,7 +701,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR) moe_attn_flash_kernel(AttnDi
         }
         __syncthreads();
         const __half *sk = sm + st * kFStage, *sv = sk + kFChunk * kFPitch;
-        if (w < G) {
+        if (hw < G) {
             // scores: 8 key tiles of 8
             float sc[8][4];
 #pragma unroll
@@ -778,7 +779,7 @@ __global__ void __launch_bounds__(NTHR, 512 / NTHR) moe_attn_flash_kernel(AttnDi
         }
         __syncthreads();  // every warp is done with this stage before it is refilled
     }
-    if (w >= G) return;
+    if (hw >= G) return;
     // the sink, and o
     const float sink = sinks[h];
 #pragma unroll
@@ -973,10 +974,9 @@ cudaError_t attn_step(moe_attn *p, const uint16_t *x, int n, RowMap rm, void *ou
     if (e == cudaSuccess && rm.seq >= 0) {
         // prefill: the flash kernel over blocks of 16 tokens (a warp per query head)
         const int G = p->d.QH / p->d.KVH;
-        e = launch_pdl(G <= 8 ? moe_attn_flash_kernel<256> : moe_attn_flash_kernel<512>,
-                       dim3((n + 15) / 16, p->d.KVH), dim3(32 * G), 0, st, p->d, (const float *)c.raw,
-                       (const float2 *)c.rope, rm, n, (const __half *)p->kc, (const __half *)p->vc,
-                       (const float *)p->w.sinks, c.o);
+        e = launch_pdl(moe_attn_flash_kernel, dim3((n + 15) / 16, p->d.KVH, (G + 7) / 8), dim3(256), 0, st, p->d,
+                       (const float *)c.raw, (const float2 *)c.rope, rm, n, (const __half *)p->kc,
+                       (const __half *)p->vc, (const float *)p->w.sinks, c.o);
     } else {
         // decode: the new rows into the cache, the streamed attention over
         // splits of each row's context, the merge

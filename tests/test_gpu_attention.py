@@ -253,3 +253,29 @@ def test_prefill_sixteen_query_heads_per_kv_head():
                         q_heads=QH, kv_heads=KVH, head_dim=64, sliding=window > 0, window=window or 1, eps=1e-5)
         check_close(out.cpu().numpy(), ref, x, what=f"prefill, 16 heads per kv head, window {window}")
         plan.close()
+
+
+def test_bad_arguments_are_refused_before_anything_runs():
+    """Sequence index and positions outside the plan, a prompt that runs past
+    the cache, too many sequences, overlapping x and out: refused with
+    MOE_EINVAL and a message, the caches untouched."""
+    import torch
+    H, QH, KVH, S, ctx = 256, 8, 2, 2, 64
+    w = synth.make_attention(81, H, QH, KVH)
+    plan = moe.AttnPlan(H, QH, KVH, S, ctx)
+    plan.load_weights({k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda()
+                       for k, v in w.items()})
+    x = torch.zeros((4, H), dtype=torch.int16, device="cuda")
+    out = torch.empty((4, H), dtype=torch.float32, device="cuda")
+    for call in (lambda: plan.prefill(x, S, 0, out),            # no sequence S
+                 lambda: plan.prefill(x, -1, 0, out),
+                 lambda: plan.prefill(x, 0, ctx - 3, out),      # rows ctx - 3 .. ctx: one past the cache
+                 lambda: plan.prefill(x, 0, -1, out),
+                 lambda: plan.decode(x[:3], torch.zeros(3, dtype=torch.int32, device="cuda"), out),  # 3 > max_seqs
+                 lambda: plan.decode(x[:2], torch.zeros(2, dtype=torch.int32, device="cuda"), x[:2])):  # out == x
+        with pytest.raises(moe.MoeError) as ei:
+            call()
+        assert ei.value.status == moe.MOE_EINVAL, ei.value
+    torch.cuda.synchronize()
+    assert not plan.k_cache.any() and not plan.v_cache.any()
+    plan.close()
