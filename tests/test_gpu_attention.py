@@ -96,6 +96,14 @@ def test_gpt_oss_attention_decode(window):
     _run(2880, 64, 8, [0, 5, 127, 128, 255, 256, 300, 1022], 1024, window, seed=1 + window)
 
 
+@pytest.mark.parametrize("window", [0, 128])
+def test_decode_at_the_benchmark_size(window):
+    """The benchmark's own launch: 16 sequences whose new token is the last
+    row of a 4096-row cache (the streamed kernel's split count and chunking
+    as timed), full and sliding."""
+    _run(2880, 64, 8, [4095] * 16, 4096, window, seed=7 + window)
+
+
 def test_ragged_batch_sizes_and_small_shapes():
     """Every MMA column tile count (1..32 sequences), a smaller head layout
     (4 query heads per kv head), the bf16 output."""
@@ -225,6 +233,40 @@ def test_prefill_gpt_oss_shape_tensor_core_projections(pos0, n):
     ref = A.prefill(wts, x, kseq, vseq, pos0, q_heads=QH, kv_heads=KVH, head_dim=64, sliding=True,
                     window=a["window"], eps=1e-5)
     check_close(out.cpu().numpy(), ref, x, what="prefill at gpt-oss shapes")
+    plan.close()
+
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_prefill_at_the_benchmark_size(window):
+    """The benchmark's own launch: one 512-token prompt into the empty cache
+    of one of 32 sequences (4096 rows each), in one block of 512 rows, full
+    and sliding: every output row within the block tolerance, the appended
+    rows within one fp16 rounding."""
+    import torch
+    a = synth.ATTN_GPT_OSS
+    H, QH, KVH, S, ctx, n = a["hidden"], a["q_heads"], a["kv_heads"], 32, 4096, 512
+    w = synth.make_attention(71 + window, H, QH, KVH)
+    dev = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda() for k, v in w.items()}
+    plan = moe.AttnPlan(H, QH, KVH, S, ctx, sliding_window=window, prefill_rows=n)
+    plan.load_weights(dev)
+    plan.k_cache.zero_()
+    plan.v_cache.zero_()
+    x = synth.f32_to_bf16_bits(np.random.default_rng(9).normal(0.0, 1.0, (n, H)))
+    out = torch.empty((n, H), dtype=torch.float32, device="cuda")
+    plan.prefill(torch.from_numpy(x.view(np.int16)).cuda(), 0, 0, out)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    wts = dict(gamma=w["gamma"], wq=_as64(w["wq"]), wk=_as64(w["wk"]), wv=_as64(w["wv"]), wo=_as64(w["wo"]),
+               bq=w["bq"].astype(np.float64), bk=w["bk"].astype(np.float64), bv=w["bv"].astype(np.float64),
+               bo=w["bo"].astype(np.float64), sinks=w["sinks"].astype(np.float64))
+    kseq, vseq = np.zeros((n, KVH, 64)), np.zeros((n, KVH, 64))
+    ref = A.prefill(wts, x, kseq, vseq, 0, q_heads=QH, kv_heads=KVH, head_dim=64, sliding=window > 0,
+                    window=window or 1, eps=1e-5)
+    check_close(out.cpu().numpy(), ref, x, what=f"prefill at the benchmark size (window {window})")
+    kc, vc = plan.k_cache[0, :n].cpu().numpy(), plan.v_cache[0, :n].cpu().numpy()
+    for got_c, r in ((kc, kseq), (vc, vseq)):
+        g = got_c.astype(np.float64)
+        assert np.all(np.abs(g - r) <= 2.0 ** -10 * np.abs(r) + 1e-5 * np.abs(r).max())
     plan.close()
 
 
