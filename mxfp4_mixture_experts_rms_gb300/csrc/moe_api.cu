@@ -136,11 +136,11 @@ int choose_path(const moe_plan *p, int tokens, bool *decode, int *nt, int *tile_
         return MOE_OK;
     }
     // the grouped GEMM needs H and F in whole 64-element stages; the GEMVs need
-    // H, F <= 4800 (register-resident activations)
+    // H, F <= 4480 (register-resident activations)
     const bool prefill_ok = b.H % 64 == 0 && b.F % 64 == 0 && p->have_maps;
     const bool decode_ok = decode_supported(b);
     if (p->path == 2 && !prefill_ok) return fail(MOE_ESHAPE, "the prefill path needs H and F multiples of 64");
-    if (p->path == 1 && !decode_ok) return fail(MOE_ESHAPE, "the decode path needs H and F <= 4800");
+    if (p->path == 1 && !decode_ok) return fail(MOE_ESHAPE, "the decode path needs H and F <= 4480");
     const int dmax = p->decode_max_tokens >= 0 ? p->decode_max_tokens : auto_decode_max(b);
     bool d = p->path == 1 || (p->path == 0 && (!prefill_ok || (decode_ok && tokens <= dmax)));
     if (d && !decode_ok) return fail(MOE_ESHAPE, "no kernel path for H=%d F=%d", b.H, b.F);
