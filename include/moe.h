@@ -116,6 +116,26 @@ void moe_plan_destroy(moe_plan *plan);
  *                       encodes the activations the same way.  Must be set
  *                       before moe_set_workspace and before
  *                       moe_load_weights.  0 (default): off
+ *   "expert_cache_slots" C in 1..n_experts: an expert cache (antirez ds4
+ *                       ds4.c, the expert cache beside `ds4_expert_profile_record`;
+ *                       goosedump gpt_oss.rs `ExpertStore`, a lease cache over
+ *                       streamed expert bytes).  The expert matrices passed to
+ *                       moe_load_weights become the store and may be pinned
+ *                       (page-locked, device-mapped) host memory; the plan
+ *                       allocates C device slots per matrix (and a device copy
+ *                       of the shared expert) and, in every forward, right
+ *                       after the routing and on the device: gives each routed
+ *                       expert a slot (resident ones hit; a missing one takes
+ *                       the least recently used slot this forward does not use,
+ *                       the lowest slot on a tie) and copies the missing
+ *                       experts' codes, scales and biases from the store into
+ *                       their slots before the GEMVs read them.  Results are
+ *                       those of the plan without the cache, bit for bit.
+ *                       Serves the decode GEMVs only: a forward that would take
+ *                       the grouped GEMM, or whose tokens x top_k (capped at
+ *                       n_experts) exceed C, fails with MOE_ESHAPE; not with
+ *                       act_fp4.  Set before moe_load_weights (which clears the
+ *                       cache).  0 (default): off, the matrices read in place
  *   "test_stall_wait"   1: test hook: the decode gate/up kernel's consumer
  *                       warps first wait on a barrier nothing completes, so a
  *                       bounded wait (about 2 s) runs out: theirs (detail 59)
@@ -213,6 +233,15 @@ int moe_get_permutation(const moe_plan *plan, int32_t *offsets, int32_t *perm_to
  * selects the shared expert) to float [rows][cols] on the device (dev_out
  * 4-byte aligned, rows x cols floats).  Test hook. */
 int moe_debug_dequant(const moe_plan *plan, int expert, int which, float *dev_out, void *stream);
+
+/* Expert cache state of a plan with expert_cache_slots (see the option):
+ * slot_of [n_experts] (host int32, may be NULL) receives each expert's slot,
+ * -1 for experts not resident; stats [3] (host, may be NULL) the cumulative
+ * hits, misses and forwards (a hit or a miss is one routed expert of one
+ * forward).  Synchronises the stream (device state after the forwards
+ * enqueued on it).  MOE_ENOTREADY when the plan has no cache; MOE_ECUDA on a
+ * CUDA error.  (antirez ds4 ds4.c, the expert profiler's cache statistics.) */
+int moe_get_cache_state(const moe_plan *plan, int32_t *slot_of, long long *stats, void *stream);
 
 /* Kernel timing for benchmarks (no passage of the pages corresponds; the
  * pages' own timers are turbospark-runtime gptoss/mod.rs's per-phase GPU

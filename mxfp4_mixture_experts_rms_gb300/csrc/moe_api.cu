@@ -98,6 +98,13 @@ struct moe_plan {
     bool have_mxf4 = false;
     uint8_t *mxf4_scales = nullptr;  // owned: weight scales repacked into the kernel's atoms
     size_t mxf4_scales_bytes = 0;
+    // expert cache (expert_cache_slots > 0): the expert matrices stay in the
+    // caller's store and `cache_slots` of them at a time in device slots
+    int cache_slots = 0;
+    MatPtrs src_gate{}, src_up{}, src_down{};  // the store's matrices (device-accessible views)
+    void *cache_mem = nullptr;       // owned: the slots' arrays, the shared expert's copy, the tables
+    CacheTables cache{};
+    CacheArrays carr{};
     // kernel timing (profile option)
     static constexpr int kSlots = 4, kMaxRec = 4096 * kSlots;
     std::vector<cudaEvent_t> ev;     // 2 events per record
@@ -116,6 +123,83 @@ struct Carve {
         return p;
     }
 };
+
+// Lays out and clears the expert cache: C slots of each of the nine arrays
+// (codes, scales and biases of gate, up and down), a device copy of the shared
+// expert, and the tables; the GEMVs then read the slots (and the shared
+// expert's copy), the copy kernel the store.
+int cache_setup(moe_plan *p) {
+    const BlockParams &b = p->bp;
+    const int C = p->cache_slots, E = b.E;
+    const MatPtrs *src[3] = {&p->src_gate, &p->src_up, &p->src_down};
+    size_t sz[kCacheArrays];
+    for (int m = 0; m < 3; m++) {
+        const size_t rows = (size_t)src[m]->rows, cols = (size_t)src[m]->cols;
+        sz[3 * m] = rows * cols / 2;         // codes (a multiple of 16 bytes: cols % 32 == 0)
+        sz[3 * m + 1] = rows * (cols / 32);  // scales (rows % 16 == 0)
+        sz[3 * m + 2] = rows * 4;            // biases
+    }
+    uint8_t *slot[kCacheArrays], *shc[kCacheArrays];
+    Carve c;
+    auto layout = [&](char *base) {
+        c.off = 0;
+        for (int a = 0; a < kCacheArrays; a++) slot[a] = c.take<uint8_t>(base, (size_t)C * sz[a]);
+        for (int a = 0; a < kCacheArrays; a++) shc[a] = b.n_shared ? c.take<uint8_t>(base, sz[a]) : nullptr;
+        p->cache.slot_of = c.take<int32_t>(base, E);
+        p->cache.expert_of = c.take<int32_t>(base, C);
+        p->cache.stamp = c.take<long long>(base, C);
+        p->cache.miss = c.take<int2>(base, E);
+        p->cache.n_miss = c.take<int32_t>(base, 1);
+        p->cache.stats = c.take<long long>(base, 3);
+        p->cache.fwd = c.take<long long>(base, 1);
+    };
+    layout(nullptr);
+    if (p->cache_mem) {
+        cudaFree(p->cache_mem);
+        p->cache_mem = nullptr;
+    }
+    cudaError_t e = cudaMalloc(&p->cache_mem, c.off);
+    if (e != cudaSuccess) {
+        p->cache_mem = nullptr;
+        return cuda_fail(e, "moe_load_weights (expert cache slots)");
+    }
+    layout(static_cast<char *>(p->cache_mem));
+    p->cache.slots = C;
+    // no expert resident, every slot empty (stamp -1), counters at zero
+    e = cudaMemset(p->cache.slot_of, 0xFF, sizeof(int32_t) * E);
+    if (e == cudaSuccess) e = cudaMemset(p->cache.expert_of, 0xFF, sizeof(int32_t) * C);
+    if (e == cudaSuccess) e = cudaMemset(p->cache.stamp, 0xFF, sizeof(long long) * C);
+    if (e == cudaSuccess) e = cudaMemset(p->cache.n_miss, 0, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemset(p->cache.stats, 0, sizeof(long long) * 3);
+    if (e == cudaSuccess) e = cudaMemset(p->cache.fwd, 0, sizeof(long long));
+    const void *store[kCacheArrays], *shared[kCacheArrays];
+    for (int m = 0; m < 3; m++) {
+        store[3 * m] = src[m]->codes;
+        store[3 * m + 1] = src[m]->scales;
+        store[3 * m + 2] = src[m]->bias;
+        shared[3 * m] = src[m]->sh_codes;
+        shared[3 * m + 1] = src[m]->sh_scales;
+        shared[3 * m + 2] = src[m]->sh_bias;
+    }
+    for (int a = 0; a < kCacheArrays && b.n_shared && e == cudaSuccess; a++)
+        e = cudaMemcpy(shc[a], shared[a], sz[a], cudaMemcpyDefault);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_load_weights (expert cache setup)");
+    for (int a = 0; a < kCacheArrays; a++) {
+        p->carr.src[a] = static_cast<const uint4 *>(store[a]);
+        p->carr.dst[a] = reinterpret_cast<uint4 *>(slot[a]);
+        p->carr.words[a] = (long long)(sz[a] / 16);
+    }
+    MatPtrs *dst[3] = {&p->gate, &p->up, &p->down};
+    for (int m = 0; m < 3; m++) {
+        dst[m]->codes = slot[3 * m];
+        dst[m]->scales = slot[3 * m + 1];
+        dst[m]->bias = reinterpret_cast<const float *>(slot[3 * m + 2]);
+        dst[m]->sh_codes = shc[3 * m];
+        dst[m]->sh_scales = shc[3 * m + 1];
+        dst[m]->sh_bias = reinterpret_cast<const float *>(shc[3 * m + 2]);
+    }
+    return MOE_OK;
+}
 
 // Largest token count for which the GEMVs beat the grouped GEMM, measured on a
 // GB300: with 32 experts the GEMV path wins up to 56 tokens and ties at 64
@@ -231,6 +315,30 @@ int check_outputs(const BlockParams &b, int tokens, const uint16_t *x, const int
     return MOE_OK;
 }
 
+// A view of p the kernels can read: device memory, or pinned / registered host
+// memory (its device mapping); null where the device cannot reach p.
+const void *device_view(const void *p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return at.devicePointer;
+}
+
+// The store's matrix m as the kernels see it (MOE_EINVAL where a pointer is not device-accessible).
+int store_view(const moe_mxfp4_matrix &m, const char *name, moe_mxfp4_matrix *out) {
+    out->codes = static_cast<const uint8_t *>(device_view(m.codes));
+    out->scales = static_cast<const uint8_t *>(device_view(m.scales));
+    out->bias = static_cast<const float *>(device_view(m.bias));
+    if (!out->codes || !out->scales || !out->bias)
+        return fail(MOE_EINVAL, "%s: with expert_cache_slots the expert matrices must be device memory or pinned "
+                    "(page-locked) host memory", name);
+    if (!aligned16(out->codes) || !aligned16(out->scales) || !aligned16(out->bias))
+        return fail(MOE_EINVAL, "%s: pointers must be 16-byte aligned", name);
+    return MOE_OK;
+}
+
 int check_matrix(const moe_mxfp4_matrix &m, const char *name) {
     if (!m.codes || !m.scales || !m.bias) return fail(MOE_EINVAL, "%s: NULL pointer", name);
     if (!aligned16(m.codes) || !aligned16(m.scales) || !aligned16(m.bias))
@@ -282,10 +390,22 @@ int enqueue_forward(moe_plan *p, const Workspace &ws, const uint16_t *x, int tok
     bool decode = false;
     int nt = 1, tile_rows = 0;
     if (int rc = choose_path(p, tokens, &decode, &nt, &tile_rows)) return rc;
+    const bool cached = p->cache_slots > 0;
+    if (cached) {
+        // every expert a forward routes to must have a slot at once
+        if (!decode) return fail(MOE_ESHAPE, "the expert cache serves the decode GEMVs; %d tokens take another path", tokens);
+        const long long reach = std::min<long long>(b.E, (long long)tokens * b.K);
+        if (reach > p->cache_slots)
+            return fail(MOE_ESHAPE, "%d tokens can route to %lld experts; the expert cache holds %d", tokens, reach,
+                        p->cache_slots);
+    }
     mark(0, true);
     const int forms = p->act_fp4 ? 0 : decode ? (p->x_bf16 ? 0 : kFormF16) : (p->pf_f16 ? kFormF16 : kFormMma);
     cudaError_t e = launch_route(b, ws, x, p->w.gamma, p->w.router_w, p->w.router_b, tokens, ids_out, rw_out,
                                  xhat_out, tile_rows, p->router_exact, forms, st);
+    // the expert cache: slots for the routed experts, the missing ones copied in
+    if (cached && e == cudaSuccess) e = launch_cache_assign(p->cache, b, ws, st);
+    if (cached && e == cudaSuccess) e = launch_cache_copy(p->cache, p->carr, st);
     mark(0, false);
     if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
     mark(1, true);
@@ -295,7 +415,7 @@ int enqueue_forward(moe_plan *p, const Workspace &ws, const uint16_t *x, int tok
         if (!decode) e = launch_gather(b, ws, tokens, p->pf_f16, st);
         if (e == cudaSuccess)
             e = decode ? launch_decode_stage(b, ws, p->gate, p->up, true, tokens, nt, p->x_bf16, p->h_bf16,
-                                             p->stall_test, st)
+                                             p->stall_test, cached, st)
                        : launch_prefill_stage(b, ws, p->gate, p->up, true, tokens, p->maps.gateup, p->pf_f16, st);
     }
     mark(1, false);
@@ -304,7 +424,8 @@ int enqueue_forward(moe_plan *p, const Workspace &ws, const uint16_t *x, int tok
     if (p->act_fp4)
         e = launch_mxf4_stage(b, ws, p->gate, p->up, p->down, p->mxf4, tokens, false, st);
     else
-        e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, 0, st)
+        e = decode ? launch_decode_stage(b, ws, p->down, p->down, false, tokens, nt, p->x_bf16, p->h_bf16, 0, cached,
+                                         st)
                    : launch_prefill_stage(b, ws, p->down, p->down, false, tokens, p->maps.down, p->pf_f16, st);
     mark(2, false);
     if (e != cudaSuccess) return cuda_fail(e, "down kernel launch");
@@ -377,6 +498,7 @@ void moe_plan_destroy(moe_plan *plan) {
     for (auto &e : plan->ev) cudaEventDestroy(e);
     if (plan->pf_scales) cudaFree(plan->pf_scales);
     if (plan->mxf4_scales) cudaFree(plan->mxf4_scales);
+    if (plan->cache_mem) cudaFree(plan->cache_mem);
     delete plan;
 }
 
@@ -406,6 +528,10 @@ int moe_plan_set_i(moe_plan *p, const char *key, long long v) {
         if (p->have_ws) return fail(MOE_EINVAL, "act_fp4 must be set before moe_set_workspace");
         p->act_fp4 = v != 0;
         p->have_w = false;  // the weights are prepared for the path at load
+    } else if (!strcmp(key, "expert_cache_slots")) {
+        if (v < 0 || v > p->bp.E) return fail(MOE_EINVAL, "expert_cache_slots must be in [0, n_experts]");
+        p->cache_slots = (int)v;
+        p->have_w = false;  // the slots are laid out at load
     } else if (!strcmp(key, "test_stall_wait")) {
         p->stall_test = v ? 1 : 0;
     } else if (!strcmp(key, "profile")) {
@@ -486,6 +612,21 @@ int moe_load_weights(moe_plan *p, const moe_weights *w) {
             (rc = check_matrix(w->sh_down, "sh_down")))
             return rc;
     }
+    if (p->cache_slots && p->act_fp4)
+        return fail(MOE_EINVAL, "the expert cache serves the decode GEMVs: act_fp4 cannot be combined with it");
+    // with the expert cache the expert matrices may live in host memory: the
+    // kernels read them through their device views
+    moe_weights wd = *w;
+    if (p->cache_slots) {
+        if ((rc = store_view(w->gate, "gate", &wd.gate)) || (rc = store_view(w->up, "up", &wd.up)) ||
+            (rc = store_view(w->down, "down", &wd.down)))
+            return rc;
+        if (p->bp.n_shared &&
+            ((rc = store_view(w->sh_gate, "sh_gate", &wd.sh_gate)) || (rc = store_view(w->sh_up, "sh_up", &wd.sh_up)) ||
+             (rc = store_view(w->sh_down, "sh_down", &wd.sh_down))))
+            return rc;
+        w = &wd;
+    }
     const BlockParams &b = p->bp;
     // reject the NaN scale code (0xFF) up front
     int32_t *flag = nullptr;
@@ -512,8 +653,17 @@ int moe_load_weights(moe_plan *p, const moe_weights *w) {
     p->gate = mat_of(w->gate, w->sh_gate, b.F, b.H);
     p->up = mat_of(w->up, w->sh_up, b.F, b.H);
     p->down = mat_of(w->down, w->sh_down, b.H, b.F);
+    p->src_gate = p->gate;
+    p->src_up = p->up;
+    p->src_down = p->down;
     p->have_maps = false;
-    if (b.H % 64 == 0 && b.F % 64 == 0 && prefill_make_maps(b, p->gate, p->up, p->down, &p->maps) == cudaSuccess) {
+    p->have_mxf4 = false;
+    if (p->cache_slots) {
+        // the GEMVs read the slots (no grouped-GEMM preparation: the cache
+        // serves the decode path)
+        if ((rc = cache_setup(p))) return rc;
+    } else if (b.H % 64 == 0 && b.F % 64 == 0 &&
+               prefill_make_maps(b, p->gate, p->up, p->down, &p->maps) == cudaSuccess) {
         const size_t nbytes = prefill_scales_bytes(b);
         if (p->pf_scales && p->pf_scales_bytes != nbytes) {
             cudaFree(p->pf_scales);
@@ -532,7 +682,6 @@ int moe_load_weights(moe_plan *p, const moe_weights *w) {
         if (e != cudaSuccess) return cuda_fail(e, "moe_load_weights (repacked scales)");
         p->have_maps = true;
     }
-    p->have_mxf4 = false;
     if (p->act_fp4 && b.H % 64 == 0 && b.F % 64 == 0 && b.H <= 4096) {
         const size_t nbytes = mxf4_scales_bytes(b);
         if (p->mxf4_scales && p->mxf4_scales_bytes != nbytes) {
@@ -628,9 +777,22 @@ int moe_debug_dequant(const moe_plan *p, int expert, int which, float *dev_out, 
     if (!aligned4(dev_out)) return fail(MOE_EINVAL, "dev_out must be 4-byte aligned");
     if (expert < 0 || expert > p->bp.E || (expert == p->bp.E && !p->bp.n_shared))
         return fail(MOE_EINVAL, "expert %d out of range", expert);
-    const MatPtrs &m = which == 0 ? p->gate : which == 1 ? p->up : p->down;
+    const MatPtrs &m = which == 0 ? p->src_gate : which == 1 ? p->src_up : p->src_down;  // the store
     cudaError_t e = launch_dequant(m, expert, p->bp.E, dev_out, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_debug_dequant");
+}
+
+int moe_get_cache_state(const moe_plan *p, int32_t *slot_of, long long *stats, void *stream) {
+    if (!p) return fail(MOE_EINVAL, "NULL plan");
+    if (!p->cache_slots || !p->have_w || !p->cache_mem)
+        return fail(MOE_ENOTREADY, "the plan has no expert cache (expert_cache_slots, then moe_load_weights)");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (slot_of) e = cudaMemcpyAsync(slot_of, p->cache.slot_of, sizeof(int32_t) * p->bp.E, cudaMemcpyDeviceToHost, st);
+    if (stats && e == cudaSuccess)
+        e = cudaMemcpyAsync(stats, p->cache.stats, sizeof(long long) * 3, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_get_cache_state");
 }
 
 int moe_profile_read(moe_plan *p, double *total_ms, int *launches, int n_slots) {

@@ -50,7 +50,7 @@ struct Workspace {
     int32_t *perm_slot;    // [R]
     float *perm_w;         // [R]
     int32_t *loc;          // [T][K + n_shared]
-    int4 *tiles;           // [max_tiles]: (expert, route start, route count, 0)
+    int4 *tiles;           // [max_tiles]: (expert, route start, route count, cache slot or 0)
     int32_t *n_tiles;      // [1]
     uint16_t *h;           // [R][F] bf16 (decode: natural order, bf16-activation plans only; prefill: pair order)
     uint16_t *h16;         // [R][F] fp16 h of the decode GEMVs (natural order)
@@ -290,11 +290,32 @@ cudaError_t launch_route(const BlockParams &bp, const Workspace &ws, const uint1
 // MOE_DEV_WAIT_TIMEOUT (detail 59) and drains.
 cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0,
                                 const MatPtrs &a1, bool gateup, int T, int nt, bool x_bf16, bool h_bf16,
-                                int stall, cudaStream_t st);
+                                int stall, bool slot_index, cudaStream_t st);
 // dst = bf16_rne(src), n elements (any n; 16-byte aligned pointers)
 cudaError_t launch_cast_bf16(const float *src, uint16_t *dst, size_t n, cudaStream_t st);
 cudaError_t launch_mx_fp4_quantize(const uint16_t *x, size_t n_blocks, uint8_t *codes, uint8_t *scales,
                                    cudaStream_t st);
+// Expert cache (plans with expert_cache_slots): device tables owned by the plan.
+struct CacheTables {
+    int32_t *slot_of;    // [E]: slot of each expert, -1 when not resident
+    int32_t *expert_of;  // [slots]: expert in each slot, -1 when empty
+    long long *stamp;    // [slots]: index of the last forward that used the slot, -1 when empty
+    int2 *miss;          // [E]: (expert, slot) of this forward's misses
+    int32_t *n_miss;     // [1]
+    long long *stats;    // [3]: hits, misses, forwards (cumulative)
+    long long *fwd;      // [1]: index of the last forward
+    int slots;
+};
+// The arrays a slot holds: codes, scales and biases of gate, up and down.
+constexpr int kCacheArrays = 9;
+struct CacheArrays {
+    const uint4 *src[kCacheArrays];  // the store's arrays (expert-major), device-accessible
+    uint4 *dst[kCacheArrays];        // the slots' arrays (slot-major)
+    long long words[kCacheArrays];   // 16-byte words per expert
+};
+cudaError_t launch_cache_assign(const CacheTables &c, const BlockParams &bp, const Workspace &ws, cudaStream_t st);
+cudaError_t launch_cache_copy(const CacheTables &c, const CacheArrays &arr, cudaStream_t st);
+
 cudaError_t launch_combine(const BlockParams &bp, const Workspace &ws, const uint16_t *x, int T,
                            void *out, int out_bf16, cudaStream_t st);
 // What the grouped GEMM reads its weights through: TMA descriptors of the

@@ -63,6 +63,7 @@ struct DecodeArgs {
     int stages;      // shared-memory ring depth
     int h_bf16;      // gate/up: write h as bf16 (else fp16)
     int stall;       // test hook: consumers first wait on a barrier nothing completes
+    int slot_index;  // expert cache: the matrices are slot-major and a tile's slot is its fourth field
 };
 
 // f16x2 holding two E2M1 values (0, +-0.5 .. +-6) -> the same values as bf16x2.
@@ -269,7 +270,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
         auto issue = [&](int k) {
             const int s = k % S, item = begin + k;
             const int4 tile = tile_of(item / RB);
-            const int e = tile.x, j0 = (item % RB) * IR;
+            // the matrix index: the expert, or with the expert cache its slot
+            // (the shared expert, index E, is never cached)
+            const int e = a.slot_index && tile.x < E ? tile.w : tile.x, j0 = (item % RB) * IR;
             unsigned char *st = dsm + (size_t)s * geo.stage;
             if (lane == 0) {
                 const uint32_t bytes = NM * 16 * (K / 2);
@@ -668,17 +671,18 @@ bool decode_supported(const BlockParams &bp) {
 }
 
 cudaError_t launch_decode_stage(const BlockParams &bp, const Workspace &ws, const MatPtrs &a0, const MatPtrs &a1,
-                                bool gateup, int T, int nt, bool x_bf16, bool h_bf16, int stall, cudaStream_t st) {
+                                bool gateup, int T, int nt, bool x_bf16, bool h_bf16, int stall, bool slot_index,
+                                cudaStream_t st) {
     const int R = T * (bp.K + bp.n_shared);
     // upper bound on the tile count: each expert's last tile may be partial
     int tiles = (R + 8 * nt - 1) / (8 * nt) + bp.E + bp.n_shared;
     if (tiles > ws.max_tiles) tiles = ws.max_tiles;
     if (gateup) {
-        DecodeArgs gu{bp, ws, a0, a1, bp.H, bp.F, 0, h_bf16 ? 1 : 0, stall};
+        DecodeArgs gu{bp, ws, a0, a1, bp.H, bp.F, 0, h_bf16 ? 1 : 0, stall, slot_index ? 1 : 0};
         const int items = tiles * (bp.F / 16);
         return nt == 1 ? launch_bf<true, 1, 2>(gu, x_bf16, items, st) : launch_bf<true, 2, 2>(gu, x_bf16, items, st);
     }
-    DecodeArgs dn{bp, ws, a0, a0, bp.F, bp.H, 0, 0, 0};
+    DecodeArgs dn{bp, ws, a0, a0, bp.F, bp.H, 0, 0, 0, slot_index ? 1 : 0};
     if (down_rows32(bp)) {
         const int items = tiles * (bp.H / 32);
         return nt == 1 ? launch_bf<false, 1, 2>(dn, h_bf16, items, st) : launch_bf<false, 2, 2>(dn, h_bf16, items, st);

@@ -24,6 +24,7 @@ EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_plan_set_i", "moe_plan_se
            "moe_workspace_bytes",
            "moe_set_workspace", "moe_load_weights", "moe_forward", "moe_forward_ex", "moe_get_expert_counts",
            "moe_get_permutation", "moe_debug_dequant", "moe_profile_read", "moe_get_device_status",
+           "moe_get_cache_state",
            "moe_forward_noalloc", "moe_cast_f32_to_bf16", "moe_mx_quantize_fp4", "moe_locality_create",
            "moe_locality_record", "moe_locality_attach", "moe_locality_read", "moe_locality_reset",
            "moe_locality_destroy", "moe_attn_create", "moe_attn_set_i", "moe_attn_set_f", "moe_attn_workspace_bytes",
@@ -92,6 +93,7 @@ def load(build_if_missing: bool = True):
     L.moe_get_permutation.argtypes = [P, P, P, P, P]
     L.moe_debug_dequant.argtypes = [P, I, I, P, P]
     L.moe_get_device_status.argtypes = [P, C.POINTER(I), P]
+    L.moe_get_cache_state.argtypes = [P, P, P, P]
     L.moe_profile_read.argtypes = [P, C.POINTER(C.c_double), C.POINTER(I), I]
     L.moe_forward_noalloc.argtypes = [P, P, I, P, P, P]
     L.moe_cast_f32_to_bf16.argtypes = [P, P, SZ, P]
@@ -204,6 +206,16 @@ class DeviceBlock:
         return w
 
 
+class HostStoreBlock(DeviceBlock):
+    """A block's weights for a plan with an expert cache: the routed experts'
+    matrices in pinned host memory (the store the cache copies from), the
+    router, the norm weight and the shared expert on the device."""
+
+    def __init__(self, blk: dict, device="cuda"):
+        super().__init__(blk, device)
+        self.mats = {m: tuple(t.cpu().pin_memory() for t in v) for m, v in self.mats.items()}
+
+
 class Plan:
     """One block shape: owns the plan handle and a torch-allocated workspace."""
 
@@ -295,6 +307,15 @@ class Plan:
         if rc not in (MOE_OK, MOE_EDEVICE):
             _check(rc)
         return s.value
+
+    def cache_state(self, stream=None):
+        """Expert cache of a plan made with expert_cache_slots: (slot of each
+        expert, -1 when not resident; cumulative hits; misses; forwards)."""
+        slots = np.empty(self.shape.n_experts, np.int32)
+        stats = np.zeros(3, np.int64)
+        _check(self.L.moe_get_cache_state(self.h, slots.ctypes.data_as(C.c_void_p),
+                                          stats.ctypes.data_as(C.c_void_p), _stream_ptr(stream)))
+        return slots, int(stats[0]), int(stats[1]), int(stats[2])
 
     def close(self):
         if getattr(self, "h", None):
