@@ -67,7 +67,7 @@ def parse():
     ap.add_argument("--quick", action="store_true",
                     help="timed region of the headline only (no clock pre-roll, kernel timing, e2e, CPU "
                          "baseline or extras); for ncu")
-    ap.add_argument("--op", default="block", choices=["block", "mx_fp4_quantize", "attention", "attention_prefill"],
+    ap.add_argument("--op", default="block", choices=["block", "mx_fp4_quantize", "attention", "attention_prefill", "expert_cache"],
                     help="block: the MoE block (the benchmark); mx_fp4_quantize: the FP4 activation "
                          "encoder alone, on --rows x --cols bf16 activations; attention: the gpt-oss "
                          "attention decode step alone; attention_prefill: its prefill of one 512-token prompt")
@@ -586,6 +586,78 @@ def attention_bench(args, seqs: int = 16, ctx: int = 4096):
             "clocks": clk, "gpu_launches": 2 * 5 * reps}
 
 
+def expert_cache_bench(args, T: int = 4, slots: int = 16, n_sets: int = 64):
+    """The gpt-oss block decoding T tokens with its expert matrices in pinned
+    host memory behind a `slots`-slot device cache (plan option
+    expert_cache_slots): the step with every routed expert resident (the same
+    tokens each step: all hits after the first), and with fresh tokens each
+    step (cycling over n_sets token sets: misses copied from host memory),
+    beside the same block with its weights resident in HBM.  Each regime is
+    timed in a CUDA graph; the hit rate and the misses come from the cache's
+    own counters over the timed replay."""
+    import numpy as np
+    import torch
+    from mxfp4_mixture_experts_rms_gb300 import moe, synth
+    wid = 0
+    blk = synth.make_block(wid)
+    shape = blk["shape"]
+    H, F = shape.hidden, shape.expert_hidden
+    per_expert = 2 * F * (H // 2 + H // 32 + 4) + H * (F // 2 + F // 32 + 4)  # gate, up, down bytes
+    ref = moe.Plan(shape, max_tokens=T).alloc_workspace().load_weights(moe.DeviceBlock(blk))
+    cached = moe.Plan(shape, max_tokens=T, expert_cache_slots=slots).alloc_workspace()
+    cached.load_weights(moe.HostStoreBlock(blk))
+    xs = [torch.from_numpy(synth.make_tokens(wid, T, H, sub=500 + i).view(np.int16)).cuda() for i in range(n_sets)]
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+    reps = n_sets
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(plan, rotate):
+        for i in range(3):
+            plan.forward(xs[i] if rotate else xs[0], out, stream=st)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                plan.forward(xs[i] if rotate else xs[0], out, stream=torch.cuda.current_stream())
+        g.replay()
+        torch.cuda.synchronize()
+        before = plan.cache_state() if plan is cached else None
+        clocks = Clocks(torch.cuda.current_device())
+        e0.record(st)
+        g.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        after = plan.cache_state() if plan is cached else None
+        del g
+        return e0.elapsed_time(e1) / reps, before, after, clk
+
+    ms_res, _, _, _ = timed(ref, True)
+    ms_hit, b0, a0, _ = timed(cached, False)
+    ms_miss, b1, a1, clk = timed(cached, True)
+    hits, misses = a1[1] - b1[1], a1[2] - b1[2]
+    moved = misses * per_expert / reps
+    ref.close()
+    cached.close()
+    return {"value": T / (ms_miss / 1e3), "unit": "tokens/s", "ms_per_step": ms_miss, "path": "gemv + expert cache",
+            "config": {"workload": f"gpt-oss MoE block decode, {T} tokens, experts in pinned host memory behind a "
+                                   f"{slots}-slot device cache",
+                       "tokens_per_step": T, "n_experts": shape.n_experts, "top_k": shape.top_k, "slots": slots,
+                       "token_sets": n_sets, "weights": "mxfp4 (e2m1 + e8m0/32)"},
+            "resident_ms_per_step": ms_res,
+            "all_hits_ms_per_step": ms_hit,
+            "all_hits_misses": a0[2] - b0[2],
+            "hit_rate": hits / max(1, hits + misses),
+            "misses_per_step": misses / reps,
+            "store_bytes_per_step": moved,
+            "store_gbs_over_hits": moved / max(1e-9, (ms_miss - ms_hit) / 1e3) / 1e9,
+            "roofline": {"bound": "host link", "achieved": moved / (ms_miss / 1e3) / 1e9, "peak": None,
+                         "peak_kind": "none measured (NVLink-C2C nominal 450 GB/s a direction)", "unit": "GB/s",
+                         "frac": None, "traffic": None},
+            "clocks": clk, "gpu_launches": 6 * reps}
+
+
 def attention_prefill_bench(args, n: int = 512, ctx: int = 4096):
     """Prefill of the attention half (moe_attn_prefill): an n-token prompt into
     the empty cache of one sequence, one sliding-window (128) layer and one
@@ -844,6 +916,8 @@ def run_ours(args, rank, world, local, wid, T):
         extras[att["config"]["workload"]] = att
         apf = attention_prefill_bench(args)
         extras[apf["config"]["workload"]] = apf
+        xc = expert_cache_bench(args)
+        extras[xc["config"]["workload"]] = xc
         if dec:
             extras[dec["config"]["workload"]] = dec
     if rank != 0:
@@ -932,15 +1006,16 @@ def main():
             return
         run_mx_fp4_quantize(args)
         return
-    if args.op in ("attention", "attention_prefill"):
+    if args.op in ("attention", "attention_prefill", "expert_cache"):
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "op": args.op,
-                              "unavailable": "the attention step is timed on the GPU only"}))
+                              "unavailable": f"the {args.op.replace('_', ' ')} step is timed on the GPU only"}))
             return
         import torch
         from mxfp4_mixture_experts_rms_gb300 import moe
         moe.load()
-        fn = attention_bench if args.op == "attention" else attention_prefill_bench
+        fn = {"attention": attention_bench, "attention_prefill": attention_prefill_bench,
+              "expert_cache": expert_cache_bench}[args.op]
         print(json.dumps(fn(args)), flush=True)
         return
     from mxfp4_mixture_experts_rms_gb300 import synth
