@@ -139,6 +139,11 @@ int cache_setup(moe_plan *p) {
         sz[3 * m + 1] = rows * (cols / 32);  // scales (rows % 16 == 0)
         sz[3 * m + 2] = rows * 4;            // biases
     }
+    long long W = 0;  // 16-byte words per expert
+    for (int a = 0; a < kCacheArrays; a++) W += (long long)(sz[a] / 16);
+    if ((long long)E * W >= (1LL << 31) - (1LL << 24))
+        return fail(MOE_ESHAPE, "expert cache: %d experts of %lld bytes exceed the copy kernel's 32-bit word range",
+                    E, W * 16);
     uint8_t *slot[kCacheArrays], *shc[kCacheArrays];
     Carve c;
     auto layout = [&](char *base) {

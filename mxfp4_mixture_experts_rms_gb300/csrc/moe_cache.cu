@@ -102,31 +102,34 @@ __global__ void __launch_bounds__(32) moe_cache_assign_kernel(CacheTables c, Blo
 
 // The missing experts' matrices (codes, scales and biases of gate, up and
 // down: kCacheArrays arrays, words[a] 16-byte words per expert each) from the
-// store into their slots; four words per thread and round in flight.
+// store into their slots, as one flat range of words (every miss's arrays
+// back to back); eight words per thread and round in flight.  The host keeps
+// E x (words per expert) below 2^31, so the index math is 32-bit.
 __global__ void __launch_bounds__(256) moe_cache_copy_kernel(CacheTables c, CacheArrays arr) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the slot assignment
     asm volatile("griddepcontrol.launch_dependents;");
     const int n = *c.n_miss;
     if (n == 0) return;
-    long long W = 0;
+    unsigned W = 0;
 #pragma unroll
-    for (int a = 0; a < kCacheArrays; a++) W += arr.words[a];
-    const long long total = (long long)n * W, stride = (long long)gridDim.x * blockDim.x;
-    auto locate = [&](long long idx, const uint4 *&src, uint4 *&dst) {
-        const long long j = idx / W;
-        long long r = idx - j * W;
+    for (int a = 0; a < kCacheArrays; a++) W += (unsigned)arr.words[a];
+    const unsigned total = (unsigned)n * W, stride = gridDim.x * blockDim.x;
+    auto locate = [&](unsigned idx, const uint4 *&src, uint4 *&dst) {
+        const unsigned j = idx / W;
+        unsigned r = idx - j * W;
         int a = 0;
-        while (a < kCacheArrays - 1 && r >= arr.words[a]) r -= arr.words[a++];
+        while (a < kCacheArrays - 1 && r >= (unsigned)arr.words[a]) r -= (unsigned)arr.words[a++];
         const int2 m = c.miss[j];
         src = arr.src[a] + (size_t)m.x * arr.words[a] + r;
         dst = arr.dst[a] + (size_t)m.y * arr.words[a] + r;
     };
-    for (long long base = (long long)blockIdx.x * blockDim.x + threadIdx.x; base < total; base += 4 * stride) {
-        uint4 v[4];
-        uint4 *d[4];
+    constexpr int kIn = 8;
+    for (unsigned base = blockIdx.x * blockDim.x + threadIdx.x; base < total; base += kIn * stride) {
+        uint4 v[kIn];
+        uint4 *d[kIn];
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const long long idx = base + q * stride;
+        for (int q = 0; q < kIn; q++) {
+            const unsigned idx = base + q * stride;
             d[q] = nullptr;
             if (idx < total) {
                 const uint4 *s;
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(256) moe_cache_copy_kernel(CacheTables c, Cach
             }
         }
 #pragma unroll
-        for (int q = 0; q < 4; q++)
+        for (int q = 0; q < kIn; q++)
             if (d[q]) *d[q] = v[q];
     }
 }
