@@ -84,6 +84,14 @@ def test_forward_before_weights_is_not_ready(L):
     assert L.moe_plan_set_i(h, b"test_stall_wait", 0) == moe.MOE_OK
     assert L.moe_plan_set_i(h, b"out_bf16", 1) == moe.MOE_OK      # out written as bf16
     assert L.moe_plan_set_i(h, b"out_bf16", 0) == moe.MOE_OK
+    # the expert cache: 0 (off) .. n_experts slots; its state only once loaded
+    assert L.moe_plan_set_i(h, b"expert_cache_slots", -1) == moe.MOE_EINVAL
+    assert L.moe_plan_set_i(h, b"expert_cache_slots", 5) == moe.MOE_EINVAL   # 4 experts
+    assert L.moe_plan_set_i(h, b"expert_cache_slots", 4) == moe.MOE_OK
+    stats = (C.c_longlong * 3)()
+    assert L.moe_get_cache_state(h, None, stats, None) == moe.MOE_ENOTREADY
+    assert L.moe_plan_set_i(h, b"expert_cache_slots", 0) == moe.MOE_OK
+    assert L.moe_get_cache_state(None, None, None, None) == moe.MOE_EINVAL
     L.moe_plan_destroy(h)
 
 
