@@ -554,6 +554,95 @@ __device__ void build_permutation(const RouteArgs &a, unsigned char *smem) {
     if (tid == 0) a.ws.tickets[0] = 0u;  // re-arm for the next launch
 }
 
+// The same permutation by one warp, one lane per expert (E + n_shared <= 32,
+// at most 256 routes: 8 per lane): each lane holds its routes' experts and
+// weights in registers, ranks them within each 32-route chunk by matching
+// lanes, and the counts, offsets, tile counts and tile offsets come from two
+// warp scans; no shared-memory histogram and no block barrier.  Same tables
+// as build_permutation, element for element.
+constexpr int kWarpPermRoutes = 256;
+__device__ void build_permutation_warp(const RouteArgs &a, int32_t *scr) {
+    const int lane = threadIdx.x & 31;
+    const int E = a.bp.E, K = a.bp.K, ns = a.bp.n_shared, EE = E + ns, KK = K + ns, T = a.T, R = T * K;
+    const int TR = a.tile_rows;
+    constexpr int RPL = kWarpPermRoutes / 32;
+    const unsigned full = 0xffffffffu, lt = (1u << lane) - 1u;
+    int ev[RPL];
+    float wv[RPL];
+#pragma unroll
+    for (int i = 0; i < RPL; i++) {
+        const int r = lane + 32 * i;
+        ev[i] = r < R ? __ldcg(a.ws.ids + r) : -1;
+        wv[i] = r < R ? __ldcg(a.ws.route_w + r) : 0.f;
+    }
+    // per 32-route chunk: each route's rank among the routes to its expert so
+    // far; lane x counts expert x's routes
+    int rk[RPL];
+    int run = 0;
+#pragma unroll
+    for (int i = 0; i < RPL; i++) {
+        rk[i] = 0;
+        if (32 * i >= R) continue;
+        if (lane + 32 * i < R && (unsigned)ev[i] >= (unsigned)E) {
+            set_device_error(a.ws.status, MOE_DEV_BAD_ROUTE, lane + 32 * i);
+            ev[i] = 0;
+        }
+        const unsigned peers = __match_any_sync(full, ev[i]);
+        rk[i] = __shfl_sync(full, run, ev[i] & 31) + __popc(peers & lt);
+        scr[lane] = 0;
+        __syncwarp();
+        if (ev[i] >= 0 && !(peers & lt)) scr[ev[i]] = __popc(peers);
+        __syncwarp();
+        run += scr[lane];
+        __syncwarp();
+    }
+    const int c = lane < E ? run : (ns && lane == E) ? T : 0;
+    const int tc = lane < EE ? (c + TR - 1) / TR : 0;
+    int incl = c, inct = tc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(full, incl, o), u = __shfl_up_sync(full, inct, o);
+        if (lane >= o) {
+            incl += v;
+            inct += u;
+        }
+    }
+    const int offs = incl - c, toff = inct - tc;
+    const int total = __shfl_sync(full, incl, 31), all_tiles = __shfl_sync(full, inct, 31);
+    if (lane < E) a.ws.counts[lane] = c;
+    if (lane < EE) a.ws.offsets[lane] = offs;
+    for (int k = 0; k < tc && toff + k < a.ws.max_tiles; k++)
+        a.ws.tiles[toff + k] = make_int4(lane, offs + k * TR, min(TR, c - k * TR), 0);
+    if (lane == 0) {
+        a.ws.offsets[EE] = total;
+        *a.ws.n_tiles = min(all_tiles, a.ws.max_tiles);
+        if (all_tiles > a.ws.max_tiles) set_device_error(a.ws.status, MOE_DEV_BAD_ROUTE, -1);
+    }
+#pragma unroll
+    for (int i = 0; i < RPL; i++) {
+        if (32 * i >= R) break;
+        const int r = lane + 32 * i;
+        const int pos = __shfl_sync(full, offs, ev[i] & 31) + rk[i];
+        if (r < R) {
+            const int t = r / K, s = r - t * K;
+            a.ws.perm_token[pos] = t;
+            a.ws.perm_slot[pos] = s;
+            a.ws.perm_w[pos] = wv[i];
+            a.ws.loc[t * KK + s] = pos;
+        }
+    }
+    if (ns) {
+        const int oE = __shfl_sync(full, offs, E & 31);
+        for (int t = lane; t < T; t += 32) {
+            a.ws.perm_token[oE + t] = t;
+            a.ws.perm_slot[oE + t] = K;
+            a.ws.perm_w[oE + t] = 1.0f;
+            a.ws.loc[t * KK + K] = oE + t;
+        }
+    }
+    if (lane == 0) a.ws.tickets[0] = 0u;  // re-arm for the next launch
+}
+
 // Normalise one token row held in registers (XC chunks of 8 per thread) into
 // xh (shared memory; skipped when null) and, if `store`, into the workspace
 // copies: bf16 natural order, and as a.forms asks, fp16 (the GEMV and the fp16
@@ -792,7 +881,11 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_small_kernel(RouteArg
     if (!s_flag) return;
     __threadfence();
     MOE_PHASE_MARK(6);
-    build_permutation<true>(a, smem + rows_b);
+    if (E + a.bp.n_shared <= 32 && a.T * a.bp.K <= kWarpPermRoutes) {
+        if (warp == 0) build_permutation_warp(a, reinterpret_cast<int32_t *>(smem + rows_b));
+    } else {
+        build_permutation<true>(a, smem + rows_b);
+    }
     MOE_PHASE_MARK(7);
 }
 
