@@ -131,3 +131,29 @@ def test_noalloc_reports_a_device_side_wait_timeout():
     assert plan.device_status() == 0
     assert np.array_equal(ids.cpu().numpy(), ids_ref)
     check_close(out.cpu().numpy(), out_ref, what="noalloc after a reported timeout")
+
+
+def test_noalloc_through_the_expert_cache():
+    """A plan with an expert cache (its store in pinned host memory) and no
+    workspace runs the allocation-free forward too: the output of moe_forward
+    on a plan with resident weights, bit for bit, and the cache counts it."""
+    import torch
+    L = moe.load()
+    blk = synth.make_block(0)
+    shape = blk["shape"]
+    ref = moe.Plan(shape, max_tokens=2).alloc_workspace().load_weights(moe.DeviceBlock(blk))
+    plan = moe.Plan(shape, max_tokens=2, expert_cache_slots=8)
+    plan.load_weights(moe.HostStoreBlock(blk))
+    x = torch.from_numpy(synth.make_tokens(0, 2, shape.hidden, sub=9).view(np.int16)).cuda()
+    got = torch.empty((2, shape.hidden), dtype=torch.float32, device="cuda")
+    want = torch.empty_like(got)
+    ids = torch.empty((2, shape.top_k), dtype=torch.int32, device="cuda")
+    assert _noalloc(L, plan, x, got, ids) == moe.MOE_OK
+    ref.forward(x, want)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    _, hits, misses, fwds = plan.cache_state()
+    assert (hits, fwds) == (0, 1) and misses == len(set(ids.cpu().numpy().ravel().tolist()))
+    assert plan.device_status() == 0
+    plan.close()
+    ref.close()
