@@ -231,7 +231,9 @@ int moe_get_permutation(const moe_plan *plan, int32_t *offsets, int32_t *perm_to
 /* Dequantise one expert matrix (ds4.c `dsv4_e2m1fn_value_cpu`: the E2M1 table,
  * times the block's E8M0 scale 2^(s-127)) (which: 0 gate, 1 up, 2 down; expert = n_experts
  * selects the shared expert) to float [rows][cols] on the device (dev_out
- * 4-byte aligned, rows x cols floats).  Test hook. */
+ * 4-byte aligned, rows x cols floats); with expert_cache_slots it reads the
+ * store (the matrices as passed to moe_load_weights), not the slots.  Test
+ * hook. */
 int moe_debug_dequant(const moe_plan *plan, int expert, int which, float *dev_out, void *stream);
 
 /* Expert cache state of a plan with expert_cache_slots (see the option):
