@@ -393,6 +393,10 @@ def measure(w, args, world, local, preroll_s):
             p.set_i("profile", 1)
     pgraph = w.capture(args.steps)
     torch.cuda.synchronize()
+    # the events keep their last recording: time the second replay (the first
+    # launch of a graph also uploads it)
+    pgraph.replay()
+    torch.cuda.synchronize()
     pgraph.replay()
     torch.cuda.synchronize()
     tot, cnt = [0.0] * 4, [0] * 4

@@ -102,6 +102,14 @@ def test_gpt_oss_block_through_a_12_slot_cache():
     assert model.hits > 0 and model.misses > 12  # the sequence both reuses and evicts
 
 
+def test_the_benchmark_launch_4_tokens_16_slots():
+    """The benchmark's own configuration: 4 tokens a step through 16 slots of
+    the gpt-oss block's 32 experts, fresh tokens every step."""
+    blk = synth.make_block(0)
+    model = _run_sequence(blk["shape"], blk, 0, 16, [4] * 8)
+    assert model.misses > 16
+
+
 def test_shared_expert_and_a_cache_of_every_expert():
     """A small shape with an always-on shared expert (kept on the device, not
     cached): 4 slots for 16 experts at top-2, then a cache as large as the
