@@ -121,6 +121,16 @@ def test_shared_expert_and_a_cache_of_every_expert():
     assert model.misses <= 16
 
 
+def test_256_experts_top_8_with_a_shared_expert():
+    """Many experts (the assignment walks them in eight groups of 32; the
+    routing uses its 16-CTA clusters): a small 256-expert, top-8 shape with a
+    shared expert through 24 slots, 1-3 tokens per forward."""
+    shape = synth.BlockShape(256, 128, 256, 8, n_shared=1)
+    blk = synth.make_block(0, shape=shape)
+    model = _run_sequence(shape, blk, 0, 24, [3, 1, 2, 3, 3, 2, 1, 3])
+    assert model.misses > 24
+
+
 def test_calls_the_cache_cannot_serve_are_refused():
     import torch
     blk = synth.make_block(0)
