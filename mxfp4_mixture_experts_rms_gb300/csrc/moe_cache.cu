@@ -153,5 +153,5 @@ cudaError_t launch_cache_copy(const CacheTables &c, const CacheArrays &arr, cuda
     int dev = 0, n_sm = 0;
     MOE_CUDA_TRY(current_device_slot(&dev));
     MOE_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
-    return launch_pdl(moe_cache_copy_kernel, dim3(4 * n_sm), dim3(256), 0, st, c, arr);
+    return launch_pdl(moe_cache_copy_kernel, dim3(n_sm), dim3(256), 0, st, c, arr);
 }
